@@ -1,0 +1,420 @@
+/*
+ * CPU oracle for the DSpark per-step hot path.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the benchmark's
+ * CPU-baseline / reference leg load this library.  The CUDA path never calls it and
+ * shares no source, header, table or helper with it.
+ *
+ * It is the plain, slow, obviously correct statement of what one speculative step
+ * computes, in fp64 from the fp32 / bf16 inputs, following the pages in their order:
+ *
+ *   draft       billytse.dev DSpark page, section 3.2 ("Sequential head": the
+ *               semi-autoregressive block distribution p_k = softmax(U_k + B_k)) and
+ *               section 3.3 ("Markov head": B(x_{k-1}, .) = W1[x_{k-1}] W2, the
+ *               left-to-right loop prev = anchor; bias; softmax; sample; prev = token).
+ *               Sampling is Gumbel-max.
+ *   confidence  weigao.cc DSpark-vs-MTP page, "3. confidence head" (c_k is one linear
+ *               layer on [h_k ; markov_embedding(prev)] followed by a sigmoid) and
+ *               billytse.dev section 5 (a_j = prod_{i<=j} c_i).
+ *   schedule    billytse.dev section 6 (B = sum_r (1 + l_r), tau = sum_r (1 + sum_{j<=l_r}
+ *               a_{r,j}), maximise Theta = tau * SPS(B) by adding positions in descending
+ *               order of expected return and stopping as soon as Theta stops rising) and
+ *               section 7 (early stopping keeps the rule non-anticipating).
+ *   verify      billytse.dev section 1 (accept x_k with probability min(1, p/q), stop at
+ *               the first reject and draw the correction from the residual) and the
+ *               xhh.club DSpark page, Q&A on the acceptance rule (residual norm(max(0,
+ *               p - q))).
+ *
+ * Readings where the pages are silent (the same list is kept with the design notes):
+ *   - Random numbers: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
+ *     Numbers: As Easy as 1, 2, 3", SC'11), key = (seed low 32 bits, seed high 32 bits),
+ *     counter = (floor(v/4), k, b, stream), the draw is output word v mod 4.  Positions k
+ *     are 1-based, requests b 0-based.  Streams: 0 draft Gumbel, 1 verify uniform (v = 0),
+ *     2 residual Gumbel, 3 bonus Gumbel.
+ *   - U01(x) = ((x >> 9) + 1/2) * 2^-23, exactly representable, strictly inside (0, 1).
+ *     w = 1 - U01(x) is formed exactly from the complemented bits and the Gumbel value is
+ *     g = -log(-log1p(-w)).
+ *   - Gumbel-max: x = argmax_v (z_v + g_v); ties go to the smallest v.
+ *   - Scheduler: a is clamped to [0, 1] (NaN -> 0) and taken in fixed point
+ *     A = floor(a * 2^32 + 1/2); items are sorted by (A desc, r asc, j asc); sums are
+ *     exact integers; Theta_n = double(R * 2^32 + S_n) * double(sps[R + n]) is compared
+ *     with Theta_{n-1} as a plain double product; the first non-rise stops.
+ *   - Verify: the bonus row is target row l + 1; the residual draw is Gumbel-max over
+ *     log(P - Q) restricted to P > Q; if that set is empty, Gumbel-max over log P with
+ *     the same stream (counted as a fallback).
+ *
+ * Parity pins live in tests/test_oracle_*.py.  Every function here is pinned there.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define DSO_OK 0
+#define DSO_ERR_ARG 1
+#define DSO_ERR_NOMEM 2
+
+/* ------------------------------------------------------------------------------------ */
+/* Counter-based random numbers                                                          */
+/* ------------------------------------------------------------------------------------ */
+
+/* Philox4x32 with 10 rounds: each round multiplies counter words 0 and 2 by the two
+ * round constants, swaps and mixes the high halves with the other counter words and the
+ * key; the key is advanced by the two Weyl constants between rounds. */
+void dso_philox4x32_10(const uint32_t ctr[4], uint64_t seed, uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFu), k1 = (uint32_t)(seed >> 32);
+    for (int round = 0; round < 10; ++round) {
+        uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+        uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+        uint32_t n0 = (uint32_t)(prod1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)prod1;
+        uint32_t n2 = (uint32_t)(prod0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)prod0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The 32-bit draw for vocabulary index v of (request b, position k, stream). */
+uint32_t dso_draw(uint64_t seed, int b, int k, int v, int stream)
+{
+    uint32_t ctr[4] = {(uint32_t)v / 4u, (uint32_t)k, (uint32_t)b, (uint32_t)stream};
+    uint32_t out[4];
+    dso_philox4x32_10(ctr, seed, out);
+    return out[(uint32_t)v % 4u];
+}
+
+double dso_u01(uint32_t x)
+{
+    return ((double)(x >> 9) + 0.5) * (1.0 / 8388608.0);
+}
+
+/* 1 - U01(x), formed exactly from the complemented top 23 bits. */
+double dso_one_minus_u01(uint32_t x)
+{
+    return ((double)((~x) >> 9 & 0x7FFFFFu) + 0.5) * (1.0 / 8388608.0);
+}
+
+/* Standard Gumbel variate g = -log(E) with E = -log(u) an Exp(1) variate. */
+double dso_gumbel(uint32_t x)
+{
+    double w = dso_one_minus_u01(x);
+    double E = -log1p(-w);
+    return -log(E);
+}
+
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Draft: Markov bias, softmax, Gumbel-max                                               */
+/* ------------------------------------------------------------------------------------ */
+
+/* z_v = U[k][v] + sum_i W1[prev][i] * W2[i][v], all in double. */
+static void draft_logits(const float *U_row, const uint16_t *W1, const uint16_t *W2,
+                         int prev, int V, int r, double *z)
+{
+    for (int v = 0; v < V; ++v) z[v] = 0.0;
+    for (int i = 0; i < r; ++i) {
+        double e = bf16_to_double(W1[(size_t)prev * r + i]);
+        const uint16_t *w2 = W2 + (size_t)i * V;
+        for (int v = 0; v < V; ++v) z[v] += e * bf16_to_double(w2[v]);
+    }
+    for (int v = 0; v < V; ++v) z[v] += (double)U_row[v];
+}
+
+static void softmax_stats(const double *z, int V, double *m_out, double *s_out)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) if (z[v] > m) m = z[v];
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) s += exp(z[v] - m);
+    *m_out = m;
+    *s_out = s;
+}
+
+/* argmax_v (score_v + g_v) over the v with mask[v] != 0 (mask NULL: all v); ties to the
+ * smallest v.  Returns -1 when no v is eligible.  *gap = best - second best score. */
+static int gumbel_argmax(const double *score, const unsigned char *mask, int V,
+                         uint64_t seed, int b, int k, int stream, double *gap)
+{
+    int best = -1;
+    double b1 = -INFINITY, b2 = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        if (mask && !mask[v]) continue;
+        double s = score[v] + dso_gumbel(dso_draw(seed, b, k, v, stream));
+        if (best < 0 || s > b1) {
+            b2 = b1;
+            b1 = s;
+            best = v;
+        } else if (s > b2) {
+            b2 = s;
+        }
+    }
+    *gap = b1 - b2;
+    return best;
+}
+
+/*
+ * U       [n_req, gamma, V]  base logits of the requests in req_ids
+ * W1      [V, r] bf16, W2 [r, V] bf16
+ * anchor  [n_req]            last committed token
+ * req_ids [n_req]            request index b used by the random counter
+ * outputs [n_req, gamma]:    tokens, q_tok = q_k(x_k), row_max, row_sumexp, gap (top-two
+ *                            Gumbel score gap of the draw, for the tie band)
+ */
+int dso_draft(const float *U, const uint16_t *W1, const uint16_t *W2, const int32_t *anchor,
+              const int32_t *req_ids, int n_req, int gamma, int V, int r, uint64_t seed,
+              int32_t *tokens, double *q_tok, double *row_max, double *row_sumexp,
+              double *gap, int nthreads)
+{
+    if (n_req < 0 || gamma < 1 || V < 1 || r < 1) return DSO_ERR_ARG;
+    int err = DSO_OK;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int i = 0; i < n_req; ++i) {
+        double *z = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!z) { err = DSO_ERR_NOMEM; continue; }
+        int b = req_ids[i];
+        int prev = anchor[i];
+        for (int k = 1; k <= gamma; ++k) {
+            size_t o = (size_t)i * gamma + (k - 1);
+            if (prev < 0 || prev >= V) { err = DSO_ERR_ARG; break; }
+            draft_logits(U + o * V, W1, W2, prev, V, r, z);
+            double m, s;
+            softmax_stats(z, V, &m, &s);
+            double g;
+            int x = gumbel_argmax(z, NULL, V, seed, b, k, 0, &g);
+            tokens[o] = x;
+            q_tok[o] = exp(z[x] - m) / s;
+            row_max[o] = m;
+            row_sumexp[o] = s;
+            gap[o] = g;
+            prev = x;
+        }
+        free(z);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Confidence head and survival                                                          */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * c[b,k] = sigmoid( sum_j w_c[j] h[b,k,j] + sum_i w_c[H+i] W1[prev,i] + b_c ),
+ * prev = anchor[b] for k = 1, tokens[b,k-1] otherwise;  a[b,k] = prod_{i<=k} c[b,i].
+ */
+int dso_confidence(const float *h, const int32_t *anchor, const int32_t *tokens,
+                   const uint16_t *W1, const float *w_c, float b_c, int n_req, int gamma,
+                   int H, int r, int V, double *c, double *a)
+{
+    if (n_req < 0 || gamma < 1 || H < 0 || r < 1) return DSO_ERR_ARG;
+    for (int i = 0; i < n_req; ++i) {
+        double surv = 1.0;
+        for (int k = 1; k <= gamma; ++k) {
+            size_t o = (size_t)i * gamma + (k - 1);
+            int prev = (k == 1) ? anchor[i] : tokens[o - 1];
+            if (prev < 0 || prev >= V) return DSO_ERR_ARG;
+            double acc = (double)b_c;
+            for (int j = 0; j < H; ++j) acc += (double)w_c[j] * (double)h[o * H + j];
+            for (int j = 0; j < r; ++j)
+                acc += (double)w_c[H + j] * bf16_to_double(W1[(size_t)prev * r + j]);
+            double ck = 1.0 / (1.0 + exp(-acc));
+            surv *= ck;
+            c[o] = ck;
+            a[o] = surv;
+        }
+    }
+    return DSO_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Hardware-aware prefix scheduler                                                       */
+/* ------------------------------------------------------------------------------------ */
+
+typedef struct { int64_t A; int r; int j; } sched_item;
+
+static int item_before(const sched_item *x, const sched_item *y)
+{
+    if (x->A != y->A) return x->A > y->A;
+    if (x->r != y->r) return x->r < y->r;
+    return x->j < y->j;
+}
+
+static int64_t fixed_point_a(float a)
+{
+    double x = (double)a;
+    if (!(x > 0.0)) return 0;          /* also NaN */
+    if (x > 1.0) x = 1.0;
+    return (int64_t)floor(x * 4294967296.0 + 0.5);
+}
+
+/* theta[0] = Theta at the returned stop; ell [R]; *B_total = R + admitted. */
+int dso_schedule(const float *a, int R, int gamma, const float *sps, int sps_len,
+                 int32_t *ell, int32_t *B_total, double *theta)
+{
+    if (R < 1 || gamma < 1 || sps_len < R * (gamma + 1) + 1) return DSO_ERR_ARG;
+    int N = R * gamma;
+    sched_item *it = (sched_item *)malloc(sizeof(sched_item) * (size_t)N);
+    sched_item *tmp = (sched_item *)malloc(sizeof(sched_item) * (size_t)N);
+    if (!it || !tmp) { free(it); free(tmp); return DSO_ERR_NOMEM; }
+    for (int r = 0; r < R; ++r)
+        for (int j = 1; j <= gamma; ++j) {
+            sched_item s = {fixed_point_a(a[(size_t)r * gamma + (j - 1)]), r, j};
+            it[(size_t)r * gamma + (j - 1)] = s;
+        }
+    /* bottom-up merge sort by (A desc, r asc, j asc) */
+    for (int width = 1; width < N; width *= 2) {
+        for (int lo = 0; lo < N; lo += 2 * width) {
+            int mid = lo + width < N ? lo + width : N;
+            int hi = lo + 2 * width < N ? lo + 2 * width : N;
+            int p = lo, q = mid, o = lo;
+            while (p < mid && q < hi) tmp[o++] = item_before(&it[q], &it[p]) ? it[q++] : it[p++];
+            while (p < mid) tmp[o++] = it[p++];
+            while (q < hi) tmp[o++] = it[q++];
+        }
+        sched_item *sw = it; it = tmp; tmp = sw;
+    }
+    for (int r = 0; r < R; ++r) ell[r] = 0;
+    const double scale = 4294967296.0;
+    int64_t S = 0;
+    double theta_prev = (double)((int64_t)R * (int64_t)4294967296LL) * (double)sps[R];
+    int admitted = 0;
+    for (int n = 1; n <= N; ++n) {
+        int64_t S_n = S + it[n - 1].A;
+        double th = (double)((int64_t)R * (int64_t)4294967296LL + S_n) * (double)sps[R + n];
+        if (!(th > theta_prev)) break;
+        S = S_n;
+        theta_prev = th;
+        admitted = n;
+        ell[it[n - 1].r] += 1;
+    }
+    *B_total = R + admitted;
+    *theta = theta_prev / scale;
+    free(it);
+    free(tmp);
+    return DSO_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Lossless verification                                                                 */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * T [n_req, gamma+1, V] target logits; U [n_req, gamma, V]; tokens [n_req, gamma];
+ * ell [n_req] verified lengths.  Outputs: accept_len [n_req], out_tokens [n_req, gamma+1]
+ * (-1 padded), n_out [n_req], band [n_req, gamma] (|u - p/q| of every accept test, NaN
+ * where no test ran), gap [n_req] (top-two score gap of the correction / bonus draw),
+ * fallback [n_req] (1 when the residual was empty and P itself was sampled).
+ */
+int dso_verify(const float *T, const float *U, const uint16_t *W1, const uint16_t *W2,
+               const int32_t *anchor, const int32_t *tokens, const int32_t *ell,
+               const int32_t *req_ids, int n_req, int gamma, int V, int r, uint64_t seed,
+               int32_t *accept_len, int32_t *out_tokens, int32_t *n_out, double *band,
+               double *gap, int32_t *fallback, int nthreads)
+{
+    if (n_req < 0 || gamma < 1 || V < 1 || r < 1) return DSO_ERR_ARG;
+    int err = DSO_OK;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int i = 0; i < n_req; ++i) {
+        int b = req_ids[i];
+        int L = ell[i];
+        for (int k = 0; k < gamma; ++k) band[(size_t)i * gamma + k] = NAN;
+        for (int k = 0; k <= gamma; ++k) out_tokens[(size_t)i * (gamma + 1) + k] = -1;
+        fallback[i] = 0;
+        if (L < 0 || L > gamma) { err = DSO_ERR_ARG; continue; }
+        double *z = (double *)malloc(sizeof(double) * (size_t)V);
+        double *P = (double *)malloc(sizeof(double) * (size_t)V);
+        double *score = (double *)malloc(sizeof(double) * (size_t)V);
+        unsigned char *mask = (unsigned char *)malloc((size_t)V);
+        if (!z || !P || !score || !mask) {
+            free(z); free(P); free(score); free(mask);
+            err = DSO_ERR_NOMEM;
+            continue;
+        }
+        int reject_at = 0;   /* 1-based position of the first reject, 0: none */
+        int prev = anchor[i];
+        for (int k = 1; k <= L; ++k) {
+            size_t o = (size_t)i * gamma + (k - 1);
+            int x = tokens[o];
+            /* target p_k = softmax(T[k]) */
+            const float *Trow = T + ((size_t)i * (gamma + 1) + (k - 1)) * V;
+            double M = -INFINITY, Ssum = 0.0;
+            for (int v = 0; v < V; ++v) if ((double)Trow[v] > M) M = (double)Trow[v];
+            for (int v = 0; v < V; ++v) Ssum += exp((double)Trow[v] - M);
+            double p = exp((double)Trow[x] - M) / Ssum;
+            /* draft q_k = softmax(U[k] + W1[prev] W2) */
+            draft_logits(U + o * V, W1, W2, prev, V, r, z);
+            double m, s;
+            softmax_stats(z, V, &m, &s);
+            double q = exp(z[x] - m) / s;
+            double u = dso_u01(dso_draw(seed, b, k, 0, 1));
+            double ratio = p / q;
+            band[o] = fabs(u - ratio);
+            if (u < ratio) {          /* accept with probability min(1, p/q) */
+                prev = x;
+                continue;
+            }
+            reject_at = k;
+            /* residual norm(max(0, P - Q)) by Gumbel-max over log(P - Q), P > Q */
+            int any = 0;
+            for (int v = 0; v < V; ++v) {
+                double Pv = exp((double)Trow[v] - M) / Ssum;
+                double Qv = exp(z[v] - m) / s;
+                P[v] = Pv;
+                mask[v] = Pv > Qv;
+                score[v] = mask[v] ? log(Pv - Qv) : -INFINITY;
+                any |= mask[v];
+            }
+            double gp;
+            int y;
+            if (any) {
+                y = gumbel_argmax(score, mask, V, seed, b, k, 2, &gp);
+            } else {
+                for (int v = 0; v < V; ++v) score[v] = log(P[v]);
+                y = gumbel_argmax(score, NULL, V, seed, b, k, 2, &gp);
+                fallback[i] = 1;
+            }
+            gap[i] = gp;
+            for (int j = 1; j < k; ++j)
+                out_tokens[(size_t)i * (gamma + 1) + (j - 1)] = tokens[(size_t)i * gamma + (j - 1)];
+            out_tokens[(size_t)i * (gamma + 1) + (k - 1)] = y;
+            accept_len[i] = k - 1;
+            n_out[i] = k;
+            break;
+        }
+        if (!reject_at) {
+            /* every verified position accepted: the target's bonus token from row L+1 */
+            const float *Trow = T + ((size_t)i * (gamma + 1) + L) * V;
+            for (int v = 0; v < V; ++v) score[v] = (double)Trow[v];
+            double gp;
+            int y = gumbel_argmax(score, NULL, V, seed, b, L + 1, 3, &gp);
+            gap[i] = gp;
+            for (int j = 1; j <= L; ++j)
+                out_tokens[(size_t)i * (gamma + 1) + (j - 1)] = tokens[(size_t)i * gamma + (j - 1)];
+            out_tokens[(size_t)i * (gamma + 1) + L] = y;
+            accept_len[i] = L;
+            n_out[i] = L + 1;
+        }
+        free(z); free(P); free(score); free(mask);
+    }
+    return err;
+}

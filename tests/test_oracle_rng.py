@@ -1,0 +1,112 @@
+"""Pins of the oracle's random numbers.
+
+* Philox4x32-10 against an independent library implementation: Triton's Philox,
+  run by Triton's CPU interpreter in a child process.
+* U01 and its exact complement against their closed forms.
+* The Gumbel transform against the Gumbel distribution's closed-form moments and CDF.
+"""
+import json
+import os
+import subprocess
+import sys
+import textwrap
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+
+_TRITON_PROBE = textwrap.dedent(
+    """
+    import json, os, sys
+    os.environ["TRITON_INTERPRET"] = "1"
+    import torch, triton, triton.language as tl
+    from triton.language.random import philox
+
+    @triton.jit
+    def k(out_ptr, c_ptr, seed, N: tl.constexpr):
+        i = tl.arange(0, N)
+        c0 = tl.load(c_ptr + i * 4 + 0).to(tl.uint32, bitcast=True)
+        c1 = tl.load(c_ptr + i * 4 + 1).to(tl.uint32, bitcast=True)
+        c2 = tl.load(c_ptr + i * 4 + 2).to(tl.uint32, bitcast=True)
+        c3 = tl.load(c_ptr + i * 4 + 3).to(tl.uint32, bitcast=True)
+        a, b, c, d = philox(seed, c0, c1, c2, c3, 10)
+        tl.store(out_ptr + i * 4 + 0, a.to(tl.int32, bitcast=True))
+        tl.store(out_ptr + i * 4 + 1, b.to(tl.int32, bitcast=True))
+        tl.store(out_ptr + i * 4 + 2, c.to(tl.int32, bitcast=True))
+        tl.store(out_ptr + i * 4 + 3, d.to(tl.int32, bitcast=True))
+
+    req = json.loads(sys.stdin.read())
+    res = []
+    for seed, ctrs in req:
+        c = torch.tensor(ctrs, dtype=torch.int64).to(torch.uint32).view(torch.int32).reshape(-1)
+        out = torch.zeros(len(ctrs) * 4, dtype=torch.int32)
+        k[(1,)](out, c, seed, len(ctrs))
+        res.append([x & 0xFFFFFFFF for x in out.tolist()])
+    print(json.dumps(res))
+    """
+)
+
+
+def test_philox_matches_triton_library():
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(7)
+    cases = []
+    for seed in [0, 1, 0x0123456789ABCDEF, (1 << 64) - 1, int(rng.integers(0, 2**63))]:
+        ctrs = [[0, 0, 0, 0], [0xFFFFFFFF] * 4, [1, 2, 3, 4], [37987, 7, 31, 2]]
+        ctrs += rng.integers(0, 2**32, size=(4, 4), dtype=np.uint64).tolist()
+        cases.append([seed if seed < 2**63 else seed - 2**64, ctrs])
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    try:
+        proc = subprocess.run([sys.executable, "-c", _TRITON_PROBE], input=json.dumps(cases),
+                              capture_output=True, text=True, env=env, timeout=600)
+    except subprocess.TimeoutExpired:  # pragma: no cover
+        pytest.skip("triton interpreter timed out")
+    if proc.returncode != 0:
+        pytest.skip("triton interpreter unavailable: " + proc.stderr.strip().splitlines()[-1])
+    ref = json.loads(proc.stdout.strip().splitlines()[-1])
+    for (seed, ctrs), want in zip(cases, ref):
+        for i, ctr in enumerate(ctrs):
+            got = oracle.philox4x32_10(ctr, seed & ((1 << 64) - 1)).tolist()
+            assert got == want[4 * i: 4 * i + 4], (seed, ctr)
+
+
+def test_draw_layout_counter_and_word():
+    # the draw for vocabulary index v is word v % 4 of the block floor(v / 4)
+    seed = 12345
+    for (b, k, v, s) in [(0, 1, 0, 0), (3, 2, 5, 0), (7, 4, 1023, 2), (1, 16, 151935, 3)]:
+        blk = oracle.philox4x32_10([v // 4, k, b, s], seed)
+        assert oracle.draw(seed, b, k, v, s) == int(blk[v % 4])
+
+
+def test_u01_closed_form_and_exact_complement():
+    assert oracle.u01(0) == 0.5 * 2.0**-23
+    assert oracle.u01(0xFFFFFFFF) == 1.0 - 0.5 * 2.0**-23
+    assert oracle.u01(0x1FF) == oracle.u01(0)          # the low 9 bits are dropped
+    rng = np.random.default_rng(3)
+    for x in rng.integers(0, 2**32, size=2000, dtype=np.uint64).tolist():
+        u, w = oracle.u01(x), oracle.one_minus_u01(x)
+        assert 0.0 < u < 1.0 and u + w == 1.0
+        assert np.float32(u) == u and np.float32(w) == w   # exact in fp32
+
+
+def test_u01_uniform():
+    xs = np.array([oracle.draw(99, 0, 1, v, 0) for v in range(40000)], dtype=np.uint64)
+    u = np.array([oracle.u01(int(x)) for x in xs])
+    hist, _ = np.histogram(u, bins=20, range=(0, 1))
+    assert stats.chisquare(hist).pvalue > 1e-3
+
+
+def test_gumbel_moments_and_cdf():
+    xs = [oracle.draw(5, b, 3, v, 2) for b in range(4) for v in range(25000)]
+    g = np.array([oracle.gumbel(x) for x in xs])
+    n = len(g)
+    euler_gamma = 0.5772156649015329
+    var = np.pi**2 / 6.0
+    assert abs(g.mean() - euler_gamma) < 4.0 * np.sqrt(var / n)
+    assert abs(g.var() - var) < 4.0 * np.sqrt(2.0 * var**2 * 2.4 / n)   # loose (excess kurtosis 2.4)
+    assert stats.kstest(g, stats.gumbel_r.cdf).pvalue > 1e-3
+    # monotone in the uniform: larger u -> larger g
+    assert oracle.gumbel(0xFFFFFFFF) > oracle.gumbel(0x80000000) > oracle.gumbel(0)
+    assert abs(oracle.gumbel(0xFFFFFFFF) - (-np.log(-np.log1p(-0.5 * 2.0**-23)))) < 1e-12
