@@ -1,0 +1,184 @@
+/*
+ * dspark.h -- C ABI of the DSpark per-step hot path on one GPU (sm_103a).
+ *
+ * One speculative step of DSpark ("DSpark: Confidence-Scheduled Speculative Decoding with
+ * Semi-Autoregressive Generation") is four calls, run in this order on one stream:
+ *
+ *   dspark_draft       semi-autoregressive block drafting with the low-rank Markov head
+ *   dspark_confidence  confidence head c_k and survival a_j = prod_{i<=j} c_i
+ *   dspark_schedule    hardware-aware prefix scheduler choosing l_r per request
+ *   dspark_verify      lossless rejection-sampling verification with correction / bonus
+ *
+ * The backbone forward (base logits U, hidden states h) and the target forward (target
+ * logits T) are not part of this library; their outputs are inputs here.
+ *
+ * Conventions shared by every call
+ *   - All array pointers are DEVICE pointers, owned by the caller, row-major and
+ *     contiguous, 16-byte aligned.  The library allocates no memory: scratch space comes
+ *     from the caller's workspace (size from dspark_workspace_bytes; 256-byte aligned,
+ *     zero-filled before its first use: its first 256 bytes hold the device status
+ *     word).  One workspace may serve all calls of a step as long as they run in order
+ *     on one stream; calls that overlap on the GPU must not share a workspace.
+ *   - bf16 weights are passed as their uint16_t bit patterns.
+ *   - Every call is asynchronous on `stream` and may be captured in a CUDA graph.
+ *   - Requests b are 0-based, draft positions k are 1-based (k = 1..gamma).
+ *   - Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by `seed` (low word,
+ *     high word); the 32-bit draw for vocabulary index v of (request b, position k,
+ *     stream s) is word v % 4 of the block with counter (v / 4, k, b, s);
+ *     U01(x) = ((x >> 9) + 1/2) * 2^-23.  Streams: 0 draft Gumbel, 1 acceptance uniform
+ *     (v = 0), 2 residual Gumbel, 3 bonus Gumbel.  Gumbel g = -log(-log U01).
+ *   - Shape limits: 1 <= B < 65536, 1 <= gamma <= 32, B * (gamma + 1) < 2^21,
+ *     8 <= V < 2^31 with V % 8 == 0, 16 <= r <= 256 with r % 16 == 0, H % 4 == 0.
+ *
+ * Errors
+ *   - Every call validates its arguments on the host before launching anything and
+ *     returns DSPARK_ERR_INVALID_ARG (null pointer, misaligned pointer, bad shape,
+ *     workspace too small, table too short) or DSPARK_ERR_UNSUPPORTED (shape outside the
+ *     limits above).  Nothing is launched in that case.
+ *   - A failed launch returns DSPARK_ERR_CUDA.
+ *   - Kernels never trap.  A device-side check (a token id out of range, a bounded wait
+ *     that ran out) writes a code into the workspace's status word and skips the access;
+ *     dspark_last_device_status() reads and clears it.
+ */
+#ifndef DSPARK_H_
+#define DSPARK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __CUDA_RUNTIME_H__
+typedef struct CUstream_st* cudaStream_t;
+#endif
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1,
+  DSPARK_ERR_UNSUPPORTED = 2,
+  DSPARK_ERR_CUDA = 3,
+  DSPARK_ERR_TIMEOUT = 4,
+  DSPARK_ERR_DEVICE_CHECK = 5
+} dspark_status;
+
+/* Human-readable name of a status code (static string). */
+const char* dspark_status_string(dspark_status s);
+
+/* Workspace bytes needed by every call on shapes (B, gamma, V, r, H); 0 on bad shapes. */
+size_t dspark_workspace_bytes(int B, int gamma, int V, int r, int H);
+
+/*
+ * Markov transition bias for a batch of predecessors.  billytse.dev DSpark page, section
+ * 3.3: the first-order Markov head adds B(x_{k-1}, .) = W1[x_{k-1}] W2 (rank r) to the
+ * base logits.  Computed on the tensor cores with fp32 accumulation:
+ *   out[b, v] = sum_i W1[prev[b * prev_stride], i] * W2[i, v]   (0 <= b < B, 0 <= v < V)
+ * A predecessor of -1 gives a zero row; any other id outside [0, V) gives a zero row and
+ * records DSPARK_ERR_DEVICE_CHECK.
+ *
+ *   W1 [V, r] bf16, W2 [r, V] bf16, prev [B * prev_stride] int32  ->  out [B, V] fp32
+ */
+dspark_status dspark_markov_bias(const uint16_t* W1, const uint16_t* W2, const int32_t* prev,
+                                 int prev_stride, int B, int V, int r, float* out,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Semi-autoregressive draft.  billytse.dev DSpark page, section 3.2 (block distribution
+ * p_k(v | x_<k) = softmax(U_k(v) + B_k(x_<k, v))) and section 3.3 (first-order Markov
+ * head B(x_{k-1}, .) = W1[x_{k-1}] W2 with rank r; the left-to-right loop prev = anchor;
+ * bias = W1[prev] @ W2; probs = softmax(base_logits[k] + bias); token = sample(probs);
+ * prev = token).  Sampling is Gumbel-max: x_k = argmax_v (z_v + g_v), ties to the
+ * smallest v, with g from stream 0.
+ *
+ *   U        [B, gamma, V] fp32   base logits U_k
+ *   W1       [V, r] bf16          previous-token embedding of the Markov head
+ *   W2       [r, V] bf16          projection back to vocabulary logits
+ *   anchor   [B] int32            last committed token of each request (0 <= id < V)
+ * outputs
+ *   tokens     [B, gamma] int32   x_k
+ *   q_tok      [B, gamma] fp32    q_k(x_k) = softmax(z_k)(x_k)
+ *   row_max    [B, gamma] fp32    max_v z_k(v)
+ *   row_sumexp [B, gamma] fp32    sum_v exp(z_k(v) - row_max)
+ */
+dspark_status dspark_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
+                           const int32_t* anchor, int B, int gamma, int V, int r,
+                           uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
+                           float* row_sumexp, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
+ * Confidence head and survival.  weigao.cc DSpark-vs-MTP page, "3. confidence head"
+ * (c_k = P(position k survives | positions < k accepted), one linear layer on
+ * [output_hidden_k ; markov_embedding(prev_token)]) and billytse.dev DSpark page,
+ * section 5 (a_j = prod_{i<=j} c_i).  The Markov embedding is the W1 row of prev
+ * (prev = anchor for k = 1, tokens[b, k-1] after that):
+ *   c[b,k] = 1 / (1 + exp(-(sum_j w_c[j] h[b,k,j] + sum_i w_c[H+i] W1[prev,i] + b_c)))
+ *   a[b,k] = c[b,1] * ... * c[b,k]   (multiplied left to right)
+ *
+ *   h [B, gamma, H] fp32, anchor [B], tokens [B, gamma], W1 [V, r] bf16,
+ *   w_c [H + r] fp32, b_c  ->  c [B, gamma] fp32, a [B, gamma] fp32
+ */
+dspark_status dspark_confidence(const float* h, const int32_t* anchor, const int32_t* tokens,
+                                const uint16_t* W1, const float* w_c, float b_c, int B,
+                                int gamma, int H, int r, int V, float* c, float* a,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Hardware-aware prefix scheduler.  billytse.dev DSpark page, section 6 (B = sum_r
+ * (1 + l_r); tau = sum_r (1 + sum_{j<=l_r} a_{r,j}); maximise Theta = tau * SPS(B) by
+ * adding positions in descending expected return and stopping as soon as Theta would
+ * fall) and section 7 (early stopping keeps the rule non-anticipating).
+ *
+ * Items (r, j) are ranked by (A desc, r asc, j asc) with A = floor(clamp(a, 0, 1) * 2^32
+ * + 1/2) (NaN counts as 0); sums are exact integers; Theta_n = double(R 2^32 + S_n) *
+ * double(sps[R + n]) and item n is admitted while Theta_n > Theta_{n-1}.  l_r is the
+ * number of admitted positions of request r (a prefix when a is non-increasing in j).
+ *
+ *   a   [R, gamma] fp32 survival; sps [sps_len] fp32 steps/s indexed by token-batch size,
+ *       sps_len >= R * (gamma + 1) + 1
+ *   ->  ell [R] int32, B_total [1] int32 (= R + admitted), theta [1] fp64 (= tau SPS(B))
+ * R * gamma must not exceed 16384.
+ */
+dspark_status dspark_schedule(const float* a, int R, int gamma, const float* sps, int sps_len,
+                              int32_t* ell, int32_t* B_total, double* theta, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Lossless verification.  billytse.dev DSpark page, section 1 (accept x_k with
+ * probability min(1, p_k(x_k) / q_k(x_k)), keep the longest accepted prefix, fix the
+ * first rejected position with a token from the residual) and xhh.club DSpark page
+ * (Q&A on the acceptance rule: the residual is norm(max(0, p - q)), so that
+ * min(q, p) + (p - min(p, q)) = p).  The target distribution is p_k = softmax(T[b, k]).
+ *
+ * For each request b and k = 1..ell[b]: u = U01(stream 1 draw at v = 0); accept iff
+ * u < p_k(x_k) / q_tok[b,k].  At the first reject j: y = argmax over {v: P_j(v) > Q_j(v)}
+ * of log(P_j(v) - Q_j(v)) + g_v (stream 2) with Q_j = softmax(U[b,j] + W1[prev_j] W2)
+ * rebuilt from row_max / row_sumexp; if that set is empty, y = argmax T[b,j,v] + g_v
+ * (stream 2).  If all ell[b] positions are accepted, y is the target's bonus token
+ * argmax T[b, ell+1, v] + g_v (stream 3).
+ *
+ *   T [B, gamma+1, V] fp32 target logits (row gamma+1 is the bonus row), U, W1, W2,
+ *   anchor, tokens, q_tok, row_max, row_sumexp as produced by dspark_draft, ell [B].
+ *   ->  accept_len [B] int32, out_tokens [B, gamma+1] int32 (accepted prefix, then the
+ *       correction or bonus token, then -1), n_out [B] int32 (= accept_len + 1)
+ */
+dspark_status dspark_verify(const float* T, const float* U, const uint16_t* W1,
+                            const uint16_t* W2, const int32_t* anchor, const int32_t* tokens,
+                            const float* q_tok, const float* row_max, const float* row_sumexp,
+                            const int32_t* ell, int B, int gamma, int V, int r, uint64_t seed,
+                            int32_t* accept_len, int32_t* out_tokens, int32_t* n_out,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Reads and clears the device status word kept in `workspace` after synchronising
+ * `stream`.  Returns DSPARK_OK, or the first device-side failure recorded since the last
+ * read (DSPARK_ERR_DEVICE_CHECK, DSPARK_ERR_TIMEOUT), or DSPARK_ERR_CUDA.
+ */
+dspark_status dspark_last_device_status(void* workspace, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H_ */

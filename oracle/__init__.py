@@ -54,6 +54,8 @@ def lib():
         L.dso_gumbel.restype = ctypes.c_double
         L.dso_draft.argtypes = [P, P, P, P, P, i32, i32, i32, i32, u64, P, P, P, P, P, i32]
         L.dso_draft.restype = i32
+        L.dso_markov_bias.argtypes = [P, P, P, i32, i32, i32, P]
+        L.dso_markov_bias.restype = i32
         L.dso_confidence.argtypes = [P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, P]
         L.dso_confidence.restype = i32
         L.dso_schedule.argtypes = [P, i32, i32, P, i32, P, P, P]
@@ -132,6 +134,17 @@ def draft(U, W1, W2, anchor, seed: int, req_ids: Optional[Sequence[int]] = None,
                          _p(out["row_sumexp"]), _p(out["gap"]), nthreads or default_threads())
     _check(rc, "draft")
     out["tokens"] = tokens
+    return out
+
+
+def markov_bias(W1, W2, prev):
+    """bias [n, V] = W1[prev] @ W2 in fp64 (prev = -1 gives a zero row)."""
+    W1 = _c(W1, np.uint16)
+    W2 = _c(W2, np.uint16)
+    V, r = W1.shape
+    prev = _c(prev, np.int32)
+    out = np.zeros((len(prev), V), dtype=np.float64)
+    _check(lib().dso_markov_bias(_p(W1), _p(W2), _p(prev), len(prev), V, r, _p(out)), "markov_bias")
     return out
 
 

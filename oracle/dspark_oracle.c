@@ -211,6 +211,24 @@ int dso_draft(const float *U, const uint16_t *W1, const uint16_t *W2, const int3
     return err;
 }
 
+/* Markov bias alone: out[i][v] = sum_k W1[prev_i][k] * W2[k][v] in double
+ * (prev_i = -1 gives a zero row). */
+int dso_markov_bias(const uint16_t *W1, const uint16_t *W2, const int32_t *prev, int n, int V,
+                    int r, double *out)
+{
+    for (int i = 0; i < n; ++i) {
+        double *o = out + (size_t)i * V;
+        for (int v = 0; v < V; ++v) o[v] = 0.0;
+        if (prev[i] == -1) continue;
+        if (prev[i] < 0 || prev[i] >= V) return DSO_ERR_ARG;
+        for (int k = 0; k < r; ++k) {
+            double e = bf16_to_double(W1[(size_t)prev[i] * r + k]);
+            for (int v = 0; v < V; ++v) o[v] += e * bf16_to_double(W2[(size_t)k * V + v]);
+        }
+    }
+    return DSO_OK;
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Confidence head and survival                                                          */
 /* ------------------------------------------------------------------------------------ */

@@ -1,0 +1,252 @@
+"""DSpark per-step hot path on one GB300 (sm_103a): Python binding of libdspark.
+
+The library behind this binding (``include/dspark.h``) holds the four calls of one
+speculative step -- ``dspark_draft``, ``dspark_confidence``, ``dspark_schedule``,
+``dspark_verify`` -- plus ``dspark_markov_bias``; every step of the computation runs in
+its CUDA kernels.  This module only marshals arguments: it passes device pointers of
+torch tensors and the current CUDA stream through ctypes, and allocates outputs and the
+workspace with torch.  There is no CPU fallback: without the built library and a CUDA
+device every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import numpy as np
+
+from . import _build
+
+STATUS = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_UNSUPPORTED",
+          3: "DSPARK_ERR_CUDA", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_DEVICE_CHECK"}
+
+# (name, restype, argtypes) of every exported symbol, in header order
+_P, _I, _U64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = [
+    ("dspark_status_string", ctypes.c_char_p, [_I]),
+    ("dspark_workspace_bytes", _SZ, [_I, _I, _I, _I, _I]),
+    ("dspark_markov_bias", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    ("dspark_draft", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_confidence", _I, [_P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    ("dspark_schedule", _I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_verify", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64,
+                           _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_last_device_status", _I, [_P, _P]),
+]
+
+_lib = None
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        super().__init__(f"{call} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libdspark.so (building it in-tree first when it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.build() if build_if_missing else _build.LIB
+        if not os.path.exists(path):
+            raise ImportError(f"libdspark.so is not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        for name, res, args in SIGNATURES:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _torch():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("the DSpark kernels need a CUDA device; there is no CPU fallback")
+    return torch
+
+
+def _ptr(t) -> int:
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(call: str, code: int):
+    if code != 0:
+        raise DSparkError(call, code)
+
+
+def workspace_bytes(B: int, gamma: int, V: int, r: int, H: int = 0) -> int:
+    n = lib().dspark_workspace_bytes(B, gamma, V, r, H)
+    if n == 0:
+        raise ValueError(f"unsupported shapes B={B} gamma={gamma} V={V} r={r} H={H}")
+    return int(n)
+
+
+class Workspace:
+    """Caller-owned scratch for the calls (zero-filled, 256-byte aligned torch buffer)."""
+
+    def __init__(self, B: int, gamma: int, V: int, r: int, H: int = 0, device="cuda"):
+        torch = _torch()
+        self.nbytes = workspace_bytes(B, gamma, V, r, H)
+        self.buf = torch.zeros(self.nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 256
+        self.ptr = self.buf.data_ptr() + off
+
+    def status(self, stream=None) -> int:
+        return int(lib().dspark_last_device_status(ctypes.c_void_p(self.ptr), _stream(stream)))
+
+
+def as_bf16_tensor(bits: np.ndarray, device="cuda"):
+    """uint16 bf16 bit patterns (numpy) -> torch.bfloat16 tensor on ``device``."""
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+# ------------------------------------------------------------------------------ calls
+
+def markov_bias(W1, W2, prev, ws: Workspace, out=None, prev_stride: int = 1, stream=None):
+    torch = _torch()
+    V, r = W1.shape
+    B = (prev.numel() + prev_stride - 1) // prev_stride
+    if out is None:
+        out = torch.empty((B, V), dtype=torch.float32, device=W1.device)
+    _check("dspark_markov_bias", lib().dspark_markov_bias(
+        _ptr(W1), _ptr(W2), _ptr(prev), prev_stride, B, V, r, _ptr(out),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
+def draft(U, W1, W2, anchor, seed: int, ws: Workspace, out: Optional[Dict] = None, stream=None):
+    torch = _torch()
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if out is None:
+        out = dict(tokens=torch.empty((B, gamma), dtype=torch.int32, device=U.device),
+                   q_tok=torch.empty((B, gamma), dtype=torch.float32, device=U.device),
+                   row_max=torch.empty((B, gamma), dtype=torch.float32, device=U.device),
+                   row_sumexp=torch.empty((B, gamma), dtype=torch.float32, device=U.device))
+    _check("dspark_draft", lib().dspark_draft(
+        _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchor), B, gamma, V, r, ctypes.c_uint64(seed),
+        _ptr(out["tokens"]), _ptr(out["q_tok"]), _ptr(out["row_max"]), _ptr(out["row_sumexp"]),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
+def confidence(h, anchor, tokens, W1, w_c, b_c: float, ws: Workspace, out=None, stream=None):
+    torch = _torch()
+    B, gamma, H = h.shape
+    V, r = W1.shape
+    if out is None:
+        out = (torch.empty((B, gamma), dtype=torch.float32, device=h.device),
+               torch.empty((B, gamma), dtype=torch.float32, device=h.device))
+    c, a = out
+    _check("dspark_confidence", lib().dspark_confidence(
+        _ptr(h), _ptr(anchor), _ptr(tokens), _ptr(W1), _ptr(w_c), ctypes.c_float(b_c), B, gamma,
+        H, r, V, _ptr(c), _ptr(a), ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return c, a
+
+
+def schedule(a, sps, ws: Workspace, out=None, stream=None):
+    torch = _torch()
+    R, gamma = a.shape
+    if out is None:
+        out = (torch.empty(R, dtype=torch.int32, device=a.device),
+               torch.empty(1, dtype=torch.int32, device=a.device),
+               torch.empty(1, dtype=torch.float64, device=a.device))
+    ell, Bt, th = out
+    _check("dspark_schedule", lib().dspark_schedule(
+        _ptr(a), R, gamma, _ptr(sps), sps.numel(), _ptr(ell), _ptr(Bt), _ptr(th),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return ell, Bt, th
+
+
+def verify(T, U, W1, W2, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed: int,
+           ws: Workspace, out: Optional[Dict] = None, stream=None):
+    torch = _torch()
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=U.device),
+                   out_tokens=torch.empty((B, gamma + 1), dtype=torch.int32, device=U.device),
+                   n_out=torch.empty(B, dtype=torch.int32, device=U.device))
+    _check("dspark_verify", lib().dspark_verify(
+        _ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchor), _ptr(tokens), _ptr(q_tok),
+        _ptr(row_max), _ptr(row_sumexp), _ptr(ell), B, gamma, V, r, ctypes.c_uint64(seed),
+        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["n_out"]),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------------ whole step
+
+class Step:
+    """One speculative step (draft -> confidence -> schedule -> verify) with preallocated
+    outputs and workspace, so that ``run`` launches kernels only (capturable in a CUDA
+    graph).  ``dev`` maps input names (U, T, W1, W2, h, w_c, anchor, sps) to device
+    tensors; ``b_c`` is the confidence-head bias."""
+
+    def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None):
+        torch = _torch()
+        self.dev = dev
+        self.b_c = float(b_c)
+        B, gamma, V = dev["U"].shape
+        r = dev["W1"].shape[1]
+        H = dev["h"].shape[2]
+        self.shape = (B, gamma, V, r, H)
+        self.ws = ws or Workspace(B, gamma, V, r, H, device=dev["U"].device)
+        d = dev["U"].device
+        f32, i32 = torch.float32, torch.int32
+        self.draft_out = dict(tokens=torch.empty((B, gamma), dtype=i32, device=d),
+                              q_tok=torch.empty((B, gamma), dtype=f32, device=d),
+                              row_max=torch.empty((B, gamma), dtype=f32, device=d),
+                              row_sumexp=torch.empty((B, gamma), dtype=f32, device=d))
+        self.conf_out = (torch.empty((B, gamma), dtype=f32, device=d),
+                         torch.empty((B, gamma), dtype=f32, device=d))
+        self.sched_out = (torch.empty(B, dtype=i32, device=d), torch.empty(1, dtype=i32, device=d),
+                          torch.empty(1, dtype=torch.float64, device=d))
+        self.verify_out = dict(accept_len=torch.empty(B, dtype=i32, device=d),
+                               out_tokens=torch.empty((B, gamma + 1), dtype=i32, device=d),
+                               n_out=torch.empty(B, dtype=i32, device=d))
+
+    def run(self, seed: int, stream=None):
+        x = self.dev
+        d = draft(x["U"], x["W1"], x["W2"], x["anchor"], seed, self.ws, self.draft_out, stream)
+        c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
+                          self.conf_out, stream)
+        ell, _, _ = schedule(a, x["sps"], self.ws, self.sched_out, stream)
+        verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d["tokens"], d["q_tok"],
+               d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
+        return self
+
+    def results(self) -> Dict[str, np.ndarray]:
+        out = {k: v.cpu().numpy() for k, v in self.draft_out.items()}
+        out["c"], out["a"] = (t.cpu().numpy() for t in self.conf_out)
+        out["ell"] = self.sched_out[0].cpu().numpy()
+        out["B_total"] = int(self.sched_out[1].item())
+        out["theta"] = float(self.sched_out[2].item())
+        out.update({k: v.cpu().numpy() for k, v in self.verify_out.items()})
+        return out
+
+
+def to_device(inp, device="cuda") -> Dict:
+    """Workload inputs (numpy, see the ``workloads`` module) -> device tensors."""
+    torch = _torch()
+    dev = dict(U=torch.from_numpy(inp.U).to(device), W1=as_bf16_tensor(inp.W1, device),
+               W2=as_bf16_tensor(inp.W2, device), h=torch.from_numpy(inp.h).to(device),
+               w_c=torch.from_numpy(inp.w_c).to(device),
+               anchor=torch.from_numpy(inp.anchor).to(device),
+               sps=torch.from_numpy(inp.sps).to(device))
+    if inp.T is not None:
+        dev["T"] = torch.from_numpy(inp.T).to(device)
+    return dev

@@ -1,0 +1,168 @@
+// extern "C" entry points of libdspark: host-side argument validation, workspace carving
+// and the launch sequence of each call.  See include/dspark.h for the contract.
+#include <stdint.h>
+
+#include "internal.h"
+
+using namespace dspark;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+dspark_status check_shape(int B, int gamma, int V, int r, int H) {
+  if (B < 1 || gamma < 1 || V < 8 || r < 1 || H < 0) return DSPARK_ERR_INVALID_ARG;
+  if (B >= 65536 || gamma > 32) return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)B * (gamma + 1) >= (1LL << 21)) return DSPARK_ERR_UNSUPPORTED;
+  if (V % 8 != 0 || r % 16 != 0 || r > 256 || r < 16 || H % 4 != 0) return DSPARK_ERR_UNSUPPORTED;
+  return DSPARK_OK;
+}
+
+dspark_status check_ws(void* ws, size_t bytes, const Plan& p) {
+  if (!aligned(ws, 256)) return DSPARK_ERR_INVALID_ARG;
+  if (bytes < p.total) return DSPARK_ERR_INVALID_ARG;
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dspark_status_string(dspark_status s) {
+  switch (s) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_ERR_INVALID_ARG: return "DSPARK_ERR_INVALID_ARG";
+    case DSPARK_ERR_UNSUPPORTED: return "DSPARK_ERR_UNSUPPORTED";
+    case DSPARK_ERR_CUDA: return "DSPARK_ERR_CUDA";
+    case DSPARK_ERR_TIMEOUT: return "DSPARK_ERR_TIMEOUT";
+    case DSPARK_ERR_DEVICE_CHECK: return "DSPARK_ERR_DEVICE_CHECK";
+  }
+  return "DSPARK_ERR_UNKNOWN";
+}
+
+size_t dspark_workspace_bytes(int B, int gamma, int V, int r, int H) {
+  if (check_shape(B, gamma, V, r, H) != DSPARK_OK) return 0;
+  return make_plan(B, gamma, V, r, H).total;
+}
+
+dspark_status dspark_markov_bias(const uint16_t* W1, const uint16_t* W2, const int32_t* prev,
+                                 int prev_stride, int B, int V, int r, float* out, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 1 || prev_stride < 1) return DSPARK_ERR_INVALID_ARG;
+  dspark_status st = check_shape(B, 1, V, r, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(W1, 16) || !aligned(W2, 16) || !aligned(prev, 4) || !aligned(out, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
+  CUtensorMap w2_map;
+  if (!encode_w2_map(&w2_map, W2, V, r)) return DSPARK_ERR_CUDA;
+  if (launch_bias_gemm(&w2_map, W1, prev, prev_stride, B, V, r, out, ws_at<int>(workspace, 0),
+                       stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
+                           const int32_t* anchor, int B, int gamma, int V, int r, uint64_t seed,
+                           int32_t* tokens, float* q_tok, float* row_max, float* row_sumexp,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  dspark_status st = check_shape(B, gamma, V, r, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(anchor, 4) ||
+      !aligned(tokens, 4) || !aligned(q_tok, 4) || !aligned(row_max, 4) || !aligned(row_sumexp, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  const Plan p = make_plan(B, gamma, V, r, 0);
+  if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
+
+  CUtensorMap w2_map;
+  if (!encode_w2_map(&w2_map, W2, V, r)) return DSPARK_ERR_CUDA;
+  int* err = ws_at<int>(workspace, p.off_err);
+  float* bias = ws_at<float>(workspace, p.off_bias);
+  RowState* part = ws_at<RowState>(workspace, p.off_part);
+  uint32_t* cnt = ws_at<uint32_t>(workspace, p.off_cnt);
+  if (cudaMemsetAsync(cnt, 0, (size_t)B * sizeof(uint32_t), stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  for (int k = 1; k <= gamma; ++k) {
+    const int32_t* prev = (k == 1) ? anchor : tokens + (k - 2);
+    const int stride = (k == 1) ? 1 : gamma;
+    if (launch_bias_gemm(&w2_map, W1, prev, stride, B, V, r, bias, err, stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (launch_draft_sample(p, U, bias, k, seed, part, cnt, tokens, q_tok, row_max, row_sumexp, err,
+                            stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  }
+  return DSPARK_OK;
+}
+
+dspark_status dspark_confidence(const float* h, const int32_t* anchor, const int32_t* tokens,
+                                const uint16_t* W1, const float* w_c, float b_c, int B, int gamma,
+                                int H, int r, int V, float* c, float* a, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  dspark_status st = check_shape(B, gamma, V, r, H);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(h, 16) || !aligned(w_c, 16) || !aligned(W1, 16) || !aligned(anchor, 4) ||
+      !aligned(tokens, 4) || !aligned(c, 4) || !aligned(a, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
+  int* err = ws_at<int>(workspace, 0);
+  if (launch_confidence(h, anchor, tokens, W1, w_c, b_c, B, gamma, H, r, V, c, a, err, stream) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_schedule(const float* a, int R, int gamma, const float* sps, int sps_len,
+                              int32_t* ell, int32_t* B_total, double* theta, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  if (R < 1 || gamma < 1) return DSPARK_ERR_INVALID_ARG;
+  if (R >= 65536 || gamma > 32 || (long long)R * gamma > kMaxScheduleItems ||
+      (long long)R * (gamma + 1) >= (1LL << 21))
+    return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)sps_len < (long long)R * (gamma + 1) + 1) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(a, 4) || !aligned(sps, 4) || !aligned(ell, 4) || !aligned(B_total, 4) ||
+      !aligned(theta, 8))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
+  int* err = ws_at<int>(workspace, 0);
+  if (launch_schedule(a, R, gamma, sps, ell, B_total, theta, err, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2,
+                            const int32_t* anchor, const int32_t* tokens, const float* q_tok,
+                            const float* row_max, const float* row_sumexp, const int32_t* ell,
+                            int B, int gamma, int V, int r, uint64_t seed, int32_t* accept_len,
+                            int32_t* out_tokens, int32_t* n_out, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+  dspark_status st = check_shape(B, gamma, V, r, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(T, 16) || !aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) ||
+      !aligned(anchor, 4) || !aligned(tokens, 4) || !aligned(q_tok, 4) || !aligned(row_max, 4) ||
+      !aligned(row_sumexp, 4) || !aligned(ell, 4) || !aligned(accept_len, 4) ||
+      !aligned(out_tokens, 4) || !aligned(n_out, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  const Plan p = make_plan(B, gamma, V, r, 0);
+  if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
+  CUtensorMap w2_map;
+  if (!encode_w2_map(&w2_map, W2, V, r)) return DSPARK_ERR_CUDA;
+  if (launch_verify(p, T, U, W1, &w2_map, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed,
+                    accept_len, out_tokens, n_out, workspace, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_last_device_status(void* workspace, cudaStream_t stream) {
+  if (!aligned(workspace, 256)) return DSPARK_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (code != 0) {
+    if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return DSPARK_ERR_CUDA;
+    return (dspark_status)code;
+  }
+  return DSPARK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// Host-side plan of the DSpark calls: launch splits and the workspace layout, plus the
+// launchers each translation unit provides.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+#include "common.cuh"
+
+namespace dspark {
+
+constexpr int kSampleThreads = 256;      // threads of the row-sampling kernels
+constexpr int kTargetCtas = 608;         // CTAs a row-sampling launch aims for (4 per SM)
+constexpr int kMaxScheduleItems = 16384; // R * gamma handled by the one-CTA scheduler
+constexpr int kGemmTileV = 128;          // vocabulary rows per tensor-core tile (MMA M)
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Split of a V-long row into `splits` segments of `seg` elements (seg % 4 == 0).
+struct RowSplit {
+  int splits, seg;
+};
+inline RowSplit row_split(int rows, int V) {
+  int want = cdiv(kTargetCtas, rows > 0 ? rows : 1);
+  int most = cdiv(V, 4 * kSampleThreads);    // at least one float4 per thread per segment
+  if (want > most) want = most;
+  if (want > 64) want = 64;
+  if (want < 1) want = 1;
+  RowSplit s;
+  s.seg = (int)align_up((size_t)cdiv(V, want), 4);
+  s.splits = cdiv(V, s.seg);
+  return s;
+}
+
+// Width of one batch chunk of the bias contraction (MMA N): a multiple of 16, <= 256.
+inline int gemm_chunk(int B) {
+  int nb = (int)align_up((size_t)B, 16);
+  return nb > 256 ? 256 : nb;
+}
+inline size_t gemm_smem_bytes(int r, int NB) {
+  return 1024 + 2 * (size_t)r * 128 + (size_t)cdiv(r, 64) * NB * 128;
+}
+
+struct Plan {
+  int B, gamma, V, r, H;
+  RowSplit draft, stats, ver;
+  // byte offsets into the workspace
+  size_t off_err, off_bias, off_part, off_cnt, off_M, off_lnS, off_p, off_mode, off_pos,
+      off_prev, off_fallback, total;
+};
+
+inline Plan make_plan(int B, int gamma, int V, int r, int H) {
+  Plan p;
+  p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.H = H;
+  p.draft = row_split(B, V);
+  p.stats = row_split(B * gamma, V);
+  p.ver = row_split(B, V);
+  size_t o = 0;
+  p.off_err = o; o += 256;
+  p.off_bias = o; o = align_up(o + (size_t)B * V * sizeof(float), 256);
+  size_t parts = (size_t)B * p.draft.splits;
+  size_t parts_v = (size_t)B * gamma * p.stats.splits + (size_t)B * p.ver.splits;
+  if (parts_v > parts) parts = parts_v;
+  p.off_part = o; o = align_up(o + parts * sizeof(RowState), 256);
+  p.off_cnt = o; o = align_up(o + ((size_t)B * gamma + 2 * (size_t)B) * sizeof(uint32_t), 256);
+  p.off_M = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
+  p.off_lnS = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
+  p.off_p = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
+  p.off_mode = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
+  p.off_pos = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
+  p.off_prev = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
+  p.off_fallback = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
+  p.total = o;
+  return p;
+}
+
+template <typename T>
+inline T* ws_at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ---- launchers (return cudaError_t of the launch) ----
+// bias[b][v] = sum_i W1[prev_b][i] * W2[i][v] for b < B, v < V (rows with prev_b == -1 are 0)
+cudaError_t launch_bias_gemm(const CUtensorMap* w2_map, const uint16_t* W1, const int32_t* prev,
+                             int prev_stride, int B, int V, int r, float* out, int* err,
+                             cudaStream_t stream);
+bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r);
+
+cudaError_t launch_draft_sample(const Plan& p, const float* U, const float* bias, int k,
+                                uint64_t seed, RowState* partials, uint32_t* counters,
+                                int32_t* tokens, float* q_tok, float* row_max, float* row_sumexp,
+                                int* err, cudaStream_t stream);
+
+cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32_t* tokens,
+                              const uint16_t* W1, const float* w_c, float b_c, int B, int gamma,
+                              int H, int r, int V, float* c, float* a, int* err,
+                              cudaStream_t stream);
+
+cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps, int32_t* ell,
+                            int32_t* B_total, double* theta, int* err, cudaStream_t stream);
+
+cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
+                          const CUtensorMap* w2_map, const int32_t* anchor,
+                          const int32_t* tokens, const float* q_tok, const float* row_max,
+                          const float* row_sumexp, const int32_t* ell, uint64_t seed,
+                          int32_t* accept_len, int32_t* out_tokens, int32_t* n_out, void* ws,
+                          cudaStream_t stream);
+
+}  // namespace dspark

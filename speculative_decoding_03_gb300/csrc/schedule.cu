@@ -1,0 +1,151 @@
+// Hardware-aware prefix scheduler in one CTA.
+//
+// billytse.dev DSpark page, section 6: with l_r positions verified for request r, the
+// target processes B = sum_r (1 + l_r) tokens and commits tau = sum_r (1 + sum_{j<=l_r}
+// a_{r,j}) in expectation; the goal is max Theta = tau * SPS(B).  Positions are taken in
+// descending expected return and added one at a time while Theta rises; section 7: the
+// first drop stops the scan (early stopping), which keeps admission non-anticipating.
+//
+// In one CTA: keys (A desc, r asc, j asc) with A = floor(clamp(a, 0, 1) 2^32 + 1/2) are
+// sorted by a bitonic network in shared memory; a block-wide prefix sum gives the exact
+// integer S_n; every n evaluates Theta_n = double(R 2^32 + S_n) * double(sps[R + n])
+// against Theta_{n-1} (plain double products, no fused multiply-add) and the smallest
+// failing n is found with a shared-memory atomicMin.
+#include "internal.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kSchedThreads = 1024;
+
+__device__ __forceinline__ long long fixed_point_a(float a) {
+  double x = (double)a;
+  if (!(x > 0.0)) return 0;
+  if (x > 1.0) x = 1.0;
+  return (long long)floor(__dadd_rn(__dmul_rn(x, 4294967296.0), 0.5));
+}
+
+__device__ __forceinline__ double theta_at(long long R, long long S, float sps) {
+  return __dmul_rn((double)(R * 4294967296LL + S), (double)sps);
+}
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
+    const float* __restrict__ a, int R, int gamma, int Npad, const float* __restrict__ sps,
+    int32_t* __restrict__ ell, int32_t* __restrict__ B_total, double* __restrict__ theta) {
+  extern __shared__ unsigned long long keys[];
+  __shared__ long long warp_tot[32];
+  __shared__ int first_fail;
+  const int tid = threadIdx.x;
+  const int N = R * gamma;
+
+  for (int i = tid; i < Npad; i += kSchedThreads) {
+    unsigned long long key = ~0ull;
+    if (i < N) {
+      const int r = i / gamma, j = i - r * gamma;
+      const long long A = fixed_point_a(a[i]);
+      key = ((unsigned long long)(4294967296LL - A) << 21) | ((unsigned long long)r << 5) |
+            (unsigned long long)j;
+    }
+    keys[i] = key;
+  }
+  for (int r = tid; r < R; r += kSchedThreads) ell[r] = 0;
+  if (tid == 0) first_fail = N + 1;
+  __syncthreads();
+
+  // bitonic sort, ascending key = (A desc, r asc, j asc)
+  for (int size = 2; size <= Npad; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < (Npad >> 1); i += kSchedThreads) {
+        const int lo = 2 * stride * (i / stride) + (i % stride);
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const unsigned long long x = keys[lo], y = keys[hi];
+        if ((x > y) == up) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // exact prefix sums S_n over the sorted A values: contiguous chunks per thread
+  const int per = (N + kSchedThreads - 1) / kSchedThreads;
+  const int c0 = min(N, tid * per), c1 = min(N, c0 + per);
+  long long local = 0;
+  for (int i = c0; i < c1; ++i) local += 4294967296LL - (long long)(keys[i] >> 21);
+  // block exclusive scan of the chunk totals
+  const int lane = tid & 31, warp = tid >> 5;
+  long long incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long t = warp_tot[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const long long u = __shfl_up_sync(0xffffffffu, t, d);
+      if (lane >= d) t += u;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  long long S = incl - local + (warp > 0 ? warp_tot[warp - 1] : 0);  // exclusive prefix
+  int fail = N + 1;
+  for (int i = c0; i < c1; ++i) {
+    const long long A = 4294967296LL - (long long)(keys[i] >> 21);
+    const int n = i + 1;
+    const double th_prev = theta_at(R, S, sps[R + n - 1]);
+    S += A;
+    const double th = theta_at(R, S, sps[R + n]);
+    if (!(th > th_prev)) {
+      fail = n;
+      break;
+    }
+  }
+  if (fail <= N) atomicMin(&first_fail, fail);
+  __syncthreads();
+  const int admitted = first_fail - 1;
+  for (int i = tid; i < admitted; i += kSchedThreads) {
+    const int r = (int)((keys[i] >> 5) & 0xFFFFull);
+    atomicAdd(&ell[r], 1);
+  }
+  // Theta at the stop: S_admitted lies in the chunk holding item `admitted`
+  if (admitted == 0) {
+    if (tid == 0) {
+      *B_total = R;
+      *theta = theta_at(R, 0, sps[R]) / 4294967296.0;
+    }
+  } else if (admitted - 1 >= c0 && admitted - 1 < c1) {
+    long long Sa = incl - local + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int i = c0; i < admitted; ++i) Sa += 4294967296LL - (long long)(keys[i] >> 21);
+    *B_total = R + admitted;
+    *theta = theta_at(R, Sa, sps[R + admitted]) / 4294967296.0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps, int32_t* ell,
+                            int32_t* B_total, double* theta, int* err, cudaStream_t stream) {
+  (void)err;
+  const int N = R * gamma;
+  int Npad = 2;
+  while (Npad < N) Npad <<= 1;
+  const size_t smem = (size_t)Npad * sizeof(unsigned long long);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kMaxScheduleItems * sizeof(unsigned long long)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  schedule_kernel<<<1, kSchedThreads, smem, stream>>>(a, R, gamma, Npad, sps, ell, B_total, theta);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

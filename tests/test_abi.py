@@ -1,0 +1,88 @@
+"""The C-ABI library on the host: it loads, exports every symbol the header declares, and
+its host-side argument validation rejects bad calls before launching anything (these
+calls never reach the GPU, so they run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_03_gb300 as ds
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+FAKE = 0x10000000          # an aligned address that is never dereferenced by these calls
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "dspark.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = ds.lib()
+    declared = _declared_symbols()
+    assert len(declared) >= 8
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(n for n, _, _ in ds.SIGNATURES) == declared
+
+
+def test_status_strings():
+    L = ds.lib()
+    for code, name in ds.STATUS.items():
+        assert L.dspark_status_string(code).decode() == name
+    assert L.dspark_status_string(99).decode() == "DSPARK_ERR_UNKNOWN"
+
+
+def test_workspace_bytes():
+    L = ds.lib()
+    for w in workloads.WORKLOADS:
+        n = L.dspark_workspace_bytes(w.B, w.gamma, w.V, w.r, w.H)
+        assert n >= w.B * w.V * 4 and n % 256 == 0
+    assert L.dspark_workspace_bytes(0, 4, 1000, 16, 64) == 0
+    assert L.dspark_workspace_bytes(4, 4, 1001, 16, 64) == 0      # V % 8 != 0
+    assert L.dspark_workspace_bytes(4, 4, 1000, 24, 64) == 0      # r % 16 != 0
+    assert L.dspark_workspace_bytes(4, 33, 1000, 16, 64) == 0     # gamma > 32
+
+
+def _draft(L, U=FAKE, W1=FAKE, W2=FAKE, anchor=FAKE, B=4, gamma=4, V=1000, r=16, out=FAKE,
+           ws=FAKE, ws_bytes=1 << 30):
+    return L.dspark_draft(U, W1, W2, anchor, B, gamma, V, r, 0, out, out, out, out, ws, ws_bytes, None)
+
+
+def test_draft_validation():
+    L = ds.lib()
+    assert _draft(L, U=None) == INVALID
+    assert _draft(L, U=FAKE + 4) == INVALID              # logits not 16-byte aligned
+    assert _draft(L, ws=FAKE + 16) == INVALID            # workspace not 256-byte aligned
+    assert _draft(L, ws_bytes=100) == INVALID            # workspace too small
+    assert _draft(L, B=0) == INVALID
+    assert _draft(L, V=1004) == UNSUPPORTED
+    assert _draft(L, r=300) == UNSUPPORTED
+    assert _draft(L, gamma=40) == UNSUPPORTED
+    assert _draft(L, B=70000) == UNSUPPORTED
+
+
+def test_schedule_validation():
+    L = ds.lib()
+    call = lambda R=4, gamma=4, sps_len=21, a=FAKE, ws=FAKE: L.dspark_schedule(
+        a, R, gamma, FAKE, sps_len, FAKE, FAKE, FAKE, ws, 1 << 20, None)
+    assert call(sps_len=20) == INVALID                   # table shorter than R (gamma+1) + 1
+    assert call(a=None) == INVALID
+    assert call(R=1024, gamma=17) == UNSUPPORTED         # more than 16384 items
+    assert call(ws=None) == INVALID
+
+
+def test_verify_confidence_and_bias_validation():
+    L = ds.lib()
+    assert L.dspark_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 4, 1000,
+                           16, 0, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == INVALID
+    assert L.dspark_confidence(FAKE + 8, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), 4, 4, 64, 16,
+                               1000, FAKE, FAKE, FAKE, 1 << 20, None) == INVALID
+    assert L.dspark_confidence(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), 4, 4, 66, 16,
+                               1000, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
+    assert L.dspark_markov_bias(FAKE, FAKE, FAKE, 0, 4, 1000, 16, FAKE, FAKE, 1 << 20, None) == INVALID
+    assert L.dspark_markov_bias(FAKE, FAKE, FAKE, 1, 4, 1000, 16, FAKE, None, 1 << 20, None) == INVALID
