@@ -229,6 +229,39 @@ class Step:
                d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
         return self
 
+    # per-step inputs (the backbone's and the target's outputs); the weights, the
+    # confidence head and the SPS table stay resident on the device
+    STEP_INPUTS = ("U", "T", "h", "anchor")
+    STEP_OUTPUTS = ("out_tokens", "accept_len", "n_out")
+
+    def pinned_host_buffers(self):
+        """Pinned host tensors shaped like the per-step inputs and outputs."""
+        torch = _torch()
+        hin = {k: torch.empty(self.dev[k].shape, dtype=self.dev[k].dtype, pin_memory=True)
+               for k in self.STEP_INPUTS}
+        hout = {k: torch.empty(self.verify_out[k].shape, dtype=self.verify_out[k].dtype,
+                               pin_memory=True) for k in self.STEP_OUTPUTS}
+        return hin, hout
+
+    def run_from_host(self, seed: int, host_in: Dict, host_out: Dict, stream=None):
+        """One step from pinned host inputs to pinned host outputs: host->device copies of
+        the step's inputs, the four calls, device->host copies of the verified tokens."""
+        torch = _torch()
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            for k in self.STEP_INPUTS:
+                self.dev[k].copy_(host_in[k], non_blocking=True)
+            self.run(seed, s)
+            for k in self.STEP_OUTPUTS:
+                host_out[k].copy_(self.verify_out[k], non_blocking=True)
+        return host_out
+
+    def step_bytes(self):
+        """(host->device, device->host) bytes of one run_from_host call."""
+        h2d = sum(self.dev[k].numel() * self.dev[k].element_size() for k in self.STEP_INPUTS)
+        d2h = sum(self.verify_out[k].numel() * self.verify_out[k].element_size() for k in self.STEP_OUTPUTS)
+        return int(h2d), int(d2h)
+
     def results(self) -> Dict[str, np.ndarray]:
         out = {k: v.cpu().numpy() for k, v in self.draft_out.items()}
         out["c"], out["a"] = (t.cpu().numpy() for t in self.conf_out)

@@ -55,7 +55,7 @@ dspark_status dspark_markov_bias(const uint16_t* W1, const uint16_t* W2, const i
     return DSPARK_ERR_INVALID_ARG;
   if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
   CUtensorMap w2_map;
-  if (!encode_w2_map(&w2_map, W2, V, r)) return DSPARK_ERR_CUDA;
+  if (!encode_w2_map(&w2_map, W2, V, r, r)) return DSPARK_ERR_CUDA;
   if (launch_bias_gemm(&w2_map, W1, prev, prev_stride, B, V, r, out, ws_at<int>(workspace, 0),
                        stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
@@ -74,23 +74,10 @@ dspark_status dspark_draft(const float* U, const uint16_t* W1, const uint16_t* W
   const Plan p = make_plan(B, gamma, V, r, 0);
   if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
 
-  CUtensorMap w2_map;
-  if (!encode_w2_map(&w2_map, W2, V, r)) return DSPARK_ERR_CUDA;
-  int* err = ws_at<int>(workspace, p.off_err);
-  float* bias = ws_at<float>(workspace, p.off_bias);
-  RowState* part = ws_at<RowState>(workspace, p.off_part);
-  uint32_t* cnt = ws_at<uint32_t>(workspace, p.off_cnt);
-  if (cudaMemsetAsync(cnt, 0, (size_t)B * sizeof(uint32_t), stream) != cudaSuccess)
+  if (launch_draft_fused(W1, W2, U, anchor, B, gamma, V, r, seed, tokens, q_tok, row_max,
+                         row_sumexp, ws_at<char>(workspace, p.off_draft),
+                         ws_at<int>(workspace, p.off_err), stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  for (int k = 1; k <= gamma; ++k) {
-    const int32_t* prev = (k == 1) ? anchor : tokens + (k - 2);
-    const int stride = (k == 1) ? 1 : gamma;
-    if (launch_bias_gemm(&w2_map, W1, prev, stride, B, V, r, bias, err, stream) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    if (launch_draft_sample(p, U, bias, k, seed, part, cnt, tokens, q_tok, row_max, row_sumexp, err,
-                            stream) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-  }
   return DSPARK_OK;
 }
 
@@ -145,7 +132,7 @@ dspark_status dspark_verify(const float* T, const float* U, const uint16_t* W1, 
   const Plan p = make_plan(B, gamma, V, r, 0);
   if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
   CUtensorMap w2_map;
-  if (!encode_w2_map(&w2_map, W2, V, r)) return DSPARK_ERR_CUDA;
+  if (!encode_w2_map(&w2_map, W2, V, r, r)) return DSPARK_ERR_CUDA;
   if (launch_verify(p, T, U, W1, &w2_map, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed,
                     accept_len, out_tokens, n_out, workspace, stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;

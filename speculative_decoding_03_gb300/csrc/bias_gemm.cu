@@ -130,12 +130,7 @@ __global__ void __launch_bounds__(128) bias_gemm_kernel(const __grid_constant__ 
 
 }  // namespace
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
+EncodeTiledFn tensor_map_encoder() {
   static EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -149,13 +144,13 @@ static EncodeTiledFn encode_fn() {
 }
 
 // W2 [r, V] bf16 row-major as a 2-D tensor {V, r}; a box is 64 vocabulary columns (128 B,
-// the 128-byte swizzle span) by all r rows.  Out-of-range columns read as zero.
-bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r) {
-  EncodeTiledFn fn = encode_fn();
+// the 128-byte swizzle span) by box_rows rank rows.  Out-of-range columns read as zero.
+bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_rows) {
+  EncodeTiledFn fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)r};
   cuuint64_t strides[1] = {(cuuint64_t)V * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)r};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W2), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

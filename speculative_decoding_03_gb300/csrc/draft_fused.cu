@@ -1,0 +1,595 @@
+// The whole draft of one step in one persistent, warp-specialised kernel.
+//
+// billytse.dev DSpark page, sections 3.2 and 3.3: for k = 1..gamma, in order,
+//   bias = W1[x_{k-1}] W2;  z = U_k + bias;  x_k ~ softmax(z)   (x_0 = the anchor)
+// for every request at once.  x_k is drawn by Gumbel-max: argmax_v z_v - log E_v with
+// E_v = -log u_v, i.e. argmax_v exp(z_v - M) / E_v for any reference M.
+//
+// Layout of the work: the vocabulary is cut into 128-row tiles; each CTA (one per SM,
+// cooperative launch) owns a contiguous run of tiles for the whole call.  For every
+// position k and every chunk of NB requests ("job") the CTA:
+//   producer warp   streams the W2^T tiles (K-chunks of up to 64 rank rows, MN-major,
+//                   128-byte swizzle) and the U tiles [NB requests x 128 v] into shared-
+//                   memory rings with TMA; neither depends on the drafted tokens, so the
+//                   rings run ahead across positions while the CTA waits for x_k;
+//   MMA warp        issues tcgen05.mma (M = 128 vocabulary rows, N = NB requests, K = r)
+//                   into one of two tensor-memory accumulators;
+//   4 transposers   read the accumulator (lane = vocabulary row), add U and write
+//                   z[b][v] row-major to shared memory;
+//   8 samplers      stream z rows with 128-bit shared loads: each warp owns NB/8 requests
+//                   and keeps, per request, the running max M, per-lane sums of
+//                   exp(z - M), and the warp-shared best ratio exp(z* - M) / E*.  Since
+//                   E = -log(1 - w) >= w (w = 1 - u), an element can only win when
+//                   exp(z - M) > best * w; only such candidates evaluate log1p.
+// After its last tile of position k a CTA publishes per-request partials (M, sum, best
+// score, index, logit) and folds its best (score, index) into a 64-bit atomicMax key;
+// one grid barrier per position (bounded spin) makes every x_k known to every CTA, which
+// then gathers W1[x_k] for the next position.  The CTA with index b mod G merges the
+// partials of request b into x_k, q_k(x_k), max and sum.
+//
+// Failure handling: every wait is bounded (2 s).  A wait that runs out records
+// DSPARK_ERR_TIMEOUT and sets a CTA-wide abort flag; from then on the sampler threads
+// run their fixed loop counts without waiting or working (so their named barriers and
+// the grid barrier still line up), the other roles stop, and the producer and the MMA
+// issuer drain their in-flight copies and MMAs before the CTA releases tensor memory.
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dspark {
+namespace {
+
+using namespace sm100;
+
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kFirstSampler = 6;      // warps 2..5 transpose, 6..13 sample
+constexpr int kSamplers = 8;
+constexpr int kSamplerThreads = kSamplers * 32;
+constexpr int kWStages = 6;           // W2 K-chunk ring (16 KB each at K-chunk 64)
+constexpr int kUStages = 3;           // U tile ring
+constexpr int kKChunkMax = 64;
+constexpr int kNamedBarSamplers = 1;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+struct DraftParams {
+  const uint16_t* W1;
+  const int32_t* anchor;
+  int B, gamma, V, r;
+  int n_tiles, n_chunks, kc;       // kc = K rows per W2 stage (<= 64)
+  uint64_t seed;
+  RowState* partials;              // [2][B][G]
+  unsigned long long* keys;        // [gamma][B], zeroed before launch
+  unsigned int* grid_count;        // zeroed before launch
+  int32_t* tokens;
+  float* q_tok;
+  float* row_max;
+  float* row_sumexp;
+  int* err;
+};
+
+template <int NB>
+struct Smem {
+  static constexpr int kWStageBytes = 2 * kKChunkMax * 128;  // two 64-column boxes
+  static constexpr int kUStageBytes = NB * 128 * 4;
+  static constexpr int kEBytes = NB * 256 * 2;                // up to r = 256
+  static constexpr int kZBytes = NB * 128 * 4;
+  static constexpr int kOffW = 0;
+  static constexpr int kOffU = kOffW + kWStages * kWStageBytes;
+  static constexpr int kOffE = kOffU + kUStages * kUStageBytes;
+  static constexpr int kOffZ = kOffE + 2 * kEBytes;
+  static constexpr int kBytes = kOffZ + 2 * kZBytes;
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Philox4x32-10 with one 32x32->64 multiply per product (the definition of common.cuh:
+// same rounds, constants and key schedule).
+__device__ __forceinline__ uint4 philox_wide(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const unsigned long long p0 = (unsigned long long)0xD2511F53u * c.x;
+    const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
+                   (uint32_t)p0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+__device__ __forceinline__ int token_of_key(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
+
+// Gather E = W1[prev_b] of one chunk (rows b0 .. b0+NB-1) into the K-major, 128-byte
+// swizzled B operand: 16-byte chunk c of row n goes to chunk (c % 8) ^ (n % 8) of the
+// 128-byte line n of K-block c / 8.  Executed by the sampler threads.
+template <int NB>
+__device__ __forceinline__ void gather_E(uint8_t* sE, const DraftParams& p, int b0, int k,
+                                         int tid) {
+  const int kchunks = p.r >> 3;
+  for (int idx = tid; idx < NB * kchunks; idx += kSamplerThreads) {
+    const int n = idx / kchunks, c = idx - n * kchunks;
+    const int b = b0 + n;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (b < p.B) {
+      const int prev = (k == 1) ? p.anchor[b]
+                                : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+      if (prev >= 0 && prev < p.V) {
+        val = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * p.r) + c);
+      } else {
+        set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
+      }
+    }
+    *reinterpret_cast<uint4*>(sE + (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 +
+                              (((c & 7) ^ (n & 7)) << 4)) = val;
+  }
+}
+
+// Merge the G partials of request b at position kp into x, q, max and sum (one warp).
+__device__ __forceinline__ void finalize_row(const DraftParams& p, int b, int kp, int G, int lane) {
+  const int x = token_of_key(__ldcg(p.keys + (size_t)(kp - 1) * p.B + b));
+  const RowState* base = p.partials + ((size_t)(kp & 1) * p.B + b) * G;
+  float m = -INFINITY, zx = -INFINITY;
+  for (int g = lane; g < G; g += 32) m = fmaxf(m, __ldcg(&base[g].m));
+  m = warp_max(m);
+  float s = 0.f;
+  for (int g = lane; g < G; g += 32) {
+    const float mg = __ldcg(&base[g].m);
+    if (mg != -INFINITY) s += __ldcg(&base[g].s) * expf(mg - m);
+    if (__ldcg(&base[g].idx) == x) zx = __ldcg(&base[g].z);
+  }
+  s = warp_sum(s);
+  zx = warp_max(zx);
+  if (lane == 0) {
+    const size_t o = (size_t)b * p.gamma + (kp - 1);
+    p.tokens[o] = x;
+    p.q_tok[o] = expf(zx - m) / s;
+    p.row_max[o] = m;
+    p.row_sumexp[o] = s;
+  }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
+    const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
+    const DraftParams p) {
+  using S = Smem<NB>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t w_full[kWStages], w_empty[kWStages];
+  __shared__ uint64_t u_full[kUStages], u_empty[kUStages];
+  __shared__ uint64_t e_full[2], e_empty[2];
+  __shared__ uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint64_t z_full[2], z_empty[2];
+  __shared__ uint64_t mma_drain;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int t_lo = (int)((long long)cta * p.n_tiles / G);
+  const int t_hi = (int)((long long)(cta + 1) * p.n_tiles / G);
+  const int my_tiles = t_hi - t_lo;
+  const int kc = p.kc;
+  const int n_kchunks = p.r / kc;
+  const int n_jobs = p.gamma * p.n_chunks;
+  const uint32_t tmem_cols = 2 * NB < 32 ? 32 : 2 * NB;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
+    for (int i = 0; i < kUStages; ++i) { mbar_init(&u_full[i], 1); mbar_init(&u_empty[i], 4); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&e_full[i], 1);
+      mbar_init(&e_empty[i], 1);
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+      mbar_init(&z_full[i], 4);
+      mbar_init(&z_empty[i], kSamplers);
+    }
+    mbar_init(&mma_drain, 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_s, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = tmem_base_s;
+
+  // one thread's bounded wait; a timeout aborts the CTA
+  auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (*(volatile int*)&abort_s) return false;
+    if (mbar_wait(bar, parity, kTimeoutNs)) return true;
+    set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+    atomicExch(&abort_s, 1);
+    return false;
+  };
+  // a whole warp's bounded wait with a warp-uniform result
+  auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+    bool ok = wait1(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&w2_map);
+      prefetch_tensormap(&u_map);
+      const uint64_t keep = policy_evict_last();
+      uint64_t stream_pol;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
+      uint32_t ws = 0, us = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+        for (int t = t_lo; t < t_hi && ok; ++t) {
+          const int v0 = t * kGemmTileV;
+          for (int i = 0; i < n_kchunks && ok; ++i) {
+            const int s = ws % kWStages;
+            if (!(ok = wait1(&w_empty[s], ((ws / kWStages) & 1) ^ 1))) break;
+            uint8_t* dst = smem + S::kOffW + s * S::kWStageBytes;
+            mbar_arrive_expect_tx(&w_full[s], 2u * (uint32_t)kc * 128u);
+            tma_load_2d(dst, &w2_map, &w_full[s], v0, i * kc, keep);
+            tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], v0 + 64, i * kc, keep);
+            ++ws;
+          }
+          if (!ok) break;
+          const int su = us % kUStages;
+          if (!(ok = wait1(&u_empty[su], ((us / kUStages) & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(&u_full[su], (uint32_t)S::kUStageBytes);
+          asm volatile(
+              "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+              ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(
+                  smem_u32(smem + S::kOffU + su * S::kUStageBytes)),
+              "l"(reinterpret_cast<uint64_t>(&u_map)), "r"(smem_u32(&u_full[su])), "r"(v0),
+              "r"(k - 1), "r"(c * NB), "l"(stream_pol)
+              : "memory");
+          ++us;
+        }
+      }
+      // drain: every issued copy has landed before the CTA may exit
+      for (uint32_t i = ws > (uint32_t)kWStages ? ws - kWStages : 0; i < ws; ++i)
+        mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, kTimeoutNs);
+      for (uint32_t i = us > (uint32_t)kUStages ? us - kUStages : 0; i < us; ++i)
+        mbar_wait(&u_full[i % kUStages], (i / kUStages) & 1, kTimeoutNs);
+    }
+  } else if (warp == kMmaWarp) {
+    // -------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
+      uint32_t ws = 0, tc = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int eb = job & 1;
+        if (!(ok = wait1(&e_full[eb], (job >> 1) & 1))) break;
+        tc_fence_after_sync();
+        const uint32_t e_addr = smem_u32(smem + S::kOffE + eb * S::kEBytes);
+        for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
+          const int ab = tc & 1;
+          if (!(ok = wait1(&acc_empty[ab], ((tc >> 1) & 1) ^ 1))) break;
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
+          for (int i = 0; i < n_kchunks; ++i, ++ws) {
+            const int s = ws % kWStages;
+            if (!(ok = wait1(&w_full[s], (ws / kWStages) & 1))) break;
+            tc_fence_after_sync();
+            const uint32_t a_addr = smem_u32(smem + S::kOffW + s * S::kWStageBytes);
+            for (int kk = 0; kk < kc / 16; ++kk) {
+              const int kg = i * (kc / 16) + kk;          // global 16-row K step
+              const uint64_t ad = smem_desc(a_addr + (uint32_t)kk * 2048u, (uint32_t)kc * 128u,
+                                            1024u, kSwizzle128B);
+              const uint64_t bd = smem_desc(e_addr + (uint32_t)(kg >> 2) * (uint32_t)NB * 128u +
+                                                (uint32_t)(kg & 3) * 32u,
+                                            16u, 1024u, kSwizzle128B);
+              umma_bf16_f32(d_tmem, ad, bd, idesc, kg > 0 ? 1u : 0u);
+            }
+            umma_commit(&w_empty[s]);
+          }
+          if (!ok) break;
+          umma_commit(&acc_full[ab]);
+        }
+        if (ok) umma_commit(&e_empty[eb]);
+      }
+      // drain: every issued MMA has completed before tensor memory is released
+      umma_commit(&mma_drain);
+      mbar_wait(&mma_drain, 0, kTimeoutNs);
+    }
+  } else if (warp < kFirstSampler) {
+    // ----------------------------------------------- transposers: TMEM (+U) -> z rows
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int vl = q * 32 + lane;                 // vocabulary row inside the tile
+    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint32_t tc = 0;
+    bool ok = true;
+    for (int job = 0; job < n_jobs && ok; ++job) {
+      for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
+        const int ab = tc & 1, zb = tc & 1, su = tc % kUStages;
+        if (!(ok = wait_warp(&acc_full[ab], (tc >> 1) & 1))) break;
+        tc_fence_after_sync();
+        if (!(ok = wait_warp(&u_full[su], (tc / kUStages) & 1))) break;
+        if (!(ok = wait_warp(&z_empty[zb], ((tc >> 1) & 1) ^ 1))) break;
+        const float* Us = reinterpret_cast<const float*>(smem + S::kOffU + su * S::kUStageBytes);
+        float* Zs = reinterpret_cast<float*>(smem + S::kOffZ + zb * S::kZBytes);
+#pragma unroll
+        for (int c16 = 0; c16 < NB; c16 += 16) {
+          float vals[16];
+          tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16), vals);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int b = c16 + j;
+            Zs[b * 128 + vl] = vals[j] + Us[b * 128 + vl];
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[ab]);
+          mbar_arrive(&u_empty[su]);
+          mbar_arrive(&z_full[zb]);
+        }
+      }
+    }
+  } else {
+    // ----------------------------------------------------------------------- samplers
+    constexpr int RPW = NB / kSamplers;           // requests per sampler warp
+    const int sw = warp - kFirstSampler;
+    const int stid = threadIdx.x - kFirstSampler * 32;
+    const uint32_t k0 = (uint32_t)p.seed, k1 = (uint32_t)(p.seed >> 32);
+    uint32_t tc = 0;
+    // publish the E operand of job `j` (chunk c, position k) into its buffer
+    auto publish_E = [&](int j, int c, int k) {
+      if (stid == 0) wait1(&e_empty[j & 1], ((j >> 1) & 1) ^ 1);
+      named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+      if (!*(volatile int*)&abort_s) gather_E<NB>(smem + S::kOffE + (j & 1) * S::kEBytes, p, c * NB, k, stid);
+      fence_proxy_async_smem();
+      named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+      if (stid == 0) mbar_arrive(&e_full[j & 1]);
+    };
+    auto grid_wait = [&](unsigned int target) {
+      if (stid == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u32(p.grid_count) < target) {
+          if (*(volatile int*)&abort_s || globaltimer_ns() - t0 > kTimeoutNs) {
+            set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+            atomicExch(&abort_s, 1);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+    };
+
+    for (int job = 0; job < n_jobs; ++job) {
+      const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+      if (c == 0) {
+        if (k > 1) grid_wait((unsigned int)G * (unsigned int)(k - 1));
+        publish_E(job, 0, k);
+        // merge this CTA's share of position k-1 (off the critical path of the MMA)
+        if (k > 1 && !*(volatile int*)&abort_s)
+          for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row(p, b, k - 1, G, lane);
+      }
+      // the next chunk of the same position only needs x_{k-1}: publish it now
+      if (c + 1 < p.n_chunks) publish_E(job + 1, c + 1, k);
+
+      // per-request running state of this warp's rows (warp-uniform except s)
+      float M[RPW], Tb[RPW], bz[RPW], s[RPW];
+      int bi[RPW];
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        M[i] = -INFINITY; Tb[i] = 0.f; bz[i] = -INFINITY; s[i] = 0.f; bi[i] = -1;
+      }
+      for (int t = 0; t < my_tiles; ++t, ++tc) {
+        const int zb = tc & 1;
+        if (!wait_warp(&z_full[zb], (tc >> 1) & 1)) continue;
+        const float* Zs = reinterpret_cast<const float*>(smem + S::kOffZ + zb * S::kZBytes);
+        const int v = (t_lo + t) * kGemmTileV + 4 * lane;
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+          const int bl = sw * RPW + i;
+          const int b = c * NB + bl;
+          if (b >= p.B) continue;
+          const float4 z4 = *reinterpret_cast<const float4*>(Zs + bl * 128 + 4 * lane);
+          float z[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (v + j >= p.V) z[j] = -INFINITY;
+          const float wm = warp_max(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])));
+          const float Mn = fmaxf(M[i], wm);
+          const float f = ex2_approx((M[i] - Mn) * kLog2e);
+          s[i] *= f;
+          Tb[i] *= f;
+          M[i] = Mn;
+          const uint4 d = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 0u), k0, k1);
+          const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+          float e[4], w[4];
+          bool cand = false;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            e[j] = ex2_approx((z[j] - Mn) * kLog2e);
+            s[i] += e[j];
+            w[j] = one_minus_u01(dw[j]);
+            cand |= e[j] > Tb[i] * w[j];
+          }
+          if (__any_sync(0xffffffffu, cand)) {
+            float br = -1.f, bzz = -INFINITY;
+            int bv = 0x7FFFFFFF;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (e[j] > Tb[i] * w[j]) {
+                const float rr = e[j] / exp1_from_w(w[j]);
+                if (rr > br) { br = rr; bv = v + j; bzz = z[j]; }
+              }
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+              const float obr = __shfl_xor_sync(0xffffffffu, br, o);
+              const int obv = __shfl_xor_sync(0xffffffffu, bv, o);
+              const float obz = __shfl_xor_sync(0xffffffffu, bzz, o);
+              if (obr > br || (obr == br && obv < bv)) { br = obr; bv = obv; bzz = obz; }
+            }
+            if (br > Tb[i]) { Tb[i] = br; bi[i] = bv; bz[i] = bzz; }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&z_empty[zb]);
+      }
+      // publish this CTA's partials of the job's requests
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        const int b = c * NB + sw * RPW + i;
+        const float st = warp_sum(s[i]);
+        if (b < p.B && lane == 0 && !*(volatile int*)&abort_s) {
+          RowState ps;
+          ps.m = M[i];
+          ps.s = st;
+          ps.idx = bi[i];
+          ps.z = bz[i];
+          ps.score = bi[i] >= 0 ? M[i] + logf(Tb[i]) : -INFINITY;
+          p.partials[((size_t)(k & 1) * p.B + b) * G + cta] = ps;
+          if (bi[i] >= 0) atomicMax(p.keys + (size_t)(k - 1) * p.B + b, argmax_key(ps.score, bi[i]));
+          __threadfence();
+        }
+      }
+      if (c + 1 == p.n_chunks) {
+        // this CTA is done with position k: count it in the grid barrier
+        named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+        if (stid == 0) {
+          __threadfence();
+          atomicAdd(p.grid_count, 1u);
+        }
+      }
+    }
+    // the last position: wait for every CTA, then merge this CTA's rows
+    grid_wait((unsigned int)G * (unsigned int)p.gamma);
+    if (!*(volatile int*)&abort_s)
+      for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row(p, b, p.gamma, G, lane);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, tmem_cols);
+}
+
+// U [B, gamma, V] fp32 as a 3-D tensor {V, gamma, B}; a box is 128 vocabulary entries of
+// one position for NB requests.  Out-of-range entries read as zero.
+bool encode_u_map(CUtensorMap* map, const float* U, int B, int gamma, int V, int NB) {
+  EncodeTiledFn fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)gamma * V * 4};
+  cuuint32_t box[3] = {128, 1, (cuuint32_t)NB};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(U), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NB>
+int max_grid() {
+  static int cached = -1;
+  if (cached < 0) {
+    int dev = 0, sms = 0, per = 0;
+    const size_t smem = Smem<NB>::kBytes + 1024;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(draft_fused_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, draft_fused_kernel<NB>, kThreads,
+                                                      smem) != cudaSuccess)
+      return 0;
+    cached = per > 0 ? sms : 0;
+  }
+  return cached;
+}
+
+template <int NB>
+cudaError_t launch_fused(const CUtensorMap& w2_map, const CUtensorMap& u_map, const DraftParams& p,
+                         int grid, cudaStream_t stream) {
+  const size_t smem = Smem<NB>::kBytes + 1024;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, draft_fused_kernel<NB>, w2_map, u_map, p);
+}
+
+}  // namespace
+
+size_t draft_region_bytes(int B, int gamma) {
+  return align_up((size_t)2 * B * kDraftMaxCtas * sizeof(RowState), 256) + 256 +
+         align_up((size_t)gamma * B * sizeof(unsigned long long), 256);
+}
+
+cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const float* U,
+                               const int32_t* anchor, int B, int gamma, int V, int r,
+                               uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
+                               float* row_sumexp, void* region, int* err, cudaStream_t stream) {
+  const int NB = B <= 16 ? 16 : 32;
+  const int n_tiles = cdiv(V, kGemmTileV);
+  int grid = NB == 16 ? max_grid<16>() : max_grid<32>();
+  if (grid <= 0) return cudaErrorInvalidConfiguration;
+  if (grid > n_tiles) grid = n_tiles;
+  if (grid > kDraftMaxCtas) grid = kDraftMaxCtas;
+  DraftParams p;
+  p.W1 = W1;
+  p.anchor = anchor;
+  p.B = B; p.gamma = gamma; p.V = V; p.r = r;
+  p.n_tiles = n_tiles;
+  p.n_chunks = cdiv(B, NB);
+  p.kc = (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16;   // divides r (r % 16 == 0)
+  p.seed = seed;
+  const size_t part_bytes = align_up((size_t)2 * B * kDraftMaxCtas * sizeof(RowState), 256);
+  char* base = static_cast<char*>(region);
+  p.partials = reinterpret_cast<RowState*>(base);
+  p.grid_count = reinterpret_cast<unsigned int*>(base + part_bytes);
+  p.keys = reinterpret_cast<unsigned long long*>(base + part_bytes + 256);
+  p.tokens = tokens;
+  p.q_tok = q_tok;
+  p.row_max = row_max;
+  p.row_sumexp = row_sumexp;
+  p.err = err;
+  cudaError_t e = cudaMemsetAsync(base + part_bytes, 0,
+                                  256 + (size_t)gamma * B * sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  CUtensorMap w2_map, u_map;
+  if (!encode_w2_map(&w2_map, W2, V, r, p.kc)) return cudaErrorInvalidValue;
+  if (!encode_u_map(&u_map, U, B, gamma, V, NB)) return cudaErrorInvalidValue;
+  return NB == 16 ? launch_fused<16>(w2_map, u_map, p, grid, stream)
+                  : launch_fused<32>(w2_map, u_map, p, grid, stream);
+}
+
+}  // namespace dspark

@@ -16,6 +16,7 @@ constexpr int kSampleThreads = 256;      // threads of the row-sampling kernels
 constexpr int kTargetCtas = 608;         // CTAs a row-sampling launch aims for (4 per SM)
 constexpr int kMaxScheduleItems = 16384; // R * gamma handled by the one-CTA scheduler
 constexpr int kGemmTileV = 128;          // vocabulary rows per tensor-core tile (MMA M)
+constexpr int kDraftMaxCtas = 160;       // upper bound of the persistent draft grid
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -45,26 +46,26 @@ inline size_t gemm_smem_bytes(int r, int NB) {
   return 1024 + 2 * (size_t)r * 128 + (size_t)cdiv(r, 64) * NB * 128;
 }
 
+size_t draft_region_bytes(int B, int gamma);
+
 struct Plan {
   int B, gamma, V, r, H;
-  RowSplit draft, stats, ver;
+  RowSplit stats, ver;
   // byte offsets into the workspace
-  size_t off_err, off_bias, off_part, off_cnt, off_M, off_lnS, off_p, off_mode, off_pos,
-      off_prev, off_fallback, total;
+  size_t off_err, off_draft, off_bias, off_part, off_cnt, off_M, off_lnS, off_p, off_mode,
+      off_pos, off_prev, off_fallback, total;
 };
 
 inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   Plan p;
   p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.H = H;
-  p.draft = row_split(B, V);
   p.stats = row_split(B * gamma, V);
   p.ver = row_split(B, V);
   size_t o = 0;
   p.off_err = o; o += 256;
+  p.off_draft = o; o = align_up(o + draft_region_bytes(B, gamma), 256);
   p.off_bias = o; o = align_up(o + (size_t)B * V * sizeof(float), 256);
-  size_t parts = (size_t)B * p.draft.splits;
-  size_t parts_v = (size_t)B * gamma * p.stats.splits + (size_t)B * p.ver.splits;
-  if (parts_v > parts) parts = parts_v;
+  const size_t parts = (size_t)B * gamma * p.stats.splits + (size_t)B * p.ver.splits;
   p.off_part = o; o = align_up(o + parts * sizeof(RowState), 256);
   p.off_cnt = o; o = align_up(o + ((size_t)B * gamma + 2 * (size_t)B) * sizeof(uint32_t), 256);
   p.off_M = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
@@ -83,17 +84,27 @@ inline T* ws_at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// ---- tensor maps ----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+// W2 [r, V] bf16 as {V, r} with boxes of 64 columns x box_rows rows, 128-byte swizzle
+bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_rows);
+
 // ---- launchers (return cudaError_t of the launch) ----
 // bias[b][v] = sum_i W1[prev_b][i] * W2[i][v] for b < B, v < V (rows with prev_b == -1 are 0)
 cudaError_t launch_bias_gemm(const CUtensorMap* w2_map, const uint16_t* W1, const int32_t* prev,
                              int prev_stride, int B, int V, int r, float* out, int* err,
                              cudaStream_t stream);
-bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r);
 
-cudaError_t launch_draft_sample(const Plan& p, const float* U, const float* bias, int k,
-                                uint64_t seed, RowState* partials, uint32_t* counters,
-                                int32_t* tokens, float* q_tok, float* row_max, float* row_sumexp,
-                                int* err, cudaStream_t stream);
+// the whole draft (all gamma positions) in one cooperative launch; `region` holds
+// draft_region_bytes(B, gamma) of workspace
+cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const float* U,
+                               const int32_t* anchor, int B, int gamma, int V, int r,
+                               uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
+                               float* row_sumexp, void* region, int* err, cudaStream_t stream);
 
 cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32_t* tokens,
                               const uint16_t* W1, const float* w_c, float b_c, int B, int gamma,

@@ -146,7 +146,7 @@ def test_schedule_random_tables_and_sizes():
         a = np.cumprod(rng.uniform(0.0, 1.0, size=(R, gamma)) ** 0.3, axis=1).astype(np.float32)
         n = np.arange(R * (gamma + 1) + 1)
         for sps in [1.0 / (1.0 + rng.uniform(0.001, 0.05) * n),
-                    np.where(n <= R * 2, 1.0, 1.0 / (1.0 + (n - R * 2) / (R + 1.0))),
+                    1.0 / (1.0 + np.maximum(0, n - R * 2) / (R + 1.0)),
                     rng.uniform(0.5, 1.0, size=n.size)]:
             sps = sps.astype(np.float32)
             ws = ds.Workspace(R, gamma, 8, 16, 0)

@@ -97,7 +97,7 @@ WORKLOADS: List[Workload] = [
     Workload("scheduler_stress", B=1024, gamma=16, V=32768, r=128, H=2048, seed=4,
              u_std=3.0, spike_p=0.01, spike_amp=8.0,
              noise_std=lambda k: 1.0,
-             sps_fn=lambda b: np.where(b <= 512, 1.0, 1.0 / (1.0 + (b - 512) / 512.0))),
+             sps_fn=lambda b: 1.0 / (1.0 + np.maximum(0, b - 512) / 512.0)),
 ]
 
 BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS}
