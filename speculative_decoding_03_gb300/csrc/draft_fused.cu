@@ -16,11 +16,15 @@
 //                   into one of two tensor-memory accumulators;
 //   4 transposers   read the accumulator (lane = vocabulary row), add U and write
 //                   z[b][v] row-major to shared memory;
-//   8 samplers      stream z rows with 128-bit shared loads: each warp owns NB/8 requests
-//                   and keeps, per request, the running max M, per-lane sums of
-//                   exp(z - M), and the warp-shared best ratio exp(z* - M) / E*.  Since
-//                   E = -log(1 - w) >= w (w = 1 - u), an element can only win when
-//                   exp(z - M) > best * w; only such candidates evaluate log1p.
+//   16 samplers     stream z rows with 128-bit shared loads: each warp owns NB/16
+//                   requests and keeps, per request, a lazy softmax reference M, per-lane
+//                   sums of exp(z - M) and maxima, and the best exact Gumbel score
+//                   z* - log E*.  Since w <= E = -log(1 - w) <= w / (1 - w) (w = 1 - u),
+//                   exp(z - M) / w bounds an element's ratio exp(z - M) / E from above and
+//                   exp(z - M)(1 - w) / w from below: an element is a candidate only if
+//                   its upper bound beats exp(best - M) and the best lower bound of the
+//                   warp's candidates; only the survivors (about one per warp) evaluate
+//                   the exact score with log1p and log, like the oracle.
 // After its last tile of position k a CTA publishes per-request partials (M, sum, best
 // score, index, logit) and folds its best (score, index) into a 64-bit atomicMax key;
 // one grid barrier per position (bounded spin) makes every x_k known to every CTA, which
@@ -40,18 +44,32 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kWarps = 14;
+constexpr int kWarps = 22;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kFirstSampler = 6;      // warps 2..5 transpose, 6..13 sample
-constexpr int kSamplers = 8;
+constexpr int kFirstSampler = 6;      // warps 2..5 transpose, 6..21 sample
+constexpr int kSamplers = 16;
 constexpr int kSamplerThreads = kSamplers * 32;
 constexpr int kWStages = 6;           // W2 K-chunk ring (16 KB each at K-chunk 64)
 constexpr int kUStages = 3;           // U tile ring
 constexpr int kKChunkMax = 64;
 constexpr int kNamedBarSamplers = 1;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr float kLazy = 32.f;             // reference raise margin (exp(32) fits fp32 sums)
+constexpr float kShrink = 1.f - 0x1.0p-16f;  // filter slack, well above fp32 rounding
+
+// 1 - U01(x) = ((~x >> 9) + 1/2) 2^-23 built exactly: the float with bits
+// 0x4B000000 | n is 2^23 + n, and one fused multiply-add removes 2^23 - 1/2.
+__device__ __forceinline__ float w_of_draw(uint32_t x) {
+  const float f = __uint_as_float(0x4B000000u | ((~x) >> 9));
+  return fmaf(f, 0x1.0p-23f, -(1.f - 0x1.0p-24f));
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct DraftParams {
   const uint16_t* W1;
@@ -399,63 +417,108 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       // the next chunk of the same position only needs x_{k-1}: publish it now
       if (c + 1 < p.n_chunks) publish_E(job + 1, c + 1, k);
 
-      // per-request running state of this warp's rows (warp-uniform except s)
-      float M[RPW], Tb[RPW], bz[RPW], s[RPW];
+      // Per-request state of this warp's rows.  Warp-uniform: the lazy reference Mr (a
+      // past warp max, raised only when a logit exceeds it by more than kLazy, so that
+      // exp(z - Mr) cannot overflow), the filter threshold Tf ~ exp(best - Mr) (shrunk by
+      // kShrink to absorb rounding), the best exact score bsc = z* - log E*, its index and
+      // logit.  Per lane: the sum of exp(z - Mr) and the max of z.
+      float Mr[RPW], Tf[RPW], bsc[RPW], bz[RPW], s[RPW], mx[RPW];
       int bi[RPW];
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
-        M[i] = -INFINITY; Tb[i] = 0.f; bz[i] = -INFINITY; s[i] = 0.f; bi[i] = -1;
+        Mr[i] = -INFINITY; Tf[i] = 0.f; bsc[i] = -INFINITY; bz[i] = -INFINITY; s[i] = 0.f;
+        mx[i] = -INFINITY; bi[i] = -1;
       }
       for (int t = 0; t < my_tiles; ++t, ++tc) {
         const int zb = tc & 1;
         if (!wait_warp(&z_full[zb], (tc >> 1) & 1)) continue;
         const float* Zs = reinterpret_cast<const float*>(smem + S::kOffZ + zb * S::kZBytes);
         const int v = (t_lo + t) * kGemmTileV + 4 * lane;
+        const bool ragged = (t_lo + t + 1) * kGemmTileV > p.V;
+        // A: the logits of this lane's 4 vocabulary entries for each row
+        float z[RPW][4];
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
-          const int bl = sw * RPW + i;
-          const int b = c * NB + bl;
-          if (b >= p.B) continue;
-          const float4 z4 = *reinterpret_cast<const float4*>(Zs + bl * 128 + 4 * lane);
-          float z[4] = {z4.x, z4.y, z4.z, z4.w};
+          const float4 z4 = *reinterpret_cast<const float4*>(Zs + (sw * RPW + i) * 128 + 4 * lane);
+          z[i][0] = z4.x; z[i][1] = z4.y; z[i][2] = z4.z; z[i][3] = z4.w;
+          if (ragged) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (v + j >= p.V) z[j] = -INFINITY;
-          const float wm = warp_max(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])));
-          const float Mn = fmaxf(M[i], wm);
-          const float f = ex2_approx((M[i] - Mn) * kLog2e);
-          s[i] *= f;
-          Tb[i] *= f;
-          M[i] = Mn;
-          const uint4 d = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 0u), k0, k1);
-          const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
-          float e[4], w[4];
-          bool cand = false;
+            for (int j = 0; j < 4; ++j)
+              if (v + j >= p.V) z[i][j] = -INFINITY;
+          }
+        }
+        // B: running max and the lazy reference
+        bool raise = false;
+        float lm[RPW];
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+          lm[i] = fmaxf(fmaxf(z[i][0], z[i][1]), fmaxf(z[i][2], z[i][3]));
+          mx[i] = fmaxf(mx[i], lm[i]);
+          raise |= lm[i] > Mr[i] + kLazy;
+        }
+        if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+          for (int i = 0; i < RPW; ++i) {
+            const float wm = warp_max(lm[i]);
+            if (wm > Mr[i] + kLazy) {
+              s[i] *= (Mr[i] == -INFINITY) ? 0.f : expf(Mr[i] - wm);
+              Mr[i] = wm;
+              Tf[i] = bi[i] >= 0 ? expf(bsc[i] - wm) * kShrink : 0.f;
+            }
+          }
+        }
+        // C: the random draws (independent chains across rows)
+        uint4 d[RPW];
+#pragma unroll
+        for (int i = 0; i < RPW; ++i)
+          d[i] = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k,
+                                        (uint32_t)(c * NB + sw * RPW + i), 0u), k0, k1);
+        // D: softmax sums and the cheap candidate test exp(z - Mr) > Tf * w
+        float e[RPW][4], w[RPW][4];
+        unsigned cm[RPW];
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+          const float mL = Mr[i] * kLog2e;
+          const uint32_t dw[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+          cm[i] = 0u;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            e[j] = ex2_approx((z[j] - Mn) * kLog2e);
-            s[i] += e[j];
-            w[j] = one_minus_u01(dw[j]);
-            cand |= e[j] > Tb[i] * w[j];
+            e[i][j] = ex2_approx(fmaf(z[i][j], kLog2e, -mL));
+            s[i] += e[i][j];
+            w[i][j] = w_of_draw(dw[j]);
+            cm[i] |= (e[i][j] > Tf[i] * w[i][j] ? 1u : 0u) << j;
           }
-          if (__any_sync(0xffffffffu, cand)) {
-            float br = -1.f, bzz = -INFINITY;
-            int bv = 0x7FFFFFFF;
+        }
+        // E: candidates.  Tighten the threshold with the best lower bound
+        // e (1 - w) / w <= e / E among them, then score the survivors exactly.
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+          if (__any_sync(0xffffffffu, cm[i] != 0u)) {
+            float L = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if ((cm[i] >> j) & 1u) L = fmaxf(L, e[i][j] * (1.f - w[i][j]) * rcp_approx(w[i][j]));
+            const float Teff = fmaxf(Tf[i], warp_max(L) * kShrink);
+            float sc = -INFINITY, szz = -INFINITY;
+            int sv = 0x7FFFFFFF;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              if (e[j] > Tb[i] * w[j]) {
-                const float rr = e[j] / exp1_from_w(w[j]);
-                if (rr > br) { br = rr; bv = v + j; bzz = z[j]; }
+              if (((cm[i] >> j) & 1u) && e[i][j] > Teff * w[i][j]) {
+                const float scj = z[i][j] - logf(exp1_from_w(w[i][j]));
+                if (scj > sc) { sc = scj; sv = v + j; szz = z[i][j]; }
               }
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) {
-              const float obr = __shfl_xor_sync(0xffffffffu, br, o);
-              const int obv = __shfl_xor_sync(0xffffffffu, bv, o);
-              const float obz = __shfl_xor_sync(0xffffffffu, bzz, o);
-              if (obr > br || (obr == br && obv < bv)) { br = obr; bv = obv; bzz = obz; }
+              const float osc = __shfl_xor_sync(0xffffffffu, sc, o);
+              const int osv = __shfl_xor_sync(0xffffffffu, sv, o);
+              const float osz = __shfl_xor_sync(0xffffffffu, szz, o);
+              if (osc > sc || (osc == sc && osv < sv)) { sc = osc; sv = osv; szz = osz; }
             }
-            if (br > Tb[i]) { Tb[i] = br; bi[i] = bv; bz[i] = bzz; }
+            if (sv != 0x7FFFFFFF && better(sc, sv, bsc[i], bi[i])) {
+              bsc[i] = sc; bi[i] = sv; bz[i] = szz;
+              Tf[i] = expf(sc - Mr[i]) * kShrink;
+            }
           }
         }
         __syncwarp();
@@ -465,16 +528,17 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
         const int b = c * NB + sw * RPW + i;
-        const float st = warp_sum(s[i]);
+        const float m = warp_max(mx[i]);
+        const float st = warp_sum(s[i]) * (Mr[i] == -INFINITY ? 0.f : expf(Mr[i] - m));
         if (b < p.B && lane == 0 && !*(volatile int*)&abort_s) {
           RowState ps;
-          ps.m = M[i];
+          ps.m = m;
           ps.s = st;
           ps.idx = bi[i];
           ps.z = bz[i];
-          ps.score = bi[i] >= 0 ? M[i] + logf(Tb[i]) : -INFINITY;
+          ps.score = bsc[i];
           p.partials[((size_t)(k & 1) * p.B + b) * G + cta] = ps;
-          if (bi[i] >= 0) atomicMax(p.keys + (size_t)(k - 1) * p.B + b, argmax_key(ps.score, bi[i]));
+          if (bi[i] >= 0) atomicMax(p.keys + (size_t)(k - 1) * p.B + b, argmax_key(bsc[i], bi[i]));
           __threadfence();
         }
       }
