@@ -171,6 +171,30 @@ dspark_status dspark_verify(const float* T, const float* U, const uint16_t* W1,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * The draft of dspark_draft for callers that cannot allocate device memory when they
+ * draft (a serving loop whose device memory is all reserved by its own pool, a plugin
+ * that is handed only its input and output buffers, code where a cudaMalloc would
+ * synchronise or fail).  The paper has no counterpart: this is a packaging of the same
+ * kernel.  Same arguments, outputs and results as dspark_draft, without the workspace:
+ * the kernel's scratch lives in a fixed array inside the library, about 1.7 MB, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Limits: B <= 256 and gamma <= 32 (otherwise DSPARK_ERR_UNSUPPORTED), plus the
+ *     shape limits above.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the array: calls whose kernels overlap on the GPU (other streams,
+ *     other host threads) race; serialise them.  Each call clears what must start at
+ *     zero on its stream.
+ *   - Device-side checks are not reported by this entry point (there is no workspace
+ *     status word); use dspark_draft to diagnose them.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree.
+ */
+dspark_status dspark_draft_noalloc(const float* U, const uint16_t* W1, const uint16_t* W2,
+                                   const int32_t* anchor, int B, int gamma, int V, int r,
+                                   uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
+                                   float* row_sumexp, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word kept in `workspace` after synchronising
  * `stream`.  Returns DSPARK_OK, or the first device-side failure recorded since the last
  * read (DSPARK_ERR_DEVICE_CHECK, DSPARK_ERR_TIMEOUT), or DSPARK_ERR_CUDA.

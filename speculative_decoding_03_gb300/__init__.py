@@ -32,6 +32,7 @@ SIGNATURES = [
     ("dspark_schedule", _I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_verify", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64,
                            _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_draft_noalloc", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P]),
     ("dspark_last_device_status", _I, [_P, _P]),
 ]
 
