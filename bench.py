@@ -209,6 +209,16 @@ def run_ours(args, w):
     for i in range(args.warmup):
         step.run(seed=w.seed + i)
     barrier()
+    n_ring = 8
+    if args.graph:
+        # a ring of captured steps with distinct seeds: one host call per step
+        graphs = step.capture([w.seed + args.warmup + j for j in range(n_ring)])
+        for g in graphs:
+            g.replay()
+        barrier()
+        run_step = lambda i: graphs[i % n_ring].replay()
+    else:
+        run_step = lambda i: step.run(seed=w.seed + args.warmup + i)
 
     # ---- timed region: K steps, inputs resident in HBM
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -216,7 +226,7 @@ def run_ours(args, w):
         barrier()
         ev0.record(stream)
         for i in range(args.steps):
-            step.run(seed=w.seed + args.warmup + i)
+            run_step(i)
         ev1.record(stream)
         barrier()
     t_ms = ev0.elapsed_time(ev1)
@@ -227,17 +237,48 @@ def run_ours(args, w):
     ms_per_step = t_ms / args.steps
     res = step.results()
 
-    # ---- dominant kernel: the draft call, timed alone with events on its stream
+    # ---- dominant kernel: the draft launch, timed alone with events on its stream
     ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x = step.dev
     n_draft = max(3, min(args.steps, 50))
+    if args.graph:
+        dgraphs = step.capture([w.seed + j for j in range(n_ring)], draft_only=True)
+        for g in dgraphs:
+            g.replay()
+        run_draft = lambda i: dgraphs[i % n_ring].replay()
+    else:
+        run_draft = lambda i: ds.draft_packed(x["U"], x["W1"], step.W2p, x["anchor"], w.seed + i,
+                                              step.ws, step.draft_out)
     barrier()
     ev_a.record(stream)
     for i in range(n_draft):
-        ds.draft(x["U"], x["W1"], x["W2"], x["anchor"], w.seed + i, step.ws, step.draft_out)
+        run_draft(i)
     ev_b.record(stream)
     barrier()
     draft_ms = ev_a.elapsed_time(ev_b) / n_draft
+
+    # ---- per-call breakdown (warm, eager, events between the calls on one stream)
+    n_bd = max(3, min(args.steps, 20))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    acc = [0.0] * 4
+    d_out, c_out, s_out, v_out = step.draft_out, step.conf_out, step.sched_out, step.verify_out
+    for i in range(n_bd):
+        sd = w.seed + 500 + i
+        evs[0].record(stream)
+        ds.draft_packed(x["U"], x["W1"], step.W2p, x["anchor"], sd, step.ws, d_out)
+        evs[1].record(stream)
+        ds.confidence(x["h"], x["anchor"], d_out["tokens"], x["W1"], x["w_c"], step.b_c, step.ws, c_out)
+        evs[2].record(stream)
+        ds.schedule(c_out[1], x["sps"], step.ws, s_out)
+        evs[3].record(stream)
+        ds.verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d_out["tokens"], d_out["q_tok"],
+                  d_out["row_max"], d_out["row_sumexp"], s_out[0], sd, step.ws, v_out)
+        evs[4].record(stream)
+        torch.cuda.synchronize()
+        for j in range(4):
+            acc[j] += evs[j].elapsed_time(evs[j + 1])
+    breakdown = {k: acc[j] / n_bd for j, k in enumerate(("draft_ms", "confidence_ms", "schedule_ms",
+                                                          "verify_ms"))}
 
     # ---- end to end through the public API with pinned host buffers
     hin, hout = step.pinned_host_buffers()
@@ -274,8 +315,9 @@ def run_ours(args, w):
         "config": dict(w.describe(), weights="bf16", logits="fp32",
                        l2="inputs larger than L2 (U+T alone %.0f MB per step)" %
                           ((w.B * w.gamma * w.V + w.B * (w.gamma + 1) * w.V) * 4 / 1e6),
-                       parallelism=f"replicas x{world}"),
-        "roofline": {"bound": "hbm", "kernel": "dspark_draft (bias contraction + sampling, all gamma positions)",
+                       parallelism=f"replicas x{world}",
+                       launch="cuda graph ring of 8 seeds" if args.graph else "eager"),
+        "roofline": {"bound": "hbm", "kernel": "draft_fused_kernel via dspark_draft_packed (bias contraction + sampling, all gamma positions)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
@@ -283,6 +325,7 @@ def run_ours(args, w):
                      "unit": "GB/s", "frac": sbytes / (ms_per_step * 1e-3) / 1e9 / peak},
         "accept": {"mean_ell": float(np.mean(res["ell"])), "mean_accept_len": float(np.mean(res["accept_len"])),
                    "B_total": res["B_total"], "theta": res["theta"]},
+        "breakdown": breakdown,
         "e2e": {"value": world * w.B * w.gamma / e2e_s, "unit": "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -305,6 +348,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-requests", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch every call from Python instead of replaying captured steps")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

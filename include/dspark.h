@@ -108,6 +108,32 @@ dspark_status dspark_draft(const float* U, const uint16_t* W1, const uint16_t* W
                            cudaStream_t stream);
 
 /*
+ * Packed Markov-head projection.  The draft kernel's tensor-core operand is the W2^T
+ * vocabulary tile; read from W2 [r, V] a tile is r short rows spread over all of W2.
+ * dspark_pack_w2 rearranges W2 once (at weight-load time) into contiguous per-tile
+ * images of exactly that operand, and dspark_draft_packed streams them with one bulk
+ * copy per 16 KB chunk.  Results are identical to dspark_draft.
+ *
+ *   dspark_packed_w2_bytes(V, r): bytes of the packed copy (ceil(V/128)*128 * r * 2);
+ *   0 on unsupported shapes.
+ *   dspark_pack_w2: W2 [r, V] bf16 -> W2p (caller-owned, W2p_bytes >= the size above,
+ *   16-byte aligned).  Layout, in 16-byte units, for tile t, rank chunk i of kc rows
+ *   (kc = 64 if r % 64 == 0, else 32 if r % 32 == 0, else 16), half h, rank row kl,
+ *   slot s:  W2p[t][i][h][kl][s] = W2[i*kc + kl][t*128 + 64h + 8(s ^ (kl % 8)) .. +7],
+ *   zero beyond V.
+ *   dspark_draft_packed: dspark_draft with W2p in place of W2 (same arguments,
+ *   workspace and outputs otherwise).
+ */
+size_t dspark_packed_w2_bytes(int V, int r);
+dspark_status dspark_pack_w2(const uint16_t* W2, int V, int r, uint16_t* W2p, size_t W2p_bytes,
+                             cudaStream_t stream);
+dspark_status dspark_draft_packed(const float* U, const uint16_t* W1, const uint16_t* W2p,
+                                  const int32_t* anchor, int B, int gamma, int V, int r,
+                                  uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
+                                  float* row_sumexp, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/*
  * Confidence head and survival.  weigao.cc DSpark-vs-MTP page, "3. confidence head"
  * (c_k = P(position k survives | positions < k accepted), one linear layer on
  * [output_hidden_k ; markov_embedding(prev_token)]) and billytse.dev DSpark page,

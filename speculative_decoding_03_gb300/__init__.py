@@ -27,6 +27,9 @@ SIGNATURES = [
     ("dspark_status_string", ctypes.c_char_p, [_I]),
     ("dspark_workspace_bytes", _SZ, [_I, _I, _I, _I, _I]),
     ("dspark_markov_bias", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    ("dspark_packed_w2_bytes", _SZ, [_I, _I]),
+    ("dspark_pack_w2", _I, [_P, _I, _I, _P, _SZ, _P]),
+    ("dspark_draft_packed", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_draft", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_confidence", _I, [_P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     ("dspark_schedule", _I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
@@ -144,6 +147,35 @@ def draft(U, W1, W2, anchor, seed: int, ws: Workspace, out: Optional[Dict] = Non
     return out
 
 
+def pack_w2(W2, stream=None):
+    """Packed copy of W2 [r, V] for draft_packed (a device tensor; done once per weights)."""
+    torch = _torch()
+    r, V = W2.shape
+    n = lib().dspark_packed_w2_bytes(V, r)
+    if n == 0:
+        raise ValueError(f"unsupported shapes V={V} r={r}")
+    W2p = torch.empty(n // 2, dtype=torch.bfloat16, device=W2.device)
+    _check("dspark_pack_w2", lib().dspark_pack_w2(_ptr(W2), V, r, _ptr(W2p), n, _stream(stream)))
+    return W2p
+
+
+def draft_packed(U, W1, W2p, anchor, seed: int, ws: Workspace, out: Optional[Dict] = None,
+                 stream=None):
+    torch = _torch()
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if out is None:
+        out = dict(tokens=torch.empty((B, gamma), dtype=torch.int32, device=U.device),
+                   q_tok=torch.empty((B, gamma), dtype=torch.float32, device=U.device),
+                   row_max=torch.empty((B, gamma), dtype=torch.float32, device=U.device),
+                   row_sumexp=torch.empty((B, gamma), dtype=torch.float32, device=U.device))
+    _check("dspark_draft_packed", lib().dspark_draft_packed(
+        _ptr(U), _ptr(W1), _ptr(W2p), _ptr(anchor), B, gamma, V, r, ctypes.c_uint64(seed),
+        _ptr(out["tokens"]), _ptr(out["q_tok"]), _ptr(out["row_max"]), _ptr(out["row_sumexp"]),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
 def confidence(h, anchor, tokens, W1, w_c, b_c: float, ws: Workspace, out=None, stream=None):
     torch = _torch()
     B, gamma, H = h.shape
@@ -197,9 +229,11 @@ class Step:
     graph).  ``dev`` maps input names (U, T, W1, W2, h, w_c, anchor, sps) to device
     tensors; ``b_c`` is the confidence-head bias."""
 
-    def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None):
+    def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None, packed: bool = True):
         torch = _torch()
         self.dev = dev
+        # the draft streams W2 from a packed copy made once here (weight preparation)
+        self.W2p = pack_w2(dev["W2"]) if packed else None
         self.b_c = float(b_c)
         B, gamma, V = dev["U"].shape
         r = dev["W1"].shape[1]
@@ -222,13 +256,34 @@ class Step:
 
     def run(self, seed: int, stream=None):
         x = self.dev
-        d = draft(x["U"], x["W1"], x["W2"], x["anchor"], seed, self.ws, self.draft_out, stream)
+        if self.W2p is not None:
+            d = draft_packed(x["U"], x["W1"], self.W2p, x["anchor"], seed, self.ws, self.draft_out, stream)
+        else:
+            d = draft(x["U"], x["W1"], x["W2"], x["anchor"], seed, self.ws, self.draft_out, stream)
         c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
                           self.conf_out, stream)
         ell, _, _ = schedule(a, x["sps"], self.ws, self.sched_out, stream)
         verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d["tokens"], d["q_tok"],
                d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
         return self
+
+    def capture(self, seeds, draft_only: bool = False):
+        """CUDA graphs of run(seed) (or of the draft call alone), one per seed.  The seed
+        is a launch argument, so each graph replays with its own random stream."""
+        torch = _torch()
+        graphs = []
+        x = self.dev
+        for sd in seeds:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                if draft_only and self.W2p is not None:
+                    draft_packed(x["U"], x["W1"], self.W2p, x["anchor"], sd, self.ws, self.draft_out)
+                elif draft_only:
+                    draft(x["U"], x["W1"], x["W2"], x["anchor"], sd, self.ws, self.draft_out)
+                else:
+                    self.run(sd)
+            graphs.append(g)
+        return graphs
 
     # per-step inputs (the backbone's and the target's outputs); the weights, the
     # confidence head and the SPS table stay resident on the device

@@ -14,9 +14,11 @@
 //                   rings run ahead across positions while the CTA waits for x_k;
 //   MMA warp        issues tcgen05.mma (M = 128 vocabulary rows, N = NB requests, K = r)
 //                   into one of two tensor-memory accumulators;
-//   4 transposers   read the accumulator (lane = vocabulary row), add U and write
-//                   z[b][v] row-major to shared memory;
-//   16 samplers     stream z rows with 128-bit shared loads: each warp owns NB/16
+//   4 transposers   read the accumulator (lane = vocabulary row) and write the bias
+//                   rows [b][v] to shared memory (four accumulators and four bias tiles
+//                   in flight, so the MMA, transposer and sampler stages overlap);
+//   16 samplers     add the U tile to the bias rows (both row-contiguous, 128-bit shared
+//                   loads) to get z rows; each warp owns NB/16
 //                   requests and keeps, per request, a lazy softmax reference M, per-lane
 //                   sums of exp(z - M) and maxima, and the best exact Gumbel score
 //                   z* - log E*.  Since w <= E = -log(1 - w) <= w / (1 - w) (w = 1 - u),
@@ -36,6 +38,8 @@
 // run their fixed loop counts without waiting or working (so their named barriers and
 // the grid barrier still line up), the other roles stop, and the producer and the MMA
 // issuer drain their in-flight copies and MMAs before the CTA releases tensor memory.
+#include <string.h>
+
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -51,8 +55,9 @@ constexpr int kMmaWarp = 1;
 constexpr int kFirstSampler = 6;      // warps 2..5 transpose, 6..21 sample
 constexpr int kSamplers = 16;
 constexpr int kSamplerThreads = kSamplers * 32;
-constexpr int kWStages = 6;           // W2 K-chunk ring (16 KB each at K-chunk 64)
-constexpr int kUStages = 3;           // U tile ring
+constexpr int kWStages = 4;           // W2 K-chunk ring (16 KB each at K-chunk 64)
+constexpr int kDepth = 4;             // accumulators in TMEM, z tiles and U tiles in flight
+constexpr int kUStages = kDepth;      // U tile ring (consumed by the samplers)
 constexpr int kKChunkMax = 64;
 constexpr int kNamedBarSamplers = 1;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -73,6 +78,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 struct DraftParams {
   const uint16_t* W1;
+  const uint16_t* W2p;             // packed W2 tile images (null: tiles come by TMA from W2)
   const int32_t* anchor;
   int B, gamma, V, r;
   int n_tiles, n_chunks, kc;       // kc = K rows per W2 stage (<= 64)
@@ -97,7 +103,7 @@ struct Smem {
   static constexpr int kOffU = kOffW + kWStages * kWStageBytes;
   static constexpr int kOffE = kOffU + kUStages * kUStageBytes;
   static constexpr int kOffZ = kOffE + 2 * kEBytes;
-  static constexpr int kBytes = kOffZ + 2 * kZBytes;
+  static constexpr int kBytes = kOffZ + kDepth * kZBytes;
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -198,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   __shared__ uint64_t w_full[kWStages], w_empty[kWStages];
   __shared__ uint64_t u_full[kUStages], u_empty[kUStages];
   __shared__ uint64_t e_full[2], e_empty[2];
-  __shared__ uint64_t acc_full[2], acc_empty[2];
-  __shared__ uint64_t z_full[2], z_empty[2];
+  __shared__ uint64_t acc_full[kDepth], acc_empty[kDepth];
+  __shared__ uint64_t z_full[kDepth], z_empty[kDepth];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -214,14 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   const int kc = p.kc;
   const int n_kchunks = p.r / kc;
   const int n_jobs = p.gamma * p.n_chunks;
-  const uint32_t tmem_cols = 2 * NB < 32 ? 32 : 2 * NB;
+  const uint32_t tmem_cols = kDepth * NB < 32 ? 32 : kDepth * NB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
-    for (int i = 0; i < kUStages; ++i) { mbar_init(&u_full[i], 1); mbar_init(&u_empty[i], 4); }
+    for (int i = 0; i < kUStages; ++i) { mbar_init(&u_full[i], 1); mbar_init(&u_empty[i], kSamplers); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&e_full[i], 1);
       mbar_init(&e_empty[i], 1);
+    }
+    for (int i = 0; i < kDepth; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
       mbar_init(&z_full[i], 4);
@@ -273,8 +281,19 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
             if (!(ok = wait1(&w_empty[s], ((ws / kWStages) & 1) ^ 1))) break;
             uint8_t* dst = smem + S::kOffW + s * S::kWStageBytes;
             mbar_arrive_expect_tx(&w_full[s], 2u * (uint32_t)kc * 128u);
-            tma_load_2d(dst, &w2_map, &w_full[s], v0, i * kc, keep);
-            tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], v0 + 64, i * kc, keep);
+            if (p.W2p) {
+              // packed: the stage image is contiguous, one 1-D bulk copy
+              const uint16_t* src = p.W2p + ((size_t)t * n_kchunks + i) * (size_t)kc * 128;
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                  " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+                  "l"(reinterpret_cast<uint64_t>(src)), "r"(2u * (uint32_t)kc * 128u),
+                  "r"(smem_u32(&w_full[s])), "l"(keep)
+                  : "memory");
+            } else {
+              tma_load_2d(dst, &w2_map, &w_full[s], v0, i * kc, keep);
+              tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], v0 + 64, i * kc, keep);
+            }
             ++ws;
           }
           if (!ok) break;
@@ -309,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         tc_fence_after_sync();
         const uint32_t e_addr = smem_u32(smem + S::kOffE + eb * S::kEBytes);
         for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-          const int ab = tc & 1;
-          if (!(ok = wait1(&acc_empty[ab], ((tc >> 1) & 1) ^ 1))) break;
+          const int ab = tc % kDepth;
+          if (!(ok = wait1(&acc_empty[ab], ((tc / kDepth) & 1) ^ 1))) break;
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
@@ -347,30 +366,24 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     bool ok = true;
     for (int job = 0; job < n_jobs && ok; ++job) {
       for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-        const int ab = tc & 1, zb = tc & 1, su = tc % kUStages;
-        if (!(ok = wait_warp(&acc_full[ab], (tc >> 1) & 1))) break;
+        const int ab = tc % kDepth;
+        const uint32_t par = (tc / kDepth) & 1;
+        if (!(ok = wait_warp(&acc_full[ab], par))) break;
         tc_fence_after_sync();
-        if (!(ok = wait_warp(&u_full[su], (tc / kUStages) & 1))) break;
-        if (!(ok = wait_warp(&z_empty[zb], ((tc >> 1) & 1) ^ 1))) break;
-        const float* Us = reinterpret_cast<const float*>(smem + S::kOffU + su * S::kUStageBytes);
-        float* Zs = reinterpret_cast<float*>(smem + S::kOffZ + zb * S::kZBytes);
+        if (!(ok = wait_warp(&z_empty[ab], par ^ 1))) break;
+        float* Zs = reinterpret_cast<float*>(smem + S::kOffZ + ab * S::kZBytes);
+        float vals[NB];
 #pragma unroll
-        for (int c16 = 0; c16 < NB; c16 += 16) {
-          float vals[16];
-          tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16), vals);
-          tmem_ld_wait();
+        for (int c16 = 0; c16 < NB; c16 += 16)
+          tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16), *reinterpret_cast<float(*)[16]>(vals + c16));
+        tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int b = c16 + j;
-            Zs[b * 128 + vl] = vals[j] + Us[b * 128 + vl];
-          }
-        }
+        for (int b = 0; b < NB; ++b) Zs[b * 128 + vl] = vals[b];
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&acc_empty[ab]);
-          mbar_arrive(&u_empty[su]);
-          mbar_arrive(&z_full[zb]);
+          mbar_arrive(&z_full[ab]);
         }
       }
     }
@@ -430,9 +443,12 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         mx[i] = -INFINITY; bi[i] = -1;
       }
       for (int t = 0; t < my_tiles; ++t, ++tc) {
-        const int zb = tc & 1;
-        if (!wait_warp(&z_full[zb], (tc >> 1) & 1)) continue;
+        const int zb = tc % kDepth;
+        const uint32_t par = (tc / kDepth) & 1;
+        if (!wait_warp(&z_full[zb], par)) continue;
+        if (!wait_warp(&u_full[zb], par)) continue;
         const float* Zs = reinterpret_cast<const float*>(smem + S::kOffZ + zb * S::kZBytes);
+        const float* Us = reinterpret_cast<const float*>(smem + S::kOffU + zb * S::kUStageBytes);
         const int v = (t_lo + t) * kGemmTileV + 4 * lane;
         const bool ragged = (t_lo + t + 1) * kGemmTileV > p.V;
         // A: the logits of this lane's 4 vocabulary entries for each row
@@ -440,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
           const float4 z4 = *reinterpret_cast<const float4*>(Zs + (sw * RPW + i) * 128 + 4 * lane);
-          z[i][0] = z4.x; z[i][1] = z4.y; z[i][2] = z4.z; z[i][3] = z4.w;
+          const float4 u4 = *reinterpret_cast<const float4*>(Us + (sw * RPW + i) * 128 + 4 * lane);
+          z[i][0] = z4.x + u4.x; z[i][1] = z4.y + u4.y; z[i][2] = z4.z + u4.z; z[i][3] = z4.w + u4.w;
           if (ragged) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -522,7 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&z_empty[zb]);
+        if (lane == 0) {
+          mbar_arrive(&z_empty[zb]);
+          mbar_arrive(&u_empty[zb]);
+        }
       }
       // publish this CTA's partials of the job's requests
 #pragma unroll
@@ -618,10 +638,14 @@ size_t draft_region_bytes(int B, int gamma) {
          align_up((size_t)gamma * B * sizeof(unsigned long long), 256);
 }
 
-cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const float* U,
-                               const int32_t* anchor, int B, int gamma, int V, int r,
-                               uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
-                               float* row_sumexp, void* region, int* err, cudaStream_t stream) {
+int draft_kchunk(int r) { return (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16; }
+
+namespace {
+cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
+                                const float* U, const int32_t* anchor, int B, int gamma, int V,
+                                int r, uint64_t seed, int32_t* tokens, float* q_tok,
+                                float* row_max, float* row_sumexp, void* region, int* err,
+                                cudaStream_t stream) {
   const int NB = B <= 16 ? 16 : 32;
   const int n_tiles = cdiv(V, kGemmTileV);
   int grid = NB == 16 ? max_grid<16>() : max_grid<32>();
@@ -630,11 +654,12 @@ cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const flo
   if (grid > kDraftMaxCtas) grid = kDraftMaxCtas;
   DraftParams p;
   p.W1 = W1;
+  p.W2p = W2p;
   p.anchor = anchor;
   p.B = B; p.gamma = gamma; p.V = V; p.r = r;
   p.n_tiles = n_tiles;
   p.n_chunks = cdiv(B, NB);
-  p.kc = (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16;   // divides r (r % 16 == 0)
+  p.kc = draft_kchunk(r);   // divides r (r % 16 == 0)
   p.seed = seed;
   const size_t part_bytes = align_up((size_t)2 * B * kDraftMaxCtas * sizeof(RowState), 256);
   char* base = static_cast<char*>(region);
@@ -650,10 +675,29 @@ cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const flo
                                   256 + (size_t)gamma * B * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;
   CUtensorMap w2_map, u_map;
-  if (!encode_w2_map(&w2_map, W2, V, r, p.kc)) return cudaErrorInvalidValue;
+  memset(&w2_map, 0, sizeof(w2_map));
+  if (!W2p && !encode_w2_map(&w2_map, W2, V, r, p.kc)) return cudaErrorInvalidValue;
   if (!encode_u_map(&u_map, U, B, gamma, V, NB)) return cudaErrorInvalidValue;
   return NB == 16 ? launch_fused<16>(w2_map, u_map, p, grid, stream)
                   : launch_fused<32>(w2_map, u_map, p, grid, stream);
+}
+}  // namespace
+
+cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const float* U,
+                               const int32_t* anchor, int B, int gamma, int V, int r,
+                               uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
+                               float* row_sumexp, void* region, int* err, cudaStream_t stream) {
+  return launch_draft_common(W1, W2, nullptr, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
+                             row_max, row_sumexp, region, err, stream);
+}
+
+cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, const float* U,
+                                      const int32_t* anchor, int B, int gamma, int V, int r,
+                                      uint64_t seed, int32_t* tokens, float* q_tok,
+                                      float* row_max, float* row_sumexp, void* region, int* err,
+                                      cudaStream_t stream) {
+  return launch_draft_common(W1, nullptr, W2p, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
+                             row_max, row_sumexp, region, err, stream);
 }
 
 }  // namespace dspark

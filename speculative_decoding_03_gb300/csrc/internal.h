@@ -106,6 +106,15 @@ cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const flo
                                uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
                                float* row_sumexp, void* region, int* err, cudaStream_t stream);
 
+// the same with W2 given as packed tile images (see pack.cu)
+cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, const float* U,
+                                      const int32_t* anchor, int B, int gamma, int V, int r,
+                                      uint64_t seed, int32_t* tokens, float* q_tok,
+                                      float* row_max, float* row_sumexp, void* region, int* err,
+                                      cudaStream_t stream);
+// rank rows per W2 stage of the draft kernel (and per packed K-chunk image)
+int draft_kchunk(int r);
+
 cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32_t* tokens,
                               const uint16_t* W1, const float* w_c, float b_c, int B, int gamma,
                               int H, int r, int V, float* c, float* a, int* err,

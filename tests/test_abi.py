@@ -18,7 +18,7 @@ FAKE = 0x10000000          # an aligned address that is never dereferenced by th
 def _declared_symbols():
     src = open(os.path.join(ROOT, "include", "dspark.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(dspark_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(dspark_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_symbol():

@@ -250,3 +250,45 @@ def test_full_size_draft_sampled_requests(name):
     for key in ("q_tok", "row_max", "row_sumexp"):
         np.testing.assert_allclose(got[key][picks][same], ref[key][same], rtol=RTOL, err_msg=key)
     assert ties <= 1
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_draft_packed_matches_draft(name):
+    """The packed-weights draft runs the same kernel arithmetic: identical outputs."""
+    _need_gpu()
+    w = CASES[name]
+    inp = workloads.generate(w, with_T=False)
+    dev = _dev(inp)
+    ws = _ws(w)
+    W2p = ds.pack_w2(dev["W2"])
+    assert W2p.numel() * 2 == ds.lib().dspark_packed_w2_bytes(w.V, w.r)
+    a = {k: v.cpu().numpy() for k, v in ds.draft(dev["U"], dev["W1"], dev["W2"], dev["anchor"],
+                                                  w.seed, ws).items()}
+    b = {k: v.cpu().numpy() for k, v in ds.draft_packed(dev["U"], dev["W1"], W2p, dev["anchor"],
+                                                         w.seed, ws).items()}
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    assert ws.status() == 0
+
+
+def test_pack_layout_matches_its_definition():
+    """dspark_pack_w2 against the layout the header states, rebuilt with numpy."""
+    _need_gpu()
+    for V, r in [(904, 64), (520, 128), (1032, 256), (1000, 16), (264, 48)]:
+        rng = np.random.default_rng(V + r)
+        W2 = rng.integers(0, 2**16, size=(r, V), dtype=np.uint16)
+        W2d = torch.from_numpy(W2.view(np.int16)).cuda().view(torch.bfloat16)
+        got = ds.pack_w2(W2d).cpu().view(torch.int16).numpy().view(np.uint16)
+        kc = 64 if r % 64 == 0 else 32 if r % 32 == 0 else 16
+        n_tiles = -(-V // 128)
+        Wpad = np.zeros((r, n_tiles * 128), np.uint16)
+        Wpad[:, :V] = W2
+        want = np.empty((n_tiles, r // kc, 2, kc, 8, 8), np.uint16)
+        for kl in range(kc):
+            for s in range(8):
+                c = s ^ (kl % 8)
+                for t in range(n_tiles):
+                    for h in range(2):
+                        v = t * 128 + 64 * h + 8 * c
+                        want[t, :, h, kl, s, :] = Wpad[kl::kc, v:v + 8].reshape(r // kc, 8)
+        np.testing.assert_array_equal(got, want.reshape(-1), err_msg=f"V={V} r={r}")
