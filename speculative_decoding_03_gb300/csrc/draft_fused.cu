@@ -220,7 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   const int kc = p.kc;
   const int n_kchunks = p.r / kc;
   const int n_jobs = p.gamma * p.n_chunks;
-  const uint32_t tmem_cols = kDepth * NB < 32 ? 32 : kDepth * NB;
+  // tcgen05.alloc takes a power of two of at least 32 columns
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < (uint32_t)(kDepth * NB)) tmem_cols <<= 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
@@ -257,28 +259,33 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     return false;
   };
   // a whole warp's bounded wait with a warp-uniform result
+  // a whole warp's bounded wait with a warp-uniform result (every lane sleeps on the
+  // barrier and acquires for itself)
   auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
-    bool ok = wait1(bar, parity);
+    const bool ok = wait1(bar, parity);
     return __all_sync(0xffffffffu, ok);
   };
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
+    // The whole warp runs the loop (warp-uniform control flow); lane 0 issues the copies.
     if (lane == 0) {
       prefetch_tensormap(&w2_map);
       prefetch_tensormap(&u_map);
-      const uint64_t keep = policy_evict_last();
-      uint64_t stream_pol;
-      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
-      uint32_t ws = 0, us = 0;
-      bool ok = true;
-      for (int job = 0; job < n_jobs && ok; ++job) {
-        const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
-        for (int t = t_lo; t < t_hi && ok; ++t) {
-          const int v0 = t * kGemmTileV;
-          for (int i = 0; i < n_kchunks && ok; ++i) {
-            const int s = ws % kWStages;
-            if (!(ok = wait1(&w_empty[s], ((ws / kWStages) & 1) ^ 1))) break;
+    }
+    const uint64_t keep = policy_evict_last();
+    uint64_t stream_pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
+    uint32_t ws = 0, us = 0;
+    bool ok = true;
+    for (int job = 0; job < n_jobs && ok; ++job) {
+      const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+      for (int t = t_lo; t < t_hi && ok; ++t) {
+        const int v0 = t * kGemmTileV;
+        for (int i = 0; i < n_kchunks && ok; ++i) {
+          const int s = ws % kWStages;
+          if (!(ok = wait_warp(&w_empty[s], ((ws / kWStages) & 1) ^ 1))) break;
+          if (lane == 0) {
             uint8_t* dst = smem + S::kOffW + s * S::kWStageBytes;
             mbar_arrive_expect_tx(&w_full[s], 2u * (uint32_t)kc * 128u);
             if (p.W2p) {
@@ -294,11 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               tma_load_2d(dst, &w2_map, &w_full[s], v0, i * kc, keep);
               tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], v0 + 64, i * kc, keep);
             }
-            ++ws;
           }
-          if (!ok) break;
-          const int su = us % kUStages;
-          if (!(ok = wait1(&u_empty[su], ((us / kUStages) & 1) ^ 1))) break;
+          __syncwarp();
+          ++ws;
+        }
+        if (!ok) break;
+        const int su = us % kUStages;
+        if (!(ok = wait_warp(&u_empty[su], ((us / kUStages) & 1) ^ 1))) break;
+        if (lane == 0) {
           mbar_arrive_expect_tx(&u_full[su], (uint32_t)S::kUStageBytes);
           asm volatile(
               "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -307,35 +317,41 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               "l"(reinterpret_cast<uint64_t>(&u_map)), "r"(smem_u32(&u_full[su])), "r"(v0),
               "r"(k - 1), "r"(c * NB), "l"(stream_pol)
               : "memory");
-          ++us;
         }
+        __syncwarp();
+        ++us;
       }
-      // drain: every issued copy has landed before the CTA may exit
+    }
+    // drain: every issued copy has landed before the CTA may exit
+    if (lane == 0) {
       for (uint32_t i = ws > (uint32_t)kWStages ? ws - kWStages : 0; i < ws; ++i)
         mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, kTimeoutNs);
       for (uint32_t i = us > (uint32_t)kUStages ? us - kUStages : 0; i < us; ++i)
         mbar_wait(&u_full[i % kUStages], (i / kUStages) & 1, kTimeoutNs);
     }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // -------------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
-      uint32_t ws = 0, tc = 0;
-      bool ok = true;
-      for (int job = 0; job < n_jobs && ok; ++job) {
-        const int eb = job & 1;
-        if (!(ok = wait1(&e_full[eb], (job >> 1) & 1))) break;
+    // The whole warp runs the loop; lane 0 issues the MMAs and the commits.
+    const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
+    uint32_t ws = 0, tc = 0;
+    bool ok = true;
+    for (int job = 0; job < n_jobs && ok; ++job) {
+      const int eb = job & 1;
+      // (the E writers fenced their stores to the async proxy before arriving)
+      if (!(ok = wait_warp(&e_full[eb], (job >> 1) & 1))) break;
+      const uint32_t e_addr = smem_u32(smem + S::kOffE + eb * S::kEBytes);
+      for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
+        const int ab = tc % kDepth;
+        if (!(ok = wait_warp(&acc_empty[ab], ((tc / kDepth) & 1) ^ 1))) break;
         tc_fence_after_sync();
-        const uint32_t e_addr = smem_u32(smem + S::kOffE + eb * S::kEBytes);
-        for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-          const int ab = tc % kDepth;
-          if (!(ok = wait1(&acc_empty[ab], ((tc / kDepth) & 1) ^ 1))) break;
-          tc_fence_after_sync();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
-          for (int i = 0; i < n_kchunks; ++i, ++ws) {
-            const int s = ws % kWStages;
-            if (!(ok = wait1(&w_full[s], (ws / kWStages) & 1))) break;
-            tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
+        for (int i = 0; i < n_kchunks; ++i, ++ws) {
+          const int s = ws % kWStages;
+          // TMA data: the barrier's transaction count orders it before the MMAs; no
+          // tcgen05 fence here (a fence per chunk would serialise on MMA completion)
+          if (!(ok = wait_warp(&w_full[s], (ws / kWStages) & 1))) break;
+          if (lane == 0) {
             const uint32_t a_addr = smem_u32(smem + S::kOffW + s * S::kWStageBytes);
             for (int kk = 0; kk < kc / 16; ++kk) {
               const int kg = i * (kc / 16) + kk;          // global 16-row K step
@@ -348,15 +364,21 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
             }
             umma_commit(&w_empty[s]);
           }
-          if (!ok) break;
-          umma_commit(&acc_full[ab]);
+          __syncwarp();
         }
-        if (ok) umma_commit(&e_empty[eb]);
+        if (!ok) break;
+        if (lane == 0) umma_commit(&acc_full[ab]);
+        __syncwarp();
       }
-      // drain: every issued MMA has completed before tensor memory is released
+      if (ok && lane == 0) umma_commit(&e_empty[eb]);
+      __syncwarp();
+    }
+    // drain: every issued MMA has completed before tensor memory is released
+    if (lane == 0) {
       umma_commit(&mma_drain);
       mbar_wait(&mma_drain, 0, kTimeoutNs);
     }
+    __syncwarp();
   } else if (warp < kFirstSampler) {
     // ----------------------------------------------- transposers: TMEM (+U) -> z rows
     const int q = warp & 3;                       // TMEM lane quarter of this warp
@@ -405,14 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     };
     auto grid_wait = [&](unsigned int target) {
       if (stid == 0) {
-        const uint64_t t0 = globaltimer_ns();
+        const long long t0 = sm_cycles();
         while (ld_acquire_u32(p.grid_count) < target) {
-          if (*(volatile int*)&abort_s || globaltimer_ns() - t0 > kTimeoutNs) {
+          if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
             set_device_error(p.err, DSPARK_ERR_TIMEOUT);
             atomicExch(&abort_s, 1);
             break;
           }
-          __nanosleep(64);
         }
       }
       named_bar_sync(kNamedBarSamplers, kSamplerThreads);
@@ -558,7 +579,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
           ps.z = bz[i];
           ps.score = bsc[i];
           p.partials[((size_t)(k & 1) * p.B + b) * G + cta] = ps;
-          if (bi[i] >= 0) atomicMax(p.keys + (size_t)(k - 1) * p.B + b, argmax_key(bsc[i], bi[i]));
+          if (bi[i] >= 0) {
+            atomicMax(p.keys + (size_t)(k - 1) * p.B + b, argmax_key(bsc[i], bi[i]));
+            // the winner is one CTA's local best: warm L2 with its W1 row for the gather
+            // that follows the grid barrier
+            if (k < p.gamma)
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                               reinterpret_cast<uint64_t>(p.W1 + (size_t)bi[i] * p.r)),
+                           "r"((uint32_t)p.r * 2u)
+                           : "memory");
+          }
           __threadfence();
         }
       }

@@ -52,6 +52,16 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   if (tid == 0) first_fail = N + 1;
   __syncthreads();
 
+  if (N <= kSchedThreads) {
+    // small batches: every key is distinct, so its rank is the number of smaller keys;
+    // one pass of broadcast shared-memory reads, no sorting network
+    const unsigned long long mine = tid < N ? keys[tid] : ~0ull;
+    int rank = 0;
+    for (int j = 0; j < N; ++j) rank += keys[j] < mine ? 1 : 0;
+    __syncthreads();
+    if (tid < N) keys[rank] = mine;
+    __syncthreads();
+  } else
   // bitonic sort, ascending key = (A desc, r asc, j asc)
   for (int size = 2; size <= Npad; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
