@@ -40,6 +40,8 @@
 // issuer drain their in-flight copies and MMAs before the CTA releases tensor memory.
 #include <string.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -250,15 +252,22 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_base_s;
 
-  // one thread's bounded wait; a timeout aborts the CTA
+  // One thread's bounded wait; a timeout aborts the CTA.  The abort flag is read only once
+  // the first (sleeping) try has not seen the phase complete: a shared-memory read ahead of
+  // every wait made the single-lane MMA issue loop measurably slower per tile on GB300.
   auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (*(volatile int*)&abort_s) return false;
-    if (mbar_wait(bar, parity, kTimeoutNs)) return true;
-    set_device_error(p.err, DSPARK_ERR_TIMEOUT);
-    atomicExch(&abort_s, 1);
-    return false;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const long long t0 = sm_cycles();
+    for (;;) {
+      if (*(volatile int*)&abort_s) return false;
+      if (mbar_try_wait_sleep(bar, parity)) return true;
+      if (sm_cycles() - t0 > kWaitCycles) {
+        set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+        atomicExch(&abort_s, 1);
+        return false;
+      }
+    }
   };
-  // a whole warp's bounded wait with a warp-uniform result
   // a whole warp's bounded wait with a warp-uniform result (every lane sleeps on the
   // barrier and acquires for itself)
   auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -266,49 +275,46 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     return __all_sync(0xffffffffu, ok);
   };
 
+  // The producer and the MMA issuer run their loops on one elected lane: a whole-warp loop
+  // (every lane waiting, then a warp vote and a __syncwarp per K-chunk) measured on GB300
+  // twice as slow per tile as the single-lane issue loop.
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
-    // The whole warp runs the loop (warp-uniform control flow); lane 0 issues the copies.
     if (lane == 0) {
       prefetch_tensormap(&w2_map);
       prefetch_tensormap(&u_map);
-    }
-    const uint64_t keep = policy_evict_last();
-    uint64_t stream_pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
-    uint32_t ws = 0, us = 0;
-    bool ok = true;
-    for (int job = 0; job < n_jobs && ok; ++job) {
-      const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
-      for (int t = t_lo; t < t_hi && ok; ++t) {
-        const int v0 = t * kGemmTileV;
-        for (int i = 0; i < n_kchunks && ok; ++i) {
-          const int s = ws % kWStages;
-          if (!(ok = wait_warp(&w_empty[s], ((ws / kWStages) & 1) ^ 1))) break;
-          if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      uint64_t stream_pol;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
+      const uint32_t w_bytes = 2u * (uint32_t)kc * 128u;
+      uint32_t ws = 0, us = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+        for (int t = t_lo; t < t_hi && ok; ++t) {
+          const int v0 = t * kGemmTileV;
+          for (int i = 0; i < n_kchunks; ++i, ++ws) {
+            const int s = ws % kWStages;
+            if (!(ok = wait1(&w_empty[s], ((ws / kWStages) & 1) ^ 1))) break;
             uint8_t* dst = smem + S::kOffW + s * S::kWStageBytes;
-            mbar_arrive_expect_tx(&w_full[s], 2u * (uint32_t)kc * 128u);
+            mbar_arrive_expect_tx(&w_full[s], w_bytes);
             if (p.W2p) {
               // packed: the stage image is contiguous, one 1-D bulk copy
               const uint16_t* src = p.W2p + ((size_t)t * n_kchunks + i) * (size_t)kc * 128;
               asm volatile(
                   "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
                   " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-                  "l"(reinterpret_cast<uint64_t>(src)), "r"(2u * (uint32_t)kc * 128u),
-                  "r"(smem_u32(&w_full[s])), "l"(keep)
+                  "l"(reinterpret_cast<uint64_t>(src)), "r"(w_bytes), "r"(smem_u32(&w_full[s])),
+                  "l"(keep)
                   : "memory");
             } else {
               tma_load_2d(dst, &w2_map, &w_full[s], v0, i * kc, keep);
               tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], v0 + 64, i * kc, keep);
             }
           }
-          __syncwarp();
-          ++ws;
-        }
-        if (!ok) break;
-        const int su = us % kUStages;
-        if (!(ok = wait_warp(&u_empty[su], ((us / kUStages) & 1) ^ 1))) break;
-        if (lane == 0) {
+          if (!ok) break;
+          const int su = us % kUStages;
+          if (!(ok = wait1(&u_empty[su], ((us / kUStages) & 1) ^ 1))) break;
           mbar_arrive_expect_tx(&u_full[su], (uint32_t)S::kUStageBytes);
           asm volatile(
               "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -317,13 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               "l"(reinterpret_cast<uint64_t>(&u_map)), "r"(smem_u32(&u_full[su])), "r"(v0),
               "r"(k - 1), "r"(c * NB), "l"(stream_pol)
               : "memory");
+          ++us;
         }
-        __syncwarp();
-        ++us;
       }
-    }
-    // drain: every issued copy has landed before the CTA may exit
-    if (lane == 0) {
+      // drain: every issued copy has landed before the CTA may exit (a stage whose wait
+      // failed above was never issued, so only stages below ws are in flight)
       for (uint32_t i = ws > (uint32_t)kWStages ? ws - kWStages : 0; i < ws; ++i)
         mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, kTimeoutNs);
       for (uint32_t i = us > (uint32_t)kUStages ? us - kUStages : 0; i < us; ++i)
@@ -332,30 +336,34 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // -------------------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop; lane 0 issues the MMAs and the commits.
-    const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
-    uint32_t ws = 0, tc = 0;
-    bool ok = true;
-    for (int job = 0; job < n_jobs && ok; ++job) {
-      const int eb = job & 1;
-      // (the E writers fenced their stores to the async proxy before arriving)
-      if (!(ok = wait_warp(&e_full[eb], (job >> 1) & 1))) break;
-      const uint32_t e_addr = smem_u32(smem + S::kOffE + eb * S::kEBytes);
-      for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-        const int ab = tc % kDepth;
-        if (!(ok = wait_warp(&acc_empty[ab], ((tc / kDepth) & 1) ^ 1))) break;
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
-        for (int i = 0; i < n_kchunks; ++i, ++ws) {
-          const int s = ws % kWStages;
-          // TMA data: the barrier's transaction count orders it before the MMAs; no
-          // tcgen05 fence here (a fence per chunk would serialise on MMA completion)
-          if (!(ok = wait_warp(&w_full[s], (ws / kWStages) & 1))) break;
-          if (lane == 0) {
+    // The 16-row K steps of one W2 stage are a compile-time count (1, 2 or 4): a runtime
+    // trip count with guarded issues slowed the issue loop on GB300 as much as the
+    // abort-flag reads did.
+    auto issue_loop = [&](auto ksteps_c) {
+      constexpr int KS = decltype(ksteps_c)::value;
+      const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
+      uint32_t ws = 0, tc = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int eb = job & 1;
+        // (the E writers fenced their stores to the async proxy before arriving)
+        if (!(ok = wait1(&e_full[eb], (job >> 1) & 1))) break;
+        const uint32_t e_addr = smem_u32(smem + S::kOffE + eb * S::kEBytes);
+        for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
+          const int ab = tc % kDepth;
+          if (!(ok = wait1(&acc_empty[ab], ((tc / kDepth) & 1) ^ 1))) break;
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
+          for (int i = 0; i < n_kchunks; ++i, ++ws) {
+            const int s = ws % kWStages;
+            // TMA data: the barrier's transaction count orders it before the MMAs; no
+            // tcgen05 fence here (a fence per chunk would serialise on MMA completion)
+            if (!(ok = wait1(&w_full[s], (ws / kWStages) & 1))) break;
             const uint32_t a_addr = smem_u32(smem + S::kOffW + s * S::kWStageBytes);
-            for (int kk = 0; kk < kc / 16; ++kk) {
-              const int kg = i * (kc / 16) + kk;          // global 16-row K step
-              const uint64_t ad = smem_desc(a_addr + (uint32_t)kk * 2048u, (uint32_t)kc * 128u,
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              const int kg = i * KS + kk;                  // global 16-row K step
+              const uint64_t ad = smem_desc(a_addr + (uint32_t)kk * 2048u, (uint32_t)KS * 2048u,
                                             1024u, kSwizzle128B);
               const uint64_t bd = smem_desc(e_addr + (uint32_t)(kg >> 2) * (uint32_t)NB * 128u +
                                                 (uint32_t)(kg & 3) * 32u,
@@ -364,17 +372,17 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
             }
             umma_commit(&w_empty[s]);
           }
-          __syncwarp();
+          if (!ok) break;
+          umma_commit(&acc_full[ab]);
         }
-        if (!ok) break;
-        if (lane == 0) umma_commit(&acc_full[ab]);
-        __syncwarp();
+        if (ok) umma_commit(&e_empty[eb]);
       }
-      if (ok && lane == 0) umma_commit(&e_empty[eb]);
-      __syncwarp();
-    }
-    // drain: every issued MMA has completed before tensor memory is released
+    };
     if (lane == 0) {
+      if (kc == 64) issue_loop(std::integral_constant<int, 4>{});
+      else if (kc == 32) issue_loop(std::integral_constant<int, 2>{});
+      else issue_loop(std::integral_constant<int, 1>{});
+      // drain: every issued MMA has completed before tensor memory is released
       umma_commit(&mma_drain);
       mbar_wait(&mma_drain, 0, kTimeoutNs);
     }
