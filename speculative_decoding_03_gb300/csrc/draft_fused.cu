@@ -339,16 +339,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     // The 16-row K steps of one W2 stage are a compile-time count (1, 2 or 4): a runtime
     // trip count with guarded issues slowed the issue loop on GB300 as much as the
     // abort-flag reads did.
+    // Descriptors are built once and advanced by adding (byte offset >> 4) to their start-
+    // address field (bits 0-13; every operand lies below 256 KB, so the sum never carries
+    // into the stride fields).  The issuing lane shares its sub-partition with sampler
+    // warps, so every instruction saved here shortens the tile cadence.
     auto issue_loop = [&](auto ksteps_c) {
       constexpr int KS = decltype(ksteps_c)::value;
       const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
+      const uint64_t a_base = smem_desc(smem_u32(smem + S::kOffW), (uint32_t)KS * 2048u, 1024u,
+                                        kSwizzle128B);
       uint32_t ws = 0, tc = 0;
       bool ok = true;
       for (int job = 0; job < n_jobs && ok; ++job) {
         const int eb = job & 1;
         // (the E writers fenced their stores to the async proxy before arriving)
         if (!(ok = wait1(&e_full[eb], (job >> 1) & 1))) break;
-        const uint32_t e_addr = smem_u32(smem + S::kOffE + eb * S::kEBytes);
+        const uint64_t b_base =
+            smem_desc(smem_u32(smem + S::kOffE + eb * S::kEBytes), 16u, 1024u, kSwizzle128B);
         for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
           const int ab = tc % kDepth;
           if (!(ok = wait1(&acc_empty[ab], ((tc / kDepth) & 1) ^ 1))) break;
@@ -359,16 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
             // TMA data: the barrier's transaction count orders it before the MMAs; no
             // tcgen05 fence here (a fence per chunk would serialise on MMA completion)
             if (!(ok = wait1(&w_full[s], (ws / kWStages) & 1))) break;
-            const uint32_t a_addr = smem_u32(smem + S::kOffW + s * S::kWStageBytes);
+            const uint64_t a_s = a_base + (uint64_t)((s * S::kWStageBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
-              const int kg = i * KS + kk;                  // global 16-row K step
-              const uint64_t ad = smem_desc(a_addr + (uint32_t)kk * 2048u, (uint32_t)KS * 2048u,
-                                            1024u, kSwizzle128B);
-              const uint64_t bd = smem_desc(e_addr + (uint32_t)(kg >> 2) * (uint32_t)NB * 128u +
-                                                (uint32_t)(kg & 3) * 32u,
-                                            16u, 1024u, kSwizzle128B);
-              umma_bf16_f32(d_tmem, ad, bd, idesc, kg > 0 ? 1u : 0u);
+              const uint32_t kg = (uint32_t)(i * KS + kk);   // global 16-row K step
+              // A: 16 K rows of the MN-major stage are 2048 bytes apart; B: K-block kg/4 of
+              // the K-major E buffer, 32 bytes per 16-element step inside its 128-byte rows
+              const uint64_t ad = a_s + (uint64_t)(kk * (2048 >> 4));
+              const uint64_t bd = b_base + (uint64_t)((kg >> 2) * (uint32_t)(NB * 128 / 16) + (kg & 3) * 2u);
+              umma_bf16_f32(d_tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
             }
             umma_commit(&w_empty[s]);
           }
@@ -573,16 +579,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
           mbar_arrive(&u_empty[zb]);
         }
       }
-      // publish this CTA's partials of the job's requests
+      // publish this CTA's partials of the job's requests: the warp reductions of all its
+      // rows first, then the stores and atomics, then one fence for all of them (a fence
+      // waits for the atomics' round trips, so one per row would serialise them)
+      float pm[RPW], pst[RPW];
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
-        const int b = c * NB + sw * RPW + i;
-        const float m = warp_max(mx[i]);
-        const float st = warp_sum(s[i]) * (Mr[i] == -INFINITY ? 0.f : expf(Mr[i] - m));
-        if (b < p.B && lane == 0 && !*(volatile int*)&abort_s) {
+        pm[i] = warp_max(mx[i]);
+        pst[i] = warp_sum(s[i]) * (Mr[i] == -INFINITY ? 0.f : expf(Mr[i] - pm[i]));
+      }
+      if (lane == 0 && !*(volatile int*)&abort_s) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+          const int b = c * NB + sw * RPW + i;
+          if (b >= p.B) continue;
           RowState ps;
-          ps.m = m;
-          ps.s = st;
+          ps.m = pm[i];
+          ps.s = pst[i];
           ps.idx = bi[i];
           ps.z = bz[i];
           ps.score = bsc[i];
@@ -597,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
                            "r"((uint32_t)p.r * 2u)
                            : "memory");
           }
-          __threadfence();
         }
+        __threadfence();
       }
       if (c + 1 == p.n_chunks) {
         // this CTA is done with position k: count it in the grid barrier
