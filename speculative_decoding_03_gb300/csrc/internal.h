@@ -37,6 +37,20 @@ inline RowSplit row_split(int rows, int V) {
   return s;
 }
 
+// Fixed segments of the verify kernels: every thread of a 256-thread CTA issues all its
+// 128-bit loads of a segment at once (16 per thread for the target statistics, 4 per
+// input row for the final sample, which loads three rows).
+constexpr int kStatsVec = 16;
+constexpr int kStatsSeg = 4 * kSampleThreads * kStatsVec;   // 16384 logits
+constexpr int kVerVec = 4;
+constexpr int kVerSeg = 4 * kSampleThreads * kVerVec;       // 4096 logits
+inline RowSplit fixed_split(int V, int seg) {
+  RowSplit s;
+  s.seg = seg;
+  s.splits = cdiv(V, seg);
+  return s;
+}
+
 // Width of one batch chunk of the bias contraction (MMA N): a multiple of 16, <= 256.
 inline int gemm_chunk(int B) {
   int nb = (int)align_up((size_t)B, 16);
@@ -59,15 +73,15 @@ struct Plan {
 inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   Plan p;
   p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.H = H;
-  p.stats = row_split(B * gamma, V);
-  p.ver = row_split(B, V);
+  p.stats = fixed_split(V, kStatsSeg);
+  p.ver = fixed_split(V, kVerSeg);
   size_t o = 0;
   p.off_err = o; o += 256;
   p.off_draft = o; o = align_up(o + draft_region_bytes(B, gamma), 256);
   p.off_bias = o; o = align_up(o + (size_t)B * V * sizeof(float), 256);
   const size_t parts = (size_t)B * gamma * p.stats.splits + (size_t)B * p.ver.splits;
   p.off_part = o; o = align_up(o + parts * sizeof(RowState), 256);
-  p.off_cnt = o; o = align_up(o + ((size_t)B * gamma + 2 * (size_t)B) * sizeof(uint32_t), 256);
+  p.off_cnt = o; o = align_up(o + (size_t)B * sizeof(uint32_t), 256);
   p.off_M = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
   p.off_lnS = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
   p.off_p = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);

@@ -8,13 +8,15 @@
 // billytse.dev section 1 counts it), drawn from target row l + 1.
 //
 // Kernels, in order on the stream:
-//   target_stats   for every verified row (b, k <= l_b): max M and log-sum-exp of T[b, k]
-//                  and p_k(x_k) (rows are split over CTAs, the last CTA merges)
-//   decide         one thread per request: the acceptance tests in order, the first
+//   target_stats   for every verified row (b, k <= l_b) and segment of it: the max and the
+//                  sum of exp of T[b, k] over the segment (a partial, no cross-CTA merge)
+//   decide         one warp per request, one lane per position: merges the row partials
+//                  into M, log S and p_k(x_k), runs the acceptance tests, finds the first
 //                  reject, the accepted prefix, and which row the final token comes from
 //   bias_gemm      (shared with the draft) W1[x_{j-1}] W2 for the rows with a reject at j
 //   final_sample   Gumbel-max over log(P_j - Q_j) on {P_j > Q_j} (residual), or over
-//                  T[b, l+1] (bonus); the last CTA of a row writes the token
+//                  T[b, l+1] (bonus): one partial (best score, index) per segment
+//   finalize       one warp per request merges the partials and writes the token
 //   fallback       only for rows whose residual support came out empty in fp32: Gumbel-
 //                  max over T[b, j] with the residual's random stream
 #include "internal.h"
@@ -43,6 +45,13 @@ __device__ __forceinline__ RowState load_partial(const RowState* src) {
   return q;
 }
 
+// 1/x on the special-function unit (PTX rcp.approx.ftz.f32, relative error below 2^-22)
+__device__ __forceinline__ float rcp_approx_ftz(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Gumbel value of the 32-bit draw x: g = -log(-log1p(-w)), w = 1 - U01(x).
 __device__ __forceinline__ float gumbel_of(uint32_t x) {
   return -logf(exp1_from_w(one_minus_u01(x)));
@@ -63,175 +72,278 @@ __device__ __forceinline__ bool publish_partial(RowState st, RowState* slot, uin
   return last;
 }
 
+// (one warp; every lane gets the merged state)
 __device__ __forceinline__ RowState merge_partials(const RowState* base, int splits) {
   RowState acc = row_state_empty();
-  for (int i = threadIdx.x; i < splits; i += 32) acc = row_state_merge(acc, load_partial(base + i));
+  for (int i = threadIdx.x & 31; i < splits; i += 32) acc = row_state_merge(acc, load_partial(base + i));
   return row_state_warp_reduce(acc);
 }
 
 // ---------------------------------------------------------------------- target stats
+// Grid (splits, B * gamma) with blockIdx.y = (k - 1) * B + b: rows ordered by position,
+// so the CTAs of verified rows (k <= l_b) come first and the rest exit at once.  Every
+// thread issues all kStatsVec of its 128-bit loads before using any of them; the CTA
+// reduces only (max, sum of exp) and publishes them as a partial.
+__device__ __forceinline__ void max_sum_merge(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  s = s * ex2_approx((m - mn) * kLog2e) + s2 * ex2_approx((m2 - mn) * kLog2e);
+  m = mn;
+}
+
 __global__ void __launch_bounds__(kSampleThreads) target_stats_kernel(
-    const float* __restrict__ T, const int32_t* __restrict__ tokens,
-    const int32_t* __restrict__ ell, int gamma, int V, int splits, int seg,
-    RowState* __restrict__ partials, uint32_t* __restrict__ counters, float* __restrict__ M_out,
-    float* __restrict__ lnS_out, float* __restrict__ p_out, int* err) {
-  __shared__ RowState red[32];
-  __shared__ int is_last;
-  const int row = blockIdx.y;                 // b * gamma + (k - 1)
-  const int b = row / gamma, k = row - b * gamma + 1;
+    const float* __restrict__ T, const int32_t* __restrict__ ell, int B, int gamma, int V,
+    int splits, float2* __restrict__ partials) {
+  __shared__ float red_m[kSampleThreads / 32], red_s[kSampleThreads / 32];
+  const int k = blockIdx.y / B + 1, b = blockIdx.y - (k - 1) * B;
   if (k > clamp_ell(ell, b, gamma, nullptr)) return;
+  const int row = b * gamma + (k - 1);
   const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
-  const int v_begin = blockIdx.x * seg, v_end = min(V, v_begin + seg);
-  float m = -INFINITY, s = 0.f;
-  for (int v = v_begin + 4 * threadIdx.x; v < v_end; v += 4 * kSampleThreads) {
-    const float4 t = ld_stream_f4(Trow + v);
-    const float mn = fmaxf(fmaxf(m, fmaxf(t.x, t.y)), fmaxf(t.z, t.w));
-    s *= ex2_approx((m - mn) * kLog2e);
-    m = mn;
-    s += ex2_approx((t.x - m) * kLog2e) + ex2_approx((t.y - m) * kLog2e) +
-         ex2_approx((t.z - m) * kLog2e) + ex2_approx((t.w - m) * kLog2e);
+  const int v0 = blockIdx.x * kStatsSeg + 4 * threadIdx.x;
+  float4 t[kStatsVec];
+#pragma unroll
+  for (int j = 0; j < kStatsVec; ++j) {
+    const int v = v0 + j * 4 * kSampleThreads;
+    t[j] = v < V ? ld_stream_f4(Trow + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   }
-  RowState st = row_state_empty();
-  st.m = m;
-  st.s = s;
-  st = row_state_block_reduce(st, red);
-  if (!publish_partial(st, partials + (size_t)row * splits + blockIdx.x, &counters[row], splits,
-                       &is_last))
-    return;
-  if (threadIdx.x < 32) {
-    const RowState acc = merge_partials(partials + (size_t)row * splits, splits);
-    if (threadIdx.x == 0) {
-      const int x = tokens[(size_t)b * gamma + (k - 1)];
-      float p = 0.f;
-      if (x >= 0 && x < V) {
-        p = expf(__ldg(Trow + x) - acc.m) / acc.s;
-      } else {
-        set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
-      }
-      M_out[row] = acc.m;
-      lnS_out[row] = logf(acc.s);
-      p_out[row] = p;
-      counters[row] = 0u;
-    }
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kStatsVec; ++j) m = fmaxf(m, fmaxf(fmaxf(t[j].x, t[j].y), fmaxf(t[j].z, t[j].w)));
+  float s = 0.f;
+  if (m != -INFINITY) {
+    const float mL = m * kLog2e;
+#pragma unroll
+    for (int j = 0; j < kStatsVec; ++j)
+      s += ex2_approx(fmaf(t[j].x, kLog2e, -mL)) + ex2_approx(fmaf(t[j].y, kLog2e, -mL)) +
+           ex2_approx(fmaf(t[j].z, kLog2e, -mL)) + ex2_approx(fmaf(t[j].w, kLog2e, -mL));
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+    max_sum_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+  if (lane == 0) { red_m[warp] = m; red_s[warp] = s; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kSampleThreads / 32; ++w) max_sum_merge(m, s, red_m[w], red_s[w]);
+    partials[(size_t)row * splits + blockIdx.x] = make_float2(m, s);
   }
 }
 
 // ----------------------------------------------------------------------------- decide
-__global__ void decide_kernel(const int32_t* __restrict__ anchor,
-                              const int32_t* __restrict__ tokens,
-                              const float* __restrict__ q_tok, const float* __restrict__ p_t,
-                              const int32_t* __restrict__ ell, int B, int gamma, uint64_t seed,
-                              int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
-                              int32_t* __restrict__ n_out, int32_t* __restrict__ mode,
-                              int32_t* __restrict__ pos, int32_t* __restrict__ prev_tok,
-                              int32_t* __restrict__ fallback, int* err) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per request; lane k - 1 owns position k.  Verified lanes merge their row's
+// target partials (M, S), compute p_k(x_k) and test u_k < p_k(x_k) / q_k(x_k); a ballot
+// gives the first reject.
+__global__ void __launch_bounds__(128) decide_kernel(
+    const float* __restrict__ T, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, const float* __restrict__ q_tok,
+    const float2* __restrict__ stats, int splits, const int32_t* __restrict__ ell, int B,
+    int gamma, int V, uint64_t seed, float* __restrict__ M_t, float* __restrict__ lnS_t,
+    float* __restrict__ p_t, int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
+    int32_t* __restrict__ n_out, int32_t* __restrict__ mode, int32_t* __restrict__ pos,
+    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
-  const int L = clamp_ell(ell, b, gamma, err);
-  int j = 0;  // first rejected position, 0 if none
-  for (int k = 1; k <= L; ++k) {
-    const size_t o = (size_t)b * gamma + (k - 1);
-    const float u = u01(draw_block(seed, 0u, (uint32_t)k, (uint32_t)b, 1u).x);
-    if (!(u < p_t[o] / q_tok[o])) {
-      j = k;
-      break;
+  const int L = clamp_ell(ell, b, gamma, lane == 0 ? err : nullptr);
+  const int k = lane + 1;
+  bool reject = false;
+  if (k <= L) {
+    const int row = b * gamma + (k - 1);
+    float m = -INFINITY, s = 0.f;
+    for (int i = 0; i < splits; ++i) {
+      const float2 q = __ldcg(stats + (size_t)row * splits + i);
+      max_sum_merge(m, s, q.x, q.y);
     }
+    const int x = tokens[(size_t)b * gamma + (k - 1)];
+    float p = 0.f;
+    if (x >= 0 && x < V) {
+      p = expf(__ldg(T + ((size_t)b * (gamma + 1) + (k - 1)) * V + x) - m) / s;
+    } else {
+      set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
+    }
+    M_t[row] = m;
+    lnS_t[row] = logf(s);
+    p_t[row] = p;
+    const float u = u01(draw_block(seed, 0u, (uint32_t)k, (uint32_t)b, 1u).x);
+    reject = !(u < p / q_tok[row]);
   }
+  const unsigned rej = __ballot_sync(0xffffffffu, reject);
+  const int j = rej ? __ffs(rej) : 0;    // first rejected position, 0 if none
   const int acc = j ? j - 1 : L;
-  for (int i = 0; i <= gamma; ++i)
+  for (int i = lane; i <= gamma; i += 32)
     out_tokens[(size_t)b * (gamma + 1) + i] = i < acc ? tokens[(size_t)b * gamma + i] : -1;
-  accept_len[b] = acc;
-  n_out[b] = acc + 1;
-  fallback[b] = 0;
-  if (j) {
-    mode[b] = kModeResidual;
-    pos[b] = j;
-    prev_tok[b] = (j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)];
-  } else {
-    mode[b] = kModeBonus;
-    pos[b] = L + 1;
-    prev_tok[b] = -1;
+  if (lane == 0) {
+    accept_len[b] = acc;
+    n_out[b] = acc + 1;
+    fallback[b] = 0;
+    if (j) {
+      mode[b] = kModeResidual;
+      pos[b] = j;
+      prev_tok[b] = (j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)];
+    } else {
+      mode[b] = kModeBonus;
+      pos[b] = L + 1;
+      prev_tok[b] = -1;
+    }
   }
 }
 
 // ----------------------------------------------------------------------- final sample
+// Gumbel-max in exponential-race form with a conservative two-phase filter.  Residual:
+// score_v = log(P_v - Q_v) - log E_v with E_v = -log1p(-w_v), and w <= E <= w / (1 - w),
+// so with r_v = P_v - Q_v
+//     r_v (1 - w_v) / w_v  <=  exp(score_v)  <=  r_v / w_v.
+// Phase 1 computes both bounds for every logit of the CTA's segment (two exp2 per logit,
+// no logarithms) and the CTA-wide best lower bound L; phase 2 scores exactly, with the same
+// fp32 formulas as an unfiltered scan, only the logits whose upper bound reaches L (a few
+// per CTA).  Bounds and L carry a 2^-12 relative slack, far above the fp32 errors of
+// either side, so the argmax is that of the unfiltered scan.  The bonus row (all drafts
+// accepted) is the same race over exp(T_v - m), m the CTA's largest logit.
+constexpr float kRaceSlack = 0x1.0p-12f;
+
+__device__ __forceinline__ float block_max_f(float x, float* red) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  x = red[0];
+#pragma unroll
+  for (int w = 1; w < kSampleThreads / 32; ++w) x = fmaxf(x, red[w]);
+  __syncthreads();
+  return x;
+}
+
 __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const float* __restrict__ T, const float* __restrict__ U, const float* __restrict__ bias,
     const float* __restrict__ row_max, const float* __restrict__ row_sumexp,
     const float* __restrict__ M_t, const float* __restrict__ lnS_t,
     const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
-    const int32_t* __restrict__ accept_len, int gamma, int V, uint64_t seed, int splits, int seg,
-    RowState* __restrict__ partials, uint32_t* __restrict__ counters,
-    int32_t* __restrict__ out_tokens, int32_t* __restrict__ fallback) {
+    int gamma, int V, uint64_t seed, int splits, RowState* __restrict__ partials) {
   __shared__ RowState red[32];
-  __shared__ int is_last;
+  __shared__ float redf[kSampleThreads / 32];
   const int b = blockIdx.y;
   const int md = mode[b], k = pos[b];
-  const int v_begin = blockIdx.x * seg, v_end = min(V, v_begin + seg);
-  RowState st = row_state_empty();
-  if (md == kModeResidual) {
+  if (md != kModeResidual && md != kModeBonus) return;
+  const bool residual = md == kModeResidual;
+  const int v0 = blockIdx.x * kVerSeg + 4 * threadIdx.x;
+  const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
+  float4 t[kVerVec], zz[kVerVec];
+#pragma unroll
+  for (int j = 0; j < kVerVec; ++j) {
+    const int v = v0 + j * 4 * kSampleThreads;
+    t[j] = v < V ? ld_stream_f4(Trow + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+  float off_a = 0.f, off_b = 0.f;   // residual: log P = T - off_a, log Q = z - off_b
+  if (residual) {
     const size_t o = (size_t)b * gamma + (k - 1);
-    const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
     const float* Urow = U + o * V;
     const float* Brow = bias + (size_t)b * V;
-    const float q_off = row_max[o] + logf(row_sumexp[o]);   // log Q = z - q_off
-    const float p_off = M_t[o] + lnS_t[o];                   // log P = T - p_off
-    for (int v = v_begin + 4 * threadIdx.x; v < v_end; v += 4 * kSampleThreads) {
-      const float4 t4 = ld_stream_f4(Trow + v);
-      const float4 u4 = ld_stream_f4(Urow + v);
-      const float4 b4 = __ldcg(reinterpret_cast<const float4*>(Brow + v));
-      const float t[4] = {t4.x, t4.y, t4.z, t4.w};
-      const float z[4] = {u4.x + b4.x, u4.y + b4.y, u4.z + b4.z, u4.w + b4.w};
-      const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 2u);
-      const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lq = z[i] - q_off;
-        const float d = (t[i] - p_off) - lq;     // log(P / Q)
-        if (d > 0.f) {
-          // log(P - Q) = log Q + log(expm1(log P - log Q)), accurate when P ~ Q; for
-          // d > 20 it is log P to within 2e-9
-          const float lres = d > 20.f ? lq + d : lq + logf(expm1f(d));
-          const float score = lres + gumbel_of(dw[i]);
-          if (better(score, v + i, st.score, st.idx)) {
-            st.score = score;
-            st.idx = v + i;
-          }
-        }
+    for (int j = 0; j < kVerVec; ++j) {
+      const int v = v0 + j * 4 * kSampleThreads;
+      if (v < V) {
+        const float4 u4 = ld_stream_f4(Urow + v);
+        const float4 b4 = __ldcg(reinterpret_cast<const float4*>(Brow + v));
+        zz[j] = make_float4(u4.x + b4.x, u4.y + b4.y, u4.z + b4.z, u4.w + b4.w);
+      } else {
+        zz[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-  } else if (md == kModeBonus) {
-    const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
-    for (int v = v_begin + 4 * threadIdx.x; v < v_end; v += 4 * kSampleThreads) {
-      const float4 t4 = ld_stream_f4(Trow + v);
-      const float t[4] = {t4.x, t4.y, t4.z, t4.w};
-      const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 3u);
-      const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float score = t[i] + gumbel_of(dw[i]);
-        if (better(score, v + i, st.score, st.idx)) {
-          st.score = score;
-          st.idx = v + i;
-        }
-      }
-    }
+    off_b = row_max[o] + logf(row_sumexp[o]);
+    off_a = M_t[o] + lnS_t[o];
   } else {
-    return;
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kVerVec; ++j) m = fmaxf(m, fmaxf(fmaxf(t[j].x, t[j].y), fmaxf(t[j].z, t[j].w)));
+    off_a = block_max_f(m, redf);
+  }
+  const uint32_t stream = residual ? 2u : 3u;
+  // phase 1: per logit the upper bound numerator r_hi (compared against L w) and the
+  // thread's best lower bound
+  float r_hi[kVerVec][4], w[kVerVec][4];
+  float Lt = 0.f;
+#pragma unroll
+  for (int j = 0; j < kVerVec; ++j) {
+    const int v = v0 + j * 4 * kSampleThreads;
+    const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, stream);
+    const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w};
+    const float tv[4] = {t[j].x, t[j].y, t[j].z, t[j].w};
+    const float zv[4] = {zz[j].x, zz[j].y, zz[j].z, zz[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[j][i] = one_minus_u01(dw[i]);
+      float r, e;
+      bool in = v < V;
+      if (residual) {
+        const float lp = tv[i] - off_a, lq = zv[i] - off_b;
+        in = in && (lp - lq > 0.f);                    // the residual's support
+        const float P = ex2_approx(lp * kLog2e), Q = ex2_approx(lq * kLog2e);
+        r = P - Q;
+        e = (P + Q) * kRaceSlack;
+        // both flushed to zero: the bounds say nothing, keep it for exact scoring
+        if (in && P + Q == 0.f) { r = INFINITY; e = 0.f; }
+      } else {
+        r = ex2_approx(fmaf(tv[i], kLog2e, -off_a * kLog2e));
+        e = r * kRaceSlack;
+      }
+      r_hi[j][i] = in ? r + e : -1.f;
+      if (in && r - e > 0.f && r != INFINITY)
+        Lt = fmaxf(Lt, (r - e) * (1.f - w[j][i]) * rcp_approx_ftz(w[j][i]) * (1.f - kRaceSlack));
+    }
+  }
+  const float L = block_max_f(Lt, redf);
+  // phase 2: exact scores of the logits whose upper bound reaches L
+  RowState st = row_state_empty();
+#pragma unroll
+  for (int j = 0; j < kVerVec; ++j) {
+    unsigned cm = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cm |= (r_hi[j][i] >= 0.f && r_hi[j][i] >= L * w[j][i] ? 1u : 0u) << i;
+    if (cm == 0u) continue;
+    const int v = v0 + j * 4 * kSampleThreads;
+    const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, stream);
+    const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w};
+    const float tv[4] = {t[j].x, t[j].y, t[j].z, t[j].w};
+    const float zv[4] = {zz[j].x, zz[j].y, zz[j].z, zz[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (!((cm >> i) & 1u)) continue;
+      float score;
+      if (residual) {
+        const float lq = zv[i] - off_b;
+        const float d = (tv[i] - off_a) - lq;          // log(P / Q) > 0
+        // log(P - Q) = log Q + log(expm1(log P - log Q)), accurate when P ~ Q; for
+        // d > 20 it is log P to within 2e-9
+        const float lres = d > 20.f ? lq + d : lq + logf(expm1f(d));
+        score = lres + gumbel_of(dw[i]);
+      } else {
+        score = tv[i] + gumbel_of(dw[i]);
+      }
+      if (better(score, v + i, st.score, st.idx)) {
+        st.score = score;
+        st.idx = v + i;
+      }
+    }
   }
   st = row_state_block_reduce(st, red);
-  if (!publish_partial(st, partials + (size_t)b * splits + blockIdx.x, &counters[b], splits,
-                       &is_last))
-    return;
-  if (threadIdx.x < 32) {
-    const RowState acc = merge_partials(partials + (size_t)b * splits, splits);
-    if (threadIdx.x == 0) {
-      if (acc.idx >= 0) {
-        out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = acc.idx;
-      } else {
-        fallback[b] = 1;
-      }
-      counters[b] = 0u;
+  if (threadIdx.x == 0) partials[(size_t)b * splits + blockIdx.x] = st;
+}
+
+// One warp per request: the best (score, index) over the row's partials is the token.
+__global__ void __launch_bounds__(128) finalize_kernel(
+    const RowState* __restrict__ partials, int splits, int B, int gamma,
+    const int32_t* __restrict__ mode, const int32_t* __restrict__ accept_len,
+    int32_t* __restrict__ out_tokens, int32_t* __restrict__ fallback) {
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b >= B) return;
+  const int md = mode[b];
+  if (md != kModeResidual && md != kModeBonus) return;
+  const RowState acc = merge_partials(partials + (size_t)b * splits, splits);
+  if ((threadIdx.x & 31) == 0) {
+    if (acc.idx >= 0) {
+      out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = acc.idx;
+    } else {
+      fallback[b] = 1;
     }
   }
 }
@@ -289,11 +401,9 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   int* err = ws_at<int>(ws, p.off_err);
   float* bias = ws_at<float>(ws, p.off_bias);
   RowState* part = ws_at<RowState>(ws, p.off_part);
-  RowState* part_stats = part;
+  float2* part_stats = reinterpret_cast<float2*>(part);
   RowState* part_ver = part + (size_t)B * gamma * p.stats.splits;
-  uint32_t* cnt_stats = ws_at<uint32_t>(ws, p.off_cnt);
-  uint32_t* cnt_ver = cnt_stats + (size_t)B * gamma;
-  uint32_t* cnt_fb = cnt_ver + B;
+  uint32_t* cnt_fb = ws_at<uint32_t>(ws, p.off_cnt);
   float* M_t = ws_at<float>(ws, p.off_M);
   float* lnS_t = ws_at<float>(ws, p.off_lnS);
   float* p_t = ws_at<float>(ws, p.off_p);
@@ -302,22 +412,24 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   int32_t* prev = ws_at<int32_t>(ws, p.off_prev);
   int32_t* fb = ws_at<int32_t>(ws, p.off_fallback);
 
-  cudaError_t e = cudaMemsetAsync(cnt_stats, 0, ((size_t)B * gamma + 2 * (size_t)B) * sizeof(uint32_t),
-                                  stream);
+  cudaError_t e = cudaMemsetAsync(cnt_fb, 0, (size_t)B * sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   target_stats_kernel<<<dim3(p.stats.splits, B * gamma), kSampleThreads, 0, stream>>>(
-      T, tokens, ell, gamma, V, p.stats.splits, p.stats.seg, part_stats, cnt_stats, M_t, lnS_t, p_t,
-      err);
+      T, ell, B, gamma, V, p.stats.splits, part_stats);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  decide_kernel<<<cdiv(B, 128), 128, 0, stream>>>(anchor, tokens, q_tok, p_t, ell, B, gamma, seed,
-                                                  accept_len, out_tokens, n_out, mode, pos, prev,
-                                                  fb, err);
+  decide_kernel<<<cdiv(B, 4), 128, 0, stream>>>(T, anchor, tokens, q_tok, part_stats,
+                                                p.stats.splits, ell, B, gamma, V, seed, M_t,
+                                                lnS_t, p_t, accept_len, out_tokens, n_out, mode,
+                                                pos, prev, fb, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_bias_gemm(w2_map, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
     return e;
   final_sample_kernel<<<dim3(p.ver.splits, B), kSampleThreads, 0, stream>>>(
-      T, U, bias, row_max, row_sumexp, M_t, lnS_t, mode, pos, accept_len, gamma, V, seed,
-      p.ver.splits, p.ver.seg, part_ver, cnt_ver, out_tokens, fb);
+      T, U, bias, row_max, row_sumexp, M_t, lnS_t, mode, pos, gamma, V, seed, p.ver.splits,
+      part_ver);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  finalize_kernel<<<cdiv(B, 4), 128, 0, stream>>>(part_ver, p.ver.splits, B, gamma, mode,
+                                                  accept_len, out_tokens, fb);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   fallback_kernel<<<dim3(p.ver.splits, B), kSampleThreads, 0, stream>>>(
       T, pos, accept_len, fb, gamma, V, seed, p.ver.splits, p.ver.seg, part_ver, cnt_fb, out_tokens);
