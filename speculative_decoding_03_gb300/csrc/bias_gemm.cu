@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(128) bias_gemm_kernel(const __grid_constant__ 
     tma_load_2d(sA, &w2_map, &bar_tma, v0, 0, pol);
     tma_load_2d(sA + (size_t)r * 128, &w2_map, &bar_tma, v0 + 64, 0, pol);
   }
+  // the W2 tile is an input; the request tokens (prev) may come from the previous kernel
+  pdl_wait();
+  pdl_launch_dependents();
 
   // Gather E = W1[prev_b] (rows b0 .. b0+NB-1) as the K-major B operand: row n is 128-byte
   // lines of 64 bf16 per K-block, 16-byte chunk c of row n stored at chunk c ^ (n % 8).
@@ -173,9 +176,8 @@ cudaError_t launch_bias_gemm(const CUtensorMap* w2_map, const uint16_t* W1, cons
     attr_set = true;
   }
   dim3 grid(cdiv(V, kGemmTileV), cdiv(B, NB));
-  bias_gemm_kernel<<<grid, 128, smem, stream>>>(*w2_map, W1, prev, prev_stride, B, V, r, NB, cols,
-                                                out, err);
-  return cudaGetLastError();
+  return launch_pdl(bias_gemm_kernel, grid, dim3(128), smem, stream, *w2_map, W1, prev, prev_stride,
+                    B, V, r, NB, cols, out, err);
 }
 
 }  // namespace dspark

@@ -147,6 +147,17 @@ __device__ __forceinline__ RowState row_state_block_reduce(RowState a, RowState*
   return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
+// may be scheduled while the previous kernel on the stream is still draining: pdl_wait()
+// (griddepcontrol.wait) blocks until that kernel has completed and its writes are visible,
+// and every such kernel calls it before reading anything an earlier kernel wrote and before
+// it can exit.  pdl_launch_dependents() lets the next kernel be scheduled once every CTA of
+// this grid has issued it.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 128-bit streaming load: read once, cache-streaming (evict-first) hint.
 __device__ __forceinline__ float4 ld_stream_f4(const float* p) {
   return __ldcs(reinterpret_cast<const float4*>(p));

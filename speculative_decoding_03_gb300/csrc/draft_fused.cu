@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_base_s;
+  // the next kernel on the stream (launched with programmatic serialization) may be
+  // scheduled as soon as SMs free up; it waits for this grid's completion itself
+  pdl_launch_dependents();
 
   // One thread's bounded wait; a timeout aborts the CTA.  The abort flag is read only once
   // the first (sleeping) try has not seen the phase complete: a shared-memory read ahead of

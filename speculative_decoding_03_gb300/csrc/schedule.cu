@@ -35,8 +35,16 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   extern __shared__ unsigned long long keys[];
   __shared__ long long warp_tot[32];
   __shared__ int first_fail;
+  __shared__ float sps_s[kSchedThreads + 1];   // sps[R .. R + N] when N <= kSchedThreads
+  __shared__ int cnt_s[kSchedThreads];         // admitted items per request when R <= kSchedThreads
+  pdl_wait();                 // the expected returns come from the previous kernel
+  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int N = R * gamma;
+  const bool small = N <= kSchedThreads;
+  // the SPS table entries the scan reads, fetched together with the expected returns
+  if (small && tid <= N) sps_s[tid] = sps[R + tid];
+  if (R <= kSchedThreads && tid < R) cnt_s[tid] = 0;
 
   for (int i = tid; i < Npad; i += kSchedThreads) {
     unsigned long long key = ~0ull;
@@ -48,16 +56,25 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     }
     keys[i] = key;
   }
-  for (int r = tid; r < R; r += kSchedThreads) ell[r] = 0;
+  if (R > kSchedThreads)
+    for (int r = tid; r < R; r += kSchedThreads) ell[r] = 0;
   if (tid == 0) first_fail = N + 1;
   __syncthreads();
 
-  if (N <= kSchedThreads) {
+  if (small) {
     // small batches: every key is distinct, so its rank is the number of smaller keys;
     // one pass of broadcast shared-memory reads, no sorting network
     const unsigned long long mine = tid < N ? keys[tid] : ~0ull;
-    int rank = 0;
-    for (int j = 0; j < N; ++j) rank += keys[j] < mine ? 1 : 0;
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    int j = 0;
+    for (; j + 4 <= N; j += 4) {
+      r0 += keys[j] < mine ? 1 : 0;
+      r1 += keys[j + 1] < mine ? 1 : 0;
+      r2 += keys[j + 2] < mine ? 1 : 0;
+      r3 += keys[j + 3] < mine ? 1 : 0;
+    }
+    for (; j < N; ++j) r0 += keys[j] < mine ? 1 : 0;
+    const int rank = r0 + r1 + r2 + r3;
     __syncthreads();
     if (tid < N) keys[rank] = mine;
     __syncthreads();
@@ -109,9 +126,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   for (int i = c0; i < c1; ++i) {
     const long long A = 4294967296LL - (long long)(keys[i] >> 21);
     const int n = i + 1;
-    const double th_prev = theta_at(R, S, sps[R + n - 1]);
+    const double th_prev = theta_at(R, S, small ? sps_s[n - 1] : sps[R + n - 1]);
     S += A;
-    const double th = theta_at(R, S, sps[R + n]);
+    const double th = theta_at(R, S, small ? sps_s[n] : sps[R + n]);
     if (!(th > th_prev)) {
       fail = n;
       break;
@@ -120,21 +137,29 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   if (fail <= N) atomicMin(&first_fail, fail);
   __syncthreads();
   const int admitted = first_fail - 1;
-  for (int i = tid; i < admitted; i += kSchedThreads) {
-    const int r = (int)((keys[i] >> 5) & 0xFFFFull);
-    atomicAdd(&ell[r], 1);
+  if (R <= kSchedThreads) {
+    // per-request counts in shared memory, then one coalesced store of ell
+    for (int i = tid; i < admitted; i += kSchedThreads)
+      atomicAdd(&cnt_s[(int)((keys[i] >> 5) & 0xFFFFull)], 1);
+    __syncthreads();
+    if (tid < R) ell[tid] = cnt_s[tid];
+  } else {
+    for (int i = tid; i < admitted; i += kSchedThreads) {
+      const int r = (int)((keys[i] >> 5) & 0xFFFFull);
+      atomicAdd(&ell[r], 1);
+    }
   }
   // Theta at the stop: S_admitted lies in the chunk holding item `admitted`
   if (admitted == 0) {
     if (tid == 0) {
       *B_total = R;
-      *theta = theta_at(R, 0, sps[R]) / 4294967296.0;
+      *theta = theta_at(R, 0, small ? sps_s[0] : sps[R]) / 4294967296.0;
     }
   } else if (admitted - 1 >= c0 && admitted - 1 < c1) {
     long long Sa = incl - local + (warp > 0 ? warp_tot[warp - 1] : 0);
     for (int i = c0; i < admitted; ++i) Sa += 4294967296LL - (long long)(keys[i] >> 21);
     *B_total = R + admitted;
-    *theta = theta_at(R, Sa, sps[R + admitted]) / 4294967296.0;
+    *theta = theta_at(R, Sa, small ? sps_s[admitted] : sps[R + admitted]) / 4294967296.0;
   }
 }
 
@@ -154,8 +179,8 @@ cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps, 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  schedule_kernel<<<1, kSchedThreads, smem, stream>>>(a, R, gamma, Npad, sps, ell, B_total, theta);
-  return cudaGetLastError();
+  return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, stream, a, R, gamma, Npad,
+                    sps, ell, B_total, theta);
 }
 
 }  // namespace dspark

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kSampleThreads) target_stats_kernel(
     const float* __restrict__ T, const int32_t* __restrict__ ell, int B, int gamma, int V,
     int splits, float2* __restrict__ partials) {
   __shared__ float red_m[kSampleThreads / 32], red_s[kSampleThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int k = blockIdx.y / B + 1, b = blockIdx.y - (k - 1) * B;
   if (k > clamp_ell(ell, b, gamma, nullptr)) return;
   const int row = b * gamma + (k - 1);
@@ -140,7 +142,10 @@ __global__ void __launch_bounds__(128) decide_kernel(
     int gamma, int V, uint64_t seed, float* __restrict__ M_t, float* __restrict__ lnS_t,
     float* __restrict__ p_t, int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ n_out, int32_t* __restrict__ mode, int32_t* __restrict__ pos,
-    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, int* err) {
+    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, uint32_t* __restrict__ fb_count,
+    int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(128) decide_kernel(
     accept_len[b] = acc;
     n_out[b] = acc + 1;
     fallback[b] = 0;
+    fb_count[b] = 0u;
     if (j) {
       mode[b] = kModeResidual;
       pos[b] = j;
@@ -221,6 +227,8 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     int gamma, int V, uint64_t seed, int splits, RowState* __restrict__ partials) {
   __shared__ RowState red[32];
   __shared__ float redf[kSampleThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.y;
   const int md = mode[b], k = pos[b];
   if (md != kModeResidual && md != kModeBonus) return;
@@ -334,6 +342,8 @@ __global__ void __launch_bounds__(128) finalize_kernel(
     const RowState* __restrict__ partials, int splits, int B, int gamma,
     const int32_t* __restrict__ mode, const int32_t* __restrict__ accept_len,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ fallback) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
   const int md = mode[b];
@@ -356,6 +366,8 @@ __global__ void __launch_bounds__(kSampleThreads) fallback_kernel(
     uint32_t* __restrict__ counters, int32_t* __restrict__ out_tokens) {
   __shared__ RowState red[32];
   __shared__ int is_last;
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.y;
   if (!fallback[b]) return;
   const int k = pos[b];
@@ -412,27 +424,28 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   int32_t* prev = ws_at<int32_t>(ws, p.off_prev);
   int32_t* fb = ws_at<int32_t>(ws, p.off_fallback);
 
-  cudaError_t e = cudaMemsetAsync(cnt_fb, 0, (size_t)B * sizeof(uint32_t), stream);
+  cudaError_t e = launch_pdl(target_stats_kernel, dim3(p.stats.splits, B * gamma),
+                             dim3(kSampleThreads), 0, stream, T, ell, B, gamma, V,
+                             p.stats.splits, part_stats);
   if (e != cudaSuccess) return e;
-  target_stats_kernel<<<dim3(p.stats.splits, B * gamma), kSampleThreads, 0, stream>>>(
-      T, ell, B, gamma, V, p.stats.splits, part_stats);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  decide_kernel<<<cdiv(B, 4), 128, 0, stream>>>(T, anchor, tokens, q_tok, part_stats,
-                                                p.stats.splits, ell, B, gamma, V, seed, M_t,
-                                                lnS_t, p_t, accept_len, out_tokens, n_out, mode,
-                                                pos, prev, fb, err);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_pdl(decide_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream, T, anchor, tokens, q_tok,
+                 (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, M_t, lnS_t,
+                 p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, cnt_fb, err);
+  if (e != cudaSuccess) return e;
   if ((e = launch_bias_gemm(w2_map, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
     return e;
-  final_sample_kernel<<<dim3(p.ver.splits, B), kSampleThreads, 0, stream>>>(
-      T, U, bias, row_max, row_sumexp, M_t, lnS_t, mode, pos, gamma, V, seed, p.ver.splits,
-      part_ver);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  finalize_kernel<<<cdiv(B, 4), 128, 0, stream>>>(part_ver, p.ver.splits, B, gamma, mode,
-                                                  accept_len, out_tokens, fb);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  fallback_kernel<<<dim3(p.ver.splits, B), kSampleThreads, 0, stream>>>(
-      T, pos, accept_len, fb, gamma, V, seed, p.ver.splits, p.ver.seg, part_ver, cnt_fb, out_tokens);
+  e = launch_pdl(final_sample_kernel, dim3(p.ver.splits, B), dim3(kSampleThreads), 0, stream, T, U,
+                 (const float*)bias, row_max, row_sumexp, (const float*)M_t, (const float*)lnS_t,
+                 (const int32_t*)mode, (const int32_t*)pos, gamma, V, seed, p.ver.splits, part_ver);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(finalize_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream,
+                 (const RowState*)part_ver, p.ver.splits, B, gamma, (const int32_t*)mode,
+                 (const int32_t*)accept_len, out_tokens, fb);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(fallback_kernel, dim3(p.ver.splits, B), dim3(kSampleThreads), 0, stream, T,
+                 (const int32_t*)pos, (const int32_t*)accept_len, (const int32_t*)fb, gamma, V,
+                 seed, p.ver.splits, p.ver.seg, part_ver, cnt_fb, out_tokens);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
