@@ -197,6 +197,21 @@ dspark_status dspark_verify(const float* T, const float* U, const uint16_t* W1,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * dspark_verify with the packed tile images of dspark_pack_w2 (W2p) in place of W2: the
+ * residual rows' bias contraction streams W2p, which a preceding dspark_draft_packed call
+ * has just brought into L2.  Same arguments, workspace, outputs and results otherwise;
+ * W2p is caller-owned, 16-byte aligned, of dspark_packed_w2_bytes(V, r) bytes.
+ */
+dspark_status dspark_verify_packed(const float* T, const float* U, const uint16_t* W1,
+                                   const uint16_t* W2p, const int32_t* anchor,
+                                   const int32_t* tokens, const float* q_tok,
+                                   const float* row_max, const float* row_sumexp,
+                                   const int32_t* ell, int B, int gamma, int V, int r,
+                                   uint64_t seed, int32_t* accept_len, int32_t* out_tokens,
+                                   int32_t* n_out, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
+/*
  * The draft of dspark_draft for callers that cannot allocate device memory when they
  * draft (a serving loop whose device memory is all reserved by its own pool, a plugin
  * that is handed only its input and output buffers, code where a cudaMalloc would

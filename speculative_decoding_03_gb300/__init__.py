@@ -2,7 +2,8 @@
 
 The library behind this binding (``include/dspark.h``) holds the four calls of one
 speculative step -- ``dspark_draft``, ``dspark_confidence``, ``dspark_schedule``,
-``dspark_verify`` -- plus ``dspark_markov_bias``; every step of the computation runs in
+``dspark_verify`` -- plus ``dspark_markov_bias`` and the packed-W2 variants of the draft and
+the verification; every step of the computation runs in
 its CUDA kernels.  This module only marshals arguments: it passes device pointers of
 torch tensors and the current CUDA stream through ctypes, and allocates outputs and the
 workspace with torch.  There is no CPU fallback: without the built library and a CUDA
@@ -35,6 +36,8 @@ SIGNATURES = [
     ("dspark_schedule", _I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_verify", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64,
                            _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_verify_packed", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64,
+                                  _P, _P, _P, _P, _SZ, _P]),
     ("dspark_draft_noalloc", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P]),
     ("dspark_last_device_status", _I, [_P, _P]),
 ]
@@ -221,6 +224,24 @@ def verify(T, U, W1, W2, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed: 
     return out
 
 
+def verify_packed(T, U, W1, W2p, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed: int,
+                  ws: Workspace, out: Optional[Dict] = None, stream=None):
+    """verify with the packed W2 of pack_w2 (the copy draft_packed streams)."""
+    torch = _torch()
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=U.device),
+                   out_tokens=torch.empty((B, gamma + 1), dtype=torch.int32, device=U.device),
+                   n_out=torch.empty(B, dtype=torch.int32, device=U.device))
+    _check("dspark_verify_packed", lib().dspark_verify_packed(
+        _ptr(T), _ptr(U), _ptr(W1), _ptr(W2p), _ptr(anchor), _ptr(tokens), _ptr(q_tok),
+        _ptr(row_max), _ptr(row_sumexp), _ptr(ell), B, gamma, V, r, ctypes.c_uint64(seed),
+        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["n_out"]),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
 # ------------------------------------------------------------------------ whole step
 
 class Step:
@@ -263,8 +284,12 @@ class Step:
         c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
                           self.conf_out, stream)
         ell, _, _ = schedule(a, x["sps"], self.ws, self.sched_out, stream)
-        verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d["tokens"], d["q_tok"],
-               d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
+        if self.W2p is not None:
+            verify_packed(x["T"], x["U"], x["W1"], self.W2p, x["anchor"], d["tokens"], d["q_tok"],
+                          d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
+        else:
+            verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d["tokens"], d["q_tok"],
+                   d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
         return self
 
     def capture(self, seeds, draft_only: bool = False):

@@ -54,10 +54,8 @@ dspark_status dspark_markov_bias(const uint16_t* W1, const uint16_t* W2, const i
   if (!aligned(W1, 16) || !aligned(W2, 16) || !aligned(prev, 4) || !aligned(out, 4))
     return DSPARK_ERR_INVALID_ARG;
   if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
-  CUtensorMap w2_map;
-  if (!encode_w2_map(&w2_map, W2, V, r, r)) return DSPARK_ERR_CUDA;
-  if (launch_bias_gemm(&w2_map, W1, prev, prev_stride, B, V, r, out, ws_at<int>(workspace, 0),
-                       stream) != cudaSuccess)
+  if (launch_bias_gemm(W2, nullptr, W1, prev, prev_stride, B, V, r, out,
+                       ws_at<int>(workspace, 0), stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
@@ -116,27 +114,60 @@ dspark_status dspark_schedule(const float* a, int R, int gamma, const float* sps
   return DSPARK_OK;
 }
 
-dspark_status dspark_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2,
-                            const int32_t* anchor, const int32_t* tokens, const float* q_tok,
-                            const float* row_max, const float* row_sumexp, const int32_t* ell,
-                            int B, int gamma, int V, int r, uint64_t seed, int32_t* accept_len,
-                            int32_t* out_tokens, int32_t* n_out, void* workspace,
-                            size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// dspark_verify and dspark_verify_packed: W2 xor W2p (the packed tile images) is given
+dspark_status verify_common(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2,
+                            const uint16_t* W2p, const int32_t* anchor, const int32_t* tokens,
+                            const float* q_tok, const float* row_max, const float* row_sumexp,
+                            const int32_t* ell, int B, int gamma, int V, int r, uint64_t seed,
+                            int32_t* accept_len, int32_t* out_tokens, int32_t* n_out,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   dspark_status st = check_shape(B, gamma, V, r, 0);
   if (st != DSPARK_OK) return st;
-  if (!aligned(T, 16) || !aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16) ||
+  if (!aligned(T, 16) || !aligned(U, 16) || !aligned(W1, 16) || !aligned(W2 ? W2 : W2p, 16) ||
       !aligned(anchor, 4) || !aligned(tokens, 4) || !aligned(q_tok, 4) || !aligned(row_max, 4) ||
       !aligned(row_sumexp, 4) || !aligned(ell, 4) || !aligned(accept_len, 4) ||
       !aligned(out_tokens, 4) || !aligned(n_out, 4))
     return DSPARK_ERR_INVALID_ARG;
   const Plan p = make_plan(B, gamma, V, r, 0);
   if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
-  CUtensorMap w2_map;
-  if (!encode_w2_map(&w2_map, W2, V, r, r)) return DSPARK_ERR_CUDA;
-  if (launch_verify(p, T, U, W1, &w2_map, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed,
+  if (launch_verify(p, T, U, W1, W2, W2p, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed,
                     accept_len, out_tokens, n_out, workspace, stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dspark_status dspark_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2,
+                            const int32_t* anchor, const int32_t* tokens, const float* q_tok,
+                            const float* row_max, const float* row_sumexp, const int32_t* ell,
+                            int B, int gamma, int V, int r, uint64_t seed, int32_t* accept_len,
+                            int32_t* out_tokens, int32_t* n_out, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+  if (!W2) return DSPARK_ERR_INVALID_ARG;
+  return verify_common(T, U, W1, W2, nullptr, anchor, tokens, q_tok, row_max, row_sumexp, ell, B,
+                       gamma, V, r, seed, accept_len, out_tokens, n_out, workspace,
+                       workspace_bytes, stream);
+}
+
+dspark_status dspark_verify_packed(const float* T, const float* U, const uint16_t* W1,
+                                   const uint16_t* W2p, const int32_t* anchor,
+                                   const int32_t* tokens, const float* q_tok,
+                                   const float* row_max, const float* row_sumexp,
+                                   const int32_t* ell, int B, int gamma, int V, int r,
+                                   uint64_t seed, int32_t* accept_len, int32_t* out_tokens,
+                                   int32_t* n_out, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  if (!W2p) return DSPARK_ERR_INVALID_ARG;
+  return verify_common(T, U, W1, nullptr, W2p, anchor, tokens, q_tok, row_max, row_sumexp, ell, B,
+                       gamma, V, r, seed, accept_len, out_tokens, n_out, workspace,
+                       workspace_bytes, stream);
 }
 
 dspark_status dspark_last_device_status(void* workspace, cudaStream_t stream) {

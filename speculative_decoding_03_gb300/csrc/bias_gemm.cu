@@ -4,49 +4,84 @@
 // request is B(x_{k-1}, .) = W1[x_{k-1}] W2, rank r.  For a whole batch this is the
 // contraction  bias^T [V, B] = W2^T [V, r] x E^T [r, B]  with E[b] = W1[prev_b].
 //
-// One CTA computes a 128-row vocabulary tile for one batch chunk of NB requests:
-//   A = W2^T tile (M = 128 vocabulary rows, K = r), MN-major in shared memory, brought in
-//       by two TMA tile loads of 64 columns x r rows with the 128-byte swizzle;
-//   B = E^T (N = NB requests, K = r), K-major, gathered from W1 rows by the CTA's threads
-//       and written in the same 128-byte-swizzled layout;
-//   D = fp32 accumulators in tensor memory (128 lanes x NB columns), issued by one thread
-//       as r / 16 tcgen05.mma instructions (kind::f16, bf16 inputs);
-// then the four warps read D back (lane = vocabulary row) and store bias[b][v] with
-// coalesced 128-byte rows.
+// A persistent, warp-specialised kernel (one or two CTAs per SM, each owning a contiguous
+// run of 128-row vocabulary tiles) computes bias^T tile by tile:
+//   producer warp   streams the W2^T tiles as K-chunks of up to 64 rank rows (two TMA boxes
+//                   of 64 vocabulary columns, 128-byte swizzle, or one bulk copy of the
+//                   packed tile image) through a 4-stage ring;
+//   MMA warp        one lane issues tcgen05.mma (M = 128 vocabulary rows, N = NB requests,
+//                   K = 16 per instruction, bf16 in, fp32 accumulators in tensor memory)
+//                   into one of four accumulators;
+//   4 epilogue warps gather E = W1[prev_b] for each chunk of NB requests into the K-major
+//                   B operand, and read the accumulators back (lane = vocabulary row) into
+//                   coalesced 128-byte stores of bias[b][v].
+// The producer starts on W2 (an input) before the previous kernel on the stream has
+// finished; the epilogue warps wait for it before reading prev.
 #include "internal.h"
 #include "sm100_ptx.cuh"
+
+#include <string.h>
+
+#include <type_traits>
 
 namespace dspark {
 namespace {
 
 using namespace sm100;
 
-__global__ void __launch_bounds__(128) bias_gemm_kernel(const __grid_constant__ CUtensorMap w2_map,
-                                                        const uint16_t* __restrict__ W1,
-                                                        const int32_t* __restrict__ prev,
-                                                        int prev_stride, int B, int V, int r,
-                                                        int NB, uint32_t tmem_cols,
-                                                        float* __restrict__ out, int* err) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_tma, bar_mma;
-  __shared__ uint32_t tmem_base_s;
+__device__ __forceinline__ void named_bar_sync_n(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
+constexpr int kBiasWarps = 6;                 // producer, MMA, 4 epilogue warps
+constexpr int kBiasThreads = kBiasWarps * 32;
+constexpr int kBiasStages = 4;                // W2 K-chunk ring (16 KB each at 64 rows)
+constexpr int kBiasDepth = 4;                 // accumulators in tensor memory
+constexpr int kBiasKChunkMax = 64;
+constexpr int kBiasNamedBar = 1;              // the epilogue warps' barrier
+
+struct BiasSmem {
+  static constexpr int kStageBytes = 2 * kBiasKChunkMax * 128;
+  static constexpr int kOffW = 0;
+  static constexpr int kOffE = kOffW + kBiasStages * kStageBytes;
+  static constexpr int kEBytes = 32 * 256 * 2;   // NB <= 32 requests x r <= 256
+  static constexpr int kBytes = kOffE + 2 * kEBytes;
+};
+
+template <int NB>
+__global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
+    const __grid_constant__ CUtensorMap w2_map, const uint16_t* __restrict__ W2p,
+    const uint16_t* __restrict__ W1, const int32_t* __restrict__ prev, int prev_stride, int B,
+    int V, int r, int kc, int n_tiles, float* __restrict__ out, int* err) {
+  using S = BiasSmem;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t w_full[kBiasStages], w_empty[kBiasStages];
+  __shared__ uint64_t e_full[2], e_empty[2];
+  __shared__ uint64_t acc_full[kBiasDepth], acc_empty[kBiasDepth];
+  __shared__ uint64_t mma_drain;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sA = smem;                          // two 64-row blocks of r x 128 bytes
-  uint8_t* sB = sA + 2 * (size_t)r * 128;      // ceil(r/64) K-blocks of NB x 128 bytes
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int t_lo = (int)((long long)cta * n_tiles / G);
+  const int t_hi = (int)((long long)(cta + 1) * n_tiles / G);
+  const int my_tiles = t_hi - t_lo;
+  const int n_kchunks = r / kc;
+  const int n_jobs = (B + NB - 1) / NB;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < (uint32_t)(kBiasDepth * NB)) tmem_cols <<= 1;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int v0 = blockIdx.x * kGemmTileV;
-  const int b0 = blockIdx.y * NB;
-
-  if (tid == 0) {
-    prefetch_tensormap(&w2_map);
-    mbar_init(&bar_tma, 1);
-    mbar_init(&bar_mma, 1);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kBiasStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&e_full[i], 1); mbar_init(&e_empty[i], 1); }
+    for (int i = 0; i < kBiasDepth; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+    mbar_init(&mma_drain, 1);
+    abort_s = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(&tmem_base_s, tmem_cols);
     tmem_relinquish();
   }
@@ -55,80 +90,185 @@ __global__ void __launch_bounds__(128) bias_gemm_kernel(const __grid_constant__ 
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_base_s;
 
-  if (tid == 0) {
-    const uint64_t pol = policy_evict_last();
-    mbar_arrive_expect_tx(&bar_tma, 2u * (uint32_t)r * 128u);
-    tma_load_2d(sA, &w2_map, &bar_tma, v0, 0, pol);
-    tma_load_2d(sA + (size_t)r * 128, &w2_map, &bar_tma, v0 + 64, 0, pol);
-  }
-  // the W2 tile is an input; the request tokens (prev) may come from the previous kernel
-  pdl_wait();
-  pdl_launch_dependents();
-
-  // Gather E = W1[prev_b] (rows b0 .. b0+NB-1) as the K-major B operand: row n is 128-byte
-  // lines of 64 bf16 per K-block, 16-byte chunk c of row n stored at chunk c ^ (n % 8).
-  const int kchunks = r >> 3;  // 16-byte chunks per W1 row
-  for (int idx = tid; idx < NB * kchunks; idx += blockDim.x) {
-    const int n = idx / kchunks, c = idx - n * kchunks;
-    const int b = b0 + n;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (b < B) {
-      const int p = prev[(size_t)b * prev_stride];
-      if (p >= 0 && p < V) {
-        val = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)p * r) + c);
-      } else if (p != -1) {
-        set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
+  // bounded wait; a timeout records the error and aborts the CTA
+  auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const long long t0 = sm_cycles();
+    for (;;) {
+      if (*(volatile int*)&abort_s) return false;
+      if (mbar_try_wait_sleep(bar, parity)) return true;
+      if (sm_cycles() - t0 > kWaitCycles) {
+        set_device_error(err, DSPARK_ERR_TIMEOUT);
+        atomicExch(&abort_s, 1);
+        return false;
       }
     }
-    const int kb = c >> 3, cc = c & 7;
-    *reinterpret_cast<uint4*>(sB + (size_t)kb * NB * 128 + (size_t)n * 128 + ((cc ^ (n & 7)) << 4)) =
-        val;
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
+  };
 
-  if (tid == 0) {
-    if (mbar_wait(&bar_tma, 0)) {
-      tc_fence_after_sync();
-      const uint32_t idesc = idesc_bf16_f32(128, NB, /*A MN-major*/ 1, /*B K-major*/ 0);
-      const uint32_t a0 = smem_u32(sA), b0s = smem_u32(sB);
-      for (int kk = 0; kk < (r >> 4); ++kk) {
-        // A: 16 K-rows = two 8-row groups (SBO = 1024 B); the second 64-row block at LBO
-        const uint64_t ad = smem_desc(a0 + (uint32_t)kk * 2048u, (uint32_t)r * 128u, 1024u,
-                                      kSwizzle128B);
-        // B: K-block kk/4, 32-byte step inside the 128-byte swizzle atom; 8-row groups 1 KB
-        const uint64_t bd = smem_desc(b0s + (uint32_t)(kk >> 2) * (uint32_t)NB * 128u +
-                                          (uint32_t)(kk & 3) * 32u,
-                                      16u, 1024u, kSwizzle128B);
-        umma_bf16_f32(tmem_base, ad, bd, idesc, kk > 0 ? 1u : 0u);
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      if (!W2p) prefetch_tensormap(&w2_map);
+      const uint64_t keep = policy_evict_last();
+      const uint32_t w_bytes = 2u * (uint32_t)kc * 128u;
+      uint32_t ws = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        for (int t = t_lo; t < t_hi && ok; ++t) {
+          for (int i = 0; i < n_kchunks; ++i, ++ws) {
+            const int s = ws % kBiasStages;
+            if (!(ok = wait1(&w_empty[s], ((ws / kBiasStages) & 1) ^ 1))) break;
+            uint8_t* dst = smem + S::kOffW + s * S::kStageBytes;
+            mbar_arrive_expect_tx(&w_full[s], w_bytes);
+            if (W2p) {
+              // packed: the stage image is contiguous, one 1-D bulk copy
+              const uint16_t* src = W2p + ((size_t)t * n_kchunks + i) * (size_t)kc * 128;
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                  " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+                  "l"(reinterpret_cast<uint64_t>(src)), "r"(w_bytes), "r"(smem_u32(&w_full[s])),
+                  "l"(keep)
+                  : "memory");
+            } else {
+              tma_load_2d(dst, &w2_map, &w_full[s], t * kGemmTileV, i * kc, keep);
+              tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], t * kGemmTileV + 64, i * kc, keep);
+            }
+          }
+        }
       }
-    } else {
-      set_device_error(err, DSPARK_ERR_TIMEOUT);
+      // drain: every issued copy has landed before the CTA may exit
+      for (uint32_t i = ws > (uint32_t)kBiasStages ? ws - kBiasStages : 0; i < ws; ++i)
+        mbar_wait(&w_full[i % kBiasStages], (i / kBiasStages) & 1, 2000000000ull);
     }
-    umma_commit(&bar_mma);
-  }
-
-  // Epilogue: warp w reads TMEM lanes 32w..32w+31 (vocabulary rows v0 + 32w + lane).
-  const bool ok = mbar_wait(&bar_mma, 0);
-  if (!ok && lane == 0) set_device_error(err, DSPARK_ERR_TIMEOUT);
-  tc_fence_after_sync();
-  const int v = v0 + warp * 32 + lane;
-  const uint32_t trow = tmem_base + ((uint32_t)(warp * 32) << 16);
-  for (int c0 = 0; c0 < NB; c0 += 16) {
-    float vals[16];
-    tmem_ld_32x32b_x16(trow + (uint32_t)c0, vals);
-    tmem_ld_wait();
-    if (ok && v < V) {
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------------------- MMA issuer
+    auto issue_loop = [&](auto ksteps_c) {
+      constexpr int KS = decltype(ksteps_c)::value;
+      const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
+      const uint64_t a_base = smem_desc(smem_u32(smem + S::kOffW), (uint32_t)KS * 2048u, 1024u,
+                                        kSwizzle128B);
+      uint32_t ws = 0, tc = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int eb = job & 1;
+        if (!(ok = wait1(&e_full[eb], (job >> 1) & 1))) break;
+        const uint64_t b_base =
+            smem_desc(smem_u32(smem + S::kOffE + eb * S::kEBytes), 16u, 1024u, kSwizzle128B);
+        for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
+          const int ab = tc % kBiasDepth;
+          if (!(ok = wait1(&acc_empty[ab], ((tc / kBiasDepth) & 1) ^ 1))) break;
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
+          for (int i = 0; i < n_kchunks; ++i, ++ws) {
+            const int s = ws % kBiasStages;
+            if (!(ok = wait1(&w_full[s], (ws / kBiasStages) & 1))) break;
+            const uint64_t a_s = a_base + (uint64_t)((s * S::kStageBytes) >> 4);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int b = b0 + c0 + j;
-        if (b < B) out[(size_t)b * V + v] = vals[j];
+            for (int kk = 0; kk < KS; ++kk) {
+              const uint32_t kg = (uint32_t)(i * KS + kk);
+              const uint64_t ad = a_s + (uint64_t)(kk * (2048 >> 4));
+              const uint64_t bd = b_base + (uint64_t)((kg >> 2) * (uint32_t)(NB * 128 / 16) + (kg & 3) * 2u);
+              umma_bf16_f32(d_tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&w_empty[s]);
+          }
+          if (!ok) break;
+          umma_commit(&acc_full[ab]);
+        }
+        if (ok) umma_commit(&e_empty[eb]);
+      }
+    };
+    if (lane == 0) {
+      if (kc == 64) issue_loop(std::integral_constant<int, 4>{});
+      else if (kc == 32) issue_loop(std::integral_constant<int, 2>{});
+      else issue_loop(std::integral_constant<int, 1>{});
+      umma_commit(&mma_drain);
+      mbar_wait(&mma_drain, 0, 2000000000ull);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------- epilogue: E gather, TMEM -> bias rows
+    pdl_wait();                 // prev may come from the previous kernel
+    pdl_launch_dependents();
+    const int et = threadIdx.x - 64;              // 0 .. 127
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+    const int kchunks = r >> 3;                   // 16-byte chunks per W1 row
+    uint32_t tc = 0;
+    for (int job = 0; job < n_jobs; ++job) {
+      const int b0 = job * NB;
+      const int eb = job & 1;
+      // E = W1[prev_b] as the K-major, 128-byte-swizzled B operand: 16-byte chunk c of row n
+      // goes to chunk (c % 8) ^ (n % 8) of line n of K-block c / 8
+      if (et == 0) wait1(&e_empty[eb], ((job >> 1) & 1) ^ 1);
+      named_bar_sync_n(kBiasNamedBar, 128);
+      uint8_t* sE = smem + S::kOffE + eb * S::kEBytes;
+      if (!*(volatile int*)&abort_s) {
+        for (int idx = et; idx < NB * kchunks; idx += 128) {
+          const int n = idx / kchunks, c = idx - n * kchunks;
+          const int b = b0 + n;
+          uint4 val = make_uint4(0u, 0u, 0u, 0u);
+          if (b < B) {
+            const int pv = prev[(size_t)b * prev_stride];
+            if (pv >= 0 && pv < V) {
+              val = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)pv * r) + c);
+            } else if (pv != -1) {
+              set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
+            }
+          }
+          *reinterpret_cast<uint4*>(sE + (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 +
+                                    (((c & 7) ^ (n & 7)) << 4)) = val;
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync_n(kBiasNamedBar, 128);
+      if (et == 0) mbar_arrive(&e_full[eb]);
+      for (int t = 0; t < my_tiles; ++t, ++tc) {
+        const int ab = tc % kBiasDepth;
+        const bool ok = wait1(&acc_full[ab], (tc / kBiasDepth) & 1);
+        if (!__all_sync(0xffffffffu, ok)) continue;
+        tc_fence_after_sync();
+        float vals[NB];
+#pragma unroll
+        for (int c16 = 0; c16 < NB; c16 += 16)
+          tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16),
+                             *reinterpret_cast<float(*)[16]>(vals + c16));
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        const int v = (t_lo + t) * kGemmTileV + q * 32 + lane;
+        if (v < V) {
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            if (b0 + j < B) out[(size_t)(b0 + j) * V + v] = vals[j];
+        }
       }
     }
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem_base, tmem_cols);
+  if (warp == 1) tmem_dealloc(tmem_base, tmem_cols);
+}
+
+template <int NB>
+int bias_grid(int n_tiles) {
+  static int per_sm = -1, sms = 0;
+  if (per_sm < 0) {
+    int dev = 0, per = 0;
+    const size_t smem = BiasSmem::kBytes + 1024;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(bias_gemm_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_gemm_kernel<NB>, kBiasThreads,
+                                                      smem) != cudaSuccess)
+      return 0;
+    per_sm = per;
+  }
+  const int g = sms * per_sm;
+  return g < n_tiles ? g : n_tiles;
 }
 
 }  // namespace
@@ -161,23 +301,25 @@ bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_r
   return res == CUDA_SUCCESS;
 }
 
-cudaError_t launch_bias_gemm(const CUtensorMap* w2_map, const uint16_t* W1, const int32_t* prev,
-                             int prev_stride, int B, int V, int r, float* out, int* err,
-                             cudaStream_t stream) {
-  const int NB = gemm_chunk(B);
-  uint32_t cols = 32;
-  while ((int)cols < NB) cols <<= 1;
-  const size_t smem = gemm_smem_bytes(r, NB);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bias_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+cudaError_t launch_bias_gemm(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
+                             const int32_t* prev, int prev_stride, int B, int V, int r, float* out,
+                             int* err, cudaStream_t stream) {
+  const int kc = draft_kchunk(r);
+  CUtensorMap w2_map;
+  memset(&w2_map, 0, sizeof(w2_map));
+  if (!W2p && !encode_w2_map(&w2_map, W2, V, r, kc)) return cudaErrorInvalidValue;
+  const int n_tiles = cdiv(V, kGemmTileV);
+  const size_t smem = BiasSmem::kBytes + 1024;
+  if (B <= 16) {
+    const int grid = bias_grid<16>(n_tiles);
+    if (grid <= 0) return cudaErrorInvalidConfiguration;
+    return launch_pdl(bias_gemm_kernel<16>, dim3(grid), dim3(kBiasThreads), smem, stream, w2_map,
+                      W2p, W1, prev, prev_stride, B, V, r, kc, n_tiles, out, err);
   }
-  dim3 grid(cdiv(V, kGemmTileV), cdiv(B, NB));
-  return launch_pdl(bias_gemm_kernel, grid, dim3(128), smem, stream, *w2_map, W1, prev, prev_stride,
-                    B, V, r, NB, cols, out, err);
+  const int grid = bias_grid<32>(n_tiles);
+  if (grid <= 0) return cudaErrorInvalidConfiguration;
+  return launch_pdl(bias_gemm_kernel<32>, dim3(grid), dim3(kBiasThreads), smem, stream, w2_map,
+                    W2p, W1, prev, prev_stride, B, V, r, kc, n_tiles, out, err);
 }
 
 }  // namespace dspark

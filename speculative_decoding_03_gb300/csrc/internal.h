@@ -51,15 +51,6 @@ inline RowSplit fixed_split(int V, int seg) {
   return s;
 }
 
-// Width of one batch chunk of the bias contraction (MMA N): a multiple of 16, <= 256.
-inline int gemm_chunk(int B) {
-  int nb = (int)align_up((size_t)B, 16);
-  return nb > 256 ? 256 : nb;
-}
-inline size_t gemm_smem_bytes(int r, int NB) {
-  return 1024 + 2 * (size_t)r * 128 + (size_t)cdiv(r, 64) * NB * 128;
-}
-
 size_t draft_region_bytes(int B, int gamma);
 
 struct Plan {
@@ -127,9 +118,10 @@ bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_r
 
 // ---- launchers (return cudaError_t of the launch) ----
 // bias[b][v] = sum_i W1[prev_b][i] * W2[i][v] for b < B, v < V (rows with prev_b == -1 are 0)
-cudaError_t launch_bias_gemm(const CUtensorMap* w2_map, const uint16_t* W1, const int32_t* prev,
-                             int prev_stride, int B, int V, int r, float* out, int* err,
-                             cudaStream_t stream);
+// (W2p: the packed tile images of pack.cu in place of W2, or null)
+cudaError_t launch_bias_gemm(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
+                             const int32_t* prev, int prev_stride, int B, int V, int r, float* out,
+                             int* err, cudaStream_t stream);
 
 // the whole draft (all gamma positions) in one cooperative launch; `region` holds
 // draft_region_bytes(B, gamma) of workspace
@@ -156,7 +148,7 @@ cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps, 
                             int32_t* B_total, double* theta, int* err, cudaStream_t stream);
 
 cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
-                          const CUtensorMap* w2_map, const int32_t* anchor,
+                          const uint16_t* W2, const uint16_t* W2p, const int32_t* anchor,
                           const int32_t* tokens, const float* q_tok, const float* row_max,
                           const float* row_sumexp, const int32_t* ell, uint64_t seed,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* n_out, void* ws,

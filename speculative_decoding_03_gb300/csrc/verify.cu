@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kSampleThreads) fallback_kernel(
 }  // namespace
 
 cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
-                          const CUtensorMap* w2_map, const int32_t* anchor,
+                          const uint16_t* W2, const uint16_t* W2p, const int32_t* anchor,
                           const int32_t* tokens, const float* q_tok, const float* row_max,
                           const float* row_sumexp, const int32_t* ell, uint64_t seed,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* n_out, void* ws,
@@ -432,7 +432,7 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
                  (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, M_t, lnS_t,
                  p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, cnt_fb, err);
   if (e != cudaSuccess) return e;
-  if ((e = launch_bias_gemm(w2_map, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
+  if ((e = launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
     return e;
   e = launch_pdl(final_sample_kernel, dim3(p.ver.splits, B), dim3(kSampleThreads), 0, stream, T, U,
                  (const float*)bias, row_max, row_sumexp, (const float*)M_t, (const float*)lnS_t,

@@ -271,6 +271,29 @@ def test_draft_packed_matches_draft(name):
     assert ws.status() == 0
 
 
+@pytest.mark.parametrize("name", list(CASES))
+def test_verify_packed_matches_verify(name):
+    """The packed-weights verification feeds the same operands to the same contraction:
+    identical outputs."""
+    _need_gpu()
+    w = CASES[name]
+    inp = workloads.generate(w)
+    dev = _dev(inp)
+    ws = _ws(w)
+    W2p = ds.pack_w2(dev["W2"])
+    d = ds.draft(dev["U"], dev["W1"], dev["W2"], dev["anchor"], w.seed, ws)
+    rng = np.random.default_rng(w.seed + 200)
+    ell = torch.from_numpy(rng.integers(0, w.gamma + 1, size=w.B).astype(np.int32)).cuda()
+    args = (d["tokens"], d["q_tok"], d["row_max"], d["row_sumexp"], ell, w.seed, ws)
+    a = {k: v.cpu().numpy() for k, v in ds.verify(dev["T"], dev["U"], dev["W1"], dev["W2"],
+                                                   dev["anchor"], *args).items()}
+    b = {k: v.cpu().numpy() for k, v in ds.verify_packed(dev["T"], dev["U"], dev["W1"], W2p,
+                                                          dev["anchor"], *args).items()}
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    assert ws.status() == 0
+
+
 def test_pack_layout_matches_its_definition():
     """dspark_pack_w2 against the layout the header states, rebuilt with numpy."""
     _need_gpu()
