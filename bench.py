@@ -271,8 +271,9 @@ def run_ours(args, w):
         evs[2].record(stream)
         ds.schedule(c_out[1], x["sps"], step.ws, s_out)
         evs[3].record(stream)
-        ds.verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d_out["tokens"], d_out["q_tok"],
-                  d_out["row_max"], d_out["row_sumexp"], s_out[0], sd, step.ws, v_out)
+        ds.verify_packed(x["T"], x["U"], x["W1"], step.W2p, x["anchor"], d_out["tokens"],
+                         d_out["q_tok"], d_out["row_max"], d_out["row_sumexp"], s_out[0], sd,
+                         step.ws, v_out)
         evs[4].record(stream)
         torch.cuda.synchronize()
         for j in range(4):
