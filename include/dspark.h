@@ -217,7 +217,7 @@ dspark_status dspark_verify_packed(const float* T, const float* U, const uint16_
  * that is handed only its input and output buffers, code where a cudaMalloc would
  * synchronise or fail).  The paper has no counterpart: this is a packaging of the same
  * kernel.  Same arguments, outputs and results as dspark_draft, without the workspace:
- * the kernel's scratch lives in a fixed array inside the library, about 1.7 MB, which
+ * the kernel's scratch lives in a fixed array inside the library, about 2.5 MB, which
  * every GPU that loads the library holds until the process exits.
  *   - Limits: B <= 256 and gamma <= 32 (otherwise DSPARK_ERR_UNSUPPORTED), plus the
  *     shape limits above.

@@ -31,7 +31,8 @@
 // score, index, logit) and folds its best (score, index) into a 64-bit atomicMax key;
 // one grid barrier per position (bounded spin) makes every x_k known to every CTA, which
 // then gathers W1[x_k] for the next position.  The CTA with index b mod G merges the
-// partials of request b into x_k, q_k(x_k), max and sum.
+// partials of request b into x_k, q_k(x_k), max and sum, while it waits at the next
+// barrier.
 //
 // Failure handling: every wait is bounded (2 s).  A wait that runs out records
 // DSPARK_ERR_TIMEOUT and sets a CTA-wide abort flag; from then on the sampler threads
@@ -85,7 +86,7 @@ struct DraftParams {
   int B, gamma, V, r;
   int n_tiles, n_chunks, kc;       // kc = K rows per W2 stage (<= 64)
   uint64_t seed;
-  RowState* partials;              // [2][B][G]
+  RowState* partials;              // [3][B][G], position k in slot k % 3
   unsigned long long* keys;        // [gamma][B], zeroed before launch
   unsigned int* grid_count;        // zeroed before launch
   int32_t* tokens;
@@ -176,7 +177,7 @@ __device__ __forceinline__ void gather_E(uint8_t* sE, const DraftParams& p, int 
 // Merge the G partials of request b at position kp into x, q, max and sum (one warp).
 __device__ __forceinline__ void finalize_row(const DraftParams& p, int b, int kp, int G, int lane) {
   const int x = token_of_key(__ldcg(p.keys + (size_t)(kp - 1) * p.B + b));
-  const RowState* base = p.partials + ((size_t)(kp & 1) * p.B + b) * G;
+  const RowState* base = p.partials + ((size_t)(kp % 3) * p.B + b) * G;
   float m = -INFINITY, zx = -INFINITY;
   for (int g = lane; g < G; g += 32) m = fmaxf(m, __ldcg(&base[g].m));
   m = warp_max(m);
@@ -461,9 +462,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       if (c == 0) {
         if (k > 1) grid_wait((unsigned int)G * (unsigned int)(k - 1));
         publish_E(job, 0, k);
-        // merge this CTA's share of position k-1 (off the critical path of the MMA)
-        if (k > 1 && !*(volatile int*)&abort_s)
-          for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row(p, b, k - 1, G, lane);
       }
       // the next chunk of the same position only needs x_{k-1}: publish it now
       if (c + 1 < p.n_chunks) publish_E(job + 1, c + 1, k);
@@ -583,8 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         }
       }
       // publish this CTA's partials of the job's requests: the warp reductions of all its
-      // rows first, then the stores and atomics, then one fence for all of them (a fence
-      // waits for the atomics' round trips, so one per row would serialise them)
+      // rows first, then the stores and atomics.  No fence here: the thread that counts
+      // the CTA into the grid barrier fences after the samplers' named barrier, which
+      // orders every sampler's stores and atomics before its release.
       float pm[RPW], pst[RPW];
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
@@ -602,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
           ps.idx = bi[i];
           ps.z = bz[i];
           ps.score = bsc[i];
-          p.partials[((size_t)(k & 1) * p.B + b) * G + cta] = ps;
+          p.partials[((size_t)(k % 3) * p.B + b) * G + cta] = ps;
           if (bi[i] >= 0) {
             atomicMax(p.keys + (size_t)(k - 1) * p.B + b, argmax_key(bsc[i], bi[i]));
             // the winner is one CTA's local best: warm L2 with its W1 row for the gather
@@ -614,7 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
                            : "memory");
           }
         }
-        __threadfence();
       }
       if (c + 1 == p.n_chunks) {
         // this CTA is done with position k: count it in the grid barrier
@@ -623,6 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
           __threadfence();
           atomicAdd(p.grid_count, 1u);
         }
+        // merge this CTA's share of position k-1 while the other CTAs finish position k
+        // (partials rotate over three slots: slot (k-1) % 3 is next written at position
+        // k+2, after the barrier this CTA has not yet passed)
+        if (k > 1 && !*(volatile int*)&abort_s)
+          for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row(p, b, k - 1, G, lane);
       }
     }
     // the last position: wait for every CTA, then merge this CTA's rows
@@ -688,7 +691,7 @@ cudaError_t launch_fused(const CUtensorMap& w2_map, const CUtensorMap& u_map, co
 }  // namespace
 
 size_t draft_region_bytes(int B, int gamma) {
-  return align_up((size_t)2 * B * kDraftMaxCtas * sizeof(RowState), 256) + 256 +
+  return align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256) + 256 +
          align_up((size_t)gamma * B * sizeof(unsigned long long), 256);
 }
 
@@ -715,7 +718,7 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
   p.n_chunks = cdiv(B, NB);
   p.kc = draft_kchunk(r);   // divides r (r % 16 == 0)
   p.seed = seed;
-  const size_t part_bytes = align_up((size_t)2 * B * kDraftMaxCtas * sizeof(RowState), 256);
+  const size_t part_bytes = align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256);
   char* base = static_cast<char*>(region);
   p.partials = reinterpret_cast<RowState*>(base);
   p.grid_count = reinterpret_cast<unsigned int*>(base + part_bytes);

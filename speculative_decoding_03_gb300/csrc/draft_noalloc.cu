@@ -7,7 +7,7 @@
 // (per-CTA partial results, the grid-barrier counter and the argmax keys) lives in a
 // fixed array inside this library instead of a workspace.
 //
-// The array is a file-scope __device__ object of kNoAllocScratchBytes (about 1.7 MB); the
+// The array is a file-scope __device__ object of kNoAllocScratchBytes (about 2.5 MB); the
 // CUDA runtime creates it on every GPU that loads the library and keeps it until the
 // process exits.  It serves batches of at most kNoAllocMaxB requests and kNoAllocMaxGamma
 // positions.  Host code cannot use the array's name as a device address, so the first
@@ -31,7 +31,7 @@ constexpr int kNoAllocMaxB = 256;
 constexpr int kNoAllocMaxGamma = 32;
 // status word (256 B) + the draft region for the largest batch served
 constexpr size_t kNoAllocScratchBytes =
-    256 + ((2ull * kNoAllocMaxB * kDraftMaxCtas * sizeof(RowState) + 255) / 256) * 256 + 256 +
+    256 + ((3ull * kNoAllocMaxB * kDraftMaxCtas * sizeof(RowState) + 255) / 256) * 256 + 256 +
     ((8ull * kNoAllocMaxB * kNoAllocMaxGamma + 255) / 256) * 256;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
