@@ -22,7 +22,8 @@
  *   - bf16 weights are passed as their uint16_t bit patterns.
  *   - Every call is asynchronous on `stream` and may be captured in a CUDA graph.
  *   - Requests b are 0-based, draft positions k are 1-based (k = 1..gamma).
- *   - Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by `seed` (low word,
+ *   - Random numbers: Philox4x32 with 7 rounds (Salmon et al., SC'11; 7 is the fewest
+ *     rounds that paper reports passing TestU01 BigCrush) keyed by `seed` (low word,
  *     high word); the 32-bit draw for vocabulary index v of (request b, position k,
  *     stream s) is word v % 4 of the block with counter (v / 4, k, b, s);
  *     U01(x) = ((x >> 9) + 1/2) * 2^-23.  Streams: 0 draft Gumbel, 1 acceptance uniform

@@ -42,8 +42,8 @@ def lib():
         L = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i32, u64, f32 = ctypes.c_int, ctypes.c_uint64, ctypes.c_float
-        L.dso_philox4x32_10.argtypes = [P, u64, P]
-        L.dso_philox4x32_10.restype = None
+        L.dso_philox4x32.argtypes = [P, u64, ctypes.c_int, P]
+        L.dso_philox4x32.restype = None
         L.dso_draw.argtypes = [u64, i32, i32, i32, i32]
         L.dso_draw.restype = ctypes.c_uint32
         L.dso_u01.argtypes = [ctypes.c_uint32]
@@ -89,10 +89,13 @@ def default_threads() -> int:
 
 # ------------------------------------------------------------------------ random numbers
 
-def philox4x32_10(counter: Sequence[int], seed: int) -> np.ndarray:
+PHILOX_ROUNDS = 7   # the generator every draw uses: Philox4x32-7
+
+
+def philox4x32(counter: Sequence[int], seed: int, rounds: int = PHILOX_ROUNDS) -> np.ndarray:
     ctr = _c(counter, np.uint32)
     out = np.zeros(4, dtype=np.uint32)
-    lib().dso_philox4x32_10(_p(ctr), ctypes.c_uint64(seed), _p(out))
+    lib().dso_philox4x32(_p(ctr), ctypes.c_uint64(seed), int(rounds), _p(out))
     return out
 
 

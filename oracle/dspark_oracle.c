@@ -26,8 +26,10 @@
  *               p - q))).
  *
  * Readings where the pages are silent (the same list is kept with the design notes):
- *   - Random numbers: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
- *     Numbers: As Easy as 1, 2, 3", SC'11), key = (seed low 32 bits, seed high 32 bits),
+ *   - Random numbers: Philox4x32 with 7 rounds (Salmon, Moraes, Dror, Shaw, "Parallel
+ *     Random Numbers: As Easy as 1, 2, 3", SC'11: the Philox4x32 round function; 7 is the
+ *     fewest rounds that paper reports passing TestU01 BigCrush, its default being 10),
+ *     key = (seed low 32 bits, seed high 32 bits),
  *     counter = (floor(v/4), k, b, stream), the draw is output word v mod 4.  Positions k
  *     are 1-based, requests b 0-based.  Streams: 0 draft Gumbel, 1 verify uniform (v = 0),
  *     2 residual Gumbel, 3 bonus Gumbel.
@@ -56,19 +58,20 @@
 #define DSO_OK 0
 #define DSO_ERR_ARG 1
 #define DSO_ERR_NOMEM 2
+#define DSO_PHILOX_ROUNDS 7   /* rounds of the generator every draw uses */
 
 /* ------------------------------------------------------------------------------------ */
 /* Counter-based random numbers                                                          */
 /* ------------------------------------------------------------------------------------ */
 
-/* Philox4x32 with 10 rounds: each round multiplies counter words 0 and 2 by the two
+/* Philox4x32 with R rounds: each round multiplies counter words 0 and 2 by the two
  * round constants, swaps and mixes the high halves with the other counter words and the
  * key; the key is advanced by the two Weyl constants between rounds. */
-void dso_philox4x32_10(const uint32_t ctr[4], uint64_t seed, uint32_t out[4])
+void dso_philox4x32(const uint32_t ctr[4], uint64_t seed, int rounds, uint32_t out[4])
 {
     uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
     uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFu), k1 = (uint32_t)(seed >> 32);
-    for (int round = 0; round < 10; ++round) {
+    for (int round = 0; round < rounds; ++round) {
         uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
         uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
         uint32_t n0 = (uint32_t)(prod1 >> 32) ^ c1 ^ k0;
@@ -87,7 +90,7 @@ uint32_t dso_draw(uint64_t seed, int b, int k, int v, int stream)
 {
     uint32_t ctr[4] = {(uint32_t)v / 4u, (uint32_t)k, (uint32_t)b, (uint32_t)stream};
     uint32_t out[4];
-    dso_philox4x32_10(ctr, seed, out);
+    dso_philox4x32(ctr, seed, DSO_PHILOX_ROUNDS, out);
     return out[(uint32_t)v % 4u];
 }
 

@@ -18,16 +18,19 @@ __device__ __forceinline__ void set_device_error(int* err, int code) {
 }
 
 // ----------------------------------------------------------------------------------------
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2,
-// 3", SC'11): ten rounds of two 32x32->64 multiplies with the round constants, the high
-// halves mixed into the other counter words and the key; the key advances by the two Weyl
-// constants between rounds.  Key = (seed low word, seed high word).  The draw for
+// Philox4x32 with kPhiloxRounds = 7 rounds (Salmon, Moraes, Dror, Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3", SC'11: the Philox4x32 round function; 7 is the fewest rounds
+// that paper reports passing TestU01 BigCrush, its default being 10): per round two
+// 32x32->64 multiplies with the round constants, the high halves mixed into the other
+// counter words and the key; the key advances by the two Weyl constants between rounds.
+// Key = (seed low word, seed high word).  The draw for
 // vocabulary index v of (request b, position k, stream s) is word v % 4 of the block with
 // counter (v / 4, k, b, s): one 128-bit block feeds one 128-bit logit load.
 // ----------------------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+constexpr int kPhiloxRounds = 7;
+__device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
-  for (int round = 0; round < 10; ++round) {
+  for (int round = 0; round < kPhiloxRounds; ++round) {
     const uint32_t lo0 = 0xD2511F53u * c.x;
     const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
     const uint32_t lo1 = 0xCD9E8D57u * c.z;
@@ -41,7 +44,7 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 
 __device__ __forceinline__ uint4 draw_block(uint64_t seed, uint32_t v4, uint32_t k, uint32_t b,
                                             uint32_t stream) {
-  return philox4x32_10(make_uint4(v4, k, b, stream), (uint32_t)seed, (uint32_t)(seed >> 32));
+  return philox4x32(make_uint4(v4, k, b, stream), (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
 // U01(x) = ((x >> 9) + 1/2) 2^-23 and its exact complement 1 - U01(x); both are exact in

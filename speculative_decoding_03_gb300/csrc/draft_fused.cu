@@ -130,11 +130,11 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Philox4x32-10 with one 32x32->64 multiply per product (the definition of common.cuh:
+// Philox4x32 with one 32x32->64 multiply per product (the definition of common.cuh:
 // same rounds, constants and key schedule).
 __device__ __forceinline__ uint4 philox_wide(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
-  for (int round = 0; round < 10; ++round) {
+  for (int round = 0; round < kPhiloxRounds; ++round) {
     const unsigned long long p0 = (unsigned long long)0xD2511F53u * c.x;
     const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c.z;
     c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,

@@ -1,7 +1,8 @@
 """Pins of the oracle's random numbers.
 
-* Philox4x32-10 against an independent library implementation: Triton's Philox,
-  run by Triton's CPU interpreter in a child process.
+* Philox4x32 (the 7 rounds every draw uses, and the published default of 10) against an
+  independent library implementation: Triton's Philox, run by Triton's CPU interpreter in
+  a child process.
 * U01 and its exact complement against their closed forms.
 * The Gumbel transform against the Gumbel distribution's closed-form moments and CDF.
 """
@@ -25,13 +26,13 @@ _TRITON_PROBE = textwrap.dedent(
     from triton.language.random import philox
 
     @triton.jit
-    def k(out_ptr, c_ptr, seed, N: tl.constexpr):
+    def k(out_ptr, c_ptr, seed, N: tl.constexpr, R: tl.constexpr):
         i = tl.arange(0, N)
         c0 = tl.load(c_ptr + i * 4 + 0).to(tl.uint32, bitcast=True)
         c1 = tl.load(c_ptr + i * 4 + 1).to(tl.uint32, bitcast=True)
         c2 = tl.load(c_ptr + i * 4 + 2).to(tl.uint32, bitcast=True)
         c3 = tl.load(c_ptr + i * 4 + 3).to(tl.uint32, bitcast=True)
-        a, b, c, d = philox(seed, c0, c1, c2, c3, 10)
+        a, b, c, d = philox(seed, c0, c1, c2, c3, R)
         tl.store(out_ptr + i * 4 + 0, a.to(tl.int32, bitcast=True))
         tl.store(out_ptr + i * 4 + 1, b.to(tl.int32, bitcast=True))
         tl.store(out_ptr + i * 4 + 2, c.to(tl.int32, bitcast=True))
@@ -39,10 +40,10 @@ _TRITON_PROBE = textwrap.dedent(
 
     req = json.loads(sys.stdin.read())
     res = []
-    for seed, ctrs in req:
+    for seed, rounds, ctrs in req:
         c = torch.tensor(ctrs, dtype=torch.int64).to(torch.uint32).view(torch.int32).reshape(-1)
         out = torch.zeros(len(ctrs) * 4, dtype=torch.int32)
-        k[(1,)](out, c, seed, len(ctrs))
+        k[(1,)](out, c, seed, len(ctrs), rounds)
         res.append([x & 0xFFFFFFFF for x in out.tolist()])
     print(json.dumps(res))
     """
@@ -56,7 +57,8 @@ def test_philox_matches_triton_library():
     for seed in [0, 1, 0x0123456789ABCDEF, (1 << 64) - 1, int(rng.integers(0, 2**63))]:
         ctrs = [[0, 0, 0, 0], [0xFFFFFFFF] * 4, [1, 2, 3, 4], [37987, 7, 31, 2]]
         ctrs += rng.integers(0, 2**32, size=(4, 4), dtype=np.uint64).tolist()
-        cases.append([seed if seed < 2**63 else seed - 2**64, ctrs])
+        for rounds in (oracle.PHILOX_ROUNDS, 10):
+            cases.append([seed if seed < 2**63 else seed - 2**64, rounds, ctrs])
     env = dict(os.environ, TRITON_INTERPRET="1")
     try:
         proc = subprocess.run([sys.executable, "-c", _TRITON_PROBE], input=json.dumps(cases),
@@ -66,17 +68,17 @@ def test_philox_matches_triton_library():
     if proc.returncode != 0:
         pytest.skip("triton interpreter unavailable: " + proc.stderr.strip().splitlines()[-1])
     ref = json.loads(proc.stdout.strip().splitlines()[-1])
-    for (seed, ctrs), want in zip(cases, ref):
+    for (seed, rounds, ctrs), want in zip(cases, ref):
         for i, ctr in enumerate(ctrs):
-            got = oracle.philox4x32_10(ctr, seed & ((1 << 64) - 1)).tolist()
-            assert got == want[4 * i: 4 * i + 4], (seed, ctr)
+            got = oracle.philox4x32(ctr, seed & ((1 << 64) - 1), rounds).tolist()
+            assert got == want[4 * i: 4 * i + 4], (seed, rounds, ctr)
 
 
 def test_draw_layout_counter_and_word():
     # the draw for vocabulary index v is word v % 4 of the block floor(v / 4)
     seed = 12345
     for (b, k, v, s) in [(0, 1, 0, 0), (3, 2, 5, 0), (7, 4, 1023, 2), (1, 16, 151935, 3)]:
-        blk = oracle.philox4x32_10([v // 4, k, b, s], seed)
+        blk = oracle.philox4x32([v // 4, k, b, s], seed)
         assert oracle.draw(seed, b, k, v, s) == int(blk[v % 4])
 
 
