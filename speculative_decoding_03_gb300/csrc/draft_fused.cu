@@ -8,10 +8,10 @@
 // Layout of the work: the vocabulary is cut into 128-row tiles; each CTA (one per SM,
 // cooperative launch) owns a contiguous run of tiles for the whole call.  For every
 // position k and every chunk of NB requests ("job") the CTA:
-//   producer warp   streams the W2^T tiles (K-chunks of up to 64 rank rows, MN-major,
-//                   128-byte swizzle) and the U tiles [NB requests x 128 v] into shared-
-//                   memory rings with TMA; neither depends on the drafted tokens, so the
-//                   rings run ahead across positions while the CTA waits for x_k;
+//   producer warps  one streams the W2^T tiles (K-chunks of up to 64 rank rows, MN-major,
+//                   128-byte swizzle), another the U tiles [NB requests x 128 v], into
+//                   shared-memory rings with TMA; neither depends on the drafted tokens,
+//                   so the rings run ahead across positions while the CTA waits for x_k;
 //   MMA warp        issues tcgen05.mma (M = 128 vocabulary rows, N = NB requests, K = r)
 //                   into one of two tensor-memory accumulators;
 //   4 transposers   read the accumulator (lane = vocabulary row) and write the bias
@@ -51,11 +51,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kWarps = 22;
+constexpr int kWarps = 23;
 constexpr int kThreads = kWarps * 32;
-constexpr int kProducerWarp = 0;
+constexpr int kProducerWarp = 0;      // W2 stages
 constexpr int kMmaWarp = 1;
 constexpr int kFirstSampler = 6;      // warps 2..5 transpose, 6..21 sample
+constexpr int kUProducerWarp = 22;    // U tiles
 constexpr int kSamplers = 16;
 constexpr int kSamplerThreads = kSamplers * 32;
 constexpr int kWStages = 4;           // W2 K-chunk ring (16 KB each at K-chunk 64)
@@ -283,18 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   // (every lane waiting, then a warp vote and a __syncwarp per K-chunk) measured on GB300
   // twice as slow per tile as the single-lane issue loop.
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ TMA producer
+    // -------------------------------------------------------------- W2 stage producer
     if (lane == 0) {
       prefetch_tensormap(&w2_map);
-      prefetch_tensormap(&u_map);
       const uint64_t keep = policy_evict_last();
-      uint64_t stream_pol;
-      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
       const uint32_t w_bytes = 2u * (uint32_t)kc * 128u;
-      uint32_t ws = 0, us = 0;
+      uint32_t ws = 0;
       bool ok = true;
       for (int job = 0; job < n_jobs && ok; ++job) {
-        const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
         for (int t = t_lo; t < t_hi && ok; ++t) {
           const int v0 = t * kGemmTileV;
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
@@ -316,7 +313,27 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], v0 + 64, i * kc, keep);
             }
           }
-          if (!ok) break;
+        }
+      }
+      // drain: every issued copy has landed before the CTA may exit (a stage whose wait
+      // failed above was never issued, so only stages below ws are in flight)
+      for (uint32_t i = ws > (uint32_t)kWStages ? ws - kWStages : 0; i < ws; ++i)
+        mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, kTimeoutNs);
+    }
+    __syncwarp();
+  } else if (warp == kUProducerWarp) {
+    // ----------------------------------------------------------------- U tile producer
+    // U does not depend on the drafted tokens: its ring runs up to kUStages tiles ahead
+    // of the samplers, across positions, independently of the W2 ring.
+    if (lane == 0) {
+      prefetch_tensormap(&u_map);
+      uint64_t stream_pol;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
+      uint32_t us = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+        for (int t = t_lo; t < t_hi; ++t, ++us) {
           const int su = us % kUStages;
           if (!(ok = wait1(&u_empty[su], ((us / kUStages) & 1) ^ 1))) break;
           mbar_arrive_expect_tx(&u_full[su], (uint32_t)S::kUStageBytes);
@@ -324,16 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
               ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(
                   smem_u32(smem + S::kOffU + su * S::kUStageBytes)),
-              "l"(reinterpret_cast<uint64_t>(&u_map)), "r"(smem_u32(&u_full[su])), "r"(v0),
-              "r"(k - 1), "r"(c * NB), "l"(stream_pol)
+              "l"(reinterpret_cast<uint64_t>(&u_map)), "r"(smem_u32(&u_full[su])),
+              "r"(t * kGemmTileV), "r"(k - 1), "r"(c * NB), "l"(stream_pol)
               : "memory");
-          ++us;
         }
       }
-      // drain: every issued copy has landed before the CTA may exit (a stage whose wait
-      // failed above was never issued, so only stages below ws are in flight)
-      for (uint32_t i = ws > (uint32_t)kWStages ? ws - kWStages : 0; i < ws; ++i)
-        mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, kTimeoutNs);
       for (uint32_t i = us > (uint32_t)kUStages ? us - kUStages : 0; i < us; ++i)
         mbar_wait(&u_full[i % kUStages], (i / kUStages) & 1, kTimeoutNs);
     }
