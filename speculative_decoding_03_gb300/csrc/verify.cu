@@ -45,6 +45,48 @@ __device__ __forceinline__ RowState load_partial(const RowState* src) {
   return q;
 }
 
+// mbarrier and 1-D bulk copy (global -> shared, completing on an mbarrier)
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init_cta(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init_cta() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_cta() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx_cta(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+// bounded wait (about 2 s of SM cycles); false on timeout
+__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(10000000u)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > 4000000000ll) return false;
+  }
+}
+
 // 1/x on the special-function unit (PTX rcp.approx.ftz.f32, relative error below 2^-22)
 __device__ __forceinline__ float rcp_approx_ftz(float x) {
   float y;
@@ -219,47 +261,17 @@ __device__ __forceinline__ float block_max_f(float x, float* red) {
   return x;
 }
 
-__global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
-    const float* __restrict__ T, const float* __restrict__ U, const float* __restrict__ bias,
-    const float* __restrict__ row_max, const float* __restrict__ row_sumexp,
-    const float* __restrict__ M_t, const float* __restrict__ lnS_t,
-    const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
-    int gamma, int V, uint64_t seed, int splits, RowState* __restrict__ partials) {
-  __shared__ RowState red[32];
-  __shared__ float redf[kSampleThreads / 32];
-  pdl_wait();
-  pdl_launch_dependents();
-  const int b = blockIdx.y;
-  const int md = mode[b], k = pos[b];
-  if (md != kModeResidual && md != kModeBonus) return;
-  const bool residual = md == kModeResidual;
-  const int v0 = blockIdx.x * kVerSeg + 4 * threadIdx.x;
-  const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
-  float4 t[kVerVec], zz[kVerVec];
-#pragma unroll
-  for (int j = 0; j < kVerVec; ++j) {
-    const int v = v0 + j * 4 * kSampleThreads;
-    t[j] = v < V ? ld_stream_f4(Trow + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  }
-  float off_a = 0.f, off_b = 0.f;   // residual: log P = T - off_a, log Q = z - off_b
-  if (residual) {
-    const size_t o = (size_t)b * gamma + (k - 1);
-    const float* Urow = U + o * V;
-    const float* Brow = bias + (size_t)b * V;
-#pragma unroll
-    for (int j = 0; j < kVerVec; ++j) {
-      const int v = v0 + j * 4 * kSampleThreads;
-      if (v < V) {
-        const float4 u4 = ld_stream_f4(Urow + v);
-        const float4 b4 = __ldcg(reinterpret_cast<const float4*>(Brow + v));
-        zz[j] = make_float4(u4.x + b4.x, u4.y + b4.y, u4.z + b4.z, u4.w + b4.w);
-      } else {
-        zz[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    off_b = row_max[o] + logf(row_sumexp[o]);
-    off_a = M_t[o] + lnS_t[o];
-  } else {
+// One CTA scores one segment of kVerSeg logits of one row: t / zz hold this thread's
+// kVerVec float4 of T and of z = U + bias (residual rows only), v0 the first vocabulary
+// index of the thread's first float4.  Every thread of the CTA calls it; returns the CTA's
+// best (score, index) in every thread.
+__device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
+                                                 const float4 (&zz)[kVerVec], int v0, int V,
+                                                 bool residual, float off_a, float off_b,
+                                                 uint64_t seed, int k, int b, RowState* red,
+                                                 float* redf) {
+  if (!residual) {
+    // bonus: reference = the CTA's largest logit (exp(T - m) <= 1)
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kVerVec; ++j) m = fmaxf(m, fmaxf(fmaxf(t[j].x, t[j].y), fmaxf(t[j].z, t[j].w)));
@@ -333,8 +345,111 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
       }
     }
   }
-  st = row_state_block_reduce(st, red);
-  if (threadIdx.x == 0) partials[(size_t)b * splits + blockIdx.x] = st;
+  // the CTA's best (score, index): two shuffles per level, one word pair per warp
+  float sc = st.score;
+  int ix = st.idx;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float osc = __shfl_xor_sync(0xffffffffu, sc, o);
+    const int oix = __shfl_xor_sync(0xffffffffu, ix, o);
+    if (better(osc, oix, sc, ix)) { sc = osc; ix = oix; }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { red[warp].score = sc; red[warp].idx = ix; }
+  __syncthreads();
+  sc = red[0].score;
+  ix = red[0].idx;
+#pragma unroll
+  for (int wi = 1; wi < kSampleThreads / 32; ++wi)
+    if (better(red[wi].score, red[wi].idx, sc, ix)) { sc = red[wi].score; ix = red[wi].idx; }
+  __syncthreads();
+  RowState out = row_state_empty();
+  out.score = sc;
+  out.idx = ix;
+  return out;
+}
+
+// Persistent: CTA g scores the segments (b, seg) = items g, g + G, ... (item = b * splits +
+// seg).  Thread 0 brings the next item's rows into the other half of a double buffer with
+// 1-D bulk copies (T, and U and bias for residual rows) while the CTA scores the current
+// one, so HBM latency overlaps the scoring.
+__global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
+    const float* __restrict__ T, const float* __restrict__ U, const float* __restrict__ bias,
+    const float* __restrict__ row_max, const float* __restrict__ row_sumexp,
+    const float* __restrict__ M_t, const float* __restrict__ lnS_t,
+    const int32_t* __restrict__ mode, const int32_t* __restrict__ pos, int B, int gamma, int V,
+    uint64_t seed, int splits, RowState* __restrict__ partials, int* err) {
+  extern __shared__ float4 fs_buf[];            // [2][3][kVerSeg / 4]
+  __shared__ uint64_t full[2];
+  __shared__ RowState red[32];
+  __shared__ float redf[kSampleThreads / 32];
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init_cta(&full[0], 1);
+    mbar_init_cta(&full[1], 1);
+    fence_mbar_init_cta();
+  }
+  __syncthreads();
+  pdl_wait();                   // mode and pos come from the decision kernel
+  pdl_launch_dependents();
+  const int n_items = B * splits, G = gridDim.x;
+  constexpr int kSlot = kVerSeg / 4;            // float4 per array slot
+  auto issue = [&](int item, int buf) {         // thread 0
+    const int b = item / splits, seg = item - b * splits;
+    const int md = mode[b], k = pos[b];
+    const int v0 = seg * kVerSeg;
+    const uint32_t bytes = (uint32_t)(min(kVerSeg, V - v0)) * 4u;
+    float4* dst = fs_buf + (size_t)buf * 3 * kSlot;
+    fence_proxy_async_cta();    // the buffer's previous generic reads come first
+    if (md == kModeResidual) {
+      const size_t o = (size_t)b * gamma + (k - 1);
+      mbar_expect_tx_cta(&full[buf], 3u * bytes);
+      bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
+      bulk_g2s(dst + kSlot, U + o * V + v0, bytes, &full[buf]);
+      bulk_g2s(dst + 2 * kSlot, bias + (size_t)b * V + v0, bytes, &full[buf]);
+    } else if (md == kModeBonus) {
+      mbar_expect_tx_cta(&full[buf], bytes);
+      bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
+    } else {
+      mbar_arrive_cta(&full[buf]);
+    }
+  };
+  if (tid == 0 && blockIdx.x < n_items) issue(blockIdx.x, 0);
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; item += G, ++it) {
+    const int buf = it & 1;
+    if (tid == 0 && item + G < n_items) issue(item + G, buf ^ 1);
+    const bool ok = mbar_wait_cta(&full[buf], (uint32_t)(it >> 1) & 1u);
+    if (!ok && tid == 0) set_device_error(err, DSPARK_ERR_TIMEOUT);
+    const int b = item / splits, seg = item - b * splits;
+    const int md = mode[b], k = pos[b];
+    const bool residual = md == kModeResidual;
+    if ((md == kModeResidual || md == kModeBonus) && __syncthreads_and(ok)) {
+      const int v0 = seg * kVerSeg + 4 * tid;
+      const int n4 = (min(kVerSeg, V - seg * kVerSeg) + 3) / 4;
+      const float4* src = fs_buf + (size_t)buf * 3 * kSlot;
+      float4 t[kVerVec], zz[kVerVec];
+#pragma unroll
+      for (int j = 0; j < kVerVec; ++j) {
+        const int q = tid + j * kSampleThreads;
+        t[j] = q < n4 ? src[q] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        zz[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (residual && q < n4) {
+          const float4 u4 = src[kSlot + q], b4 = src[2 * kSlot + q];
+          zz[j] = make_float4(u4.x + b4.x, u4.y + b4.y, u4.z + b4.z, u4.w + b4.w);
+        }
+      }
+      float off_a = 0.f, off_b = 0.f;   // residual: log P = T - off_a, log Q = z - off_b
+      if (residual) {
+        const size_t o = (size_t)b * gamma + (k - 1);
+        off_b = row_max[o] + logf(row_sumexp[o]);
+        off_a = M_t[o] + lnS_t[o];
+      }
+      const RowState st = race_segment(t, zz, v0, V, residual, off_a, off_b, seed, k, b, red, redf);
+      if (tid == 0) partials[item] = st;
+    }
+    __syncthreads();            // every thread is done with this buffer before it is refilled
+  }
 }
 
 // One warp per request: the best (score, index) over the row's partials is the token.
@@ -403,6 +518,27 @@ __global__ void __launch_bounds__(kSampleThreads) fallback_kernel(
 
 }  // namespace
 
+namespace {
+constexpr size_t kFinalSmem = 2 * 3 * kVerSeg * sizeof(float);
+int final_sample_grid(int n_items) {
+  static int per_sm = -1, sms = 0;
+  if (per_sm < 0) {
+    int dev = 0, per = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(final_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFinalSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, final_sample_kernel, kSampleThreads,
+                                                      kFinalSmem) != cudaSuccess ||
+        per < 1)
+      return 1;
+    per_sm = per;
+  }
+  const int g = sms * per_sm;
+  return g < n_items ? g : n_items;
+}
+}  // namespace
+
 cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
                           const uint16_t* W2, const uint16_t* W2p, const int32_t* anchor,
                           const int32_t* tokens, const float* q_tok, const float* row_max,
@@ -434,9 +570,10 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   if (e != cudaSuccess) return e;
   if ((e = launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
     return e;
-  e = launch_pdl(final_sample_kernel, dim3(p.ver.splits, B), dim3(kSampleThreads), 0, stream, T, U,
-                 (const float*)bias, row_max, row_sumexp, (const float*)M_t, (const float*)lnS_t,
-                 (const int32_t*)mode, (const int32_t*)pos, gamma, V, seed, p.ver.splits, part_ver);
+  e = launch_pdl(final_sample_kernel, dim3(final_sample_grid(B * p.ver.splits)),
+                 dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias, row_max,
+                 row_sumexp, (const float*)M_t, (const float*)lnS_t, (const int32_t*)mode,
+                 (const int32_t*)pos, B, gamma, V, seed, p.ver.splits, part_ver, err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(finalize_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream,
                  (const RowState*)part_ver, p.ver.splits, B, gamma, (const int32_t*)mode,
