@@ -6,63 +6,69 @@
 // here followed by a sigmoid; the Markov embedding is the W1 row of the predecessor.
 // billytse.dev DSpark page, section 5: a_j = prod_{i<=j} c_i.
 //
-// One CTA per request, one warp per draft position: each lane accumulates its share of
-// the two dot products (batches of eight independent 128-bit loads of h and w_c in flight
-// per lane, one 16-byte load of the bf16 Markov row), the warp reduces, and thread 0
-// applies the sigmoid and multiplies the survival left to right.
+// One CTA per request, wpp warps per draft position (wpp = min(4, 32 / gamma)): each
+// warp accumulates its share of the h dot product with up to eight independent 128-bit
+// loads per lane in flight (h is an input, so the first of them are issued before the
+// kernel waits for the draft), the position's first warp adds the bf16 Markov row, and
+// thread 0 applies the sigmoid and multiplies the survival left to right.
 #include "internal.h"
 
 namespace dspark {
 namespace {
 
-__global__ void confidence_kernel(const float* __restrict__ h, const int32_t* __restrict__ anchor,
-                                  const int32_t* __restrict__ tokens,
-                                  const uint16_t* __restrict__ W1, const float* __restrict__ w_c,
-                                  float b_c, int gamma, int H, int r, int V,
-                                  float* __restrict__ c_out, float* __restrict__ a_out, int* err) {
-  __shared__ float logit[32];
+__global__ void __launch_bounds__(1024) confidence_kernel(
+    const float* __restrict__ h, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, const uint16_t* __restrict__ W1,
+    const float* __restrict__ w_c, float b_c, int gamma, int H, int r, int V, int wpp,
+    float* __restrict__ c_out, float* __restrict__ a_out, int* err) {
+  __shared__ float part_s[32];
+  constexpr int kBatch = 8;
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = warp / wpp, part = warp - k * wpp;    // 0-based position, share of H
+  const size_t o = (size_t)b * gamma + k;
+  const int H4 = H >> 2, stride = 32 * wpp;
+  const float4* hv = reinterpret_cast<const float4*>(h + o * H);
+  const float4* wv = reinterpret_cast<const float4*>(w_c);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  auto load_batch = [&](int base, float4 (&x)[kBatch]) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + stride * u;
+      x[u] = i < H4 ? __ldcs(hv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto use_batch = [&](int base, const float4 (&x)[kBatch]) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + stride * u;
+      if (i < H4) {
+        const float4 w = __ldg(wv + i);
+        acc[u & 3] = fmaf(x[u].x, w.x, acc[u & 3]);
+        acc[u & 3] = fmaf(x[u].y, w.y, acc[u & 3]);
+        acc[u & 3] = fmaf(x[u].z, w.z, acc[u & 3]);
+        acc[u & 3] = fmaf(x[u].w, w.w, acc[u & 3]);
+      }
+    }
+  };
+  // h does not depend on the previous kernel: the first batch is in flight while it drains
+  const int base0 = part * 32 + lane;
+  float4 x[kBatch];
+  load_batch(base0, x);
   pdl_wait();                 // the drafted tokens come from the previous kernel
   pdl_launch_dependents();
-  const int b = blockIdx.x;
-  const int k = threadIdx.x >> 5;  // 0-based position handled by this warp
-  const int lane = threadIdx.x & 31;
-  if (k < gamma) {
-    const size_t o = (size_t)b * gamma + k;
+  use_batch(base0, x);
+  for (int base = base0 + stride * kBatch; base < H4; base += stride * kBatch) {
+    load_batch(base, x);
+    use_batch(base, x);
+  }
+  if (part == 0) {
+    // the Markov row: 8 bf16 (16 bytes) per lane and step (r % 16 == 0)
     int prev = (k == 0) ? anchor[b] : tokens[o - 1];
-    bool ok = prev >= 0 && prev < V;
-    if (!ok) {
+    if (!(prev >= 0 && prev < V)) {
       if (lane == 0) set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
       prev = 0;
     }
-    constexpr int kBatch = 8;
-    float acc[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) acc[u] = 0.f;
-    const float4* hv = reinterpret_cast<const float4*>(h + o * H);
-    const float4* wv = reinterpret_cast<const float4*>(w_c);
-    const int H4 = H >> 2;
-    for (int i0 = lane; i0 < H4; i0 += 32 * kBatch) {
-      float4 x[kBatch], w[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int i = i0 + 32 * u;
-        if (i < H4) {
-          x[u] = __ldcs(hv + i);
-          w[u] = __ldg(wv + i);
-        } else {
-          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          w[u] = x[u];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        acc[u] = fmaf(x[u].x, w[u].x, acc[u]);
-        acc[u] = fmaf(x[u].y, w[u].y, acc[u]);
-        acc[u] = fmaf(x[u].z, w[u].z, acc[u]);
-        acc[u] = fmaf(x[u].w, w[u].w, acc[u]);
-      }
-    }
-    // the Markov row: 8 bf16 (16 bytes) per lane and step (r % 16 == 0)
     const uint16_t* e = W1 + (size_t)prev * r;
     for (int i = 8 * lane; i < r; i += 256) {
       const uint4 q = __ldg(reinterpret_cast<const uint4*>(e + i));
@@ -72,23 +78,23 @@ __global__ void confidence_kernel(const float* __restrict__ h, const int32_t* __
       acc[1] = fmaf(__uint_as_float(q.x & 0xFFFF0000u), w0.y, acc[1]);
       acc[2] = fmaf(__uint_as_float(q.y << 16), w0.z, acc[2]);
       acc[3] = fmaf(__uint_as_float(q.y & 0xFFFF0000u), w0.w, acc[3]);
-      acc[4] = fmaf(__uint_as_float(q.z << 16), w1.x, acc[4]);
-      acc[5] = fmaf(__uint_as_float(q.z & 0xFFFF0000u), w1.y, acc[5]);
-      acc[6] = fmaf(__uint_as_float(q.w << 16), w1.z, acc[6]);
-      acc[7] = fmaf(__uint_as_float(q.w & 0xFFFF0000u), w1.w, acc[7]);
+      acc[0] = fmaf(__uint_as_float(q.z << 16), w1.x, acc[0]);
+      acc[1] = fmaf(__uint_as_float(q.z & 0xFFFF0000u), w1.y, acc[1]);
+      acc[2] = fmaf(__uint_as_float(q.w << 16), w1.z, acc[2]);
+      acc[3] = fmaf(__uint_as_float(q.w & 0xFFFF0000u), w1.w, acc[3]);
     }
-    float accs = 0.f;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) accs += acc[u];
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) accs += __shfl_xor_sync(0xffffffffu, accs, m);
-    if (lane == 0) logit[k] = accs;
   }
+  float accs = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) accs += __shfl_xor_sync(0xffffffffu, accs, m);
+  if (lane == 0) part_s[warp] = accs;
   __syncthreads();
   if (threadIdx.x == 0) {
     float surv = 1.f;
     for (int j = 0; j < gamma; ++j) {
-      const float c = 1.f / (1.f + expf(-(logit[j] + b_c)));
+      float logit = 0.f;
+      for (int q = 0; q < wpp; ++q) logit += part_s[j * wpp + q];
+      const float c = 1.f / (1.f + expf(-(logit + b_c)));
       surv *= c;
       c_out[(size_t)b * gamma + j] = c;
       a_out[(size_t)b * gamma + j] = surv;
@@ -102,8 +108,11 @@ cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32
                               const uint16_t* W1, const float* w_c, float b_c, int B, int gamma,
                               int H, int r, int V, float* c, float* a, int* err,
                               cudaStream_t stream) {
-  return launch_pdl(confidence_kernel, dim3(B), dim3(32 * gamma), 0, stream, h, anchor, tokens, W1,
-                    w_c, b_c, gamma, H, r, V, c, a, err);
+  int wpp = 32 / gamma;
+  if (wpp > 4) wpp = 4;
+  if (wpp < 1) wpp = 1;
+  return launch_pdl(confidence_kernel, dim3(B), dim3(32 * wpp * gamma), 0, stream, h, anchor,
+                    tokens, W1, w_c, b_c, gamma, H, r, V, wpp, c, a, err);
 }
 
 }  // namespace dspark

@@ -66,14 +66,16 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     // one pass of broadcast shared-memory reads, no sorting network
     const unsigned long long mine = tid < N ? keys[tid] : ~0ull;
     int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-    int j = 0;
-    for (; j + 4 <= N; j += 4) {
-      r0 += keys[j] < mine ? 1 : 0;
-      r1 += keys[j + 1] < mine ? 1 : 0;
-      r2 += keys[j + 2] < mine ? 1 : 0;
-      r3 += keys[j + 3] < mine ? 1 : 0;
+    if (tid < N) {            // only the threads that own a key rank it
+      int j = 0;
+      for (; j + 4 <= N; j += 4) {
+        r0 += keys[j] < mine ? 1 : 0;
+        r1 += keys[j + 1] < mine ? 1 : 0;
+        r2 += keys[j + 2] < mine ? 1 : 0;
+        r3 += keys[j + 3] < mine ? 1 : 0;
+      }
+      for (; j < N; ++j) r0 += keys[j] < mine ? 1 : 0;
     }
-    for (; j < N; ++j) r0 += keys[j] < mine ? 1 : 0;
     const int rank = r0 + r1 + r2 + r3;
     __syncthreads();
     if (tid < N) keys[rank] = mine;

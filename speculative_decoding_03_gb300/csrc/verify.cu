@@ -196,15 +196,24 @@ __global__ void __launch_bounds__(128) decide_kernel(
   bool reject = false;
   if (k <= L) {
     const int row = b * gamma + (k - 1);
-    float m = -INFINITY, s = 0.f;
-    for (int i = 0; i < splits; ++i) {
-      const float2 q = __ldcg(stats + (size_t)row * splits + i);
-      max_sum_merge(m, s, q.x, q.y);
-    }
+    // the token, its target logit and the row partials are independent loads: issue them
+    // together (partials in batches of 16), then merge
     const int x = tokens[(size_t)b * gamma + (k - 1)];
+    const bool x_ok = x >= 0 && x < V;
+    const float tx = x_ok ? __ldg(T + ((size_t)b * (gamma + 1) + (k - 1)) * V + x) : 0.f;
+    float m = -INFINITY, s = 0.f;
+    for (int i0 = 0; i0 < splits; i0 += 16) {
+      float2 q[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        q[u] = i0 + u < splits ? __ldcg(stats + (size_t)row * splits + i0 + u)
+                               : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) max_sum_merge(m, s, q[u].x, q[u].y);
+    }
     float p = 0.f;
-    if (x >= 0 && x < V) {
-      p = expf(__ldg(T + ((size_t)b * (gamma + 1) + (k - 1)) * V + x) - m) / s;
+    if (x_ok) {
+      p = expf(tx - m) / s;
     } else {
       set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
     }
