@@ -57,7 +57,7 @@ struct Plan {
   int B, gamma, V, r, H;
   RowSplit stats, ver;
   // byte offsets into the workspace
-  size_t off_err, off_draft, off_bias, off_part, off_cnt, off_M, off_lnS, off_p, off_mode,
+  size_t off_err, off_draft, off_bias, off_part, off_M, off_lnS, off_p, off_mode,
       off_pos, off_prev, off_fallback, total;
 };
 
@@ -72,7 +72,6 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_bias = o; o = align_up(o + (size_t)B * V * sizeof(float), 256);
   const size_t parts = (size_t)B * gamma * p.stats.splits + (size_t)B * p.ver.splits;
   p.off_part = o; o = align_up(o + parts * sizeof(RowState), 256);
-  p.off_cnt = o; o = align_up(o + (size_t)B * sizeof(uint32_t), 256);
   p.off_M = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
   p.off_lnS = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
   p.off_p = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);

@@ -16,9 +16,9 @@
 //   bias_gemm      (shared with the draft) W1[x_{j-1}] W2 for the rows with a reject at j
 //   final_sample   Gumbel-max over log(P_j - Q_j) on {P_j > Q_j} (residual), or over
 //                  T[b, l+1] (bonus): one partial (best score, index) per segment
-//   finalize       one warp per request merges the partials and writes the token
-//   fallback       only for rows whose residual support came out empty in fp32: Gumbel-
-//                  max over T[b, j] with the residual's random stream
+//   finalize       one CTA per request merges the partials and writes the token; only
+//                  for a row whose residual support came out empty in fp32 it draws the
+//                  fallback: Gumbel-max over T[b, j] with the residual's random stream
 #include "internal.h"
 
 namespace dspark {
@@ -99,21 +99,6 @@ __device__ __forceinline__ float gumbel_of(uint32_t x) {
   return -logf(exp1_from_w(one_minus_u01(x)));
 }
 
-// Writes this CTA's partial and returns true in the CTA that completes the row.
-__device__ __forceinline__ bool publish_partial(RowState st, RowState* slot, uint32_t* counter,
-                                                int splits, int* is_last_s) {
-  if (threadIdx.x == 0) {
-    *slot = st;
-    __threadfence();
-    const uint32_t done = atomicAdd(counter, 1u);
-    *is_last_s = (done == (uint32_t)splits - 1);
-  }
-  __syncthreads();
-  const bool last = *is_last_s != 0;
-  if (last) __threadfence();
-  return last;
-}
-
 // (one warp; every lane gets the merged state)
 __device__ __forceinline__ RowState merge_partials(const RowState* base, int splits) {
   RowState acc = row_state_empty();
@@ -184,8 +169,7 @@ __global__ void __launch_bounds__(128) decide_kernel(
     int gamma, int V, uint64_t seed, float* __restrict__ M_t, float* __restrict__ lnS_t,
     float* __restrict__ p_t, int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ n_out, int32_t* __restrict__ mode, int32_t* __restrict__ pos,
-    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, uint32_t* __restrict__ fb_count,
-    int* err) {
+    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, int* err) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -232,7 +216,6 @@ __global__ void __launch_bounds__(128) decide_kernel(
     accept_len[b] = acc;
     n_out[b] = acc + 1;
     fallback[b] = 0;
-    fb_count[b] = 0u;
     if (j) {
       mode[b] = kModeResidual;
       pos[b] = j;
@@ -461,44 +444,37 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
   }
 }
 
-// One warp per request: the best (score, index) over the row's partials is the token.
-__global__ void __launch_bounds__(128) finalize_kernel(
-    const RowState* __restrict__ partials, int splits, int B, int gamma,
-    const int32_t* __restrict__ mode, const int32_t* __restrict__ accept_len,
-    int32_t* __restrict__ out_tokens, int32_t* __restrict__ fallback) {
+// One CTA per request.  Warp 0 merges the row's partials; the best (score, index) is the
+// token.  If the residual's support came out empty in fp32 (no partial has an index), the
+// whole CTA draws the fallback instead: Gumbel-max over T[b, j] with the residual's random
+// stream (a path the acceptance rule practically never takes, so it is not split further).
+__global__ void __launch_bounds__(kSampleThreads) finalize_kernel(
+    const float* __restrict__ T, const RowState* __restrict__ partials, int splits, int gamma,
+    int V, uint64_t seed, const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
+    const int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
+    int32_t* __restrict__ fallback) {
+  __shared__ RowState red[32];
+  __shared__ int best_s;
   pdl_wait();
   pdl_launch_dependents();
-  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (b >= B) return;
+  const int b = blockIdx.x;
   const int md = mode[b];
   if (md != kModeResidual && md != kModeBonus) return;
-  const RowState acc = merge_partials(partials + (size_t)b * splits, splits);
-  if ((threadIdx.x & 31) == 0) {
-    if (acc.idx >= 0) {
-      out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = acc.idx;
-    } else {
-      fallback[b] = 1;
-    }
+  if (threadIdx.x < 32) {
+    const RowState acc = merge_partials(partials + (size_t)b * splits, splits);
+    if (threadIdx.x == 0) best_s = acc.idx;
   }
-}
-
-// --------------------------------------------------------------------------- fallback
-__global__ void __launch_bounds__(kSampleThreads) fallback_kernel(
-    const float* __restrict__ T, const int32_t* __restrict__ pos,
-    const int32_t* __restrict__ accept_len, const int32_t* __restrict__ fallback, int gamma,
-    int V, uint64_t seed, int splits, int seg, RowState* __restrict__ partials,
-    uint32_t* __restrict__ counters, int32_t* __restrict__ out_tokens) {
-  __shared__ RowState red[32];
-  __shared__ int is_last;
-  pdl_wait();
-  pdl_launch_dependents();
-  const int b = blockIdx.y;
-  if (!fallback[b]) return;
+  __syncthreads();
+  const int best = best_s;
+  if (best >= 0) {
+    if (threadIdx.x == 0) out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = best;
+    return;
+  }
+  // fallback
   const int k = pos[b];
   const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
-  const int v_begin = blockIdx.x * seg, v_end = min(V, v_begin + seg);
   RowState st = row_state_empty();
-  for (int v = v_begin + 4 * threadIdx.x; v < v_end; v += 4 * kSampleThreads) {
+  for (int v = 4 * threadIdx.x; v < V; v += 4 * kSampleThreads) {
     const float4 t4 = ld_stream_f4(Trow + v);
     const float t[4] = {t4.x, t4.y, t4.z, t4.w};
     const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 2u);
@@ -513,15 +489,9 @@ __global__ void __launch_bounds__(kSampleThreads) fallback_kernel(
     }
   }
   st = row_state_block_reduce(st, red);
-  if (!publish_partial(st, partials + (size_t)b * splits + blockIdx.x, &counters[b], splits,
-                       &is_last))
-    return;
-  if (threadIdx.x < 32) {
-    const RowState acc = merge_partials(partials + (size_t)b * splits, splits);
-    if (threadIdx.x == 0) {
-      out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = acc.idx;
-      counters[b] = 0u;
-    }
+  if (threadIdx.x == 0) {
+    fallback[b] = 1;
+    out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = st.idx;
   }
 }
 
@@ -560,7 +530,6 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   RowState* part = ws_at<RowState>(ws, p.off_part);
   float2* part_stats = reinterpret_cast<float2*>(part);
   RowState* part_ver = part + (size_t)B * gamma * p.stats.splits;
-  uint32_t* cnt_fb = ws_at<uint32_t>(ws, p.off_cnt);
   float* M_t = ws_at<float>(ws, p.off_M);
   float* lnS_t = ws_at<float>(ws, p.off_lnS);
   float* p_t = ws_at<float>(ws, p.off_p);
@@ -575,7 +544,7 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   if (e != cudaSuccess) return e;
   e = launch_pdl(decide_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream, T, anchor, tokens, q_tok,
                  (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, M_t, lnS_t,
-                 p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, cnt_fb, err);
+                 p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, err);
   if (e != cudaSuccess) return e;
   if ((e = launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
     return e;
@@ -584,13 +553,9 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
                  row_sumexp, (const float*)M_t, (const float*)lnS_t, (const int32_t*)mode,
                  (const int32_t*)pos, B, gamma, V, seed, p.ver.splits, part_ver, err);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(finalize_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream,
-                 (const RowState*)part_ver, p.ver.splits, B, gamma, (const int32_t*)mode,
-                 (const int32_t*)accept_len, out_tokens, fb);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(fallback_kernel, dim3(p.ver.splits, B), dim3(kSampleThreads), 0, stream, T,
-                 (const int32_t*)pos, (const int32_t*)accept_len, (const int32_t*)fb, gamma, V,
-                 seed, p.ver.splits, p.ver.seg, part_ver, cnt_fb, out_tokens);
+  e = launch_pdl(finalize_kernel, dim3(B), dim3(kSampleThreads), 0, stream, T,
+                 (const RowState*)part_ver, p.ver.splits, gamma, V, seed, (const int32_t*)mode,
+                 (const int32_t*)pos, (const int32_t*)accept_len, out_tokens, fb);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
