@@ -176,17 +176,37 @@ __device__ __forceinline__ void gather_E(uint8_t* sE, const DraftParams& p, int 
 }
 
 // Merge the G partials of request b at position kp into x, q, max and sum (one warp).
+// One pass: every lane issues the loads of all its partials (G <= kDraftMaxCtas, so at
+// most five per lane) and of the token key together, then merges locally and across the
+// warp; a CTA that merges runs this right after its grid-barrier arrival, so it is kept
+// to about one L2 round trip.
+constexpr int kMergePerLane = (kDraftMaxCtas + 31) / 32;
 __device__ __forceinline__ void finalize_row(const DraftParams& p, int b, int kp, int G, int lane) {
-  const int x = token_of_key(__ldcg(p.keys + (size_t)(kp - 1) * p.B + b));
+  const unsigned long long key = __ldcg(p.keys + (size_t)(kp - 1) * p.B + b);
   const RowState* base = p.partials + ((size_t)(kp % 3) * p.B + b) * G;
-  float m = -INFINITY, zx = -INFINITY;
-  for (int g = lane; g < G; g += 32) m = fmaxf(m, __ldcg(&base[g].m));
+  float pm[kMergePerLane], ps[kMergePerLane], pz[kMergePerLane];
+  int pi[kMergePerLane];
+#pragma unroll
+  for (int u = 0; u < kMergePerLane; ++u) {
+    const int g = lane + 32 * u;
+    pm[u] = -INFINITY; ps[u] = 0.f; pz[u] = -INFINITY; pi[u] = -1;
+    if (g < G) {
+      pm[u] = __ldcg(&base[g].m);
+      ps[u] = __ldcg(&base[g].s);
+      pz[u] = __ldcg(&base[g].z);
+      pi[u] = __ldcg(&base[g].idx);
+    }
+  }
+  const int x = token_of_key(key);
+  float m = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kMergePerLane; ++u) m = fmaxf(m, pm[u]);
   m = warp_max(m);
-  float s = 0.f;
-  for (int g = lane; g < G; g += 32) {
-    const float mg = __ldcg(&base[g].m);
-    if (mg != -INFINITY) s += __ldcg(&base[g].s) * expf(mg - m);
-    if (__ldcg(&base[g].idx) == x) zx = __ldcg(&base[g].z);
+  float s = 0.f, zx = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kMergePerLane; ++u) {
+    if (pm[u] != -INFINITY) s += ps[u] * expf(pm[u] - m);
+    if (pi[u] == x) zx = pz[u];
   }
   s = warp_sum(s);
   zx = warp_max(zx);
