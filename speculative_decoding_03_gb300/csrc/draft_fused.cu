@@ -120,10 +120,18 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
+// Order-preserving map of a (non-NaN) float to a 32-bit unsigned key and back: larger
+// float <-> larger key, so the warp's integer max reduction (redux.sync) gives the exact
+// float maximum in one instruction.
+__device__ __forceinline__ uint32_t float_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 __device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
+  return key_float(__reduce_max_sync(0xffffffffu, float_key(x)));
 }
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -593,12 +601,17 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
                 if (scj > sc) { sc = scj; sv = v + j; szz = z[i][j]; }
               }
             }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-              const float osc = __shfl_xor_sync(0xffffffffu, sc, o);
-              const int osv = __shfl_xor_sync(0xffffffffu, sv, o);
-              const float osz = __shfl_xor_sync(0xffffffffu, szz, o);
-              if (osc > sc || (osc == sc && osv < sv)) { sc = osc; sv = osv; szz = osz; }
+            // the warp's best (largest score, then smallest index): two integer reductions,
+            // a ballot and one shuffle
+            {
+              const uint32_t kme = float_key(sc + 0.f);   // +0 and -0 compare equal
+              const uint32_t kmax = __reduce_max_sync(0xffffffffu, kme);
+              const bool top = kme == kmax;
+              const uint32_t vmin = __reduce_min_sync(0xffffffffu, top ? (uint32_t)sv : 0xFFFFFFFFu);
+              const int src = __ffs(__ballot_sync(0xffffffffu, top && (uint32_t)sv == vmin)) - 1;
+              sc = key_float(kmax);
+              sv = (int)vmin;
+              szz = __shfl_sync(0xffffffffu, szz, src);
             }
             if (sv != 0x7FFFFFFF && better(sc, sv, bsc[i], bi[i])) {
               bsc[i] = sc; bi[i] = sv; bz[i] = szz;
@@ -614,8 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       }
       // publish this CTA's partials of the job's requests: the warp reductions of all its
       // rows first, then the stores and atomics.  No fence here: the thread that counts
-      // the CTA into the grid barrier fences after the samplers' named barrier, which
-      // orders every sampler's stores and atomics before its release.
+      // the CTA into the grid barrier does so with a release reduction after the
+      // samplers' named barrier, which orders every sampler's stores and atomics first.
       float pm[RPW], pst[RPW];
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
@@ -650,8 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         // this CTA is done with position k: count it in the grid barrier
         named_bar_sync(kNamedBarSamplers, kSamplerThreads);
         if (stid == 0) {
-          __threadfence();
-          atomicAdd(p.grid_count, 1u);
+          // a release reduction: every sampler's partials and key updates (ordered before
+          // this thread by the named barrier) become visible before the count does, and
+          // the thread does not wait for the add to return
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.grid_count) : "memory");
         }
         // merge this CTA's share of position k-1 while the other CTAs finish position k
         // (partials rotate over three slots: slot (k-1) % 3 is next written at position
