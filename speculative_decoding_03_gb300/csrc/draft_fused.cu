@@ -64,6 +64,8 @@ constexpr int kDepth = 4;             // accumulators in TMEM, z tiles and U til
 constexpr int kUStages = kDepth;      // U tile ring (consumed by the samplers)
 constexpr int kKChunkMax = 64;
 constexpr int kNamedBarSamplers = 1;
+constexpr int kGatherWarps = 4;       // sampler warps 0..3 also gather E
+constexpr int kNamedBarGather = 2;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kLazy = 32.f;             // reference raise margin (exp(32) fits fp32 sums)
 constexpr float kShrink = 1.f - 0x1.0p-16f;  // filter slack, well above fp32 rounding
@@ -156,31 +158,6 @@ __device__ __forceinline__ uint4 philox_wide(uint4 c, uint32_t k0, uint32_t k1) 
 
 __device__ __forceinline__ int token_of_key(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-}
-
-// Gather E = W1[prev_b] of one chunk (rows b0 .. b0+NB-1) into the K-major, 128-byte
-// swizzled B operand: 16-byte chunk c of row n goes to chunk (c % 8) ^ (n % 8) of the
-// 128-byte line n of K-block c / 8.  Executed by the sampler threads.
-template <int NB>
-__device__ __forceinline__ void gather_E(uint8_t* sE, const DraftParams& p, int b0, int k,
-                                         int tid) {
-  const int kchunks = p.r >> 3;
-  for (int idx = tid; idx < NB * kchunks; idx += kSamplerThreads) {
-    const int n = idx / kchunks, c = idx - n * kchunks;
-    const int b = b0 + n;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (b < p.B) {
-      const int prev = (k == 1) ? p.anchor[b]
-                                : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
-      if (prev >= 0 && prev < p.V) {
-        val = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * p.r) + c);
-      } else {
-        set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
-      }
-    }
-    *reinterpret_cast<uint4*>(sE + (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 +
-                              (((c & 7) ^ (n & 7)) << 4)) = val;
-  }
 }
 
 // Merge the G partials of request b at position kp into x, q, max and sum (one warp).
@@ -474,15 +451,62 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     const int stid = threadIdx.x - kFirstSampler * 32;
     const uint32_t k0 = (uint32_t)p.seed, k1 = (uint32_t)(p.seed >> 32);
     uint32_t tc = 0;
-    // publish the E operand of job `j` (chunk c, position k) into its buffer
-    auto publish_E = [&](int j, int c, int k) {
-      if (stid == 0) wait1(&e_empty[j & 1], ((j >> 1) & 1) ^ 1);
-      named_bar_sync(kNamedBarSamplers, kSamplerThreads);
-      if (!*(volatile int*)&abort_s) gather_E<NB>(smem + S::kOffE + (j & 1) * S::kEBytes, p, c * NB, k, stid);
+    // The first kGatherWarps sampler warps publish the E operand of job `j` (chunk c,
+    // position k): E = W1[x_{k-1}] as the K-major, 128-byte-swizzled B operand (16-byte
+    // chunk q of row n goes to chunk (q % 8) ^ (n % 8) of line n of K-block q / 8).  Thread
+    // t takes row t % NB and every (128 / NB)-th chunk of it, all its loads in flight at
+    // once.  For k > 1 they first wait for the grid barrier (one lane polls).  The other
+    // sampler warps take no part: their first z tile cannot complete before E is published.
+    constexpr int kGatherThreads = kGatherWarps * 32;
+    constexpr int kGatherGroups = kGatherThreads / NB;
+    auto publish_E = [&](int j, int c, int k, bool wait_grid) {
+      if (sw >= kGatherWarps) return;
+      if (stid == 0) {
+        if (wait_grid) {
+          const unsigned int target = (unsigned int)G * (unsigned int)(k - 1);
+          const long long t0 = sm_cycles();
+          while (ld_acquire_u32(p.grid_count) < target) {
+            if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
+              set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+              atomicExch(&abort_s, 1);
+              break;
+            }
+          }
+        }
+        wait1(&e_empty[j & 1], ((j >> 1) & 1) ^ 1);
+      }
+      named_bar_sync(kNamedBarGather, kGatherThreads);
+      if (!*(volatile int*)&abort_s) {
+        uint8_t* sE = smem + S::kOffE + (j & 1) * S::kEBytes;
+        const int n = stid % NB, grp = stid / NB;
+        const int b = c * NB + n;
+        const int kchunks = p.r >> 3;               // 16-byte chunks per W1 row (<= 32)
+        int prev = -1;
+        if (b < p.B)
+          prev = (k == 1) ? p.anchor[b] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+        const bool ok = b < p.B && prev >= 0 && prev < p.V;
+        if (b < p.B && !ok) set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
+        const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)(ok ? prev : 0) * p.r);
+        constexpr int kPer = 32 / kGatherGroups > 0 ? (32 + kGatherGroups - 1) / kGatherGroups : 1;
+        uint4 val[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int q = grp + i * kGatherGroups;
+          val[i] = (ok && q < kchunks) ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int q = grp + i * kGatherGroups;
+          if (q < kchunks)
+            *reinterpret_cast<uint4*>(sE + (size_t)(q >> 3) * NB * 128 + (size_t)n * 128 +
+                                      (((q & 7) ^ (n & 7)) << 4)) = val[i];
+        }
+      }
       fence_proxy_async_smem();
-      named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+      named_bar_sync(kNamedBarGather, kGatherThreads);
       if (stid == 0) mbar_arrive(&e_full[j & 1]);
     };
+    // every sampler waits for the grid barrier (only at the end of the call)
     auto grid_wait = [&](unsigned int target) {
       if (stid == 0) {
         const long long t0 = sm_cycles();
@@ -499,12 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
 
     for (int job = 0; job < n_jobs; ++job) {
       const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
-      if (c == 0) {
-        if (k > 1) grid_wait((unsigned int)G * (unsigned int)(k - 1));
-        publish_E(job, 0, k);
-      }
+      if (c == 0) publish_E(job, 0, k, k > 1);
       // the next chunk of the same position only needs x_{k-1}: publish it now
-      if (c + 1 < p.n_chunks) publish_E(job + 1, c + 1, k);
+      if (c + 1 < p.n_chunks) publish_E(job + 1, c + 1, k, false);
 
       // Per-request state of this warp's rows.  Warp-uniform: the lazy reference Mr (a
       // past warp max, raised only when a logit exceeds it by more than kLazy, so that
