@@ -63,6 +63,14 @@ def lib():
         L.dso_verify.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, u64,
                                  P, P, P, P, P, P, i32]
         L.dso_verify.restype = i32
+        L.dso_draft_greedy.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, P, P, i32]
+        L.dso_draft_greedy.restype = i32
+        L.dso_verify_greedy.argtypes = [P, P, P, P, i32, i32, i32, u64, P, P, P, P, P, P, i32]
+        L.dso_verify_greedy.restype = i32
+        L.dso_schedule_async.argtypes = [P, i32, i32, P, i32, i32, P, P, P, P]
+        L.dso_schedule_async.restype = i32
+        L.dso_schedule_threshold.argtypes = [P, i32, i32, f32, P, P]
+        L.dso_schedule_threshold.restype = i32
         _lib = L
     return _lib
 
@@ -206,6 +214,81 @@ def verify(T, U, W1, W2, anchor, tokens, ell, seed: int, req_ids: Optional[Seque
                           nthreads or default_threads())
     _check(rc, "verify")
     return res
+
+
+# ------------------------------------------------------------------------------ variants
+
+def draft_greedy(U, W1, W2, anchor, nthreads: Optional[int] = None):
+    """Greedy draft: x_k = argmax z (ties to the smallest v), q_tok = 1.
+
+    Returns dict(tokens, q_tok, row_max, row_sumexp, gap) with [n, gamma] arrays (gap is
+    the top-two logit gap)."""
+    U = _c(U, np.float32)
+    n, gamma, V = U.shape
+    W1 = _c(W1, np.uint16)
+    W2 = _c(W2, np.uint16)
+    r = W1.shape[1]
+    assert W1.shape == (V, r) and W2.shape == (r, V)
+    anchor = _c(anchor, np.int32)
+    out = {k: np.zeros((n, gamma), dtype=np.float64) for k in ("q_tok", "row_max", "row_sumexp", "gap")}
+    tokens = np.zeros((n, gamma), dtype=np.int32)
+    rc = lib().dso_draft_greedy(_p(U), _p(W1), _p(W2), _p(anchor), n, gamma, V, r, _p(tokens),
+                                _p(out["q_tok"]), _p(out["row_max"]), _p(out["row_sumexp"]),
+                                _p(out["gap"]), nthreads or default_threads())
+    _check(rc, "draft_greedy")
+    out["tokens"] = tokens
+    return out
+
+
+def verify_greedy(T, tokens, ell, seed: int, req_ids: Optional[Sequence[int]] = None,
+                  nthreads: Optional[int] = None):
+    """Verification of greedily drafted tokens (proposal = point mass at each token).
+
+    Same outputs as ``verify``."""
+    T = _c(T, np.float32)
+    n, g1, V = T.shape
+    gamma = g1 - 1
+    tokens = _c(tokens, np.int32)
+    assert tokens.shape == (n, gamma)
+    ids = _c(np.arange(n) if req_ids is None else req_ids, np.int32)
+    res = dict(accept_len=np.zeros(n, np.int32), out_tokens=np.zeros((n, gamma + 1), np.int32),
+               n_out=np.zeros(n, np.int32), band=np.zeros((n, gamma), np.float64),
+               gap=np.zeros(n, np.float64), fallback=np.zeros(n, np.int32))
+    rc = lib().dso_verify_greedy(_p(T), _p(tokens), _p(_c(ell, np.int32)), _p(ids), n, gamma, V,
+                                 ctypes.c_uint64(seed), _p(res["accept_len"]),
+                                 _p(res["out_tokens"]), _p(res["n_out"]), _p(res["band"]),
+                                 _p(res["gap"]), _p(res["fallback"]), nthreads or default_threads())
+    _check(rc, "verify_greedy")
+    return res
+
+
+def schedule_async(a, sps, K_in: int):
+    """Two-step capacity scheduler: the first K_in items of this step's order (K_in < 0:
+    this step's own early-stop count).  Returns (ell [R], B_total, Theta, K_out)."""
+    a = _c(a, np.float32)
+    R, gamma = a.shape
+    sps = _c(sps, np.float32)
+    ell = np.zeros(R, dtype=np.int32)
+    Bt = np.zeros(1, dtype=np.int32)
+    th = np.zeros(1, dtype=np.float64)
+    ko = np.zeros(1, dtype=np.int32)
+    rc = lib().dso_schedule_async(_p(a), R, gamma, _p(sps), len(sps), int(K_in), _p(ell), _p(Bt),
+                                  _p(th), _p(ko))
+    _check(rc, "schedule_async")
+    return ell, int(Bt[0]), float(th[0]), int(ko[0])
+
+
+def schedule_threshold(a, threshold: float):
+    """Fixed-threshold truncation: l_r = leading run of a[r, j] > threshold.
+
+    Returns (ell [R], B_total)."""
+    a = _c(a, np.float32)
+    R, gamma = a.shape
+    ell = np.zeros(R, dtype=np.int32)
+    Bt = np.zeros(1, dtype=np.int32)
+    rc = lib().dso_schedule_threshold(_p(a), R, gamma, ctypes.c_float(threshold), _p(ell), _p(Bt))
+    _check(rc, "schedule_threshold")
+    return ell, int(Bt[0])
 
 
 def step(inp, seed: int, nthreads: Optional[int] = None):

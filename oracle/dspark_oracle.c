@@ -24,6 +24,12 @@
  *               the first reject and draw the correction from the residual) and the
  *               xhh.club DSpark page, Q&A on the acceptance rule (residual norm(max(0,
  *               p - q))).
+ *   variants    greedy drafting (billytse.dev section 11, the serving example's draft
+ *               sampling method) with its point-mass proposal in verification; the
+ *               asynchronous two-step capacity scheduler (weigao.cc "4. hardware-aware
+ *               prefix scheduler"; billytse.dev section 7); fixed confidence-threshold
+ *               truncation (billytse.dev section 8; xhh.club page on load-dependent
+ *               thresholds).
  *
  * Readings where the pages are silent (the same list is kept with the design notes):
  *   - Random numbers: Philox4x32 with 7 rounds (Salmon, Moraes, Dror, Shaw, "Parallel
@@ -44,6 +50,14 @@
  *   - Verify: the bonus row is target row l + 1; the residual draw is Gumbel-max over
  *     log(P - Q) restricted to P > Q; if that set is empty, Gumbel-max over log P with
  *     the same stream (counted as a fallback).
+ *   - Greedy draft: x_k = argmax z_k, ties to the smallest v; the proposal is the point
+ *     mass at x_k (q = 1), so verification accepts with probability p(x_k) and the
+ *     residual is p without x_k.
+ *   - Two-step scheduler: K for step t is the early-stop count of step t - 2; the steps
+ *     without such history use their own count; the K admitted items are the first K in
+ *     the scheduler's order (a desc, r asc, j asc).
+ *   - Threshold truncation: l_r is the leading run of positions with a[r, j] > threshold
+ *     (strict, like the marginal rule of the adaptive scheduler).
  *
  * Parity pins live in tests/test_oracle_*.py.  Every function here is pinned there.
  */
@@ -214,6 +228,56 @@ int dso_draft(const float *U, const uint16_t *W1, const uint16_t *W2, const int3
     return err;
 }
 
+/*
+ * Greedy draft (billytse.dev DSpark page, section 11: the serving example selects the
+ * greedy draft sampling method): the same loop as dso_draft with x_k = argmax_v z_v, ties
+ * to the smallest v.  The proposal is then the point mass at x_k, so q_tok = 1; row_max
+ * and row_sumexp are still the softmax statistics of z, and gap is the top-two logit gap
+ * (the tie band of this draw).  No random numbers are used.
+ */
+int dso_draft_greedy(const float *U, const uint16_t *W1, const uint16_t *W2,
+                     const int32_t *anchor, int n_req, int gamma, int V, int r, int32_t *tokens,
+                     double *q_tok, double *row_max, double *row_sumexp, double *gap,
+                     int nthreads)
+{
+    if (n_req < 0 || gamma < 1 || V < 1 || r < 1) return DSO_ERR_ARG;
+    int err = DSO_OK;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int i = 0; i < n_req; ++i) {
+        double *z = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!z) { err = DSO_ERR_NOMEM; continue; }
+        int prev = anchor[i];
+        for (int k = 1; k <= gamma; ++k) {
+            size_t o = (size_t)i * gamma + (k - 1);
+            if (prev < 0 || prev >= V) { err = DSO_ERR_ARG; break; }
+            draft_logits(U + o * V, W1, W2, prev, V, r, z);
+            double m, s;
+            softmax_stats(z, V, &m, &s);
+            int x = 0;
+            double second = -INFINITY;
+            for (int v = 1; v < V; ++v) {
+                if (z[v] > z[x]) {
+                    second = z[x];
+                    x = v;
+                } else if (z[v] > second) {
+                    second = z[v];
+                }
+            }
+            tokens[o] = x;
+            q_tok[o] = 1.0;
+            row_max[o] = m;
+            row_sumexp[o] = s;
+            gap[o] = z[x] - second;
+            prev = x;
+        }
+        free(z);
+    }
+    return err;
+}
+
 /* Markov bias alone: out[i][v] = sum_k W1[prev_i][k] * W2[k][v] in double
  * (prev_i = -1 gives a zero row). */
 int dso_markov_bias(const uint16_t *W1, const uint16_t *W2, const int32_t *prev, int n, int V,
@@ -285,21 +349,19 @@ static int64_t fixed_point_a(float a)
     return (int64_t)floor(x * 4294967296.0 + 0.5);
 }
 
-/* theta[0] = Theta at the returned stop; ell [R]; *B_total = R + admitted. */
-int dso_schedule(const float *a, int R, int gamma, const float *sps, int sps_len,
-                 int32_t *ell, int32_t *B_total, double *theta)
+/* The R * gamma items (A, r, j) sorted by (A desc, r asc, j asc); NULL if out of memory. */
+static sched_item *sorted_items(const float *a, int R, int gamma)
 {
-    if (R < 1 || gamma < 1 || sps_len < R * (gamma + 1) + 1) return DSO_ERR_ARG;
     int N = R * gamma;
     sched_item *it = (sched_item *)malloc(sizeof(sched_item) * (size_t)N);
     sched_item *tmp = (sched_item *)malloc(sizeof(sched_item) * (size_t)N);
-    if (!it || !tmp) { free(it); free(tmp); return DSO_ERR_NOMEM; }
+    if (!it || !tmp) { free(it); free(tmp); return NULL; }
     for (int r = 0; r < R; ++r)
         for (int j = 1; j <= gamma; ++j) {
             sched_item s = {fixed_point_a(a[(size_t)r * gamma + (j - 1)]), r, j};
             it[(size_t)r * gamma + (j - 1)] = s;
         }
-    /* bottom-up merge sort by (A desc, r asc, j asc) */
+    /* bottom-up merge sort */
     for (int width = 1; width < N; width *= 2) {
         for (int lo = 0; lo < N; lo += 2 * width) {
             int mid = lo + width < N ? lo + width : N;
@@ -311,6 +373,18 @@ int dso_schedule(const float *a, int R, int gamma, const float *sps, int sps_len
         }
         sched_item *sw = it; it = tmp; tmp = sw;
     }
+    free(tmp);
+    return it;
+}
+
+/* theta[0] = Theta at the returned stop; ell [R]; *B_total = R + admitted. */
+int dso_schedule(const float *a, int R, int gamma, const float *sps, int sps_len,
+                 int32_t *ell, int32_t *B_total, double *theta)
+{
+    if (R < 1 || gamma < 1 || sps_len < R * (gamma + 1) + 1) return DSO_ERR_ARG;
+    int N = R * gamma;
+    sched_item *it = sorted_items(a, R, gamma);
+    if (!it) return DSO_ERR_NOMEM;
     for (int r = 0; r < R; ++r) ell[r] = 0;
     const double scale = 4294967296.0;
     int64_t S = 0;
@@ -328,7 +402,77 @@ int dso_schedule(const float *a, int R, int gamma, const float *sps, int sps_len
     *B_total = R + admitted;
     *theta = theta_prev / scale;
     free(it);
-    free(tmp);
+    return DSO_OK;
+}
+
+/*
+ * Asynchronous two-step capacity scheduler (weigao.cc DSpark-vs-MTP page, "4. hardware-
+ * aware prefix scheduler", last paragraph; billytse.dev DSpark page, section 7): the number
+ * of positions the target verifies at step t, K, is fixed from the survival probabilities
+ * of step t - 2, so that the batch size is known ahead of the step; the K positions
+ * themselves are the first K in the order of the current survival probabilities.
+ *
+ * K_in >= 0: the capacity decided two steps earlier (clamped to [0, R gamma]).
+ * K_in < 0:  no earlier decision (the first steps of a sequence): K is this step's own
+ *            early-stop count, which makes the call equal to dso_schedule.
+ * Outputs: ell [R] (request r's count among the first K items), B_total = R + K,
+ * theta = (R + S_K) SPS(R + K) with the same fixed-point sum as dso_schedule, and K_out =
+ * the early-stop count n* of this step's a (dso_schedule's B_total - R): the capacity
+ * for step t + 2.
+ */
+int dso_schedule_async(const float *a, int R, int gamma, const float *sps, int sps_len,
+                       int K_in, int32_t *ell, int32_t *B_total, double *theta, int32_t *K_out)
+{
+    if (R < 1 || gamma < 1 || sps_len < R * (gamma + 1) + 1) return DSO_ERR_ARG;
+    int N = R * gamma;
+    int32_t *ell_now = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
+    if (!ell_now) return DSO_ERR_NOMEM;
+    int32_t Bt_now;
+    double th_now;
+    int rc = dso_schedule(a, R, gamma, sps, sps_len, ell_now, &Bt_now, &th_now);
+    free(ell_now);
+    if (rc != DSO_OK) return rc;
+    int n_star = Bt_now - R;
+    int K = K_in < 0 ? n_star : (K_in > N ? N : K_in);
+    sched_item *it = sorted_items(a, R, gamma);
+    if (!it) return DSO_ERR_NOMEM;
+    for (int r = 0; r < R; ++r) ell[r] = 0;
+    int64_t S = 0;
+    for (int n = 1; n <= K; ++n) {
+        S += it[n - 1].A;
+        ell[it[n - 1].r] += 1;
+    }
+    *B_total = R + K;
+    *theta = (double)((int64_t)R * (int64_t)4294967296LL + S) * (double)sps[R + K] / 4294967296.0;
+    *K_out = n_star;
+    free(it);
+    return DSO_OK;
+}
+
+/*
+ * Fixed confidence-threshold truncation (billytse.dev DSpark page, section 8: the
+ * confidence-threshold sweep under fixed-length verification; xhh.club DSpark page, on why
+ * the scheduler's threshold must move with the load: a fixed threshold on the survival
+ * probability is the load-blind baseline).  Request r keeps its draft positions 1..l_r
+ * where l_r is the last j of the leading run with a[r, j] > threshold (the scan stops at
+ * the first j that fails, so admission looks only at positions up to j).  B_total =
+ * sum_r (1 + l_r).  threshold < 0 verifies every position (fixed-length verification).
+ */
+int dso_schedule_threshold(const float *a, int R, int gamma, float threshold, int32_t *ell,
+                           int32_t *B_total)
+{
+    if (R < 1 || gamma < 1) return DSO_ERR_ARG;
+    int64_t total = 0;
+    for (int r = 0; r < R; ++r) {
+        int l = 0;
+        for (int j = 1; j <= gamma; ++j) {
+            if (!((double)a[(size_t)r * gamma + (j - 1)] > (double)threshold)) break;
+            l = j;
+        }
+        ell[r] = l;
+        total += 1 + l;
+    }
+    *B_total = (int32_t)total;
     return DSO_OK;
 }
 
@@ -342,14 +486,21 @@ int dso_schedule(const float *a, int R, int gamma, const float *sps, int sps_len
  * (-1 padded), n_out [n_req], band [n_req, gamma] (|u - p/q| of every accept test, NaN
  * where no test ran), gap [n_req] (top-two score gap of the correction / bonus draw),
  * fallback [n_req] (1 when the residual was empty and P itself was sampled).
+ *
+ * point_mass = 0: the proposal of position k is Q_k = softmax(U[k] + W1[prev] W2), the
+ * distribution the tokens were sampled from.  point_mass = 1: the tokens were drafted
+ * greedily, so the proposal is the point mass at x_k (Q_k(v) = 1 if v = x_k, else 0) and
+ * U, W1, W2 are not read.  The acceptance test and the residual are the same formulas
+ * with that Q.
  */
-int dso_verify(const float *T, const float *U, const uint16_t *W1, const uint16_t *W2,
-               const int32_t *anchor, const int32_t *tokens, const int32_t *ell,
-               const int32_t *req_ids, int n_req, int gamma, int V, int r, uint64_t seed,
-               int32_t *accept_len, int32_t *out_tokens, int32_t *n_out, double *band,
-               double *gap, int32_t *fallback, int nthreads)
+static int verify_impl(const float *T, const float *U, const uint16_t *W1, const uint16_t *W2,
+                       const int32_t *anchor, const int32_t *tokens, const int32_t *ell,
+                       const int32_t *req_ids, int n_req, int gamma, int V, int r,
+                       uint64_t seed, int point_mass, int32_t *accept_len,
+                       int32_t *out_tokens, int32_t *n_out, double *band, double *gap,
+                       int32_t *fallback, int nthreads)
 {
-    if (n_req < 0 || gamma < 1 || V < 1 || r < 1) return DSO_ERR_ARG;
+    if (n_req < 0 || gamma < 1 || V < 1 || (!point_mass && r < 1)) return DSO_ERR_ARG;
     int err = DSO_OK;
 #ifdef _OPENMP
     if (nthreads < 1) nthreads = 1;
@@ -364,29 +515,36 @@ int dso_verify(const float *T, const float *U, const uint16_t *W1, const uint16_
         if (L < 0 || L > gamma) { err = DSO_ERR_ARG; continue; }
         double *z = (double *)malloc(sizeof(double) * (size_t)V);
         double *P = (double *)malloc(sizeof(double) * (size_t)V);
+        double *Q = (double *)malloc(sizeof(double) * (size_t)V);
         double *score = (double *)malloc(sizeof(double) * (size_t)V);
         unsigned char *mask = (unsigned char *)malloc((size_t)V);
-        if (!z || !P || !score || !mask) {
-            free(z); free(P); free(score); free(mask);
+        if (!z || !P || !Q || !score || !mask) {
+            free(z); free(P); free(Q); free(score); free(mask);
             err = DSO_ERR_NOMEM;
             continue;
         }
         int reject_at = 0;   /* 1-based position of the first reject, 0: none */
-        int prev = anchor[i];
+        int prev = anchor ? anchor[i] : -1;
         for (int k = 1; k <= L; ++k) {
             size_t o = (size_t)i * gamma + (k - 1);
             int x = tokens[o];
+            if (x < 0 || x >= V) { err = DSO_ERR_ARG; break; }
             /* target p_k = softmax(T[k]) */
             const float *Trow = T + ((size_t)i * (gamma + 1) + (k - 1)) * V;
             double M = -INFINITY, Ssum = 0.0;
             for (int v = 0; v < V; ++v) if ((double)Trow[v] > M) M = (double)Trow[v];
             for (int v = 0; v < V; ++v) Ssum += exp((double)Trow[v] - M);
             double p = exp((double)Trow[x] - M) / Ssum;
-            /* draft q_k = softmax(U[k] + W1[prev] W2) */
-            draft_logits(U + o * V, W1, W2, prev, V, r, z);
-            double m, s;
-            softmax_stats(z, V, &m, &s);
-            double q = exp(z[x] - m) / s;
+            /* the proposal Q_k the token was drawn from */
+            if (point_mass) {
+                for (int v = 0; v < V; ++v) Q[v] = (v == x) ? 1.0 : 0.0;
+            } else {
+                draft_logits(U + o * V, W1, W2, prev, V, r, z);
+                double m, s;
+                softmax_stats(z, V, &m, &s);
+                for (int v = 0; v < V; ++v) Q[v] = exp(z[v] - m) / s;
+            }
+            double q = Q[x];
             double u = dso_u01(dso_draw(seed, b, k, 0, 1));
             double ratio = p / q;
             band[o] = fabs(u - ratio);
@@ -399,7 +557,7 @@ int dso_verify(const float *T, const float *U, const uint16_t *W1, const uint16_
             int any = 0;
             for (int v = 0; v < V; ++v) {
                 double Pv = exp((double)Trow[v] - M) / Ssum;
-                double Qv = exp(z[v] - m) / s;
+                double Qv = Q[v];
                 P[v] = Pv;
                 mask[v] = Pv > Qv;
                 score[v] = mask[v] ? log(Pv - Qv) : -INFINITY;
@@ -435,7 +593,27 @@ int dso_verify(const float *T, const float *U, const uint16_t *W1, const uint16_
             accept_len[i] = L;
             n_out[i] = L + 1;
         }
-        free(z); free(P); free(score); free(mask);
+        free(z); free(P); free(Q); free(score); free(mask);
     }
     return err;
+}
+
+int dso_verify(const float *T, const float *U, const uint16_t *W1, const uint16_t *W2,
+               const int32_t *anchor, const int32_t *tokens, const int32_t *ell,
+               const int32_t *req_ids, int n_req, int gamma, int V, int r, uint64_t seed,
+               int32_t *accept_len, int32_t *out_tokens, int32_t *n_out, double *band,
+               double *gap, int32_t *fallback, int nthreads)
+{
+    return verify_impl(T, U, W1, W2, anchor, tokens, ell, req_ids, n_req, gamma, V, r, seed, 0,
+                       accept_len, out_tokens, n_out, band, gap, fallback, nthreads);
+}
+
+/* Verification of greedily drafted tokens (proposal = point mass at each token). */
+int dso_verify_greedy(const float *T, const int32_t *tokens, const int32_t *ell,
+                      const int32_t *req_ids, int n_req, int gamma, int V, uint64_t seed,
+                      int32_t *accept_len, int32_t *out_tokens, int32_t *n_out, double *band,
+                      double *gap, int32_t *fallback, int nthreads)
+{
+    return verify_impl(T, NULL, NULL, NULL, NULL, tokens, ell, req_ids, n_req, gamma, V, 0, seed,
+                       1, accept_len, out_tokens, n_out, band, gap, fallback, nthreads);
 }
