@@ -237,6 +237,78 @@ dspark_status dspark_draft_noalloc(const float* U, const uint16_t* W1, const uin
                                    float* row_sumexp, cudaStream_t stream);
 
 /*
+ * Greedy draft.  billytse.dev DSpark page, section 11: the serving example selects the
+ * greedy draft sampling method.  The loop of dspark_draft with x_k = argmax_v z_k(v) (ties
+ * to the smallest v) in place of the random draw; no random numbers are used.  The
+ * proposal is the point mass at x_k, so q_tok = 1; row_max and row_sumexp are the softmax
+ * statistics of z_k as in dspark_draft.
+ *
+ *   Exactly one of W2 ([r, V] bf16) and W2p (the packed copy of dspark_pack_w2) is
+ *   non-NULL; otherwise the arguments, workspace and outputs are those of dspark_draft.
+ *   Verify its tokens with dspark_verify_greedy.
+ */
+dspark_status dspark_draft_greedy(const float* U, const uint16_t* W1, const uint16_t* W2,
+                                  const uint16_t* W2p, const int32_t* anchor, int B, int gamma,
+                                  int V, int r, int32_t* tokens, float* q_tok, float* row_max,
+                                  float* row_sumexp, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/*
+ * Lossless verification of a greedy draft.  The rule of dspark_verify with the greedy
+ * proposal Q_k = point mass at x_k: accept iff u < p_k(x_k) (u from stream 1 as before);
+ * at the first reject j the residual max(0, P_j - Q_j) is P_j without x_j, so
+ * y = argmax over v != x_j of T[b,j,v] + g_v (stream 2); the bonus token is as in
+ * dspark_verify.  U, W1, W2 and the draft's row statistics are not needed.
+ *
+ *   T [B, gamma+1, V] fp32, tokens [B, gamma] int32 (from dspark_draft_greedy or any
+ *   deterministic proposer), ell [B] int32  ->  accept_len, out_tokens, n_out as in
+ *   dspark_verify.  The workspace is one of dspark_workspace_bytes(B, gamma, V, r, H)
+ *   bytes for any r and H.
+ */
+dspark_status dspark_verify_greedy(const float* T, const int32_t* tokens, const int32_t* ell,
+                                   int B, int gamma, int V, uint64_t seed, int32_t* accept_len,
+                                   int32_t* out_tokens, int32_t* n_out, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Asynchronous two-step capacity scheduler.  weigao.cc DSpark-vs-MTP page, "4. hardware-
+ * aware prefix scheduler" (the production scheduler fixes the next step's capacity from
+ * the predictions of two steps earlier, so that CUDA-graph replay and zero-overhead
+ * scheduling know the batch ahead, while the current candidates are still ranked by
+ * their latest cumulative confidence) and billytse.dev DSpark page, section 7 (the old
+ * information decides only how large the top-K is, never whether a given token is
+ * admitted).
+ *
+ * With K = *K_in (clamped to R * gamma) the first K items in the order of
+ * dspark_schedule are admitted: ell [R] counts each request's items among them, B_total =
+ * R + K, theta = (R + S_K) * SPS(R + K) with the fixed-point sum of dspark_schedule.
+ * *K_out receives n*, this step's own early-stop count (dspark_schedule's B_total - R),
+ * the capacity for the step after next.  K_in == NULL or *K_in < 0 admits n* itself, so
+ * the call then equals dspark_schedule.  K_in and K_out are device int32 words; they may
+ * be the same word (the input is read before the output is written), and K_out may be
+ * NULL.  A two-slot ring, slot t % 2 for step t, starting at -1, gives the pipeline.
+ * Arguments, limits and workspace otherwise as dspark_schedule.
+ */
+dspark_status dspark_schedule_async(const float* a, int R, int gamma, const float* sps,
+                                    int sps_len, const int32_t* K_in, int32_t* K_out,
+                                    int32_t* ell, int32_t* B_total, double* theta,
+                                    void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
+
+/*
+ * Fixed confidence-threshold truncation.  billytse.dev DSpark page, section 8 (the
+ * confidence-threshold sweep under fixed-length verification) and the xhh.club DSpark page
+ * (a fixed threshold on the survival probability cannot follow the load: the baseline the
+ * adaptive scheduler improves on).  ell[r] = the number of leading positions j = 1, 2, ...
+ * with a[r, j] > threshold (strict; the scan stops at the first failure), B_total =
+ * sum_r (1 + ell[r]).  threshold < 0 verifies every position (fixed-length verification).
+ *
+ *   a [R, gamma] fp32, 1 <= gamma <= 32, 1 <= R < 65536  ->  ell [R] int32, B_total [1] int32
+ */
+dspark_status dspark_schedule_threshold(const float* a, int R, int gamma, float threshold,
+                                        int32_t* ell, int32_t* B_total, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word kept in `workspace` after synchronising
  * `stream`.  Returns DSPARK_OK, or the first device-side failure recorded since the last
  * read (DSPARK_ERR_DEVICE_CHECK, DSPARK_ERR_TIMEOUT), or DSPARK_ERR_CUDA.

@@ -2,8 +2,9 @@
 
 The library behind this binding (``include/dspark.h``) holds the four calls of one
 speculative step -- ``dspark_draft``, ``dspark_confidence``, ``dspark_schedule``,
-``dspark_verify`` -- plus ``dspark_markov_bias`` and the packed-W2 variants of the draft and
-the verification; every step of the computation runs in
+``dspark_verify`` -- plus ``dspark_markov_bias``, the packed-W2 variants of the draft and
+the verification, greedy drafting with its verification, the asynchronous two-step
+capacity scheduler and fixed-threshold truncation; every step of the computation runs in
 its CUDA kernels.  This module only marshals arguments: it passes device pointers of
 torch tensors and the current CUDA stream through ctypes, and allocates outputs and the
 workspace with torch.  There is no CPU fallback: without the built library and a CUDA
@@ -39,6 +40,10 @@ SIGNATURES = [
     ("dspark_verify_packed", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64,
                                   _P, _P, _P, _P, _SZ, _P]),
     ("dspark_draft_noalloc", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P]),
+    ("dspark_draft_greedy", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_verify_greedy", _I, [_P, _P, _P, _I, _I, _I, _U64, _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_schedule_async", _I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    ("dspark_schedule_threshold", _I, [_P, _I, _I, _F, _P, _P, _P]),
     ("dspark_last_device_status", _I, [_P, _P]),
 ]
 
@@ -242,16 +247,119 @@ def verify_packed(T, U, W1, W2p, anchor, tokens, q_tok, row_max, row_sumexp, ell
     return out
 
 
+def _draft_outputs(B, gamma, device):
+    torch = _torch()
+    return dict(tokens=torch.empty((B, gamma), dtype=torch.int32, device=device),
+                q_tok=torch.empty((B, gamma), dtype=torch.float32, device=device),
+                row_max=torch.empty((B, gamma), dtype=torch.float32, device=device),
+                row_sumexp=torch.empty((B, gamma), dtype=torch.float32, device=device))
+
+
+def _verify_outputs(B, gamma, device):
+    torch = _torch()
+    return dict(accept_len=torch.empty(B, dtype=torch.int32, device=device),
+                out_tokens=torch.empty((B, gamma + 1), dtype=torch.int32, device=device),
+                n_out=torch.empty(B, dtype=torch.int32, device=device))
+
+
+def draft_greedy(U, W1, W2, anchor, ws: Workspace, out: Optional[Dict] = None, packed: bool = False,
+                 stream=None):
+    """Greedy draft (x_k = argmax z_k, q_tok = 1).  ``W2`` is the [r, V] matrix, or the
+    packed copy of pack_w2 when ``packed``."""
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if out is None:
+        out = _draft_outputs(B, gamma, U.device)
+    w2, w2p = (None, W2) if packed else (W2, None)
+    _check("dspark_draft_greedy", lib().dspark_draft_greedy(
+        _ptr(U), _ptr(W1), None if w2 is None else _ptr(w2), None if w2p is None else _ptr(w2p),
+        _ptr(anchor), B, gamma, V, r,
+        _ptr(out["tokens"]), _ptr(out["q_tok"]), _ptr(out["row_max"]), _ptr(out["row_sumexp"]),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
+def verify_greedy(T, tokens, ell, seed: int, ws: Workspace, out: Optional[Dict] = None,
+                  stream=None):
+    """Verification of greedily drafted tokens (point-mass proposals)."""
+    B, g1, V = T.shape
+    gamma = g1 - 1
+    if out is None:
+        out = _verify_outputs(B, gamma, T.device)
+    _check("dspark_verify_greedy", lib().dspark_verify_greedy(
+        _ptr(T), _ptr(tokens), _ptr(ell), B, gamma, V, ctypes.c_uint64(seed),
+        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["n_out"]),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
+def schedule_async(a, sps, K_in, K_out, ws: Workspace, out=None, stream=None):
+    """Two-step capacity scheduler: admits the first ``*K_in`` items of this step's order
+    (``K_in`` None or holding a negative value: this step's own early-stop count) and
+    writes that count to ``K_out`` (device int32 tensors of one element; may be the same
+    tensor, or None)."""
+    torch = _torch()
+    R, gamma = a.shape
+    if out is None:
+        out = (torch.empty(R, dtype=torch.int32, device=a.device),
+               torch.empty(1, dtype=torch.int32, device=a.device),
+               torch.empty(1, dtype=torch.float64, device=a.device))
+    ell, Bt, th = out
+    _check("dspark_schedule_async", lib().dspark_schedule_async(
+        _ptr(a), R, gamma, _ptr(sps), sps.numel(), None if K_in is None else _ptr(K_in),
+        None if K_out is None else _ptr(K_out), _ptr(ell), _ptr(Bt), _ptr(th),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return ell, Bt, th
+
+
+class CapacityRing:
+    """The two device words of the two-step pipeline: step t reads slot t % 2 (written at
+    step t - 2) and overwrites it with its own early-stop count.  Both start at -1, so
+    the first two steps admit their own count."""
+
+    def __init__(self, device="cuda"):
+        torch = _torch()
+        self.slots = torch.full((2,), -1, dtype=torch.int32, device=device)
+
+    def slot(self, t: int):
+        return self.slots[t % 2:t % 2 + 1]
+
+
+def schedule_threshold(a, threshold: float, out=None, stream=None):
+    """Fixed-threshold truncation: ell[r] = leading positions with a[r, j] > threshold."""
+    torch = _torch()
+    R, gamma = a.shape
+    if out is None:
+        out = (torch.empty(R, dtype=torch.int32, device=a.device),
+               torch.empty(1, dtype=torch.int32, device=a.device))
+    ell, Bt = out
+    _check("dspark_schedule_threshold", lib().dspark_schedule_threshold(
+        _ptr(a), R, gamma, ctypes.c_float(threshold), _ptr(ell), _ptr(Bt), _stream(stream)))
+    return ell, Bt
+
+
 # ------------------------------------------------------------------------ whole step
 
 class Step:
     """One speculative step (draft -> confidence -> schedule -> verify) with preallocated
     outputs and workspace, so that ``run`` launches kernels only (capturable in a CUDA
     graph).  ``dev`` maps input names (U, T, W1, W2, h, w_c, anchor, sps) to device
-    tensors; ``b_c`` is the confidence-head bias."""
+    tensors; ``b_c`` is the confidence-head bias.
 
-    def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None, packed: bool = True):
+    ``sampling``: "gumbel" (the draft samples from q_k) or "greedy" (argmax drafts, verified
+    as point-mass proposals).  ``scheduler``: "theta" (the early-stop scheduler), "async"
+    (the two-step capacity scheduler; ``run(seed, t=...)`` picks the ring slot of step t)
+    or "threshold" (fixed truncation at ``threshold``)."""
+
+    SAMPLING = ("gumbel", "greedy")
+    SCHEDULERS = ("theta", "async", "threshold")
+
+    def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None, packed: bool = True,
+                 sampling: str = "gumbel", scheduler: str = "theta", threshold: float = 0.5):
         torch = _torch()
+        if sampling not in self.SAMPLING or scheduler not in self.SCHEDULERS:
+            raise ValueError(f"sampling {sampling!r} / scheduler {scheduler!r}")
+        self.sampling, self.scheduler, self.threshold = sampling, scheduler, float(threshold)
         self.dev = dev
         # the draft streams W2 from a packed copy made once here (weight preparation)
         self.W2p = pack_w2(dev["W2"]) if packed else None
@@ -274,16 +382,25 @@ class Step:
         self.verify_out = dict(accept_len=torch.empty(B, dtype=i32, device=d),
                                out_tokens=torch.empty((B, gamma + 1), dtype=i32, device=d),
                                n_out=torch.empty(B, dtype=i32, device=d))
+        self.ring = CapacityRing(d) if scheduler == "async" else None
 
-    def run(self, seed: int, stream=None):
+    def run(self, seed: int, stream=None, t: int = 0):
         x = self.dev
+        if self.sampling == "greedy":
+            w2, packed = (self.W2p, True) if self.W2p is not None else (x["W2"], False)
+            d = draft_greedy(x["U"], x["W1"], w2, x["anchor"], self.ws, self.draft_out, packed, stream)
+            c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
+                              self.conf_out, stream)
+            ell = self._schedule(a, stream, t)
+            verify_greedy(x["T"], d["tokens"], ell, seed, self.ws, self.verify_out, stream)
+            return self
         if self.W2p is not None:
             d = draft_packed(x["U"], x["W1"], self.W2p, x["anchor"], seed, self.ws, self.draft_out, stream)
         else:
             d = draft(x["U"], x["W1"], x["W2"], x["anchor"], seed, self.ws, self.draft_out, stream)
         c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
                           self.conf_out, stream)
-        ell, _, _ = schedule(a, x["sps"], self.ws, self.sched_out, stream)
+        ell = self._schedule(a, stream, t)
         if self.W2p is not None:
             verify_packed(x["T"], x["U"], x["W1"], self.W2p, x["anchor"], d["tokens"], d["q_tok"],
                           d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
@@ -292,13 +409,24 @@ class Step:
                    d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
         return self
 
+    def _schedule(self, a, stream, t: int):
+        if self.scheduler == "async":
+            k = self.ring.slot(t)
+            ell, _, _ = schedule_async(a, self.dev["sps"], k, k, self.ws, self.sched_out, stream)
+        elif self.scheduler == "threshold":
+            ell, _ = schedule_threshold(a, self.threshold, self.sched_out[:2], stream)
+        else:
+            ell, _, _ = schedule(a, self.dev["sps"], self.ws, self.sched_out, stream)
+        return ell
+
     def capture(self, seeds, draft_only: bool = False):
         """CUDA graphs of run(seed) (or of the draft call alone), one per seed.  The seed
-        is a launch argument, so each graph replays with its own random stream."""
+        is a launch argument, so each graph replays with its own random stream.  With the
+        two-step scheduler, graph i uses capacity slot i % 2."""
         torch = _torch()
         graphs = []
         x = self.dev
-        for sd in seeds:
+        for i, sd in enumerate(seeds):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 if draft_only and self.W2p is not None:
@@ -306,7 +434,7 @@ class Step:
                 elif draft_only:
                     draft(x["U"], x["W1"], x["W2"], x["anchor"], sd, self.ws, self.draft_out)
                 else:
-                    self.run(sd)
+                    self.run(sd, t=i)
             graphs.append(g)
         return graphs
 
@@ -348,7 +476,8 @@ class Step:
         out["c"], out["a"] = (t.cpu().numpy() for t in self.conf_out)
         out["ell"] = self.sched_out[0].cpu().numpy()
         out["B_total"] = int(self.sched_out[1].item())
-        out["theta"] = float(self.sched_out[2].item())
+        if self.scheduler != "threshold":
+            out["theta"] = float(self.sched_out[2].item())
         out.update({k: v.cpu().numpy() for k, v in self.verify_out.items()})
         return out
 

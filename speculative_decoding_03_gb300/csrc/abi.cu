@@ -109,7 +109,79 @@ dspark_status dspark_schedule(const float* a, int R, int gamma, const float* sps
     return DSPARK_ERR_INVALID_ARG;
   if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
   int* err = ws_at<int>(workspace, 0);
-  if (launch_schedule(a, R, gamma, sps, ell, B_total, theta, err, stream) != cudaSuccess)
+  if (launch_schedule(a, R, gamma, sps, nullptr, nullptr, ell, B_total, theta, err, stream) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_schedule_async(const float* a, int R, int gamma, const float* sps,
+                                    int sps_len, const int32_t* K_in, int32_t* K_out,
+                                    int32_t* ell, int32_t* B_total, double* theta,
+                                    void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+  if (R < 1 || gamma < 1) return DSPARK_ERR_INVALID_ARG;
+  if (R >= 65536 || gamma > 32 || (long long)R * gamma > kMaxScheduleItems ||
+      (long long)R * (gamma + 1) >= (1LL << 21))
+    return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)sps_len < (long long)R * (gamma + 1) + 1) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(a, 4) || !aligned(sps, 4) || !aligned(ell, 4) || !aligned(B_total, 4) ||
+      !aligned(theta, 8) || (K_in && !aligned(K_in, 4)) || (K_out && !aligned(K_out, 4)))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
+  int* err = ws_at<int>(workspace, 0);
+  if (launch_schedule(a, R, gamma, sps, K_in, K_out, ell, B_total, theta, err, stream) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_schedule_threshold(const float* a, int R, int gamma, float threshold,
+                                        int32_t* ell, int32_t* B_total, cudaStream_t stream) {
+  if (R < 1 || gamma < 1) return DSPARK_ERR_INVALID_ARG;
+  if (R >= 65536 || gamma > 32) return DSPARK_ERR_UNSUPPORTED;
+  if (threshold != threshold) return DSPARK_ERR_INVALID_ARG;     // NaN
+  if (!aligned(a, 4) || !aligned(ell, 4) || !aligned(B_total, 4)) return DSPARK_ERR_INVALID_ARG;
+  if (launch_schedule_threshold(a, R, gamma, threshold, ell, B_total, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_draft_greedy(const float* U, const uint16_t* W1, const uint16_t* W2,
+                                  const uint16_t* W2p, const int32_t* anchor, int B, int gamma,
+                                  int V, int r, int32_t* tokens, float* q_tok, float* row_max,
+                                  float* row_sumexp, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+  if ((W2 == nullptr) == (W2p == nullptr)) return DSPARK_ERR_INVALID_ARG;
+  dspark_status st = check_shape(B, gamma, V, r, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2 ? W2 : W2p, 16) || !aligned(anchor, 4) ||
+      !aligned(tokens, 4) || !aligned(q_tok, 4) || !aligned(row_max, 4) || !aligned(row_sumexp, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  const Plan p = make_plan(B, gamma, V, r, 0);
+  if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
+  if (launch_draft_fused_greedy(W1, W2, W2p, U, anchor, B, gamma, V, r, tokens, q_tok, row_max,
+                                row_sumexp, ws_at<char>(workspace, p.off_draft),
+                                ws_at<int>(workspace, p.off_err), stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_verify_greedy(const float* T, const int32_t* tokens, const int32_t* ell,
+                                   int B, int gamma, int V, uint64_t seed, int32_t* accept_len,
+                                   int32_t* out_tokens, int32_t* n_out, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+  // the workspace layout does not depend on r or H: any supported r gives the same plan
+  dspark_status st = check_shape(B, gamma, V, 16, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(T, 16) || !aligned(tokens, 4) || !aligned(ell, 4) || !aligned(accept_len, 4) ||
+      !aligned(out_tokens, 4) || !aligned(n_out, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  const Plan p = make_plan(B, gamma, V, 16, 0);
+  if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
+  if (launch_verify(p, T, nullptr, nullptr, nullptr, nullptr, nullptr, tokens, nullptr, nullptr,
+                    nullptr, ell, seed, accept_len, out_tokens, n_out, workspace, stream) !=
+      cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }

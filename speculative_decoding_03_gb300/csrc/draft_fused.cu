@@ -5,6 +5,11 @@
 // for every request at once.  x_k is drawn by Gumbel-max: argmax_v z_v - log E_v with
 // E_v = -log u_v, i.e. argmax_v exp(z_v - M) / E_v for any reference M.
 //
+// The greedy variant (billytse.dev section 11: the serving example drafts greedily) is the
+// same kernel with x_k = argmax_v z_v (ties to the smallest v): the samplers keep the
+// softmax sums and the warp's first largest logit instead of the race, and q_k(x_k) = 1
+// because the proposal is the point mass at x_k.
+//
 // Layout of the work: the vocabulary is cut into 128-row tiles; each CTA (one per SM,
 // cooperative launch) owns a contiguous run of tiles for the whole call.  For every
 // position k and every chunk of NB requests ("job") the CTA:
@@ -166,6 +171,7 @@ __device__ __forceinline__ int token_of_key(unsigned long long key) {
 // warp; a CTA that merges runs this right after its grid-barrier arrival, so it is kept
 // to about one L2 round trip.
 constexpr int kMergePerLane = (kDraftMaxCtas + 31) / 32;
+template <bool Greedy>
 __device__ __forceinline__ void finalize_row(const DraftParams& p, int b, int kp, int G, int lane) {
   const unsigned long long key = __ldcg(p.keys + (size_t)(kp - 1) * p.B + b);
   const RowState* base = p.partials + ((size_t)(kp % 3) * p.B + b) * G;
@@ -198,13 +204,14 @@ __device__ __forceinline__ void finalize_row(const DraftParams& p, int b, int kp
   if (lane == 0) {
     const size_t o = (size_t)b * p.gamma + (kp - 1);
     p.tokens[o] = x;
-    p.q_tok[o] = expf(zx - m) / s;
+    // a greedy draft proposes the point mass at x: q(x) = 1
+    p.q_tok[o] = Greedy ? 1.f : expf(zx - m) / s;
     p.row_max[o] = m;
     p.row_sumexp[o] = s;
   }
 }
 
-template <int NB>
+template <int NB, bool Greedy>
 __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
     const DraftParams p) {
@@ -581,62 +588,86 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
             }
           }
         }
-        // C: the random draws (independent chains across rows)
-        uint4 d[RPW];
+        if constexpr (Greedy) {
+          // greedy: the softmax sums, and the first index of the warp's largest logit when
+          // it beats the best so far (an equal logit of a later tile has a larger index)
 #pragma unroll
-        for (int i = 0; i < RPW; ++i)
-          d[i] = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k,
-                                        (uint32_t)(c * NB + sw * RPW + i), 0u), k0, k1);
-        // D: softmax sums and the cheap candidate test exp(z - Mr) > Tf * w
-        float e[RPW][4], w[RPW][4];
-        unsigned cm[RPW];
+          for (int i = 0; i < RPW; ++i) {
+            const float mL = Mr[i] * kLog2e;
 #pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-          const float mL = Mr[i] * kLog2e;
-          const uint32_t dw[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
-          cm[i] = 0u;
+            for (int j = 0; j < 4; ++j) s[i] += ex2_approx(fmaf(z[i][j], kLog2e, -mL));
+            const uint32_t kme = float_key(lm[i] + 0.f);   // +0 and -0 compare equal
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, kme);
+            const float wmax = key_float(kmax);
+            if (wmax > bsc[i]) {
+              int jl = 3;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            e[i][j] = ex2_approx(fmaf(z[i][j], kLog2e, -mL));
-            s[i] += e[i][j];
-            w[i][j] = w_of_draw(dw[j]);
-            cm[i] |= (e[i][j] > Tf[i] * w[i][j] ? 1u : 0u) << j;
+              for (int j = 2; j >= 0; --j)
+                if (z[i][j] == lm[i]) jl = j;
+              bi[i] = (int)__reduce_min_sync(0xffffffffu,
+                                             kme == kmax ? (uint32_t)(v + jl) : 0xFFFFFFFFu);
+              bsc[i] = wmax;
+              bz[i] = wmax;
+            }
           }
-        }
-        // E: candidates.  Tighten the threshold with the best lower bound
-        // e (1 - w) / w <= e / E among them, then score the survivors exactly.
+        } else {
+          // C: the random draws (independent chains across rows)
+          uint4 d[RPW];
 #pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-          if (__any_sync(0xffffffffu, cm[i] != 0u)) {
-            float L = 0.f;
+          for (int i = 0; i < RPW; ++i)
+            d[i] = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k,
+                                          (uint32_t)(c * NB + sw * RPW + i), 0u), k0, k1);
+          // D: softmax sums and the cheap candidate test exp(z - Mr) > Tf * w
+          float e[RPW][4], w[RPW][4];
+          unsigned cm[RPW];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if ((cm[i] >> j) & 1u) L = fmaxf(L, e[i][j] * (1.f - w[i][j]) * rcp_approx(w[i][j]));
-            const float Teff = fmaxf(Tf[i], warp_max(L) * kShrink);
-            float sc = -INFINITY, szz = -INFINITY;
-            int sv = 0x7FFFFFFF;
+          for (int i = 0; i < RPW; ++i) {
+            const float mL = Mr[i] * kLog2e;
+            const uint32_t dw[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+            cm[i] = 0u;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              if (((cm[i] >> j) & 1u) && e[i][j] > Teff * w[i][j]) {
-                const float scj = z[i][j] - logf(exp1_from_w(w[i][j]));
-                if (scj > sc) { sc = scj; sv = v + j; szz = z[i][j]; }
+              e[i][j] = ex2_approx(fmaf(z[i][j], kLog2e, -mL));
+              s[i] += e[i][j];
+              w[i][j] = w_of_draw(dw[j]);
+              cm[i] |= (e[i][j] > Tf[i] * w[i][j] ? 1u : 0u) << j;
+            }
+          }
+          // E: candidates.  Tighten the threshold with the best lower bound
+          // e (1 - w) / w <= e / E among them, then score the survivors exactly.
+#pragma unroll
+          for (int i = 0; i < RPW; ++i) {
+            if (__any_sync(0xffffffffu, cm[i] != 0u)) {
+              float L = 0.f;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if ((cm[i] >> j) & 1u) L = fmaxf(L, e[i][j] * (1.f - w[i][j]) * rcp_approx(w[i][j]));
+              const float Teff = fmaxf(Tf[i], warp_max(L) * kShrink);
+              float sc = -INFINITY, szz = -INFINITY;
+              int sv = 0x7FFFFFFF;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                if (((cm[i] >> j) & 1u) && e[i][j] > Teff * w[i][j]) {
+                  const float scj = z[i][j] - logf(exp1_from_w(w[i][j]));
+                  if (scj > sc) { sc = scj; sv = v + j; szz = z[i][j]; }
+                }
               }
-            }
-            // the warp's best (largest score, then smallest index): two integer reductions,
-            // a ballot and one shuffle
-            {
-              const uint32_t kme = float_key(sc + 0.f);   // +0 and -0 compare equal
-              const uint32_t kmax = __reduce_max_sync(0xffffffffu, kme);
-              const bool top = kme == kmax;
-              const uint32_t vmin = __reduce_min_sync(0xffffffffu, top ? (uint32_t)sv : 0xFFFFFFFFu);
-              const int src = __ffs(__ballot_sync(0xffffffffu, top && (uint32_t)sv == vmin)) - 1;
-              sc = key_float(kmax);
-              sv = (int)vmin;
-              szz = __shfl_sync(0xffffffffu, szz, src);
-            }
-            if (sv != 0x7FFFFFFF && better(sc, sv, bsc[i], bi[i])) {
-              bsc[i] = sc; bi[i] = sv; bz[i] = szz;
-              Tf[i] = expf(sc - Mr[i]) * kShrink;
+              // the warp's best (largest score, then smallest index): two integer reductions,
+              // a ballot and one shuffle
+              {
+                const uint32_t kme = float_key(sc + 0.f);   // +0 and -0 compare equal
+                const uint32_t kmax = __reduce_max_sync(0xffffffffu, kme);
+                const bool top = kme == kmax;
+                const uint32_t vmin = __reduce_min_sync(0xffffffffu, top ? (uint32_t)sv : 0xFFFFFFFFu);
+                const int src = __ffs(__ballot_sync(0xffffffffu, top && (uint32_t)sv == vmin)) - 1;
+                sc = key_float(kmax);
+                sv = (int)vmin;
+                szz = __shfl_sync(0xffffffffu, szz, src);
+              }
+              if (sv != 0x7FFFFFFF && better(sc, sv, bsc[i], bi[i])) {
+                bsc[i] = sc; bi[i] = sv; bz[i] = szz;
+                Tf[i] = expf(sc - Mr[i]) * kShrink;
+              }
             }
           }
         }
@@ -693,13 +724,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         // (partials rotate over three slots: slot (k-1) % 3 is next written at position
         // k+2, after the barrier this CTA has not yet passed)
         if (k > 1 && !*(volatile int*)&abort_s)
-          for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row(p, b, k - 1, G, lane);
+          for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row<Greedy>(p, b, k - 1, G, lane);
       }
     }
     // the last position: wait for every CTA, then merge this CTA's rows
     grid_wait((unsigned int)G * (unsigned int)p.gamma);
     if (!*(volatile int*)&abort_s)
-      for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row(p, b, p.gamma, G, lane);
+      for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row<Greedy>(p, b, p.gamma, G, lane);
   }
 
   tc_fence_before_sync();
@@ -721,7 +752,7 @@ bool encode_u_map(CUtensorMap* map, const float* U, int B, int gamma, int V, int
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NB>
+template <int NB, bool Greedy>
 int max_grid() {
   static int cached = -1;
   if (cached < 0) {
@@ -729,9 +760,9 @@ int max_grid() {
     const size_t smem = Smem<NB>::kBytes + 1024;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(draft_fused_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(draft_fused_kernel<NB, Greedy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, draft_fused_kernel<NB>, kThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, draft_fused_kernel<NB, Greedy>, kThreads,
                                                       smem) != cudaSuccess)
       return 0;
     cached = per > 0 ? sms : 0;
@@ -739,7 +770,7 @@ int max_grid() {
   return cached;
 }
 
-template <int NB>
+template <int NB, bool Greedy>
 cudaError_t launch_fused(const CUtensorMap& w2_map, const CUtensorMap& u_map, const DraftParams& p,
                          int grid, cudaStream_t stream) {
   const size_t smem = Smem<NB>::kBytes + 1024;
@@ -753,7 +784,7 @@ cudaError_t launch_fused(const CUtensorMap& w2_map, const CUtensorMap& u_map, co
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, draft_fused_kernel<NB>, w2_map, u_map, p);
+  return cudaLaunchKernelEx(&cfg, draft_fused_kernel<NB, Greedy>, w2_map, u_map, p);
 }
 
 }  // namespace
@@ -770,10 +801,11 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
                                 const float* U, const int32_t* anchor, int B, int gamma, int V,
                                 int r, uint64_t seed, int32_t* tokens, float* q_tok,
                                 float* row_max, float* row_sumexp, void* region, int* err,
-                                cudaStream_t stream) {
+                                bool greedy, cudaStream_t stream) {
   const int NB = B <= 16 ? 16 : 32;
   const int n_tiles = cdiv(V, kGemmTileV);
-  int grid = NB == 16 ? max_grid<16>() : max_grid<32>();
+  int grid = greedy ? (NB == 16 ? max_grid<16, true>() : max_grid<32, true>())
+                    : (NB == 16 ? max_grid<16, false>() : max_grid<32, false>());
   if (grid <= 0) return cudaErrorInvalidConfiguration;
   if (grid > n_tiles) grid = n_tiles;
   if (grid > kDraftMaxCtas) grid = kDraftMaxCtas;
@@ -803,8 +835,11 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
   memset(&w2_map, 0, sizeof(w2_map));
   if (!W2p && !encode_w2_map(&w2_map, W2, V, r, p.kc)) return cudaErrorInvalidValue;
   if (!encode_u_map(&u_map, U, B, gamma, V, NB)) return cudaErrorInvalidValue;
-  return NB == 16 ? launch_fused<16>(w2_map, u_map, p, grid, stream)
-                  : launch_fused<32>(w2_map, u_map, p, grid, stream);
+  if (greedy)
+    return NB == 16 ? launch_fused<16, true>(w2_map, u_map, p, grid, stream)
+                    : launch_fused<32, true>(w2_map, u_map, p, grid, stream);
+  return NB == 16 ? launch_fused<16, false>(w2_map, u_map, p, grid, stream)
+                  : launch_fused<32, false>(w2_map, u_map, p, grid, stream);
 }
 }  // namespace
 
@@ -813,7 +848,7 @@ cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const flo
                                uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
                                float* row_sumexp, void* region, int* err, cudaStream_t stream) {
   return launch_draft_common(W1, W2, nullptr, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
-                             row_max, row_sumexp, region, err, stream);
+                             row_max, row_sumexp, region, err, false, stream);
 }
 
 cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, const float* U,
@@ -822,7 +857,16 @@ cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, c
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream) {
   return launch_draft_common(W1, nullptr, W2p, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
-                             row_max, row_sumexp, region, err, stream);
+                             row_max, row_sumexp, region, err, false, stream);
+}
+
+cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
+                                      const float* U, const int32_t* anchor, int B, int gamma,
+                                      int V, int r, int32_t* tokens, float* q_tok,
+                                      float* row_max, float* row_sumexp, void* region, int* err,
+                                      cudaStream_t stream) {
+  return launch_draft_common(W1, W2p ? nullptr : W2, W2p, U, anchor, B, gamma, V, r, 0, tokens,
+                             q_tok, row_max, row_sumexp, region, err, true, stream);
 }
 
 }  // namespace dspark

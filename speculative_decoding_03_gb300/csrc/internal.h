@@ -135,6 +135,13 @@ cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, c
                                       uint64_t seed, int32_t* tokens, float* q_tok,
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream);
+// the greedy draft (x_k = argmax z_k, q_tok = 1) with W2 or, when W2p is not null, the
+// packed tile images
+cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
+                                      const float* U, const int32_t* anchor, int B, int gamma,
+                                      int V, int r, int32_t* tokens, float* q_tok,
+                                      float* row_max, float* row_sumexp, void* region, int* err,
+                                      cudaStream_t stream);
 // rank rows per W2 stage of the draft kernel (and per packed K-chunk image)
 int draft_kchunk(int r);
 
@@ -143,8 +150,13 @@ cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32
                               int H, int r, int V, float* c, float* a, int* err,
                               cudaStream_t stream);
 
-cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps, int32_t* ell,
-                            int32_t* B_total, double* theta, int* err, cudaStream_t stream);
+// K_in / K_out: the two-step capacity (both may be null; see schedule.cu)
+cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps,
+                            const int32_t* K_in, int32_t* K_out, int32_t* ell, int32_t* B_total,
+                            double* theta, int* err, cudaStream_t stream);
+
+cudaError_t launch_schedule_threshold(const float* a, int R, int gamma, float threshold,
+                                      int32_t* ell, int32_t* B_total, cudaStream_t stream);
 
 cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
                           const uint16_t* W2, const uint16_t* W2p, const int32_t* anchor,

@@ -11,6 +11,15 @@
 // integer S_n; every n evaluates Theta_n = double(R 2^32 + S_n) * double(sps[R + n])
 // against Theta_{n-1} (plain double products, no fused multiply-add) and the smallest
 // failing n is found with a shared-memory atomicMin.
+//
+// Two-step capacity (weigao.cc DSpark-vs-MTP page, "4. hardware-aware prefix scheduler";
+// billytse.dev section 7): when a capacity K decided two steps earlier is given, the
+// first K items of this step's order are admitted instead of the first n* (n* = the early-
+// stop count), and n* is written out as the capacity of the step after next.
+//
+// Fixed-threshold truncation (billytse.dev section 8; xhh.club page on load-dependent
+// thresholds): one warp per request, lane j - 1 tests a[r, j] > threshold and a ballot
+// gives the leading run.
 #include "internal.h"
 
 namespace dspark {
@@ -29,12 +38,16 @@ __device__ __forceinline__ double theta_at(long long R, long long S, float sps) 
   return __dmul_rn((double)(R * 4294967296LL + S), (double)sps);
 }
 
+// K_in (may be null, may alias K_out): the capacity decided two steps earlier; a negative
+// value or null admits this step's own early-stop count.  K_out (may be null) receives
+// that count.
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     const float* __restrict__ a, int R, int gamma, int Npad, const float* __restrict__ sps,
-    int32_t* __restrict__ ell, int32_t* __restrict__ B_total, double* __restrict__ theta) {
+    const int32_t* K_in, int32_t* K_out, int32_t* __restrict__ ell,
+    int32_t* __restrict__ B_total, double* __restrict__ theta) {
   extern __shared__ unsigned long long keys[];
   __shared__ long long warp_tot[32];
-  __shared__ int first_fail;
+  __shared__ int first_fail, k_in_s;
   __shared__ float sps_s[kSchedThreads + 1];   // sps[R .. R + N] when N <= kSchedThreads
   __shared__ int cnt_s[kSchedThreads];         // admitted items per request when R <= kSchedThreads
   pdl_wait();                 // the expected returns come from the previous kernel
@@ -58,7 +71,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   }
   if (R > kSchedThreads)
     for (int r = tid; r < R; r += kSchedThreads) ell[r] = 0;
-  if (tid == 0) first_fail = N + 1;
+  if (tid == 0) {
+    first_fail = N + 1;
+    k_in_s = K_in ? *K_in : -1;     // read before K_out (which may alias it) is written
+  }
   __syncthreads();
 
   if (small) {
@@ -138,7 +154,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   }
   if (fail <= N) atomicMin(&first_fail, fail);
   __syncthreads();
-  const int admitted = first_fail - 1;
+  const int n_star = first_fail - 1;
+  const int admitted = k_in_s < 0 ? n_star : min(k_in_s, N);
+  if (K_out && tid == 0) *K_out = n_star;
   if (R <= kSchedThreads) {
     // per-request counts in shared memory, then one coalesced store of ell
     for (int i = tid; i < admitted; i += kSchedThreads)
@@ -165,10 +183,44 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   }
 }
 
+constexpr int kThreshThreads = 1024;
+
+__global__ void __launch_bounds__(kThreshThreads) schedule_threshold_kernel(
+    const float* __restrict__ a, int R, int gamma, float threshold, int32_t* __restrict__ ell,
+    int32_t* __restrict__ B_total) {
+  __shared__ int warp_tot[kThreshThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int total = 0;
+  for (int r = warp; r < R; r += kThreshThreads / 32) {
+    // lanes past gamma count as failures, so the leading run stops at gamma at most
+    const bool pass = lane < gamma && a[(size_t)r * gamma + lane] > threshold;
+    const unsigned fail = ~__ballot_sync(0xffffffffu, pass);
+    const int l = fail ? __ffs(fail) - 1 : 32;    // all 32 pass only when gamma == 32
+    if (lane == 0) ell[r] = l;
+    total += 1 + l;
+  }
+  if (lane == 0) warp_tot[warp] = total;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long t = 0;
+    for (int w = 0; w < kThreshThreads / 32; ++w) t += warp_tot[w];
+    *B_total = (int32_t)t;
+  }
+}
+
 }  // namespace
 
-cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps, int32_t* ell,
-                            int32_t* B_total, double* theta, int* err, cudaStream_t stream) {
+cudaError_t launch_schedule_threshold(const float* a, int R, int gamma, float threshold,
+                                      int32_t* ell, int32_t* B_total, cudaStream_t stream) {
+  return launch_pdl(schedule_threshold_kernel, dim3(1), dim3(kThreshThreads), 0, stream, a, R,
+                    gamma, threshold, ell, B_total);
+}
+
+cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps,
+                            const int32_t* K_in, int32_t* K_out, int32_t* ell, int32_t* B_total,
+                            double* theta, int* err, cudaStream_t stream) {
   (void)err;
   const int N = R * gamma;
   int Npad = 2;
@@ -182,7 +234,7 @@ cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps, 
     attr_set = true;
   }
   return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, stream, a, R, gamma, Npad,
-                    sps, ell, B_total, theta);
+                    sps, K_in, K_out, ell, B_total, theta);
 }
 
 }  // namespace dspark

@@ -19,12 +19,17 @@
 //   finalize       one CTA per request merges the partials and writes the token; only
 //                  for a row whose residual support came out empty in fp32 it draws the
 //                  fallback: Gumbel-max over T[b, j] with the residual's random stream
+//
+// Greedy drafts (billytse.dev section 11) propose the point mass at x_k: q_k(x_k) = 1, so
+// the test is u < p_k(x_k), and the residual max(0, P_j - Q_j) is P_j without x_j.  Then
+// no bias is needed (no bias_gemm launch) and final_sample runs the bonus race over T[b, j]
+// with the residual's stream and x_j excluded.
 #include "internal.h"
 
 namespace dspark {
 namespace {
 
-enum : int { kModeNone = 0, kModeResidual = 1, kModeBonus = 2 };
+enum : int { kModeNone = 0, kModeResidual = 1, kModeBonus = 2, kModePointResidual = 3 };
 
 __device__ __forceinline__ int clamp_ell(const int32_t* ell, int b, int gamma, int* err) {
   int L = ell[b];
@@ -161,7 +166,7 @@ __global__ void __launch_bounds__(kSampleThreads) target_stats_kernel(
 // ----------------------------------------------------------------------------- decide
 // One warp per request; lane k - 1 owns position k.  Verified lanes merge their row's
 // target partials (M, S), compute p_k(x_k) and test u_k < p_k(x_k) / q_k(x_k); a ballot
-// gives the first reject.
+// gives the first reject.  q_tok == null: greedy drafts, q_k(x_k) = 1.
 __global__ void __launch_bounds__(128) decide_kernel(
     const float* __restrict__ T, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const float* __restrict__ q_tok,
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(128) decide_kernel(
     lnS_t[row] = logf(s);
     p_t[row] = p;
     const float u = u01(draw_block(seed, 0u, (uint32_t)k, (uint32_t)b, 1u).x);
-    reject = !(u < p / q_tok[row]);
+    reject = q_tok ? !(u < p / q_tok[row]) : !(u < p);
   }
   const unsigned rej = __ballot_sync(0xffffffffu, reject);
   const int j = rej ? __ffs(rej) : 0;    // first rejected position, 0 if none
@@ -216,7 +221,11 @@ __global__ void __launch_bounds__(128) decide_kernel(
     accept_len[b] = acc;
     n_out[b] = acc + 1;
     fallback[b] = 0;
-    if (j) {
+    if (j && !q_tok) {
+      mode[b] = kModePointResidual;
+      pos[b] = j;
+      prev_tok[b] = -1;
+    } else if (j) {
       mode[b] = kModeResidual;
       pos[b] = j;
       prev_tok[b] = (j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)];
@@ -255,13 +264,14 @@ __device__ __forceinline__ float block_max_f(float x, float* red) {
 
 // One CTA scores one segment of kVerSeg logits of one row: t / zz hold this thread's
 // kVerVec float4 of T and of z = U + bias (residual rows only), v0 the first vocabulary
-// index of the thread's first float4.  Every thread of the CTA calls it; returns the CTA's
-// best (score, index) in every thread.
+// index of the thread's first float4.  Not residual: the race over T alone with random
+// stream `stream`, skipping index `excl` (-1: none).  Every thread of the CTA calls it;
+// returns the CTA's best (score, index) in every thread.
 __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
                                                  const float4 (&zz)[kVerVec], int v0, int V,
                                                  bool residual, float off_a, float off_b,
-                                                 uint64_t seed, int k, int b, RowState* red,
-                                                 float* redf) {
+                                                 uint32_t stream, int excl, uint64_t seed,
+                                                 int k, int b, RowState* red, float* redf) {
   if (!residual) {
     // bonus: reference = the CTA's largest logit (exp(T - m) <= 1)
     float m = -INFINITY;
@@ -269,7 +279,6 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
     for (int j = 0; j < kVerVec; ++j) m = fmaxf(m, fmaxf(fmaxf(t[j].x, t[j].y), fmaxf(t[j].z, t[j].w)));
     off_a = block_max_f(m, redf);
   }
-  const uint32_t stream = residual ? 2u : 3u;
   // phase 1: per logit the upper bound numerator r_hi (compared against L w) and the
   // thread's best lower bound
   float r_hi[kVerVec][4], w[kVerVec][4];
@@ -295,6 +304,7 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
         // both flushed to zero: the bounds say nothing, keep it for exact scoring
         if (in && P + Q == 0.f) { r = INFINITY; e = 0.f; }
       } else {
+        in = in && v + i != excl;
         r = ex2_approx(fmaf(tv[i], kLog2e, -off_a * kLog2e));
         e = r * kRaceSlack;
       }
@@ -369,8 +379,9 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const float* __restrict__ T, const float* __restrict__ U, const float* __restrict__ bias,
     const float* __restrict__ row_max, const float* __restrict__ row_sumexp,
     const float* __restrict__ M_t, const float* __restrict__ lnS_t,
-    const int32_t* __restrict__ mode, const int32_t* __restrict__ pos, int B, int gamma, int V,
-    uint64_t seed, int splits, RowState* __restrict__ partials, int* err) {
+    const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
+    const int32_t* __restrict__ tokens, int B, int gamma, int V, uint64_t seed, int splits,
+    RowState* __restrict__ partials, int* err) {
   extern __shared__ float4 fs_buf[];            // [2][3][kVerSeg / 4]
   __shared__ uint64_t full[2];
   __shared__ RowState red[32];
@@ -399,7 +410,7 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
       bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
       bulk_g2s(dst + kSlot, U + o * V + v0, bytes, &full[buf]);
       bulk_g2s(dst + 2 * kSlot, bias + (size_t)b * V + v0, bytes, &full[buf]);
-    } else if (md == kModeBonus) {
+    } else if (md == kModeBonus || md == kModePointResidual) {
       mbar_expect_tx_cta(&full[buf], bytes);
       bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
     } else {
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const int b = item / splits, seg = item - b * splits;
     const int md = mode[b], k = pos[b];
     const bool residual = md == kModeResidual;
-    if ((md == kModeResidual || md == kModeBonus) && __syncthreads_and(ok)) {
+    if (md != kModeNone && __syncthreads_and(ok)) {
       const int v0 = seg * kVerSeg + 4 * tid;
       const int n4 = (min(kVerSeg, V - seg * kVerSeg) + 3) / 4;
       const float4* src = fs_buf + (size_t)buf * 3 * kSlot;
@@ -437,7 +448,10 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
         off_b = row_max[o] + logf(row_sumexp[o]);
         off_a = M_t[o] + lnS_t[o];
       }
-      const RowState st = race_segment(t, zz, v0, V, residual, off_a, off_b, seed, k, b, red, redf);
+      const uint32_t stream = md == kModeBonus ? 3u : 2u;
+      const int excl = md == kModePointResidual ? tokens[(size_t)b * gamma + (k - 1)] : -1;
+      const RowState st =
+          race_segment(t, zz, v0, V, residual, off_a, off_b, stream, excl, seed, k, b, red, redf);
       if (tid == 0) partials[item] = st;
     }
     __syncthreads();            // every thread is done with this buffer before it is refilled
@@ -459,7 +473,7 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(
   pdl_launch_dependents();
   const int b = blockIdx.x;
   const int md = mode[b];
-  if (md != kModeResidual && md != kModeBonus) return;
+  if (md == kModeNone) return;
   if (threadIdx.x < 32) {
     const RowState acc = merge_partials(partials + (size_t)b * splits, splits);
     if (threadIdx.x == 0) best_s = acc.idx;
@@ -524,6 +538,9 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
                           const float* row_sumexp, const int32_t* ell, uint64_t seed,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* n_out, void* ws,
                           cudaStream_t stream) {
+  // q_tok == null: greedy drafts (point-mass proposals; U, W1, W2 and the row statistics
+  // are not read)
+  const bool point_mass = q_tok == nullptr;
   const int B = p.B, gamma = p.gamma, V = p.V;
   int* err = ws_at<int>(ws, p.off_err);
   float* bias = ws_at<float>(ws, p.off_bias);
@@ -546,12 +563,13 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
                  (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, M_t, lnS_t,
                  p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, err);
   if (e != cudaSuccess) return e;
-  if ((e = launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
+  if (!point_mass &&
+      (e = launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
     return e;
   e = launch_pdl(final_sample_kernel, dim3(final_sample_grid(B * p.ver.splits)),
                  dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias, row_max,
                  row_sumexp, (const float*)M_t, (const float*)lnS_t, (const int32_t*)mode,
-                 (const int32_t*)pos, B, gamma, V, seed, p.ver.splits, part_ver, err);
+                 (const int32_t*)pos, tokens, B, gamma, V, seed, p.ver.splits, part_ver, err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(finalize_kernel, dim3(B), dim3(kSampleThreads), 0, stream, T,
                  (const RowState*)part_ver, p.ver.splits, gamma, V, seed, (const int32_t*)mode,
