@@ -280,6 +280,43 @@ def run_ours(args, w):
     barrier()
     draft_ms = ev_a.elapsed_time(ev_b) / n_draft
 
+    # ---- the variants of the step (greedy drafting, two-step capacity scheduler, fixed
+    # threshold): whole steps in a graph ring, and the greedy draft launch alone
+    variants = {}
+    n_var = max(3, min(args.steps, 50))
+
+    def time_graphs(gs, n):
+        for g in gs:
+            g.replay()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            gs[i % len(gs)].replay()
+        e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) / n
+
+    for sampling, scheduler in (("greedy", "theta"), ("gumbel", "async"), ("greedy", "threshold")):
+        vs = ds.Step(dev, float(inp.b_c), ws=step.ws, W2p=step.W2p, sampling=sampling,
+                     scheduler=scheduler, threshold=0.5)
+        for i in range(3):
+            vs.run(seed=w.seed + i, t=i)
+        ms = time_graphs(vs.capture([w.seed + j for j in range(n_ring)]), n_var)
+        vr = vs.results()
+        entry = {"ms_per_step": ms, "value": world * w.B * w.gamma / (ms * 1e-3),
+                 "mean_ell": float(np.mean(vr["ell"])),
+                 "mean_accept_len": float(np.mean(vr["accept_len"])), "B_total": vr["B_total"]}
+        if sampling == "greedy" and scheduler == "theta":
+            gd_ms = time_graphs(vs.capture([w.seed + j for j in range(n_ring)], draft_only=True), n_var)
+            gd_ach = draft_bytes(w) / (gd_ms * 1e-3) / 1e9
+            entry["draft"] = {"ms_per_launch": gd_ms, "achieved_gbs": gd_ach}
+        variants[f"{sampling}+{scheduler}"] = entry
+        del vs
+    if args.graph:
+        run_step(0)            # back to the main step's outputs
+        barrier()
+
     # ---- per-call breakdown (warm, eager, events between the calls on one stream)
     n_bd = max(3, min(args.steps, 20))
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
@@ -350,6 +387,7 @@ def run_ours(args, w):
         "accept": {"mean_ell": float(np.mean(res["ell"])), "mean_accept_len": float(np.mean(res["accept_len"])),
                    "B_total": res["B_total"], "theta": res["theta"]},
         "breakdown": breakdown,
+        "variants": variants,
         "e2e": {"value": world * w.B * w.gamma / e2e_s, "unit": "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

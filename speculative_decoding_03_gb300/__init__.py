@@ -355,14 +355,16 @@ class Step:
     SCHEDULERS = ("theta", "async", "threshold")
 
     def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None, packed: bool = True,
-                 sampling: str = "gumbel", scheduler: str = "theta", threshold: float = 0.5):
+                 sampling: str = "gumbel", scheduler: str = "theta", threshold: float = 0.5,
+                 W2p=None):
         torch = _torch()
         if sampling not in self.SAMPLING or scheduler not in self.SCHEDULERS:
             raise ValueError(f"sampling {sampling!r} / scheduler {scheduler!r}")
         self.sampling, self.scheduler, self.threshold = sampling, scheduler, float(threshold)
         self.dev = dev
-        # the draft streams W2 from a packed copy made once here (weight preparation)
-        self.W2p = pack_w2(dev["W2"]) if packed else None
+        # the draft streams W2 from a packed copy made once here (weight preparation), or
+        # from the copy ``W2p`` of an earlier pack_w2 call
+        self.W2p = (W2p if W2p is not None else pack_w2(dev["W2"])) if packed else None
         self.b_c = float(b_c)
         B, gamma, V = dev["U"].shape
         r = dev["W1"].shape[1]
@@ -386,28 +388,31 @@ class Step:
 
     def run(self, seed: int, stream=None, t: int = 0):
         x = self.dev
-        if self.sampling == "greedy":
-            w2, packed = (self.W2p, True) if self.W2p is not None else (x["W2"], False)
-            d = draft_greedy(x["U"], x["W1"], w2, x["anchor"], self.ws, self.draft_out, packed, stream)
-            c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
-                              self.conf_out, stream)
-            ell = self._schedule(a, stream, t)
-            verify_greedy(x["T"], d["tokens"], ell, seed, self.ws, self.verify_out, stream)
-            return self
-        if self.W2p is not None:
-            d = draft_packed(x["U"], x["W1"], self.W2p, x["anchor"], seed, self.ws, self.draft_out, stream)
-        else:
-            d = draft(x["U"], x["W1"], x["W2"], x["anchor"], seed, self.ws, self.draft_out, stream)
+        d = self.draft(seed, stream)
         c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
                           self.conf_out, stream)
         ell = self._schedule(a, stream, t)
-        if self.W2p is not None:
+        if self.sampling == "greedy":
+            verify_greedy(x["T"], d["tokens"], ell, seed, self.ws, self.verify_out, stream)
+        elif self.W2p is not None:
             verify_packed(x["T"], x["U"], x["W1"], self.W2p, x["anchor"], d["tokens"], d["q_tok"],
                           d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
         else:
             verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d["tokens"], d["q_tok"],
                    d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
         return self
+
+    def draft(self, seed: int, stream=None):
+        """The draft call of the step alone (into the step's draft outputs)."""
+        x = self.dev
+        if self.sampling == "greedy":
+            w2, packed = (self.W2p, True) if self.W2p is not None else (x["W2"], False)
+            return draft_greedy(x["U"], x["W1"], w2, x["anchor"], self.ws, self.draft_out, packed,
+                                stream)
+        if self.W2p is not None:
+            return draft_packed(x["U"], x["W1"], self.W2p, x["anchor"], seed, self.ws,
+                                self.draft_out, stream)
+        return draft(x["U"], x["W1"], x["W2"], x["anchor"], seed, self.ws, self.draft_out, stream)
 
     def _schedule(self, a, stream, t: int):
         if self.scheduler == "async":
@@ -425,14 +430,11 @@ class Step:
         two-step scheduler, graph i uses capacity slot i % 2."""
         torch = _torch()
         graphs = []
-        x = self.dev
         for i, sd in enumerate(seeds):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                if draft_only and self.W2p is not None:
-                    draft_packed(x["U"], x["W1"], self.W2p, x["anchor"], sd, self.ws, self.draft_out)
-                elif draft_only:
-                    draft(x["U"], x["W1"], x["W2"], x["anchor"], sd, self.ws, self.draft_out)
+                if draft_only:
+                    self.draft(sd)
                 else:
                     self.run(sd, t=i)
             graphs.append(g)
