@@ -71,6 +71,14 @@ def lib():
         L.dso_schedule_async.restype = i32
         L.dso_schedule_threshold.argtypes = [P, i32, i32, f32, P, P]
         L.dso_schedule_threshold.restype = i32
+        L.dso_rnn_project.argtypes = [P, P, P, i32, i32, i32, P]
+        L.dso_rnn_project.restype = i32
+        L.dso_draft_rnn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, u64, i32,
+                                    P, P, P, P, P, P, P, i32]
+        L.dso_draft_rnn.restype = i32
+        L.dso_verify_rnn.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, u64,
+                                     P, P, P, P, P, P, i32]
+        L.dso_verify_rnn.restype = i32
         _lib = L
     return _lib
 
@@ -289,6 +297,73 @@ def schedule_threshold(a, threshold: float):
     rc = lib().dso_schedule_threshold(_p(a), R, gamma, ctypes.c_float(threshold), _p(ell), _p(Bt))
     _check(rc, "schedule_threshold")
     return ell, int(Bt[0])
+
+
+# ------------------------------------------------------------------------------ RNN head
+
+def rnn_project(h, W_rnn, b_rnn):
+    """hp [n, 3r] = h [n, H] W_rnn[2r:] + b_rnn in fp64 (h may be [B, gamma, H])."""
+    h = _c(h, np.float32)
+    lead = h.shape[:-1]
+    H = h.shape[-1]
+    W_rnn = _c(W_rnn, np.uint16)
+    r = W_rnn.shape[1] // 3
+    assert W_rnn.shape == (2 * r + H, 3 * r)
+    n = int(np.prod(lead))
+    hp = np.zeros((n, 3 * r), dtype=np.float64)
+    _check(lib().dso_rnn_project(_p(h), _p(W_rnn), _p(_c(b_rnn, np.float32)), n, H, r, _p(hp)),
+           "rnn_project")
+    return hp.reshape(lead + (3 * r,))
+
+
+def draft_rnn(U, h, W1, W2, W_rnn, b_rnn, anchor, seed: int, greedy: bool = False,
+              req_ids: Optional[Sequence[int]] = None, nthreads: Optional[int] = None):
+    """Draft with the RNN head.  Returns dict(tokens, q_tok, row_max, row_sumexp, gap,
+    E [n, gamma, r] (tanh(output) rows), state [n, r])."""
+    U = _c(U, np.float32)
+    n, gamma, V = U.shape
+    h = _c(h, np.float32)
+    H = h.shape[2]
+    W1 = _c(W1, np.uint16)
+    W2 = _c(W2, np.uint16)
+    r = W1.shape[1]
+    W_rnn = _c(W_rnn, np.uint16)
+    assert W_rnn.shape == (2 * r + H, 3 * r) and h.shape == (n, gamma, H)
+    ids = _c(np.arange(n) if req_ids is None else req_ids, np.int32)
+    out = {k: np.zeros((n, gamma), dtype=np.float64) for k in ("q_tok", "row_max", "row_sumexp", "gap")}
+    tokens = np.zeros((n, gamma), dtype=np.int32)
+    E = np.zeros((n, gamma, r), dtype=np.float64)
+    state = np.zeros((n, r), dtype=np.float64)
+    rc = lib().dso_draft_rnn(_p(U), _p(h), _p(W1), _p(W2), _p(W_rnn), _p(_c(b_rnn, np.float32)),
+                             _p(_c(anchor, np.int32)), _p(ids), n, gamma, V, r, H,
+                             ctypes.c_uint64(seed), int(bool(greedy)), _p(tokens), _p(out["q_tok"]),
+                             _p(out["row_max"]), _p(out["row_sumexp"]), _p(out["gap"]), _p(E),
+                             _p(state), nthreads or default_threads())
+    _check(rc, "draft_rnn")
+    out.update(tokens=tokens, E=E, state=state)
+    return out
+
+
+def verify_rnn(T, U, E, W2, tokens, ell, seed: int, req_ids: Optional[Sequence[int]] = None,
+               nthreads: Optional[int] = None):
+    """Verification of an RNN-head draft (proposal softmax(U + E W2)); outputs as verify."""
+    T = _c(T, np.float32)
+    U = _c(U, np.float32)
+    n, gamma, V = U.shape
+    E = _c(E, np.float64)
+    r = E.shape[2]
+    W2 = _c(W2, np.uint16)
+    ids = _c(np.arange(n) if req_ids is None else req_ids, np.int32)
+    res = dict(accept_len=np.zeros(n, np.int32), out_tokens=np.zeros((n, gamma + 1), np.int32),
+               n_out=np.zeros(n, np.int32), band=np.zeros((n, gamma), np.float64),
+               gap=np.zeros(n, np.float64), fallback=np.zeros(n, np.int32))
+    rc = lib().dso_verify_rnn(_p(T), _p(U), _p(E), _p(W2), _p(_c(tokens, np.int32)),
+                              _p(_c(ell, np.int32)), _p(ids), n, gamma, V, r, ctypes.c_uint64(seed),
+                              _p(res["accept_len"]), _p(res["out_tokens"]), _p(res["n_out"]),
+                              _p(res["band"]), _p(res["gap"]), _p(res["fallback"]),
+                              nthreads or default_threads())
+    _check(rc, "verify_rnn")
+    return res
 
 
 def step(inp, seed: int, nthreads: Optional[int] = None):

@@ -29,7 +29,7 @@
  *               asynchronous two-step capacity scheduler (weigao.cc "4. hardware-aware
  *               prefix scheduler"; billytse.dev section 7); fixed confidence-threshold
  *               truncation (billytse.dev section 8; xhh.club page on load-dependent
- *               thresholds).
+ *               thresholds); the RNN head (weigao.cc "2. Markov head and RNN head").
  *
  * Readings where the pages are silent (the same list is kept with the design notes):
  *   - Random numbers: Philox4x32 with 7 rounds (Salmon, Moraes, Dror, Shaw, "Parallel
@@ -58,6 +58,9 @@
  *     the scheduler's order (a desc, r asc, j asc).
  *   - Threshold truncation: l_r is the leading run of positions with a[r, j] > threshold
  *     (strict, like the marginal rule of the adaptive scheduler).
+ *   - RNN head: state of r entries, token embedding = W1 row, gate = sigmoid, candidate =
+ *     tanh, s_0 = 0, one linear layer W_rnn [2r + H, 3r] (+ b_rnn) on [s; W1[prev]; h_k]
+ *     with column blocks (gate, candidate, output), E_k = tanh(output) unrounded.
  *
  * Parity pins live in tests/test_oracle_*.py.  Every function here is pinned there.
  */
@@ -139,17 +142,24 @@ static double bf16_to_double(uint16_t b)
 /* Draft: Markov bias, softmax, Gumbel-max                                               */
 /* ------------------------------------------------------------------------------------ */
 
-/* z_v = U[k][v] + sum_i W1[prev][i] * W2[i][v], all in double. */
-static void draft_logits(const float *U_row, const uint16_t *W1, const uint16_t *W2,
-                         int prev, int V, int r, double *z)
+/* z_v = U[k][v] + sum_i e[i] * W2[i][v], all in double; e is the head's output row
+ * (W1[prev] for the Markov head, tanh(output) for the RNN head). */
+static void draft_logits(const float *U_row, const double *erow, const uint16_t *W2,
+                         int V, int r, double *z)
 {
     for (int v = 0; v < V; ++v) z[v] = 0.0;
     for (int i = 0; i < r; ++i) {
-        double e = bf16_to_double(W1[(size_t)prev * r + i]);
+        double e = erow[i];
         const uint16_t *w2 = W2 + (size_t)i * V;
         for (int v = 0; v < V; ++v) z[v] += e * bf16_to_double(w2[v]);
     }
     for (int v = 0; v < V; ++v) z[v] += (double)U_row[v];
+}
+
+/* the bf16 row W1[prev] in double */
+static void markov_row(const uint16_t *W1, int prev, int r, double *e)
+{
+    for (int i = 0; i < r; ++i) e[i] = bf16_to_double(W1[(size_t)prev * r + i]);
 }
 
 static void softmax_stats(const double *z, int V, double *m_out, double *s_out)
@@ -205,13 +215,15 @@ int dso_draft(const float *U, const uint16_t *W1, const uint16_t *W2, const int3
 #endif
     for (int i = 0; i < n_req; ++i) {
         double *z = (double *)malloc(sizeof(double) * (size_t)V);
-        if (!z) { err = DSO_ERR_NOMEM; continue; }
+        double *e = (double *)malloc(sizeof(double) * (size_t)r);
+        if (!z || !e) { free(z); free(e); err = DSO_ERR_NOMEM; continue; }
         int b = req_ids[i];
         int prev = anchor[i];
         for (int k = 1; k <= gamma; ++k) {
             size_t o = (size_t)i * gamma + (k - 1);
             if (prev < 0 || prev >= V) { err = DSO_ERR_ARG; break; }
-            draft_logits(U + o * V, W1, W2, prev, V, r, z);
+            markov_row(W1, prev, r, e);
+            draft_logits(U + o * V, e, W2, V, r, z);
             double m, s;
             softmax_stats(z, V, &m, &s);
             double g;
@@ -224,6 +236,7 @@ int dso_draft(const float *U, const uint16_t *W1, const uint16_t *W2, const int3
             prev = x;
         }
         free(z);
+        free(e);
     }
     return err;
 }
@@ -248,12 +261,14 @@ int dso_draft_greedy(const float *U, const uint16_t *W1, const uint16_t *W2,
 #endif
     for (int i = 0; i < n_req; ++i) {
         double *z = (double *)malloc(sizeof(double) * (size_t)V);
-        if (!z) { err = DSO_ERR_NOMEM; continue; }
+        double *e = (double *)malloc(sizeof(double) * (size_t)r);
+        if (!z || !e) { free(z); free(e); err = DSO_ERR_NOMEM; continue; }
         int prev = anchor[i];
         for (int k = 1; k <= gamma; ++k) {
             size_t o = (size_t)i * gamma + (k - 1);
             if (prev < 0 || prev >= V) { err = DSO_ERR_ARG; break; }
-            draft_logits(U + o * V, W1, W2, prev, V, r, z);
+            markov_row(W1, prev, r, e);
+            draft_logits(U + o * V, e, W2, V, r, z);
             double m, s;
             softmax_stats(z, V, &m, &s);
             int x = 0;
@@ -274,6 +289,7 @@ int dso_draft_greedy(const float *U, const uint16_t *W1, const uint16_t *W2,
             prev = x;
         }
         free(z);
+        free(e);
     }
     return err;
 }
@@ -294,6 +310,118 @@ int dso_markov_bias(const uint16_t *W1, const uint16_t *W2, const int32_t *prev,
         }
     }
     return DSO_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* RNN head                                                                              */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * The hidden-state block of the RNN head's linear layer (weigao.cc DSpark-vs-MTP page,
+ * "2. Markov head and RNN head": one linear layer on [state; previous-token embedding;
+ * hidden state]; this block does not depend on the drafted tokens):
+ *   hp[i][c] = b_rnn[c] + sum_j h[i][j] * W_rnn[2r + j][c],   c < 3r
+ * h [n, H] fp32, W_rnn [2r + H, 3r] bf16, b_rnn [3r] fp32 -> hp [n, 3r] double.
+ */
+int dso_rnn_project(const float *h, const uint16_t *W_rnn, const float *b_rnn, int n, int H,
+                    int r, double *hp)
+{
+    if (n < 0 || H < 0 || r < 1) return DSO_ERR_ARG;
+    const int C = 3 * r;
+    for (int i = 0; i < n; ++i) {
+        double *o = hp + (size_t)i * C;
+        for (int c = 0; c < C; ++c) o[c] = (double)b_rnn[c];
+        for (int j = 0; j < H; ++j) {
+            double hv = (double)h[(size_t)i * H + j];
+            const uint16_t *w = W_rnn + (size_t)(2 * r + j) * C;
+            for (int c = 0; c < C; ++c) o[c] += hv * bf16_to_double(w[c]);
+        }
+    }
+    return DSO_OK;
+}
+
+/*
+ * Draft with the RNN head (weigao.cc page, "2. Markov head and RNN head"; billytse.dev
+ * section 3.3 names it as the head that remembers the whole block prefix).  For k = 1..gamma:
+ *   y = [s_{k-1}; W1[x_{k-1}]; h_k] W_rnn + b_rnn          (3r values; x_0 = the anchor)
+ *   gate = sigmoid(y[0:r]), cand = tanh(y[r:2r]), out = y[2r:3r]
+ *   s_k = gate * s_{k-1} + (1 - gate) * cand,  s_0 = 0
+ *   E_k = tanh(out),  z = U_k + E_k W2,  x_k drawn from softmax(z) as in dso_draft
+ *   (greedy = 1: x_k = argmax z as in dso_draft_greedy, q_tok = 1).
+ * Readings: the state has r entries (W2 [r, V] projects tanh(output)); the token embedding
+ * is the head's W1 row; gate = sigmoid and candidate = tanh of their blocks; s_0 = 0; the
+ * head computes in the precision of the rest of the path (no rounding of E).
+ * Outputs as dso_draft / dso_draft_greedy, plus E [n, gamma, r] (the projected rows) and
+ * state [n, r] (s_gamma).
+ */
+int dso_draft_rnn(const float *U, const float *h, const uint16_t *W1, const uint16_t *W2,
+                  const uint16_t *W_rnn, const float *b_rnn, const int32_t *anchor,
+                  const int32_t *req_ids, int n_req, int gamma, int V, int r, int H,
+                  uint64_t seed, int greedy, int32_t *tokens, double *q_tok, double *row_max,
+                  double *row_sumexp, double *gap, double *E, double *state, int nthreads)
+{
+    if (n_req < 0 || gamma < 1 || V < 1 || r < 1 || H < 0) return DSO_ERR_ARG;
+    const int C = 3 * r;
+    int err = DSO_OK;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int i = 0; i < n_req; ++i) {
+        double *z = (double *)malloc(sizeof(double) * (size_t)V);
+        double *y = (double *)malloc(sizeof(double) * (size_t)C);
+        double *st = (double *)calloc((size_t)r, sizeof(double));
+        if (!z || !y || !st) { free(z); free(y); free(st); err = DSO_ERR_NOMEM; continue; }
+        int b = req_ids[i];
+        int prev = anchor[i];
+        for (int k = 1; k <= gamma; ++k) {
+            size_t o = (size_t)i * gamma + (k - 1);
+            if (prev < 0 || prev >= V) { err = DSO_ERR_ARG; break; }
+            /* the linear layer on [s_{k-1}; W1[prev]; h_k] */
+            dso_rnn_project(h + o * H, W_rnn, b_rnn, 1, H, r, y);
+            for (int j = 0; j < r; ++j) {
+                const uint16_t *ws = W_rnn + (size_t)j * C;
+                const uint16_t *we = W_rnn + (size_t)(r + j) * C;
+                double sv = st[j];
+                double ev = bf16_to_double(W1[(size_t)prev * r + j]);
+                for (int c = 0; c < C; ++c)
+                    y[c] += sv * bf16_to_double(ws[c]) + ev * bf16_to_double(we[c]);
+            }
+            double *Erow = E + o * (size_t)r;
+            for (int j = 0; j < r; ++j) {
+                double gate = 1.0 / (1.0 + exp(-y[j]));
+                double cand = tanh(y[r + j]);
+                st[j] = gate * st[j] + (1.0 - gate) * cand;
+                Erow[j] = tanh(y[2 * r + j]);
+            }
+            draft_logits(U + o * V, Erow, W2, V, r, z);
+            double m, s;
+            softmax_stats(z, V, &m, &s);
+            int x;
+            double g;
+            if (greedy) {
+                x = 0;
+                double second = -INFINITY;
+                for (int v = 1; v < V; ++v) {
+                    if (z[v] > z[x]) { second = z[x]; x = v; }
+                    else if (z[v] > second) second = z[v];
+                }
+                g = z[x] - second;
+                q_tok[o] = 1.0;
+            } else {
+                x = gumbel_argmax(z, NULL, V, seed, b, k, 0, &g);
+                q_tok[o] = exp(z[x] - m) / s;
+            }
+            tokens[o] = x;
+            row_max[o] = m;
+            row_sumexp[o] = s;
+            gap[o] = g;
+            prev = x;
+        }
+        for (int j = 0; j < r; ++j) state[(size_t)i * r + j] = st[j];
+        free(z); free(y); free(st);
+    }
+    return err;
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -488,15 +616,16 @@ int dso_schedule_threshold(const float *a, int R, int gamma, float threshold, in
  * fallback [n_req] (1 when the residual was empty and P itself was sampled).
  *
  * point_mass = 0: the proposal of position k is Q_k = softmax(U[k] + W1[prev] W2), the
- * distribution the tokens were sampled from.  point_mass = 1: the tokens were drafted
+ * distribution the tokens were sampled from; with E_rows ([n_req, gamma, r], the RNN
+ * head's output rows tanh(output) of the draft) it is softmax(U[k] + E_rows[k] W2).  point_mass = 1: the tokens were drafted
  * greedily, so the proposal is the point mass at x_k (Q_k(v) = 1 if v = x_k, else 0) and
  * U, W1, W2 are not read.  The acceptance test and the residual are the same formulas
  * with that Q.
  */
 static int verify_impl(const float *T, const float *U, const uint16_t *W1, const uint16_t *W2,
-                       const int32_t *anchor, const int32_t *tokens, const int32_t *ell,
-                       const int32_t *req_ids, int n_req, int gamma, int V, int r,
-                       uint64_t seed, int point_mass, int32_t *accept_len,
+                       const double *E_rows, const int32_t *anchor, const int32_t *tokens,
+                       const int32_t *ell, const int32_t *req_ids, int n_req, int gamma, int V,
+                       int r, uint64_t seed, int point_mass, int32_t *accept_len,
                        int32_t *out_tokens, int32_t *n_out, double *band, double *gap,
                        int32_t *fallback, int nthreads)
 {
@@ -518,8 +647,9 @@ static int verify_impl(const float *T, const float *U, const uint16_t *W1, const
         double *Q = (double *)malloc(sizeof(double) * (size_t)V);
         double *score = (double *)malloc(sizeof(double) * (size_t)V);
         unsigned char *mask = (unsigned char *)malloc((size_t)V);
-        if (!z || !P || !Q || !score || !mask) {
-            free(z); free(P); free(Q); free(score); free(mask);
+        double *erow_m = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+        if (!z || !P || !Q || !score || !mask || !erow_m) {
+            free(z); free(P); free(Q); free(score); free(mask); free(erow_m);
             err = DSO_ERR_NOMEM;
             continue;
         }
@@ -539,7 +669,12 @@ static int verify_impl(const float *T, const float *U, const uint16_t *W1, const
             if (point_mass) {
                 for (int v = 0; v < V; ++v) Q[v] = (v == x) ? 1.0 : 0.0;
             } else {
-                draft_logits(U + o * V, W1, W2, prev, V, r, z);
+                const double *erow = erow_m;
+                if (E_rows)
+                    erow = E_rows + o * (size_t)r;
+                else
+                    markov_row(W1, prev, r, erow_m);
+                draft_logits(U + o * V, erow, W2, V, r, z);
                 double m, s;
                 softmax_stats(z, V, &m, &s);
                 for (int v = 0; v < V; ++v) Q[v] = exp(z[v] - m) / s;
@@ -593,7 +728,7 @@ static int verify_impl(const float *T, const float *U, const uint16_t *W1, const
             accept_len[i] = L;
             n_out[i] = L + 1;
         }
-        free(z); free(P); free(Q); free(score); free(mask);
+        free(z); free(P); free(Q); free(score); free(mask); free(erow_m);
     }
     return err;
 }
@@ -604,8 +739,8 @@ int dso_verify(const float *T, const float *U, const uint16_t *W1, const uint16_
                int32_t *accept_len, int32_t *out_tokens, int32_t *n_out, double *band,
                double *gap, int32_t *fallback, int nthreads)
 {
-    return verify_impl(T, U, W1, W2, anchor, tokens, ell, req_ids, n_req, gamma, V, r, seed, 0,
-                       accept_len, out_tokens, n_out, band, gap, fallback, nthreads);
+    return verify_impl(T, U, W1, W2, NULL, anchor, tokens, ell, req_ids, n_req, gamma, V, r, seed,
+                       0, accept_len, out_tokens, n_out, band, gap, fallback, nthreads);
 }
 
 /* Verification of greedily drafted tokens (proposal = point mass at each token). */
@@ -614,6 +749,18 @@ int dso_verify_greedy(const float *T, const int32_t *tokens, const int32_t *ell,
                       int32_t *accept_len, int32_t *out_tokens, int32_t *n_out, double *band,
                       double *gap, int32_t *fallback, int nthreads)
 {
-    return verify_impl(T, NULL, NULL, NULL, NULL, tokens, ell, req_ids, n_req, gamma, V, 0, seed,
-                       1, accept_len, out_tokens, n_out, band, gap, fallback, nthreads);
+    return verify_impl(T, NULL, NULL, NULL, NULL, NULL, tokens, ell, req_ids, n_req, gamma, V, 0,
+                       seed, 1, accept_len, out_tokens, n_out, band, gap, fallback, nthreads);
+}
+
+/* Verification of an RNN-head draft: Q_k = softmax(U[k] + E[k] W2), E from dso_draft_rnn. */
+int dso_verify_rnn(const float *T, const float *U, const double *E, const uint16_t *W2,
+                   const int32_t *tokens, const int32_t *ell, const int32_t *req_ids, int n_req,
+                   int gamma, int V, int r, uint64_t seed, int32_t *accept_len,
+                   int32_t *out_tokens, int32_t *n_out, double *band, double *gap,
+                   int32_t *fallback, int nthreads)
+{
+    if (!E) return DSO_ERR_ARG;
+    return verify_impl(T, U, NULL, W2, E, NULL, tokens, ell, req_ids, n_req, gamma, V, r, seed, 0,
+                       accept_len, out_tokens, n_out, band, gap, fallback, nthreads);
 }

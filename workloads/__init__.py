@@ -19,7 +19,10 @@ billytse.dev, section 3.1 "Parallel backbone" and section 3.3 "Markov head"):
   [h_k ; W1[prev]] followed by a sigmoid);
 * ``anchor`` [B] int32 -- the last committed token of each request;
 * ``sps`` [R*(gamma+1) + 1] fp32 -- the profiled steps-per-second curve SPS(B)
-  indexed by the integer token-batch size B.
+  indexed by the integer token-batch size B;
+* ``W_rnn`` [2r + H, 3r] bf16 and ``b_rnn`` [3r] fp32 (``gen_rnn_weights``) -- the RNN
+  head's one linear layer on [state ; previous-token embedding ; hidden state], its
+  output columns in three blocks (gate, candidate, output).
 
 The pages measure on live traffic and on datasets that are not available here;
 these seeded draws stand in for them.  Every request's rows come from their own
@@ -34,7 +37,7 @@ from typing import Callable, Dict, List, Optional, Sequence
 import numpy as np
 
 # random-stream identifiers, one per tensor
-_S_U, _S_T, _S_W1, _S_W2, _S_H, _S_WC, _S_ANCHOR = range(7)
+_S_U, _S_T, _S_W1, _S_W2, _S_H, _S_WC, _S_ANCHOR, _S_WRNN = range(8)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -159,6 +162,19 @@ def gen_weights(w: Workload):
                           * np.float32(w.w_std))
     w_c = (_rng(w.seed, _S_WC).standard_normal(w.H + w.r) / np.sqrt(w.H + w.r)).astype(np.float32)
     return W1, W2, w_c, np.float32(w.b_c)
+
+
+def gen_rnn_weights(w: Workload):
+    """W_rnn [2r + H, 3r] bf16 bits and b_rnn [3r] fp32 of the RNN head.
+
+    W_rnn ~ N(0, 1/(r + H)) so that a pre-activation, a sum over r state entries in
+    (-1, 1), r small embedding entries and H unit-variance hidden entries, is of order
+    one; the gate block's bias is +1 (the state is mostly kept), the other biases 0."""
+    rng = _rng(w.seed, _S_WRNN)
+    W = rng.standard_normal((2 * w.r + w.H, 3 * w.r), dtype=np.float32) * np.float32(1.0 / np.sqrt(w.r + w.H))
+    b = np.zeros(3 * w.r, dtype=np.float32)
+    b[:w.r] = 1.0
+    return f32_to_bf16_bits(W), b
 
 
 def gen_h(w: Workload, b: int) -> np.ndarray:
