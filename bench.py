@@ -313,9 +313,35 @@ def run_ours(args, w):
             entry["draft"] = {"ms_per_launch": gd_ms, "achieved_gbs": gd_ach}
         variants[f"{sampling}+{scheduler}"] = entry
         del vs
-    if args.graph:
-        run_step(0)            # back to the main step's outputs
-        barrier()
+    # the RNN head (its own weights; the step projects the hidden states first)
+    W_rnn, b_rnn = workloads.gen_rnn_weights(wr)
+    ds.rnn_to_device(W_rnn, b_rnn, dev, f"cuda:{local}")
+    vs = ds.Step(dev, float(inp.b_c), ws=step.ws, W2p=step.W2p, head="rnn")
+    for i in range(3):
+        vs.run(seed=w.seed + i)
+    ms = time_graphs(vs.capture([w.seed + j for j in range(n_ring)]), n_var)
+    vr = vs.results()
+    rd_ms = time_graphs(vs.capture([w.seed + j for j in range(n_ring)], draft_only=True), n_var)
+    # the projection and the RNN draft kernel alone, each in its own graphs
+    pg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pg):
+        for i in range(10):
+            ds.rnn_project(x["h"], dev["W_rnn"], dev["b_rnn"], vs.hp)
+    proj_ms = time_graphs([pg], max(1, n_var // 10)) / 10
+    dgs = []
+    for j in range(n_ring):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ds.draft_rnn(x["U"], x["W1"], step.W2p, vs.Wrec, vs.hp, x["anchor"], w.seed + j, step.ws,
+                         packed=True, out=vs.draft_out)
+        dgs.append(g)
+    dk_ms = time_graphs(dgs, n_var)
+    variants["gumbel+theta+rnn_head"] = {
+        "ms_per_step": ms, "value": world * w.B * w.gamma / (ms * 1e-3),
+        "mean_ell": float(np.mean(vr["ell"])), "mean_accept_len": float(np.mean(vr["accept_len"])),
+        "B_total": vr["B_total"],
+        "draft": {"ms_per_call": rd_ms, "project_ms": proj_ms, "draft_kernel_ms": dk_ms}}
+    del vs
 
     # ---- per-call breakdown (warm, eager, events between the calls on one stream)
     n_bd = max(3, min(args.steps, 20))

@@ -309,6 +309,52 @@ dspark_status dspark_schedule_threshold(const float* a, int R, int gamma, float 
                                         int32_t* ell, int32_t* B_total, cudaStream_t stream);
 
 /*
+ * RNN head.  weigao.cc DSpark-vs-MTP page, "2. Markov head and RNN head": the head keeps a
+ * recurrent state inside the draft block; each step concatenates the previous state, the
+ * previous token's embedding and the position's hidden state, one linear layer splits the
+ * result into gate, candidate and output, state_k = gate * state_{k-1} + (1 - gate) *
+ * candidate, and the bias is W2 tanh(output) (billytse.dev section 3.3: the head that lets
+ * every position remember the whole block prefix).  Readings: the state has r entries;
+ * the token embedding is the W1 row; gate = sigmoid, candidate = tanh of their blocks;
+ * state_0 = 0; the layer is W_rnn [2r + H, 3r] bf16 + b_rnn [3r] fp32, rows [0, r) for the
+ * state, [r, 2r) for W1[prev], [2r, 2r + H) for h_k, column blocks gate | candidate |
+ * output; the head computes in fp32, and its output rows E_k = tanh(output) enter the
+ * tensor-core contraction as two bf16 terms (hi + lo, |E - hi - lo| <= 2^-18 |E|).
+ *
+ *   dspark_rnn_packed_bytes(r): bytes of the transposed recurrent rows (3r * 2r * 2); 0 on
+ *   an unsupported r.
+ *   dspark_rnn_pack: Wrec[c][j] = W_rnn[j][c] for c < 3r, j < 2r (caller-owned, 16-byte
+ *   aligned; once per weights).
+ *   dspark_rnn_project: hp[b, k, c] = b_rnn[c] + sum_j h[b, k, j] W_rnn[2r + j][c] for every
+ *   (b, k) -- the part of the layer that does not depend on drafted tokens.  h [B, gamma, H]
+ *   fp32 (H % 4 == 0), hp [B, gamma, 3r] fp32; all 16-byte aligned.
+ *   dspark_draft_rnn: dspark_draft (greedy == 0) or dspark_draft_greedy (greedy != 0) with
+ *   the RNN head's bias in place of the Markov bias: exactly one of W2 and W2p non-NULL,
+ *   Wrec from dspark_rnn_pack, hp from dspark_rnn_project.  Also writes E [B, gamma, r]
+ *   fp32, the output rows tanh(output) (16-byte aligned), which dspark_verify_rnn needs.
+ *   dspark_verify_rnn: dspark_verify for a Gumbel-sampled RNN draft: the residual's
+ *   proposal is Q_j = softmax(U[b, j] + E[b, j] W2); W1 and the anchors are not needed.
+ *   (A greedy RNN draft is verified with dspark_verify_greedy.)
+ */
+size_t dspark_rnn_packed_bytes(int r);
+dspark_status dspark_rnn_pack(const uint16_t* W_rnn, int r, uint16_t* Wrec, size_t Wrec_bytes,
+                              cudaStream_t stream);
+dspark_status dspark_rnn_project(const float* h, const uint16_t* W_rnn, const float* b_rnn,
+                                 int B, int gamma, int H, int r, float* hp, cudaStream_t stream);
+dspark_status dspark_draft_rnn(const float* U, const uint16_t* W1, const uint16_t* W2,
+                               const uint16_t* W2p, const uint16_t* Wrec, const float* hp,
+                               const int32_t* anchor, int B, int gamma, int V, int r,
+                               uint64_t seed, int greedy, int32_t* tokens, float* q_tok,
+                               float* row_max, float* row_sumexp, float* E, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+dspark_status dspark_verify_rnn(const float* T, const float* U, const float* E, const uint16_t* W2,
+                                const uint16_t* W2p, const int32_t* tokens, const float* q_tok,
+                                const float* row_max, const float* row_sumexp, const int32_t* ell,
+                                int B, int gamma, int V, int r, uint64_t seed,
+                                int32_t* accept_len, int32_t* out_tokens, int32_t* n_out,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word kept in `workspace` after synchronising
  * `stream`.  Returns DSPARK_OK, or the first device-side failure recorded since the last
  * read (DSPARK_ERR_DEVICE_CHECK, DSPARK_ERR_TIMEOUT), or DSPARK_ERR_CUDA.

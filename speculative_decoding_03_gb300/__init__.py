@@ -4,7 +4,7 @@ The library behind this binding (``include/dspark.h``) holds the four calls of o
 speculative step -- ``dspark_draft``, ``dspark_confidence``, ``dspark_schedule``,
 ``dspark_verify`` -- plus ``dspark_markov_bias``, the packed-W2 variants of the draft and
 the verification, greedy drafting with its verification, the asynchronous two-step
-capacity scheduler and fixed-threshold truncation; every step of the computation runs in
+capacity scheduler, fixed-threshold truncation and the RNN head; every step of the computation runs in
 its CUDA kernels.  This module only marshals arguments: it passes device pointers of
 torch tensors and the current CUDA stream through ctypes, and allocates outputs and the
 workspace with torch.  There is no CPU fallback: without the built library and a CUDA
@@ -44,6 +44,13 @@ SIGNATURES = [
     ("dspark_verify_greedy", _I, [_P, _P, _P, _I, _I, _I, _U64, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_schedule_async", _I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_schedule_threshold", _I, [_P, _I, _I, _F, _P, _P, _P]),
+    ("dspark_rnn_packed_bytes", _SZ, [_I]),
+    ("dspark_rnn_pack", _I, [_P, _I, _P, _SZ, _P]),
+    ("dspark_rnn_project", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    ("dspark_draft_rnn", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64, _I, _P, _P, _P, _P,
+                              _P, _P, _SZ, _P]),
+    ("dspark_verify_rnn", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P,
+                               _P, _P, _SZ, _P]),
     ("dspark_last_device_status", _I, [_P, _P]),
 ]
 
@@ -338,6 +345,64 @@ def schedule_threshold(a, threshold: float, out=None, stream=None):
     return ell, Bt
 
 
+def rnn_pack(W_rnn, r: int, stream=None):
+    """Transposed recurrent rows of the RNN head's layer (once per weights)."""
+    torch = _torch()
+    n = lib().dspark_rnn_packed_bytes(r)
+    if n == 0:
+        raise ValueError(f"unsupported rank r={r}")
+    Wrec = torch.empty(n // 2, dtype=torch.bfloat16, device=W_rnn.device)
+    _check("dspark_rnn_pack", lib().dspark_rnn_pack(_ptr(W_rnn), r, _ptr(Wrec), n, _stream(stream)))
+    return Wrec
+
+
+def rnn_project(h, W_rnn, b_rnn, out=None, stream=None):
+    """hp [B, gamma, 3r] = h W_rnn[2r:] + b_rnn (the token-independent part of the layer)."""
+    torch = _torch()
+    B, gamma, H = h.shape
+    r = W_rnn.shape[1] // 3
+    if out is None:
+        out = torch.empty((B, gamma, 3 * r), dtype=torch.float32, device=h.device)
+    _check("dspark_rnn_project", lib().dspark_rnn_project(
+        _ptr(h), _ptr(W_rnn), _ptr(b_rnn), B, gamma, H, r, _ptr(out), _stream(stream)))
+    return out
+
+
+def draft_rnn(U, W1, W2, Wrec, hp, anchor, seed: int, ws: Workspace, greedy: bool = False,
+              packed: bool = False, out: Optional[Dict] = None, stream=None):
+    """Draft with the RNN head; ``out`` also gets ``E`` [B, gamma, r] (tanh(output) rows)."""
+    torch = _torch()
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    if out is None:
+        out = _draft_outputs(B, gamma, U.device)
+    if "E" not in out:
+        out["E"] = torch.empty((B, gamma, r), dtype=torch.float32, device=U.device)
+    w2, w2p = (None, W2) if packed else (W2, None)
+    _check("dspark_draft_rnn", lib().dspark_draft_rnn(
+        _ptr(U), _ptr(W1), None if w2 is None else _ptr(w2), None if w2p is None else _ptr(w2p),
+        _ptr(Wrec), _ptr(hp), _ptr(anchor), B, gamma, V, r, ctypes.c_uint64(seed), int(bool(greedy)),
+        _ptr(out["tokens"]), _ptr(out["q_tok"]), _ptr(out["row_max"]), _ptr(out["row_sumexp"]),
+        _ptr(out["E"]), ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
+def verify_rnn(T, U, E, W2, tokens, q_tok, row_max, row_sumexp, ell, seed: int, ws: Workspace,
+               packed: bool = False, out: Optional[Dict] = None, stream=None):
+    """Verification of a Gumbel-sampled RNN draft (``E`` from draft_rnn)."""
+    B, gamma, V = U.shape
+    r = E.shape[2]
+    if out is None:
+        out = _verify_outputs(B, gamma, U.device)
+    w2, w2p = (None, W2) if packed else (W2, None)
+    _check("dspark_verify_rnn", lib().dspark_verify_rnn(
+        _ptr(T), _ptr(U), _ptr(E), None if w2 is None else _ptr(w2), None if w2p is None else _ptr(w2p),
+        _ptr(tokens), _ptr(q_tok), _ptr(row_max), _ptr(row_sumexp), _ptr(ell), B, gamma, V, r,
+        ctypes.c_uint64(seed), _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["n_out"]),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return out
+
+
 # ------------------------------------------------------------------------ whole step
 
 class Step:
@@ -347,19 +412,22 @@ class Step:
     tensors; ``b_c`` is the confidence-head bias.
 
     ``sampling``: "gumbel" (the draft samples from q_k) or "greedy" (argmax drafts, verified
-    as point-mass proposals).  ``scheduler``: "theta" (the early-stop scheduler), "async"
+    as point-mass proposals).  ``head``: "markov" or "rnn" (``dev`` then also holds W_rnn
+    and b_rnn; each step first projects the hidden states).  ``scheduler``: "theta" (the early-stop scheduler), "async"
     (the two-step capacity scheduler; ``run(seed, t=...)`` picks the ring slot of step t)
     or "threshold" (fixed truncation at ``threshold``)."""
 
     SAMPLING = ("gumbel", "greedy")
+    HEADS = ("markov", "rnn")
     SCHEDULERS = ("theta", "async", "threshold")
 
     def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None, packed: bool = True,
                  sampling: str = "gumbel", scheduler: str = "theta", threshold: float = 0.5,
-                 W2p=None):
+                 W2p=None, head: str = "markov"):
         torch = _torch()
-        if sampling not in self.SAMPLING or scheduler not in self.SCHEDULERS:
-            raise ValueError(f"sampling {sampling!r} / scheduler {scheduler!r}")
+        if sampling not in self.SAMPLING or scheduler not in self.SCHEDULERS or head not in self.HEADS:
+            raise ValueError(f"sampling {sampling!r} / scheduler {scheduler!r} / head {head!r}")
+        self.head = head
         self.sampling, self.scheduler, self.threshold = sampling, scheduler, float(threshold)
         self.dev = dev
         # the draft streams W2 from a packed copy made once here (weight preparation), or
@@ -385,6 +453,10 @@ class Step:
                                out_tokens=torch.empty((B, gamma + 1), dtype=i32, device=d),
                                n_out=torch.empty(B, dtype=i32, device=d))
         self.ring = CapacityRing(d) if scheduler == "async" else None
+        if head == "rnn":
+            self.Wrec = rnn_pack(dev["W_rnn"], r)
+            self.hp = torch.empty((B, gamma, 3 * r), dtype=f32, device=d)
+            self.draft_out["E"] = torch.empty((B, gamma, r), dtype=f32, device=d)
 
     def run(self, seed: int, stream=None, t: int = 0):
         x = self.dev
@@ -394,6 +466,11 @@ class Step:
         ell = self._schedule(a, stream, t)
         if self.sampling == "greedy":
             verify_greedy(x["T"], d["tokens"], ell, seed, self.ws, self.verify_out, stream)
+        elif self.head == "rnn":
+            packed = self.W2p is not None
+            verify_rnn(x["T"], x["U"], d["E"], self.W2p if packed else x["W2"], d["tokens"],
+                       d["q_tok"], d["row_max"], d["row_sumexp"], ell, seed, self.ws, packed,
+                       self.verify_out, stream)
         elif self.W2p is not None:
             verify_packed(x["T"], x["U"], x["W1"], self.W2p, x["anchor"], d["tokens"], d["q_tok"],
                           d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
@@ -405,6 +482,12 @@ class Step:
     def draft(self, seed: int, stream=None):
         """The draft call of the step alone (into the step's draft outputs)."""
         x = self.dev
+        if self.head == "rnn":
+            rnn_project(x["h"], x["W_rnn"], x["b_rnn"], self.hp, stream)
+            packed = self.W2p is not None
+            return draft_rnn(x["U"], x["W1"], self.W2p if packed else x["W2"], self.Wrec, self.hp,
+                             x["anchor"], seed, self.ws, self.sampling == "greedy", packed,
+                             self.draft_out, stream)
         if self.sampling == "greedy":
             w2, packed = (self.W2p, True) if self.W2p is not None else (x["W2"], False)
             return draft_greedy(x["U"], x["W1"], w2, x["anchor"], self.ws, self.draft_out, packed,
@@ -475,6 +558,8 @@ class Step:
 
     def results(self) -> Dict[str, np.ndarray]:
         out = {k: v.cpu().numpy() for k, v in self.draft_out.items()}
+        if self.head == "rnn":
+            out["hp"] = self.hp.cpu().numpy()
         out["c"], out["a"] = (t.cpu().numpy() for t in self.conf_out)
         out["ell"] = self.sched_out[0].cpu().numpy()
         out["B_total"] = int(self.sched_out[1].item())
@@ -494,4 +579,12 @@ def to_device(inp, device="cuda") -> Dict:
                sps=torch.from_numpy(inp.sps).to(device))
     if inp.T is not None:
         dev["T"] = torch.from_numpy(inp.T).to(device)
+    return dev
+
+
+def rnn_to_device(W_rnn, b_rnn, dev: Dict, device="cuda") -> Dict:
+    """Add the RNN head's weights (numpy bf16 bits and fp32) to a device input dict."""
+    torch = _torch()
+    dev["W_rnn"] = as_bf16_tensor(W_rnn, device)
+    dev["b_rnn"] = torch.from_numpy(np.ascontiguousarray(b_rnn, dtype=np.float32)).to(device)
     return dev

@@ -179,8 +179,8 @@ dspark_status dspark_verify_greedy(const float* T, const int32_t* tokens, const 
     return DSPARK_ERR_INVALID_ARG;
   const Plan p = make_plan(B, gamma, V, 16, 0);
   if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
-  if (launch_verify(p, T, nullptr, nullptr, nullptr, nullptr, nullptr, tokens, nullptr, nullptr,
-                    nullptr, ell, seed, accept_len, out_tokens, n_out, workspace, stream) !=
+  if (launch_verify(p, T, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, tokens, nullptr,
+                    nullptr, nullptr, ell, seed, accept_len, out_tokens, n_out, workspace, stream) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
@@ -206,8 +206,8 @@ dspark_status verify_common(const float* T, const float* U, const uint16_t* W1, 
     return DSPARK_ERR_INVALID_ARG;
   const Plan p = make_plan(B, gamma, V, r, 0);
   if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
-  if (launch_verify(p, T, U, W1, W2, W2p, anchor, tokens, q_tok, row_max, row_sumexp, ell, seed,
-                    accept_len, out_tokens, n_out, workspace, stream) != cudaSuccess)
+  if (launch_verify(p, T, U, W1, W2, W2p, nullptr, anchor, tokens, q_tok, row_max, row_sumexp, ell,
+                    seed, accept_len, out_tokens, n_out, workspace, stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
@@ -240,6 +240,82 @@ dspark_status dspark_verify_packed(const float* T, const float* U, const uint16_
   return verify_common(T, U, W1, nullptr, W2p, anchor, tokens, q_tok, row_max, row_sumexp, ell, B,
                        gamma, V, r, seed, accept_len, out_tokens, n_out, workspace,
                        workspace_bytes, stream);
+}
+
+size_t dspark_rnn_packed_bytes(int r) {
+  if (r < 16 || r > 256 || r % 16 != 0) return 0;
+  return (size_t)3 * r * 2 * r * sizeof(uint16_t);
+}
+
+dspark_status dspark_rnn_pack(const uint16_t* W_rnn, int r, uint16_t* Wrec, size_t Wrec_bytes,
+                              cudaStream_t stream) {
+  const size_t need = dspark_rnn_packed_bytes(r);
+  if (need == 0) return DSPARK_ERR_UNSUPPORTED;
+  if (!aligned(W_rnn, 16) || !aligned(Wrec, 16) || Wrec_bytes < need) return DSPARK_ERR_INVALID_ARG;
+  if (launch_rnn_pack(W_rnn, r, Wrec, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_rnn_project(const float* h, const uint16_t* W_rnn, const float* b_rnn,
+                                 int B, int gamma, int H, int r, float* hp, cudaStream_t stream) {
+  if (B < 1 || gamma < 1 || H < 1) return DSPARK_ERR_INVALID_ARG;
+  if (r < 16 || r > 256 || r % 16 != 0 || H % 4 != 0 || gamma > 32 || B >= 65536)
+    return DSPARK_ERR_UNSUPPORTED;
+  if (!aligned(h, 16) || !aligned(W_rnn, 16) || !aligned(b_rnn, 16) || !aligned(hp, 16))
+    return DSPARK_ERR_INVALID_ARG;
+  if (launch_rnn_project(h, W_rnn, b_rnn, B * gamma, H, r, hp, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_draft_rnn(const float* U, const uint16_t* W1, const uint16_t* W2,
+                               const uint16_t* W2p, const uint16_t* Wrec, const float* hp,
+                               const int32_t* anchor, int B, int gamma, int V, int r,
+                               uint64_t seed, int greedy, int32_t* tokens, float* q_tok,
+                               float* row_max, float* row_sumexp, float* E, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  if ((W2 == nullptr) == (W2p == nullptr)) return DSPARK_ERR_INVALID_ARG;
+  dspark_status st = check_shape(B, gamma, V, r, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2 ? W2 : W2p, 16) || !aligned(Wrec, 16) ||
+      !aligned(hp, 16) || !aligned(E, 16) || !aligned(anchor, 4) || !aligned(tokens, 4) ||
+      !aligned(q_tok, 4) || !aligned(row_max, 4) || !aligned(row_sumexp, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  const Plan p = make_plan(B, gamma, V, r, 0);
+  if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
+  RnnDraftArgs rnn;
+  rnn.Wrec = Wrec;
+  rnn.hp = hp;
+  rnn.E_all = E;
+  rnn.state = ws_at<float>(workspace, p.off_rnn_state);
+  rnn.E_hl = reinterpret_cast<uint16_t*>(rnn.state + (size_t)2 * B * r);
+  if (launch_draft_fused_rnn(W1, W2, W2p, U, anchor, B, gamma, V, r, seed, greedy != 0, rnn, tokens,
+                             q_tok, row_max, row_sumexp, ws_at<char>(workspace, p.off_draft),
+                             ws_at<int>(workspace, p.off_err), stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_verify_rnn(const float* T, const float* U, const float* E, const uint16_t* W2,
+                                const uint16_t* W2p, const int32_t* tokens, const float* q_tok,
+                                const float* row_max, const float* row_sumexp, const int32_t* ell,
+                                int B, int gamma, int V, int r, uint64_t seed,
+                                int32_t* accept_len, int32_t* out_tokens, int32_t* n_out,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if ((W2 == nullptr) == (W2p == nullptr)) return DSPARK_ERR_INVALID_ARG;
+  dspark_status st = check_shape(B, gamma, V, r, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(T, 16) || !aligned(U, 16) || !aligned(E, 16) || !aligned(W2 ? W2 : W2p, 16) ||
+      !aligned(tokens, 4) || !aligned(q_tok, 4) || !aligned(row_max, 4) ||
+      !aligned(row_sumexp, 4) || !aligned(ell, 4) || !aligned(accept_len, 4) ||
+      !aligned(out_tokens, 4) || !aligned(n_out, 4))
+    return DSPARK_ERR_INVALID_ARG;
+  const Plan p = make_plan(B, gamma, V, r, 0);
+  if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
+  if (launch_verify(p, T, U, nullptr, W2, W2p, E, nullptr, tokens, q_tok, row_max, row_sumexp, ell,
+                    seed, accept_len, out_tokens, n_out, workspace, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
 }
 
 dspark_status dspark_last_device_status(void* workspace, cudaStream_t stream) {

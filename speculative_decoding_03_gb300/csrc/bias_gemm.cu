@@ -17,6 +17,11 @@
 //                   coalesced 128-byte stores of bias[b][v].
 // The producer starts on W2 (an input) before the previous kernel on the stream has
 // finished; the epilogue warps wait for it before reading prev.
+//
+// Split mode (the RNN head's verification): E[b] = Ef[prev_b], fp32 rows of a table of
+// table_rows rows; each row enters the contraction as two bf16 images, hi = bf16(E) and
+// lo = bf16(E - hi), and every K step issues one MMA per image on the same W2 rows, so
+// the bias keeps fp32-level accuracy (|E - hi - lo| <= 2^-18 |E|).
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -40,20 +45,28 @@ constexpr int kBiasDepth = 4;                 // accumulators in tensor memory
 constexpr int kBiasKChunkMax = 64;
 constexpr int kBiasNamedBar = 1;              // the epilogue warps' barrier
 
+template <bool Split>
 struct BiasSmem {
   static constexpr int kStageBytes = 2 * kBiasKChunkMax * 128;
   static constexpr int kOffW = 0;
   static constexpr int kOffE = kOffW + kBiasStages * kStageBytes;
-  static constexpr int kEBytes = 32 * 256 * 2;   // NB <= 32 requests x r <= 256
+  static constexpr int kEHalf = 32 * 256 * 2;    // NB <= 32 requests x r <= 256, one image
+  static constexpr int kEBytes = (Split ? 2 : 1) * kEHalf;
   static constexpr int kBytes = kOffE + 2 * kEBytes;
 };
 
-template <int NB>
+__device__ __forceinline__ uint32_t bf16_bits_rne(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+template <int NB, bool Split>
 __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
     const __grid_constant__ CUtensorMap w2_map, const uint16_t* __restrict__ W2p,
-    const uint16_t* __restrict__ W1, const int32_t* __restrict__ prev, int prev_stride, int B,
-    int V, int r, int kc, int n_tiles, float* __restrict__ out, int* err) {
-  using S = BiasSmem;
+    const uint16_t* __restrict__ W1, const float* __restrict__ Ef, int table_rows,
+    const int32_t* __restrict__ prev, int prev_stride, int B, int V, int r, int kc, int n_tiles,
+    float* __restrict__ out, int* err) {
+  using S = BiasSmem<Split>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t w_full[kBiasStages], w_empty[kBiasStages];
   __shared__ uint64_t e_full[2], e_empty[2];
@@ -170,6 +183,7 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
               const uint64_t ad = a_s + (uint64_t)(kk * (2048 >> 4));
               const uint64_t bd = b_base + (uint64_t)((kg >> 2) * (uint32_t)(NB * 128 / 16) + (kg & 3) * 2u);
               umma_bf16_f32(d_tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+              if constexpr (Split) umma_bf16_f32(d_tmem, ad, bd + (uint64_t)(S::kEHalf >> 4), idesc, 1u);
             }
             umma_commit(&w_empty[s]);
           }
@@ -208,17 +222,34 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
         for (int idx = et; idx < NB * kchunks; idx += 128) {
           const int n = idx / kchunks, c = idx - n * kchunks;
           const int b = b0 + n;
-          uint4 val = make_uint4(0u, 0u, 0u, 0u);
+          uint4 val = make_uint4(0u, 0u, 0u, 0u), lo = val;
           if (b < B) {
             const int pv = prev[(size_t)b * prev_stride];
-            if (pv >= 0 && pv < V) {
-              val = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)pv * r) + c);
+            if (pv >= 0 && pv < table_rows) {
+              if constexpr (Split) {
+                const float4* src = reinterpret_cast<const float4*>(Ef + (size_t)pv * r) + 2 * c;
+                const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                uint32_t hb[8], lb[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  hb[e] = bf16_bits_rne(x[e]);
+                  lb[e] = bf16_bits_rne(x[e] - __uint_as_float(hb[e] << 16));
+                }
+                val = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
+                                 hb[6] | (hb[7] << 16));
+                lo = make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16),
+                                lb[6] | (lb[7] << 16));
+              } else {
+                val = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)pv * r) + c);
+              }
             } else if (pv != -1) {
               set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
             }
           }
-          *reinterpret_cast<uint4*>(sE + (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 +
-                                    (((c & 7) ^ (n & 7)) << 4)) = val;
+          const size_t off = (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 + (((c & 7) ^ (n & 7)) << 4);
+          *reinterpret_cast<uint4*>(sE + off) = val;
+          if constexpr (Split) *reinterpret_cast<uint4*>(sE + S::kEHalf + off) = lo;
         }
       }
       fence_proxy_async_smem();
@@ -252,17 +283,17 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
   if (warp == 1) tmem_dealloc(tmem_base, tmem_cols);
 }
 
-template <int NB>
+template <int NB, bool Split>
 int bias_grid(int n_tiles) {
   static int per_sm = -1, sms = 0;
   if (per_sm < 0) {
     int dev = 0, per = 0;
-    const size_t smem = BiasSmem::kBytes + 1024;
+    const size_t smem = BiasSmem<Split>::kBytes + 1024;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(bias_gemm_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(bias_gemm_kernel<NB, Split>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_gemm_kernel<NB>, kBiasThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_gemm_kernel<NB, Split>, kBiasThreads,
                                                       smem) != cudaSuccess)
       return 0;
     per_sm = per;
@@ -301,25 +332,45 @@ bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_r
   return res == CUDA_SUCCESS;
 }
 
-cudaError_t launch_bias_gemm(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
-                             const int32_t* prev, int prev_stride, int B, int V, int r, float* out,
-                             int* err, cudaStream_t stream) {
+namespace {
+template <bool Split>
+cudaError_t launch_bias_common(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
+                               const float* Ef, int table_rows, const int32_t* prev,
+                               int prev_stride, int B, int V, int r, float* out, int* err,
+                               cudaStream_t stream) {
   const int kc = draft_kchunk(r);
   CUtensorMap w2_map;
   memset(&w2_map, 0, sizeof(w2_map));
   if (!W2p && !encode_w2_map(&w2_map, W2, V, r, kc)) return cudaErrorInvalidValue;
   const int n_tiles = cdiv(V, kGemmTileV);
-  const size_t smem = BiasSmem::kBytes + 1024;
+  const size_t smem = BiasSmem<Split>::kBytes + 1024;
   if (B <= 16) {
-    const int grid = bias_grid<16>(n_tiles);
+    const int grid = bias_grid<16, Split>(n_tiles);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
-    return launch_pdl(bias_gemm_kernel<16>, dim3(grid), dim3(kBiasThreads), smem, stream, w2_map,
-                      W2p, W1, prev, prev_stride, B, V, r, kc, n_tiles, out, err);
+    return launch_pdl(bias_gemm_kernel<16, Split>, dim3(grid), dim3(kBiasThreads), smem, stream,
+                      w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, V, r, kc, n_tiles,
+                      out, err);
   }
-  const int grid = bias_grid<32>(n_tiles);
+  const int grid = bias_grid<32, Split>(n_tiles);
   if (grid <= 0) return cudaErrorInvalidConfiguration;
-  return launch_pdl(bias_gemm_kernel<32>, dim3(grid), dim3(kBiasThreads), smem, stream, w2_map,
-                    W2p, W1, prev, prev_stride, B, V, r, kc, n_tiles, out, err);
+  return launch_pdl(bias_gemm_kernel<32, Split>, dim3(grid), dim3(kBiasThreads), smem, stream,
+                    w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, V, r, kc, n_tiles, out,
+                    err);
+}
+}  // namespace
+
+cudaError_t launch_bias_gemm(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
+                             const int32_t* prev, int prev_stride, int B, int V, int r, float* out,
+                             int* err, cudaStream_t stream) {
+  return launch_bias_common<false>(W2, W2p, W1, nullptr, V, prev, prev_stride, B, V, r, out, err,
+                                   stream);
+}
+
+cudaError_t launch_bias_gemm_rows(const uint16_t* W2, const uint16_t* W2p, const float* Ef,
+                                  int table_rows, const int32_t* prev, int B, int V, int r,
+                                  float* out, int* err, cudaStream_t stream) {
+  return launch_bias_common<true>(W2, W2p, nullptr, Ef, table_rows, prev, 1, B, V, r, out, err,
+                                  stream);
 }
 
 }  // namespace dspark

@@ -65,8 +65,7 @@ constexpr int kUProducerWarp = 22;    // U tiles
 constexpr int kSamplers = 16;
 constexpr int kSamplerThreads = kSamplers * 32;
 constexpr int kWStages = 4;           // W2 K-chunk ring (16 KB each at K-chunk 64)
-constexpr int kDepth = 4;             // accumulators in TMEM, z tiles and U tiles in flight
-constexpr int kUStages = kDepth;      // U tile ring (consumed by the samplers)
+constexpr int kDepthMarkov = 4;       // accumulators in TMEM, z tiles and U tiles in flight
 constexpr int kKChunkMax = 64;
 constexpr int kNamedBarSamplers = 1;
 constexpr int kGatherWarps = 4;       // sampler warps 0..3 also gather E
@@ -102,13 +101,27 @@ struct DraftParams {
   float* row_max;
   float* row_sumexp;
   int* err;
+  // RNN head (unused by the Markov head)
+  const uint16_t* Wrec;            // [3r][2r] the recurrent rows of W_rnn, transposed
+  const float* hp;                 // [B][gamma][3r] hidden-state block of the layer, with bias
+  float* E_all;                    // [B][gamma][r] tanh(output) of every position (written)
+  uint16_t* E_hl;                  // [B][2][r] the current position's rows as bf16 hi and lo
+  float* state;                    // [2][B][r] s_{k-1} / s_k
+  unsigned int* rec_count;         // arrivals of the recurrence CTAs
+  int n_rec, dpc;                  // recurrence CTAs, state entries per recurrence CTA
 };
 
-template <int NB>
+// Shared-memory layout.  The RNN head's E operand has 2 NB rows (the hi and the lo bf16
+// image of each request's row, see the MMA issue loop), so it takes one accumulator / z
+// tile / U tile less in flight.
+template <int NB, bool Rnn>
 struct Smem {
+  static constexpr int kDepth = Rnn ? 3 : kDepthMarkov;
+  static constexpr int kUStages = kDepth;
   static constexpr int kWStageBytes = 2 * kKChunkMax * 128;  // two 64-column boxes
   static constexpr int kUStageBytes = NB * 128 * 4;
-  static constexpr int kEBytes = NB * 256 * 2;                // up to r = 256
+  static constexpr int kNE = Rnn ? 2 * NB : NB;               // rows of the E operand (MMA N)
+  static constexpr int kEBytes = kNE * 256 * 2;               // up to r = 256
   static constexpr int kZBytes = NB * 128 * 4;
   static constexpr int kOffW = 0;
   static constexpr int kOffU = kOffW + kWStages * kWStageBytes;
@@ -165,6 +178,198 @@ __device__ __forceinline__ int token_of_key(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
 
+// bf16 bits of a finite float, rounded to nearest even
+__device__ __forceinline__ uint32_t bf16_rne(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+__device__ __forceinline__ float bf16_val(uint32_t b) { return __uint_as_float(b << 16); }
+
+// One step of the RNN head for state entries [d0, d0 + dpc) of every request, by the 16
+// sampler warps of a recurrence CTA, which run it between the end of position k-1's tiles
+// and the publication of E_k: the CTA's z-tile buffers are idle then (the samplers have
+// consumed position k-1's tiles and nothing is transposed before E_k exists), so the gate,
+// candidate and output rows of Wrec for the CTA's entries are staged there, in rounds of
+// as many entries as fit.  An item is one (entry, request b); warp w takes items w, w + 16,
+// ...  Lane l holds L = 2r / 32 consecutive entries of [s_{k-1}[b] ; W1[x_{k-1}]] (lanes
+// 0-15 the state, 16-31 the embedding).  The predecessor tokens of four items are loaded
+// together with the staging, and each item's loads (x, and for lane 0 the hidden-state
+// block hp and s_{k-1}[b][i]) are issued one item ahead.  A warp reduction gives the
+// three pre-activations; lane 0 writes s_k[b][i], E_k[b][i] = tanh(output) and E_k's two
+// bf16 terms hi = bf16(E), lo = bf16(E - hi) for the tensor-core operand.  Everything
+// other CTAs wrote in this call (the state, the argmax keys) is read through L2.
+constexpr int kRnnMaxL = 16;           // 2r / 32 for r <= 256
+constexpr int kRnnBatch = 4;           // predecessor tokens loaded together
+
+struct RnnOperands {
+  float x[kRnnMaxL];
+  float hg, hc, ho, sold;
+};
+
+__device__ __forceinline__ void rnn_load(const DraftParams& p, int k, int i, int b, int prev,
+                                         int lane, int L, bool vec, RnnOperands& o) {
+  const int r = p.r, C = 3 * r;
+  const float* s_prev = p.state + (size_t)((k - 1) & 1) * p.B * r;
+  const int jl = (lane & 15) * L;
+  o.hg = o.hc = o.ho = o.sold = 0.f;
+  if (lane == 0) {
+    const float* hpr = p.hp + ((size_t)b * p.gamma + (k - 1)) * C;
+    o.hg = __ldg(hpr + i);
+    o.hc = __ldg(hpr + r + i);
+    o.ho = __ldg(hpr + 2 * r + i);
+    if (k > 1) o.sold = __ldcg(s_prev + (size_t)b * r + i);
+  }
+  if (lane < 16) {
+    const float* src = s_prev + (size_t)b * r + jl;
+    if (k == 1) {
+#pragma unroll
+      for (int e = 0; e < kRnnMaxL; ++e) o.x[e] = 0.f;
+    } else if (vec) {
+#pragma unroll
+      for (int q = 0; q < kRnnMaxL / 4; ++q) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q * 4 < L) v = __ldcg(reinterpret_cast<const float4*>(src) + q);
+        o.x[4 * q] = v.x; o.x[4 * q + 1] = v.y; o.x[4 * q + 2] = v.z; o.x[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kRnnMaxL; ++e) o.x[e] = e < L ? __ldcg(src + e) : 0.f;
+    }
+  } else {
+    const uint16_t* src = p.W1 + (size_t)prev * r + jl;
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < kRnnMaxL / 8; ++q) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (q * 8 < L) v = __ldg(reinterpret_cast<const uint4*>(src) + q);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          o.x[8 * q + 2 * h] = bf16_val(w4[h] & 0xFFFFu);
+          o.x[8 * q + 2 * h + 1] = bf16_val(w4[h] >> 16);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kRnnMaxL; ++e) o.x[e] = e < L ? bf16_val(__ldg(src + e)) : 0.f;
+    }
+  }
+}
+
+__device__ __noinline__ void rnn_step(const DraftParams& p, int k, int d0, int sw, int lane,
+                                      int stid, uint8_t* zs, int zbytes) {
+  const int r = p.r, R2 = 2 * r, L = R2 / 32;
+  const bool vec = (L & 7) == 0;       // r a multiple of 128: 16-byte loads
+  float* s_next = p.state + (size_t)(k & 1) * p.B * r;
+  const uint16_t* ws = reinterpret_cast<const uint16_t*>(zs);
+  const int row_chunks = R2 / 8;       // 16-byte chunks per Wrec row
+  const int e_max = zbytes / (3 * R2 * 2);
+  for (int e0 = 0; e0 < p.dpc; e0 += e_max) {
+    const int ne = min(e_max, p.dpc - e0);
+    const int n_items = ne * p.B;
+    // the first four predecessor tokens of this warp, loaded with the staging
+    int pv[kRnnBatch];
+#pragma unroll
+    for (int t = 0; t < kRnnBatch; ++t) {
+      const int it = sw + t * kSamplers;
+      pv[t] = 0;
+      if (it < n_items) {
+        const int b = it % p.B;
+        pv[t] = k == 1 ? p.anchor[b] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+      }
+    }
+    // rows (g, e) = Wrec[g r + d0 + e0 + e], g = gate / candidate / output, e < ne
+    for (int idx = stid; idx < 3 * ne * row_chunks; idx += kSamplerThreads) {
+      const int row = idx / row_chunks, q = idx - row * row_chunks;
+      const int g = row / ne, e = row - g * ne;
+      reinterpret_cast<uint4*>(zs)[idx] =
+          __ldg(reinterpret_cast<const uint4*>(p.Wrec + (size_t)(g * r + d0 + e0 + e) * R2) + q);
+    }
+    named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+    for (int it0 = sw; it0 < n_items; it0 += kRnnBatch * kSamplers) {
+      if (it0 != sw) {
+#pragma unroll
+        for (int t = 0; t < kRnnBatch; ++t) {
+          const int it = it0 + t * kSamplers;
+          pv[t] = 0;
+          if (it < n_items) {
+            const int b = it % p.B;
+            pv[t] = k == 1 ? p.anchor[b] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kRnnBatch; ++t) {
+        if (pv[t] < 0 || pv[t] >= p.V) {
+          if (it0 + t * kSamplers < n_items && lane == 0) set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
+          pv[t] = 0;
+        }
+      }
+      RnnOperands cur, nxt;
+      rnn_load(p, k, d0 + e0 + it0 / p.B, it0 % p.B, pv[0], lane, L, vec, cur);
+#pragma unroll
+      for (int t = 0; t < kRnnBatch; ++t) {
+        const int it = it0 + t * kSamplers;
+        if (it >= n_items) break;
+        const int e = it / p.B, b = it - e * p.B, i = d0 + e0 + e;
+        const int itn = it + kSamplers;
+        if (t + 1 < kRnnBatch && itn < n_items)
+          rnn_load(p, k, d0 + e0 + itn / p.B, itn % p.B, pv[t + 1], lane, L, vec, nxt);
+        // this lane's L weights of the three rows, from shared memory
+        const uint16_t* wg = ws + (size_t)(0 * ne + e) * R2 + lane * L;
+        const uint16_t* wc = ws + (size_t)(1 * ne + e) * R2 + lane * L;
+        const uint16_t* wo = ws + (size_t)(2 * ne + e) * R2 + lane * L;
+        float ag = 0.f, ac = 0.f, ao = 0.f;
+        if (vec) {
+          // 16-byte shared loads (lane stride L * 2 bytes: at most two-way bank conflicts)
+#pragma unroll
+          for (int q = 0; q < kRnnMaxL / 8; ++q) {
+            if (q * 8 >= L) break;
+            const uint4 g4 = reinterpret_cast<const uint4*>(wg)[q];
+            const uint4 c4 = reinterpret_cast<const uint4*>(wc)[q];
+            const uint4 o4 = reinterpret_cast<const uint4*>(wo)[q];
+            const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, cw[4] = {c4.x, c4.y, c4.z, c4.w},
+                           ow[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              const int sh = (h & 1) ? 16 : 0;
+              const float xv = cur.x[8 * q + h];
+              ag = fmaf(xv, bf16_val((gw[h >> 1] >> sh) & 0xFFFFu), ag);
+              ac = fmaf(xv, bf16_val((cw[h >> 1] >> sh) & 0xFFFFu), ac);
+              ao = fmaf(xv, bf16_val((ow[h >> 1] >> sh) & 0xFFFFu), ao);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e2 = 0; e2 < kRnnMaxL; ++e2) {
+            if (e2 >= L) break;
+            ag = fmaf(cur.x[e2], bf16_val(wg[e2]), ag);
+            ac = fmaf(cur.x[e2], bf16_val(wc[e2]), ac);
+            ao = fmaf(cur.x[e2], bf16_val(wo[e2]), ao);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ag += __shfl_xor_sync(0xffffffffu, ag, o);
+          ac += __shfl_xor_sync(0xffffffffu, ac, o);
+          ao += __shfl_xor_sync(0xffffffffu, ao, o);
+        }
+        if (lane == 0) {
+          const float gate = 1.f / (1.f + expf(-(ag + cur.hg)));
+          s_next[(size_t)b * r + i] = gate * cur.sold + (1.f - gate) * tanhf(ac + cur.hc);
+          const float ev = tanhf(ao + cur.ho);
+          p.E_all[((size_t)b * p.gamma + (k - 1)) * r + i] = ev;
+          const uint32_t hi = bf16_rne(ev);
+          p.E_hl[(size_t)b * 2 * r + i] = (uint16_t)hi;
+          p.E_hl[(size_t)b * 2 * r + r + i] = (uint16_t)bf16_rne(ev - bf16_val(hi));
+        }
+        cur = nxt;
+      }
+    }
+    named_bar_sync(kNamedBarSamplers, kSamplerThreads);   // the rows are read before restaging
+  }
+}
+
 // Merge the G partials of request b at position kp into x, q, max and sum (one warp).
 // One pass: every lane issues the loads of all its partials (G <= kDraftMaxCtas, so at
 // most five per lane) and of the token key together, then merges locally and across the
@@ -211,17 +416,17 @@ __device__ __forceinline__ void finalize_row(const DraftParams& p, int b, int kp
   }
 }
 
-template <int NB, bool Greedy>
+template <int NB, bool Greedy, bool Rnn>
 __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
     const DraftParams p) {
-  using S = Smem<NB>;
+  using S = Smem<NB, Rnn>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t w_full[kWStages], w_empty[kWStages];
-  __shared__ uint64_t u_full[kUStages], u_empty[kUStages];
+  __shared__ uint64_t u_full[S::kUStages], u_empty[S::kUStages];
   __shared__ uint64_t e_full[2], e_empty[2];
-  __shared__ uint64_t acc_full[kDepth], acc_empty[kDepth];
-  __shared__ uint64_t z_full[kDepth], z_empty[kDepth];
+  __shared__ uint64_t acc_full[S::kDepth], acc_empty[S::kDepth];
+  __shared__ uint64_t z_full[S::kDepth], z_empty[S::kDepth];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -238,16 +443,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   const int n_jobs = p.gamma * p.n_chunks;
   // tcgen05.alloc takes a power of two of at least 32 columns
   uint32_t tmem_cols = 32;
-  while (tmem_cols < (uint32_t)(kDepth * NB)) tmem_cols <<= 1;
+  while (tmem_cols < (uint32_t)(S::kDepth * S::kNE)) tmem_cols <<= 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
-    for (int i = 0; i < kUStages; ++i) { mbar_init(&u_full[i], 1); mbar_init(&u_empty[i], kSamplers); }
+    for (int i = 0; i < S::kUStages; ++i) { mbar_init(&u_full[i], 1); mbar_init(&u_empty[i], kSamplers); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&e_full[i], 1);
       mbar_init(&e_empty[i], 1);
     }
-    for (int i = 0; i < kDepth; ++i) {
+    for (int i = 0; i < S::kDepth; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
       mbar_init(&z_full[i], 4);
@@ -335,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     __syncwarp();
   } else if (warp == kUProducerWarp) {
     // ----------------------------------------------------------------- U tile producer
-    // U does not depend on the drafted tokens: its ring runs up to kUStages tiles ahead
+    // U does not depend on the drafted tokens: its ring runs a ring's depth of tiles ahead
     // of the samplers, across positions, independently of the W2 ring.
     if (lane == 0) {
       prefetch_tensormap(&u_map);
@@ -346,8 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       for (int job = 0; job < n_jobs && ok; ++job) {
         const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
         for (int t = t_lo; t < t_hi; ++t, ++us) {
-          const int su = us % kUStages;
-          if (!(ok = wait1(&u_empty[su], ((us / kUStages) & 1) ^ 1))) break;
+          const int su = us % S::kUStages;
+          if (!(ok = wait1(&u_empty[su], ((us / S::kUStages) & 1) ^ 1))) break;
           mbar_arrive_expect_tx(&u_full[su], (uint32_t)S::kUStageBytes);
           asm volatile(
               "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -358,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               : "memory");
         }
       }
-      for (uint32_t i = us > (uint32_t)kUStages ? us - kUStages : 0; i < us; ++i)
-        mbar_wait(&u_full[i % kUStages], (i / kUStages) & 1, kTimeoutNs);
+      for (uint32_t i = us > (uint32_t)S::kUStages ? us - S::kUStages : 0; i < us; ++i)
+        mbar_wait(&u_full[i % S::kUStages], (i / S::kUStages) & 1, kTimeoutNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -373,7 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     // warps, so every instruction saved here shortens the tile cadence.
     auto issue_loop = [&](auto ksteps_c) {
       constexpr int KS = decltype(ksteps_c)::value;
-      const uint32_t idesc = idesc_bf16_f32(128, NB, 1, 0);
+      // N = NB (Markov head) or 2 NB (RNN head: hi rows, then lo rows; the transposers add
+      // the two accumulator halves), so one MMA per K step either way
+      const uint32_t idesc = idesc_bf16_f32(128, S::kNE, 1, 0);
       const uint64_t a_base = smem_desc(smem_u32(smem + S::kOffW), (uint32_t)KS * 2048u, 1024u,
                                         kSwizzle128B);
       uint32_t ws = 0, tc = 0;
@@ -385,10 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         const uint64_t b_base =
             smem_desc(smem_u32(smem + S::kOffE + eb * S::kEBytes), 16u, 1024u, kSwizzle128B);
         for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-          const int ab = tc % kDepth;
-          if (!(ok = wait1(&acc_empty[ab], ((tc / kDepth) & 1) ^ 1))) break;
+          const int ab = tc % S::kDepth;
+          if (!(ok = wait1(&acc_empty[ab], ((tc / S::kDepth) & 1) ^ 1))) break;
           tc_fence_after_sync();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(ab * S::kNE);
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
             const int s = ws % kWStages;
             // TMA data: the barrier's transaction count orders it before the MMAs; no
@@ -401,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               // A: 16 K rows of the MN-major stage are 2048 bytes apart; B: K-block kg/4 of
               // the K-major E buffer, 32 bytes per 16-element step inside its 128-byte rows
               const uint64_t ad = a_s + (uint64_t)(kk * (2048 >> 4));
-              const uint64_t bd = b_base + (uint64_t)((kg >> 2) * (uint32_t)(NB * 128 / 16) + (kg & 3) * 2u);
+              const uint64_t bd = b_base + (uint64_t)((kg >> 2) * (uint32_t)(S::kNE * 128 / 16) + (kg & 3) * 2u);
               umma_bf16_f32(d_tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
             }
             umma_commit(&w_empty[s]);
@@ -430,19 +637,32 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     bool ok = true;
     for (int job = 0; job < n_jobs && ok; ++job) {
       for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-        const int ab = tc % kDepth;
-        const uint32_t par = (tc / kDepth) & 1;
+        const int ab = tc % S::kDepth;
+        const uint32_t par = (tc / S::kDepth) & 1;
         if (!(ok = wait_warp(&acc_full[ab], par))) break;
         tc_fence_after_sync();
         if (!(ok = wait_warp(&z_empty[ab], par ^ 1))) break;
         float* Zs = reinterpret_cast<float*>(smem + S::kOffZ + ab * S::kZBytes);
-        float vals[NB];
+        if constexpr (Rnn) {
+          // bias = the hi columns + the lo columns, 16 requests at a time
 #pragma unroll
-        for (int c16 = 0; c16 < NB; c16 += 16)
-          tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16), *reinterpret_cast<float(*)[16]>(vals + c16));
-        tmem_ld_wait();
+          for (int c16 = 0; c16 < NB; c16 += 16) {
+            float vh[16], vlo[16];
+            tmem_ld_32x32b_x16(trow + (uint32_t)(ab * S::kNE + c16), vh);
+            tmem_ld_32x32b_x16(trow + (uint32_t)(ab * S::kNE + NB + c16), vlo);
+            tmem_ld_wait();
 #pragma unroll
-        for (int b = 0; b < NB; ++b) Zs[b * 128 + vl] = vals[b];
+            for (int b = 0; b < 16; ++b) Zs[(c16 + b) * 128 + vl] = vh[b] + vlo[b];
+          }
+        } else {
+          float vals[NB];
+#pragma unroll
+          for (int c16 = 0; c16 < NB; c16 += 16)
+            tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16), *reinterpret_cast<float(*)[16]>(vals + c16));
+          tmem_ld_wait();
+#pragma unroll
+          for (int b = 0; b < NB; ++b) Zs[b * 128 + vl] = vals[b];
+        }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
@@ -466,7 +686,86 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     // sampler warps take no part: their first z tile cannot complete before E is published.
     constexpr int kGatherThreads = kGatherWarps * 32;
     constexpr int kGatherGroups = kGatherThreads / NB;
+    // RNN head: at the first chunk of position k, the recurrence CTAs (cta < n_rec) first
+    // wait for the grid barrier of position k - 1 (x_{k-1} known), run the recurrence for
+    // their state entries with all sampler warps and count themselves in rec_count (a
+    // release reduction after the samplers' named barrier); the sampler warps of every CTA
+    // then wait until all n_rec have arrived for position k and load E_k as 2 NB operand
+    // rows: hi = bf16(E) for request n in row n, lo = bf16(E - hi) in row NB + n, in the
+    // same swizzled K-major layout.
+    auto publish_E_rnn = [&](int j, int c, int k, bool wait_grid) {
+      const bool rec = c == 0 && cta < p.n_rec;
+      if (rec) {
+        if (stid == 0 && wait_grid) {
+          const unsigned int target = (unsigned int)G * (unsigned int)(k - 1);
+          const long long t0 = sm_cycles();
+          while (ld_acquire_u32(p.grid_count) < target) {
+            if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
+              set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+              atomicExch(&abort_s, 1);
+              break;
+            }
+          }
+        }
+        named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+        // called by every sampler thread whatever the abort flag says (the step's named
+        // barriers need all of them; it has no other waits)
+        rnn_step(p, k, cta * p.dpc, sw, lane, stid, smem + S::kOffZ, S::kDepth * S::kZBytes);
+        named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+        if (stid == 0)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.rec_count) : "memory");
+      }
+      // every sampler warp gathers: 2 NB rows of r bf16 (hi rows, then lo rows), one row per
+      // thread group, each thread's (at most four) 16-byte loads in flight together
+      if (stid == 0) {
+        if (c == 0) {
+          const unsigned int target = (unsigned int)p.n_rec * (unsigned int)k;
+          const long long t0 = sm_cycles();
+          while (ld_acquire_u32(p.rec_count) < target) {
+            if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
+              set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+              atomicExch(&abort_s, 1);
+              break;
+            }
+          }
+        }
+        wait1(&e_empty[j & 1], ((j >> 1) & 1) ^ 1);
+      }
+      named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+      if (!*(volatile int*)&abort_s) {
+        constexpr int kRows = 2 * NB;
+        constexpr int kGroups = kSamplerThreads / kRows;
+        constexpr int kPerR = (32 + kGroups - 1) / kGroups;   // r / 8 <= 32 chunks per row
+        uint8_t* sE = smem + S::kOffE + (j & 1) * S::kEBytes;
+        const int n = stid % kRows, grp = stid / kRows;
+        const int b = c * NB + (n % NB);
+        const int kchunks = p.r >> 3;
+        const bool ok = b < p.B;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.E_hl + ((size_t)(ok ? b : 0) * 2 + (n >= NB ? 1 : 0)) * p.r);
+        uint4 val[kPerR];
+#pragma unroll
+        for (int u = 0; u < kPerR; ++u) {
+          const int q = grp + u * kGroups;
+          val[u] = (ok && q < kchunks) ? __ldcg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kPerR; ++u) {
+          const int q = grp + u * kGroups;
+          if (q < kchunks)
+            *reinterpret_cast<uint4*>(sE + (size_t)(q >> 3) * kRows * 128 + (size_t)n * 128 +
+                                      (((q & 7) ^ (n & 7)) << 4)) = val[u];
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kNamedBarSamplers, kSamplerThreads);
+      if (stid == 0) mbar_arrive(&e_full[j & 1]);
+    };
     auto publish_E = [&](int j, int c, int k, bool wait_grid) {
+      if constexpr (Rnn) {
+        publish_E_rnn(j, c, k, wait_grid);
+        return;
+      }
       if (sw >= kGatherWarps) return;
       if (stid == 0) {
         if (wait_grid) {
@@ -547,8 +846,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         mx[i] = -INFINITY; bi[i] = -1;
       }
       for (int t = 0; t < my_tiles; ++t, ++tc) {
-        const int zb = tc % kDepth;
-        const uint32_t par = (tc / kDepth) & 1;
+        const int zb = tc % S::kDepth;
+        const uint32_t par = (tc / S::kDepth) & 1;
         if (!wait_warp(&z_full[zb], par)) continue;
         if (!wait_warp(&u_full[zb], par)) continue;
         const float* Zs = reinterpret_cast<const float*>(smem + S::kOffZ + zb * S::kZBytes);
@@ -752,28 +1051,28 @@ bool encode_u_map(CUtensorMap* map, const float* U, int B, int gamma, int V, int
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NB, bool Greedy>
+template <int NB, bool Greedy, bool Rnn>
 int max_grid() {
   static int cached = -1;
   if (cached < 0) {
     int dev = 0, sms = 0, per = 0;
-    const size_t smem = Smem<NB>::kBytes + 1024;
+    const size_t smem = Smem<NB, Rnn>::kBytes + 1024;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(draft_fused_kernel<NB, Greedy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, draft_fused_kernel<NB, Greedy>, kThreads,
-                                                      smem) != cudaSuccess)
+        cudaFuncSetAttribute(draft_fused_kernel<NB, Greedy, Rnn>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, draft_fused_kernel<NB, Greedy, Rnn>,
+                                                      kThreads, smem) != cudaSuccess)
       return 0;
     cached = per > 0 ? sms : 0;
   }
   return cached;
 }
 
-template <int NB, bool Greedy>
+template <int NB, bool Greedy, bool Rnn>
 cudaError_t launch_fused(const CUtensorMap& w2_map, const CUtensorMap& u_map, const DraftParams& p,
                          int grid, cudaStream_t stream) {
-  const size_t smem = Smem<NB>::kBytes + 1024;
+  const size_t smem = Smem<NB, Rnn>::kBytes + 1024;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -784,7 +1083,7 @@ cudaError_t launch_fused(const CUtensorMap& w2_map, const CUtensorMap& u_map, co
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, draft_fused_kernel<NB, Greedy>, w2_map, u_map, p);
+  return cudaLaunchKernelEx(&cfg, draft_fused_kernel<NB, Greedy, Rnn>, w2_map, u_map, p);
 }
 
 }  // namespace
@@ -797,19 +1096,30 @@ size_t draft_region_bytes(int B, int gamma) {
 int draft_kchunk(int r) { return (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16; }
 
 namespace {
+template <bool Greedy, bool Rnn>
+int grid_for(int NB) { return NB == 16 ? max_grid<16, Greedy, Rnn>() : max_grid<32, Greedy, Rnn>(); }
+
+template <bool Greedy, bool Rnn>
+cudaError_t launch_for(int NB, const CUtensorMap& w2_map, const CUtensorMap& u_map,
+                       const DraftParams& p, int grid, cudaStream_t stream) {
+  return NB == 16 ? launch_fused<16, Greedy, Rnn>(w2_map, u_map, p, grid, stream)
+                  : launch_fused<32, Greedy, Rnn>(w2_map, u_map, p, grid, stream);
+}
+
 cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
                                 const float* U, const int32_t* anchor, int B, int gamma, int V,
                                 int r, uint64_t seed, int32_t* tokens, float* q_tok,
                                 float* row_max, float* row_sumexp, void* region, int* err,
-                                bool greedy, cudaStream_t stream) {
+                                bool greedy, const RnnDraftArgs* rnn, cudaStream_t stream) {
   const int NB = B <= 16 ? 16 : 32;
   const int n_tiles = cdiv(V, kGemmTileV);
-  int grid = greedy ? (NB == 16 ? max_grid<16, true>() : max_grid<32, true>())
-                    : (NB == 16 ? max_grid<16, false>() : max_grid<32, false>());
+  int grid = rnn ? (greedy ? grid_for<true, true>(NB) : grid_for<false, true>(NB))
+                 : (greedy ? grid_for<true, false>(NB) : grid_for<false, false>(NB));
   if (grid <= 0) return cudaErrorInvalidConfiguration;
   if (grid > n_tiles) grid = n_tiles;
   if (grid > kDraftMaxCtas) grid = kDraftMaxCtas;
   DraftParams p;
+  memset(&p, 0, sizeof(p));
   p.W1 = W1;
   p.W2p = W2p;
   p.anchor = anchor;
@@ -828,6 +1138,19 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
   p.row_max = row_max;
   p.row_sumexp = row_sumexp;
   p.err = err;
+  if (rnn) {
+    p.Wrec = rnn->Wrec;
+    p.hp = rnn->hp;
+    p.E_all = rnn->E_all;
+    p.state = rnn->state;
+    p.E_hl = rnn->E_hl;
+    p.rec_count = p.grid_count + 32;     // same zeroed 256-byte slot, another 128-byte line
+    // recurrence CTAs: the largest divisor of r that the grid holds
+    int n_rec = grid < r ? grid : r;
+    while (r % n_rec) --n_rec;
+    p.n_rec = n_rec;
+    p.dpc = r / n_rec;
+  }
   cudaError_t e = cudaMemsetAsync(base + part_bytes, 0,
                                   256 + (size_t)gamma * B * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;
@@ -835,11 +1158,11 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
   memset(&w2_map, 0, sizeof(w2_map));
   if (!W2p && !encode_w2_map(&w2_map, W2, V, r, p.kc)) return cudaErrorInvalidValue;
   if (!encode_u_map(&u_map, U, B, gamma, V, NB)) return cudaErrorInvalidValue;
-  if (greedy)
-    return NB == 16 ? launch_fused<16, true>(w2_map, u_map, p, grid, stream)
-                    : launch_fused<32, true>(w2_map, u_map, p, grid, stream);
-  return NB == 16 ? launch_fused<16, false>(w2_map, u_map, p, grid, stream)
-                  : launch_fused<32, false>(w2_map, u_map, p, grid, stream);
+  if (rnn)
+    return greedy ? launch_for<true, true>(NB, w2_map, u_map, p, grid, stream)
+                  : launch_for<false, true>(NB, w2_map, u_map, p, grid, stream);
+  return greedy ? launch_for<true, false>(NB, w2_map, u_map, p, grid, stream)
+                : launch_for<false, false>(NB, w2_map, u_map, p, grid, stream);
 }
 }  // namespace
 
@@ -848,7 +1171,7 @@ cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const flo
                                uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
                                float* row_sumexp, void* region, int* err, cudaStream_t stream) {
   return launch_draft_common(W1, W2, nullptr, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
-                             row_max, row_sumexp, region, err, false, stream);
+                             row_max, row_sumexp, region, err, false, nullptr, stream);
 }
 
 cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, const float* U,
@@ -857,7 +1180,7 @@ cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, c
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream) {
   return launch_draft_common(W1, nullptr, W2p, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
-                             row_max, row_sumexp, region, err, false, stream);
+                             row_max, row_sumexp, region, err, false, nullptr, stream);
 }
 
 cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
@@ -866,7 +1189,16 @@ cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, co
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream) {
   return launch_draft_common(W1, W2p ? nullptr : W2, W2p, U, anchor, B, gamma, V, r, 0, tokens,
-                             q_tok, row_max, row_sumexp, region, err, true, stream);
+                             q_tok, row_max, row_sumexp, region, err, true, nullptr, stream);
+}
+
+cudaError_t launch_draft_fused_rnn(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
+                                   const float* U, const int32_t* anchor, int B, int gamma, int V,
+                                   int r, uint64_t seed, bool greedy, const RnnDraftArgs& rnn,
+                                   int32_t* tokens, float* q_tok, float* row_max,
+                                   float* row_sumexp, void* region, int* err, cudaStream_t stream) {
+  return launch_draft_common(W1, W2p ? nullptr : W2, W2p, U, anchor, B, gamma, V, r, seed, tokens,
+                             q_tok, row_max, row_sumexp, region, err, greedy, &rnn, stream);
 }
 
 }  // namespace dspark

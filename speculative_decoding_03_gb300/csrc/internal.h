@@ -58,7 +58,7 @@ struct Plan {
   RowSplit stats, ver;
   // byte offsets into the workspace
   size_t off_err, off_draft, off_bias, off_part, off_M, off_lnS, off_p, off_mode,
-      off_pos, off_prev, off_fallback, total;
+      off_pos, off_prev, off_fallback, off_rnn_state, total;
 };
 
 inline Plan make_plan(int B, int gamma, int V, int r, int H) {
@@ -79,6 +79,8 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_pos = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_prev = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_fallback = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
+  // RNN head: state [2][B][r] fp32, then the current position's rows [B][2][r] bf16
+  p.off_rnn_state = o; o = align_up(o + (size_t)2 * B * r * sizeof(float) + (size_t)2 * B * r * 2, 256);
   p.total = o;
   return p;
 }
@@ -121,6 +123,11 @@ bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_r
 cudaError_t launch_bias_gemm(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
                              const int32_t* prev, int prev_stride, int B, int V, int r, float* out,
                              int* err, cudaStream_t stream);
+// bias[b][v] = sum_i Ef[prev_b][i] * W2[i][v] with fp32 rows Ef [table_rows][r] taken as two
+// bf16 terms each (rows with prev_b == -1 are 0)
+cudaError_t launch_bias_gemm_rows(const uint16_t* W2, const uint16_t* W2p, const float* Ef,
+                                  int table_rows, const int32_t* prev, int B, int V, int r,
+                                  float* out, int* err, cudaStream_t stream);
 
 // the whole draft (all gamma positions) in one cooperative launch; `region` holds
 // draft_region_bytes(B, gamma) of workspace
@@ -142,6 +149,24 @@ cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, co
                                       int V, int r, int32_t* tokens, float* q_tok,
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream);
+// the draft with the RNN head (see draft_fused.cu and rnn.cu): Wrec [3r][2r] (rnn_pack),
+// hp [B][gamma][3r] (rnn_project), E_all [B][gamma][r] written, state [2][B][r] and
+// E_hl [B][2][r] bf16 scratch
+struct RnnDraftArgs {
+  const uint16_t* Wrec;
+  const float* hp;
+  float* E_all;
+  float* state;
+  uint16_t* E_hl;
+};
+cudaError_t launch_draft_fused_rnn(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
+                                   const float* U, const int32_t* anchor, int B, int gamma, int V,
+                                   int r, uint64_t seed, bool greedy, const RnnDraftArgs& rnn,
+                                   int32_t* tokens, float* q_tok, float* row_max,
+                                   float* row_sumexp, void* region, int* err, cudaStream_t stream);
+cudaError_t launch_rnn_pack(const uint16_t* W_rnn, int r, uint16_t* Wrec, cudaStream_t stream);
+cudaError_t launch_rnn_project(const float* h, const uint16_t* W_rnn, const float* b_rnn, int M,
+                               int H, int r, float* hp, cudaStream_t stream);
 // rank rows per W2 stage of the draft kernel (and per packed K-chunk image)
 int draft_kchunk(int r);
 
@@ -158,8 +183,10 @@ cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps,
 cudaError_t launch_schedule_threshold(const float* a, int R, int gamma, float threshold,
                                       int32_t* ell, int32_t* B_total, cudaStream_t stream);
 
+// E_all (null for the Markov head): the RNN head's output rows [B][gamma][r] of the draft
 cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
-                          const uint16_t* W2, const uint16_t* W2p, const int32_t* anchor,
+                          const uint16_t* W2, const uint16_t* W2p, const float* E_all,
+                          const int32_t* anchor,
                           const int32_t* tokens, const float* q_tok, const float* row_max,
                           const float* row_sumexp, const int32_t* ell, uint64_t seed,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* n_out, void* ws,

@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(kSampleThreads) target_stats_kernel(
 // ----------------------------------------------------------------------------- decide
 // One warp per request; lane k - 1 owns position k.  Verified lanes merge their row's
 // target partials (M, S), compute p_k(x_k) and test u_k < p_k(x_k) / q_k(x_k); a ballot
-// gives the first reject.  q_tok == null: greedy drafts, q_k(x_k) = 1.
+// gives the first reject.  q_tok == null: greedy drafts, q_k(x_k) = 1.  rnn_rows: the
+// residual's bias rows are the RNN head's output rows instead of W1 rows.
 __global__ void __launch_bounds__(128) decide_kernel(
     const float* __restrict__ T, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const float* __restrict__ q_tok,
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(128) decide_kernel(
     int gamma, int V, uint64_t seed, float* __restrict__ M_t, float* __restrict__ lnS_t,
     float* __restrict__ p_t, int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ n_out, int32_t* __restrict__ mode, int32_t* __restrict__ pos,
-    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, int* err) {
+    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, int* err, int rnn_rows) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -228,7 +229,10 @@ __global__ void __launch_bounds__(128) decide_kernel(
     } else if (j) {
       mode[b] = kModeResidual;
       pos[b] = j;
-      prev_tok[b] = (j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)];
+      // the bias operand of the rejected row: the Markov head's predecessor token, or the
+      // RNN head's output row (b, j) of the draft
+      prev_tok[b] = rnn_rows ? b * gamma + (j - 1)
+                             : ((j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)]);
     } else {
       mode[b] = kModeBonus;
       pos[b] = L + 1;
@@ -533,7 +537,8 @@ int final_sample_grid(int n_items) {
 }  // namespace
 
 cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
-                          const uint16_t* W2, const uint16_t* W2p, const int32_t* anchor,
+                          const uint16_t* W2, const uint16_t* W2p, const float* E_all,
+                          const int32_t* anchor,
                           const int32_t* tokens, const float* q_tok, const float* row_max,
                           const float* row_sumexp, const int32_t* ell, uint64_t seed,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* n_out, void* ws,
@@ -561,11 +566,13 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   if (e != cudaSuccess) return e;
   e = launch_pdl(decide_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream, T, anchor, tokens, q_tok,
                  (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, M_t, lnS_t,
-                 p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, err);
+                 p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, err, E_all ? 1 : 0);
   if (e != cudaSuccess) return e;
-  if (!point_mass &&
-      (e = launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream)) != cudaSuccess)
-    return e;
+  if (!point_mass) {
+    e = E_all ? launch_bias_gemm_rows(W2, W2p, E_all, B * gamma, prev, B, V, p.r, bias, err, stream)
+              : launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream);
+    if (e != cudaSuccess) return e;
+  }
   e = launch_pdl(final_sample_kernel, dim3(final_sample_grid(B * p.ver.splits)),
                  dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias, row_max,
                  row_sumexp, (const float*)M_t, (const float*)lnS_t, (const int32_t*)mode,

@@ -1,0 +1,185 @@
+"""Parity of the CUDA RNN head with the CPU oracle: the weight packing, the hidden-state
+projection, the RNN draft (Gumbel and greedy), its verification and the whole step.
+
+The bars match the main parity tests.  Tokens must be bit-exact except inside the tie
+band (top-two score gap within 1e-5, or |u - p/q| within 1e-5).  q_tok, row max and sum
+must be within 1e-5 relative.  The head's output rows E and the projection must be within
+1e-5 of the oracle's fp64 values, scaled by the magnitude of the terms summed.  Each call
+is fed the oracle's upstream outputs: the projection, and the draft's tokens and rows.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from workloads import bf16_bits_to_f32
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+ds = pytest.importorskip("speculative_decoding_03_gb300")
+
+TIE = 1e-5
+RTOL = 1e-5
+
+CASES = {
+    "tiny": workloads.get("tiny"),
+    "qwen_small": workloads.scaled(workloads.get("qwen3_4b_like"), B=5, gamma=3, V=904, r=64, H=32),
+    "prod_small": workloads.scaled(workloads.get("production"), B=40, gamma=5, V=2056, r=256, H=64),
+    "long_small": workloads.scaled(workloads.get("long_block"), B=7, gamma=15, V=1032, r=256, H=16,
+                                   noise_std=lambda k: 0.5 + 1.5 * (k - 1) / 14.0),
+    "wide_batch": workloads.scaled(workloads.get("scheduler_stress"), B=300, gamma=2, V=520, r=128, H=8),
+}
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _cuda(x, dt):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=dt)).cuda()
+
+
+def _setup(w, with_T=True, requests=None):
+    inp = workloads.generate(w, requests=requests, with_T=with_T)
+    W_rnn, b_rnn = workloads.gen_rnn_weights(w)
+    dev = ds.rnn_to_device(W_rnn, b_rnn, ds.to_device(inp))
+    return inp, W_rnn, b_rnn, dev
+
+
+def _compare(got, ref, label, greedy=False):
+    """Tokens equal until the first tie-band position of a row; statistics and E rows
+    within tolerance on the agreeing prefix; returns the number of tie-band divergences."""
+    ties = 0
+    for i in range(got["tokens"].shape[0]):
+        for k in range(got["tokens"].shape[1]):
+            if got["tokens"][i, k] != ref["tokens"][i, k]:
+                assert ref["gap"][i, k] <= TIE, (label, i, k, got["tokens"][i, k], ref["tokens"][i, k])
+                ties += 1
+                break
+    same = np.cumprod(got["tokens"] == ref["tokens"], axis=1).astype(bool)
+    for key in ("q_tok", "row_max", "row_sumexp"):
+        np.testing.assert_allclose(got[key][same], ref[key][same], rtol=RTOL, err_msg=f"{label} {key}")
+    # E at position k depends on tokens before k only: compare where the prefix before k agrees
+    before = np.concatenate([np.ones((same.shape[0], 1), bool), same[:, :-1]], axis=1)
+    np.testing.assert_allclose(got["E"][before], ref["E"][before], atol=RTOL, err_msg=f"{label} E")
+    if greedy:
+        np.testing.assert_array_equal(got["q_tok"], 1.0)
+    return ties
+
+
+def test_rnn_pack_is_the_transpose_of_the_recurrent_rows():
+    _need_gpu()
+    for r, H in [(16, 8), (64, 32), (256, 40), (48, 4)]:
+        w = workloads.scaled(workloads.get("tiny"), r=r, H=H)
+        W_rnn, _ = workloads.gen_rnn_weights(w)
+        Wrec = ds.rnn_pack(ds.as_bf16_tensor(W_rnn), r)
+        got = Wrec.view(torch.int16).cpu().numpy().view(np.uint16).reshape(3 * r, 2 * r)
+        np.testing.assert_array_equal(got, W_rnn[:2 * r].T)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_rnn_project(name):
+    _need_gpu()
+    w = CASES[name]
+    inp, W_rnn, b_rnn, dev = _setup(w, with_T=False)
+    got = ds.rnn_project(dev["h"], dev["W_rnn"], dev["b_rnn"]).cpu().numpy()
+    ref = oracle.rnn_project(inp.h, W_rnn, b_rnn)
+    mag = np.abs(inp.h).astype(np.float64) @ np.abs(bf16_bits_to_f32(W_rnn)[2 * w.r:]).astype(np.float64)
+    np.testing.assert_array_less(np.abs(got - ref), RTOL * (mag + np.abs(b_rnn)) + 1e-12)
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+@pytest.mark.parametrize("name", list(CASES))
+def test_draft_rnn(name, greedy):
+    _need_gpu()
+    w = CASES[name]
+    inp, W_rnn, b_rnn, dev = _setup(w, with_T=False)
+    ws = ds.Workspace(w.B, w.gamma, w.V, w.r, w.H)
+    hp = _cuda(oracle.rnn_project(inp.h, W_rnn, b_rnn), np.float32)
+    Wrec = ds.rnn_pack(dev["W_rnn"], w.r)
+    out = ds.draft_rnn(dev["U"], dev["W1"], dev["W2"], Wrec, hp, dev["anchor"], w.seed, ws, greedy=greedy)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    ref = oracle.draft_rnn(inp.U, inp.h, inp.W1, inp.W2, W_rnn, b_rnn, inp.anchor, w.seed, greedy=greedy)
+    ties = _compare(got, ref, name, greedy)
+    assert ties <= max(1, 1e-4 * got["tokens"].size)
+    # the packed weights give identical outputs
+    W2p = ds.pack_w2(dev["W2"])
+    out_p = ds.draft_rnn(dev["U"], dev["W1"], W2p, Wrec, hp, dev["anchor"], w.seed, ws, greedy=greedy,
+                         packed=True)
+    for key in got:
+        np.testing.assert_array_equal(got[key], out_p[key].cpu().numpy(), err_msg=key)
+    assert ws.status() == 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_verify_rnn(name):
+    _need_gpu()
+    w = CASES[name]
+    inp, W_rnn, b_rnn, dev = _setup(w)
+    ws = ds.Workspace(w.B, w.gamma, w.V, w.r, w.H)
+    d = oracle.draft_rnn(inp.U, inp.h, inp.W1, inp.W2, W_rnn, b_rnn, inp.anchor, w.seed)
+    rng = np.random.default_rng(w.seed + 600)
+    ell = rng.integers(0, w.gamma + 1, size=w.B).astype(np.int32)
+    out = ds.verify_rnn(dev["T"], dev["U"], _cuda(d["E"], np.float32), dev["W2"],
+                        _cuda(d["tokens"], np.int32), _cuda(d["q_tok"], np.float32),
+                        _cuda(d["row_max"], np.float32), _cuda(d["row_sumexp"], np.float32),
+                        _cuda(ell, np.int32), w.seed, ws)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    ref = oracle.verify_rnn(inp.T, inp.U, d["E"], inp.W2, d["tokens"], ell, w.seed)
+    ties = 0
+    for i in range(w.B):
+        if got["accept_len"][i] == ref["accept_len"][i] and \
+                np.array_equal(got["out_tokens"][i], ref["out_tokens"][i]):
+            continue
+        band = ref["band"][i]
+        in_band = np.any(~np.isnan(band)) and np.nanmin(band) <= TIE
+        assert in_band or ref["gap"][i] <= TIE, (name, i, got["out_tokens"][i], ref["out_tokens"][i])
+        ties += 1
+    assert ties <= max(1, 1e-4 * w.B * w.gamma)
+    assert (got["accept_len"] < ell).sum() > 0 or w.B < 8
+    assert ws.status() == 0
+
+
+def test_full_size_draft_rnn_sampled_requests():
+    """qwen3_4b_like at full size in one launch; the oracle recomputes sampled requests."""
+    _need_gpu()
+    w = workloads.get("qwen3_4b_like")
+    inp, W_rnn, b_rnn, dev = _setup(w, with_T=False)
+    ws = ds.Workspace(w.B, w.gamma, w.V, w.r, w.H)
+    hp = ds.rnn_project(dev["h"], dev["W_rnn"], dev["b_rnn"])
+    Wrec = ds.rnn_pack(dev["W_rnn"], w.r)
+    got = {k: v.cpu().numpy() for k, v in ds.draft_rnn(dev["U"], dev["W1"], dev["W2"], Wrec, hp,
+                                                        dev["anchor"], w.seed, ws).items()}
+    assert ws.status() == 0
+    assert np.all((got["tokens"] >= 0) & (got["tokens"] < w.V))
+    picks = sorted({0, w.B - 1, w.B // 2, 7 % w.B})
+    sub = workloads.generate(w, requests=picks, with_T=False)
+    ref = oracle.draft_rnn(sub.U, sub.h, sub.W1, sub.W2, W_rnn, b_rnn, sub.anchor, w.seed, req_ids=picks)
+    assert _compare({k: v[picks] for k, v in got.items()}, ref, "qwen3_4b_like") <= 1
+
+
+@pytest.mark.parametrize("sampling", ["gumbel", "greedy"])
+@pytest.mark.parametrize("name", ["tiny", "qwen_small", "prod_small"])
+def test_rnn_step_end_to_end(name, sampling):
+    _need_gpu()
+    w = CASES[name]
+    inp, W_rnn, b_rnn, dev = _setup(w)
+    step = ds.Step(dev, float(inp.b_c), head="rnn", sampling=sampling).run(seed=w.seed)
+    got = step.results()
+    greedy = sampling == "greedy"
+    d = oracle.draft_rnn(inp.U, inp.h, inp.W1, inp.W2, W_rnn, b_rnn, inp.anchor, w.seed, greedy=greedy)
+    if _compare({k: got[k] for k in ("tokens", "q_tok", "row_max", "row_sumexp", "E")}, d, name, greedy):
+        return
+    _, a = oracle.confidence(inp.h, inp.anchor, d["tokens"], inp.W1, inp.w_c, float(inp.b_c))
+    np.testing.assert_allclose(got["a"], a, rtol=RTOL)
+    ell_r, Bt_r, _ = oracle.schedule(got["a"], inp.sps)
+    np.testing.assert_array_equal(got["ell"], ell_r)
+    v = (oracle.verify_greedy(inp.T, d["tokens"], got["ell"], w.seed) if greedy else
+         oracle.verify_rnn(inp.T, inp.U, d["E"], inp.W2, d["tokens"], got["ell"], w.seed))
+    mism = np.nonzero(np.any(got["out_tokens"] != v["out_tokens"], axis=1))[0]
+    for i in mism:
+        band = v["band"][i]
+        assert (np.any(~np.isnan(band)) and np.nanmin(band) <= TIE) or v["gap"][i] <= TIE
+    assert step.ws.status() == 0
