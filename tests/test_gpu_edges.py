@@ -1,0 +1,132 @@
+"""Parity of the CUDA path with the oracle on the degenerate and extreme shapes.
+
+The shapes cover: one request and one position; the smallest vocabulary (8, one ragged
+128-row tile, a grid of one CTA); the largest block (gamma = 32, every lane of the
+decision warp); a second request chunk holding a single request; a rank that is not a
+multiple of 32 (r = 48, 16-row K chunks); a vocabulary of exactly one tile.  They also
+cover the acceptance extremes: every position accepted (target = draft distribution,
+bonus from the last row) and every first position rejected (a target peaked elsewhere).
+The tie band and tolerances are those of the main parity tests.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+ds = pytest.importorskip("speculative_decoding_03_gb300")
+
+TIE = 1e-5
+RTOL = 1e-5
+
+BASE = workloads.get("qwen3_4b_like")
+SHAPES = {
+    "B1_g1_V8": workloads.scaled(BASE, B=1, gamma=1, V=8, r=16, H=4),
+    "B1_g32": workloads.scaled(BASE, B=1, gamma=32, V=264, r=16, H=4),
+    "B2_g32_r48": workloads.scaled(BASE, B=2, gamma=32, V=392, r=48, H=8),
+    "B17_r48": workloads.scaled(BASE, B=17, gamma=2, V=136, r=48, H=8),
+    "B33_V128": workloads.scaled(BASE, B=33, gamma=3, V=128, r=32, H=4),
+}
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _first_divergence_ok(got, ref, gap):
+    """Tokens equal until the first tie-band position of each row."""
+    for i in range(got.shape[0]):
+        for k in range(got.shape[1]):
+            if got[i, k] != ref[i, k]:
+                assert gap[i, k] <= TIE, (i, k, got[i, k], ref[i, k], gap[i, k])
+                return False
+    return True
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_step_on_edge_shapes(name):
+    _need_gpu()
+    w = SHAPES[name]
+    inp = workloads.generate(w)
+    step = ds.Step(ds.to_device(inp), float(inp.b_c)).run(seed=w.seed)
+    got = step.results()
+    ref = oracle.step(inp, seed=w.seed)
+    assert step.ws.status() == 0
+    if not _first_divergence_ok(got["tokens"], ref["draft"]["tokens"], ref["draft"]["gap"]):
+        return
+    for key in ("q_tok", "row_max", "row_sumexp"):
+        np.testing.assert_allclose(got[key], ref["draft"][key], rtol=RTOL, err_msg=key)
+    np.testing.assert_allclose(got["c"], ref["c"], rtol=RTOL)
+    np.testing.assert_allclose(got["a"], ref["a"], rtol=RTOL)
+    ell_g, Bt_g, _ = oracle.schedule(got["a"], inp.sps)
+    np.testing.assert_array_equal(got["ell"], ell_g)
+    assert got["B_total"] == Bt_g
+    v = oracle.verify(inp.T, inp.U, inp.W1, inp.W2, inp.anchor, got["tokens"], got["ell"], w.seed)
+    for i in range(w.B):
+        if np.array_equal(got["out_tokens"][i], v["out_tokens"][i]):
+            continue
+        band = v["band"][i]
+        assert (np.any(~np.isnan(band)) and np.nanmin(band) <= TIE) or v["gap"][i] <= TIE, i
+    np.testing.assert_array_equal(got["n_out"], got["accept_len"] + 1)
+
+
+def _manual(B, gamma, V, r, seed):
+    rng = np.random.default_rng(seed)
+    U = rng.normal(0, 2, size=(B, gamma, V)).astype(np.float32)
+    W1 = np.zeros((V, r), np.uint16)                       # no Markov bias: z = U exactly
+    W2 = workloads.f32_to_bf16_bits(rng.normal(0, 0.02, size=(r, V)).astype(np.float32))
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    return rng, U, W1, W2, anchor
+
+
+def _run(U, T, W1, W2, anchor, ell, seed):
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    ws = ds.Workspace(B, gamma, V, r)
+    cu = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x, dtype=dt)).cuda()
+    W1d, W2d = ds.as_bf16_tensor(W1), ds.as_bf16_tensor(W2)
+    d = ds.draft(cu(U, np.float32), W1d, W2d, cu(anchor, np.int32), seed, ws)
+    out = ds.verify(cu(T, np.float32), cu(U, np.float32), W1d, W2d, cu(anchor, np.int32), d["tokens"],
+                    d["q_tok"], d["row_max"], d["row_sumexp"], cu(ell, np.int32), seed, ws)
+    assert ws.status() == 0
+    return {k: v.cpu().numpy() for k, v in d.items()}, {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def test_target_equal_to_draft_accepts_every_position_and_takes_the_bonus():
+    _need_gpu()
+    B, gamma, V, r, seed = 64, 6, 1000, 16, 21
+    rng, U, W1, W2, anchor = _manual(B, gamma, V, r, seed)
+    T = np.concatenate([U, rng.normal(0, 2, size=(B, 1, V)).astype(np.float32)], axis=1)
+    ell = np.full(B, gamma, np.int32)
+    d, v = _run(U, T, W1, W2, anchor, ell, seed)
+    ref_d = oracle.draft(U, W1, W2, anchor, seed)
+    _first_divergence_ok(d["tokens"], ref_d["tokens"], ref_d["gap"])
+    ref = oracle.verify(T, U, W1, W2, anchor, d["tokens"], ell, seed)
+    # p = q at every position: everything is accepted except inside the band |u - 1| <= 1e-5
+    np.testing.assert_array_equal(ref["accept_len"], gamma)
+    inside = np.nanmin(ref["band"], axis=1) <= TIE
+    assert np.all(v["accept_len"][~inside] == gamma)
+    np.testing.assert_array_equal(v["out_tokens"][~inside, :gamma], d["tokens"][~inside])
+    same = ~inside & (ref["gap"] > TIE)
+    np.testing.assert_array_equal(v["out_tokens"][same, gamma], ref["out_tokens"][same, gamma])
+
+
+def test_target_peaked_elsewhere_rejects_every_first_position():
+    _need_gpu()
+    B, gamma, V, r, seed = 64, 4, 1000, 16, 22
+    rng, U, W1, W2, anchor = _manual(B, gamma, V, r, seed)
+    d0 = oracle.draft(U, W1, W2, anchor, seed)
+    T = rng.normal(0, 1, size=(B, gamma + 1, V)).astype(np.float32)
+    peak = (d0["tokens"][:, 0] + 1 + rng.integers(0, V - 1, B)) % V
+    T[np.arange(B), 0, peak] = 40.0                       # p(x_1) ~ e^-40
+    ell = np.full(B, gamma, np.int32)
+    d, v = _run(U, T, W1, W2, anchor, ell, seed)
+    np.testing.assert_array_equal(d["tokens"][:, 0], d0["tokens"][:, 0])
+    np.testing.assert_array_equal(v["accept_len"], 0)
+    np.testing.assert_array_equal(v["n_out"], 1)
+    np.testing.assert_array_equal(v["out_tokens"][:, 0], peak)       # the residual's mass
+    np.testing.assert_array_equal(v["out_tokens"][:, 1:], -1)
