@@ -285,20 +285,17 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
 
 template <int NB, bool Split>
 int bias_grid(int n_tiles) {
-  static int per_sm = -1, sms = 0;
-  if (per_sm < 0) {
-    int dev = 0, per = 0;
+  static std::atomic<int> cache[kMaxCachedDevices];
+  const int g = per_device_grid(cache, [] {
+    int per = 0;
     const size_t smem = BiasSmem<Split>::kBytes + 1024;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(bias_gemm_kernel<NB, Split>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(bias_gemm_kernel<NB, Split>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_gemm_kernel<NB, Split>, kBiasThreads,
                                                       smem) != cudaSuccess)
-      return 0;
-    per_sm = per;
-  }
-  const int g = sms * per_sm;
+      return -1;
+    return per;
+  });
   return g < n_tiles ? g : n_tiles;
 }
 

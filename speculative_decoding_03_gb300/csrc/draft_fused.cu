@@ -1051,22 +1051,20 @@ bool encode_u_map(CUtensorMap* map, const float* U, int B, int gamma, int V, int
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// one CTA per SM (the cooperative grid), or 0 if the kernel does not fit an SM
 template <int NB, bool Greedy, bool Rnn>
 int max_grid() {
-  static int cached = -1;
-  if (cached < 0) {
-    int dev = 0, sms = 0, per = 0;
+  static std::atomic<int> cache[kMaxCachedDevices];
+  return per_device_grid(cache, [] {
+    int per = 0;
     const size_t smem = Smem<NB, Rnn>::kBytes + 1024;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(draft_fused_kernel<NB, Greedy, Rnn>,
+    if (cudaFuncSetAttribute(draft_fused_kernel<NB, Greedy, Rnn>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, draft_fused_kernel<NB, Greedy, Rnn>,
                                                       kThreads, smem) != cudaSuccess)
-      return 0;
-    cached = per > 0 ? sms : 0;
-  }
-  return cached;
+      return -1;
+    return per > 0 ? 1 : 0;
+  });
 }
 
 template <int NB, bool Greedy, bool Rnn>

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/dspark.h"
 #include "common.cuh"
 
@@ -83,6 +85,25 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_rnn_state = o; o = align_up(o + (size_t)2 * B * r * sizeof(float) + (size_t)2 * B * r * 2, 256);
   p.total = o;
   return p;
+}
+
+// Per-device launch setup.  A kernel's dynamic shared-memory attribute and the number of
+// its CTAs an SM holds belong to a device, so `setup` (which sets the attribute on the
+// current device and returns the CTAs per SM, or a negative value on failure) runs once
+// per device; the SM count times its result is cached per device (failures are not).
+// Returns 0 when the device cannot be queried or setup fails.
+constexpr int kMaxCachedDevices = 64;
+template <typename F>
+inline int per_device_grid(std::atomic<int> (&cache)[kMaxCachedDevices], F&& setup) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxCachedDevices) return 0;
+  const int v = cache[dev].load(std::memory_order_acquire);
+  if (v != 0) return v - 1;            // stored plus one: zero means "not set up yet"
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  const int per = setup();
+  if (per < 0) return 0;
+  cache[dev].store(sms * per + 1, std::memory_order_release);
+  return sms * per;
 }
 
 template <typename T>

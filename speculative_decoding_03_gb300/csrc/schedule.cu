@@ -226,13 +226,14 @@ cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps,
   int Npad = 2;
   while (Npad < N) Npad <<= 1;
   const size_t smem = (size_t)Npad * sizeof(unsigned long long);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kMaxScheduleItems * sizeof(unsigned long long)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the shared-memory attribute is set once per device
+  static std::atomic<int> cache[kMaxCachedDevices];
+  const int ok = per_device_grid(cache, [] {
+    return cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(kMaxScheduleItems * sizeof(unsigned long long))) == cudaSuccess
+               ? 1 : -1;
+  });
+  if (ok <= 0) return cudaErrorInvalidConfiguration;
   return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, stream, a, R, gamma, Npad,
                     sps, K_in, K_out, ell, B_total, theta);
 }

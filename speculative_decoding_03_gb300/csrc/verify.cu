@@ -518,20 +518,18 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(
 namespace {
 constexpr size_t kFinalSmem = 2 * 3 * kVerSeg * sizeof(float);
 int final_sample_grid(int n_items) {
-  static int per_sm = -1, sms = 0;
-  if (per_sm < 0) {
-    int dev = 0, per = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(final_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static std::atomic<int> cache[kMaxCachedDevices];
+  int g = per_device_grid(cache, [] {
+    int per = 0;
+    if (cudaFuncSetAttribute(final_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFinalSmem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, final_sample_kernel, kSampleThreads,
                                                       kFinalSmem) != cudaSuccess ||
         per < 1)
-      return 1;
-    per_sm = per;
-  }
-  const int g = sms * per_sm;
+      return -1;
+    return per;
+  });
+  if (g < 1) g = 1;
   return g < n_items ? g : n_items;
 }
 }  // namespace
