@@ -42,9 +42,9 @@ METRIC = "draft+verify positions/sec (B×γ) at V=151936, r=256; achieved HBM GB
 DRAFT_TRAFFIC = {"workload": "qwen3_4b_like", "bytes": 231_629_312,
                  "sources_sha1": "a32cd45a6c7be6ee2de3ee7b21070472aea5a087"}
 DRAFT_SOURCES = ("draft_fused.cu", "sm100_ptx.cuh", "common.cuh", "internal.h")
-# kernels of one step: draft 1, confidence 1, schedule 1, verify 5 (target statistics,
-# decision, bias contraction, final sample, finalize)
-KERNELS_PER_STEP = 8
+# kernels of one step: draft 1, confidence with the scheduler in its last CTA 1, verify 5
+# (target statistics, decision, bias contraction, final sample, finalize)
+KERNELS_PER_STEP = 7
 
 
 def _draft_traffic(w):
@@ -343,10 +343,11 @@ def run_ours(args, w):
         "draft": {"ms_per_call": rd_ms, "project_ms": proj_ms, "draft_kernel_ms": dk_ms}}
     del vs
 
-    # ---- per-call breakdown (warm, eager, events between the calls on one stream)
+    # ---- per-call breakdown (warm, eager, events between the calls on one stream); the
+    # step runs confidence and schedule as one launch, timed here both ways
     n_bd = max(3, min(args.steps, 20))
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    acc = [0.0] * 4
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    acc = [0.0] * 5
     d_out, c_out, s_out, v_out = step.draft_out, step.conf_out, step.sched_out, step.verify_out
     for i in range(n_bd):
         sd = w.seed + 500 + i
@@ -357,15 +358,18 @@ def run_ours(args, w):
         evs[2].record(stream)
         ds.schedule(c_out[1], x["sps"], step.ws, s_out)
         evs[3].record(stream)
+        ds.confidence_schedule(x["h"], x["anchor"], d_out["tokens"], x["W1"], x["w_c"], step.b_c,
+                               x["sps"], step.ws, c_out, s_out)
+        evs[4].record(stream)
         ds.verify_packed(x["T"], x["U"], x["W1"], step.W2p, x["anchor"], d_out["tokens"],
                          d_out["q_tok"], d_out["row_max"], d_out["row_sumexp"], s_out[0], sd,
                          step.ws, v_out)
-        evs[4].record(stream)
+        evs[5].record(stream)
         torch.cuda.synchronize()
-        for j in range(4):
+        for j in range(5):
             acc[j] += evs[j].elapsed_time(evs[j + 1])
     breakdown = {k: acc[j] / n_bd for j, k in enumerate(("draft_ms", "confidence_ms", "schedule_ms",
-                                                          "verify_ms"))}
+                                                          "confidence_schedule_ms", "verify_ms"))}
 
     # ---- end to end through the public API with pinned host buffers
     hin, hout = step.pinned_host_buffers()

@@ -172,6 +172,21 @@ dspark_status dspark_schedule(const float* a, int R, int gamma, const float* sps
                               size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * dspark_confidence followed by dspark_schedule in one launch: the confidence kernel's
+ * last CTA to finish runs the prefix scheduler over all survivals (the CTAs count
+ * themselves in a counter kept in the workspace's first 256 bytes, which the call leaves at
+ * zero).  Arguments, outputs, limits and results are those of the two calls (R = B, and
+ * B * gamma must not exceed 16384).
+ */
+dspark_status dspark_confidence_schedule(const float* h, const int32_t* anchor,
+                                         const int32_t* tokens, const uint16_t* W1,
+                                         const float* w_c, float b_c, int B, int gamma, int H,
+                                         int r, int V, const float* sps, int sps_len, float* c,
+                                         float* a, int32_t* ell, int32_t* B_total,
+                                         double* theta, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
+/*
  * Lossless verification.  billytse.dev DSpark page, section 1 (accept x_k with
  * probability min(1, p_k(x_k) / q_k(x_k)), keep the longest accepted prefix, fix the
  * first rejected position with a token from the residual) and xhh.club DSpark page

@@ -34,6 +34,8 @@ SIGNATURES = [
     ("dspark_draft_packed", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_draft", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_confidence", _I, [_P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    ("dspark_confidence_schedule", _I, [_P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _I, _P, _P,
+                                        _P, _P, _P, _P, _SZ, _P]),
     ("dspark_schedule", _I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_verify", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64,
                            _P, _P, _P, _P, _SZ, _P]),
@@ -203,6 +205,28 @@ def confidence(h, anchor, tokens, W1, w_c, b_c: float, ws: Workspace, out=None, 
         _ptr(h), _ptr(anchor), _ptr(tokens), _ptr(W1), _ptr(w_c), ctypes.c_float(b_c), B, gamma,
         H, r, V, _ptr(c), _ptr(a), ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
     return c, a
+
+
+def confidence_schedule(h, anchor, tokens, W1, w_c, b_c: float, sps, ws: Workspace, conf_out=None,
+                        sched_out=None, stream=None):
+    """confidence and schedule in one launch (the last CTA schedules)."""
+    torch = _torch()
+    B, gamma, H = h.shape
+    V, r = W1.shape
+    if conf_out is None:
+        conf_out = (torch.empty((B, gamma), dtype=torch.float32, device=h.device),
+                    torch.empty((B, gamma), dtype=torch.float32, device=h.device))
+    if sched_out is None:
+        sched_out = (torch.empty(B, dtype=torch.int32, device=h.device),
+                     torch.empty(1, dtype=torch.int32, device=h.device),
+                     torch.empty(1, dtype=torch.float64, device=h.device))
+    c, a = conf_out
+    ell, Bt, th = sched_out
+    _check("dspark_confidence_schedule", lib().dspark_confidence_schedule(
+        _ptr(h), _ptr(anchor), _ptr(tokens), _ptr(W1), _ptr(w_c), ctypes.c_float(b_c), B, gamma,
+        H, r, V, _ptr(sps), sps.numel(), _ptr(c), _ptr(a), _ptr(ell), _ptr(Bt), _ptr(th),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return (c, a), (ell, Bt, th)
 
 
 def schedule(a, sps, ws: Workspace, out=None, stream=None):
@@ -461,9 +485,16 @@ class Step:
     def run(self, seed: int, stream=None, t: int = 0):
         x = self.dev
         d = self.draft(seed, stream)
-        c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
-                          self.conf_out, stream)
-        ell = self._schedule(a, stream, t)
+        B, gamma = d["tokens"].shape
+        if self.scheduler == "theta" and B * gamma <= 16384:
+            # the early-stop scheduler runs in the confidence kernel's last CTA
+            _, (ell, _, _) = confidence_schedule(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"],
+                                                 self.b_c, x["sps"], self.ws, self.conf_out,
+                                                 self.sched_out, stream)
+        else:
+            c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
+                              self.conf_out, stream)
+            ell = self._schedule(a, stream, t)
         if self.sampling == "greedy":
             verify_greedy(x["T"], d["tokens"], ell, seed, self.ws, self.verify_out, stream)
         elif self.head == "rnn":

@@ -96,6 +96,31 @@ dspark_status dspark_confidence(const float* h, const int32_t* anchor, const int
   return DSPARK_OK;
 }
 
+dspark_status dspark_confidence_schedule(const float* h, const int32_t* anchor,
+                                         const int32_t* tokens, const uint16_t* W1,
+                                         const float* w_c, float b_c, int B, int gamma, int H,
+                                         int r, int V, const float* sps, int sps_len, float* c,
+                                         float* a, int32_t* ell, int32_t* B_total,
+                                         double* theta, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+  dspark_status st = check_shape(B, gamma, V, r, H);
+  if (st != DSPARK_OK) return st;
+  if ((long long)B * gamma > kMaxScheduleItems) return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)sps_len < (long long)B * (gamma + 1) + 1) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(h, 16) || !aligned(w_c, 16) || !aligned(W1, 16) || !aligned(anchor, 4) ||
+      !aligned(tokens, 4) || !aligned(c, 4) || !aligned(a, 4) || !aligned(sps, 4) ||
+      !aligned(ell, 4) || !aligned(B_total, 4) || !aligned(theta, 8))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
+  int* err = ws_at<int>(workspace, 0);
+  // the CTA counter shares the status word's 256-byte slot (byte 128; zero between calls)
+  unsigned int* done = ws_at<unsigned int>(workspace, 128);
+  if (launch_confidence_schedule(h, anchor, tokens, W1, w_c, b_c, B, gamma, H, r, V, sps, c, a,
+                                 ell, B_total, theta, done, err, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
 dspark_status dspark_schedule(const float* a, int R, int gamma, const float* sps, int sps_len,
                               int32_t* ell, int32_t* B_total, double* theta, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream) {

@@ -11,17 +11,33 @@
 // loads per lane in flight (h is an input, so the first of them are issued before the
 // kernel waits for the draft), the position's first warp adds the bf16 Markov row, and
 // thread 0 applies the sigmoid and multiplies the survival left to right.
-#include "internal.h"
+//
+// With the scheduler fused in (dspark_confidence_schedule), every CTA counts itself in a
+// workspace counter after its survivals are written (a fence, then an atomic add); the CTA
+// that counts last runs the prefix scheduler of schedule.cu over all of them and resets
+// the counter.  Nothing waits: the last CTA simply finds every other one done.
+#include "schedule_block.cuh"
 
 namespace dspark {
 namespace {
 
+struct SchedArgs {
+  const float* sps;
+  int32_t* ell;
+  int32_t* B_total;
+  double* theta;
+  unsigned int* done;        // zero between calls
+  int Npad;
+};
+
+template <bool Sched>
 __global__ void __launch_bounds__(1024) confidence_kernel(
     const float* __restrict__ h, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const uint16_t* __restrict__ W1,
     const float* __restrict__ w_c, float b_c, int gamma, int H, int r, int V, int wpp,
-    float* __restrict__ c_out, float* __restrict__ a_out, int* err) {
+    float* __restrict__ c_out, float* __restrict__ a_out, int* err, SchedArgs sa) {
   __shared__ float part_s[32];
+  __shared__ int last_s;
   constexpr int kBatch = 8;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,6 +116,20 @@ __global__ void __launch_bounds__(1024) confidence_kernel(
       a_out[(size_t)b * gamma + j] = surv;
     }
   }
+  if constexpr (Sched) {
+    if (threadIdx.x == 0) {
+      __threadfence();            // this CTA's survivals before its count
+      last_s = atomicAdd(sa.done, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (last_s) {
+      __threadfence();            // every other CTA's survivals after their counts
+      extern __shared__ unsigned long long keys[];
+      schedule_block(a_out, (int)gridDim.x, gamma, sa.Npad, sa.sps, nullptr, nullptr, sa.ell,
+                     sa.B_total, sa.theta, keys);
+      if (threadIdx.x == 0) *sa.done = 0u;
+    }
+  }
 }
 
 }  // namespace
@@ -111,8 +141,40 @@ cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32
   int wpp = 32 / gamma;
   if (wpp > 4) wpp = 4;
   if (wpp < 1) wpp = 1;
-  return launch_pdl(confidence_kernel, dim3(B), dim3(32 * wpp * gamma), 0, stream, h, anchor,
-                    tokens, W1, w_c, b_c, gamma, H, r, V, wpp, c, a, err);
+  SchedArgs sa = {};
+  return launch_pdl(confidence_kernel<false>, dim3(B), dim3(32 * wpp * gamma), 0, stream, h,
+                    anchor, tokens, W1, w_c, b_c, gamma, H, r, V, wpp, c, a, err, sa);
+}
+
+cudaError_t launch_confidence_schedule(const float* h, const int32_t* anchor,
+                                       const int32_t* tokens, const uint16_t* W1,
+                                       const float* w_c, float b_c, int B, int gamma, int H,
+                                       int r, int V, const float* sps, float* c, float* a,
+                                       int32_t* ell, int32_t* B_total, double* theta,
+                                       unsigned int* done, int* err, cudaStream_t stream) {
+  int wpp = 32 / gamma;
+  if (wpp > 4) wpp = 4;
+  if (wpp < 1) wpp = 1;
+  const int N = B * gamma;
+  int Npad = 2;
+  while (Npad < N) Npad <<= 1;
+  static std::atomic<int> cache[kMaxCachedDevices];
+  const int ok = per_device_grid(cache, [] {
+    return cudaFuncSetAttribute(confidence_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(kMaxScheduleItems * sizeof(unsigned long long))) == cudaSuccess
+               ? 1 : -1;
+  });
+  if (ok <= 0) return cudaErrorInvalidConfiguration;
+  SchedArgs sa;
+  sa.sps = sps;
+  sa.ell = ell;
+  sa.B_total = B_total;
+  sa.theta = theta;
+  sa.done = done;
+  sa.Npad = Npad;
+  return launch_pdl(confidence_kernel<true>, dim3(B), dim3(32 * wpp * gamma),
+                    (size_t)Npad * sizeof(unsigned long long), stream, h, anchor, tokens, W1, w_c,
+                    b_c, gamma, H, r, V, wpp, c, a, err, sa);
 }
 
 }  // namespace dspark

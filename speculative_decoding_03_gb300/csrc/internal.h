@@ -197,6 +197,15 @@ cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32
                               cudaStream_t stream);
 
 // K_in / K_out: the two-step capacity (both may be null; see schedule.cu)
+// confidence + survival and then, in the grid's last CTA, the prefix scheduler over all of
+// them; `done` is a workspace counter that is zero between calls
+cudaError_t launch_confidence_schedule(const float* h, const int32_t* anchor,
+                                       const int32_t* tokens, const uint16_t* W1,
+                                       const float* w_c, float b_c, int B, int gamma, int H,
+                                       int r, int V, const float* sps, float* c, float* a,
+                                       int32_t* ell, int32_t* B_total, double* theta,
+                                       unsigned int* done, int* err, cudaStream_t stream);
+
 cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps,
                             const int32_t* K_in, int32_t* K_out, int32_t* ell, int32_t* B_total,
                             double* theta, int* err, cudaStream_t stream);

@@ -315,3 +315,43 @@ def test_pack_layout_matches_its_definition():
                         v = t * 128 + 64 * h + 8 * c
                         want[t, :, h, kl, s, :] = Wpad[kl::kc, v:v + 8].reshape(r // kc, 8)
         np.testing.assert_array_equal(got, want.reshape(-1), err_msg=f"V={V} r={r}")
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_confidence_schedule_fused_matches_the_two_calls(name):
+    """The confidence kernel's last CTA runs the scheduler: identical c, a, l, B, Theta."""
+    _need_gpu()
+    w = CASES[name]
+    if w.B * w.gamma > 16384:
+        pytest.skip("beyond the one-CTA scheduler")
+    inp = workloads.generate(w, with_T=False)
+    dev = _dev(inp)
+    ws = _ws(w)
+    d = oracle.draft(inp.U, inp.W1, inp.W2, inp.anchor, w.seed)
+    tok = torch.from_numpy(d["tokens"]).cuda()
+    args = (dev["h"], dev["anchor"], tok, dev["W1"], dev["w_c"], float(inp.b_c))
+    c1, a1 = ds.confidence(*args, ws)
+    ell1, Bt1, th1 = ds.schedule(a1, dev["sps"], ws)
+    for _ in range(2):          # twice: the CTA counter is back at zero after a call
+        (c2, a2), (ell2, Bt2, th2) = ds.confidence_schedule(*args, dev["sps"], ws)
+        np.testing.assert_array_equal(c1.cpu().numpy(), c2.cpu().numpy())
+        np.testing.assert_array_equal(a1.cpu().numpy(), a2.cpu().numpy())
+        np.testing.assert_array_equal(ell1.cpu().numpy(), ell2.cpu().numpy())
+        assert int(Bt1.item()) == int(Bt2.item()) and float(th1.item()) == float(th2.item())
+    ell_r, Bt_r, th_r = oracle.schedule(a2.cpu().numpy(), inp.sps)
+    np.testing.assert_array_equal(ell2.cpu().numpy(), ell_r)
+    assert ws.status() == 0
+
+
+def test_schedule_with_exactly_one_block_of_items():
+    """R * gamma equal to the scheduler's thread count (the last SPS entry is staged too)."""
+    _need_gpu()
+    rng = np.random.default_rng(12)
+    for R, gamma in [(64, 16), (128, 8), (1024, 1)]:
+        a = np.cumprod(rng.uniform(0.6, 1.0, size=(R, gamma)), axis=1).astype(np.float32)
+        sps = np.ones(R * (gamma + 1) + 1, np.float32)       # flat: every item is admitted
+        ws = ds.Workspace(R, gamma, 8, 16, 0)
+        ell, Bt, th = ds.schedule(torch.from_numpy(a).cuda(), torch.from_numpy(sps).cuda(), ws)
+        ell_ref, Bt_ref, th_ref = oracle.schedule(a, sps)
+        np.testing.assert_array_equal(ell.cpu().numpy(), ell_ref)
+        assert int(Bt.item()) == Bt_ref == R * (gamma + 1) and float(th.item()) == th_ref
