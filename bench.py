@@ -201,6 +201,28 @@ def run_reference(args, w):
     return 0
 
 
+# ------------------------------------------------------------- replicas (N > 1)
+
+def replica_workload(w, rank: int):
+    """Each rank is an independent replica with its own batch: the data seed shifts by rank."""
+    return workloads.scaled(w, seed=w.seed + 1000 * rank) if rank else w
+
+
+def max_over_ranks(t_ms: float, dist, device: str = "cpu") -> float:
+    """The slowest rank's time (the whole job finishes with it); dist None: one process."""
+    if dist is None:
+        return t_ms
+    import torch
+    t = torch.tensor([t_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, w, ms_per_step: float) -> float:
+    """Positions per second of all replicas together: every rank does B * gamma per step."""
+    return world * w.B * w.gamma / (ms_per_step * 1e-3)
+
+
 # --------------------------------------------------------------------- our arm
 
 def run_ours(args, w):
@@ -223,7 +245,7 @@ def run_ours(args, w):
 
     ds.lib()
     # each rank is an independent replica with its own batch: shift the data seed by rank
-    wr = workloads.scaled(w, seed=w.seed + 1000 * rank) if rank else w
+    wr = replica_workload(w, rank)
     inp = workloads.generate(wr)
     dev = ds.to_device(inp, f"cuda:{local}")
     step = ds.Step(dev, float(inp.b_c))
@@ -253,10 +275,7 @@ def run_ours(args, w):
         ev1.record(stream)
         barrier()
     t_ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([t_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = float(t.item())
+    t_ms = max_over_ranks(t_ms, dist, "cuda")
     ms_per_step = t_ms / args.steps
     res = step.results()
 
@@ -304,7 +323,7 @@ def run_ours(args, w):
             vs.run(seed=w.seed + i, t=i)
         ms = time_graphs(vs.capture([w.seed + j for j in range(n_ring)]), n_var)
         vr = vs.results()
-        entry = {"ms_per_step": ms, "value": world * w.B * w.gamma / (ms * 1e-3),
+        entry = {"ms_per_step": ms, "value": whole_job_rate(world, w, ms),
                  "mean_ell": float(np.mean(vr["ell"])),
                  "mean_accept_len": float(np.mean(vr["accept_len"])), "B_total": vr["B_total"]}
         if sampling == "greedy" and scheduler == "theta":
@@ -337,7 +356,7 @@ def run_ours(args, w):
         dgs.append(g)
     dk_ms = time_graphs(dgs, n_var)
     variants["gumbel+theta+rnn_head"] = {
-        "ms_per_step": ms, "value": world * w.B * w.gamma / (ms * 1e-3),
+        "ms_per_step": ms, "value": whole_job_rate(world, w, ms),
         "mean_ell": float(np.mean(vr["ell"])), "mean_accept_len": float(np.mean(vr["accept_len"])),
         "B_total": vr["B_total"],
         "draft": {"ms_per_call": rd_ms, "project_ms": proj_ms, "draft_kernel_ms": dk_ms}}
@@ -397,7 +416,7 @@ def run_ours(args, w):
     launches_per_step = KERNELS_PER_STEP
     line = {
         "metric": METRIC,
-        "value": world * w.B * w.gamma / (ms_per_step * 1e-3),
+        "value": whole_job_rate(world, w, ms_per_step),
         "unit": "positions/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step,
@@ -418,7 +437,7 @@ def run_ours(args, w):
                    "B_total": res["B_total"], "theta": res["theta"]},
         "breakdown": breakdown,
         "variants": variants,
-        "e2e": {"value": world * w.B * w.gamma / e2e_s, "unit": "positions/s",
+        "e2e": {"value": whole_job_rate(world, w, e2e_s * 1e3), "unit": "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
