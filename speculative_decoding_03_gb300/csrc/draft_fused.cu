@@ -64,7 +64,8 @@ constexpr int kFirstSampler = 6;      // warps 2..5 transpose, 6..21 sample
 constexpr int kUProducerWarp = 22;    // U tiles
 constexpr int kSamplers = 16;
 constexpr int kSamplerThreads = kSamplers * 32;
-constexpr int kWStages = 4;           // W2 K-chunk ring (16 KB each at K-chunk 64)
+constexpr int kWStagesMarkov = 4;     // W2 K-chunk ring (16 KB each at K-chunk 64)
+constexpr int kRnnRecBytes = 16384;   // shared memory for a recurrence CTA's rows of Wrec
 constexpr int kDepthMarkov = 4;       // accumulators in TMEM, z tiles and U tiles in flight
 constexpr int kKChunkMax = 64;
 constexpr int kNamedBarSamplers = 1;
@@ -116,6 +117,7 @@ struct DraftParams {
 // tile / U tile less in flight.
 template <int NB, bool Rnn>
 struct Smem {
+  static constexpr int kWStages = Rnn ? 3 : kWStagesMarkov;
   static constexpr int kDepth = Rnn ? 3 : kDepthMarkov;
   static constexpr int kUStages = kDepth;
   static constexpr int kWStageBytes = 2 * kKChunkMax * 128;  // two 64-column boxes
@@ -127,7 +129,9 @@ struct Smem {
   static constexpr int kOffU = kOffW + kWStages * kWStageBytes;
   static constexpr int kOffE = kOffU + kUStages * kUStageBytes;
   static constexpr int kOffZ = kOffE + 2 * kEBytes;
-  static constexpr int kBytes = kOffZ + kDepth * kZBytes;
+  static constexpr int kOffRec = kOffZ + kDepth * kZBytes;
+  static constexpr int kRecBytes = Rnn ? kRnnRecBytes : 0;     // a recurrence CTA's Wrec rows
+  static constexpr int kBytes = kOffRec + kRecBytes;
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -185,188 +189,136 @@ __device__ __forceinline__ uint32_t bf16_rne(float x) {
 }
 __device__ __forceinline__ float bf16_val(uint32_t b) { return __uint_as_float(b << 16); }
 
-// One step of the RNN head for state entries [d0, d0 + dpc) of every request, by the 16
-// sampler warps of a recurrence CTA, which run it between the end of position k-1's tiles
-// and the publication of E_k: the CTA's z-tile buffers are idle then (the samplers have
-// consumed position k-1's tiles and nothing is transposed before E_k exists), so the gate,
-// candidate and output rows of Wrec for the CTA's entries are staged there, in rounds of
-// as many entries as fit.  An item is one (entry, request b); warp w takes items w, w + 16,
-// ...  Lane l holds L = 2r / 32 consecutive entries of [s_{k-1}[b] ; W1[x_{k-1}]] (lanes
-// 0-15 the state, 16-31 the embedding).  The predecessor tokens of four items are loaded
-// together with the staging, and each item's loads (x, and for lane 0 the hidden-state
-// block hp and s_{k-1}[b][i]) are issued one item ahead.  A warp reduction gives the
-// three pre-activations; lane 0 writes s_k[b][i], E_k[b][i] = tanh(output) and E_k's two
-// bf16 terms hi = bf16(E), lo = bf16(E - hi) for the tensor-core operand.  Everything
-// other CTAs wrote in this call (the state, the argmax keys) is read through L2.
-constexpr int kRnnMaxL = 16;           // 2r / 32 for r <= 256
-constexpr int kRnnBatch = 4;           // predecessor tokens loaded together
+// One step k of the RNN head for state entries [d0, d0 + dpc) of every request, by the 16
+// sampler warps of a recurrence CTA, after the grid barrier of position k-1 (x_{k-1} known)
+// and before E_k exists.  The CTA's z-tile buffers are idle then (position k-1's tiles are
+// consumed and nothing is transposed before E_k), so the operands go there with cp.async,
+// which holds no registers: the previous state rows s_{k-1}[b] (none at k = 1, where the
+// state is zero) and, once the argmax keys give x_{k-1}, the embedding rows W1[x_{k-1}] --
+// all of a round's copies in flight together, about two L2 round trips in all.  Requests
+// go in rounds of as many as fit.  An item is one (entry e, request b of the round); half-
+// warp h (warp h / 2, lanes 16 (h % 2) ..) takes items h, h + 32, ...  Lane l of a half-warp
+// forms the sums over the 8-entry chunks l, l + 16, ... of both halves of the 2r-long
+// operand [s_{k-1}[b] ; W1[x_{k-1}]] against the three rows of Wrec (shared memory when a
+// recurrence CTA's 3 dpc rows were staged there, row (g, e) at (g dpc + e) 2r, else global
+// memory), and four shuffles reduce them.  Lane 0 then writes s_k[b][i] = gate s_{k-1}[b][i]
+// + (1 - gate) tanh(cand), E_k[b][i] = tanh(output) and E_k's two bf16 terms
+// hi = bf16(E), lo = bf16(E - hi) for the tensor-core operand.  Everything other CTAs wrote
+// in this call (the state, the argmax keys) is read through L2.
+constexpr int kRnnHalves = 2 * kSamplers;
 
-struct RnnOperands {
-  float x[kRnnMaxL];
-  float hg, hc, ho, sold;
-};
-
-__device__ __forceinline__ void rnn_load(const DraftParams& p, int k, int i, int b, int prev,
-                                         int lane, int L, bool vec, RnnOperands& o) {
-  const int r = p.r, C = 3 * r;
-  const float* s_prev = p.state + (size_t)((k - 1) & 1) * p.B * r;
-  const int jl = (lane & 15) * L;
-  o.hg = o.hc = o.ho = o.sold = 0.f;
-  if (lane == 0) {
-    const float* hpr = p.hp + ((size_t)b * p.gamma + (k - 1)) * C;
-    o.hg = __ldg(hpr + i);
-    o.hc = __ldg(hpr + r + i);
-    o.ho = __ldg(hpr + 2 * r + i);
-    if (k > 1) o.sold = __ldcg(s_prev + (size_t)b * r + i);
-  }
-  if (lane < 16) {
-    const float* src = s_prev + (size_t)b * r + jl;
-    if (k == 1) {
-#pragma unroll
-      for (int e = 0; e < kRnnMaxL; ++e) o.x[e] = 0.f;
-    } else if (vec) {
-#pragma unroll
-      for (int q = 0; q < kRnnMaxL / 4; ++q) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (q * 4 < L) v = __ldcg(reinterpret_cast<const float4*>(src) + q);
-        o.x[4 * q] = v.x; o.x[4 * q + 1] = v.y; o.x[4 * q + 2] = v.z; o.x[4 * q + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < kRnnMaxL; ++e) o.x[e] = e < L ? __ldcg(src + e) : 0.f;
-    }
-  } else {
-    const uint16_t* src = p.W1 + (size_t)prev * r + jl;
-    if (vec) {
-#pragma unroll
-      for (int q = 0; q < kRnnMaxL / 8; ++q) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (q * 8 < L) v = __ldg(reinterpret_cast<const uint4*>(src) + q);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          o.x[8 * q + 2 * h] = bf16_val(w4[h] & 0xFFFFu);
-          o.x[8 * q + 2 * h + 1] = bf16_val(w4[h] >> 16);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < kRnnMaxL; ++e) o.x[e] = e < L ? bf16_val(__ldg(src + e)) : 0.f;
-    }
-  }
+// row (g, e) of this CTA's recurrent weights: shared memory when staged, else global
+__device__ __forceinline__ const uint16_t* rnn_row(const DraftParams& p, const uint16_t* wsm,
+                                                   int g, int e, int d0) {
+  const int R2 = 2 * p.r;
+  return wsm ? wsm + (size_t)(g * p.dpc + e) * R2 : p.Wrec + (size_t)(g * p.r + d0 + e) * R2;
 }
 
-__device__ __noinline__ void rnn_step(const DraftParams& p, int k, int d0, int sw, int lane,
-                                      int stid, uint8_t* zs, int zbytes) {
-  const int r = p.r, R2 = 2 * r, L = R2 / 32;
-  const bool vec = (L & 7) == 0;       // r a multiple of 128: 16-byte loads
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ float half_warp_sum(float a) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+  return a;
+}
+
+// a += sum over 8 entries of x (8 floats at xf, or 8 bf16 at xb) times the 8 bf16 at w
+__device__ __forceinline__ float dot8_f32(const float* xf, uint4 w, float a) {
+  const float4 x0 = reinterpret_cast<const float4*>(xf)[0];
+  const float4 x1 = reinterpret_cast<const float4*>(xf)[1];
+  a = fmaf(x0.x, bf16_val(w.x & 0xFFFFu), a); a = fmaf(x0.y, bf16_val(w.x >> 16), a);
+  a = fmaf(x0.z, bf16_val(w.y & 0xFFFFu), a); a = fmaf(x0.w, bf16_val(w.y >> 16), a);
+  a = fmaf(x1.x, bf16_val(w.z & 0xFFFFu), a); a = fmaf(x1.y, bf16_val(w.z >> 16), a);
+  a = fmaf(x1.z, bf16_val(w.w & 0xFFFFu), a); a = fmaf(x1.w, bf16_val(w.w >> 16), a);
+  return a;
+}
+__device__ __forceinline__ float dot8_bf16(uint4 x, uint4 w, float a) {
+  a = fmaf(bf16_val(x.x & 0xFFFFu), bf16_val(w.x & 0xFFFFu), a);
+  a = fmaf(bf16_val(x.x >> 16), bf16_val(w.x >> 16), a);
+  a = fmaf(bf16_val(x.y & 0xFFFFu), bf16_val(w.y & 0xFFFFu), a);
+  a = fmaf(bf16_val(x.y >> 16), bf16_val(w.y >> 16), a);
+  a = fmaf(bf16_val(x.z & 0xFFFFu), bf16_val(w.z & 0xFFFFu), a);
+  a = fmaf(bf16_val(x.z >> 16), bf16_val(w.z >> 16), a);
+  a = fmaf(bf16_val(x.w & 0xFFFFu), bf16_val(w.w & 0xFFFFu), a);
+  a = fmaf(bf16_val(x.w >> 16), bf16_val(w.w >> 16), a);
+  return a;
+}
+
+__device__ __noinline__ void rnn_step(const DraftParams& p, const uint16_t* wsm, uint8_t* zs,
+                                      int zbytes, int k, int d0, int sw, int lane, int stid) {
+  const int r = p.r, C = 3 * r, chunks = r / 8;   // 8-entry chunks per half (r % 16 == 0)
+  const int half = lane >> 4, hl = lane & 15;
+  const float* s_prev = p.state + (size_t)((k - 1) & 1) * p.B * r;
   float* s_next = p.state + (size_t)(k & 1) * p.B * r;
-  const uint16_t* ws = reinterpret_cast<const uint16_t*>(zs);
-  const int row_chunks = R2 / 8;       // 16-byte chunks per Wrec row
-  const int e_max = zbytes / (3 * R2 * 2);
-  for (int e0 = 0; e0 < p.dpc; e0 += e_max) {
-    const int ne = min(e_max, p.dpc - e0);
-    const int n_items = ne * p.B;
-    // the first four predecessor tokens of this warp, loaded with the staging
-    int pv[kRnnBatch];
-#pragma unroll
-    for (int t = 0; t < kRnnBatch; ++t) {
-      const int it = sw + t * kSamplers;
-      pv[t] = 0;
-      if (it < n_items) {
-        const int b = it % p.B;
-        pv[t] = k == 1 ? p.anchor[b] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+  const int Bc = min(p.B, zbytes / (6 * r));       // requests per round (>= 32 for r <= 256)
+  float* xs = reinterpret_cast<float*>(zs);                             // [Bc][r] s_{k-1}
+  uint16_t* xe = reinterpret_cast<uint16_t*>(zs + (size_t)Bc * r * 4);   // [Bc][r] W1 rows
+  for (int b0 = 0; b0 < p.B; b0 += Bc) {
+    const int nb = min(Bc, p.B - b0);
+    if (k > 1)
+      for (int idx = stid; idx < nb * r / 4; idx += kSamplerThreads)
+        cp_async16(xs + (size_t)idx * 4, s_prev + (size_t)b0 * r + (size_t)idx * 4);
+    for (int idx = stid; idx < nb * chunks; idx += kSamplerThreads) {
+      const int bl = idx / chunks, q = idx - bl * chunks, b = b0 + bl;
+      int prev = k == 1 ? p.anchor[b] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+      if (prev < 0 || prev >= p.V) {
+        if (q == 0) set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
+        prev = 0;
       }
+      cp_async16(xe + (size_t)bl * r + q * 8, p.W1 + (size_t)prev * r + q * 8);
     }
-    // rows (g, e) = Wrec[g r + d0 + e0 + e], g = gate / candidate / output, e < ne
-    for (int idx = stid; idx < 3 * ne * row_chunks; idx += kSamplerThreads) {
-      const int row = idx / row_chunks, q = idx - row * row_chunks;
-      const int g = row / ne, e = row - g * ne;
-      reinterpret_cast<uint4*>(zs)[idx] =
-          __ldg(reinterpret_cast<const uint4*>(p.Wrec + (size_t)(g * r + d0 + e0 + e) * R2) + q);
-    }
+    cp_async_wait_all();
     named_bar_sync(kNamedBarSamplers, kSamplerThreads);
-    for (int it0 = sw; it0 < n_items; it0 += kRnnBatch * kSamplers) {
-      if (it0 != sw) {
-#pragma unroll
-        for (int t = 0; t < kRnnBatch; ++t) {
-          const int it = it0 + t * kSamplers;
-          pv[t] = 0;
-          if (it < n_items) {
-            const int b = it % p.B;
-            pv[t] = k == 1 ? p.anchor[b] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
-          }
+    const int n_items = p.dpc * nb;
+    for (int base = 2 * sw; base < n_items; base += kRnnHalves) {
+      const int it = base + half;
+      const bool valid = it < n_items;
+      const int e = valid ? it / nb : 0, bl = valid ? it - e * nb : 0, i = d0 + e;
+      const uint16_t* wg = rnn_row(p, wsm, 0, e, d0);
+      const uint16_t* wc = rnn_row(p, wsm, 1, e, d0);
+      const uint16_t* wo = rnn_row(p, wsm, 2, e, d0);
+      float hg = 0.f, hc = 0.f, ho = 0.f;
+      if (valid && hl == 0) {
+        const float* hpr = p.hp + ((size_t)(b0 + bl) * p.gamma + (k - 1)) * C + i;
+        hg = __ldg(hpr);
+        hc = __ldg(hpr + r);
+        ho = __ldg(hpr + 2 * r);
+      }
+      float ag = 0.f, ac = 0.f, ao = 0.f;
+      for (int q = hl; q < chunks; q += 16) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xe + (size_t)bl * r + q * 8);
+        ag = dot8_bf16(xv, *reinterpret_cast<const uint4*>(wg + r + q * 8), ag);
+        ac = dot8_bf16(xv, *reinterpret_cast<const uint4*>(wc + r + q * 8), ac);
+        ao = dot8_bf16(xv, *reinterpret_cast<const uint4*>(wo + r + q * 8), ao);
+        if (k > 1) {
+          const float* xf = xs + (size_t)bl * r + q * 8;
+          ag = dot8_f32(xf, *reinterpret_cast<const uint4*>(wg + q * 8), ag);
+          ac = dot8_f32(xf, *reinterpret_cast<const uint4*>(wc + q * 8), ac);
+          ao = dot8_f32(xf, *reinterpret_cast<const uint4*>(wo + q * 8), ao);
         }
       }
-#pragma unroll
-      for (int t = 0; t < kRnnBatch; ++t) {
-        if (pv[t] < 0 || pv[t] >= p.V) {
-          if (it0 + t * kSamplers < n_items && lane == 0) set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
-          pv[t] = 0;
-        }
-      }
-      RnnOperands cur, nxt;
-      rnn_load(p, k, d0 + e0 + it0 / p.B, it0 % p.B, pv[0], lane, L, vec, cur);
-#pragma unroll
-      for (int t = 0; t < kRnnBatch; ++t) {
-        const int it = it0 + t * kSamplers;
-        if (it >= n_items) break;
-        const int e = it / p.B, b = it - e * p.B, i = d0 + e0 + e;
-        const int itn = it + kSamplers;
-        if (t + 1 < kRnnBatch && itn < n_items)
-          rnn_load(p, k, d0 + e0 + itn / p.B, itn % p.B, pv[t + 1], lane, L, vec, nxt);
-        // this lane's L weights of the three rows, from shared memory
-        const uint16_t* wg = ws + (size_t)(0 * ne + e) * R2 + lane * L;
-        const uint16_t* wc = ws + (size_t)(1 * ne + e) * R2 + lane * L;
-        const uint16_t* wo = ws + (size_t)(2 * ne + e) * R2 + lane * L;
-        float ag = 0.f, ac = 0.f, ao = 0.f;
-        if (vec) {
-          // 16-byte shared loads (lane stride L * 2 bytes: at most two-way bank conflicts)
-#pragma unroll
-          for (int q = 0; q < kRnnMaxL / 8; ++q) {
-            if (q * 8 >= L) break;
-            const uint4 g4 = reinterpret_cast<const uint4*>(wg)[q];
-            const uint4 c4 = reinterpret_cast<const uint4*>(wc)[q];
-            const uint4 o4 = reinterpret_cast<const uint4*>(wo)[q];
-            const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, cw[4] = {c4.x, c4.y, c4.z, c4.w},
-                           ow[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-              const int sh = (h & 1) ? 16 : 0;
-              const float xv = cur.x[8 * q + h];
-              ag = fmaf(xv, bf16_val((gw[h >> 1] >> sh) & 0xFFFFu), ag);
-              ac = fmaf(xv, bf16_val((cw[h >> 1] >> sh) & 0xFFFFu), ac);
-              ao = fmaf(xv, bf16_val((ow[h >> 1] >> sh) & 0xFFFFu), ao);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int e2 = 0; e2 < kRnnMaxL; ++e2) {
-            if (e2 >= L) break;
-            ag = fmaf(cur.x[e2], bf16_val(wg[e2]), ag);
-            ac = fmaf(cur.x[e2], bf16_val(wc[e2]), ac);
-            ao = fmaf(cur.x[e2], bf16_val(wo[e2]), ao);
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          ag += __shfl_xor_sync(0xffffffffu, ag, o);
-          ac += __shfl_xor_sync(0xffffffffu, ac, o);
-          ao += __shfl_xor_sync(0xffffffffu, ao, o);
-        }
-        if (lane == 0) {
-          const float gate = 1.f / (1.f + expf(-(ag + cur.hg)));
-          s_next[(size_t)b * r + i] = gate * cur.sold + (1.f - gate) * tanhf(ac + cur.hc);
-          const float ev = tanhf(ao + cur.ho);
-          p.E_all[((size_t)b * p.gamma + (k - 1)) * r + i] = ev;
-          const uint32_t hi = bf16_rne(ev);
-          p.E_hl[(size_t)b * 2 * r + i] = (uint16_t)hi;
-          p.E_hl[(size_t)b * 2 * r + r + i] = (uint16_t)bf16_rne(ev - bf16_val(hi));
-        }
-        cur = nxt;
+      ag = half_warp_sum(ag);
+      ac = half_warp_sum(ac);
+      ao = half_warp_sum(ao);
+      if (valid && hl == 0) {
+        const int b = b0 + bl;
+        const float sold = k > 1 ? xs[(size_t)bl * r + i] : 0.f;
+        const float gate = 1.f / (1.f + expf(-(ag + hg)));
+        s_next[(size_t)b * r + i] = gate * sold + (1.f - gate) * tanhf(ac + hc);
+        const float ev = tanhf(ao + ho);
+        p.E_all[((size_t)b * p.gamma + (k - 1)) * r + i] = ev;
+        const uint32_t hi = bf16_rne(ev);
+        p.E_hl[(size_t)b * 2 * r + i] = (uint16_t)hi;
+        p.E_hl[(size_t)b * 2 * r + r + i] = (uint16_t)bf16_rne(ev - bf16_val(hi));
       }
     }
-    named_bar_sync(kNamedBarSamplers, kSamplerThreads);   // the rows are read before restaging
+    named_bar_sync(kNamedBarSamplers, kSamplerThreads);   // the rows are read before the next round
   }
 }
 
@@ -422,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     const DraftParams p) {
   using S = Smem<NB, Rnn>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t w_full[kWStages], w_empty[kWStages];
+  __shared__ uint64_t w_full[S::kWStages], w_empty[S::kWStages];
   __shared__ uint64_t u_full[S::kUStages], u_empty[S::kUStages];
   __shared__ uint64_t e_full[2], e_empty[2];
   __shared__ uint64_t acc_full[S::kDepth], acc_empty[S::kDepth];
@@ -446,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   while (tmem_cols < (uint32_t)(S::kDepth * S::kNE)) tmem_cols <<= 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
+    for (int i = 0; i < S::kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
     for (int i = 0; i < S::kUStages; ++i) { mbar_init(&u_full[i], 1); mbar_init(&u_empty[i], kSamplers); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&e_full[i], 1);
@@ -512,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         for (int t = t_lo; t < t_hi && ok; ++t) {
           const int v0 = t * kGemmTileV;
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
-            const int s = ws % kWStages;
-            if (!(ok = wait1(&w_empty[s], ((ws / kWStages) & 1) ^ 1))) break;
+            const int s = ws % S::kWStages;
+            if (!(ok = wait1(&w_empty[s], ((ws / S::kWStages) & 1) ^ 1))) break;
             uint8_t* dst = smem + S::kOffW + s * S::kWStageBytes;
             mbar_arrive_expect_tx(&w_full[s], w_bytes);
             if (p.W2p) {
@@ -534,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       }
       // drain: every issued copy has landed before the CTA may exit (a stage whose wait
       // failed above was never issued, so only stages below ws are in flight)
-      for (uint32_t i = ws > (uint32_t)kWStages ? ws - kWStages : 0; i < ws; ++i)
-        mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, kTimeoutNs);
+      for (uint32_t i = ws > (uint32_t)S::kWStages ? ws - S::kWStages : 0; i < ws; ++i)
+        mbar_wait(&w_full[i % S::kWStages], (i / S::kWStages) & 1, kTimeoutNs);
     }
     __syncwarp();
   } else if (warp == kUProducerWarp) {
@@ -597,10 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + (uint32_t)(ab * S::kNE);
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
-            const int s = ws % kWStages;
+            const int s = ws % S::kWStages;
             // TMA data: the barrier's transaction count orders it before the MMAs; no
             // tcgen05 fence here (a fence per chunk would serialise on MMA completion)
-            if (!(ok = wait1(&w_full[s], (ws / kWStages) & 1))) break;
+            if (!(ok = wait1(&w_full[s], (ws / S::kWStages) & 1))) break;
             const uint64_t a_s = a_base + (uint64_t)((s * S::kWStageBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
@@ -678,6 +630,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     const int stid = threadIdx.x - kFirstSampler * 32;
     const uint32_t k0 = (uint32_t)p.seed, k1 = (uint32_t)(p.seed >> 32);
     uint32_t tc = 0;
+    // RNN head: a recurrence CTA stages its rows of Wrec (gate, candidate and output of its
+    // dpc state entries) in shared memory once, when they fit; the samplers' named barrier
+    // ahead of the first recurrence step orders the copy before any use
+    const uint16_t* wrec_s = nullptr;
+    if constexpr (Rnn) {
+      if (cta < p.n_rec && 3 * p.dpc * 4 * p.r <= S::kRecBytes) {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(smem + S::kOffRec);
+        const int R2 = 2 * p.r, chunks = R2 / 8;   // 16-byte chunks per row
+        for (int idx = stid; idx < 3 * p.dpc * chunks; idx += kSamplerThreads) {
+          const int row = idx / chunks, q = idx - row * chunks;
+          const int g = row / p.dpc, e = row - g * p.dpc;
+          reinterpret_cast<uint4*>(dst)[idx] = __ldg(
+              reinterpret_cast<const uint4*>(p.Wrec + (size_t)(g * p.r + cta * p.dpc + e) * R2) + q);
+        }
+        wrec_s = dst;
+      }
+    }
     // The first kGatherWarps sampler warps publish the E operand of job `j` (chunk c,
     // position k): E = W1[x_{k-1}] as the K-major, 128-byte-swizzled B operand (16-byte
     // chunk q of row n goes to chunk (q % 8) ^ (n % 8) of line n of K-block q / 8).  Thread
@@ -710,7 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         named_bar_sync(kNamedBarSamplers, kSamplerThreads);
         // called by every sampler thread whatever the abort flag says (the step's named
         // barriers need all of them; it has no other waits)
-        rnn_step(p, k, cta * p.dpc, sw, lane, stid, smem + S::kOffZ, S::kDepth * S::kZBytes);
+        rnn_step(p, wrec_s, smem + S::kOffZ, S::kDepth * S::kZBytes, k, cta * p.dpc, sw, lane,
+                 stid);
         named_bar_sync(kNamedBarSamplers, kSamplerThreads);
         if (stid == 0)
           asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.rec_count) : "memory");
