@@ -18,12 +18,14 @@
 //                   shared-memory rings with TMA; neither depends on the drafted tokens,
 //                   so the rings run ahead across positions while the CTA waits for x_k;
 //   MMA warp        issues tcgen05.mma (M = 128 vocabulary rows, N = NB requests, K = r)
-//                   into one of two tensor-memory accumulators;
-//   4 transposers   read the accumulator (lane = vocabulary row) and write the bias
-//                   rows [b][v] to shared memory (four accumulators and four bias tiles
-//                   in flight, so the MMA, transposer and sampler stages overlap);
-//   16 samplers     add the U tile to the bias rows (both row-contiguous, 128-bit shared
-//                   loads) to get z rows; each warp owns NB/16
+//                   into one of four tensor-memory accumulators;
+//   4 transposers   read the accumulator (lane = vocabulary row) and add it to the U
+//                   tile in place, so the U stage holds the z rows [b][v] (four
+//                   accumulators and four U / z tiles in flight, so the MMA, transposer
+//                   and sampler stages overlap; without a separate z ring the W2 ring
+//                   gets the shared memory for eight stages);
+//   16 samplers     read the z rows (row-contiguous, 128-bit shared loads); each warp owns
+//                   NB/16
 //                   requests and keeps, per request, a lazy softmax reference M, per-lane
 //                   sums of exp(z - M) and maxima, and the best exact Gumbel score
 //                   z* - log E*.  Since w <= E = -log(1 - w) <= w / (1 - w) (w = 1 - u),
@@ -64,7 +66,7 @@ constexpr int kFirstSampler = 6;      // warps 2..5 transpose, 6..21 sample
 constexpr int kUProducerWarp = 22;    // U tiles
 constexpr int kSamplers = 16;
 constexpr int kSamplerThreads = kSamplers * 32;
-constexpr int kWStagesMarkov = 4;     // W2 K-chunk ring (16 KB each at K-chunk 64)
+constexpr int kWStagesMarkov = 8;     // W2 K-chunk ring (16 KB each at K-chunk 64)
 constexpr int kRnnRecBytes = 16384;   // shared memory for a recurrence CTA's rows of Wrec
 constexpr int kDepthMarkov = 4;       // accumulators in TMEM, z tiles and U tiles in flight
 constexpr int kKChunkMax = 64;
@@ -112,9 +114,11 @@ struct DraftParams {
   int n_rec, dpc;                  // recurrence CTAs, state entries per recurrence CTA
 };
 
-// Shared-memory layout.  The RNN head's E operand has 2 NB rows (the hi and the lo bf16
-// image of each request's row, see the MMA issue loop), so it takes one accumulator / z
-// tile / U tile less in flight.
+// Shared-memory layout: the W2 ring, the U ring (whose stages the transposers turn into
+// z tiles in place), two E operand buffers, and for the RNN head the recurrence's scratch
+// and its Wrec rows.  The RNN head's E operand has 2 NB rows (the hi and the lo bf16 image
+// of each request's row, see the MMA issue loop), so it takes one accumulator and U tile
+// less in flight and a 3-stage W2 ring.
 template <int NB, bool Rnn>
 struct Smem {
   static constexpr int kWStages = Rnn ? 3 : kWStagesMarkov;
@@ -124,12 +128,12 @@ struct Smem {
   static constexpr int kUStageBytes = NB * 128 * 4;
   static constexpr int kNE = Rnn ? 2 * NB : NB;               // rows of the E operand (MMA N)
   static constexpr int kEBytes = kNE * 256 * 2;               // up to r = 256
-  static constexpr int kZBytes = NB * 128 * 4;
+  static constexpr int kZBytes = NB * 128 * 4;             // RNN: the recurrence's scratch
   static constexpr int kOffW = 0;
   static constexpr int kOffU = kOffW + kWStages * kWStageBytes;
   static constexpr int kOffE = kOffU + kUStages * kUStageBytes;
   static constexpr int kOffZ = kOffE + 2 * kEBytes;
-  static constexpr int kOffRec = kOffZ + kDepth * kZBytes;
+  static constexpr int kOffRec = kOffZ + (Rnn ? kDepth * kZBytes : 0);
   static constexpr int kRecBytes = Rnn ? kRnnRecBytes : 0;     // a recurrence CTA's Wrec rows
   static constexpr int kBytes = kOffRec + kRecBytes;
 };
@@ -191,9 +195,8 @@ __device__ __forceinline__ float bf16_val(uint32_t b) { return __uint_as_float(b
 
 // One step k of the RNN head for state entries [d0, d0 + dpc) of every request, by the 16
 // sampler warps of a recurrence CTA, after the grid barrier of position k-1 (x_{k-1} known)
-// and before E_k exists.  The CTA's z-tile buffers are idle then (position k-1's tiles are
-// consumed and nothing is transposed before E_k), so the operands go there with cp.async,
-// which holds no registers: the previous state rows s_{k-1}[b] (none at k = 1, where the
+// and before E_k exists.  The operands go to a scratch region of shared memory (the size
+// of three z tiles) with cp.async, which holds no registers: the previous state rows s_{k-1}[b] (none at k = 1, where the
 // state is zero) and, once the argmax keys give x_{k-1}, the embedding rows W1[x_{k-1}] --
 // all of a round's copies in flight together, about two L2 round trips in all.  Requests
 // go in rounds of as many as fit.  An item is one (entry e, request b of the round); half-
@@ -378,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
   __shared__ uint64_t u_full[S::kUStages], u_empty[S::kUStages];
   __shared__ uint64_t e_full[2], e_empty[2];
   __shared__ uint64_t acc_full[S::kDepth], acc_empty[S::kDepth];
-  __shared__ uint64_t z_full[S::kDepth], z_empty[S::kDepth];
+  __shared__ uint64_t z_full[S::kDepth];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -408,7 +411,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
       mbar_init(&z_full[i], 4);
-      mbar_init(&z_empty[i], kSamplers);
     }
     mbar_init(&mma_drain, 1);
     abort_s = 0;
@@ -593,10 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         const uint32_t par = (tc / S::kDepth) & 1;
         if (!(ok = wait_warp(&acc_full[ab], par))) break;
         tc_fence_after_sync();
-        if (!(ok = wait_warp(&z_empty[ab], par ^ 1))) break;
-        float* Zs = reinterpret_cast<float*>(smem + S::kOffZ + ab * S::kZBytes);
+        // the U tile of the same tile count (the U ring has the accumulators' depth)
+        if (!(ok = wait_warp(&u_full[ab], par))) break;
+        float* Zs = reinterpret_cast<float*>(smem + S::kOffU + ab * S::kUStageBytes);
         if constexpr (Rnn) {
-          // bias = the hi columns + the lo columns, 16 requests at a time
+          // bias = the hi columns + the lo columns, 16 requests at a time; z = bias + U
 #pragma unroll
           for (int c16 = 0; c16 < NB; c16 += 16) {
             float vh[16], vlo[16];
@@ -604,7 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
             tmem_ld_32x32b_x16(trow + (uint32_t)(ab * S::kNE + NB + c16), vlo);
             tmem_ld_wait();
 #pragma unroll
-            for (int b = 0; b < 16; ++b) Zs[(c16 + b) * 128 + vl] = vh[b] + vlo[b];
+            for (int b = 0; b < 16; ++b) {
+              float* zp = Zs + (c16 + b) * 128 + vl;
+              *zp = (vh[b] + vlo[b]) + *zp;
+            }
           }
         } else {
           float vals[NB];
@@ -613,9 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
             tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16), *reinterpret_cast<float(*)[16]>(vals + c16));
           tmem_ld_wait();
 #pragma unroll
-          for (int b = 0; b < NB; ++b) Zs[b * 128 + vl] = vals[b];
+          for (int b = 0; b < NB; ++b) Zs[b * 128 + vl] = vals[b] + Zs[b * 128 + vl];
         }
         tc_fence_before_sync();
+        // the stage is next written by the U producer's TMA (async proxy)
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&acc_empty[ab]);
@@ -819,9 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         const int zb = tc % S::kDepth;
         const uint32_t par = (tc / S::kDepth) & 1;
         if (!wait_warp(&z_full[zb], par)) continue;
-        if (!wait_warp(&u_full[zb], par)) continue;
-        const float* Zs = reinterpret_cast<const float*>(smem + S::kOffZ + zb * S::kZBytes);
-        const float* Us = reinterpret_cast<const float*>(smem + S::kOffU + zb * S::kUStageBytes);
+        const float* Zs = reinterpret_cast<const float*>(smem + S::kOffU + zb * S::kUStageBytes);
         const int v = (t_lo + t) * kGemmTileV + 4 * lane;
         const bool ragged = (t_lo + t + 1) * kGemmTileV > p.V;
         // A: the logits of this lane's 4 vocabulary entries for each row
@@ -829,8 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
           const float4 z4 = *reinterpret_cast<const float4*>(Zs + (sw * RPW + i) * 128 + 4 * lane);
-          const float4 u4 = *reinterpret_cast<const float4*>(Us + (sw * RPW + i) * 128 + 4 * lane);
-          z[i][0] = z4.x + u4.x; z[i][1] = z4.y + u4.y; z[i][2] = z4.z + u4.z; z[i][3] = z4.w + u4.w;
+          z[i][0] = z4.x; z[i][1] = z4.y; z[i][2] = z4.z; z[i][3] = z4.w;
           if (ragged) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -941,10 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
           }
         }
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&z_empty[zb]);
-          mbar_arrive(&u_empty[zb]);
-        }
+        if (lane == 0) mbar_arrive(&u_empty[zb]);
       }
       // publish this CTA's partials of the job's requests: the warp reductions of all its
       // rows first, then the stores and atomics.  No fence here: the thread that counts
