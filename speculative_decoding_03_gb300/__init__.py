@@ -581,6 +581,10 @@ class Step:
                 host_out[k].copy_(self.verify_out[k], non_blocking=True)
         return host_out
 
+    def pipeline(self):
+        """A HostPipeline over this step (see there)."""
+        return HostPipeline(self)
+
     def step_bytes(self):
         """(host->device, device->host) bytes of one run_from_host call."""
         h2d = sum(self.dev[k].numel() * self.dev[k].element_size() for k in self.STEP_INPUTS)
@@ -598,6 +602,62 @@ class Step:
             out["theta"] = float(self.sched_out[2].item())
         out.update({k: v.cpu().numpy() for k, v in self.verify_out.items()})
         return out
+
+
+class HostPipeline:
+    """Steps fed from pinned host buffers, with the next step's host->device copies
+    overlapped with the current step's kernels.
+
+    The step's per-step inputs get a second device copy; step i reads input set i % 2,
+    whose copies run on a separate copy stream and are ordered before the step by an
+    event, and step i + 2's copies into the same set wait for an event recorded after
+    step i's kernels.  Every step's inputs are still copied from the host and every
+    step's verified tokens are copied back, on the step's stream.  The step object is
+    given its own dictionary of device tensors, so the caller's dictionary is unchanged.
+    """
+
+    def __init__(self, step: "Step"):
+        torch = _torch()
+        self.step = step
+        step.dev = dict(step.dev)
+        dev0 = {k: step.dev[k] for k in step.STEP_INPUTS}
+        self.sets = [dev0, {k: torch.empty_like(v) for k, v in dev0.items()}]
+        device = dev0["U"].device
+        self.copy_stream = torch.cuda.Stream(device=device)
+        self.ready = [torch.cuda.Event(), torch.cuda.Event()]
+        self.free = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def _copy_in(self, i: int, host_in: Dict):
+        torch = _torch()
+        b = i % 2
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.free[b])
+            for k, v in self.sets[b].items():
+                v.copy_(host_in[k], non_blocking=True)
+            self.ready[b].record(self.copy_stream)
+
+    def run(self, seeds, host_ins, host_outs, stream=None):
+        """Steps i = 0.. with seed seeds[i], inputs host_ins[i] and outputs host_outs[i]
+        (dicts of pinned tensors shaped like Step.pinned_host_buffers()); returns after
+        enqueueing everything on `stream` (default: the current stream)."""
+        torch = _torch()
+        s = stream if stream is not None else torch.cuda.current_stream()
+        n = len(seeds)
+        if n == 0:
+            return host_outs
+        self._copy_in(0, host_ins[0])
+        for i in range(n):
+            if i + 1 < n:
+                self._copy_in(i + 1, host_ins[i + 1])
+            b = i % 2
+            s.wait_event(self.ready[b])
+            self.step.dev.update(self.sets[b])
+            self.step.run(seeds[i], s, t=i)
+            self.free[b].record(s)
+            with torch.cuda.stream(s):
+                for k in self.step.STEP_OUTPUTS:
+                    host_outs[i][k].copy_(self.step.verify_out[k], non_blocking=True)
+        return host_outs
 
 
 def to_device(inp, device="cuda") -> Dict:
