@@ -917,14 +917,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
               for (int j = 0; j < 4; ++j)
                 if ((cm[i] >> j) & 1u) L = fmaxf(L, e[i][j] * (1.f - w[i][j]) * rcp_approx(w[i][j]));
               const float Teff = fmaxf(Tf[i], warp_max(L) * kShrink);
+              unsigned sm = 0u;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                sm |= (((cm[i] >> j) & 1u) && e[i][j] > Teff * w[i][j] ? 1u : 0u) << j;
               float sc = -INFINITY, szz = -INFINITY;
               int sv = 0x7FFFFFFF;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                if (((cm[i] >> j) & 1u) && e[i][j] > Teff * w[i][j]) {
-                  const float scj = z[i][j] - logf(exp1_from_w(w[i][j]));
-                  if (scj > sc) { sc = scj; sv = v + j; szz = z[i][j]; }
-                }
+              // exact scores for the survivors only (about one per warp and tile), in
+              // increasing j as before, so that equal scores keep the smallest index: a loop
+              // over the set bits runs the logarithms once per survivor instead of under a
+              // predicate for every element
+              while (sm) {
+                const int j = __ffs(sm) - 1;
+                sm &= sm - 1u;
+                const float wj = j == 0 ? w[i][0] : j == 1 ? w[i][1] : j == 2 ? w[i][2] : w[i][3];
+                const float zj = j == 0 ? z[i][0] : j == 1 ? z[i][1] : j == 2 ? z[i][2] : z[i][3];
+                const float scj = zj - logf(exp1_from_w(wj));
+                if (scj > sc) { sc = scj; sv = v + j; szz = zj; }
               }
               // the warp's best (largest score, then smallest index): two integer reductions,
               // a ballot and one shuffle
