@@ -90,6 +90,29 @@ def test_rnn_project(name):
     np.testing.assert_array_less(np.abs(got - ref), RTOL * (mag + np.abs(b_rnn)) + 1e-12)
 
 
+# the projection alone on shapes that span its tiles: the full hidden size of the
+# 32 x 7, r = 256 workload (40 K chunks, 5 per cluster rank, 6 column tiles, 2 row tiles);
+# 144 output columns (a partial second column tile) with a ragged last K chunk (H = 1000);
+# 600 rows (5 row tiles) with a K that gives most cluster ranks no chunk at all (H = 12)
+PROJECT_SHAPES = {
+    "B32_g7_r256_H2560": dict(B=32, gamma=7, r=256, H=2560),
+    "B9_g3_r48_H1000": dict(B=9, gamma=3, r=48, H=1000),
+    "B300_g2_r16_H12": dict(B=300, gamma=2, r=16, H=12),
+}
+
+
+@pytest.mark.parametrize("name", list(PROJECT_SHAPES))
+def test_rnn_project_tiles(name):
+    _need_gpu()
+    w = workloads.scaled(workloads.get("qwen3_4b_like"), V=1024, **PROJECT_SHAPES[name])
+    inp, W_rnn, b_rnn, dev = _setup(w, with_T=False)
+    got = ds.rnn_project(dev["h"], dev["W_rnn"], dev["b_rnn"]).cpu().numpy()
+    ref = oracle.rnn_project(inp.h, W_rnn, b_rnn)
+    assert np.all(np.isfinite(got))
+    mag = np.abs(inp.h).astype(np.float64) @ np.abs(bf16_bits_to_f32(W_rnn)[2 * w.r:]).astype(np.float64)
+    np.testing.assert_array_less(np.abs(got - ref), RTOL * (mag + np.abs(b_rnn)) + 1e-12)
+
+
 @pytest.mark.parametrize("greedy", [False, True])
 @pytest.mark.parametrize("name", list(CASES))
 def test_draft_rnn(name, greedy):
