@@ -342,7 +342,9 @@ dspark_status dspark_schedule_threshold(const float* a, int R, int gamma, float 
  *   aligned; once per weights).
  *   dspark_rnn_project: hp[b, k, c] = b_rnn[c] + sum_j h[b, k, j] W_rnn[2r + j][c] for every
  *   (b, k) -- the part of the layer that does not depend on drafted tokens.  h [B, gamma, H]
- *   fp32 (H % 4 == 0), hp [B, gamma, 3r] fp32; all 16-byte aligned.
+ *   fp32 (H % 4 == 0), hp [B, gamma, 3r] fp32; all 16-byte aligned.  Computed on the tensor
+ *   cores with fp32 accuracy (h as three exact bf16 terms).  The call has no status word: if
+ *   one of its bounded device waits runs out, the affected 128 x 128 tiles of hp are NaN.
  *   dspark_draft_rnn: dspark_draft (greedy == 0) or dspark_draft_greedy (greedy != 0) with
  *   the RNN head's bias in place of the Markov bias: exactly one of W2 and W2p non-NULL,
  *   Wrec from dspark_rnn_pack, hp from dspark_rnn_project.  Also writes E [B, gamma, r]
