@@ -252,6 +252,39 @@ def test_full_size_draft_sampled_requests(name):
     assert ties <= 1
 
 
+def test_full_size_step_sampled_requests():
+    """The step as the benchmark runs it (packed W2, the scheduler in the confidence
+    kernel's last CTA, the packed verification) on the full 32 x 7 x 151936, r = 256
+    workload.  The oracle recomputes sampled requests: their draft, the confidence and
+    survival of the drafted tokens, and the verification of those tokens with the
+    verified lengths; the schedule is recomputed over every request's survival."""
+    _need_gpu()
+    w = workloads.get("qwen3_4b_like")
+    inp = workloads.generate(w)
+    step = ds.Step(ds.to_device(inp), float(inp.b_c)).run(seed=w.seed)
+    got = step.results()
+    assert step.ws.status() == 0
+    picks = sorted({0, 5, w.B // 2, w.B - 1})
+    sub = workloads.generate(w, requests=picks)
+    ref = oracle.draft(sub.U, sub.W1, sub.W2, sub.anchor, w.seed, req_ids=picks)
+    ties = _compare_tokens(got["tokens"][picks], ref["tokens"], ref["gap"], "full step")
+    assert ties <= 1
+    c, a = oracle.confidence(sub.h, sub.anchor, got["tokens"][picks], sub.W1, sub.w_c, float(sub.b_c))
+    np.testing.assert_allclose(got["c"][picks], c, rtol=RTOL)
+    np.testing.assert_allclose(got["a"][picks], a, rtol=RTOL)
+    ell, B_total, _ = oracle.schedule(got["a"], inp.sps)
+    np.testing.assert_array_equal(got["ell"], ell)
+    assert got["B_total"] == B_total
+    v = oracle.verify(sub.T, sub.U, sub.W1, sub.W2, sub.anchor, got["tokens"][picks],
+                      got["ell"][picks], w.seed, req_ids=picks)
+    for i, b in enumerate(picks):
+        if np.array_equal(got["out_tokens"][b], v["out_tokens"][i]):
+            continue
+        band = v["band"][i]
+        assert (np.any(~np.isnan(band)) and np.nanmin(band) <= TIE) or v["gap"][i] <= TIE, b
+    np.testing.assert_array_equal(got["n_out"], got["accept_len"] + 1)
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_draft_packed_matches_draft(name):
     """The packed-weights draft runs the same kernel arithmetic: identical outputs."""
