@@ -313,7 +313,7 @@ dspark_status dspark_draft_rnn(const float* U, const uint16_t* W1, const uint16_
   rnn.hp = hp;
   rnn.E_all = E;
   rnn.state = ws_at<float>(workspace, p.off_rnn_state);
-  rnn.E_hl = reinterpret_cast<uint16_t*>(rnn.state + (size_t)2 * B * r);
+  rnn.E_hl = reinterpret_cast<uint16_t*>(rnn.state + (size_t)kRnnStateCopies * 2 * B * r);
   if (launch_draft_fused_rnn(W1, W2, W2p, U, anchor, B, gamma, V, r, seed, greedy != 0, rnn, tokens,
                              q_tok, row_max, row_sumexp, ws_at<char>(workspace, p.off_draft),
                              ws_at<int>(workspace, p.off_err), stream) != cudaSuccess)

@@ -68,6 +68,14 @@ constexpr int kSamplers = 16;
 constexpr int kSamplerThreads = kSamplers * 32;
 constexpr int kWStagesMarkov = 8;     // W2 K-chunk ring (16 KB each at K-chunk 64)
 constexpr int kRnnRecBytes = 16384;   // shared memory for a recurrence CTA's rows of Wrec
+// The state and the E rows are read by every CTA right after the recurrence CTAs write
+// them: 152 CTAs reading the same lines at once queue on the few L2 slices that hold them
+// (measured: 4.2 us for a 32 KB gather against 2.2 us when each CTA reads other lines), so
+// the writers keep kRnnCopies copies and CTA c reads copy c % kRnnCopies.  Every copy
+// costs the writers stores before their release; two copies measured best (RNN draft
+// 209.7 / 203.3 / 204.6 / 208.5 us with 1 / 2 / 4 / 8 copies).
+constexpr int kRnnCopies = kRnnStateCopies;
+static_assert(kRnnCopies <= 16, "one copy per lane of a half-warp");
 constexpr int kDepthMarkov = 4;       // accumulators in TMEM, z tiles and U tiles in flight
 constexpr int kKChunkMax = 64;
 constexpr int kNamedBarSamplers = 1;
@@ -108,8 +116,8 @@ struct DraftParams {
   const uint16_t* Wrec;            // [3r][2r] the recurrent rows of W_rnn, transposed
   const float* hp;                 // [B][gamma][3r] hidden-state block of the layer, with bias
   float* E_all;                    // [B][gamma][r] tanh(output) of every position (written)
-  uint16_t* E_hl;                  // [B][2][r] the current position's rows as bf16 hi and lo
-  float* state;                    // [2][B][r] s_{k-1} / s_k
+  uint16_t* E_hl;                  // [kRnnCopies][B][2][r] the current position's rows as bf16 hi, lo
+  float* state;                    // [kRnnCopies][2][B][r] s_{k-1} / s_k
   unsigned int* rec_count;         // arrivals of the recurrence CTAs
   int n_rec, dpc;                  // recurrence CTAs, state entries per recurrence CTA
 };
@@ -257,8 +265,9 @@ __device__ __noinline__ void rnn_step(const DraftParams& p, const uint16_t* wsm,
                                       int zbytes, int k, int d0, int sw, int lane, int stid) {
   const int r = p.r, C = 3 * r, chunks = r / 8;   // 8-entry chunks per half (r % 16 == 0)
   const int half = lane >> 4, hl = lane & 15;
-  const float* s_prev = p.state + (size_t)((k - 1) & 1) * p.B * r;
-  float* s_next = p.state + (size_t)(k & 1) * p.B * r;
+  const size_t scopy = (size_t)2 * p.B * r;        // floats per state copy
+  const float* s_prev = p.state + (blockIdx.x % kRnnCopies) * scopy + (size_t)((k - 1) & 1) * p.B * r;
+  float* s_next = p.state + (size_t)(k & 1) * p.B * r;  // copy 0; every copy is written
   const int Bc = min(p.B, zbytes / (6 * r));       // requests per round (>= 32 for r <= 256)
   float* xs = reinterpret_cast<float*>(zs);                             // [Bc][r] s_{k-1}
   uint16_t* xe = reinterpret_cast<uint16_t*>(zs + (size_t)Bc * r * 4);   // [Bc][r] W1 rows
@@ -287,7 +296,7 @@ __device__ __noinline__ void rnn_step(const DraftParams& p, const uint16_t* wsm,
       const uint16_t* wc = rnn_row(p, wsm, 1, e, d0);
       const uint16_t* wo = rnn_row(p, wsm, 2, e, d0);
       float hg = 0.f, hc = 0.f, ho = 0.f;
-      if (valid && hl == 0) {
+      if (valid) {                        // every lane of the half-warp: one address each
         const float* hpr = p.hp + ((size_t)(b0 + bl) * p.gamma + (k - 1)) * C + i;
         hg = __ldg(hpr);
         hc = __ldg(hpr + r);
@@ -309,16 +318,22 @@ __device__ __noinline__ void rnn_step(const DraftParams& p, const uint16_t* wsm,
       ag = half_warp_sum(ag);
       ac = half_warp_sum(ac);
       ao = half_warp_sum(ao);
-      if (valid && hl == 0) {
+      if (valid) {
+        // every lane has the sums; lane c of the half-warp writes copy c of s_k and of the
+        // E rows (one store instruction per value), lane 0 the fp32 row kept for verification
         const int b = b0 + bl;
         const float sold = k > 1 ? xs[(size_t)bl * r + i] : 0.f;
         const float gate = 1.f / (1.f + expf(-(ag + hg)));
-        s_next[(size_t)b * r + i] = gate * sold + (1.f - gate) * tanhf(ac + hc);
+        const float sn = gate * sold + (1.f - gate) * tanhf(ac + hc);
         const float ev = tanhf(ao + ho);
-        p.E_all[((size_t)b * p.gamma + (k - 1)) * r + i] = ev;
-        const uint32_t hi = bf16_rne(ev);
-        p.E_hl[(size_t)b * 2 * r + i] = (uint16_t)hi;
-        p.E_hl[(size_t)b * 2 * r + r + i] = (uint16_t)bf16_rne(ev - bf16_val(hi));
+        if (hl == 0) p.E_all[((size_t)b * p.gamma + (k - 1)) * r + i] = ev;
+        if (hl < kRnnCopies) {
+          const uint32_t hi = bf16_rne(ev);
+          const size_t ecopy = (size_t)p.B * 2 * r;    // bf16 per E copy
+          s_next[hl * scopy + (size_t)b * r + i] = sn;
+          p.E_hl[hl * ecopy + (size_t)b * 2 * r + i] = (uint16_t)hi;
+          p.E_hl[hl * ecopy + (size_t)b * 2 * r + r + i] = (uint16_t)bf16_rne(ev - bf16_val(hi));
+        }
       }
     }
     named_bar_sync(kNamedBarSamplers, kSamplerThreads);   // the rows are read before the next round
@@ -720,7 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
         const int kchunks = p.r >> 3;
         const bool ok = b < p.B;
         const uint4* src = reinterpret_cast<const uint4*>(
-            p.E_hl + ((size_t)(ok ? b : 0) * 2 + (n >= NB ? 1 : 0)) * p.r);
+            p.E_hl + (size_t)(cta % kRnnCopies) * p.B * 2 * p.r +
+            ((size_t)(ok ? b : 0) * 2 + (n >= NB ? 1 : 0)) * p.r);
         uint4 val[kPerR];
 #pragma unroll
         for (int u = 0; u < kPerR; ++u) {

@@ -55,6 +55,9 @@ inline RowSplit fixed_split(int V, int seg) {
 
 size_t draft_region_bytes(int B, int gamma);
 
+// copies of the RNN head's state and E rows kept in the workspace (see draft_fused.cu)
+constexpr int kRnnStateCopies = 2;
+
 struct Plan {
   int B, gamma, V, r, H;
   RowSplit stats, ver;
@@ -82,7 +85,9 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_prev = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_fallback = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   // RNN head: state [2][B][r] fp32, then the current position's rows [B][2][r] bf16
-  p.off_rnn_state = o; o = align_up(o + (size_t)2 * B * r * sizeof(float) + (size_t)2 * B * r * 2, 256);
+  // RNN head: kRnnStateCopies copies of the state [2][B][r] fp32 and of the E rows [B][2][r] bf16
+  p.off_rnn_state = o;
+  o = align_up(o + (size_t)kRnnStateCopies * ((size_t)2 * B * r * sizeof(float) + (size_t)2 * B * r * 2), 256);
   p.total = o;
   return p;
 }
@@ -171,8 +176,8 @@ cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, co
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream);
 // the draft with the RNN head (see draft_fused.cu and rnn.cu): Wrec [3r][2r] (rnn_pack),
-// hp [B][gamma][3r] (rnn_project), E_all [B][gamma][r] written, state [2][B][r] and
-// E_hl [B][2][r] bf16 scratch
+// hp [B][gamma][3r] (rnn_project), E_all [B][gamma][r] written, state
+// [kRnnStateCopies][2][B][r] and E_hl [kRnnStateCopies][B][2][r] bf16 scratch
 struct RnnDraftArgs {
   const uint16_t* Wrec;
   const float* hp;
