@@ -41,7 +41,7 @@ METRIC = "draft+verify positions/sec (B×γ) at V=151936, r=256; achieved HBM GB
 # it was taken on: the sha1 of those files is checked at run time and the figure dropped
 # (traffic null) once they change.
 DRAFT_TRAFFIC = {"workload": "qwen3_4b_like", "bytes": 233_439_488,
-                 "sources_sha1": "32aad1f17d988ee94f1d2537f1a06036ec8c9526"}
+                 "sources_sha1": "cc3f613891caf90194e51300c102c39659c24a88"}
 DRAFT_SOURCES = ("draft_fused.cu", "sm100_ptx.cuh", "common.cuh", "internal.h")
 # kernels of one step: draft 1, confidence with the scheduler in its last CTA 1, verify 5
 # (target statistics, decision, bias contraction, final sample, finalize)

@@ -204,18 +204,20 @@ __device__ __forceinline__ float bf16_val(uint32_t b) { return __uint_as_float(b
 // One step k of the RNN head for state entries [d0, d0 + dpc) of every request, by the 16
 // sampler warps of a recurrence CTA, after the grid barrier of position k-1 (x_{k-1} known)
 // and before E_k exists.  The operands go to a scratch region of shared memory (the size
-// of three z tiles) with cp.async, which holds no registers: the previous state rows s_{k-1}[b] (none at k = 1, where the
-// state is zero) and, once the argmax keys give x_{k-1}, the embedding rows W1[x_{k-1}] --
-// all of a round's copies in flight together, about two L2 round trips in all.  Requests
-// go in rounds of as many as fit.  An item is one (entry e, request b of the round); half-
-// warp h (warp h / 2, lanes 16 (h % 2) ..) takes items h, h + 32, ...  Lane l of a half-warp
-// forms the sums over the 8-entry chunks l, l + 16, ... of both halves of the 2r-long
-// operand [s_{k-1}[b] ; W1[x_{k-1}]] against the three rows of Wrec (shared memory when a
-// recurrence CTA's 3 dpc rows were staged there, row (g, e) at (g dpc + e) 2r, else global
-// memory), and four shuffles reduce them.  Lane 0 then writes s_k[b][i] = gate s_{k-1}[b][i]
-// + (1 - gate) tanh(cand), E_k[b][i] = tanh(output) and E_k's two bf16 terms
-// hi = bf16(E), lo = bf16(E - hi) for the tensor-core operand.  Everything other CTAs wrote
-// in this call (the state, the argmax keys) is read through L2.
+// of three z tiles) with cp.async, which holds no registers: the previous state rows
+// s_{k-1}[b] (none at k = 1, where the state is zero) and, once the argmax keys give
+// x_{k-1}, the embedding rows W1[x_{k-1}] -- all of a round's copies in flight together,
+// about two L2 round trips in all.  Requests go in rounds of as many as fit.  An item is
+// one (entry e, request b of the round); half-warp h (warp h / 2, lanes 16 (h % 2) ..)
+// takes items h, h + 32, ...  Lane l of a half-warp forms the sums over the 8-entry chunks
+// l, l + 16, ... of both halves of the 2r-long operand [s_{k-1}[b] ; W1[x_{k-1}]] against
+// the three rows of Wrec (shared memory when a recurrence CTA's 3 dpc rows were staged
+// there, row (g, e) at (g dpc + e) 2r, else global memory), and four shuffles reduce them,
+// leaving the same sums in every lane.  Then s_k[b][i] = gate s_{k-1}[b][i] +
+// (1 - gate) tanh(cand), E_k[b][i] = tanh(output) and E_k's two bf16 terms hi = bf16(E),
+// lo = bf16(E - hi) for the tensor-core operand are written: lane c of the half-warp
+// writes copy c of the state and of the bf16 terms, lane 0 the fp32 row.  Everything other
+// CTAs wrote in this call (the state, the argmax keys) is read through L2.
 constexpr int kRnnHalves = 2 * kSamplers;
 
 // row (g, e) of this CTA's recurrent weights: shared memory when staged, else global
