@@ -86,3 +86,43 @@ def test_verify_confidence_and_bias_validation():
                                1000, FAKE, FAKE, FAKE, 1 << 20, None) == UNSUPPORTED
     assert L.dspark_markov_bias(FAKE, FAKE, FAKE, 0, 4, 1000, 16, FAKE, FAKE, 1 << 20, None) == INVALID
     assert L.dspark_markov_bias(FAKE, FAKE, FAKE, 1, 4, 1000, 16, FAKE, None, 1 << 20, None) == INVALID
+
+
+def _compile(compiler, std, source, extra=()):
+    import shutil
+    import subprocess
+    import tempfile
+    if shutil.which(compiler) is None:
+        pytest.skip(f"{compiler} not found")
+    with tempfile.TemporaryDirectory() as d:
+        ext = ".c" if compiler == "gcc" else ".cpp"
+        src = os.path.join(d, "use" + ext)
+        with open(src, "w") as f:
+            f.write(source)
+        cmd = [compiler, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-c", src,
+               "-o", os.path.join(d, "use.o"), "-I", os.path.join(ROOT, "include"), *extra]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        assert res.returncode == 0, res.stderr
+
+
+def _use_every_entry_point(prefix=""):
+    names = _declared_symbols()
+    body = "\n".join(f"  (void *)&{n}," for n in names)
+    return (prefix + '#include "dspark.h"\n'
+            "void *dspark_entry_points[] = {\n" + body + "\n};\n")
+
+
+def test_header_is_plain_c():
+    """include/dspark.h compiles as C11 on its own (no CUDA headers needed) and declares
+    every entry point the library exports."""
+    _compile("gcc", "c11", _use_every_entry_point())
+
+
+def test_header_is_valid_cpp_with_and_without_the_cuda_runtime():
+    """From C++ (extern "C" guard), alone and after cuda_runtime.h, whose cudaStream_t the
+    header's own typedef must match."""
+    _compile("g++", "c++17", _use_every_entry_point())
+    cuda_inc = "/usr/local/cuda/include"
+    if os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        _compile("g++", "c++17", _use_every_entry_point("#include <cuda_runtime.h>\n"),
+                 ("-I", cuda_inc, "-Wno-unused-parameter"))
