@@ -126,3 +126,12 @@ def test_header_is_valid_cpp_with_and_without_the_cuda_runtime():
     if os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
         _compile("g++", "c++17", _use_every_entry_point("#include <cuda_runtime.h>\n"),
                  ("-I", cuda_inc, "-Wno-unused-parameter"))
+
+
+def test_readme_c_example_compiles():
+    """The C example of one step in README.md compiles as C11 against the header."""
+    text = open(os.path.join(ROOT, "README.md")).read()
+    blocks = re.findall(r"```c\n(.*?)```", text, flags=re.S)
+    assert blocks, "no C example in README.md"
+    for block in blocks:
+        _compile("gcc", "c11", block)
