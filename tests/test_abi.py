@@ -129,9 +129,10 @@ def test_header_is_valid_cpp_with_and_without_the_cuda_runtime():
 
 
 def test_readme_c_example_compiles():
-    """The C example of one step in README.md compiles as C11 against the header."""
+    """The C example of one step in the user documentation compiles as C11 against the
+    header."""
     text = open(os.path.join(ROOT, "README.md")).read()
     blocks = re.findall(r"```c\n(.*?)```", text, flags=re.S)
-    assert blocks, "no C example in README.md"
+    assert blocks, "no C example in the user documentation"
     for block in blocks:
         _compile("gcc", "c11", block)
