@@ -174,14 +174,31 @@ def cpu_baseline(w, n_req: int):
 # --------------------------------------------------------------------- reference arm
 
 def run_reference(args, w):
+    """The oracle as it stands, timed on this host's cores, rank 0 only.  Each step is a
+    bounded sample of the workload (its first requests as their own batch): the first
+    warm-up step runs the full sample and measures it, and the sample of the other steps
+    is then sized so that the whole run (warm-up and timed steps) fits --ref-budget-s, down
+    to one request per OpenMP thread (below that a step would not get shorter)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import oracle
     n = _cores()
     oracle.lib()
-    n_req = min(w.B, args.ref_requests)
-    for i in range(args.warmup):
+    n_full = min(w.B, args.ref_requests)
+    t0 = time.perf_counter()
+    oracle_sample_step(w, w.seed, n_full, n)
+    t_full = time.perf_counter() - t0
+    # the oracle runs the requests in rounds of its OpenMP threads: size the sample in whole
+    # rounds (at least one, so every thread still has a request)
+    n_req = n_full
+    remaining = (args.warmup - 1) + args.steps
+    rounds_full = -(-n_full // max(1, n))
+    if remaining > 0 and t_full * (1 + remaining) > args.ref_budget_s:
+        per_step = max(0.0, args.ref_budget_s - t_full) / remaining
+        rounds = max(1, int(per_step / (t_full / rounds_full)))
+        n_req = min(n_full, rounds * max(1, n))
+    for i in range(1, args.warmup):
         oracle_sample_step(w, w.seed + i, n_req, n)
     t0 = time.perf_counter()
     pos = 0
@@ -195,7 +212,9 @@ def run_reference(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": dict(w.describe(), sample_requests=n_req),
             "cpu_baseline": {"value": value, "unit": "positions/s", "cores": n, "kind": "oracle",
-                             "sample": f"first {n_req} requests of {w.name} as their own batch per step"},
+                             "sample": f"first {n_req} requests of {w.name} as their own batch per "
+                                       f"step (sized to a {args.ref_budget_s:.0f} s run; the full "
+                                       f"{n_full}-request step took {t_full:.1f} s)"},
             "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -462,6 +481,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen3_4b_like", choices=[w.name for w in workloads.WORKLOADS])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-requests", type=int, default=32)
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="wall-time budget of the reference arm (its per-step sample is sized to it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every call from Python instead of replaying captured steps")
