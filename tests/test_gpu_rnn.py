@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 import workloads
+from _parity import assert_rate, band_cases_draft, band_cases_verify, draft_rows, verify_rows
 from workloads import bf16_bits_to_f32
 
 pytestmark = pytest.mark.gpu
@@ -49,16 +50,10 @@ def _setup(w, with_T=True, requests=None):
 
 
 def _compare(got, ref, label, greedy=False):
-    """Tokens equal until the first tie-band position of a row; statistics and E rows
-    within tolerance on the agreeing prefix; returns the number of tie-band divergences."""
-    ties = 0
-    for i in range(got["tokens"].shape[0]):
-        for k in range(got["tokens"].shape[1]):
-            if got["tokens"][i, k] != ref["tokens"][i, k]:
-                assert ref["gap"][i, k] <= TIE, (label, i, k, got["tokens"][i, k], ref["tokens"][i, k])
-                ties += 1
-                break
-    same = np.cumprod(got["tokens"] == ref["tokens"], axis=1).astype(bool)
+    """Tokens equal until the first differing position of a row, which must be in the tie
+    band; statistics and E rows within tolerance on the agreeing prefix; the tie-band
+    cases below the rate bound.  Returns the number of diverged rows."""
+    diverged, same = draft_rows(got["tokens"], ref["tokens"], ref["gap"], label)
     for key in ("q_tok", "row_max", "row_sumexp"):
         np.testing.assert_allclose(got[key][same], ref[key][same], rtol=RTOL, err_msg=f"{label} {key}")
     # E at position k depends on tokens before k only: compare where the prefix before k agrees
@@ -66,7 +61,8 @@ def _compare(got, ref, label, greedy=False):
     np.testing.assert_allclose(got["E"][before], ref["E"][before], atol=RTOL, err_msg=f"{label} E")
     if greedy:
         np.testing.assert_array_equal(got["q_tok"], 1.0)
-    return ties
+    assert_rate(band_cases_draft(ref["gap"]), got["tokens"].size, label)
+    return diverged
 
 
 def test_rnn_pack_is_the_transpose_of_the_recurrent_rows():
@@ -125,8 +121,7 @@ def test_draft_rnn(name, greedy):
     out = ds.draft_rnn(dev["U"], dev["W1"], dev["W2"], Wrec, hp, dev["anchor"], w.seed, ws, greedy=greedy)
     got = {k: v.cpu().numpy() for k, v in out.items()}
     ref = oracle.draft_rnn(inp.U, inp.h, inp.W1, inp.W2, W_rnn, b_rnn, inp.anchor, w.seed, greedy=greedy)
-    ties = _compare(got, ref, name, greedy)
-    assert ties <= max(1, 1e-4 * got["tokens"].size)
+    _compare(got, ref, name, greedy)
     # the packed weights give identical outputs
     W2p = ds.pack_w2(dev["W2"])
     out_p = ds.draft_rnn(dev["U"], dev["W1"], W2p, Wrec, hp, dev["anchor"], w.seed, ws, greedy=greedy,
@@ -151,16 +146,8 @@ def test_verify_rnn(name):
                         _cuda(ell, np.int32), w.seed, ws)
     got = {k: v.cpu().numpy() for k, v in out.items()}
     ref = oracle.verify_rnn(inp.T, inp.U, d["E"], inp.W2, d["tokens"], ell, w.seed)
-    ties = 0
-    for i in range(w.B):
-        if got["accept_len"][i] == ref["accept_len"][i] and \
-                np.array_equal(got["out_tokens"][i], ref["out_tokens"][i]):
-            continue
-        band = ref["band"][i]
-        in_band = np.any(~np.isnan(band)) and np.nanmin(band) <= TIE
-        assert in_band or ref["gap"][i] <= TIE, (name, i, got["out_tokens"][i], ref["out_tokens"][i])
-        ties += 1
-    assert ties <= max(1, 1e-4 * w.B * w.gamma)
+    verify_rows(got, ref, name)
+    assert_rate(band_cases_verify(ref), w.B * w.gamma, name)
     assert (got["accept_len"] < ell).sum() > 0 or w.B < 8
     assert ws.status() == 0
 
@@ -180,7 +167,7 @@ def test_full_size_draft_rnn_sampled_requests():
     picks = sorted({0, w.B - 1, w.B // 2, 7 % w.B})
     sub = workloads.generate(w, requests=picks, with_T=False)
     ref = oracle.draft_rnn(sub.U, sub.h, sub.W1, sub.W2, W_rnn, b_rnn, sub.anchor, w.seed, req_ids=picks)
-    assert _compare({k: v[picks] for k, v in got.items()}, ref, "qwen3_4b_like") <= 1
+    _compare({k: v[picks] for k, v in got.items()}, ref, "qwen3_4b_like")
 
 
 @pytest.mark.parametrize("sampling", ["gumbel", "greedy"])
@@ -197,12 +184,12 @@ def test_rnn_step_end_to_end(name, sampling):
         return
     _, a = oracle.confidence(inp.h, inp.anchor, d["tokens"], inp.W1, inp.w_c, float(inp.b_c))
     np.testing.assert_allclose(got["a"], a, rtol=RTOL)
-    ell_r, Bt_r, _ = oracle.schedule(got["a"], inp.sps)
+    # the oracle's chain schedules its own fp32 survivals: the same l unless a stop decision
+    # sits within the two chains' rounding, which seeded data does not produce
+    ell_r, Bt_r, _ = oracle.schedule(a.astype(np.float32), inp.sps)
     np.testing.assert_array_equal(got["ell"], ell_r)
-    v = (oracle.verify_greedy(inp.T, d["tokens"], got["ell"], w.seed) if greedy else
-         oracle.verify_rnn(inp.T, inp.U, d["E"], inp.W2, d["tokens"], got["ell"], w.seed))
-    mism = np.nonzero(np.any(got["out_tokens"] != v["out_tokens"], axis=1))[0]
-    for i in mism:
-        band = v["band"][i]
-        assert (np.any(~np.isnan(band)) and np.nanmin(band) <= TIE) or v["gap"][i] <= TIE
+    assert got["B_total"] == Bt_r
+    v = (oracle.verify_greedy(inp.T, d["tokens"], ell_r, w.seed) if greedy else
+         oracle.verify_rnn(inp.T, inp.U, d["E"], inp.W2, d["tokens"], ell_r, w.seed))
+    verify_rows(got, v, name)
     assert step.ws.status() == 0

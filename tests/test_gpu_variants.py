@@ -13,6 +13,8 @@ import pytest
 
 import oracle
 import workloads
+from _parity import (assert_rate, band_cases_draft, band_cases_verify, draft_rows, draft_stats,
+                     verify_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,20 +48,14 @@ def _ws(w):
 
 
 def _compare_greedy(got, ref, label):
-    """Tokens equal until the first tie-band position of a row; row statistics within
-    RTOL on the agreeing prefix; returns the number of tie-band divergences."""
-    ties = 0
-    for i in range(got["tokens"].shape[0]):
-        for k in range(got["tokens"].shape[1]):
-            if got["tokens"][i, k] != ref["tokens"][i, k]:
-                assert ref["gap"][i, k] <= TIE, (label, i, k, got["tokens"][i, k], ref["tokens"][i, k])
-                ties += 1
-                break
-    same = np.cumprod(got["tokens"] == ref["tokens"], axis=1).astype(bool)
-    for key in ("row_max", "row_sumexp"):
-        np.testing.assert_allclose(got[key][same], ref[key][same], rtol=RTOL, err_msg=f"{label} {key}")
+    """Tokens equal until the first differing position of a row, which must be in the tie
+    band; row statistics within RTOL on the agreeing prefix; the tie-band cases of the
+    batch below the rate bound.  Returns the number of diverged rows."""
+    diverged, same = draft_rows(got["tokens"], ref["tokens"], ref["gap"], label)
+    draft_stats(got, ref, same, keys=("row_max", "row_sumexp"), label=label)
     np.testing.assert_array_equal(got["q_tok"], 1.0)
-    return ties
+    assert_rate(band_cases_draft(ref["gap"]), got["tokens"].size, label)
+    return diverged
 
 
 # ------------------------------------------------------------------------ greedy draft
@@ -74,8 +70,7 @@ def test_draft_greedy(name):
     got = {k: v.cpu().numpy() for k, v in ds.draft_greedy(dev["U"], dev["W1"], dev["W2"],
                                                            dev["anchor"], ws).items()}
     ref = oracle.draft_greedy(inp.U, inp.W1, inp.W2, inp.anchor)
-    ties = _compare_greedy(got, ref, name)
-    assert ties <= max(1, 1e-4 * got["tokens"].size)
+    _compare_greedy(got, ref, name)
     # the packed weights give identical outputs
     W2p = ds.pack_w2(dev["W2"])
     got_p = {k: v.cpu().numpy() for k, v in ds.draft_greedy(dev["U"], dev["W1"], W2p,
@@ -120,7 +115,7 @@ def test_full_size_draft_greedy_sampled_requests(name):
     picks = sorted({0, w.B - 1, w.B // 2, 7 % w.B})
     sub = workloads.generate(w, requests=picks, with_T=False)
     ref = oracle.draft_greedy(sub.U, sub.W1, sub.W2, sub.anchor)
-    assert _compare_greedy({k: v[picks] for k, v in got.items()}, ref, name) <= 1
+    _compare_greedy({k: v[picks] for k, v in got.items()}, ref, name)
 
 
 # ---------------------------------------------------------------------- greedy verify
@@ -138,16 +133,8 @@ def test_verify_greedy(name):
     out = ds.verify_greedy(dev["T"], _cuda(d["tokens"], np.int32), _cuda(ell, np.int32), w.seed, ws)
     got = {k: v.cpu().numpy() for k, v in out.items()}
     ref = oracle.verify_greedy(inp.T, d["tokens"], ell, w.seed)
-    ties = 0
-    for i in range(w.B):
-        if got["accept_len"][i] == ref["accept_len"][i] and \
-                np.array_equal(got["out_tokens"][i], ref["out_tokens"][i]):
-            continue
-        band = ref["band"][i]
-        in_band = np.any(~np.isnan(band)) and np.nanmin(band) <= TIE
-        assert in_band or ref["gap"][i] <= TIE, (name, i, got["out_tokens"][i], ref["out_tokens"][i])
-        ties += 1
-    assert ties <= max(1, 1e-4 * w.B * w.gamma)
+    verify_rows(got, ref, name)
+    assert_rate(band_cases_verify(ref), w.B * w.gamma, name)
     np.testing.assert_array_equal(got["n_out"], got["accept_len"] + 1)
     # a correction is never the rejected draft token
     for i in range(w.B):
@@ -282,21 +269,19 @@ def test_greedy_step_end_to_end(name, scheduler):
     step.run(seed=w.seed, t=0)
     got = step.results()
     d = oracle.draft_greedy(inp.U, inp.W1, inp.W2, inp.anchor)
-    ties = _compare_greedy({k: got[k] for k in ("tokens", "q_tok", "row_max", "row_sumexp")}, d, name)
-    if ties:
+    if _compare_greedy({k: got[k] for k in ("tokens", "q_tok", "row_max", "row_sumexp")}, d, name):
         return
     _, a = oracle.confidence(inp.h, inp.anchor, d["tokens"], inp.W1, inp.w_c, float(inp.b_c))
     np.testing.assert_allclose(got["a"], a, rtol=RTOL)
-    # the schedulers see the GPU's fp32 survivals: exact against the oracle on those
+    # the oracle's chain schedules its own survivals (fp32): the same l unless a decision
+    # sits within the two chains' rounding, which seeded data does not produce
+    a32 = a.astype(np.float32)
     if scheduler == "threshold":
-        ell_r, Bt_r = oracle.schedule_threshold(got["a"], 0.4)
+        ell_r, Bt_r = oracle.schedule_threshold(a32, 0.4)
     else:
-        ell_r, Bt_r, _, _ = oracle.schedule_async(got["a"], inp.sps, -1)
+        ell_r, Bt_r, _, _ = oracle.schedule_async(a32, inp.sps, -1)
     np.testing.assert_array_equal(got["ell"], ell_r)
     assert got["B_total"] == Bt_r
-    v = oracle.verify_greedy(inp.T, d["tokens"], got["ell"], w.seed)
-    mism = np.nonzero(np.any(got["out_tokens"] != v["out_tokens"], axis=1))[0]
-    for i in mism:
-        band = v["band"][i]
-        assert (np.any(~np.isnan(band)) and np.nanmin(band) <= TIE) or v["gap"][i] <= TIE
+    v = oracle.verify_greedy(inp.T, d["tokens"], ell_r, w.seed)
+    verify_rows(got, v, name)
     assert step.ws.status() == 0
