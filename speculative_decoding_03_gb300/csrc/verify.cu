@@ -129,37 +129,42 @@ __global__ void __launch_bounds__(kSampleThreads) target_stats_kernel(
   __shared__ float red_m[kSampleThreads / 32], red_s[kSampleThreads / 32];
   pdl_wait();
   pdl_launch_dependents();
-  const int k = blockIdx.y / B + 1, b = blockIdx.y - (k - 1) * B;
-  if (k > clamp_ell(ell, b, gamma, nullptr)) return;
-  const int row = b * gamma + (k - 1);
-  const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
-  const int v0 = blockIdx.x * kStatsSeg + 4 * threadIdx.x;
-  float4 t[kStatsVec];
+  // rows (k, b) in position order; the grid's y extent is capped at 65535, so a CTA takes
+  // every gridDim.y-th row
+  for (int y = blockIdx.y; y < B * gamma; y += gridDim.y) {
+    const int k = y / B + 1, b = y - (k - 1) * B;
+    if (k > clamp_ell(ell, b, gamma, nullptr)) continue;
+    const int row = b * gamma + (k - 1);
+    const float* Trow = T + ((size_t)b * (gamma + 1) + (k - 1)) * V;
+    const int v0 = blockIdx.x * kStatsSeg + 4 * threadIdx.x;
+    float4 t[kStatsVec];
 #pragma unroll
-  for (int j = 0; j < kStatsVec; ++j) {
-    const int v = v0 + j * 4 * kSampleThreads;
-    t[j] = v < V ? ld_stream_f4(Trow + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  }
-  float m = -INFINITY;
+    for (int j = 0; j < kStatsVec; ++j) {
+      const int v = v0 + j * 4 * kSampleThreads;
+      t[j] = v < V ? ld_stream_f4(Trow + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    float m = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < kStatsVec; ++j) m = fmaxf(m, fmaxf(fmaxf(t[j].x, t[j].y), fmaxf(t[j].z, t[j].w)));
-  float s = 0.f;
-  if (m != -INFINITY) {
-    const float mL = m * kLog2e;
+    for (int j = 0; j < kStatsVec; ++j) m = fmaxf(m, fmaxf(fmaxf(t[j].x, t[j].y), fmaxf(t[j].z, t[j].w)));
+    float s = 0.f;
+    if (m != -INFINITY) {
+      const float mL = m * kLog2e;
 #pragma unroll
-    for (int j = 0; j < kStatsVec; ++j)
-      s += ex2_approx(fmaf(t[j].x, kLog2e, -mL)) + ex2_approx(fmaf(t[j].y, kLog2e, -mL)) +
-           ex2_approx(fmaf(t[j].z, kLog2e, -mL)) + ex2_approx(fmaf(t[j].w, kLog2e, -mL));
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+      for (int j = 0; j < kStatsVec; ++j)
+        s += ex2_approx(fmaf(t[j].x, kLog2e, -mL)) + ex2_approx(fmaf(t[j].y, kLog2e, -mL)) +
+             ex2_approx(fmaf(t[j].z, kLog2e, -mL)) + ex2_approx(fmaf(t[j].w, kLog2e, -mL));
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1)
-    max_sum_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
-  if (lane == 0) { red_m[warp] = m; red_s[warp] = s; }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kSampleThreads / 32; ++w) max_sum_merge(m, s, red_m[w], red_s[w]);
-    partials[(size_t)row * splits + blockIdx.x] = make_float2(m, s);
+    for (int o = 16; o >= 1; o >>= 1)
+      max_sum_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+    if (lane == 0) { red_m[warp] = m; red_s[warp] = s; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kSampleThreads / 32; ++w) max_sum_merge(m, s, red_m[w], red_s[w]);
+      partials[(size_t)row * splits + blockIdx.x] = make_float2(m, s);
+    }
+    __syncthreads();   // red_m / red_s are rewritten by the next row
   }
 }
 
@@ -558,7 +563,7 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   int32_t* prev = ws_at<int32_t>(ws, p.off_prev);
   int32_t* fb = ws_at<int32_t>(ws, p.off_fallback);
 
-  cudaError_t e = launch_pdl(target_stats_kernel, dim3(p.stats.splits, B * gamma),
+  cudaError_t e = launch_pdl(target_stats_kernel, dim3(p.stats.splits, B * gamma < 65535 ? B * gamma : 65535),
                              dim3(kSampleThreads), 0, stream, T, ell, B, gamma, V,
                              p.stats.splits, part_stats);
   if (e != cudaSuccess) return e;
