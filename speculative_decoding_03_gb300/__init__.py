@@ -54,6 +54,7 @@ SIGNATURES = [
     ("dspark_verify_rnn", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P,
                                _P, _P, _SZ, _P]),
     ("dspark_last_device_status", _I, [_P, _P]),
+    ("dspark_testing_set_wait_limit", None, [ctypes.c_longlong, _I]),
 ]
 
 _lib = None
@@ -132,6 +133,14 @@ def as_bf16_tensor(bits: np.ndarray, device="cuda"):
     """uint16 bf16 bit patterns (numpy) -> torch.bfloat16 tensor on ``device``."""
     torch = _torch()
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def testing_set_wait_limit(wait_cycles: int = 0, unreachable_barrier: bool = False):
+    """Bound of the draft kernel's waits (SM cycles, 0: the default of about 2 s) and, when
+    ``unreachable_barrier``, a grid barrier that cannot complete, for the draft launches
+    that follow (tests of the timeout path; ``testing_set_wait_limit()`` restores the
+    production setting)."""
+    lib().dspark_testing_set_wait_limit(int(wait_cycles), int(bool(unreachable_barrier)))
 
 
 # ------------------------------------------------------------------------------ calls

@@ -356,4 +356,8 @@ dspark_status dspark_last_device_status(void* workspace, cudaStream_t stream) {
   return DSPARK_OK;
 }
 
+void dspark_testing_set_wait_limit(long long wait_cycles, int unreachable_barrier) {
+  set_draft_wait_limit(wait_cycles > 0 ? wait_cycles : 0, unreachable_barrier ? (1u << 30) : 0u);
+}
+
 }  // extern "C"

@@ -1,0 +1,844 @@
+// The draft of one step (all gamma positions) in one persistent, warp-specialised kernel,
+// with the Markov bias contraction laid out request-major in tensor memory.
+//
+// billytse.dev DSpark page, sections 3.2 and 3.3: for k = 1..gamma, in order,
+//   bias = W1[x_{k-1}] W2;  z = U_k + bias;  x_k ~ softmax(z)   (x_0 = the anchor)
+// for every request at once.  x_k is drawn by Gumbel-max: argmax_v z_v - log E_v with
+// E_v = -log u_v (stream 0), i.e. argmax_v exp(z_v - M) / E_v for any reference M.  The
+// greedy variant (section 11: the serving example drafts greedily) takes x_k = argmax_v z_v
+// (ties to the smallest v) and q_k(x_k) = 1, the proposal being the point mass at x_k.
+//
+// Layout of the work.  The vocabulary is cut into 128-column tiles; each CTA (one per SM,
+// cooperative launch) owns a contiguous run of tiles for the whole call.  A job is one
+// position k and one chunk of NBJ requests (NBJ = 32, 64 or 128).  Per job and tile the
+// tensor core computes D[m][n] = sum_i A[m][i] B[i][n] with M = 128, N = 128, K = r:
+//   A  the E rows W1[x_{k-1}] of the chunk, in tensor memory: row m on lane m, two bf16
+//      per 32-bit column.  A chunk of NBJ < 128 requests is repeated 128 / NBJ times down
+//      the lanes, so that every warp quadrant (a warp reads only the 32 lanes of its
+//      quadrant) holds the rows it samples;
+//   B  the W2 tile, streamed through a shared-memory ring as the packed images of pack.cu
+//      (MN-major, 128-byte swizzle), or as two TMA boxes per stage from W2 itself.
+// A request's accumulator row is one tensor-memory lane with the vocabulary along the
+// columns, so a sampler thread owns one request and a run of 8, 16 or 32 columns of every
+// tile: one tcgen05.ld brings the bias, the U tile comes from a TMA ring (128-byte
+// swizzle, so that the threads of a warp, 32 requests, read it without bank conflicts),
+// and the request's softmax sums and Gumbel race stay in the thread's registers.
+//
+// Roles (19 warps): warps 0..15 sample (warp w reads the lanes of quadrant w % 4), warp 16
+// lane 0 streams W2 stages, warp 17 lane 0 streams U tiles (TMA), warp 18 allocates tensor
+// memory and its lane 0 issues the MMAs.  The producers do not depend on the drafted
+// tokens and run ahead across positions.
+//
+// Sampler, per thread and octet of 8 columns: z = bias + U; running max; the softmax sum
+// against a lazy per-thread reference M (raised only when a logit exceeds it by more than
+// 32, so exp(z - M) cannot overflow); two Philox blocks give the 8 draws; with
+// w = 1 - u (exact), w <= E = -log1p(-w) <= w / (1 - w), so exp(z - M) / w bounds an
+// element's ratio exp(z - M) / E from above and exp(z - M)(1 - w) / w from below: an
+// element is a candidate only if its upper bound beats exp(best - M), where best is the
+// best exact score any thread of the CTA has found for the request (a 64-bit shared-memory
+// atomic max, tagged with the job so that no reset is needed); among a thread's candidates
+// the best lower bound tightens the threshold further, and only the survivors evaluate the
+// exact score z - log E with log1p and log.
+//
+// After its last tile of a job, every sampler thread leaves its partial (max, sum, best
+// score, index, logit) in shared memory; the first NBJ sampler threads merge the partials
+// of one request each, publish the CTA's partial and fold the CTA's best (score, index)
+// into a 64-bit atomic max key.  One grid barrier per position (a release reduction per
+// CTA, one bounded poller) makes x_k known everywhere; the samplers then gather the next
+// position's E rows into the other A buffer with tcgen05.st.  The CTA with index b mod G
+// merges the G partials of request b into x_k, q_k(x_k), max and sum after its arrival at
+// the next barrier.
+//
+// Failure handling: every wait is bounded (LParams::wait_cycles SM cycles).  A wait that
+// runs out records DSPARK_ERR_TIMEOUT and sets a CTA-wide abort flag; from then on the
+// sampler threads run their fixed loop counts without waiting or working (so that their
+// named barriers line up), the producers and the MMA issuer stop issuing and drain what
+// they issued, and the CTA releases tensor memory and exits.
+#include <string.h>
+
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dspark {
+namespace {
+
+using namespace sm100;
+
+constexpr int kSamplers = 16;         // warps 0..15; sampler w sits in quadrant w % 4
+constexpr int kWProducerWarp = 16;
+constexpr int kUProducerWarp = 17;
+constexpr int kMmaWarp = 18;
+constexpr int kWarps = 19;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSamplerThreads = kSamplers * 32;
+constexpr int kBarSamplers = 1;       // named barrier of the sampler threads
+constexpr uint32_t kTmemCols = 512;   // A buffers at columns 0 and 128, accumulators at 256, 384
+constexpr uint32_t kAccCol = 256;
+constexpr int kTileN = 128;           // vocabulary columns per tile (MMA N)
+constexpr int kWStageBytes = 16384;   // one K-chunk of up to 64 rank rows of a W2 tile
+constexpr int kMergeStride = 5 * 32 + 1;    // words per sampler warp in the merge area (the pad
+                                            // spreads a merging warp's reads over the banks)
+constexpr float kLazy = 32.f;               // reference raise margin (exp(32) fits fp32 sums)
+constexpr float kShrink = 1.f - 0x1.0p-16f;  // filter slack, well above fp32 rounding
+
+// Shared-memory plan of one NBJ (requests per job).
+template <int NBJ>
+struct LSmem {
+  static constexpr int kCopies = 128 / NBJ;          // replicas of the chunk down the lanes
+  static constexpr int kCols = NBJ / 4;              // columns of a tile per sampler thread
+  static constexpr int kOct = kCols / 8;             // octets per tile per sampler thread
+  static constexpr int kWStages = NBJ == 32 ? 8 : NBJ == 64 ? 6 : 4;
+  static constexpr int kUStages = NBJ == 32 ? 4 : NBJ == 64 ? 3 : 2;
+  static constexpr int kUStageBytes = NBJ * kTileN * 4;
+  static constexpr int kOffW = 0;
+  static constexpr int kOffU = kOffW + kWStages * kWStageBytes;
+  static constexpr int kOffMerge = kOffU + kUStages * kUStageBytes;   // [16 warps][5][32] + pad
+  static constexpr int kMergeBytes = kSamplers * kMergeStride * 4;
+  static constexpr int kOffThr = kOffMerge + kMergeBytes;             // [NBJ] u64
+  static constexpr int kBytes = kOffThr + NBJ * 8;
+};
+
+struct LParams {
+  const uint16_t* W1;
+  const uint16_t* W2p;             // packed W2 tile images (null: TMA boxes from W2)
+  const int32_t* anchor;
+  int B, gamma, V, r;
+  int n_tiles, n_chunks, kc;       // kc = rank rows per W2 stage (<= 64)
+  uint64_t seed;
+  RowState* partials;              // [3][B][G], position k in slot k % 3
+  unsigned long long* keys;        // [gamma][B], zeroed before launch
+  unsigned int* grid_count;        // zeroed before launch
+  int32_t* tokens;
+  float* q_tok;
+  float* row_max;
+  float* row_sumexp;
+  int* err;
+  long long wait_cycles;           // bound of every wait
+  unsigned int grid_extra;         // added to every grid-barrier target (0; tests: unreachable)
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_volatile_shared_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void atomic_max_shared_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("atom.shared.max.u64 _, [%0], %1;" ::"r"(smem_u32(p)), "l"(v) : "memory");
+}
+
+// Order-preserving map of a (non-NaN) float to a 32-bit unsigned key and back.
+__device__ __forceinline__ uint32_t float_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// 1 - U01(x) = ((~x >> 9) + 1/2) 2^-23 built exactly: the float with bits
+// 0x4B000000 | n is 2^23 + n, and one fused multiply-add removes 2^23 - 1/2.
+__device__ __forceinline__ float w_of_draw(uint32_t x) {
+  const float f = __uint_as_float(0x4B000000u | ((~x) >> 9));
+  return fmaf(f, 0x1.0p-23f, -(1.f - 0x1.0p-24f));
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Philox4x32 with one 32x32->64 multiply per product (the definition of common.cuh: same
+// rounds, constants and key schedule).
+__device__ __forceinline__ uint4 philox_wide(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < kPhiloxRounds; ++round) {
+    const unsigned long long p0 = (unsigned long long)0xD2511F53u * c.x;
+    const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
+                   (uint32_t)p0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+__device__ __forceinline__ int token_of_key(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
+
+// Merge the G partials of request b at position kp into x, q, max and sum (one warp; every
+// lane issues all its loads together, so a merge is about one L2 round trip).
+constexpr int kMergePerLane = (kDraftMaxCtas + 31) / 32;
+template <bool Greedy>
+__device__ __forceinline__ void finalize_row(const LParams& p, int b, int kp, int G, int lane) {
+  const unsigned long long key = __ldcg(p.keys + (size_t)(kp - 1) * p.B + b);
+  const RowState* base = p.partials + ((size_t)(kp % 3) * p.B + b) * G;
+  float pm[kMergePerLane], ps[kMergePerLane], pz[kMergePerLane];
+  int pi[kMergePerLane];
+#pragma unroll
+  for (int u = 0; u < kMergePerLane; ++u) {
+    const int g = lane + 32 * u;
+    pm[u] = -INFINITY; ps[u] = 0.f; pz[u] = -INFINITY; pi[u] = -1;
+    if (g < G) {
+      pm[u] = __ldcg(&base[g].m);
+      ps[u] = __ldcg(&base[g].s);
+      pz[u] = __ldcg(&base[g].z);
+      pi[u] = __ldcg(&base[g].idx);
+    }
+  }
+  const int x = token_of_key(key);
+  float m = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kMergePerLane; ++u) m = fmaxf(m, pm[u]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f, zx = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kMergePerLane; ++u) {
+    if (pm[u] != -INFINITY) s += ps[u] * expf(pm[u] - m);
+    if (pi[u] == x) zx = pz[u];
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    zx = fmaxf(zx, __shfl_xor_sync(0xffffffffu, zx, o));
+  }
+  if (lane == 0) {
+    const size_t o = (size_t)b * p.gamma + (kp - 1);
+    p.tokens[o] = x;
+    p.q_tok[o] = Greedy ? 1.f : expf(zx - m) / s;
+    p.row_max[o] = m;
+    p.row_sumexp[o] = s;
+  }
+}
+
+template <int NBJ, bool Greedy>
+__global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
+    const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
+    const LParams p) {
+  using S = LSmem<NBJ>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t w_full[S::kWStages], w_empty[S::kWStages];
+  __shared__ uint64_t u_full[S::kUStages], u_empty[S::kUStages];
+  __shared__ uint64_t a_full[2], a_empty[2];
+  __shared__ uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint64_t mma_drain;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int t_lo = (int)((long long)cta * p.n_tiles / G);
+  const int t_hi = (int)((long long)(cta + 1) * p.n_tiles / G);
+  const int my_tiles = t_hi - t_lo;
+  const int kc = p.kc;
+  const int n_kchunks = p.r / kc;
+  const int n_jobs = p.gamma * p.n_chunks;
+  unsigned long long* thr = reinterpret_cast<unsigned long long*>(smem + S::kOffThr);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S::kWStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
+    for (int i = 0; i < S::kUStages; ++i) {
+      mbar_init(&u_full[i], 1);
+      mbar_init(&u_empty[i], kSamplers);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&a_full[i], kSamplers);
+      mbar_init(&a_empty[i], 1);
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kSamplers);
+    }
+    mbar_init(&mma_drain, 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < NBJ; i += kThreads) thr[i] = 0ull;   // below every tagged key
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_s, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = tmem_base_s;
+  pdl_launch_dependents();
+
+  // One thread's bounded wait; a timeout aborts the CTA.  The abort flag is read only once
+  // the first (sleeping) try has not seen the phase complete, so the issue loops pay
+  // nothing for it.
+  auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const long long t0 = sm_cycles();
+    for (;;) {
+      if (*(volatile int*)&abort_s) return false;
+      if (mbar_try_wait_sleep(bar, parity)) return true;
+      if (sm_cycles() - t0 > p.wait_cycles) {
+        set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+        atomicExch(&abort_s, 1);
+        return false;
+      }
+    }
+  };
+
+  if (warp == kWProducerWarp) {
+    // ---------------------------------------------------------------- W2 stage producer
+    if (lane == 0) {
+      if (!p.W2p) prefetch_tensormap(&w2_map);
+      const uint64_t keep = policy_evict_last();
+      const uint32_t w_bytes = 2u * (uint32_t)kc * 128u;
+      uint32_t ws = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        for (int t = t_lo; t < t_hi && ok; ++t) {
+          for (int i = 0; i < n_kchunks; ++i, ++ws) {
+            const int s = ws % S::kWStages;
+            if (!(ok = wait1(&w_empty[s], ((ws / S::kWStages) & 1) ^ 1))) break;
+            uint8_t* dst = smem + S::kOffW + s * kWStageBytes;
+            mbar_arrive_expect_tx(&w_full[s], w_bytes);
+            if (p.W2p) {
+              const uint16_t* src = p.W2p + ((size_t)t * n_kchunks + i) * (size_t)kc * 128;
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                  " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+                  "l"(reinterpret_cast<uint64_t>(src)), "r"(w_bytes), "r"(smem_u32(&w_full[s])),
+                  "l"(keep)
+                  : "memory");
+            } else {
+              tma_load_2d(dst, &w2_map, &w_full[s], t * kTileN, i * kc, keep);
+              tma_load_2d(dst + kc * 128, &w2_map, &w_full[s], t * kTileN + 64, i * kc, keep);
+            }
+          }
+        }
+      }
+      // every issued copy lands before the CTA may exit (a stage whose wait failed was
+      // never issued, so only the stages below ws can be in flight)
+      for (uint32_t i = ws > (uint32_t)S::kWStages ? ws - S::kWStages : 0; i < ws; ++i)
+        mbar_wait(&w_full[i % S::kWStages], (i / S::kWStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kUProducerWarp) {
+    // ------------------------------------------------------------------ U tile producer
+    if (lane == 0) {
+      prefetch_tensormap(&u_map);
+      uint64_t stream_pol;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
+      uint32_t us = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+        for (int t = t_lo; t < t_hi; ++t, ++us) {
+          const int su = us % S::kUStages;
+          if (!(ok = wait1(&u_empty[su], ((us / S::kUStages) & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(&u_full[su], (uint32_t)S::kUStageBytes);
+          // four boxes of 32 columns x NBJ requests (128 bytes a row: the swizzle's span)
+#pragma unroll
+          for (int jb = 0; jb < 4; ++jb)
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(
+                    smem_u32(smem + S::kOffU + su * S::kUStageBytes + jb * NBJ * 128)),
+                "l"(reinterpret_cast<uint64_t>(&u_map)), "r"(smem_u32(&u_full[su])),
+                "r"(t * kTileN + 32 * jb), "r"(k - 1), "r"(c * NBJ), "l"(stream_pol)
+                : "memory");
+        }
+      }
+      for (uint32_t i = us > (uint32_t)S::kUStages ? us - S::kUStages : 0; i < us; ++i)
+        mbar_wait(&u_full[i % S::kUStages], (i / S::kUStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // -------------------------------------------------------------------- MMA issuer
+    // The K steps of one W2 stage are a compile-time count (1, 2 or 4); descriptors are
+    // built once and advanced by adding (byte offset >> 4) to their start-address field.
+    auto issue_loop = [&](auto ksteps_c) {
+      constexpr int KS = decltype(ksteps_c)::value;
+      const uint32_t idesc = idesc_bf16_f32(128, kTileN, 0, 1);
+      const uint64_t b_base = smem_desc(smem_u32(smem + S::kOffW), (uint32_t)KS * 2048u, 1024u,
+                                        kSwizzle128B);
+      uint32_t ws = 0, tc = 0;
+      bool ok = true;
+      for (int job = 0; job < n_jobs && ok; ++job) {
+        const int ab = job & 1;
+        if (!(ok = wait1(&a_full[ab], (job >> 1) & 1))) break;
+        tc_fence_after_sync();
+        const uint32_t a_t = tmem_base + (uint32_t)(128 * ab);
+        for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
+          const int acc = tc & 1;
+          if (!(ok = wait1(&acc_empty[acc], ((tc >> 1) & 1) ^ 1))) break;
+          tc_fence_after_sync();
+          const uint32_t d_t = tmem_base + kAccCol + (uint32_t)(kTileN * acc);
+          for (int i = 0; i < n_kchunks; ++i, ++ws) {
+            const int s = ws % S::kWStages;
+            if (!(ok = wait1(&w_full[s], (ws / S::kWStages) & 1))) break;
+            const uint64_t b_s = b_base + (uint64_t)((s * kWStageBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              // 16 K rows of the MN-major stage are 2048 bytes apart; K step g of A is
+              // columns 8g .. 8g + 7
+              const uint32_t g = (uint32_t)(i * KS + kk);
+              umma_ts_bf16_f32(d_t, a_t + 8u * g, b_s + (uint64_t)(kk * (2048 >> 4)), idesc,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&w_empty[s]);
+          }
+          if (!ok) break;
+          umma_commit(&acc_full[acc]);
+        }
+        if (ok) umma_commit(&a_empty[ab]);
+      }
+    };
+    if (lane == 0) {
+      if (kc == 64) issue_loop(std::integral_constant<int, 4>{});
+      else if (kc == 32) issue_loop(std::integral_constant<int, 2>{});
+      else issue_loop(std::integral_constant<int, 1>{});
+      // every issued MMA completes before tensor memory is released
+      umma_commit(&mma_drain);
+      mbar_wait(&mma_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------------------- samplers
+    const int sw = warp;
+    const int stid = threadIdx.x;
+    const int quad = warp & 3;                                  // TMEM lane quadrant
+    const int ml = (32 * quad + lane) % NBJ;                    // request row in the chunk
+    // column run of this warp: the warps whose quadrants hold the same rows split a tile
+    const int sidx = (sw >> 2) * S::kCopies + quad / (NBJ / 32);
+    const int c0 = sidx * S::kCols;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * quad) << 16);
+    const uint32_t k0 = (uint32_t)p.seed, k1 = (uint32_t)(p.seed >> 32);
+    float* merge = reinterpret_cast<float*>(smem + S::kOffMerge);
+    // U tile address of this thread's first column: box c0 / 32, row ml, 16-byte chunk
+    // (c0 % 32) / 4 (two chunks per octet), 128-byte swizzle (chunk ^ row % 8)
+    const int u_row = ml * 128;
+    const int u_sw = ml & 7;
+
+    // a whole warp's bounded wait (abort first: after an abort nothing waits)
+    auto swait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (*(volatile int*)&abort_s) return false;
+      return __all_sync(0xffffffffu, wait1(bar, parity));
+    };
+    auto grid_wait = [&](unsigned int target) {
+      if (stid == 0 && !*(volatile int*)&abort_s) {
+        const long long t0 = sm_cycles();
+        while (ld_acquire_u32(p.grid_count) < target) {
+          if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
+            set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+            atomicExch(&abort_s, 1);
+            break;
+          }
+        }
+      }
+      named_bar_sync(kBarSamplers, kSamplerThreads);
+    };
+    // E rows of job j into A buffer j & 1: this thread's lane holds row 32 quad + lane
+    // (request c NBJ + ml), this warp writes columns [jq r / 8, (jq + 1) r / 8) of it
+    auto gather = [&](int j) {
+      const int k = j / p.n_chunks + 1, c = j % p.n_chunks;
+      const int ab = j & 1;
+      if (j >= 2 && !swait(&a_empty[ab], ((j >> 1) & 1) ^ 1)) return;
+      // warp-uniform: the tensor-memory stores below are whole-warp instructions
+      if (__any_sync(0xffffffffu, *(volatile int*)&abort_s != 0)) return;
+      tc_fence_after_sync();
+      const int b = c * NBJ + ml;
+      int prev = -1;
+      if (b < p.B) {
+        prev = (k == 1) ? p.anchor[b] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+        if (prev < 0 || prev >= p.V) {
+          set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
+          prev = -1;
+        }
+      }
+      const int jq = sw >> 2;
+      const int ncol = p.r >> 3;                      // 32-bit columns per warp
+      const uint32_t taddr = lane_base + (uint32_t)(128 * ab + jq * ncol);
+      const uint16_t* src = p.W1 + (size_t)(prev < 0 ? 0 : prev) * p.r + (size_t)jq * (p.r >> 2);
+      if ((ncol & 7) == 0) {
+        // 8 columns = 16 bf16 = two 16-byte loads per store; the loads of two stores at a
+        // time in flight
+        const int n8 = ncol >> 3;                     // 1..4
+#pragma unroll
+        for (int h = 0; h < 4; h += 2) {
+          uint4 v[4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (h + u < n8) {
+              v[2 * u] = prev < 0 ? make_uint4(0u, 0u, 0u, 0u) : __ldg(reinterpret_cast<const uint4*>(src) + 2 * (h + u));
+              v[2 * u + 1] = prev < 0 ? make_uint4(0u, 0u, 0u, 0u) : __ldg(reinterpret_cast<const uint4*>(src) + 2 * (h + u) + 1);
+            }
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (h + u < n8) {
+              const uint32_t cols[8] = {v[2 * u].x, v[2 * u].y, v[2 * u].z, v[2 * u].w,
+                                        v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
+              tmem_st_32x32b_x8(taddr + 8u * (h + u), cols);
+            }
+        }
+      } else {
+        // 2 columns = 4 bf16 = one 8-byte load per store
+        for (int u = 0; u < (ncol >> 1); ++u) {
+          const uint2 v = prev < 0 ? make_uint2(0u, 0u) : __ldg(reinterpret_cast<const uint2*>(src) + u);
+          tmem_st_32x32b_x2(taddr + 2u * u, v.x, v.y);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[ab]);
+    };
+
+    uint32_t tc = 0;
+    gather(0);
+    for (int job = 0; job < n_jobs; ++job) {
+      const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+      // the next chunk of the same position only needs x_{k-1}: gather it now
+      if (c + 1 < p.n_chunks) gather(job + 1);
+      const int b = c * NBJ + ml;
+      const bool valid = b < p.B;
+      const unsigned long long tag = (unsigned long long)(job + 1) << 32;
+      // per-thread state: lazy reference Mr, filter threshold Tf ~ exp(best_known - Mr),
+      // the best exact score known for the request (this thread's or another's), the
+      // thread's own best (score, index, logit), the softmax sum against Mr, the max
+      float Mr = -INFINITY, Tf = 0.f, known = -INFINITY, ssum = 0.f, mx = -INFINITY;
+      float bsc = -INFINITY, bz = -INFINITY;
+      int bi = -1;
+      for (int t = 0; t < my_tiles; ++t, ++tc) {
+        const int acc = tc & 1;
+        const int su = tc % S::kUStages;
+        // both stages are held until the tile is done (two accumulators and the U ring
+        // keep the tensor core and the copies a tile ahead)
+        const bool have = swait(&acc_full[acc], (tc >> 1) & 1) &&
+                          swait(&u_full[su], (tc / S::kUStages) & 1);
+        if (have) {
+          tc_fence_after_sync();
+          const int vt = (t_lo + t) * kTileN + c0;
+          const bool ragged = (t_lo + t + 1) * kTileN > p.V;
+          const uint8_t* us = smem + S::kOffU + su * S::kUStageBytes;
+          if (!Greedy && valid) {
+            // the best exact score any thread of the CTA has found for the request in this
+            // job (keys of earlier jobs carry a smaller tag and read as nothing)
+            const unsigned long long sh = ld_volatile_shared_u64(&thr[ml]);
+            if (sh >= tag) {
+              const float ks = key_float((uint32_t)sh);
+              if (ks > known) {
+                known = ks;
+                if (Mr != -INFINITY) Tf = ex2_approx((known - Mr) * kLog2e) * kShrink;
+              }
+            }
+          }
+#pragma unroll 1
+          for (int o = 0; o < S::kOct; ++o) {
+            const int v = vt + 8 * o;
+            const int col = c0 + 8 * o;                 // a multiple of 8
+            uint32_t a8[8];
+            __syncwarp();                               // a whole-warp load: every lane, converged
+            tmem_ld_32x32b_sync<8>(lane_base + kAccCol + (uint32_t)(kTileN * acc + col), a8);
+            if (!valid) continue;                       // a row beyond the batch
+            // U: box col / 32, row ml, 16-byte chunks (col % 32) / 4 and the next one,
+            // 128-byte swizzle (chunk ^ row % 8)
+            const uint8_t* row = us + (col >> 5) * (NBJ * 128) + u_row;
+            const int ch = (col & 31) >> 2;
+            const float4 u0 = *reinterpret_cast<const float4*>(row + ((ch ^ u_sw) << 4));
+            const float4 u1 = *reinterpret_cast<const float4*>(row + (((ch + 1) ^ u_sw) << 4));
+            float zo[8] = {__uint_as_float(a8[0]) + u0.x, __uint_as_float(a8[1]) + u0.y,
+                           __uint_as_float(a8[2]) + u0.z, __uint_as_float(a8[3]) + u0.w,
+                           __uint_as_float(a8[4]) + u1.x, __uint_as_float(a8[5]) + u1.y,
+                           __uint_as_float(a8[6]) + u1.z, __uint_as_float(a8[7]) + u1.w};
+            if (ragged) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (v + j >= p.V) zo[j] = -INFINITY;
+            }
+            float lm = zo[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) lm = fmaxf(lm, zo[j]);
+            if (lm == -INFINITY) continue;              // wholly beyond the vocabulary
+            mx = fmaxf(mx, lm);
+            if (lm > Mr + kLazy) {
+              ssum = (Mr == -INFINITY) ? 0.f : ssum * ex2_approx((Mr - lm) * kLog2e);
+              Mr = lm;
+              Tf = (known == -INFINITY) ? 0.f : ex2_approx((known - Mr) * kLog2e) * kShrink;
+            }
+            const float mL = Mr * kLog2e;
+            if constexpr (Greedy) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) ssum += ex2_approx(fmaf(zo[j], kLog2e, -mL));
+              if (lm > bsc) {                           // a later equal maximum has a larger v
+                int jl = 7;
+#pragma unroll
+                for (int j = 6; j >= 0; --j)
+                  if (zo[j] == lm) jl = j;
+                bsc = lm; bz = lm; bi = v + jl;
+              }
+            } else {
+              const uint4 d0 = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 0u), k0, k1);
+              const uint4 d1 = philox_wide(make_uint4((uint32_t)(v >> 2) + 1u, (uint32_t)k, (uint32_t)b, 0u), k0, k1);
+              const uint32_t dw[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+              unsigned cm = 0u;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float e = ex2_approx(fmaf(zo[j], kLog2e, -mL));
+                ssum += e;
+                cm |= (e > Tf * w_of_draw(dw[j]) ? 1u : 0u) << j;
+              }
+              if (cm) {
+                // candidates (rare past a job's first octet): recompute e and w, tighten
+                // with the best lower bound e (1 - w) / w <= e / E among them, keep the
+                // survivors of the tightened test, and score those exactly in increasing v
+                // (equal scores keep the smallest index).  The loop runs once per set bit of
+                // the lane's survivors, so a warp pays for its busiest lane only.
+                float ec[8], wc[8];
+                float L = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  ec[j] = ex2_approx(fmaf(zo[j], kLog2e, -mL));
+                  wc[j] = w_of_draw(dw[j]);
+                  if ((cm >> j) & 1u) L = fmaxf(L, ec[j] * (1.f - wc[j]) * rcp_approx(wc[j]));
+                }
+                const float Teff = fmaxf(Tf, L * kShrink);
+                unsigned sm = 0u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) sm |= (((cm >> j) & 1u) && ec[j] > Teff * wc[j] ? 1u : 0u) << j;
+                bool improved = false;
+                while (sm) {
+                  const int j = __ffs(sm) - 1;
+                  sm &= sm - 1u;
+                  const float wj = j < 4 ? (j < 2 ? (j == 0 ? wc[0] : wc[1]) : (j == 2 ? wc[2] : wc[3]))
+                                         : (j < 6 ? (j == 4 ? wc[4] : wc[5]) : (j == 6 ? wc[6] : wc[7]));
+                  const float zj = j < 4 ? (j < 2 ? (j == 0 ? zo[0] : zo[1]) : (j == 2 ? zo[2] : zo[3]))
+                                         : (j < 6 ? (j == 4 ? zo[4] : zo[5]) : (j == 6 ? zo[6] : zo[7]));
+                  const float scj = zj - logf(exp1_from_w(wj));
+                  if (scj > bsc) { bsc = scj; bi = v + j; bz = zj; improved = true; }
+                }
+                if (improved) {
+                  if (bsc > known) {
+                    known = bsc;
+                    Tf = ex2_approx((known - Mr) * kLog2e) * kShrink;
+                  }
+                  atomic_max_shared_u64(&thr[ml], tag | (unsigned long long)float_key(bsc));
+                }
+              }
+            }
+          }
+        }
+        if (have) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&acc_empty[acc]);
+            mbar_arrive(&u_empty[su]);
+          }
+        }
+      }
+      // ---- this thread's partial, then a shuffle tree per request of the chunk: every
+      // request has E = 512 / NBJ partials (one per sampler warp holding its rows), and
+      // sampler thread t merges entry t % E of request t / E with its E - 1 neighbours
+      {
+        const float st = (Mr == -INFINITY || mx == -INFINITY) ? 0.f : ssum * ex2_approx((Mr - mx) * kLog2e);
+        float* mw = merge + sw * kMergeStride + lane;
+        mw[0] = mx;
+        mw[32] = st;
+        mw[64] = bsc;
+        mw[96] = bz;
+        mw[128] = __int_as_float(bi);
+      }
+      named_bar_sync(kBarSamplers, kSamplerThreads);
+      {
+        constexpr int E = kSamplerThreads / NBJ;       // 16, 8 or 4 consecutive lanes
+        const int mrow = stid / E, e = stid % E;
+        const int src = (mrow >> 5) + (NBJ / 32) * e;  // the e-th warp holding row mrow
+        const float* mr = merge + src * kMergeStride + (mrow & 31);
+        float m = mr[0], s = mr[32], sc = mr[64], zz = mr[96];
+        int ix = __float_as_int(mr[128]);
+#pragma unroll
+        for (int o = E / 2; o >= 1; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+          const float sc2 = __shfl_xor_sync(0xffffffffu, sc, o);
+          const float z2 = __shfl_xor_sync(0xffffffffu, zz, o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, ix, o);
+          const float mm = fmaxf(m, m2);
+          if (mm != -INFINITY)
+            s = (m == -INFINITY ? 0.f : s * ex2_approx((m - mm) * kLog2e)) +
+                (m2 == -INFINITY ? 0.f : s2 * ex2_approx((m2 - mm) * kLog2e));
+          m = mm;
+          if (better(sc2, i2, sc, ix)) { sc = sc2; ix = i2; zz = z2; }
+        }
+        const int bm = c * NBJ + mrow;
+        if (e == 0 && bm < p.B && !*(volatile int*)&abort_s) {
+          RowState ps;
+          ps.m = m; ps.s = s; ps.score = sc; ps.z = zz; ps.idx = ix;
+          p.partials[((size_t)(k % 3) * p.B + bm) * G + cta] = ps;
+          if (ix >= 0) {
+            atomicMax(p.keys + (size_t)(k - 1) * p.B + bm, argmax_key(sc, ix));
+            // one CTA's local best: warm L2 with its W1 row for the gather after the barrier
+            if (k < p.gamma)
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                               reinterpret_cast<uint64_t>(p.W1 + (size_t)ix * p.r)),
+                           "r"((uint32_t)p.r * 2u)
+                           : "memory");
+          }
+        }
+      }
+      // the partials and keys are ordered before the grid arrival by this barrier; the
+      // merge area is free again after it
+      named_bar_sync(kBarSamplers, kSamplerThreads);
+      if (c + 1 == p.n_chunks) {
+        if (stid == 0 && !*(volatile int*)&abort_s)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.grid_count) : "memory");
+        // merge this CTA's share of position k - 1 while the other CTAs finish position k
+        // (slot (k - 1) % 3 is next written at position k + 2, after a barrier this CTA
+        // has not yet passed)
+        if (k > 1 && !*(volatile int*)&abort_s)
+          for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G) finalize_row<Greedy>(p, bb, k - 1, G, lane);
+        if (job + 1 < n_jobs) {
+          grid_wait((unsigned int)G * (unsigned int)k + p.grid_extra);
+          gather(job + 1);
+        }
+      }
+    }
+    // the last position: wait for every CTA, then merge this CTA's rows
+    grid_wait((unsigned int)G * (unsigned int)p.gamma + p.grid_extra);
+    if (!*(volatile int*)&abort_s)
+      for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G) finalize_row<Greedy>(p, bb, p.gamma, G, lane);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// U [B, gamma, V] fp32 as a 3-D tensor {V, gamma, B}; a box is 32 vocabulary entries (128
+// bytes, the 128-byte swizzle's span) of one position for NBJ requests.  Entries out of
+// range read as zero.
+bool encode_u_map_sw(CUtensorMap* map, const float* U, int B, int gamma, int V, int NBJ) {
+  EncodeTiledFn fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)gamma * V * 4};
+  cuuint32_t box[3] = {32, 1, (cuuint32_t)NBJ};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(U), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NBJ, bool Greedy>
+int lanes_grid() {
+  static std::atomic<int> cache[kMaxCachedDevices];
+  return per_device_grid(cache, [] {
+    int per = 0;
+    const size_t smem = LSmem<NBJ>::kBytes + 1024;
+    if (cudaFuncSetAttribute(draft_lanes_kernel<NBJ, Greedy>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, draft_lanes_kernel<NBJ, Greedy>,
+                                                      kThreads, smem) != cudaSuccess)
+      return -1;
+    return per > 0 ? 1 : 0;
+  });
+}
+
+template <int NBJ, bool Greedy>
+cudaError_t launch_lanes(const CUtensorMap& w2_map, const CUtensorMap& u_map, const LParams& p,
+                         int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = LSmem<NBJ>::kBytes + 1024;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, draft_lanes_kernel<NBJ, Greedy>, w2_map, u_map, p);
+}
+
+template <bool Greedy>
+int grid_of(int NBJ) {
+  return NBJ == 32 ? lanes_grid<32, Greedy>() : NBJ == 64 ? lanes_grid<64, Greedy>()
+                                                          : lanes_grid<128, Greedy>();
+}
+template <bool Greedy>
+cudaError_t launch_of(int NBJ, const CUtensorMap& w2_map, const CUtensorMap& u_map,
+                      const LParams& p, int grid, cudaStream_t stream) {
+  return NBJ == 32 ? launch_lanes<32, Greedy>(w2_map, u_map, p, grid, stream)
+       : NBJ == 64 ? launch_lanes<64, Greedy>(w2_map, u_map, p, grid, stream)
+                   : launch_lanes<128, Greedy>(w2_map, u_map, p, grid, stream);
+}
+
+// bound of the draft kernel's waits and the grid-barrier offset used by the next launches
+// (dspark_testing_set_wait_limit); 0 / 0 is the production setting
+std::atomic<long long> g_wait_cycles{0};
+std::atomic<unsigned int> g_grid_extra{0};
+
+}  // namespace
+
+void set_draft_wait_limit(long long cycles, unsigned int grid_extra) {
+  g_wait_cycles.store(cycles);
+  g_grid_extra.store(grid_extra);
+}
+
+size_t draft_region_bytes(int B, int gamma) {
+  return align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256) + 256 +
+         align_up((size_t)gamma * B * sizeof(unsigned long long), 256);
+}
+
+int draft_kchunk(int r) { return (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16; }
+
+cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
+                               const float* U, const int32_t* anchor, int B, int gamma, int V,
+                               int r, uint64_t seed, bool greedy, int32_t* tokens, float* q_tok,
+                               float* row_max, float* row_sumexp, void* region, int* err,
+                               cudaStream_t stream) {
+  const int NBJ = B <= 32 ? 32 : B <= 64 ? 64 : 128;
+  const int n_tiles = cdiv(V, kTileN);
+  int grid = greedy ? grid_of<true>(NBJ) : grid_of<false>(NBJ);
+  if (grid <= 0) return cudaErrorInvalidConfiguration;
+  if (grid > n_tiles) grid = n_tiles;
+  if (grid > kDraftMaxCtas) grid = kDraftMaxCtas;
+  LParams p;
+  memset(&p, 0, sizeof(p));
+  p.W1 = W1;
+  p.W2p = W2p;
+  p.anchor = anchor;
+  p.B = B; p.gamma = gamma; p.V = V; p.r = r;
+  p.n_tiles = n_tiles;
+  p.n_chunks = cdiv(B, NBJ);
+  p.kc = draft_kchunk(r);
+  p.seed = seed;
+  const size_t part_bytes = align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256);
+  char* base = static_cast<char*>(region);
+  p.partials = reinterpret_cast<RowState*>(base);
+  p.grid_count = reinterpret_cast<unsigned int*>(base + part_bytes);
+  p.keys = reinterpret_cast<unsigned long long*>(base + part_bytes + 256);
+  p.tokens = tokens;
+  p.q_tok = q_tok;
+  p.row_max = row_max;
+  p.row_sumexp = row_sumexp;
+  p.err = err;
+  const long long wc = g_wait_cycles.load();
+  p.wait_cycles = wc > 0 ? wc : kWaitCycles;
+  p.grid_extra = g_grid_extra.load();
+  cudaError_t e = cudaMemsetAsync(base + part_bytes, 0,
+                                  256 + (size_t)gamma * B * sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  CUtensorMap w2_map, u_map;
+  memset(&w2_map, 0, sizeof(w2_map));
+  if (!W2p && !encode_w2_map(&w2_map, W2, V, r, p.kc)) return cudaErrorInvalidValue;
+  if (!encode_u_map_sw(&u_map, U, B, gamma, V, NBJ)) return cudaErrorInvalidValue;
+  return greedy ? launch_of<true>(NBJ, w2_map, u_map, p, grid, stream)
+                : launch_of<false>(NBJ, w2_map, u_map, p, grid, stream);
+}
+
+}  // namespace dspark

@@ -1085,13 +1085,6 @@ cudaError_t launch_fused(const CUtensorMap& w2_map, const CUtensorMap& u_map, co
 
 }  // namespace
 
-size_t draft_region_bytes(int B, int gamma) {
-  return align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256) + 256 +
-         align_up((size_t)gamma * B * sizeof(unsigned long long), 256);
-}
-
-int draft_kchunk(int r) { return (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16; }
-
 namespace {
 template <bool Greedy, bool Rnn>
 int grid_for(int NB) { return NB == 16 ? max_grid<16, Greedy, Rnn>() : max_grid<32, Greedy, Rnn>(); }
@@ -1108,10 +1101,10 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
                                 int r, uint64_t seed, int32_t* tokens, float* q_tok,
                                 float* row_max, float* row_sumexp, void* region, int* err,
                                 bool greedy, const RnnDraftArgs* rnn, cudaStream_t stream) {
+  if (!rnn) return cudaErrorInvalidValue;
   const int NB = B <= 16 ? 16 : 32;
   const int n_tiles = cdiv(V, kGemmTileV);
-  int grid = rnn ? (greedy ? grid_for<true, true>(NB) : grid_for<false, true>(NB))
-                 : (greedy ? grid_for<true, false>(NB) : grid_for<false, false>(NB));
+  int grid = greedy ? grid_for<true, true>(NB) : grid_for<false, true>(NB);
   if (grid <= 0) return cudaErrorInvalidConfiguration;
   if (grid > n_tiles) grid = n_tiles;
   if (grid > kDraftMaxCtas) grid = kDraftMaxCtas;
@@ -1155,11 +1148,8 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
   memset(&w2_map, 0, sizeof(w2_map));
   if (!W2p && !encode_w2_map(&w2_map, W2, V, r, p.kc)) return cudaErrorInvalidValue;
   if (!encode_u_map(&u_map, U, B, gamma, V, NB)) return cudaErrorInvalidValue;
-  if (rnn)
-    return greedy ? launch_for<true, true>(NB, w2_map, u_map, p, grid, stream)
-                  : launch_for<false, true>(NB, w2_map, u_map, p, grid, stream);
-  return greedy ? launch_for<true, false>(NB, w2_map, u_map, p, grid, stream)
-                : launch_for<false, false>(NB, w2_map, u_map, p, grid, stream);
+  return greedy ? launch_for<true, true>(NB, w2_map, u_map, p, grid, stream)
+                : launch_for<false, true>(NB, w2_map, u_map, p, grid, stream);
 }
 }  // namespace
 
@@ -1167,8 +1157,8 @@ cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const flo
                                const int32_t* anchor, int B, int gamma, int V, int r,
                                uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,
                                float* row_sumexp, void* region, int* err, cudaStream_t stream) {
-  return launch_draft_common(W1, W2, nullptr, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
-                             row_max, row_sumexp, region, err, false, nullptr, stream);
+  return launch_draft_lanes(W1, W2, nullptr, U, anchor, B, gamma, V, r, seed, false, tokens,
+                            q_tok, row_max, row_sumexp, region, err, stream);
 }
 
 cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, const float* U,
@@ -1176,8 +1166,8 @@ cudaError_t launch_draft_fused_packed(const uint16_t* W1, const uint16_t* W2p, c
                                       uint64_t seed, int32_t* tokens, float* q_tok,
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream) {
-  return launch_draft_common(W1, nullptr, W2p, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
-                             row_max, row_sumexp, region, err, false, nullptr, stream);
+  return launch_draft_lanes(W1, nullptr, W2p, U, anchor, B, gamma, V, r, seed, false, tokens,
+                            q_tok, row_max, row_sumexp, region, err, stream);
 }
 
 cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
@@ -1185,8 +1175,8 @@ cudaError_t launch_draft_fused_greedy(const uint16_t* W1, const uint16_t* W2, co
                                       int V, int r, int32_t* tokens, float* q_tok,
                                       float* row_max, float* row_sumexp, void* region, int* err,
                                       cudaStream_t stream) {
-  return launch_draft_common(W1, W2p ? nullptr : W2, W2p, U, anchor, B, gamma, V, r, 0, tokens,
-                             q_tok, row_max, row_sumexp, region, err, true, nullptr, stream);
+  return launch_draft_lanes(W1, W2p ? nullptr : W2, W2p, U, anchor, B, gamma, V, r, 0, true,
+                            tokens, q_tok, row_max, row_sumexp, region, err, stream);
 }
 
 cudaError_t launch_draft_fused_rnn(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,

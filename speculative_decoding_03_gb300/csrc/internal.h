@@ -155,8 +155,19 @@ cudaError_t launch_bias_gemm_rows(const uint16_t* W2, const uint16_t* W2p, const
                                   int table_rows, const int32_t* prev, int B, int V, int r,
                                   float* out, int* err, cudaStream_t stream);
 
-// the whole draft (all gamma positions) in one cooperative launch; `region` holds
-// draft_region_bytes(B, gamma) of workspace
+// the whole draft (all gamma positions) in one cooperative launch of the request-major
+// kernel of draft.cu (W2p: packed tile images, else W2 by TMA; greedy: x = argmax z);
+// `region` holds draft_region_bytes(B, gamma) of workspace
+cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
+                               const float* U, const int32_t* anchor, int B, int gamma, int V,
+                               int r, uint64_t seed, bool greedy, int32_t* tokens, float* q_tok,
+                               float* row_max, float* row_sumexp, void* region, int* err,
+                               cudaStream_t stream);
+// bound (SM cycles, 0: the default of about 2 s) of that kernel's waits and an offset added
+// to its grid-barrier targets, for the launches that follow (tests of the timeout path)
+void set_draft_wait_limit(long long cycles, unsigned int grid_extra);
+
+// the same entry points under their ABI names (see draft_fused.cu)
 cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const float* U,
                                const int32_t* anchor, int B, int gamma, int V, int r,
                                uint64_t seed, int32_t* tokens, float* q_tok, float* row_max,

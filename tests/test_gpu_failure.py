@@ -1,0 +1,54 @@
+"""Failure detection on the GPU without a GPU fault: a bounded wait of the draft kernel is
+made to run out, and the library must report it and stay usable.
+
+The draft kernel bounds every wait (its shared-memory pipelines, its grid barrier).  The
+library's testing hook shortens the bound to about a millisecond and moves the grid
+barrier's target out of reach, so the first position's barrier cannot complete: every CTA
+gives up, records DSPARK_ERR_TIMEOUT, drains its copies and MMAs, frees its tensor memory
+and returns.  The host then reads the status, restores the production setting, and a
+normal draft on the same workspace must succeed and match the oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from _parity import draft_rows, draft_stats
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+ds = pytest.importorskip("speculative_decoding_03_gb300")
+
+TIMEOUT = 4          # DSPARK_ERR_TIMEOUT
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.mark.parametrize("name,greedy", [("qwen_small", False), ("wide_batch", True)])
+def test_draft_wait_runs_out_and_the_next_call_succeeds(name, greedy):
+    _need_gpu()
+    w = {"qwen_small": workloads.scaled(workloads.get("qwen3_4b_like"), B=5, gamma=3, V=904, r=64, H=32),
+         "wide_batch": workloads.scaled(workloads.get("scheduler_stress"), B=300, gamma=2, V=520, r=128, H=8)}[name]
+    inp = workloads.generate(w, with_T=False)
+    dev = ds.to_device(inp)
+    ws = ds.Workspace(w.B, w.gamma, w.V, w.r, w.H)
+    call = (lambda: ds.draft_greedy(dev["U"], dev["W1"], dev["W2"], dev["anchor"], ws)) if greedy else \
+        (lambda: ds.draft(dev["U"], dev["W1"], dev["W2"], dev["anchor"], w.seed, ws))
+    try:
+        ds.testing_set_wait_limit(2_000_000, unreachable_barrier=True)   # ~1 ms at 2 GHz
+        call()
+        assert ws.status() == TIMEOUT
+    finally:
+        ds.testing_set_wait_limit()
+    assert ws.status() == 0                                 # read and cleared
+    got = {k: v.cpu().numpy() for k, v in call().items()}
+    assert ws.status() == 0
+    ref = oracle.draft_greedy(inp.U, inp.W1, inp.W2, inp.anchor) if greedy else \
+        oracle.draft(inp.U, inp.W1, inp.W2, inp.anchor, w.seed)
+    _, same = draft_rows(got["tokens"], ref["tokens"], ref["gap"], name)
+    draft_stats(got, ref, same, keys=("row_max", "row_sumexp") if greedy else
+                ("q_tok", "row_max", "row_sumexp"), label=name)
