@@ -42,10 +42,16 @@ METRIC = "draft+verify positions/sec (B×γ) at V=151936, r=256; achieved HBM GB
 # (traffic null) once they change.
 DRAFT_TRAFFIC = {"workload": "qwen3_4b_like", "bytes": 233_439_488,
                  "sources_sha1": "cc3f613891caf90194e51300c102c39659c24a88"}
-DRAFT_SOURCES = ("draft_fused.cu", "sm100_ptx.cuh", "common.cuh", "internal.h")
+DRAFT_SOURCES = ("draft.cu", "sm100_ptx.cuh", "common.cuh", "internal.h")
 # kernels of one step: draft 1, confidence with the scheduler in its last CTA 1, verify 5
 # (target statistics, decision, bias contraction, final sample, finalize)
 KERNELS_PER_STEP = 7
+
+
+def launches_per_step(w) -> int:
+    """Kernels of one benchmarked step: the scheduler runs inside the confidence kernel
+    up to 16384 items, else in a launch of its own."""
+    return KERNELS_PER_STEP + (0 if w.B * w.gamma <= 16384 else 1)
 
 
 def _draft_traffic(w):
@@ -146,39 +152,50 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- CPU oracle
 
-def oracle_sample_step(w, seed: int, n_req: int, nthreads: int):
-    """One oracle step on the first n_req requests (their own batch); returns positions."""
+def oracle_sample_step(inp, seed: int, nthreads: int):
+    """One oracle step (draft, confidence, schedule, verify) on already generated inputs
+    (their requests as their own batch); returns the positions it drafted."""
     import oracle
-    inp = workloads.generate(w, requests=range(n_req))
     d = oracle.draft(inp.U, inp.W1, inp.W2, inp.anchor, seed, inp.requests, nthreads)
     _, a = oracle.confidence(inp.h, inp.anchor, d["tokens"], inp.W1, inp.w_c, float(inp.b_c))
     ell, _, _ = oracle.schedule(a.astype(np.float32), inp.sps)
     oracle.verify(inp.T, inp.U, inp.W1, inp.W2, inp.anchor, d["tokens"], ell, seed, inp.requests, nthreads)
-    return n_req * w.gamma
+    return len(inp.requests) * inp.w.gamma
 
 
 def cpu_baseline(w, n_req: int):
-    """The oracle as it stands on this host's cores, on a bounded request sample."""
+    """The oracle as it stands on this host's cores, on a bounded request sample: one step
+    of the first n_req requests with every core (OpenMP over requests), and one request on
+    one thread.  Inputs are generated before the timed regions."""
     import oracle
     n = _cores()
     oracle.lib()
+    n_req = max(1, min(w.B, n_req))
+    inp = workloads.generate(w, requests=range(n_req))
     t0 = time.perf_counter()
-    pos = oracle_sample_step(w, w.seed, n_req, n)
+    pos = oracle_sample_step(inp, w.seed, n)
     dt = time.perf_counter() - t0
+    one = workloads.generate(w, requests=[0])
+    t0 = time.perf_counter()
+    pos1 = oracle_sample_step(one, w.seed, 1)
+    dt1 = time.perf_counter() - t0
     return {"value": pos / dt, "unit": "positions/s", "cores": n, "kind": "oracle",
+            "single_thread": {"value": pos1 / dt1, "unit": "positions/s", "cores": 1,
+                              "sample": f"request 0 of {w.name}, one thread ({dt1:.2f} s)"},
             "sample": f"one full step (draft, confidence, schedule, verify) of the first {n_req} "
-                      f"requests of {w.name} as their own batch, fp64, OpenMP over requests; "
-                      f"{dt:.1f} s wall incl. input generation"}
+                      f"requests of {w.name} as their own batch, fp64, OpenMP over requests on "
+                      f"{n} cores; {dt:.2f} s wall, input generation outside the timed region"}
 
 
 # --------------------------------------------------------------------- reference arm
 
 def run_reference(args, w):
     """The oracle as it stands, timed on this host's cores, rank 0 only.  Each step is a
-    bounded sample of the workload (its first requests as their own batch): the first
-    warm-up step runs the full sample and measures it, and the sample of the other steps
-    is then sized so that the whole run (warm-up and timed steps) fits --ref-budget-s, down
-    to one request per OpenMP thread (below that a step would not get shorter)."""
+    bounded sample of the workload (its first requests as their own batch, generated once
+    before any timing; every step draws with its own seed): the first warm-up step runs
+    the full sample and measures it, and the sample of the other steps is then sized so
+    that the whole run (warm-up and timed steps) fits --ref-budget-s, down to one request
+    per OpenMP thread (below that a step would not get shorter)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
@@ -186,8 +203,9 @@ def run_reference(args, w):
     n = _cores()
     oracle.lib()
     n_full = min(w.B, args.ref_requests)
+    inp_full = workloads.generate(w, requests=range(n_full))
     t0 = time.perf_counter()
-    oracle_sample_step(w, w.seed, n_full, n)
+    oracle_sample_step(inp_full, w.seed, n)
     t_full = time.perf_counter() - t0
     # the oracle runs the requests in rounds of its OpenMP threads: size the sample in whole
     # rounds (at least one, so every thread still has a request)
@@ -198,12 +216,13 @@ def run_reference(args, w):
         per_step = max(0.0, args.ref_budget_s - t_full) / remaining
         rounds = max(1, int(per_step / (t_full / rounds_full)))
         n_req = min(n_full, rounds * max(1, n))
+    inp = workloads.generate(w, requests=range(n_req)) if n_req != n_full else inp_full
     for i in range(1, args.warmup):
-        oracle_sample_step(w, w.seed + i, n_req, n)
+        oracle_sample_step(inp, w.seed + i, n)
     t0 = time.perf_counter()
     pos = 0
     for i in range(args.steps):
-        pos += oracle_sample_step(w, w.seed + args.warmup + i, n_req, n)
+        pos += oracle_sample_step(inp, w.seed + args.warmup + i, n)
     dt = time.perf_counter() - t0
     value = pos / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
@@ -213,7 +232,8 @@ def run_reference(args, w):
             "config": dict(w.describe(), sample_requests=n_req),
             "cpu_baseline": {"value": value, "unit": "positions/s", "cores": n, "kind": "oracle",
                              "sample": f"first {n_req} requests of {w.name} as their own batch per "
-                                       f"step (sized to a {args.ref_budget_s:.0f} s run; the full "
+                                       f"step, generated once before timing, a new seed per step "
+                                       f"(sized to a {args.ref_budget_s:.0f} s run; the full "
                                        f"{n_full}-request step took {t_full:.1f} s)"},
             "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -241,6 +261,62 @@ def max_over_ranks(t_ms: float, dist, device: str = "cpu") -> float:
 def whole_job_rate(world: int, w, ms_per_step: float) -> float:
     """Positions per second of all replicas together: every rank does B * gamma per step."""
     return world * w.B * w.gamma / (ms_per_step * 1e-3)
+
+
+# ------------------------------------------------------------ the other workloads
+
+def measure_workload(w, args, world: int, rank: int, local: int, barrier, dist=None):
+    """The same step on another workload (the headline's procedure at a smaller step
+    count): graph-replayed steps with inputs resident in HBM, the draft launch alone, the
+    roofline of both, and the oracle's rate on a bounded sample of the same workload."""
+    import torch
+    import speculative_decoding_03_gb300 as ds
+    wr = replica_workload(w, rank)
+    inp = workloads.generate(wr)
+    dev = ds.to_device(inp, f"cuda:{local}")
+    step = ds.Step(dev, float(inp.b_c))
+    stream = torch.cuda.current_stream()
+    for i in range(3):
+        step.run(seed=w.seed + i)
+    n = max(3, min(args.steps, 50))
+    n_ring = 8
+
+    def time_graphs(gs):
+        for g in gs:
+            g.replay()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            gs[i % len(gs)].replay()
+        e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) / n
+
+    ms = time_graphs(step.capture([w.seed + 10 + j for j in range(n_ring)]))
+    ms = max_over_ranks(ms, dist, f"cuda:{local}")
+    res = step.results()
+    draft_ms = time_graphs(step.capture([w.seed + 20 + j for j in range(n_ring)], draft_only=True))
+    peak, peak_kind = _peaks()
+    dbytes = draft_bytes(w)
+    sbytes = step_bytes(w, res["n_out"], res["accept_len"], res["ell"])
+    out = {"config": w.describe(), "ms_per_step": ms, "value": whole_job_rate(world, w, ms),
+           "unit": "positions/s",
+           "roofline": {"bound": "hbm", "kernel": "draft (request-major, dspark_draft_packed)",
+                        "achieved": dbytes / (draft_ms * 1e-3) / 1e9, "peak": peak,
+                        "peak_kind": peak_kind, "unit": "GB/s",
+                        "frac": dbytes / (draft_ms * 1e-3) / 1e9 / peak,
+                        "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
+           "step_hbm": {"algorithmic_bytes": sbytes, "achieved": sbytes / (ms * 1e-3) / 1e9,
+                        "unit": "GB/s", "frac": sbytes / (ms * 1e-3) / 1e9 / peak},
+           "accept": {"mean_ell": float(np.mean(res["ell"])),
+                      "mean_accept_len": float(np.mean(res["accept_len"])), "B_total": res["B_total"]},
+           "gpu_launches_per_step": launches_per_step(w)}
+    del step, dev
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, min(w.B, args.ref_requests))
+    return out
 
 
 # --------------------------------------------------------------------- our arm
@@ -427,6 +503,13 @@ def run_ours(args, w):
     e2e_s = (time.perf_counter() - t0) / n_e2e
     h2d, d2h = step.step_bytes()
 
+    # the other workloads, each measured the same way on every replica (barriers included)
+    per_workload = {}
+    if args.per_workload:
+        for other in workloads.WORKLOADS:
+            if other.name != w.name:
+                per_workload[other.name] = measure_workload(other, args, world, rank, local, barrier, dist)
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -436,7 +519,6 @@ def run_ours(args, w):
     dbytes = draft_bytes(w)
     achieved = dbytes / (draft_ms * 1e-3) / 1e9
     sbytes = step_bytes(w, res["n_out"], res["accept_len"], res["ell"])
-    launches_per_step = KERNELS_PER_STEP
     line = {
         "metric": METRIC,
         "value": whole_job_rate(world, w, ms_per_step),
@@ -450,7 +532,7 @@ def run_ours(args, w):
                           ((w.B * w.gamma * w.V + w.B * (w.gamma + 1) * w.V) * 4 / 1e6),
                        parallelism=f"replicas x{world}",
                        launch="cuda graph ring of 8 seeds" if args.graph else "eager"),
-        "roofline": {"bound": "hbm", "kernel": "draft_fused_kernel via dspark_draft_packed (bias contraction + sampling, all gamma positions)",
+        "roofline": {"bound": "hbm", "kernel": "draft_lanes_kernel via dspark_draft_packed (bias contraction + sampling, all gamma positions)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _draft_traffic(w),
                      "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
@@ -462,11 +544,13 @@ def run_ours(args, w):
         "variants": variants,
         "e2e": {"value": whole_job_rate(world, w, e2e_s * 1e3), "unit": "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, min(w.B, args.ref_requests))
+    if per_workload:
+        line["per_workload"] = per_workload
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -484,6 +568,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="wall-time budget of the reference arm (its per-step sample is sized to it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", dest="per_workload", action="store_false",
+                    help="skip the other workloads' block")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every call from Python instead of replaying captured steps")
     args = ap.parse_args(argv)

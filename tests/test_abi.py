@@ -46,6 +46,11 @@ def test_workspace_bytes():
     assert L.dspark_workspace_bytes(4, 4, 1001, 16, 64) == 0      # V % 8 != 0
     assert L.dspark_workspace_bytes(4, 4, 1000, 24, 64) == 0      # r % 16 != 0
     assert L.dspark_workspace_bytes(4, 33, 1000, 16, 64) == 0     # gamma > 32
+    # the largest accepted batches: B * gamma beyond a 65535-CTA grid dimension is accepted
+    # (the verification folds its rows into the grid), B * (gamma + 1) >= 2^21 is not
+    assert L.dspark_workspace_bytes(4096, 16, 64, 16, 0) > 0
+    assert L.dspark_workspace_bytes(65535, 31, 8, 16, 0) > 0
+    assert L.dspark_workspace_bytes(65535, 32, 8, 16, 0) == 0
 
 
 def _draft(L, U=FAKE, W1=FAKE, W2=FAKE, anchor=FAKE, B=4, gamma=4, V=1000, r=16, out=FAKE,

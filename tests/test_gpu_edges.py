@@ -128,3 +128,30 @@ def test_target_peaked_elsewhere_rejects_every_first_position():
     np.testing.assert_array_equal(v["n_out"], 1)
     np.testing.assert_array_equal(v["out_tokens"][:, 0], peak)       # the residual's mass
     np.testing.assert_array_equal(v["out_tokens"][:, 1:], -1)
+
+
+def test_verify_with_more_rows_than_a_grid_dimension():
+    """B * gamma = 65536 verified rows (one more than a grid's y extent): the statistics
+    kernel folds them and the outcomes match the oracle."""
+    _need_gpu()
+    B, gamma, V, r, seed = 4096, 16, 64, 16, 31
+    rng = np.random.default_rng(seed)
+    U = rng.normal(0, 2, size=(B, gamma, V)).astype(np.float32)
+    T = (np.concatenate([U, rng.normal(0, 2, size=(B, 1, V)).astype(np.float32)], axis=1) +
+         rng.normal(0, 1, size=(B, gamma + 1, V)).astype(np.float32))
+    W1 = workloads.f32_to_bf16_bits(rng.normal(0, 0.02, size=(V, r)).astype(np.float32))
+    W2 = workloads.f32_to_bf16_bits(rng.normal(0, 0.02, size=(r, V)).astype(np.float32))
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    ell = np.full(B, gamma, np.int32)
+    d = oracle.draft(U, W1, W2, anchor, seed)
+    ref = oracle.verify(T, U, W1, W2, anchor, d["tokens"], ell, seed)
+    ws = ds.Workspace(B, gamma, V, r)
+    cu = lambda x, dt: torch.from_numpy(np.ascontiguousarray(x, dtype=dt)).cuda()
+    out = ds.verify(cu(T, np.float32), cu(U, np.float32), ds.as_bf16_tensor(W1), ds.as_bf16_tensor(W2),
+                    cu(anchor, np.int32), cu(d["tokens"], np.int32), cu(d["q_tok"], np.float32),
+                    cu(d["row_max"], np.float32), cu(d["row_sumexp"], np.float32), cu(ell, np.int32),
+                    seed, ws)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    assert ws.status() == 0
+    verify_rows(got, ref, "B4096_g16")
+    assert np.mean(got["accept_len"] == ref["accept_len"]) > 0.999

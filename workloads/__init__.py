@@ -32,6 +32,7 @@ regenerated on its own (the oracle checks sampled requests at full size).
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import Callable, Dict, List, Optional, Sequence
 
 import numpy as np
@@ -214,12 +215,28 @@ def generate(w: Workload, requests: Optional[Sequence[int]] = None, with_T: bool
     U = np.empty((n, w.gamma, w.V), dtype=np.float32)
     T = np.empty((n, w.gamma + 1, w.V), dtype=np.float32) if with_T else None
     h = np.empty((n, w.gamma, w.H), dtype=np.float32)
-    for i, b in enumerate(reqs):
-        u, t = gen_U_T(w, int(b), with_T)
+
+    def one(i: int) -> None:
+        b = int(reqs[i])
+        u, t = gen_U_T(w, b, with_T)
         U[i] = u
         if with_T:
             T[i] = t
-        h[i] = gen_h(w, int(b))
+        h[i] = gen_h(w, b)
+
+    # every request draws from its own generator, so the rows do not depend on the order
+    # (or the thread) they are made in; numpy releases the GIL while it fills large arrays
+    if n * w.gamma * w.V >= (1 << 24):
+        import concurrent.futures as cf
+        try:
+            workers = max(1, min(16, len(os.sched_getaffinity(0))))
+        except AttributeError:  # pragma: no cover
+            workers = max(1, min(16, os.cpu_count() or 1))
+        with cf.ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, range(n)))
+    else:
+        for i in range(n):
+            one(i)
     W1, W2, w_c, b_c = gen_weights(w)
     anchor = gen_anchor(w)[reqs]
     return Inputs(w, U, T, W1, W2, h, w_c, b_c, anchor, gen_sps(w), reqs)
