@@ -54,7 +54,7 @@ dspark_status dspark_markov_bias(const uint16_t* W1, const uint16_t* W2, const i
   if (!aligned(W1, 16) || !aligned(W2, 16) || !aligned(prev, 4) || !aligned(out, 4))
     return DSPARK_ERR_INVALID_ARG;
   if (!aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_INVALID_ARG;
-  if (launch_bias_gemm(W2, nullptr, W1, prev, prev_stride, B, V, r, out,
+  if (launch_bias_gemm(W2, nullptr, W1, prev, prev_stride, B, nullptr, V, r, out,
                        ws_at<int>(workspace, 0), stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;

@@ -18,6 +18,12 @@
 // The producer starts on W2 (an input) before the previous kernel on the stream has
 // finished; the epilogue warps wait for it before reading prev.
 //
+// Compact mode (verification): the row count is a device value written by the previous
+// kernel (the number of rejected requests), read by the epilogue after that kernel has
+// finished and published to the producer and the MMA issuer through an mbarrier; the first
+// pass over W2 is streamed before the count is known, later passes only when needed.  A
+// pass covers NB <= 128 rows (one tensor-core N per vocabulary tile).
+//
 // Split mode (the RNN head's verification): E[b] = Ef[prev_b], fp32 rows of a table of
 // table_rows rows; each row enters the contraction as two bf16 images, hi = bf16(E) and
 // lo = bf16(E - hi), and every K step issues one MMA per image on the same W2 rows, so
@@ -45,12 +51,12 @@ constexpr int kBiasDepth = 4;                 // accumulators in tensor memory
 constexpr int kBiasKChunkMax = 64;
 constexpr int kBiasNamedBar = 1;              // the epilogue warps' barrier
 
-template <bool Split>
+template <int NB, bool Split>
 struct BiasSmem {
   static constexpr int kStageBytes = 2 * kBiasKChunkMax * 128;
   static constexpr int kOffW = 0;
   static constexpr int kOffE = kOffW + kBiasStages * kStageBytes;
-  static constexpr int kEHalf = 32 * 256 * 2;    // NB <= 32 requests x r <= 256, one image
+  static constexpr int kEHalf = NB * 256 * 2;    // NB rows x r <= 256, one image
   static constexpr int kEBytes = (Split ? 2 : 1) * kEHalf;
   static constexpr int kBytes = kOffE + 2 * kEBytes;
 };
@@ -64,16 +70,18 @@ template <int NB, bool Split>
 __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
     const __grid_constant__ CUtensorMap w2_map, const uint16_t* __restrict__ W2p,
     const uint16_t* __restrict__ W1, const float* __restrict__ Ef, int table_rows,
-    const int32_t* __restrict__ prev, int prev_stride, int B, int V, int r, int kc, int n_tiles,
-    float* __restrict__ out, int* err) {
-  using S = BiasSmem<Split>;
+    const int32_t* __restrict__ prev, int prev_stride, int B, const int* __restrict__ n_rows,
+    int V, int r, int kc, int n_tiles, float* __restrict__ out, int* err) {
+  using S = BiasSmem<NB, Split>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t w_full[kBiasStages], w_empty[kBiasStages];
   __shared__ uint64_t e_full[2], e_empty[2];
   __shared__ uint64_t acc_full[kBiasDepth], acc_empty[kBiasDepth];
   __shared__ uint64_t mma_drain;
+  __shared__ uint64_t count_ready;   // the epilogue has published the pass count
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
+  __shared__ int rows_s, jobs_s;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,7 +90,6 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
   const int t_hi = (int)((long long)(cta + 1) * n_tiles / G);
   const int my_tiles = t_hi - t_lo;
   const int n_kchunks = r / kc;
-  const int n_jobs = (B + NB - 1) / NB;
   uint32_t tmem_cols = 32;
   while (tmem_cols < (uint32_t)(kBiasDepth * NB)) tmem_cols <<= 1;
 
@@ -91,6 +98,7 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
     for (int i = 0; i < 2; ++i) { mbar_init(&e_full[i], 1); mbar_init(&e_empty[i], 1); }
     for (int i = 0; i < kBiasDepth; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
     mbar_init(&mma_drain, 1);
+    mbar_init(&count_ready, 1);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -118,6 +126,13 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
     }
   };
 
+  // the number of passes over W2: known to the epilogue after the previous kernel; the
+  // first pass needs no count (it runs in every case), the others wait for it
+  auto passes_after_first = [&]() -> int {
+    if (!wait1(&count_ready, 0)) return 0;
+    return *(volatile int*)&jobs_s;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -126,7 +141,9 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
       const uint32_t w_bytes = 2u * (uint32_t)kc * 128u;
       uint32_t ws = 0;
       bool ok = true;
+      int n_jobs = 0x7FFFFFFF;                    // decided before the second pass
       for (int job = 0; job < n_jobs && ok; ++job) {
+        if (job == 1 && (n_jobs = passes_after_first()) <= 1) break;
         for (int t = t_lo; t < t_hi && ok; ++t) {
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
             const int s = ws % kBiasStages;
@@ -163,7 +180,9 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
                                         kSwizzle128B);
       uint32_t ws = 0, tc = 0;
       bool ok = true;
+      int n_jobs = 0x7FFFFFFF;
       for (int job = 0; job < n_jobs && ok; ++job) {
+        if (job == 1 && (n_jobs = passes_after_first()) <= 1) break;
         const int eb = job & 1;
         if (!(ok = wait1(&e_full[eb], (job >> 1) & 1))) break;
         const uint64_t b_base =
@@ -203,12 +222,25 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
     __syncwarp();
   } else {
     // --------------------------------------------- epilogue: E gather, TMEM -> bias rows
-    pdl_wait();                 // prev may come from the previous kernel
+    pdl_wait();                 // prev (and the row count) may come from the previous kernel
     pdl_launch_dependents();
     const int et = threadIdx.x - 64;              // 0 .. 127
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
     const int kchunks = r >> 3;                   // 16-byte chunks per W1 row
+    if (et == 0) {
+      int rows = B;
+      if (n_rows) {
+        rows = *n_rows;
+        rows = rows < 0 ? 0 : rows > B ? B : rows;
+      }
+      rows_s = rows;
+      jobs_s = rows > NB ? (rows + NB - 1) / NB : 1;
+      mbar_arrive(&count_ready);                  // release: rows_s and jobs_s first
+    }
+    named_bar_sync_n(kBiasNamedBar, 128);
+    const int rows = *(volatile int*)&rows_s;
+    const int n_jobs = *(volatile int*)&jobs_s;
     uint32_t tc = 0;
     for (int job = 0; job < n_jobs; ++job) {
       const int b0 = job * NB;
@@ -223,7 +255,7 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
           const int n = idx / kchunks, c = idx - n * kchunks;
           const int b = b0 + n;
           uint4 val = make_uint4(0u, 0u, 0u, 0u), lo = val;
-          if (b < B) {
+          if (b < rows) {
             const int pv = prev[(size_t)b * prev_stride];
             if (pv >= 0 && pv < table_rows) {
               if constexpr (Split) {
@@ -260,21 +292,21 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
         const bool ok = wait1(&acc_full[ab], (tc / kBiasDepth) & 1);
         if (!__all_sync(0xffffffffu, ok)) continue;
         tc_fence_after_sync();
-        float vals[NB];
+        const int v = (t_lo + t) * kGemmTileV + q * 32 + lane;
+        // 16 columns (rows b) at a time; the accumulator is released after the last
+#pragma unroll 1
+        for (int c16 = 0; c16 < NB && b0 + c16 < rows; c16 += 16) {
+          uint32_t vals[16];
+          tmem_ld_32x32b_sync<16>(trow + (uint32_t)(ab * NB + c16), vals);
+          if (v < V) {
 #pragma unroll
-        for (int c16 = 0; c16 < NB; c16 += 16)
-          tmem_ld_32x32b_x16(trow + (uint32_t)(ab * NB + c16),
-                             *reinterpret_cast<float(*)[16]>(vals + c16));
-        tmem_ld_wait();
+            for (int j = 0; j < 16; ++j)
+              if (b0 + c16 + j < rows) out[(size_t)(b0 + c16 + j) * V + v] = __uint_as_float(vals[j]);
+          }
+        }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[ab]);
-        const int v = (t_lo + t) * kGemmTileV + q * 32 + lane;
-        if (v < V) {
-#pragma unroll
-          for (int j = 0; j < NB; ++j)
-            if (b0 + j < B) out[(size_t)(b0 + j) * V + v] = vals[j];
-        }
       }
     }
   }
@@ -288,7 +320,7 @@ int bias_grid(int n_tiles) {
   static std::atomic<int> cache[kMaxCachedDevices];
   const int g = per_device_grid(cache, [] {
     int per = 0;
-    const size_t smem = BiasSmem<Split>::kBytes + 1024;
+    const size_t smem = BiasSmem<NB, Split>::kBytes + 1024;
     if (cudaFuncSetAttribute(bias_gemm_kernel<NB, Split>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_gemm_kernel<NB, Split>, kBiasThreads,
@@ -330,44 +362,56 @@ bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_r
 }
 
 namespace {
+template <int NB, bool Split>
+cudaError_t launch_bias_nb(const CUtensorMap& w2_map, const uint16_t* W2p, const uint16_t* W1,
+                           const float* Ef, int table_rows, const int32_t* prev, int prev_stride,
+                           int B, const int* n_rows, int V, int r, int kc, int n_tiles, float* out,
+                           int* err, cudaStream_t stream) {
+  const int grid = bias_grid<NB, Split>(n_tiles);
+  if (grid <= 0) return cudaErrorInvalidConfiguration;
+  return launch_pdl(bias_gemm_kernel<NB, Split>, dim3(grid), dim3(kBiasThreads),
+                    (size_t)BiasSmem<NB, Split>::kBytes + 1024, stream, w2_map, W2p, W1, Ef,
+                    table_rows, prev, prev_stride, B, n_rows, V, r, kc, n_tiles, out, err);
+}
+
 template <bool Split>
 cudaError_t launch_bias_common(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
                                const float* Ef, int table_rows, const int32_t* prev,
-                               int prev_stride, int B, int V, int r, float* out, int* err,
-                               cudaStream_t stream) {
+                               int prev_stride, int B, const int* n_rows, int V, int r, float* out,
+                               int* err, cudaStream_t stream) {
   const int kc = draft_kchunk(r);
   CUtensorMap w2_map;
   memset(&w2_map, 0, sizeof(w2_map));
   if (!W2p && !encode_w2_map(&w2_map, W2, V, r, kc)) return cudaErrorInvalidValue;
   const int n_tiles = cdiv(V, kGemmTileV);
-  const size_t smem = BiasSmem<Split>::kBytes + 1024;
-  if (B <= 16) {
-    const int grid = bias_grid<16, Split>(n_tiles);
-    if (grid <= 0) return cudaErrorInvalidConfiguration;
-    return launch_pdl(bias_gemm_kernel<16, Split>, dim3(grid), dim3(kBiasThreads), smem, stream,
-                      w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, V, r, kc, n_tiles,
-                      out, err);
-  }
-  const int grid = bias_grid<32, Split>(n_tiles);
-  if (grid <= 0) return cudaErrorInvalidConfiguration;
-  return launch_pdl(bias_gemm_kernel<32, Split>, dim3(grid), dim3(kBiasThreads), smem, stream,
-                    w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, V, r, kc, n_tiles, out,
-                    err);
+  // rows per pass: the smallest tensor-core N that holds the batch (the split mode's two
+  // operand images fit 64 rows)
+  if (B <= 16)
+    return launch_bias_nb<16, Split>(w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, n_rows,
+                                     V, r, kc, n_tiles, out, err, stream);
+  if (B <= 32)
+    return launch_bias_nb<32, Split>(w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, n_rows,
+                                     V, r, kc, n_tiles, out, err, stream);
+  if (B <= 64 || Split)
+    return launch_bias_nb<64, Split>(w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, n_rows,
+                                     V, r, kc, n_tiles, out, err, stream);
+  return launch_bias_nb<128, false>(w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, n_rows,
+                                    V, r, kc, n_tiles, out, err, stream);
 }
 }  // namespace
 
 cudaError_t launch_bias_gemm(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
-                             const int32_t* prev, int prev_stride, int B, int V, int r, float* out,
-                             int* err, cudaStream_t stream) {
-  return launch_bias_common<false>(W2, W2p, W1, nullptr, V, prev, prev_stride, B, V, r, out, err,
-                                   stream);
+                             const int32_t* prev, int prev_stride, int B, const int* n_rows, int V,
+                             int r, float* out, int* err, cudaStream_t stream) {
+  return launch_bias_common<false>(W2, W2p, W1, nullptr, V, prev, prev_stride, B, n_rows, V, r, out,
+                                   err, stream);
 }
 
 cudaError_t launch_bias_gemm_rows(const uint16_t* W2, const uint16_t* W2p, const float* Ef,
-                                  int table_rows, const int32_t* prev, int B, int V, int r,
-                                  float* out, int* err, cudaStream_t stream) {
-  return launch_bias_common<true>(W2, W2p, nullptr, Ef, table_rows, prev, 1, B, V, r, out, err,
-                                  stream);
+                                  int table_rows, const int32_t* prev, int B, const int* n_rows,
+                                  int V, int r, float* out, int* err, cudaStream_t stream) {
+  return launch_bias_common<true>(W2, W2p, nullptr, Ef, table_rows, prev, 1, B, n_rows, V, r, out,
+                                  err, stream);
 }
 
 }  // namespace dspark

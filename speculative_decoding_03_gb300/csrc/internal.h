@@ -63,7 +63,7 @@ struct Plan {
   RowSplit stats, ver;
   // byte offsets into the workspace
   size_t off_err, off_draft, off_bias, off_part, off_M, off_lnS, off_p, off_mode,
-      off_pos, off_prev, off_fallback, off_rnn_state, total;
+      off_pos, off_prev, off_slot, off_nres, off_fallback, off_rnn_state, total;
 };
 
 inline Plan make_plan(int B, int gamma, int V, int r, int H) {
@@ -82,7 +82,9 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_p = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
   p.off_mode = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_pos = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
-  p.off_prev = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
+  p.off_prev = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);   // by residual slot
+  p.off_slot = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);   // slot of request b
+  p.off_nres = o; o += 256;                                              // residual count
   p.off_fallback = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   // RNN head: state [2][B][r] fp32, then the current position's rows [B][2][r] bf16
   // RNN head: kRnnStateCopies copies of the state [2][B][r] fp32 and of the E rows [B][2][r] bf16
@@ -144,16 +146,17 @@ EncodeTiledFn tensor_map_encoder();
 bool encode_w2_map(CUtensorMap* map, const uint16_t* W2, int V, int r, int box_rows);
 
 // ---- launchers (return cudaError_t of the launch) ----
-// bias[b][v] = sum_i W1[prev_b][i] * W2[i][v] for b < B, v < V (rows with prev_b == -1 are 0)
-// (W2p: the packed tile images of pack.cu in place of W2, or null)
+// bias[b][v] = sum_i W1[prev_b][i] * W2[i][v] for b < rows, v < V (rows with prev_b == -1
+// are 0); rows = B, or min(B, *n_rows) when n_rows (a device value the previous kernel on
+// the stream writes) is not null.  W2p: the packed tile images of pack.cu in place of W2.
 cudaError_t launch_bias_gemm(const uint16_t* W2, const uint16_t* W2p, const uint16_t* W1,
-                             const int32_t* prev, int prev_stride, int B, int V, int r, float* out,
-                             int* err, cudaStream_t stream);
+                             const int32_t* prev, int prev_stride, int B, const int* n_rows, int V,
+                             int r, float* out, int* err, cudaStream_t stream);
 // bias[b][v] = sum_i Ef[prev_b][i] * W2[i][v] with fp32 rows Ef [table_rows][r] taken as two
-// bf16 terms each (rows with prev_b == -1 are 0)
+// bf16 terms each (rows with prev_b == -1 are 0); rows as above
 cudaError_t launch_bias_gemm_rows(const uint16_t* W2, const uint16_t* W2p, const float* Ef,
-                                  int table_rows, const int32_t* prev, int B, int V, int r,
-                                  float* out, int* err, cudaStream_t stream);
+                                  int table_rows, const int32_t* prev, int B, const int* n_rows,
+                                  int V, int r, float* out, int* err, cudaStream_t stream);
 
 // the whole draft (all gamma positions) in one cooperative launch of the request-major
 // kernel of draft.cu (W2p: packed tile images, else W2 by TMA; greedy: x = argmax z);

@@ -125,10 +125,12 @@ __device__ __forceinline__ void max_sum_merge(float& m, float& s, float m2, floa
 
 __global__ void __launch_bounds__(kSampleThreads) target_stats_kernel(
     const float* __restrict__ T, const int32_t* __restrict__ ell, int B, int gamma, int V,
-    int splits, float2* __restrict__ partials) {
+    int splits, float2* __restrict__ partials, int* __restrict__ n_res) {
   __shared__ float red_m[kSampleThreads / 32], red_s[kSampleThreads / 32];
   pdl_wait();
   pdl_launch_dependents();
+  // the decision kernel that follows counts the residual rows from zero
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *n_res = 0;
   // rows (k, b) in position order; the grid's y extent is capped at 65535, so a CTA takes
   // every gridDim.y-th row
   for (int y = blockIdx.y; y < B * gamma; y += gridDim.y) {
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(128) decide_kernel(
     int gamma, int V, uint64_t seed, float* __restrict__ M_t, float* __restrict__ lnS_t,
     float* __restrict__ p_t, int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ n_out, int32_t* __restrict__ mode, int32_t* __restrict__ pos,
-    int32_t* __restrict__ prev_tok, int32_t* __restrict__ fallback, int* err, int rnn_rows) {
+    int32_t* __restrict__ res_prev, int32_t* __restrict__ slot_of, int* __restrict__ n_res,
+    int32_t* __restrict__ fallback, int* err, int rnn_rows) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -230,18 +233,20 @@ __global__ void __launch_bounds__(128) decide_kernel(
     if (j && !q_tok) {
       mode[b] = kModePointResidual;
       pos[b] = j;
-      prev_tok[b] = -1;
+      slot_of[b] = -1;
     } else if (j) {
       mode[b] = kModeResidual;
       pos[b] = j;
-      // the bias operand of the rejected row: the Markov head's predecessor token, or the
-      // RNN head's output row (b, j) of the draft
-      prev_tok[b] = rnn_rows ? b * gamma + (j - 1)
-                             : ((j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)]);
+      // a slot of the compact residual rows, and the bias operand of the rejected row: the
+      // Markov head's predecessor token, or the RNN head's output row (b, j) of the draft
+      const int slot = atomicAdd(n_res, 1);
+      slot_of[b] = slot;
+      res_prev[slot] = rnn_rows ? b * gamma + (j - 1)
+                                : ((j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)]);
     } else {
       mode[b] = kModeBonus;
       pos[b] = L + 1;
-      prev_tok[b] = -1;
+      slot_of[b] = -1;
     }
   }
 }
@@ -389,8 +394,8 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const float* __restrict__ row_max, const float* __restrict__ row_sumexp,
     const float* __restrict__ M_t, const float* __restrict__ lnS_t,
     const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
-    const int32_t* __restrict__ tokens, int B, int gamma, int V, uint64_t seed, int splits,
-    RowState* __restrict__ partials, int* err) {
+    const int32_t* __restrict__ slot_of, const int32_t* __restrict__ tokens, int B, int gamma,
+    int V, uint64_t seed, int splits, RowState* __restrict__ partials, int* err) {
   extern __shared__ float4 fs_buf[];            // [2][3][kVerSeg / 4]
   __shared__ uint64_t full[2];
   __shared__ RowState red[32];
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
       mbar_expect_tx_cta(&full[buf], 3u * bytes);
       bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
       bulk_g2s(dst + kSlot, U + o * V + v0, bytes, &full[buf]);
-      bulk_g2s(dst + 2 * kSlot, bias + (size_t)b * V + v0, bytes, &full[buf]);
+      bulk_g2s(dst + 2 * kSlot, bias + (size_t)slot_of[b] * V + v0, bytes, &full[buf]);
     } else if (md == kModeBonus || md == kModePointResidual) {
       mbar_expect_tx_cta(&full[buf], bytes);
       bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
@@ -560,26 +565,32 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   float* p_t = ws_at<float>(ws, p.off_p);
   int32_t* mode = ws_at<int32_t>(ws, p.off_mode);
   int32_t* pos = ws_at<int32_t>(ws, p.off_pos);
-  int32_t* prev = ws_at<int32_t>(ws, p.off_prev);
+  int32_t* res_prev = ws_at<int32_t>(ws, p.off_prev);
+  int32_t* slot_of = ws_at<int32_t>(ws, p.off_slot);
+  int* n_res = ws_at<int>(ws, p.off_nres);
   int32_t* fb = ws_at<int32_t>(ws, p.off_fallback);
 
   cudaError_t e = launch_pdl(target_stats_kernel, dim3(p.stats.splits, B * gamma < 65535 ? B * gamma : 65535),
                              dim3(kSampleThreads), 0, stream, T, ell, B, gamma, V,
-                             p.stats.splits, part_stats);
+                             p.stats.splits, part_stats, n_res);
   if (e != cudaSuccess) return e;
   e = launch_pdl(decide_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream, T, anchor, tokens, q_tok,
                  (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, M_t, lnS_t,
-                 p_t, accept_len, out_tokens, n_out, mode, pos, prev, fb, err, E_all ? 1 : 0);
+                 p_t, accept_len, out_tokens, n_out, mode, pos, res_prev, slot_of, n_res, fb,
+                 err, E_all ? 1 : 0);
   if (e != cudaSuccess) return e;
   if (!point_mass) {
-    e = E_all ? launch_bias_gemm_rows(W2, W2p, E_all, B * gamma, prev, B, V, p.r, bias, err, stream)
-              : launch_bias_gemm(W2, W2p, W1, prev, 1, B, V, p.r, bias, err, stream);
+    // only the rejected requests' rows, in the slots the decision kernel gave them
+    e = E_all ? launch_bias_gemm_rows(W2, W2p, E_all, B * gamma, res_prev, B, n_res, V, p.r, bias,
+                                      err, stream)
+              : launch_bias_gemm(W2, W2p, W1, res_prev, 1, B, n_res, V, p.r, bias, err, stream);
     if (e != cudaSuccess) return e;
   }
   e = launch_pdl(final_sample_kernel, dim3(final_sample_grid(B * p.ver.splits)),
                  dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias, row_max,
                  row_sumexp, (const float*)M_t, (const float*)lnS_t, (const int32_t*)mode,
-                 (const int32_t*)pos, tokens, B, gamma, V, seed, p.ver.splits, part_ver, err);
+                 (const int32_t*)pos, (const int32_t*)slot_of, tokens, B, gamma, V, seed,
+                 p.ver.splits, part_ver, err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(finalize_kernel, dim3(B), dim3(kSampleThreads), 0, stream, T,
                  (const RowState*)part_ver, p.ver.splits, gamma, V, seed, (const int32_t*)mode,
