@@ -43,15 +43,17 @@ METRIC = "draft+verify positions/sec (B×γ) at V=151936, r=256; achieved HBM GB
 DRAFT_TRAFFIC = {"workload": "qwen3_4b_like", "bytes": 233_439_488,
                  "sources_sha1": "cc3f613891caf90194e51300c102c39659c24a88"}
 DRAFT_SOURCES = ("draft.cu", "sm100_ptx.cuh", "common.cuh", "internal.h")
-# kernels of one step: draft 1, confidence with the scheduler in its last CTA 1, verify 5
-# (target statistics, decision, bias contraction, final sample, finalize)
-KERNELS_PER_STEP = 7
+FIRST_KERNEL = ("draft_lanes_kernel via dspark_draft_confidence_schedule (bias contraction, "
+                "sampling, confidence and schedule, all gamma positions)")
+VERIFY_KERNELS = 5          # target statistics, decision, bias rows, final draw, finalize
+FUSED_SCHEDULE_ITEMS = 384  # the draft launch schedules in its first CTA up to this B*gamma
 
 
 def launches_per_step(w) -> int:
-    """Kernels of one benchmarked step: the scheduler runs inside the confidence kernel
-    up to 16384 items, else in a launch of its own."""
-    return KERNELS_PER_STEP + (0 if w.B * w.gamma <= 16384 else 1)
+    """Kernels of one benchmarked step: one launch drafts, scores confidence and (up to
+    384 items) schedules; larger batches schedule in a launch of their own; then the
+    verification's kernels."""
+    return 1 + (0 if w.B * w.gamma <= FUSED_SCHEDULE_ITEMS else 1) + VERIFY_KERNELS
 
 
 def _draft_traffic(w):
@@ -88,6 +90,12 @@ def draft_bytes(w) -> int:
     gathered, and the outputs (tokens, q, max, sum)."""
     return (w.B * w.gamma * w.V * 4 + w.r * w.V * 2 + w.B * w.gamma * w.r * 2 +
             w.B * w.gamma * 16)
+
+
+def first_launch_bytes(w) -> int:
+    """Bytes the step's first launch must move at least once: the draft's, the hidden
+    states h, the confidence outputs c and a, and (scheduled in the same launch) ell."""
+    return draft_bytes(w) + w.B * w.gamma * (w.H * 4 + 8) + w.H * 4 + w.B * 4
 
 
 def step_bytes(w, n_out: np.ndarray, accept_len: np.ndarray, ell: np.ndarray) -> int:
@@ -296,17 +304,20 @@ def measure_workload(w, args, world: int, rank: int, local: int, barrier, dist=N
     ms = time_graphs(step.capture([w.seed + 10 + j for j in range(n_ring)]))
     ms = max_over_ranks(ms, dist, f"cuda:{local}")
     res = step.results()
-    draft_ms = time_graphs(step.capture([w.seed + 20 + j for j in range(n_ring)], draft_only=True))
+    first_ms = time_graphs(step.capture([w.seed + 20 + j for j in range(n_ring)], first_only=True))
+    draft_ms = time_graphs(step.capture([w.seed + 30 + j for j in range(n_ring)], draft_only=True))
     peak, peak_kind = _peaks()
-    dbytes = draft_bytes(w)
+    fbytes, dbytes = first_launch_bytes(w), draft_bytes(w)
     sbytes = step_bytes(w, res["n_out"], res["accept_len"], res["ell"])
     out = {"config": w.describe(), "ms_per_step": ms, "value": whole_job_rate(world, w, ms),
            "unit": "positions/s",
-           "roofline": {"bound": "hbm", "kernel": "draft (request-major, dspark_draft_packed)",
-                        "achieved": dbytes / (draft_ms * 1e-3) / 1e9, "peak": peak,
+           "roofline": {"bound": "hbm", "kernel": FIRST_KERNEL,
+                        "achieved": fbytes / (first_ms * 1e-3) / 1e9, "peak": peak,
                         "peak_kind": peak_kind, "unit": "GB/s",
-                        "frac": dbytes / (draft_ms * 1e-3) / 1e9 / peak,
-                        "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
+                        "frac": fbytes / (first_ms * 1e-3) / 1e9 / peak,
+                        "algorithmic_bytes_per_launch": fbytes, "ms_per_launch": first_ms,
+                        "draft_alone": {"ms_per_launch": draft_ms, "algorithmic_bytes": dbytes,
+                                        "achieved": dbytes / (draft_ms * 1e-3) / 1e9}},
            "step_hbm": {"algorithmic_bytes": sbytes, "achieved": sbytes / (ms * 1e-3) / 1e9,
                         "unit": "GB/s", "frac": sbytes / (ms * 1e-3) / 1e9 / peak},
            "accept": {"mean_ell": float(np.mean(res["ell"])),
@@ -375,25 +386,32 @@ def run_ours(args, w):
     ms_per_step = t_ms / args.steps
     res = step.results()
 
-    # ---- dominant kernel: the draft launch, timed alone with events on its stream
+    # ---- dominant kernel: the step's first launch (draft, confidence and schedule), and
+    # the draft call alone, each timed with events on its stream
     ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x = step.dev
     n_draft = max(3, min(args.steps, 50))
+
+    def time_launch(run):
+        barrier()
+        ev_a.record(stream)
+        for i in range(n_draft):
+            run(i)
+        ev_b.record(stream)
+        barrier()
+        return ev_a.elapsed_time(ev_b) / n_draft
+
     if args.graph:
+        fgraphs = step.capture([w.seed + j for j in range(n_ring)], first_only=True)
         dgraphs = step.capture([w.seed + j for j in range(n_ring)], draft_only=True)
-        for g in dgraphs:
+        for g in fgraphs + dgraphs:
             g.replay()
-        run_draft = lambda i: dgraphs[i % n_ring].replay()
+        first_ms = time_launch(lambda i: fgraphs[i % n_ring].replay())
+        draft_ms = time_launch(lambda i: dgraphs[i % n_ring].replay())
     else:
-        run_draft = lambda i: ds.draft_packed(x["U"], x["W1"], step.W2p, x["anchor"], w.seed + i,
-                                              step.ws, step.draft_out)
-    barrier()
-    ev_a.record(stream)
-    for i in range(n_draft):
-        run_draft(i)
-    ev_b.record(stream)
-    barrier()
-    draft_ms = ev_a.elapsed_time(ev_b) / n_draft
+        first_ms = time_launch(lambda i: step.first_launch(w.seed + i))
+        draft_ms = time_launch(lambda i: ds.draft_packed(x["U"], x["W1"], step.W2p, x["anchor"],
+                                                         w.seed + i, step.ws, step.draft_out))
 
     # ---- the variants of the step (greedy drafting, two-step capacity scheduler, fixed
     # threshold): whole steps in a graph ring, and the greedy draft launch alone
@@ -461,8 +479,8 @@ def run_ours(args, w):
     # ---- per-call breakdown (warm, eager, events between the calls on one stream); the
     # step runs confidence and schedule as one launch, timed here both ways
     n_bd = max(3, min(args.steps, 20))
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    acc = [0.0] * 5
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    acc = [0.0] * 6
     d_out, c_out, s_out, v_out = step.draft_out, step.conf_out, step.sched_out, step.verify_out
     for i in range(n_bd):
         sd = w.seed + 500 + i
@@ -480,11 +498,14 @@ def run_ours(args, w):
                          d_out["q_tok"], d_out["row_max"], d_out["row_sumexp"], s_out[0], sd,
                          step.ws, v_out)
         evs[5].record(stream)
+        step.first_launch(sd)
+        evs[6].record(stream)
         torch.cuda.synchronize()
-        for j in range(5):
+        for j in range(6):
             acc[j] += evs[j].elapsed_time(evs[j + 1])
-    breakdown = {k: acc[j] / n_bd for j, k in enumerate(("draft_ms", "confidence_ms", "schedule_ms",
-                                                          "confidence_schedule_ms", "verify_ms"))}
+    breakdown = {k: acc[j] / n_bd for j, k in enumerate(
+        ("draft_ms", "confidence_ms", "schedule_ms", "confidence_schedule_ms", "verify_ms",
+         "draft_confidence_schedule_ms"))}
 
     # ---- end to end through the public API with pinned host buffers
     hin, hout = step.pinned_host_buffers()
@@ -516,8 +537,8 @@ def run_ours(args, w):
         return 0
 
     peak, peak_kind = _peaks()
-    dbytes = draft_bytes(w)
-    achieved = dbytes / (draft_ms * 1e-3) / 1e9
+    fbytes, dbytes = first_launch_bytes(w), draft_bytes(w)
+    achieved = fbytes / (first_ms * 1e-3) / 1e9
     sbytes = step_bytes(w, res["n_out"], res["accept_len"], res["ell"])
     line = {
         "metric": METRIC,
@@ -532,10 +553,12 @@ def run_ours(args, w):
                           ((w.B * w.gamma * w.V + w.B * (w.gamma + 1) * w.V) * 4 / 1e6),
                        parallelism=f"replicas x{world}",
                        launch="cuda graph ring of 8 seeds" if args.graph else "eager"),
-        "roofline": {"bound": "hbm", "kernel": "draft_lanes_kernel via dspark_draft_packed (bias contraction + sampling, all gamma positions)",
+        "roofline": {"bound": "hbm", "kernel": FIRST_KERNEL,
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _draft_traffic(w),
-                     "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
+                     "algorithmic_bytes_per_launch": fbytes, "ms_per_launch": first_ms,
+                     "draft_alone": {"ms_per_launch": draft_ms, "algorithmic_bytes": dbytes,
+                                     "achieved": dbytes / (draft_ms * 1e-3) / 1e9}},
         "step_hbm": {"algorithmic_bytes": sbytes, "achieved": sbytes / (ms_per_step * 1e-3) / 1e9,
                      "unit": "GB/s", "frac": sbytes / (ms_per_step * 1e-3) / 1e9 / peak},
         "accept": {"mean_ell": float(np.mean(res["ell"])), "mean_accept_len": float(np.mean(res["accept_len"])),

@@ -379,6 +379,32 @@ dspark_status dspark_verify_rnn(const float* T, const float* U, const float* E, 
 dspark_status dspark_last_device_status(void* workspace, cudaStream_t stream);
 
 /*
+ * One launch for the first three calls of a step: dspark_draft_packed, then
+ * dspark_confidence_schedule on the drafted tokens.  The draft kernel computes the
+ * confidence head and survival of position k (weigao.cc DSpark-vs-MTP page, "3.
+ * confidence head"; billytse.dev DSpark page, section 5) in a warp of its own, the h_k part
+ * while position k - 1 is drawn and the rest once x_{k-1} is known; when B * gamma <= 384 it
+ * runs the prefix scheduler
+ * (billytse.dev sections 6 and 7) in one CTA after the last position; larger batches get the
+ * scheduler kernel as a second launch.  Outputs and their meaning are those of the three
+ * calls (tokens, q_tok, row_max, row_sumexp; c, a; ell, B_total, theta); the draft's
+ * outputs are identical to dspark_draft_packed's, c and a agree with dspark_confidence's to
+ * fp32 rounding (another summation order), and ell, B_total, theta are the scheduler's
+ * on this a.  W2p is the packed W2 of dspark_pack_w2; h, w_c, b_c, sps as in
+ * dspark_confidence_schedule.  The workspace is one of dspark_workspace_bytes(B, gamma, V,
+ * r, H).  Requires B * gamma <= 16384; DSPARK_ERR_UNSUPPORTED also when the vocabulary is
+ * so small that the draft grid keeps no survival slot for some request (B > 512 x the
+ * draft grid, the smaller of the number of 128-column vocabulary tiles and the number of
+ * CTAs the device holds at once).
+ */
+dspark_status dspark_draft_confidence_schedule(
+    const float* U, const uint16_t* W1, const uint16_t* W2p, const int32_t* anchor, const float* h,
+    const float* w_c, float b_c, const float* sps, int sps_len, int B, int gamma, int V, int r, int H,
+    uint64_t seed, int32_t* tokens, float* q_tok, float* row_max, float* row_sumexp, float* c,
+    float* a, int32_t* ell, int32_t* B_total, double* theta, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Testing hook for the failure path of the draft (no passage of the pages: the bounded
  * waits are this library's own failure detection).  Every wait inside the draft kernel of
  * dspark_draft, dspark_draft_packed, dspark_draft_greedy and dspark_draft_noalloc is

@@ -54,6 +54,8 @@ SIGNATURES = [
     ("dspark_verify_rnn", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _U64, _P, _P,
                                _P, _P, _SZ, _P]),
     ("dspark_last_device_status", _I, [_P, _P]),
+    ("dspark_draft_confidence_schedule", _I, [_P, _P, _P, _P, _P, _P, _F, _P, _I, _I, _I, _I, _I, _I,
+                                              _U64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_testing_set_wait_limit", None, [ctypes.c_longlong, _I]),
 ]
 
@@ -236,6 +238,35 @@ def confidence_schedule(h, anchor, tokens, W1, w_c, b_c: float, sps, ws: Workspa
         H, r, V, _ptr(sps), sps.numel(), _ptr(c), _ptr(a), _ptr(ell), _ptr(Bt), _ptr(th),
         ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
     return (c, a), (ell, Bt, th)
+
+
+def draft_confidence_schedule(U, W1, W2p, anchor, h, w_c, b_c: float, sps, seed: int, ws: Workspace,
+                              draft_out: Optional[Dict] = None, conf_out=None, sched_out=None,
+                              stream=None):
+    """draft (packed W2), confidence, survival and schedule in one launch (two when
+    B * gamma > 384: the scheduler kernel follows)."""
+    torch = _torch()
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    H = h.shape[2]
+    if draft_out is None:
+        draft_out = _draft_outputs(B, gamma, U.device)
+    if conf_out is None:
+        conf_out = (torch.empty((B, gamma), dtype=torch.float32, device=U.device),
+                    torch.empty((B, gamma), dtype=torch.float32, device=U.device))
+    if sched_out is None:
+        sched_out = (torch.empty(B, dtype=torch.int32, device=U.device),
+                     torch.empty(1, dtype=torch.int32, device=U.device),
+                     torch.empty(1, dtype=torch.float64, device=U.device))
+    c, a = conf_out
+    ell, Bt, th = sched_out
+    _check("dspark_draft_confidence_schedule", lib().dspark_draft_confidence_schedule(
+        _ptr(U), _ptr(W1), _ptr(W2p), _ptr(anchor), _ptr(h), _ptr(w_c), ctypes.c_float(b_c),
+        _ptr(sps), sps.numel(), B, gamma, V, r, H, ctypes.c_uint64(seed),
+        _ptr(draft_out["tokens"]), _ptr(draft_out["q_tok"]), _ptr(draft_out["row_max"]),
+        _ptr(draft_out["row_sumexp"]), _ptr(c), _ptr(a), _ptr(ell), _ptr(Bt), _ptr(th),
+        ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
+    return draft_out, (c, a), (ell, Bt, th)
 
 
 def schedule(a, sps, ws: Workspace, out=None, stream=None):
@@ -448,7 +479,9 @@ class Step:
     as point-mass proposals).  ``head``: "markov" or "rnn" (``dev`` then also holds W_rnn
     and b_rnn; each step first projects the hidden states).  ``scheduler``: "theta" (the early-stop scheduler), "async"
     (the two-step capacity scheduler; ``run(seed, t=...)`` picks the ring slot of step t)
-    or "threshold" (fixed truncation at ``threshold``)."""
+    or "threshold" (fixed truncation at ``threshold``).  ``fused``: the default step
+    (Gumbel, Markov head, early-stop scheduler, packed W2) drafts, scores confidence and
+    schedules in one launch (``draft_confidence_schedule``); False runs the calls one by one."""
 
     SAMPLING = ("gumbel", "greedy")
     HEADS = ("markov", "rnn")
@@ -456,7 +489,7 @@ class Step:
 
     def __init__(self, dev: Dict, b_c: float, ws: Optional[Workspace] = None, packed: bool = True,
                  sampling: str = "gumbel", scheduler: str = "theta", threshold: float = 0.5,
-                 W2p=None, head: str = "markov"):
+                 W2p=None, head: str = "markov", fused: bool = True):
         torch = _torch()
         if sampling not in self.SAMPLING or scheduler not in self.SCHEDULERS or head not in self.HEADS:
             raise ValueError(f"sampling {sampling!r} / scheduler {scheduler!r} / head {head!r}")
@@ -486,6 +519,10 @@ class Step:
                                out_tokens=torch.empty((B, gamma + 1), dtype=i32, device=d),
                                n_out=torch.empty(B, dtype=i32, device=d))
         self.ring = CapacityRing(d) if scheduler == "async" else None
+        # the default step (Gumbel drafts, the Markov head, the early-stop scheduler, packed
+        # W2) drafts, scores confidence and schedules in one launch
+        self.fused = (fused and sampling == "gumbel" and head == "markov" and scheduler == "theta"
+                      and self.W2p is not None and B * gamma <= 16384)
         if head == "rnn":
             self.Wrec = rnn_pack(dev["W_rnn"], r)
             self.hp = torch.empty((B, gamma, 3 * r), dtype=f32, device=d)
@@ -493,8 +530,14 @@ class Step:
 
     def run(self, seed: int, stream=None, t: int = 0):
         x = self.dev
+        B, gamma = x["U"].shape[:2]
+        if self.fused:
+            # draft, confidence, survival and schedule in one launch, then verification
+            d, (ell, _, _) = self.first_launch(seed, stream)
+            verify_packed(x["T"], x["U"], x["W1"], self.W2p, x["anchor"], d["tokens"], d["q_tok"],
+                          d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
+            return self
         d = self.draft(seed, stream)
-        B, gamma = d["tokens"].shape
         if self.scheduler == "theta" and B * gamma <= 16384:
             # the early-stop scheduler runs in the confidence kernel's last CTA
             _, (ell, _, _) = confidence_schedule(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"],
@@ -518,6 +561,14 @@ class Step:
             verify(x["T"], x["U"], x["W1"], x["W2"], x["anchor"], d["tokens"], d["q_tok"],
                    d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
         return self
+
+    def first_launch(self, seed: int, stream=None):
+        """The fused step's first launch alone: draft, confidence and schedule."""
+        x = self.dev
+        d, _, sched = draft_confidence_schedule(
+            x["U"], x["W1"], self.W2p, x["anchor"], x["h"], x["w_c"], self.b_c, x["sps"], seed,
+            self.ws, self.draft_out, self.conf_out, self.sched_out, stream)
+        return d, sched
 
     def draft(self, seed: int, stream=None):
         """The draft call of the step alone (into the step's draft outputs)."""
@@ -547,16 +598,21 @@ class Step:
             ell, _, _ = schedule(a, self.dev["sps"], self.ws, self.sched_out, stream)
         return ell
 
-    def capture(self, seeds, draft_only: bool = False):
-        """CUDA graphs of run(seed) (or of the draft call alone), one per seed.  The seed
-        is a launch argument, so each graph replays with its own random stream.  With the
-        two-step scheduler, graph i uses capacity slot i % 2."""
+    def capture(self, seeds, draft_only: bool = False, first_only: bool = False):
+        """CUDA graphs of run(seed) (or of the draft call alone, or of the fused step's
+        first launch alone), one per seed.  The seed is a launch argument, so each graph
+        replays with its own random stream.  With the two-step scheduler, graph i uses
+        capacity slot i % 2."""
         torch = _torch()
+        if first_only and not self.fused:
+            raise ValueError("first_only needs the fused step")
         graphs = []
         for i, sd in enumerate(seeds):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                if draft_only:
+                if first_only:
+                    self.first_launch(sd)
+                elif draft_only:
                     self.draft(sd)
                 else:
                     self.run(sd, t=i)

@@ -121,6 +121,40 @@ dspark_status dspark_confidence_schedule(const float* h, const int32_t* anchor,
   return DSPARK_OK;
 }
 
+dspark_status dspark_draft_confidence_schedule(
+    const float* U, const uint16_t* W1, const uint16_t* W2p, const int32_t* anchor, const float* h,
+    const float* w_c, float b_c, const float* sps, int sps_len, int B, int gamma, int V, int r, int H,
+    uint64_t seed, int32_t* tokens, float* q_tok, float* row_max, float* row_sumexp, float* c,
+    float* a, int32_t* ell, int32_t* B_total, double* theta, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream) {
+  dspark_status st = check_shape(B, gamma, V, r, H);
+  if (st != DSPARK_OK) return st;
+  if ((long long)B * gamma > kMaxScheduleItems) return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)sps_len < (long long)B * (gamma + 1) + 1) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2p, 16) || !aligned(anchor, 4) ||
+      !aligned(h, 16) || !aligned(w_c, 16) || !aligned(sps, 4) || !aligned(tokens, 4) ||
+      !aligned(q_tok, 4) || !aligned(row_max, 4) || !aligned(row_sumexp, 4) || !aligned(c, 4) ||
+      !aligned(a, 4) || !aligned(ell, 4) || !aligned(B_total, 4) || !aligned(theta, 8))
+    return DSPARK_ERR_INVALID_ARG;
+  const Plan p = make_plan(B, gamma, V, r, H);
+  if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
+  DraftStepArgs step;
+  step.h = h; step.w_c = w_c; step.b_c = b_c; step.H = H; step.c = c; step.a = a;
+  step.sps = sps; step.ell = ell; step.B_total = B_total; step.theta = theta;
+  int* err = ws_at<int>(workspace, p.off_err);
+  const cudaError_t e = launch_draft_lanes(W1, nullptr, W2p, U, anchor, B, gamma, V, r, seed,
+                                           false, tokens, q_tok, row_max, row_sumexp,
+                                           ws_at<char>(workspace, p.off_draft), err, stream, &step);
+  if (e == cudaErrorNotSupported) return DSPARK_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  // batches beyond the draft's in-kernel scheduler: the scheduler kernel follows
+  if ((long long)B * gamma > draft_fused_schedule_limit() &&
+      launch_schedule(a, B, gamma, sps, nullptr, nullptr, ell, B_total, theta, err, stream) !=
+          cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
 dspark_status dspark_schedule(const float* a, int R, int gamma, const float* sps, int sps_len,
                               int32_t* ell, int32_t* B_total, double* theta, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream) {

@@ -19,13 +19,13 @@
 //   B  the W2 tile, streamed through a shared-memory ring as the packed images of pack.cu
 //      (MN-major, 128-byte swizzle), or as two TMA boxes per stage from W2 itself.
 // A request's accumulator row is one tensor-memory lane with the vocabulary along the
-// columns, so a sampler thread owns one request and a run of 8, 16 or 32 columns of every
-// tile: one tcgen05.ld brings the bias, the U tile comes from a TMA ring (128-byte
+// columns, so a sampler thread owns one request and a run of 16, 32 or 64 columns of every
+// tile: tcgen05.ld brings the bias, the U tile comes from a TMA ring (128-byte
 // swizzle, so that the threads of a warp, 32 requests, read it without bank conflicts),
 // and the request's softmax sums and Gumbel race stay in the thread's registers.
 //
-// Roles (19 warps): warps 0..15 sample (warp w reads the lanes of quadrant w % 4), warp 16
-// lane 0 streams W2 stages, warp 17 lane 0 streams U tiles (TMA), warp 18 allocates tensor
+// Roles (12 warps): warps 0..7 sample (warp w reads the lanes of quadrant w % 4), warp 8
+// lane 0 streams W2 stages, warp 9 lane 0 streams U tiles (TMA), warp 11 allocates tensor
 // memory and its lane 0 issues the MMAs.  The producers do not depend on the drafted
 // tokens and run ahead across positions.
 //
@@ -46,8 +46,8 @@
 // into a 64-bit atomic max key.  One grid barrier per position (a release reduction per
 // CTA, one bounded poller) makes x_k known everywhere; the samplers then gather the next
 // position's E rows into the other A buffer with tcgen05.st.  The CTA with index b mod G
-// merges the G partials of request b into x_k, q_k(x_k), max and sum after its arrival at
-// the next barrier.
+// then merges the G partials of request b into x_k, q_k(x_k), max and sum while the tensor
+// core computes the next position's first tile.
 //
 // Failure handling: every wait is bounded (LParams::wait_cycles SM cycles).  A wait that
 // runs out records DSPARK_ERR_TIMEOUT and sets a CTA-wide abort flag; from then on the
@@ -57,6 +57,7 @@
 #include <string.h>
 
 #include "internal.h"
+#include "schedule_block.cuh"
 #include "sm100_ptx.cuh"
 
 namespace dspark {
@@ -64,14 +65,20 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kSamplers = 16;         // warps 0..15; sampler w sits in quadrant w % 4
-constexpr int kWProducerWarp = 16;
-constexpr int kUProducerWarp = 17;
-constexpr int kMmaWarp = 18;
-constexpr int kWarps = 19;
+// Eight sampler warps (two per sub-partition, so that the MMA lane's sub-partition has
+// issue slots to spare) that each take 2, 4 or 8 octets of a tile: warps 0..7, sampler w
+// sits in quadrant w % 4; warp 8 streams W2, warp 9 streams U, warp 11 (the sub-partition
+// of samplers 3 and 7) issues the MMAs; warp 10 scores the confidence head.
+constexpr int kSamplers = 8;
+constexpr int kWProducerWarp = 8;
+constexpr int kUProducerWarp = 9;
+constexpr int kConfWarp = 10;
+constexpr int kMmaWarp = 11;
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSamplerThreads = kSamplers * 32;
 constexpr int kBarSamplers = 1;       // named barrier of the sampler threads
+constexpr int kConfSlots = 512;       // requests per CTA whose survival it keeps
 constexpr uint32_t kTmemCols = 512;   // A buffers at columns 0 and 128, accumulators at 256, 384
 constexpr uint32_t kAccCol = 256;
 constexpr int kTileN = 128;           // vocabulary columns per tile (MMA N)
@@ -85,7 +92,9 @@ constexpr float kShrink = 1.f - 0x1.0p-16f;  // filter slack, well above fp32 ro
 template <int NBJ>
 struct LSmem {
   static constexpr int kCopies = 128 / NBJ;          // replicas of the chunk down the lanes
-  static constexpr int kCols = NBJ / 4;              // columns of a tile per sampler thread
+  // columns of a tile per sampler thread: 128 over the kSamplers / 4 * kCopies warps
+  // that hold the same rows
+  static constexpr int kCols = 4 * NBJ / kSamplers;
   static constexpr int kOct = kCols / 8;             // octets per tile per sampler thread
   static constexpr int kWStages = NBJ == 32 ? 8 : NBJ == 64 ? 6 : 4;
   static constexpr int kUStages = NBJ == 32 ? 4 : NBJ == 64 ? 3 : 2;
@@ -115,6 +124,19 @@ struct LParams {
   int* err;
   long long wait_cycles;           // bound of every wait
   unsigned int grid_extra;         // added to every grid-barrier target (0; tests: unreachable)
+  // the confidence head and survival, computed by the confidence warp (c_out null: not
+  // computed here)
+  const float* h;                  // [B][gamma][H]
+  const float* w_c;                // [H + r]
+  float b_c;
+  int H;
+  float* c_out;                    // [B][gamma]
+  float* a_out;                    // [B][gamma]
+  // the prefix scheduler, run by CTA 0 after the last position (ell null: not run here)
+  const float* sps;
+  int32_t* ell;
+  int32_t* B_total;
+  double* theta;
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -233,6 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
+  __shared__ float surv_s[kConfSlots];   // a_{k-1} of this CTA's requests
+  __shared__ float hdot_s[kConfSlots];   // h_k . w_c[0:H] of the same
+  __shared__ int conf_done_s;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -260,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     }
     mbar_init(&mma_drain, 1);
     abort_s = 0;
+    conf_done_s = 0;
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < NBJ; i += kThreads) thr[i] = 0ull;   // below every tagged key
@@ -360,8 +386,30 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     // -------------------------------------------------------------------- MMA issuer
     // The K steps of one W2 stage are a compile-time count (1, 2 or 4); descriptors are
     // built once and advanced by adding (byte offset >> 4) to their start-address field.
-    auto issue_loop = [&](auto ksteps_c) {
+    // The issuing lane shares its sub-partition with four busy sampler warps, so every
+    // instruction of this loop costs several issue slots: a tile's MMAs are unrolled with
+    // compile-time K steps per stage (KS) and stages per tile (NKC, 0: a runtime count),
+    // descriptors are advanced by adds to their start-address field (every operand lies
+    // below 256 KB, so the sum never carries into the stride fields), and the waits spin
+    // on test_wait (one spinning lane costs the others nothing) instead of suspending.
+    auto spin_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (mbar_test_wait(bar, parity)) return true;
+      const long long t0 = sm_cycles();
+      for (;;) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*(volatile int*)&abort_s) return false;
+        if (sm_cycles() - t0 > p.wait_cycles) {
+          set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+          atomicExch(&abort_s, 1);
+          return false;
+        }
+      }
+    };
+    auto issue_loop = [&](auto ksteps_c, auto nkc_c) {
       constexpr int KS = decltype(ksteps_c)::value;
+      constexpr int NKC = decltype(nkc_c)::value;
+      constexpr int WS = S::kWStages;
+      const int nkc = NKC > 0 ? NKC : n_kchunks;
       const uint32_t idesc = idesc_bf16_f32(128, kTileN, 0, 1);
       const uint64_t b_base = smem_desc(smem_u32(smem + S::kOffW), (uint32_t)KS * 2048u, 1024u,
                                         kSwizzle128B);
@@ -374,22 +422,29 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
         const uint32_t a_t = tmem_base + (uint32_t)(128 * ab);
         for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
           const int acc = tc & 1;
-          if (!(ok = wait1(&acc_empty[acc], ((tc >> 1) & 1) ^ 1))) break;
+          if (!(ok = spin_wait(&acc_empty[acc], ((tc >> 1) & 1) ^ 1))) break;
           tc_fence_after_sync();
           const uint32_t d_t = tmem_base + kAccCol + (uint32_t)(kTileN * acc);
-          for (int i = 0; i < n_kchunks; ++i, ++ws) {
-            const int s = ws % S::kWStages;
-            if (!(ok = wait1(&w_full[s], (ws / S::kWStages) & 1))) break;
-            const uint64_t b_s = b_base + (uint64_t)((s * kWStageBytes) >> 4);
+          auto chunk = [&](int i) {
+            uint32_t st = ws % WS;
+            const uint32_t par = (ws / WS) & 1u;
+            ++ws;
+            if (!ok || !(ok = spin_wait(&w_full[st], par))) return;
+            // K step g of A is columns 8g .. 8g + 7; 16 K rows of the MN-major stage are
+            // 2048 bytes apart
+            const uint64_t b_s = b_base + (uint64_t)(st * (kWStageBytes >> 4));
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-              // 16 K rows of the MN-major stage are 2048 bytes apart; K step g of A is
-              // columns 8g .. 8g + 7
-              const uint32_t g = (uint32_t)(i * KS + kk);
-              umma_ts_bf16_f32(d_t, a_t + 8u * g, b_s + (uint64_t)(kk * (2048 >> 4)), idesc,
+            for (int kk = 0; kk < KS; ++kk)
+              umma_ts_bf16_f32(d_t, a_t + 8u * (uint32_t)(i * KS + kk),
+                               b_s + (uint64_t)(kk * (2048 >> 4)), idesc,
                                (i > 0 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(&w_empty[s]);
+            umma_commit(&w_empty[st]);
+          };
+          if constexpr (NKC > 0) {
+#pragma unroll
+            for (int i = 0; i < NKC; ++i) chunk(i);
+          } else {
+            for (int i = 0; i < nkc; ++i) chunk(i);
           }
           if (!ok) break;
           umma_commit(&acc_full[acc]);
@@ -398,21 +453,122 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       }
     };
     if (lane == 0) {
-      if (kc == 64) issue_loop(std::integral_constant<int, 4>{});
-      else if (kc == 32) issue_loop(std::integral_constant<int, 2>{});
-      else issue_loop(std::integral_constant<int, 1>{});
+      using std::integral_constant;
+      if (kc == 64 && n_kchunks == 4) issue_loop(integral_constant<int, 4>{}, integral_constant<int, 4>{});
+      else if (kc == 64 && n_kchunks == 2) issue_loop(integral_constant<int, 4>{}, integral_constant<int, 2>{});
+      else if (kc == 64 && n_kchunks == 1) issue_loop(integral_constant<int, 4>{}, integral_constant<int, 1>{});
+      else if (kc == 64) issue_loop(integral_constant<int, 4>{}, integral_constant<int, 0>{});
+      else if (kc == 32) issue_loop(integral_constant<int, 2>{}, integral_constant<int, 0>{});
+      else issue_loop(integral_constant<int, 1>{}, integral_constant<int, 0>{});
       // every issued MMA completes before tensor memory is released
       umma_commit(&mma_drain);
       mbar_wait(&mma_drain, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp == kConfWarp) {
+    // ---------------------------------------------------------------- confidence head
+    // Position k of this CTA's requests b = cta + i G (slot i): weigao.cc DSpark-vs-MTP
+    // page, "3. confidence head" (one linear layer on [h_k ; W1[x_{k-1}]], a sigmoid) and
+    // billytse.dev section 5 (a_k = a_{k-1} c_k, multiplied left to right).  The h_k part
+    // of the logit needs no draft: it is summed while the samplers draw position k - 1;
+    // the W1[x_{k-1}] part follows once every CTA has published position k - 1.  One warp
+    // per request, lanes across the features.
+    if (p.c_out) {
+      const int H4 = p.H >> 2;
+      const float4* wv = reinterpret_cast<const float4*>(p.w_c);
+      bool ok = true;
+      for (int k = 1; k <= p.gamma && ok; ++k) {
+        int i = 0;
+        for (int bb = cta; bb < p.B; bb += G, ++i) {
+          const float4* hv = reinterpret_cast<const float4*>(p.h + ((size_t)bb * p.gamma + (k - 1)) * p.H);
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int q0 = lane; q0 < H4; q0 += 128) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int q = q0 + 32 * j;
+              if (q < H4) {
+                const float4 x = __ldcs(hv + q), w = __ldg(wv + q);
+                acc[j] = fmaf(x.x, w.x, acc[j]);
+                acc[j] = fmaf(x.y, w.y, acc[j]);
+                acc[j] = fmaf(x.z, w.z, acc[j]);
+                acc[j] = fmaf(x.w, w.w, acc[j]);
+              }
+            }
+          }
+          float d = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1) d += __shfl_xor_sync(0xffffffffu, d, m);
+          if (lane == 0) hdot_s[i] = d;
+        }
+        if (k >= 2) {
+          // x_{k-1} is final once every CTA has arrived for position k - 1 (a bounded,
+          // sleeping poll: this warp is off the samplers' critical path)
+          if (lane == 0) {
+            const unsigned int target = (unsigned int)G * (unsigned int)(k - 1) + p.grid_extra;
+            const long long t0 = sm_cycles();
+            while (ld_acquire_u32(p.grid_count) < target) {
+              if (*(volatile int*)&abort_s) { ok = false; break; }
+              if (sm_cycles() - t0 > p.wait_cycles) {
+                set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+                atomicExch(&abort_s, 1);
+                ok = false;
+                break;
+              }
+              __nanosleep(256);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+        i = 0;
+        for (int bb = cta; bb < p.B; bb += G, ++i) {
+          int prev = (k == 1) ? p.anchor[bb] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + bb));
+          if (!(prev >= 0 && prev < p.V)) {
+            if (lane == 0) set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
+            prev = 0;
+          }
+          const uint16_t* e = p.W1 + (size_t)prev * p.r;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int q = 8 * lane; q < p.r; q += 256) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(e + q));
+            const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.w_c + p.H + q));
+            const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.w_c + p.H + q + 4));
+            acc[0] = fmaf(__uint_as_float(u.x << 16), w0.x, acc[0]);
+            acc[1] = fmaf(__uint_as_float(u.x & 0xFFFF0000u), w0.y, acc[1]);
+            acc[2] = fmaf(__uint_as_float(u.y << 16), w0.z, acc[2]);
+            acc[3] = fmaf(__uint_as_float(u.y & 0xFFFF0000u), w0.w, acc[3]);
+            acc[0] = fmaf(__uint_as_float(u.z << 16), w1.x, acc[0]);
+            acc[1] = fmaf(__uint_as_float(u.z & 0xFFFF0000u), w1.y, acc[1]);
+            acc[2] = fmaf(__uint_as_float(u.w << 16), w1.z, acc[2]);
+            acc[3] = fmaf(__uint_as_float(u.w & 0xFFFF0000u), w1.w, acc[3]);
+          }
+          float d = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1) d += __shfl_xor_sync(0xffffffffu, d, m);
+          if (lane == 0) {
+            const float c = 1.f / (1.f + expf(-(hdot_s[i] + d + p.b_c)));
+            const float a = (k == 1 ? 1.f : surv_s[i]) * c;
+            surv_s[i] = a;
+            const size_t o = (size_t)bb * p.gamma + (k - 1);
+            p.c_out[o] = c;
+            p.a_out[o] = a;
+          }
+        }
+      }
+      // c and a are ordered before the flag the samplers wait for ahead of their last
+      // grid arrival
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) *(volatile int*)&conf_done_s = 1;
+    }
+  } else if (warp < kSamplers) {
     // ----------------------------------------------------------------------- samplers
     const int sw = warp;
     const int stid = threadIdx.x;
     const int quad = warp & 3;                                  // TMEM lane quadrant
     const int ml = (32 * quad + lane) % NBJ;                    // request row in the chunk
     // column run of this warp: the warps whose quadrants hold the same rows split a tile
+    // (kSamplers / 4 warps per quadrant, kCopies quadrants per row set)
     const int sidx = (sw >> 2) * S::kCopies + quad / (NBJ / 32);
     const int c0 = sidx * S::kCols;
     const uint32_t lane_base = tmem_base + ((uint32_t)(32 * quad) << 16);
@@ -459,25 +615,31 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
           prev = -1;
         }
       }
+      // the kSamplers / 4 warps of a quadrant split the row's r / 2 columns
+      constexpr int kPerQuad = kSamplers / 4;
       const int jq = sw >> 2;
-      const int ncol = p.r >> 3;                      // 32-bit columns per warp
+      const int ncol = (p.r >> 1) / kPerQuad;         // 32-bit columns per warp
       const uint32_t taddr = lane_base + (uint32_t)(128 * ab + jq * ncol);
-      const uint16_t* src = p.W1 + (size_t)(prev < 0 ? 0 : prev) * p.r + (size_t)jq * (p.r >> 2);
+      const uint16_t* src = p.W1 + (size_t)(prev < 0 ? 0 : prev) * p.r + (size_t)jq * (2 * ncol);
       if ((ncol & 7) == 0) {
-        // 8 columns = 16 bf16 = two 16-byte loads per store; the loads of two stores at a
-        // time in flight
-        const int n8 = ncol >> 3;                     // 1..4
+        // 8 columns = 16 bf16 = two 16-byte loads per store.  One chunk of at most 32
+        // requests is gathered on the critical path between positions: four stores' loads
+        // in flight at a time (two round trips for r = 256; all eight would spill the
+        // sampler's registers); chunks of 64 and 128 requests, whose next chunk is gathered
+        // while the current one is sampled, keep two stores' loads in flight
+        constexpr int kBatch = 2;
+        const int n8 = ncol >> 3;                     // 1..8
 #pragma unroll
-        for (int h = 0; h < 4; h += 2) {
-          uint4 v[4];
+        for (int h = 0; h < 8; h += kBatch) {
+          uint4 v[2 * kBatch];
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
+          for (int u = 0; u < kBatch; ++u)
             if (h + u < n8) {
               v[2 * u] = prev < 0 ? make_uint4(0u, 0u, 0u, 0u) : __ldg(reinterpret_cast<const uint4*>(src) + 2 * (h + u));
               v[2 * u + 1] = prev < 0 ? make_uint4(0u, 0u, 0u, 0u) : __ldg(reinterpret_cast<const uint4*>(src) + 2 * (h + u) + 1);
             }
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
+          for (int u = 0; u < kBatch; ++u)
             if (h + u < n8) {
               const uint32_t cols[8] = {v[2 * u].x, v[2 * u].y, v[2 * u].z, v[2 * u].w,
                                         v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
@@ -536,32 +698,37 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
               }
             }
           }
+          // octets in pairs (16 columns): one tensor-memory load, four independent Philox
+          // chains and one candidate mask per pair
 #pragma unroll 1
-          for (int o = 0; o < S::kOct; ++o) {
+          for (int o = 0; o < S::kOct; o += 2) {
             const int v = vt + 8 * o;
-            const int col = c0 + 8 * o;                 // a multiple of 8
-            uint32_t a8[8];
+            const int col = c0 + 8 * o;                 // a multiple of 16
+            uint32_t a16[16];
             __syncwarp();                               // a whole-warp load: every lane, converged
-            tmem_ld_32x32b_sync<8>(lane_base + kAccCol + (uint32_t)(kTileN * acc + col), a8);
+            tmem_ld_32x32b_sync<16>(lane_base + kAccCol + (uint32_t)(kTileN * acc + col), a16);
             if (!valid) continue;                       // a row beyond the batch
-            // U: box col / 32, row ml, 16-byte chunks (col % 32) / 4 and the next one,
-            // 128-byte swizzle (chunk ^ row % 8)
+            // U: box col / 32, row ml, 16-byte chunks (col % 32) / 4 .. + 3, 128-byte
+            // swizzle (chunk ^ row % 8)
             const uint8_t* row = us + (col >> 5) * (NBJ * 128) + u_row;
-            const int ch = (col & 31) >> 2;
-            const float4 u0 = *reinterpret_cast<const float4*>(row + ((ch ^ u_sw) << 4));
-            const float4 u1 = *reinterpret_cast<const float4*>(row + (((ch + 1) ^ u_sw) << 4));
-            float zo[8] = {__uint_as_float(a8[0]) + u0.x, __uint_as_float(a8[1]) + u0.y,
-                           __uint_as_float(a8[2]) + u0.z, __uint_as_float(a8[3]) + u0.w,
-                           __uint_as_float(a8[4]) + u1.x, __uint_as_float(a8[5]) + u1.y,
-                           __uint_as_float(a8[6]) + u1.z, __uint_as_float(a8[7]) + u1.w};
+            const int ch = (col & 31) >> 2;             // 0 or 4
+            float zo[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 u4 = *reinterpret_cast<const float4*>(row + (((ch + q) ^ u_sw) << 4));
+              zo[4 * q + 0] = __uint_as_float(a16[4 * q + 0]) + u4.x;
+              zo[4 * q + 1] = __uint_as_float(a16[4 * q + 1]) + u4.y;
+              zo[4 * q + 2] = __uint_as_float(a16[4 * q + 2]) + u4.z;
+              zo[4 * q + 3] = __uint_as_float(a16[4 * q + 3]) + u4.w;
+            }
             if (ragged) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
+              for (int j = 0; j < 16; ++j)
                 if (v + j >= p.V) zo[j] = -INFINITY;
             }
             float lm = zo[0];
 #pragma unroll
-            for (int j = 1; j < 8; ++j) lm = fmaxf(lm, zo[j]);
+            for (int j = 1; j < 16; ++j) lm = fmaxf(lm, zo[j]);
             if (lm == -INFINITY) continue;              // wholly beyond the vocabulary
             mx = fmaxf(mx, lm);
             if (lm > Mr + kLazy) {
@@ -572,52 +739,58 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
             const float mL = Mr * kLog2e;
             if constexpr (Greedy) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) ssum += ex2_approx(fmaf(zo[j], kLog2e, -mL));
+              for (int j = 0; j < 16; ++j) ssum += ex2_approx(fmaf(zo[j], kLog2e, -mL));
               if (lm > bsc) {                           // a later equal maximum has a larger v
-                int jl = 7;
+                int jl = 15;
 #pragma unroll
-                for (int j = 6; j >= 0; --j)
+                for (int j = 14; j >= 0; --j)
                   if (zo[j] == lm) jl = j;
                 bsc = lm; bz = lm; bi = v + jl;
               }
             } else {
-              const uint4 d0 = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 0u), k0, k1);
-              const uint4 d1 = philox_wide(make_uint4((uint32_t)(v >> 2) + 1u, (uint32_t)k, (uint32_t)b, 0u), k0, k1);
-              const uint32_t dw[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+              uint32_t dw[16];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 d = philox_wide(make_uint4((uint32_t)(v >> 2) + (uint32_t)q, (uint32_t)k,
+                                                       (uint32_t)b, 0u), k0, k1);
+                dw[4 * q + 0] = d.x; dw[4 * q + 1] = d.y; dw[4 * q + 2] = d.z; dw[4 * q + 3] = d.w;
+              }
               unsigned cm = 0u;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
+              for (int j = 0; j < 16; ++j) {
                 const float e = ex2_approx(fmaf(zo[j], kLog2e, -mL));
                 ssum += e;
                 cm |= (e > Tf * w_of_draw(dw[j]) ? 1u : 0u) << j;
               }
               if (cm) {
-                // candidates (rare past a job's first octet): recompute e and w, tighten
-                // with the best lower bound e (1 - w) / w <= e / E among them, keep the
-                // survivors of the tightened test, and score those exactly in increasing v
-                // (equal scores keep the smallest index).  The loop runs once per set bit of
-                // the lane's survivors, so a warp pays for its busiest lane only.
-                float ec[8], wc[8];
+                // candidates (rare past a job's first pair): recompute e and w, tighten with
+                // the best lower bound e (1 - w) / w <= e / E among them, keep the survivors
+                // of the tightened test, and score those exactly in increasing v (equal
+                // scores keep the smallest index).  The loop runs once per set bit of the
+                // lane's survivors, so a warp pays for its busiest lane only.
                 float L = 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  ec[j] = ex2_approx(fmaf(zo[j], kLog2e, -mL));
-                  wc[j] = w_of_draw(dw[j]);
-                  if ((cm >> j) & 1u) L = fmaxf(L, ec[j] * (1.f - wc[j]) * rcp_approx(wc[j]));
-                }
+                for (int j = 0; j < 16; ++j)
+                  if ((cm >> j) & 1u) {
+                    const float e = ex2_approx(fmaf(zo[j], kLog2e, -mL)), w = w_of_draw(dw[j]);
+                    L = fmaxf(L, e * (1.f - w) * rcp_approx(w));
+                  }
                 const float Teff = fmaxf(Tf, L * kShrink);
                 unsigned sm = 0u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) sm |= (((cm >> j) & 1u) && ec[j] > Teff * wc[j] ? 1u : 0u) << j;
+                for (int j = 0; j < 16; ++j)
+                  if ((cm >> j) & 1u)
+                    sm |= (ex2_approx(fmaf(zo[j], kLog2e, -mL)) > Teff * w_of_draw(dw[j]) ? 1u : 0u) << j;
                 bool improved = false;
                 while (sm) {
                   const int j = __ffs(sm) - 1;
                   sm &= sm - 1u;
-                  const float wj = j < 4 ? (j < 2 ? (j == 0 ? wc[0] : wc[1]) : (j == 2 ? wc[2] : wc[3]))
-                                         : (j < 6 ? (j == 4 ? wc[4] : wc[5]) : (j == 6 ? wc[6] : wc[7]));
-                  const float zj = j < 4 ? (j < 2 ? (j == 0 ? zo[0] : zo[1]) : (j == 2 ? zo[2] : zo[3]))
-                                         : (j < 6 ? (j == 4 ? zo[4] : zo[5]) : (j == 6 ? zo[6] : zo[7]));
-                  const float scj = zj - logf(exp1_from_w(wj));
+                  float zj = zo[0];
+                  uint32_t dj = dw[0];
+#pragma unroll
+                  for (int q = 1; q < 16; ++q)
+                    if (q == j) { zj = zo[q]; dj = dw[q]; }
+                  const float scj = zj - logf(exp1_from_w(w_of_draw(dj)));
                   if (scj > bsc) { bsc = scj; bi = v + j; bz = zj; improved = true; }
                 }
                 if (improved) {
@@ -641,8 +814,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
         }
       }
       // ---- this thread's partial, then a shuffle tree per request of the chunk: every
-      // request has E = 512 / NBJ partials (one per sampler warp holding its rows), and
-      // sampler thread t merges entry t % E of request t / E with its E - 1 neighbours
+      // request has E = kSamplerThreads / NBJ partials (one per sampler warp holding its
+      // rows), and sampler thread t merges entry t % E of request t / E with its E - 1
+      // neighbours
       {
         const float st = (Mr == -INFINITY || mx == -INFINITY) ? 0.f : ssum * ex2_approx((Mr - mx) * kLog2e);
         float* mw = merge + sw * kMergeStride + lane;
@@ -654,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       }
       named_bar_sync(kBarSamplers, kSamplerThreads);
       {
-        constexpr int E = kSamplerThreads / NBJ;       // 16, 8 or 4 consecutive lanes
+        constexpr int E = kSamplerThreads / NBJ;       // 8, 4 or 2 consecutive lanes
         const int mrow = stid / E, e = stid % E;
         const int src = (mrow >> 5) + (NBJ / 32) * e;  // the e-th warp holding row mrow
         const float* mr = merge + src * kMergeStride + (mrow & 31);
@@ -694,16 +868,31 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       // merge area is free again after it
       named_bar_sync(kBarSamplers, kSamplerThreads);
       if (c + 1 == p.n_chunks) {
-        if (stid == 0 && !*(volatile int*)&abort_s)
-          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.grid_count) : "memory");
-        // merge this CTA's share of position k - 1 while the other CTAs finish position k
-        // (slot (k - 1) % 3 is next written at position k + 2, after a barrier this CTA
-        // has not yet passed)
-        if (k > 1 && !*(volatile int*)&abort_s)
-          for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G) finalize_row<Greedy>(p, bb, k - 1, G, lane);
+        if (stid == 0 && !*(volatile int*)&abort_s) {
+          // the last arrival also carries this CTA's survivals: wait for the confidence warp
+          if (k == p.gamma && p.c_out) {
+            const long long t0 = sm_cycles();
+            while (!*(volatile int*)&conf_done_s) {
+              if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
+                set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+                atomicExch(&abort_s, 1);
+                break;
+              }
+            }
+            __threadfence();
+          }
+          if (!*(volatile int*)&abort_s)
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.grid_count) : "memory");
+        }
         if (job + 1 < n_jobs) {
           grid_wait((unsigned int)G * (unsigned int)k + p.grid_extra);
           gather(job + 1);
+          // every CTA has published position k: merge this CTA's share of it while the
+          // tensor core computes the next position's first tile (slot k % 3 is next
+          // written at position k + 3)
+          if (!*(volatile int*)&abort_s) {
+            for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G) finalize_row<Greedy>(p, bb, k, G, lane);
+          }
         }
       }
     }
@@ -716,6 +905,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
+  // The prefix scheduler over every request's survivals, by CTA 0 once the last position
+  // is done: every CTA wrote its survivals before its last grid arrival, which the
+  // samplers' final wait acquired and the barrier above passed on to every thread.  The
+  // W2 ring (its copies and MMAs drained) holds the keys.
+  if (p.ell && cta == 0 && !*(volatile int*)&abort_s) {
+    int Npad = 2;
+    while (Npad < p.B * p.gamma) Npad <<= 1;
+    schedule_block(p.a_out, p.B, p.gamma, Npad, p.sps, nullptr, nullptr, p.ell, p.B_total,
+                   p.theta, reinterpret_cast<unsigned long long*>(smem + S::kOffW));
+  }
 }
 
 // U [B, gamma, V] fp32 as a 3-D tensor {V, gamma, B}; a box is 32 vocabulary entries (128
@@ -796,11 +995,13 @@ size_t draft_region_bytes(int B, int gamma) {
 
 int draft_kchunk(int r) { return (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16; }
 
+int draft_fused_schedule_limit() { return kThreads; }
+
 cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
                                const float* U, const int32_t* anchor, int B, int gamma, int V,
                                int r, uint64_t seed, bool greedy, int32_t* tokens, float* q_tok,
                                float* row_max, float* row_sumexp, void* region, int* err,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const DraftStepArgs* step) {
   const int NBJ = B <= 32 ? 32 : B <= 64 ? 64 : 128;
   const int n_tiles = cdiv(V, kTileN);
   int grid = greedy ? grid_of<true>(NBJ) : grid_of<false>(NBJ);
@@ -830,6 +1031,15 @@ cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uin
   const long long wc = g_wait_cycles.load();
   p.wait_cycles = wc > 0 ? wc : kWaitCycles;
   p.grid_extra = g_grid_extra.load();
+  if (step) {
+    // survivals are kept for kConfSlots requests of every CTA
+    if ((long long)B > (long long)kConfSlots * grid) return cudaErrorNotSupported;
+    p.h = step->h; p.w_c = step->w_c; p.b_c = step->b_c; p.H = step->H;
+    p.c_out = step->c; p.a_out = step->a;
+    if (step->ell && (long long)B * gamma <= kThreads) {
+      p.sps = step->sps; p.ell = step->ell; p.B_total = step->B_total; p.theta = step->theta;
+    }
+  }
   cudaError_t e = cudaMemsetAsync(base + part_bytes, 0,
                                   256 + (size_t)gamma * B * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;

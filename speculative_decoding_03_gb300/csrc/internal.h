@@ -161,11 +161,27 @@ cudaError_t launch_bias_gemm_rows(const uint16_t* W2, const uint16_t* W2p, const
 // the whole draft (all gamma positions) in one cooperative launch of the request-major
 // kernel of draft.cu (W2p: packed tile images, else W2 by TMA; greedy: x = argmax z);
 // `region` holds draft_region_bytes(B, gamma) of workspace
+// with `step` (may be null) the same launch also computes the confidence head and the
+// survivals at every position boundary, and, when B * gamma <= draft_fused_schedule_limit(),
+// runs the prefix scheduler in its CTA 0 after the last position
+struct DraftStepArgs {
+  const float* h;      // [B][gamma][H]
+  const float* w_c;    // [H + r]
+  float b_c;
+  int H;
+  float* c;            // [B][gamma]
+  float* a;            // [B][gamma]
+  const float* sps;    // the scheduler (ell null: not run in the draft)
+  int32_t* ell;
+  int32_t* B_total;
+  double* theta;
+};
+int draft_fused_schedule_limit();
 cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
                                const float* U, const int32_t* anchor, int B, int gamma, int V,
                                int r, uint64_t seed, bool greedy, int32_t* tokens, float* q_tok,
                                float* row_max, float* row_sumexp, void* region, int* err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const DraftStepArgs* step = nullptr);
 // bound (SM cycles, 0: the default of about 2 s) of that kernel's waits and an offset added
 // to its grid-barrier targets, for the launches that follow (tests of the timeout path)
 void set_draft_wait_limit(long long cycles, unsigned int grid_extra);

@@ -219,8 +219,9 @@ def test_full_size_every_request(name):
     configuration (packed W2, the scheduler in the confidence kernel's last CTA, the packed
     verification), against the oracle on every request.  Each call gets the oracle's
     upstream outputs; the tie-band cases of the whole batch are counted and held below
-    1e-4 of its positions.  The captured step (what the benchmark replays) must then give
-    the per-call results wherever its inputs coincide with them."""
+    1e-4 of its positions.  The captured step (what the benchmark replays: the draft,
+    confidence and schedule in one launch, then the verification) must then give the
+    per-call results wherever its inputs coincide with them."""
     _need_gpu()
     w = workloads.get(name)
     inp = workloads.generate(w)
@@ -277,9 +278,12 @@ def test_full_size_every_request(name):
     for key in ("q_tok", "row_max", "row_sumexp"):
         np.testing.assert_array_equal(st[key], gd[key], err_msg=key)
     if diverged == 0:
-        np.testing.assert_array_equal(st["c"], c.cpu().numpy())
-        np.testing.assert_array_equal(st["a"], a.cpu().numpy())
-        np.testing.assert_array_equal(st["ell"], ell.cpu().numpy())
+        # the step computes confidence inside the draft launch (another summation order)
+        np.testing.assert_allclose(st["c"], c_ref, rtol=RTOL)
+        np.testing.assert_allclose(st["a"], a_ref, rtol=RTOL)
+        ell_st, Bt_st, th_st = ds.schedule(torch.from_numpy(st["a"]).cuda(), dev["sps"], ws)
+        np.testing.assert_array_equal(st["ell"], ell_st.cpu().numpy())
+        assert st["B_total"] == int(Bt_st.item())
         if np.array_equal(st["ell"], ell_ref):
             # the step verifies with its own fp32 draft statistics: the oracle's outcomes
             # outside the tie band
@@ -374,6 +378,43 @@ def test_confidence_schedule_fused_matches_the_two_calls(name):
         assert int(Bt1.item()) == int(Bt2.item()) and float(th1.item()) == float(th2.item())
     ell_r, Bt_r, th_r = oracle.schedule(a2.cpu().numpy(), inp.sps)
     np.testing.assert_array_equal(ell2.cpu().numpy(), ell_r)
+    assert ws.status() == 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_draft_confidence_schedule_in_one_launch(name):
+    """The fused first three calls: the draft identical to dspark_draft_packed's, the
+    confidence and survival of the drafted tokens within the tolerance of the confidence
+    call (and of the oracle), the schedule that of the scheduler on the fused survivals."""
+    _need_gpu()
+    w = CASES[name]
+    if w.B * w.gamma > 16384:
+        pytest.skip("beyond the one-CTA scheduler")
+    inp = workloads.generate(w, with_T=False)
+    dev = _dev(inp)
+    ws = _ws(w)
+    W2p = ds.pack_w2(dev["W2"])
+    d1 = {k: t.cpu().numpy() for k, t in ds.draft_packed(dev["U"], dev["W1"], W2p, dev["anchor"],
+                                                          w.seed, ws).items()}
+    for _ in range(2):       # twice: nothing in the workspace carries over
+        d2, (c2, a2), (ell2, Bt2, th2) = ds.draft_confidence_schedule(
+            dev["U"], dev["W1"], W2p, dev["anchor"], dev["h"], dev["w_c"], float(inp.b_c), dev["sps"],
+            w.seed, ws)
+        for key in d1:
+            np.testing.assert_array_equal(d2[key].cpu().numpy(), d1[key], err_msg=key)
+        c1, a1 = ds.confidence(dev["h"], dev["anchor"], d2["tokens"], dev["W1"], dev["w_c"],
+                               float(inp.b_c), ws)
+        np.testing.assert_allclose(c2.cpu().numpy(), c1.cpu().numpy(), rtol=RTOL)
+        np.testing.assert_allclose(a2.cpu().numpy(), a1.cpu().numpy(), rtol=RTOL)
+        ell1, Bt1, th1 = ds.schedule(a2, dev["sps"], ws)
+        np.testing.assert_array_equal(ell2.cpu().numpy(), ell1.cpu().numpy())
+        assert int(Bt2.item()) == int(Bt1.item()) and float(th2.item()) == float(th1.item())
+    # against the oracle on its own chain (equal while no draft decision is in the band)
+    ref = oracle.draft(inp.U, inp.W1, inp.W2, inp.anchor, w.seed)
+    if draft_rows(d1["tokens"], ref["tokens"], ref["gap"], name)[0] == 0:
+        c_ref, a_ref = oracle.confidence(inp.h, inp.anchor, ref["tokens"], inp.W1, inp.w_c, float(inp.b_c))
+        np.testing.assert_allclose(c2.cpu().numpy(), c_ref, rtol=RTOL)
+        np.testing.assert_allclose(a2.cpu().numpy(), a_ref, rtol=RTOL)
     assert ws.status() == 0
 
 
