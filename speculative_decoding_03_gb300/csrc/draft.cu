@@ -22,30 +22,32 @@
 // columns, so a sampler thread owns one request and a run of 16, 32 or 64 columns of every
 // tile: tcgen05.ld brings the bias, the U tile comes from a TMA ring (128-byte
 // swizzle, so that the threads of a warp, 32 requests, read it without bank conflicts),
-// and the request's softmax sums and Gumbel race stay in the thread's registers.
+// and the request's softmax sums and Gumbel race stay in the thread's registers.  Tensor
+// memory holds one A buffer and three accumulators when a position is one job (up to 64
+// requests), two of each for 128-request chunks.
 //
 // Roles (12 warps): warps 0..7 sample (warp w reads the lanes of quadrant w % 4), warp 8
-// lane 0 streams W2 stages, warp 9 lane 0 streams U tiles (TMA), warp 11 allocates tensor
-// memory and its lane 0 issues the MMAs.  The producers do not depend on the drafted
-// tokens and run ahead across positions.
+// lane 0 streams W2 stages, warp 9 lane 0 streams U tiles (TMA), warp 10 scores the
+// confidence head (when asked), warp 11 allocates tensor memory and its lane 0 issues the
+// MMAs.  The producers do not depend on the drafted tokens and run ahead across positions.
 //
-// Sampler, per thread and octet of 8 columns: z = bias + U; running max; the softmax sum
-// against a lazy per-thread reference M (raised only when a logit exceeds it by more than
-// 32, so exp(z - M) cannot overflow); two Philox blocks give the 8 draws; with
+// Sampler, per thread and pair of octets (16 columns): z = bias + U; running max; the
+// softmax sum against a lazy per-thread reference M (raised only when a logit exceeds it by
+// more than 32, so exp(z - M) cannot overflow); four Philox blocks give the 16 draws; with
 // w = 1 - u (exact), w <= E = -log1p(-w) <= w / (1 - w), so exp(z - M) / w bounds an
 // element's ratio exp(z - M) / E from above and exp(z - M)(1 - w) / w from below: an
 // element is a candidate only if its upper bound beats exp(best - M), where best is the
 // best exact score any thread of the CTA has found for the request (a 64-bit shared-memory
-// atomic max, tagged with the job so that no reset is needed); among a thread's candidates
-// the best lower bound tightens the threshold further, and only the survivors evaluate the
-// exact score z - log E with log1p and log.
+// atomic max, tagged with the job so that no reset is needed); a thread with many
+// candidates tightens the threshold with their best lower bound, and only the survivors
+// evaluate the exact score z - log E with log1p and log.
 //
 // After its last tile of a job, every sampler thread leaves its partial (max, sum, best
-// score, index, logit) in shared memory; the first NBJ sampler threads merge the partials
-// of one request each, publish the CTA's partial and fold the CTA's best (score, index)
-// into a 64-bit atomic max key.  One grid barrier per position (a release reduction per
-// CTA, one bounded poller) makes x_k known everywhere; the samplers then gather the next
-// position's E rows into the other A buffer with tcgen05.st.  The CTA with index b mod G
+// score, index, logit) in shared memory; the sampler threads merge them with a shuffle tree
+// per request, publish the CTA's partial and fold the CTA's best (score, index) into a
+// 64-bit atomic max key.  One grid barrier per position (a release reduction per CTA, one
+// bounded poller) makes x_k known everywhere; the samplers then gather the next position's
+// E rows into an A buffer with tcgen05.st.  The CTA with index b mod G
 // then merges the G partials of request b into x_k, q_k(x_k), max and sum while the tensor
 // core computes the next position's first tile.
 //
@@ -79,8 +81,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kSamplerThreads = kSamplers * 32;
 constexpr int kBarSamplers = 1;       // named barrier of the sampler threads
 constexpr int kConfSlots = 512;       // requests per CTA whose survival it keeps
-constexpr uint32_t kTmemCols = 512;   // A buffers at columns 0 and 128, accumulators at 256, 384
-constexpr uint32_t kAccCol = 256;
+constexpr uint32_t kTmemCols = 512;   // 128-column A buffers, then 128-column accumulators
 constexpr int kTileN = 128;           // vocabulary columns per tile (MMA N)
 constexpr int kWStageBytes = 16384;   // one K-chunk of up to 64 rank rows of a W2 tile
 constexpr int kMergeStride = 5 * 32 + 1;    // words per sampler warp in the merge area (the pad
@@ -99,6 +100,13 @@ struct LSmem {
   static constexpr int kWStages = NBJ == 32 ? 8 : NBJ == 64 ? 6 : 4;
   static constexpr int kUStages = NBJ == 32 ? 4 : NBJ == 64 ? 3 : 2;
   static constexpr int kUStageBytes = NBJ * kTileN * 4;
+  // Tensor memory: up to 64 requests make one job per position, whose E rows are gathered
+  // only after the grid barrier (one A buffer; three accumulators keep the tensor core and
+  // the samplers apart); 128-request chunks gather the next chunk during the current one
+  // (two A buffers, two accumulators).
+  static constexpr int kABufs = NBJ == 128 ? 2 : 1;
+  static constexpr int kAccBufs = 4 - kABufs;
+  static constexpr uint32_t kAccCol = 128u * kABufs;
   static constexpr int kOffW = 0;
   static constexpr int kOffU = kOffW + kWStages * kWStageBytes;
   static constexpr int kOffMerge = kOffU + kUStages * kUStageBytes;   // [16 warps][5][32] + pad
@@ -250,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t w_full[S::kWStages], w_empty[S::kWStages];
   __shared__ uint64_t u_full[S::kUStages], u_empty[S::kUStages];
-  __shared__ uint64_t a_full[2], a_empty[2];
-  __shared__ uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint64_t a_full[S::kABufs], a_empty[S::kABufs];
+  __shared__ uint64_t acc_full[S::kAccBufs], acc_empty[S::kAccBufs];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -277,9 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       mbar_init(&u_full[i], 1);
       mbar_init(&u_empty[i], kSamplers);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < S::kABufs; ++i) {
       mbar_init(&a_full[i], kSamplers);
       mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < S::kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kSamplers);
     }
@@ -299,11 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   const uint32_t tmem_base = tmem_base_s;
   pdl_launch_dependents();
 
-  // One thread's bounded wait; a timeout aborts the CTA.  The abort flag is read only once
-  // the first (sleeping) try has not seen the phase complete, so the issue loops pay
-  // nothing for it.
+  // One thread's bounded wait; a timeout aborts the CTA.  A completed phase is seen by a
+  // non-blocking test; the abort flag is read only once the first (sleeping) try has not
+  // seen the phase complete, so the issue loops pay nothing for it.
   auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity) || mbar_try_wait_sleep(bar, parity)) return true;
     const long long t0 = sm_cycles();
     for (;;) {
       if (*(volatile int*)&abort_s) return false;
@@ -416,15 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       uint32_t ws = 0, tc = 0;
       bool ok = true;
       for (int job = 0; job < n_jobs && ok; ++job) {
-        const int ab = job & 1;
-        if (!(ok = wait1(&a_full[ab], (job >> 1) & 1))) break;
+        const int ab = job % S::kABufs;
+        if (!(ok = wait1(&a_full[ab], (job / S::kABufs) & 1))) break;
         tc_fence_after_sync();
         const uint32_t a_t = tmem_base + (uint32_t)(128 * ab);
         for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-          const int acc = tc & 1;
-          if (!(ok = spin_wait(&acc_empty[acc], ((tc >> 1) & 1) ^ 1))) break;
+          const int acc = tc % S::kAccBufs;
+          if (!(ok = spin_wait(&acc_empty[acc], ((tc / S::kAccBufs) & 1) ^ 1))) break;
           tc_fence_after_sync();
-          const uint32_t d_t = tmem_base + kAccCol + (uint32_t)(kTileN * acc);
+          const uint32_t d_t = tmem_base + S::kAccCol + (uint32_t)(kTileN * acc);
           auto chunk = [&](int i) {
             uint32_t st = ws % WS;
             const uint32_t par = (ws / WS) & 1u;
@@ -597,12 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       }
       named_bar_sync(kBarSamplers, kSamplerThreads);
     };
-    // E rows of job j into A buffer j & 1: this thread's lane holds row 32 quad + lane
+    // E rows of job j into A buffer j % kABufs: this thread's lane holds row 32 quad + lane
     // (request c NBJ + ml), this warp writes columns [jq r / 8, (jq + 1) r / 8) of it
     auto gather = [&](int j) {
       const int k = j / p.n_chunks + 1, c = j % p.n_chunks;
-      const int ab = j & 1;
-      if (j >= 2 && !swait(&a_empty[ab], ((j >> 1) & 1) ^ 1)) return;
+      const int ab = j % S::kABufs;
+      if (j >= S::kABufs && !swait(&a_empty[ab], ((j / S::kABufs) & 1) ^ 1)) return;
       // warp-uniform: the tensor-memory stores below are whole-warp instructions
       if (__any_sync(0xffffffffu, *(volatile int*)&abort_s != 0)) return;
       tc_fence_after_sync();
@@ -675,11 +685,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       float bsc = -INFINITY, bz = -INFINITY;
       int bi = -1;
       for (int t = 0; t < my_tiles; ++t, ++tc) {
-        const int acc = tc & 1;
+        const int acc = tc % S::kAccBufs;
         const int su = tc % S::kUStages;
-        // both stages are held until the tile is done (two accumulators and the U ring
-        // keep the tensor core and the copies a tile ahead)
-        const bool have = swait(&acc_full[acc], (tc >> 1) & 1) &&
+        // both stages are held until the tile is done (the other accumulators and the U
+        // ring keep the tensor core and the copies ahead)
+        const bool have = swait(&acc_full[acc], (tc / S::kAccBufs) & 1) &&
                           swait(&u_full[su], (tc / S::kUStages) & 1);
         if (have) {
           tc_fence_after_sync();
@@ -706,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
             const int col = c0 + 8 * o;                 // a multiple of 16
             uint32_t a16[16];
             __syncwarp();                               // a whole-warp load: every lane, converged
-            tmem_ld_32x32b_sync<16>(lane_base + kAccCol + (uint32_t)(kTileN * acc + col), a16);
+            tmem_ld_32x32b_sync<16>(lane_base + S::kAccCol + (uint32_t)(kTileN * acc + col), a16);
             if (!valid) continue;                       // a row beyond the batch
             // U: box col / 32, row ml, 16-byte chunks (col % 32) / 4 .. + 3, 128-byte
             // swizzle (chunk ^ row % 8)
@@ -763,33 +773,55 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
                 cm |= (e > Tf * w_of_draw(dw[j]) ? 1u : 0u) << j;
               }
               if (cm) {
-                // candidates (rare past a job's first pair): recompute e and w, tighten with
-                // the best lower bound e (1 - w) / w <= e / E among them, keep the survivors
-                // of the tightened test, and score those exactly in increasing v (equal
-                // scores keep the smallest index).  The loop runs once per set bit of the
-                // lane's survivors, so a warp pays for its busiest lane only.
-                float L = 0.f;
+                // candidates (rare past a job's first pair) are scored exactly in increasing
+                // v (equal scores keep the smallest index).  A lane with more than two first
+                // tightens its test with the best lower bound e (1 - w) / w <= e / E among
+                // them and keeps the survivors.  The scoring loop runs once per set bit of
+                // the lane's survivors, so a warp pays for its busiest lane only.
+                unsigned sm = cm;
+                if (__popc(cm) > 2) {
+                  float L = 0.f;
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if ((cm >> j) & 1u) {
-                    const float e = ex2_approx(fmaf(zo[j], kLog2e, -mL)), w = w_of_draw(dw[j]);
-                    L = fmaxf(L, e * (1.f - w) * rcp_approx(w));
-                  }
-                const float Teff = fmaxf(Tf, L * kShrink);
-                unsigned sm = 0u;
+                  for (int j = 0; j < 16; ++j)
+                    if ((cm >> j) & 1u) {
+                      const float e = ex2_approx(fmaf(zo[j], kLog2e, -mL)), w = w_of_draw(dw[j]);
+                      L = fmaxf(L, e * (1.f - w) * rcp_approx(w));
+                    }
+                  const float Teff = fmaxf(Tf, L * kShrink);
+                  sm = 0u;
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if ((cm >> j) & 1u)
-                    sm |= (ex2_approx(fmaf(zo[j], kLog2e, -mL)) > Teff * w_of_draw(dw[j]) ? 1u : 0u) << j;
+                  for (int j = 0; j < 16; ++j)
+                    if ((cm >> j) & 1u)
+                      sm |= (ex2_approx(fmaf(zo[j], kLog2e, -mL)) > Teff * w_of_draw(dw[j]) ? 1u : 0u) << j;
+                }
                 bool improved = false;
                 while (sm) {
                   const int j = __ffs(sm) - 1;
                   sm &= sm - 1u;
-                  float zj = zo[0];
-                  uint32_t dj = dw[0];
+                  // element j's logit and draw: a select tree on the bits of j (depth 4)
+                  float zj;
+                  uint32_t dj;
+                  {
+                    float z8[8];
+                    uint32_t d8[8];
 #pragma unroll
-                  for (int q = 1; q < 16; ++q)
-                    if (q == j) { zj = zo[q]; dj = dw[q]; }
+                    for (int q = 0; q < 8; ++q) {
+                      z8[q] = (j & 1) ? zo[2 * q + 1] : zo[2 * q];
+                      d8[q] = (j & 1) ? dw[2 * q + 1] : dw[2 * q];
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                      z8[q] = (j & 2) ? z8[2 * q + 1] : z8[2 * q];
+                      d8[q] = (j & 2) ? d8[2 * q + 1] : d8[2 * q];
+                    }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                      z8[q] = (j & 4) ? z8[2 * q + 1] : z8[2 * q];
+                      d8[q] = (j & 4) ? d8[2 * q + 1] : d8[2 * q];
+                    }
+                    zj = (j & 8) ? z8[1] : z8[0];
+                    dj = (j & 8) ? d8[1] : d8[0];
+                  }
                   const float scj = zj - logf(exp1_from_w(w_of_draw(dj)));
                   if (scj > bsc) { bsc = scj; bi = v + j; bz = zj; improved = true; }
                 }
