@@ -98,7 +98,7 @@ struct LSmem {
   static constexpr int kCols = 4 * NBJ / kSamplers;
   static constexpr int kOct = kCols / 8;             // octets per tile per sampler thread
   static constexpr int kWStages = NBJ == 32 ? 8 : NBJ == 64 ? 6 : 4;
-  static constexpr int kUStages = NBJ == 32 ? 4 : NBJ == 64 ? 3 : 2;
+  static constexpr int kUStages = NBJ == 32 ? 3 : NBJ == 64 ? 3 : 2;
   static constexpr int kUStageBytes = NBJ * kTileN * 4;
   // Tensor memory: up to 64 requests make one job per position, whose E rows are gathered
   // only after the grid barrier (one A buffer; three accumulators keep the tensor core and
@@ -112,7 +112,12 @@ struct LSmem {
   static constexpr int kOffMerge = kOffU + kUStages * kUStageBytes;   // [16 warps][5][32] + pad
   static constexpr int kMergeBytes = kSamplers * kMergeStride * 4;
   static constexpr int kOffThr = kOffMerge + kMergeBytes;             // [NBJ] u64
-  static constexpr int kBytes = kOffThr + NBJ * 8;
+  // 32 requests: the E rows staged in shared memory, one copy (16-byte chunk c of row i at
+  // i * 512 + (c ^ (i % 8)) * 16), from which every warp stores its quadrant's copy into
+  // tensor memory; larger chunks store their rows from global memory directly
+  static constexpr int kOffA = (kOffThr + NBJ * 8 + 1023) / 1024 * 1024;
+  static constexpr int kABytes = NBJ == 32 ? 32 * 512 : 0;
+  static constexpr int kBytes = kOffA + kABytes;
 };
 
 struct LParams {
@@ -612,6 +617,61 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     auto gather = [&](int j) {
       const int k = j / p.n_chunks + 1, c = j % p.n_chunks;
       const int ab = j % S::kABufs;
+      if constexpr (NBJ == 32) {
+        // One copy of the 32 rows into the staging area (warp w loads 16-byte chunks w,
+        // w + 8, ..: all in flight at once), a sampler barrier, then each warp stores its
+        // quadrant's copy of its half of the columns from shared memory into the A buffer.
+        // Every sampler thread reaches the barrier: an abort or a timeout skips only the
+        // tensor-memory stores after it.
+        const bool ready = j < S::kABufs || swait(&a_empty[ab], ((j / S::kABufs) & 1) ^ 1);
+        int prev = -1;
+        if (lane < p.B) {
+          prev = (k == 1) ? p.anchor[lane] : token_of_key(__ldcg(p.keys + (size_t)(k - 2) * p.B + lane));
+          if (prev < 0 || prev >= p.V) {
+            set_device_error(p.err, DSPARK_ERR_DEVICE_CHECK);
+            prev = -1;
+          }
+        }
+        const int nch = p.r >> 3;                       // 16-byte chunks of a row
+        const uint4* row = reinterpret_cast<const uint4*>(p.W1 + (size_t)(prev < 0 ? 0 : prev) * p.r);
+        uint8_t* stage = smem + S::kOffA + lane * 512;
+        uint4 v[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          if (sw + 8 * m < nch) v[m] = prev < 0 ? make_uint4(0u, 0u, 0u, 0u) : __ldg(row + sw + 8 * m);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          if (sw + 8 * m < nch)
+            *reinterpret_cast<uint4*>(stage + (((sw + 8 * m) ^ (lane & 7)) << 4)) = v[m];
+        named_bar_sync(kBarSamplers, kSamplerThreads);
+        // warp-uniform: the tensor-memory stores below are whole-warp instructions
+        if (!__all_sync(0xffffffffu, ready) || __any_sync(0xffffffffu, *(volatile int*)&abort_s != 0))
+          return;
+        tc_fence_after_sync();
+        // this warp: lanes of quadrant sw % 4 (row = lane), chunks [h0, h0 + nch / 2)
+        const int half = nch >> 1, h0 = (sw >> 2) * half;
+        const uint32_t taddr = lane_base + (uint32_t)(128 * ab + 4 * h0);
+        if ((half & 1) == 0) {
+          // two chunks (8 columns) per store
+          for (int q = 0; q < half; q += 2) {
+            const uint4 x = *reinterpret_cast<const uint4*>(stage + (((h0 + q) ^ (lane & 7)) << 4));
+            const uint4 y = *reinterpret_cast<const uint4*>(stage + (((h0 + q + 1) ^ (lane & 7)) << 4));
+            const uint32_t cols[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+            tmem_st_32x32b_x8(taddr + 4u * (uint32_t)q, cols);
+          }
+        } else {
+          for (int q = 0; q < half; ++q) {
+            const uint4 x = *reinterpret_cast<const uint4*>(stage + (((h0 + q) ^ (lane & 7)) << 4));
+            tmem_st_32x32b_x2(taddr + 4u * (uint32_t)q, x.x, x.y);
+            tmem_st_32x32b_x2(taddr + 4u * (uint32_t)q + 2u, x.z, x.w);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[ab]);
+        return;
+      }
       if (j >= S::kABufs && !swait(&a_empty[ab], ((j / S::kABufs) & 1) ^ 1)) return;
       // warp-uniform: the tensor-memory stores below are whole-warp instructions
       if (__any_sync(0xffffffffu, *(volatile int*)&abort_s != 0)) return;
