@@ -258,15 +258,6 @@ __device__ __forceinline__ void umma_ts_bf16_f32(uint32_t d_tmem, uint32_t a_tme
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Copy 32 rows x 128 bits from shared memory into tensor memory, replicated into all four
-// lane quadrants (lane 32 q + i receives row i): tcgen05.cp 32x128b.warpx4.  The source is
-// a K-major matrix without swizzle (smem_desc with swizzle 0: rows 16 bytes apart inside an
-// 8-row group, groups sbo bytes apart); the copy is asynchronous and ordered with this
-// thread's later tcgen05.mma, and a later umma_commit covers it.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t src_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
-               : "memory");
-}
 // arrive on `bar` once every previously issued tcgen05.mma of this thread has completed
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
