@@ -125,8 +125,8 @@ __global__ void __launch_bounds__(1024) confidence_kernel(
     if (last_s) {
       __threadfence();            // every other CTA's survivals after their counts
       extern __shared__ unsigned long long keys[];
-      schedule_block(a_out, (int)gridDim.x, gamma, sa.Npad, sa.sps, nullptr, nullptr, sa.ell,
-                     sa.B_total, sa.theta, keys);
+      schedule_block<false>(a_out, (int)gridDim.x, gamma, sa.Npad, sa.sps, nullptr, nullptr, sa.ell,
+                     sa.B_total, sa.theta, keys, (size_t)sa.Npad * sizeof(unsigned long long));
       if (threadIdx.x == 0) *sa.done = 0u;
     }
   }

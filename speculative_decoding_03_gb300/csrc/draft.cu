@@ -1004,8 +1004,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   if (p.ell && cta == 0 && !*(volatile int*)&abort_s) {
     int Npad = 2;
     while (Npad < p.B * p.gamma) Npad <<= 1;
-    schedule_block(p.a_out, p.B, p.gamma, Npad, p.sps, nullptr, nullptr, p.ell, p.B_total,
-                   p.theta, reinterpret_cast<unsigned long long*>(smem + S::kOffW));
+    schedule_block<false>(p.a_out, p.B, p.gamma, Npad, p.sps, nullptr, nullptr, p.ell, p.B_total,
+                   p.theta, reinterpret_cast<unsigned long long*>(smem + S::kOffW),
+                   (size_t)S::kWStages * kWStageBytes);
   }
 }
 

@@ -29,11 +29,11 @@ namespace {
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     const float* __restrict__ a, int R, int gamma, int Npad, const float* __restrict__ sps,
     const int32_t* K_in, int32_t* K_out, int32_t* __restrict__ ell,
-    int32_t* __restrict__ B_total, double* __restrict__ theta) {
+    int32_t* __restrict__ B_total, double* __restrict__ theta, size_t scratch_bytes) {
   extern __shared__ unsigned long long keys[];
   pdl_wait();                 // the expected returns come from the previous kernel
   pdl_launch_dependents();
-  schedule_block(a, R, gamma, Npad, sps, K_in, K_out, ell, B_total, theta, keys);
+  schedule_block<true>(a, R, gamma, Npad, sps, K_in, K_out, ell, B_total, theta, keys, scratch_bytes);
 }
 
 constexpr int kThreshThreads = 1024;
@@ -78,17 +78,21 @@ cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps,
   const int N = R * gamma;
   int Npad = 2;
   while (Npad < N) Npad <<= 1;
-  const size_t smem = (size_t)Npad * sizeof(unsigned long long);
+  // the keys of the ranking or the network (Npad words), or the radix sort's arrays
+  size_t smem = (size_t)Npad * sizeof(unsigned long long);
+  if (N > kSchedThreads && schedule_radix_bytes(N) > smem) smem = schedule_radix_bytes(N);
   // the shared-memory attribute is set once per device
   static std::atomic<int> cache[kMaxCachedDevices];
   const int ok = per_device_grid(cache, [] {
+    size_t most = (size_t)kMaxScheduleItems * sizeof(unsigned long long);
+    if (schedule_radix_bytes(kMaxScheduleItems) > most) most = schedule_radix_bytes(kMaxScheduleItems);
     return cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(kMaxScheduleItems * sizeof(unsigned long long))) == cudaSuccess
+                                (int)most) == cudaSuccess
                ? 1 : -1;
   });
   if (ok <= 0) return cudaErrorInvalidConfiguration;
   return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, stream, a, R, gamma, Npad,
-                    sps, K_in, K_out, ell, B_total, theta);
+                    sps, K_in, K_out, ell, B_total, theta, smem);
 }
 
 }  // namespace dspark

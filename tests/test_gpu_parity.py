@@ -144,6 +144,44 @@ def test_schedule_random_tables_and_sizes():
             assert int(Bt.item()) == Bt_ref and float(th.item()) == th_ref
 
 
+def test_schedule_radix_path_edge_values():
+    """More items than the scheduler's threads (the radix path): exact ties inside and
+    across requests, survivals of 0, NaN, 1 and above, subnormal, and the two smallest
+    fixed-point values (A = 0 and A = 1, which differ in the key's 33rd bit)."""
+    _need_gpu()
+    rng = np.random.default_rng(5)
+    R, gamma = 600, 4                                    # 2400 items
+    a = np.cumprod(rng.uniform(0.0, 1.0, size=(R, gamma)) ** 0.2, axis=1).astype(np.float32)
+    a[10:60, :] = a[5, :]                                # exact ties across requests
+    a[70, :] = 0.0
+    a[71, :] = np.float32(np.nan)
+    a[72, :] = np.float32(1.0)
+    a[73, :] = np.float32(1.5)
+    a[74, :] = np.float32(1e-45)                         # subnormal: A = 0
+    a[75, :] = np.float32(2.0 ** -32)                    # A = 1
+    a[76, :] = np.float32(2.0 ** -33)                    # rounds half up to A = 1
+    a[77, :] = np.float32(np.nextafter(np.float32(2.0 ** -33), np.float32(0)))   # A = 0
+    n = np.arange(R * (gamma + 1) + 1)
+    for sps in [1.0 / (1.0 + 0.0005 * n), 1.0 / (1.0 + np.maximum(0, n - R) / (4.0 * R))]:
+        sps = sps.astype(np.float32)
+        ws = ds.Workspace(R, gamma, 8, 16, 0)
+        ell, Bt, th = ds.schedule(torch.from_numpy(a).cuda(), torch.from_numpy(sps).cuda(), ws)
+        ell_ref, Bt_ref, th_ref = oracle.schedule(a, sps)
+        np.testing.assert_array_equal(ell.cpu().numpy(), ell_ref)
+        assert int(Bt.item()) == Bt_ref and float(th.item()) == th_ref
+        # a capacity that stops inside the zero-survival tail: the order of the last items
+        # (A = 0 after A = 1, then request order) decides which requests keep a position
+        for K in (R * gamma - 7, R * gamma - 13):
+            K_in = torch.tensor([K], dtype=torch.int32, device="cuda")
+            K_out = torch.zeros(1, dtype=torch.int32, device="cuda")
+            ell, Bt, th = ds.schedule_async(torch.from_numpy(a).cuda(), torch.from_numpy(sps).cuda(),
+                                            K_in, K_out, ws)
+            ell_r, Bt_r, th_r, ko_r = oracle.schedule_async(a, sps, K)
+            np.testing.assert_array_equal(ell.cpu().numpy(), ell_r)
+            assert int(Bt.item()) == Bt_r and float(th.item()) == th_r and int(K_out.item()) == ko_r
+        assert ws.status() == 0
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_verify(name):
     _need_gpu()

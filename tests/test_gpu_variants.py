@@ -221,10 +221,10 @@ def test_schedule_async_ring_pipeline():
     assert ws.status() == 0
 
 
-def test_schedule_async_large_batch_uses_the_sorting_network():
+def test_schedule_async_large_batch_uses_the_radix_sort():
     _need_gpu()
     rng = np.random.default_rng(42)
-    R, gamma = 1024, 16                      # 16384 items: bitonic path
+    R, gamma = 1024, 16                      # 16384 items: radix path
     a = _survival(rng, R, gamma, lo=0.5)
     n = np.arange(R * (gamma + 1) + 1)
     sps = (1.0 / (1.0 + np.maximum(0, n - 512) / 512.0)).astype(np.float32)
