@@ -411,19 +411,46 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
   pdl_launch_dependents();
   const int n_items = B * splits, G = gridDim.x;
   constexpr int kSlot = kVerSeg / 4;            // float4 per array slot
-  auto issue = [&](int item, int buf) {         // thread 0
+  // What an item needs besides its rows, loaded by thread 0 one item ahead of its copies and
+  // published with them (the expect-tx arrival releases the record): the mode, the row, the
+  // residual's log normalisers and the excluded token.
+  struct ItemMeta {
+    int md, k, excl, slot;
+    float off_a, off_b;
+  };
+  __shared__ ItemMeta meta_s[2];
+  auto load_meta = [&](int item) -> ItemMeta {  // thread 0
+    ItemMeta m;
+    const int b = item / splits;
+    m.md = mode[b];
+    m.k = pos[b];
+    m.excl = -1;
+    m.slot = 0;
+    m.off_a = m.off_b = 0.f;
+    if (m.md == kModeResidual) {
+      const size_t o = (size_t)b * gamma + (m.k - 1);
+      m.slot = slot_of[b];
+      m.off_b = row_max[o] + logf(row_sumexp[o]);   // log Q = z - off_b
+      m.off_a = M_t[o] + lnS_t[o];                  // log P = T - off_a
+    } else if (m.md == kModePointResidual) {
+      m.excl = tokens[(size_t)b * gamma + (m.k - 1)];
+    }
+    return m;
+  };
+  auto issue = [&](int item, int buf, const ItemMeta& m) {   // thread 0
     const int b = item / splits, seg = item - b * splits;
-    const int md = mode[b], k = pos[b];
+    const int md = m.md, k = m.k;
     const int v0 = seg * kVerSeg;
     const uint32_t bytes = (uint32_t)(min(kVerSeg, V - v0)) * 4u;
     float4* dst = fs_buf + (size_t)buf * 3 * kSlot;
+    meta_s[buf] = m;
     fence_proxy_async_cta();    // the buffer's previous generic reads come first
     if (md == kModeResidual) {
       const size_t o = (size_t)b * gamma + (k - 1);
       mbar_expect_tx_cta(&full[buf], 3u * bytes);
       bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
       bulk_g2s(dst + kSlot, U + o * V + v0, bytes, &full[buf]);
-      bulk_g2s(dst + 2 * kSlot, bias + (size_t)slot_of[b] * V + v0, bytes, &full[buf]);
+      bulk_g2s(dst + 2 * kSlot, bias + (size_t)m.slot * V + v0, bytes, &full[buf]);
     } else if (md == kModeBonus || md == kModePointResidual) {
       mbar_expect_tx_cta(&full[buf], bytes);
       bulk_g2s(dst, T + ((size_t)b * (gamma + 1) + (k - 1)) * V + v0, bytes, &full[buf]);
@@ -431,15 +458,23 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
       mbar_arrive_cta(&full[buf]);
     }
   };
-  if (tid == 0 && blockIdx.x < n_items) issue(blockIdx.x, 0);
+  ItemMeta next;                                // thread 0: the record of item + G
+  if (tid == 0 && blockIdx.x < n_items) {
+    issue(blockIdx.x, 0, load_meta(blockIdx.x));
+    if (blockIdx.x + G < n_items) next = load_meta(blockIdx.x + G);
+  }
   int it = 0;
   for (int item = blockIdx.x; item < n_items; item += G, ++it) {
     const int buf = it & 1;
-    if (tid == 0 && item + G < n_items) issue(item + G, buf ^ 1);
+    if (tid == 0 && item + G < n_items) {
+      issue(item + G, buf ^ 1, next);
+      if (item + 2 * G < n_items) next = load_meta(item + 2 * G);
+    }
     const bool ok = mbar_wait_cta(&full[buf], (uint32_t)(it >> 1) & 1u);
     if (!ok && tid == 0) set_device_error(err, DSPARK_ERR_TIMEOUT);
     const int b = item / splits, seg = item - b * splits;
-    const int md = mode[b], k = pos[b];
+    const ItemMeta m = meta_s[buf];
+    const int md = m.md, k = m.k;
     const bool residual = md == kModeResidual;
     if (md != kModeNone && __syncthreads_and(ok)) {
       const int v0 = seg * kVerSeg + 4 * tid;
@@ -456,14 +491,9 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
           zz[j] = make_float4(u4.x + b4.x, u4.y + b4.y, u4.z + b4.z, u4.w + b4.w);
         }
       }
-      float off_a = 0.f, off_b = 0.f;   // residual: log P = T - off_a, log Q = z - off_b
-      if (residual) {
-        const size_t o = (size_t)b * gamma + (k - 1);
-        off_b = row_max[o] + logf(row_sumexp[o]);
-        off_a = M_t[o] + lnS_t[o];
-      }
+      const float off_a = m.off_a, off_b = m.off_b;   // residual: log P = T - off_a, log Q = z - off_b
       const uint32_t stream = md == kModeBonus ? 3u : 2u;
-      const int excl = md == kModePointResidual ? tokens[(size_t)b * gamma + (k - 1)] : -1;
+      const int excl = m.excl;
       const RowState st =
           race_segment(t, zz, v0, V, residual, off_a, off_b, stream, excl, seed, k, b, red, redf);
       if (tid == 0) partials[item] = st;
