@@ -406,14 +406,15 @@ dspark_status dspark_draft_confidence_schedule(
 
 /*
  * Testing hook for the failure path of the draft (no passage of the pages: the bounded
- * waits are this library's own failure detection).  Every wait inside the draft kernel of
- * dspark_draft, dspark_draft_packed, dspark_draft_greedy and dspark_draft_noalloc is
- * bounded, by default to about 2 s of SM clock; a wait that runs out records
- * DSPARK_ERR_TIMEOUT in the status word and the kernel drains its copies and MMAs, frees
- * its tensor memory and returns.  This call changes, for the draft launches that follow in
- * the process, the bound to `wait_cycles` SM cycles (<= 0: the default) and, when
- * `unreachable_barrier` is non-zero, adds an offset to the kernel's grid-barrier target so
- * that its first barrier cannot complete and a wait must run out.  (0, 0) restores the
+ * waits are this library's own failure detection).  Every wait inside the draft kernels of
+ * dspark_draft, dspark_draft_packed, dspark_draft_greedy, dspark_draft_noalloc,
+ * dspark_draft_confidence_schedule and dspark_draft_rnn is bounded, by default to about 2 s
+ * of SM clock; a wait that runs out records DSPARK_ERR_TIMEOUT in the status word and the
+ * kernel drains its copies and MMAs, frees its tensor memory and returns.  This call
+ * changes, for the draft launches that follow in the process, the bound to `wait_cycles`
+ * SM cycles (<= 0: the default) and, when `unreachable_barrier` is non-zero, adds an offset
+ * to the kernels' barrier targets (the grid barrier, and the RNN head's recurrence count)
+ * so that the first barrier cannot complete and a wait must run out.  (0, 0) restores the
  * production setting.  Not for use while draft launches are in flight or being captured.
  */
 void dspark_testing_set_wait_limit(long long wait_cycles, int unreachable_barrier);

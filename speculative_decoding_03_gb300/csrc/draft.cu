@@ -1081,6 +1081,12 @@ void set_draft_wait_limit(long long cycles, unsigned int grid_extra) {
   g_grid_extra.store(grid_extra);
 }
 
+long long draft_wait_limit() {
+  const long long wc = g_wait_cycles.load();
+  return wc > 0 ? wc : kWaitCycles;
+}
+unsigned int draft_barrier_offset() { return g_grid_extra.load(); }
+
 size_t draft_region_bytes(int B, int gamma) {
   return align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256) + 256 +
          align_up((size_t)gamma * B * sizeof(unsigned long long), 256);

@@ -112,6 +112,8 @@ struct DraftParams {
   float* row_max;
   float* row_sumexp;
   int* err;
+  long long wait_cycles;           // bound of every wait
+  unsigned int grid_extra;         // added to every barrier target (0; tests: unreachable)
   // RNN head (unused by the Markov head)
   const uint16_t* Wrec;            // [3r][2r] the recurrent rows of W_rnn, transposed
   const float* hp;                 // [B][gamma][3r] hidden-state block of the layer, with bias
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     for (;;) {
       if (*(volatile int*)&abort_s) return false;
       if (mbar_try_wait_sleep(bar, parity)) return true;
-      if (sm_cycles() - t0 > kWaitCycles) {
+      if (sm_cycles() - t0 > p.wait_cycles) {
         set_device_error(p.err, DSPARK_ERR_TIMEOUT);
         atomicExch(&abort_s, 1);
         return false;
@@ -691,10 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       const bool rec = c == 0 && cta < p.n_rec;
       if (rec) {
         if (stid == 0 && wait_grid) {
-          const unsigned int target = (unsigned int)G * (unsigned int)(k - 1);
+          const unsigned int target = (unsigned int)G * (unsigned int)(k - 1) + p.grid_extra;
           const long long t0 = sm_cycles();
           while (ld_acquire_u32(p.grid_count) < target) {
-            if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
+            if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
               set_device_error(p.err, DSPARK_ERR_TIMEOUT);
               atomicExch(&abort_s, 1);
               break;
@@ -714,10 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       // thread group, each thread's (at most four) 16-byte loads in flight together
       if (stid == 0) {
         if (c == 0) {
-          const unsigned int target = (unsigned int)p.n_rec * (unsigned int)k;
+          const unsigned int target = (unsigned int)p.n_rec * (unsigned int)k + p.grid_extra;
           const long long t0 = sm_cycles();
           while (ld_acquire_u32(p.rec_count) < target) {
-            if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
+            if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
               set_device_error(p.err, DSPARK_ERR_TIMEOUT);
               atomicExch(&abort_s, 1);
               break;
@@ -765,10 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       if (sw >= kGatherWarps) return;
       if (stid == 0) {
         if (wait_grid) {
-          const unsigned int target = (unsigned int)G * (unsigned int)(k - 1);
+          const unsigned int target = (unsigned int)G * (unsigned int)(k - 1) + p.grid_extra;
           const long long t0 = sm_cycles();
           while (ld_acquire_u32(p.grid_count) < target) {
-            if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
+            if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
               set_device_error(p.err, DSPARK_ERR_TIMEOUT);
               atomicExch(&abort_s, 1);
               break;
@@ -813,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       if (stid == 0) {
         const long long t0 = sm_cycles();
         while (ld_acquire_u32(p.grid_count) < target) {
-          if (*(volatile int*)&abort_s || sm_cycles() - t0 > kWaitCycles) {
+          if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
             set_device_error(p.err, DSPARK_ERR_TIMEOUT);
             atomicExch(&abort_s, 1);
             break;
@@ -1026,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
       }
     }
     // the last position: wait for every CTA, then merge this CTA's rows
-    grid_wait((unsigned int)G * (unsigned int)p.gamma);
+    grid_wait((unsigned int)G * (unsigned int)p.gamma + p.grid_extra);
     if (!*(volatile int*)&abort_s)
       for (int b = cta + sw * G; b < p.B; b += kSamplers * G) finalize_row<Greedy>(p, b, p.gamma, G, lane);
   }
@@ -1128,6 +1130,8 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
   p.row_max = row_max;
   p.row_sumexp = row_sumexp;
   p.err = err;
+  p.wait_cycles = draft_wait_limit();
+  p.grid_extra = draft_barrier_offset();
   if (rnn) {
     p.Wrec = rnn->Wrec;
     p.hp = rnn->hp;

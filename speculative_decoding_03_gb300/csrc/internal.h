@@ -185,6 +185,10 @@ cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uin
 // bound (SM cycles, 0: the default of about 2 s) of that kernel's waits and an offset added
 // to its grid-barrier targets, for the launches that follow (tests of the timeout path)
 void set_draft_wait_limit(long long cycles, unsigned int grid_extra);
+// the current setting of that hook: the bound of every wait (0: the production bound) and
+// the offset added to every grid-barrier target
+long long draft_wait_limit();
+unsigned int draft_barrier_offset();
 
 // the same entry points under their ABI names (see draft_fused.cu)
 cudaError_t launch_draft_fused(const uint16_t* W1, const uint16_t* W2, const float* U,
