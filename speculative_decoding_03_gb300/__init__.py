@@ -521,8 +521,11 @@ class Step:
         self.ring = CapacityRing(d) if scheduler == "async" else None
         # the default step (Gumbel drafts, the Markov head, the early-stop scheduler, packed
         # W2) drafts, scores confidence and schedules in one launch
+        # (the draft grid keeps the survivals of 512 requests per CTA and holds at least
+        # min(vocabulary tiles, 148) CTAs on a GB300)
         self.fused = (fused and sampling == "gumbel" and head == "markov" and scheduler == "theta"
-                      and self.W2p is not None and B * gamma <= 16384)
+                      and self.W2p is not None and B * gamma <= 16384
+                      and B <= 512 * min((V + 127) // 128, 148))
         if head == "rnn":
             self.Wrec = rnn_pack(dev["W_rnn"], r)
             self.hp = torch.empty((B, gamma, 3 * r), dtype=f32, device=d)
