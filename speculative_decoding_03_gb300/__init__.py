@@ -2,10 +2,11 @@
 
 The library behind this binding (``include/dspark.h``) holds the four calls of one
 speculative step -- ``dspark_draft``, ``dspark_confidence``, ``dspark_schedule``,
-``dspark_verify`` -- plus ``dspark_markov_bias``, the packed-W2 variants of the draft and
-the verification, greedy drafting with its verification, the asynchronous two-step
-capacity scheduler, fixed-threshold truncation and the RNN head; every step of the computation runs in
-its CUDA kernels.  This module only marshals arguments: it passes device pointers of
+``dspark_verify`` -- plus ``dspark_draft_confidence_schedule`` (the first three in one
+launch), ``dspark_markov_bias``, the packed-W2 variants of the draft and the verification,
+greedy drafting with its verification, the asynchronous two-step capacity scheduler,
+fixed-threshold truncation and the RNN head; every step of the computation runs in its
+CUDA kernels.  This module only marshals arguments: it passes device pointers of
 torch tensors and the current CUDA stream through ctypes, and allocates outputs and the
 workspace with torch.  There is no CPU fallback: without the built library and a CUDA
 device every call raises.
@@ -138,10 +139,10 @@ def as_bf16_tensor(bits: np.ndarray, device="cuda"):
 
 
 def testing_set_wait_limit(wait_cycles: int = 0, unreachable_barrier: bool = False):
-    """Bound of the draft kernel's waits (SM cycles, 0: the default of about 2 s) and, when
-    ``unreachable_barrier``, a grid barrier that cannot complete, for the draft launches
-    that follow (tests of the timeout path; ``testing_set_wait_limit()`` restores the
-    production setting)."""
+    """Bound of the draft kernels' waits (SM cycles, 0: the default of about 2 s) and, when
+    ``unreachable_barrier``, barriers that cannot complete, for the draft launches that
+    follow (tests of the timeout path; ``testing_set_wait_limit()`` restores the production
+    setting)."""
     lib().dspark_testing_set_wait_limit(int(wait_cycles), int(bool(unreachable_barrier)))
 
 
