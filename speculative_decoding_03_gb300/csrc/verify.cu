@@ -337,8 +337,6 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
     for (int i = 0; i < 4; ++i) cm |= (r_hi[j][i] >= 0.f && r_hi[j][i] >= L * w[j][i] ? 1u : 0u) << i;
     if (cm == 0u) continue;
     const int v = v0 + j * 4 * kSampleThreads;
-    const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, stream);
-    const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w};
     const float tv[4] = {t[j].x, t[j].y, t[j].z, t[j].w};
     const float zv[4] = {zz[j].x, zz[j].y, zz[j].z, zz[j].w};
 #pragma unroll
@@ -351,9 +349,9 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
         // log(P - Q) = log Q + log(expm1(log P - log Q)), accurate when P ~ Q; for
         // d > 20 it is log P to within 2e-9
         const float lres = d > 20.f ? lq + d : lq + logf(expm1f(d));
-        score = lres + gumbel_of(dw[i]);
+        score = lres - logf(exp1_from_w(w[j][i]));   // g = -log E, from phase 1's w
       } else {
-        score = tv[i] + gumbel_of(dw[i]);
+        score = tv[i] - logf(exp1_from_w(w[j][i]));
       }
       if (better(score, v + i, st.score, st.idx)) {
         st.score = score;
