@@ -38,9 +38,10 @@
 // element's ratio exp(z - M) / E from above and exp(z - M)(1 - w) / w from below: an
 // element is a candidate only if its upper bound beats exp(best - M), where best is the
 // best exact score any thread of the CTA has found for the request (a 64-bit shared-memory
-// atomic max, tagged with the job so that no reset is needed); a thread with many
-// candidates tightens the threshold with their best lower bound, and only the survivors
-// evaluate the exact score z - log E with log1p and log.
+// atomic max, tagged with the job so that no reset is needed; for chunks of 64 or more
+// requests also the best any CTA has published in the request's argmax key); a thread with
+// many candidates tightens the threshold with their best lower bound, and only the
+// survivors evaluate the exact score z - log E with log1p and log.
 //
 // After its last tile of a job, every sampler thread leaves its partial (max, sum, best
 // score, index, logit) in shared memory; the sampler threads merge them with a shuffle tree
@@ -744,9 +745,24 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       float Mr = -INFINITY, Tf = 0.f, known = -INFINITY, ssum = 0.f, mx = -INFINITY;
       float bsc = -INFINITY, bz = -INFINITY;
       int bi = -1;
+      // Chunks of 64 or more requests also share bounds between CTAs: the argmax key of the
+      // request at this position holds the best (score, index) any CTA has published so far
+      // (every value published there is an exact score of one of the request's elements,
+      // so the final maximum is unchanged).  One reader per request and CTA folds it into
+      // the CTA's bound a tile after loading it; a thread holding the CTA's best publishes
+      // it after its second and fourth tiles.  (For 32 requests the traffic on the few key
+      // lines costs more than the bound saves.)
+      [[maybe_unused]] unsigned long long* kp = p.keys + (size_t)(k - 1) * p.B + (valid ? b : 0);
+      [[maybe_unused]] unsigned long long gk = 0ull;
       for (int t = 0; t < my_tiles; ++t, ++tc) {
         const int acc = tc % S::kAccBufs;
         const int su = tc % S::kUStages;
+        if constexpr (!Greedy && NBJ >= 64) {
+          if (sidx == 0 && valid) {
+            if (gk) atomic_max_shared_u64(&thr[ml], tag | (gk >> 32));
+            if (t >= 1 && t + 1 < my_tiles) gk = __ldcg(kp);
+          }
+        }
         // both stages are held until the tile is done (the other accumulators and the U
         // ring keep the tensor core and the copies ahead)
         const bool have = swait(&acc_full[acc], (tc / S::kAccBufs) & 1) &&
@@ -895,6 +911,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
               }
             }
           }
+        }
+        if constexpr (!Greedy && NBJ >= 64) {
+          if (valid && (t == 1 || t == 3) && t + 2 < my_tiles && bi >= 0 && bsc >= known)
+            atomicMax(kp, argmax_key(bsc, bi));
         }
         if (have) {
           tc_fence_before_sync();
