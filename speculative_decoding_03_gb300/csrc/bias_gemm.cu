@@ -22,7 +22,8 @@
 // kernel (the number of rejected requests), read by the epilogue after that kernel has
 // finished and published to the producer and the MMA issuer through an mbarrier; the first
 // pass over W2 is streamed before the count is known, later passes only when needed.  A
-// pass covers NB <= 128 rows (one tensor-core N per vocabulary tile).
+// pass covers NB <= 256 rows (one tensor-core N per vocabulary tile; 256 only when the
+// whole batch fits one pass).
 //
 // Split mode (the RNN head's verification): E[b] = Ef[prev_b], fp32 rows of a table of
 // table_rows rows; each row enters the contraction as two bf16 images, hi = bf16(E) and
@@ -58,7 +59,10 @@ struct BiasSmem {
   static constexpr int kOffE = kOffW + kBiasStages * kStageBytes;
   static constexpr int kEHalf = NB * 256 * 2;    // NB rows x r <= 256, one image
   static constexpr int kEBytes = (Split ? 2 : 1) * kEHalf;
-  static constexpr int kBytes = kOffE + 2 * kEBytes;
+  // 256-row passes: one E buffer and two accumulators (512 tensor-memory columns)
+  static constexpr int kEBufs = NB == 256 ? 1 : 2;
+  static constexpr int kDepth = NB == 256 ? 2 : kBiasDepth;
+  static constexpr int kBytes = kOffE + kEBufs * kEBytes;
 };
 
 __device__ __forceinline__ uint32_t bf16_bits_rne(float x) {
@@ -75,13 +79,14 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
   using S = BiasSmem<NB, Split>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t w_full[kBiasStages], w_empty[kBiasStages];
-  __shared__ uint64_t e_full[2], e_empty[2];
-  __shared__ uint64_t acc_full[kBiasDepth], acc_empty[kBiasDepth];
+  __shared__ uint64_t e_full[S::kEBufs], e_empty[S::kEBufs];
+  __shared__ uint64_t acc_full[S::kDepth], acc_empty[S::kDepth];
   __shared__ uint64_t mma_drain;
   __shared__ uint64_t count_ready;   // the epilogue has published the pass count
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ int rows_s, jobs_s;
+  __shared__ int pv_s[NB];           // the current pass's predecessor rows
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,12 +96,12 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
   const int my_tiles = t_hi - t_lo;
   const int n_kchunks = r / kc;
   uint32_t tmem_cols = 32;
-  while (tmem_cols < (uint32_t)(kBiasDepth * NB)) tmem_cols <<= 1;
+  while (tmem_cols < (uint32_t)(S::kDepth * NB)) tmem_cols <<= 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kBiasStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&e_full[i], 1); mbar_init(&e_empty[i], 1); }
-    for (int i = 0; i < kBiasDepth; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+    for (int i = 0; i < S::kEBufs; ++i) { mbar_init(&e_full[i], 1); mbar_init(&e_empty[i], 1); }
+    for (int i = 0; i < S::kDepth; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
     mbar_init(&mma_drain, 1);
     mbar_init(&count_ready, 1);
     abort_s = 0;
@@ -183,13 +188,13 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
       int n_jobs = 0x7FFFFFFF;
       for (int job = 0; job < n_jobs && ok; ++job) {
         if (job == 1 && (n_jobs = passes_after_first()) <= 1) break;
-        const int eb = job & 1;
-        if (!(ok = wait1(&e_full[eb], (job >> 1) & 1))) break;
+        const int eb = job % S::kEBufs;
+        if (!(ok = wait1(&e_full[eb], (job / S::kEBufs) & 1))) break;
         const uint64_t b_base =
             smem_desc(smem_u32(smem + S::kOffE + eb * S::kEBytes), 16u, 1024u, kSwizzle128B);
         for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
-          const int ab = tc % kBiasDepth;
-          if (!(ok = wait1(&acc_empty[ab], ((tc / kBiasDepth) & 1) ^ 1))) break;
+          const int ab = tc % S::kDepth;
+          if (!(ok = wait1(&acc_empty[ab], ((tc / S::kDepth) & 1) ^ 1))) break;
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + (uint32_t)(ab * NB);
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
@@ -244,52 +249,78 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
     uint32_t tc = 0;
     for (int job = 0; job < n_jobs; ++job) {
       const int b0 = job * NB;
-      const int eb = job & 1;
+      const int eb = job % S::kEBufs;
       // E = W1[prev_b] as the K-major, 128-byte-swizzled B operand: 16-byte chunk c of row n
       // goes to chunk (c % 8) ^ (n % 8) of line n of K-block c / 8
-      if (et == 0) wait1(&e_empty[eb], ((job >> 1) & 1) ^ 1);
+      if (et == 0) wait1(&e_empty[eb], ((job / S::kEBufs) & 1) ^ 1);
       named_bar_sync_n(kBiasNamedBar, 128);
       uint8_t* sE = smem + S::kOffE + eb * S::kEBytes;
+      // the pass's predecessor rows, once (checked here), then the operand rows; a 256-row
+      // pass keeps four 16-byte loads in flight per thread (measured: one is best at 128)
+      for (int n = et; n < NB; n += 128) {
+        const int b = b0 + n;
+        int pv = -1;
+        if (b < rows) {
+          pv = prev[(size_t)b * prev_stride];
+          if (pv < -1 || pv >= table_rows) {
+            set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
+            pv = -1;
+          }
+        }
+        pv_s[n] = pv;
+      }
+      named_bar_sync_n(kBiasNamedBar, 128);
       if (!*(volatile int*)&abort_s) {
-        for (int idx = et; idx < NB * kchunks; idx += 128) {
-          const int n = idx / kchunks, c = idx - n * kchunks;
-          const int b = b0 + n;
-          uint4 val = make_uint4(0u, 0u, 0u, 0u), lo = val;
-          if (b < rows) {
-            const int pv = prev[(size_t)b * prev_stride];
-            if (pv >= 0 && pv < table_rows) {
-              if constexpr (Split) {
-                const float4* src = reinterpret_cast<const float4*>(Ef + (size_t)pv * r) + 2 * c;
-                const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
-                const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                uint32_t hb[8], lb[8];
+        constexpr int kBatch = NB == 256 ? 4 : 1;
+        for (int idx0 = et; idx0 < NB * kchunks; idx0 += 128 * kBatch) {
+          uint4 val[kBatch], lo[kBatch];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  hb[e] = bf16_bits_rne(x[e]);
-                  lb[e] = bf16_bits_rne(x[e] - __uint_as_float(hb[e] << 16));
+          for (int u = 0; u < kBatch; ++u) {
+            const int idx = idx0 + 128 * u;
+            val[u] = make_uint4(0u, 0u, 0u, 0u);
+            lo[u] = val[u];
+            if (idx < NB * kchunks) {
+              const int n = idx / kchunks, c = idx - n * kchunks;
+              const int pv = pv_s[n];
+              if (pv >= 0) {
+                if constexpr (Split) {
+                  const float4* src = reinterpret_cast<const float4*>(Ef + (size_t)pv * r) + 2 * c;
+                  const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                  const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                  uint32_t hb[8], lb[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    hb[e] = bf16_bits_rne(x[e]);
+                    lb[e] = bf16_bits_rne(x[e] - __uint_as_float(hb[e] << 16));
+                  }
+                  val[u] = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
+                                      hb[6] | (hb[7] << 16));
+                  lo[u] = make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16),
+                                     lb[6] | (lb[7] << 16));
+                } else {
+                  val[u] = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)pv * r) + c);
                 }
-                val = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
-                                 hb[6] | (hb[7] << 16));
-                lo = make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16),
-                                lb[6] | (lb[7] << 16));
-              } else {
-                val = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)pv * r) + c);
               }
-            } else if (pv != -1) {
-              set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
             }
           }
-          const size_t off = (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 + (((c & 7) ^ (n & 7)) << 4);
-          *reinterpret_cast<uint4*>(sE + off) = val;
-          if constexpr (Split) *reinterpret_cast<uint4*>(sE + S::kEHalf + off) = lo;
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int idx = idx0 + 128 * u;
+            if (idx < NB * kchunks) {
+              const int n = idx / kchunks, c = idx - n * kchunks;
+              const size_t off = (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 + (((c & 7) ^ (n & 7)) << 4);
+              *reinterpret_cast<uint4*>(sE + off) = val[u];
+              if constexpr (Split) *reinterpret_cast<uint4*>(sE + S::kEHalf + off) = lo[u];
+            }
+          }
         }
       }
       fence_proxy_async_smem();
       named_bar_sync_n(kBiasNamedBar, 128);
       if (et == 0) mbar_arrive(&e_full[eb]);
       for (int t = 0; t < my_tiles; ++t, ++tc) {
-        const int ab = tc % kBiasDepth;
-        const bool ok = wait1(&acc_full[ab], (tc / kBiasDepth) & 1);
+        const int ab = tc % S::kDepth;
+        const bool ok = wait1(&acc_full[ab], (tc / S::kDepth) & 1);
         if (!__all_sync(0xffffffffu, ok)) continue;
         tc_fence_after_sync();
         const int v = (t_lo + t) * kGemmTileV + q * 32 + lane;
@@ -395,6 +426,12 @@ cudaError_t launch_bias_common(const uint16_t* W2, const uint16_t* W2p, const ui
   if (B <= 64 || Split)
     return launch_bias_nb<64, Split>(w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, n_rows,
                                      V, r, kc, n_tiles, out, err, stream);
+  // up to 256 rows: one pass over W2 with N = 256 (two accumulators); a larger batch takes
+  // passes of 128 rows, whose four accumulators keep the stores of one tile under the
+  // contraction of the next (faster when the bias is store-bound)
+  if (B > 128 && B <= 256)
+    return launch_bias_nb<256, false>(w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, n_rows,
+                                      V, r, kc, n_tiles, out, err, stream);
   return launch_bias_nb<128, false>(w2_map, W2p, W1, Ef, table_rows, prev, prev_stride, B, n_rows,
                                     V, r, kc, n_tiles, out, err, stream);
 }

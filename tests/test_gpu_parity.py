@@ -33,7 +33,8 @@ def _need_gpu():
 
 
 # small cases that span several 128-row vocabulary tiles, a ragged last tile, batch
-# chunks of the tensor-core contraction (B > 256), and every Markov rank shape
+# chunks of the tensor-core contraction (B > 256), the one-pass 256-row contraction
+# (128 < B <= 256), and every Markov rank shape
 CASES = {
     "tiny": workloads.get("tiny"),
     "qwen_small": workloads.scaled(workloads.get("qwen3_4b_like"), B=5, gamma=3, V=904, r=64, H=32),
@@ -41,6 +42,7 @@ CASES = {
     "long_small": workloads.scaled(workloads.get("long_block"), B=7, gamma=15, V=1032, r=256, H=16,
                                    noise_std=lambda k: 0.5 + 1.5 * (k - 1) / 14.0),
     "wide_batch": workloads.scaled(workloads.get("scheduler_stress"), B=300, gamma=2, V=520, r=128, H=8),
+    "mid_batch": workloads.scaled(workloads.get("production"), B=200, gamma=3, V=1160, r=256, H=16),
 }
 
 
