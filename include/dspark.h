@@ -29,7 +29,8 @@
  *     U01(x) = ((x >> 9) + 1/2) * 2^-23.  Streams: 0 draft Gumbel, 1 acceptance uniform
  *     (v = 0), 2 residual Gumbel, 3 bonus Gumbel.  Gumbel g = -log(-log U01).
  *   - Shape limits: 1 <= B < 65536, 1 <= gamma <= 32, B * (gamma + 1) < 2^21,
- *     8 <= V < 2^31 with V % 8 == 0, 16 <= r <= 256 with r % 16 == 0, H % 4 == 0.
+ *     8 <= V < 2^31 with V % 8 == 0, 16 <= r <= 256 with r % 16 == 0, H % 4 == 0; the
+ *     draft calls also need ceil(B / 128) * ceil(V / 128) < 26843545 (2^32 / 160).
  *
  * Errors
  *   - Every call validates its arguments on the host before launching anything and

@@ -72,11 +72,9 @@ dspark_status dspark_draft(const float* U, const uint16_t* W1, const uint16_t* W
   const Plan p = make_plan(B, gamma, V, r, 0);
   if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
 
-  if (launch_draft_fused(W1, W2, U, anchor, B, gamma, V, r, seed, tokens, q_tok, row_max,
-                         row_sumexp, ws_at<char>(workspace, p.off_draft),
-                         ws_at<int>(workspace, p.off_err), stream) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
-  return DSPARK_OK;
+  return draft_status(launch_draft_fused(W1, W2, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
+                                         row_max, row_sumexp, ws_at<char>(workspace, p.off_draft),
+                                         ws_at<int>(workspace, p.off_err), stream));
 }
 
 dspark_status dspark_confidence(const float* h, const int32_t* anchor, const int32_t* tokens,
@@ -219,11 +217,10 @@ dspark_status dspark_draft_greedy(const float* U, const uint16_t* W1, const uint
     return DSPARK_ERR_INVALID_ARG;
   const Plan p = make_plan(B, gamma, V, r, 0);
   if ((st = check_ws(workspace, workspace_bytes, p)) != DSPARK_OK) return st;
-  if (launch_draft_fused_greedy(W1, W2, W2p, U, anchor, B, gamma, V, r, tokens, q_tok, row_max,
-                                row_sumexp, ws_at<char>(workspace, p.off_draft),
-                                ws_at<int>(workspace, p.off_err), stream) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
-  return DSPARK_OK;
+  return draft_status(launch_draft_fused_greedy(W1, W2, W2p, U, anchor, B, gamma, V, r, tokens,
+                                                q_tok, row_max, row_sumexp,
+                                                ws_at<char>(workspace, p.off_draft),
+                                                ws_at<int>(workspace, p.off_err), stream));
 }
 
 dspark_status dspark_verify_greedy(const float* T, const int32_t* tokens, const int32_t* ell,

@@ -8,10 +8,14 @@
 // greedy variant (section 11: the serving example drafts greedily) takes x_k = argmax_v z_v
 // (ties to the smallest v) and q_k(x_k) = 1, the proposal being the point mass at x_k.
 //
-// Layout of the work.  The vocabulary is cut into 128-column tiles; each CTA (one per SM,
-// cooperative launch) owns a contiguous run of tiles for the whole call.  A job is one
-// position k and one chunk of NBJ requests (NBJ = 32, 64 or 128).  Per job and tile the
-// tensor core computes D[m][n] = sum_i A[m][i] B[i][n] with M = 128, N = 128, K = r:
+// Layout of the work.  The vocabulary is cut into 128-column tiles and the batch into
+// chunks of NBJ requests (NBJ = 32, 64 or 128); a position's work is chunks x tiles units,
+// and each CTA (one per SM, cooperative launch) owns the same contiguous run of units at
+// every position: a run of tiles of one chunk, or the end of one chunk and the start of
+// the next, so that large batches with small vocabularies still give every CTA many
+// tiles per position.  A job is one position k and one chunk the CTA holds units of.  Per
+// job and tile the tensor core computes D[m][n] = sum_i A[m][i] B[i][n] with M = 128,
+// N = 128, K = r:
 //   A  the E rows W1[x_{k-1}] of the chunk, in tensor memory: row m on lane m, two bf16
 //      per 32-bit column.  A chunk of NBJ < 128 requests is repeated 128 / NBJ times down
 //      the lanes, so that every warp quadrant (a warp reads only the 32 lanes of its
@@ -49,8 +53,8 @@
 // 64-bit atomic max key.  One grid barrier per position (a release reduction per CTA, one
 // bounded poller) makes x_k known everywhere; the samplers then gather the next position's
 // E rows into an A buffer with tcgen05.st.  The CTA with index b mod G
-// then merges the G partials of request b into x_k, q_k(x_k), max and sum while the tensor
-// core computes the next position's first tile.
+// then merges the partials of request b (from the CTAs that hold its chunk) into x_k,
+// q_k(x_k), max and sum while the tensor core computes the next position's first tile.
 //
 // Failure handling: every wait is bounded (LParams::wait_cycles SM cycles).  A wait that
 // runs out records DSPARK_ERR_TIMEOUT and sets a CTA-wide abort flag; from then on the
@@ -210,20 +214,64 @@ __device__ __forceinline__ int token_of_key(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
 
-// Merge the G partials of request b at position kp into x, q, max and sum (one warp; every
-// lane issues all its loads together, so a merge is about one L2 round trip).
+// The work of a position is n_chunks x n_tiles units (one chunk of NBJ requests on one
+// 128-column vocabulary tile, chunk-major); CTA g owns units [g U / G, (g + 1) U / G) of
+// every position: a run of tiles of one chunk, or of the end of one chunk and the start
+// of the next ones.  A job is one position and one chunk that the CTA holds units of, with
+// the CTA's tile range in that chunk.  (One chunk: the CTA's tiles are the same for every
+// job.)
+// The launch keeps U G below 2^32, so these products and quotients are 32-bit (64-bit
+// division here cost the single-chunk draft 3 % in code size).
+struct JobMap {
+  int u_lo, u_hi, c_first, jpp, n_tiles;   // jpp: jobs per position
+  __device__ __forceinline__ JobMap(int cta, int G, int n_chunks, int n_tiles_)
+      : n_tiles(n_tiles_) {
+    const unsigned U = (unsigned)n_chunks * (unsigned)n_tiles_;
+    u_lo = (int)((unsigned)cta * U / (unsigned)G);
+    u_hi = (int)((unsigned)(cta + 1) * U / (unsigned)G);
+    c_first = u_lo / n_tiles_;
+    jpp = (u_hi - 1) / n_tiles_ - c_first + 1;
+  }
+  __device__ __forceinline__ int k(int j) const { return jpp == 1 ? j + 1 : j / jpp + 1; }
+  __device__ __forceinline__ int c(int j) const { return jpp == 1 ? c_first : c_first + j % jpp; }
+  __device__ __forceinline__ int t_begin(int j) const {
+    const int a = u_lo - c(j) * n_tiles;
+    return a > 0 ? a : 0;
+  }
+  __device__ __forceinline__ int t_end(int j) const {
+    const int e = u_hi - c(j) * n_tiles;
+    return e < n_tiles ? e : n_tiles;
+  }
+  __device__ __forceinline__ bool last_of_position(int j) const {
+    return jpp == 1 || j % jpp == jpp - 1;
+  }
+};
+// The CTAs that hold units of chunk c (and so publish partials of its requests) are
+// [first, last]: the owners of the chunk's first and last unit, unit u being owned by CTA
+// ((u + 1) G - 1) / U.
+__device__ __forceinline__ int2 chunk_holders(int G, int c, int n_chunks, int n_tiles) {
+  if (n_chunks == 1) return make_int2(0, G - 1);
+  const unsigned U = (unsigned)n_chunks * (unsigned)n_tiles, u0 = (unsigned)c * (unsigned)n_tiles;
+  return make_int2((int)(((u0 + 1u) * (unsigned)G - 1u) / U),
+                   (int)(((u0 + (unsigned)n_tiles) * (unsigned)G - 1u) / U));
+}
+
+// Merge the partials of request b (chunk c) at position kp from the CTAs that hold its
+// chunk into x, q, max and sum (one warp; every lane issues all its loads together, so a
+// merge is about one L2 round trip).
 constexpr int kMergePerLane = (kDraftMaxCtas + 31) / 32;
 template <bool Greedy>
-__device__ __forceinline__ void finalize_row(const LParams& p, int b, int kp, int G, int lane) {
+__device__ __forceinline__ void finalize_row(const LParams& p, int b, int c, int kp, int G, int lane) {
   const unsigned long long key = __ldcg(p.keys + (size_t)(kp - 1) * p.B + b);
   const RowState* base = p.partials + ((size_t)(kp % 3) * p.B + b) * G;
+  const int2 hold = chunk_holders(G, c, p.n_chunks, p.n_tiles);
   float pm[kMergePerLane], ps[kMergePerLane], pz[kMergePerLane];
   int pi[kMergePerLane];
 #pragma unroll
   for (int u = 0; u < kMergePerLane; ++u) {
     const int g = lane + 32 * u;
     pm[u] = -INFINITY; ps[u] = 0.f; pz[u] = -INFINITY; pi[u] = -1;
-    if (g < G) {
+    if (g >= hold.x && g <= hold.y) {
       pm[u] = __ldcg(&base[g].m);
       ps[u] = __ldcg(&base[g].s);
       pz[u] = __ldcg(&base[g].z);
@@ -277,12 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int t_lo = (int)((long long)cta * p.n_tiles / G);
-  const int t_hi = (int)((long long)(cta + 1) * p.n_tiles / G);
-  const int my_tiles = t_hi - t_lo;
+  const JobMap jm(cta, G, p.n_chunks, p.n_tiles);
   const int kc = p.kc;
   const int n_kchunks = p.r / kc;
-  const int n_jobs = p.gamma * p.n_chunks;
+  const int n_jobs = p.gamma * jm.jpp;
   unsigned long long* thr = reinterpret_cast<unsigned long long*>(smem + S::kOffThr);
 
   if (threadIdx.x == 0) {
@@ -341,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       uint32_t ws = 0;
       bool ok = true;
       for (int job = 0; job < n_jobs && ok; ++job) {
-        for (int t = t_lo; t < t_hi && ok; ++t) {
+        const int t_end = jm.t_end(job);
+        for (int t = jm.t_begin(job); t < t_end && ok; ++t) {
           for (int i = 0; i < n_kchunks; ++i, ++ws) {
             const int s = ws % S::kWStages;
             if (!(ok = wait1(&w_empty[s], ((ws / S::kWStages) & 1) ^ 1))) break;
@@ -377,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       uint32_t us = 0;
       bool ok = true;
       for (int job = 0; job < n_jobs && ok; ++job) {
-        const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
-        for (int t = t_lo; t < t_hi; ++t, ++us) {
+        const int k = jm.k(job), c = jm.c(job), t_end = jm.t_end(job);
+        for (int t = jm.t_begin(job); t < t_end; ++t, ++us) {
           const int su = us % S::kUStages;
           if (!(ok = wait1(&u_empty[su], ((us / S::kUStages) & 1) ^ 1))) break;
           mbar_arrive_expect_tx(&u_full[su], (uint32_t)S::kUStageBytes);
@@ -436,7 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
         if (!(ok = wait1(&a_full[ab], (job / S::kABufs) & 1))) break;
         tc_fence_after_sync();
         const uint32_t a_t = tmem_base + (uint32_t)(128 * ab);
-        for (int t = 0; t < my_tiles && ok; ++t, ++tc) {
+        const int n_t = jm.t_end(job) - jm.t_begin(job);
+        for (int t = 0; t < n_t && ok; ++t, ++tc) {
           const int acc = tc % S::kAccBufs;
           if (!(ok = spin_wait(&acc_empty[acc], ((tc / S::kAccBufs) & 1) ^ 1))) break;
           tc_fence_after_sync();
@@ -616,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     // E rows of job j into A buffer j % kABufs: this thread's lane holds row 32 quad + lane
     // (request c NBJ + ml), this warp writes columns [jq r / 8, (jq + 1) r / 8) of it
     auto gather = [&](int j) {
-      const int k = j / p.n_chunks + 1, c = j % p.n_chunks;
+      const int k = jm.k(j), c = jm.c(j);
       const int ab = j % S::kABufs;
       if constexpr (NBJ == 32) {
         // One copy of the 32 rows into the staging area (warp w loads 16-byte chunks w,
@@ -733,9 +781,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     uint32_t tc = 0;
     gather(0);
     for (int job = 0; job < n_jobs; ++job) {
-      const int k = job / p.n_chunks + 1, c = job % p.n_chunks;
+      const int k = jm.k(job), c = jm.c(job);
+      const int t_lo = jm.t_begin(job), my_tiles = jm.t_end(job) - t_lo;
       // the next chunk of the same position only needs x_{k-1}: gather it now
-      if (c + 1 < p.n_chunks) gather(job + 1);
+      if (!jm.last_of_position(job)) gather(job + 1);
       const int b = c * NBJ + ml;
       const bool valid = b < p.B;
       const unsigned long long tag = (unsigned long long)(job + 1) << 32;
@@ -979,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       // the partials and keys are ordered before the grid arrival by this barrier; the
       // merge area is free again after it
       named_bar_sync(kBarSamplers, kSamplerThreads);
-      if (c + 1 == p.n_chunks) {
+      if (jm.last_of_position(job)) {
         if (stid == 0 && !*(volatile int*)&abort_s) {
           // the last arrival also carries this CTA's survivals: wait for the confidence warp
           if (k == p.gamma && p.c_out) {
@@ -1003,7 +1052,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
           // tensor core computes the next position's first tile (slot k % 3 is next
           // written at position k + 3)
           if (!*(volatile int*)&abort_s) {
-            for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G) finalize_row<Greedy>(p, bb, k, G, lane);
+            for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G)
+              finalize_row<Greedy>(p, bb, bb / NBJ, k, G, lane);
           }
         }
       }
@@ -1011,7 +1061,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     // the last position: wait for every CTA, then merge this CTA's rows
     grid_wait((unsigned int)G * (unsigned int)p.gamma + p.grid_extra);
     if (!*(volatile int*)&abort_s)
-      for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G) finalize_row<Greedy>(p, bb, p.gamma, G, lane);
+      for (int bb = cta + sw * G; bb < p.B; bb += kSamplers * G)
+        finalize_row<Greedy>(p, bb, bb / NBJ, p.gamma, G, lane);
   }
 
   tc_fence_before_sync();
@@ -1135,6 +1186,10 @@ cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uin
   p.B = B; p.gamma = gamma; p.V = V; p.r = r;
   p.n_tiles = n_tiles;
   p.n_chunks = cdiv(B, NBJ);
+  // the kernel's unit arithmetic is 32-bit: (chunks x tiles) x CTAs < 2^32
+  if ((unsigned long long)p.n_chunks * (unsigned long long)n_tiles * (unsigned long long)grid >=
+      (1ull << 32))
+    return cudaErrorNotSupported;
   p.kc = draft_kchunk(r);
   p.seed = seed;
   const size_t part_bytes = align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256);

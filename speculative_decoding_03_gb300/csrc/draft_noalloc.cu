@@ -84,8 +84,6 @@ extern "C" dspark_status dspark_draft_noalloc(const float* U, const uint16_t* W1
   char* scratch = static_cast<char*>(base);
   int* err = reinterpret_cast<int*>(scratch);
   if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (launch_draft_fused(W1, W2, U, anchor, B, gamma, V, r, seed, tokens, q_tok, row_max,
-                         row_sumexp, scratch + 256, err, stream) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
-  return DSPARK_OK;
+  return draft_status(launch_draft_fused(W1, W2, U, anchor, B, gamma, V, r, seed, tokens, q_tok,
+                                         row_max, row_sumexp, scratch + 256, err, stream));
 }

@@ -229,6 +229,12 @@ cudaError_t launch_rnn_project(const float* h, const uint16_t* W_rnn, const floa
                                int H, int r, float* hp, cudaStream_t stream);
 // rank rows per W2 stage of the draft kernel (and per packed K-chunk image)
 int draft_kchunk(int r);
+// the ABI status of a draft launch: cudaErrorNotSupported (a shape beyond the draft
+// kernel's limits) is DSPARK_ERR_UNSUPPORTED, any other failure DSPARK_ERR_CUDA
+inline dspark_status draft_status(cudaError_t e) {
+  return e == cudaSuccess ? DSPARK_OK
+       : e == cudaErrorNotSupported ? DSPARK_ERR_UNSUPPORTED : DSPARK_ERR_CUDA;
+}
 
 cudaError_t launch_confidence(const float* h, const int32_t* anchor, const int32_t* tokens,
                               const uint16_t* W1, const float* w_c, float b_c, int B, int gamma,

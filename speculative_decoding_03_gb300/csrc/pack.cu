@@ -90,11 +90,10 @@ dspark_status dspark_draft_packed(const float* U, const uint16_t* W1, const uint
     return DSPARK_ERR_INVALID_ARG;
   const Plan p = make_plan(B, gamma, V, r, 0);
   if (!aligned_ptr(workspace, 256) || workspace_bytes < p.total) return DSPARK_ERR_INVALID_ARG;
-  if (launch_draft_fused_packed(W1, W2p, U, anchor, B, gamma, V, r, seed, tokens, q_tok, row_max,
-                                row_sumexp, ws_at<char>(workspace, p.off_draft),
-                                ws_at<int>(workspace, p.off_err), stream) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
-  return DSPARK_OK;
+  return draft_status(launch_draft_fused_packed(W1, W2p, U, anchor, B, gamma, V, r, seed, tokens,
+                                                q_tok, row_max, row_sumexp,
+                                                ws_at<char>(workspace, p.off_draft),
+                                                ws_at<int>(workspace, p.off_err), stream));
 }
 
 }  // extern "C"
