@@ -62,8 +62,8 @@ struct Plan {
   int B, gamma, V, r, H;
   RowSplit stats, ver;
   // byte offsets into the workspace
-  size_t off_err, off_draft, off_bias, off_part, off_M, off_lnS, off_p, off_mode,
-      off_pos, off_prev, off_slot, off_nres, off_fallback, off_rnn_state, total;
+  size_t off_err, off_draft, off_bias, off_part, off_mode,
+      off_pos, off_prev, off_slot, off_nres, off_fallback, off_rec, off_rnn_state, total;
 };
 
 inline Plan make_plan(int B, int gamma, int V, int r, int H) {
@@ -77,15 +77,13 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_bias = o; o = align_up(o + (size_t)B * V * sizeof(float), 256);
   const size_t parts = (size_t)B * gamma * p.stats.splits + (size_t)B * p.ver.splits;
   p.off_part = o; o = align_up(o + parts * sizeof(RowState), 256);
-  p.off_M = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
-  p.off_lnS = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
-  p.off_p = o; o = align_up(o + (size_t)B * gamma * sizeof(float), 256);
   p.off_mode = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_pos = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_prev = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);   // by residual slot
   p.off_slot = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);   // slot of request b
   p.off_nres = o; o += 256;                                              // residual count
   p.off_fallback = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
+  p.off_rec = o; o = align_up(o + (size_t)B * 32, 256);                 // final-draw records
   // RNN head: state [2][B][r] fp32, then the current position's rows [B][2][r] bf16
   // RNN head: kRnnStateCopies copies of the state [2][B][r] fp32 and of the E rows [B][2][r] bf16
   p.off_rnn_state = o;

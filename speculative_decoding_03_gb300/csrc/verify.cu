@@ -12,7 +12,8 @@
 //                  sum of exp of T[b, k] over the segment (a partial, no cross-CTA merge)
 //   decide         one warp per request, one lane per position: merges the row partials
 //                  into M, log S and p_k(x_k), runs the acceptance tests, finds the first
-//                  reject, the accepted prefix, and which row the final token comes from
+//                  reject, the accepted prefix, and which row the final token comes from,
+//                  and writes the final draw's record (row, mode, log normalisers)
 //   bias_gemm      (shared with the draft) W1[x_{j-1}] W2 for the rows with a reject at j
 //   final_sample   Gumbel-max over log(P_j - Q_j) on {P_j > Q_j} (residual), or over
 //                  T[b, l+1] (bonus): one partial (best score, index) per segment
@@ -30,6 +31,16 @@ namespace dspark {
 namespace {
 
 enum : int { kModeNone = 0, kModeResidual = 1, kModeBonus = 2, kModePointResidual = 3 };
+
+// What the final draw of request b needs besides the rows it reads, written by the
+// decision kernel: the mode, the position k of the row drawn from (T[b, k - 1]), the
+// excluded token (greedy drafts' point residual, else -1), the residual's compact bias
+// slot, and its log normalisers (log P = T - off_a, log Q = z - off_b).  32 bytes, so the
+// final-sample kernel fetches it with two independent 16-byte loads.
+struct __align__(16) ItemRec {
+  int md, k, excl, slot;
+  float off_a, off_b, pad0, pad1;
+};
 
 __device__ __forceinline__ int clamp_ell(const int32_t* ell, int b, int gamma, int* err) {
   int L = ell[b];
@@ -179,11 +190,12 @@ __global__ void __launch_bounds__(128) decide_kernel(
     const float* __restrict__ T, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const float* __restrict__ q_tok,
     const float2* __restrict__ stats, int splits, const int32_t* __restrict__ ell, int B,
-    int gamma, int V, uint64_t seed, float* __restrict__ M_t, float* __restrict__ lnS_t,
-    float* __restrict__ p_t, int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
-    int32_t* __restrict__ n_out, int32_t* __restrict__ mode, int32_t* __restrict__ pos,
+    int gamma, int V, uint64_t seed, int32_t* __restrict__ accept_len,
+    int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_out, int32_t* __restrict__ mode,
+    int32_t* __restrict__ pos,
     int32_t* __restrict__ res_prev, int32_t* __restrict__ slot_of, int* __restrict__ n_res,
-    int32_t* __restrict__ fallback, int* err, int rnn_rows) {
+    int32_t* __restrict__ fallback, int* err, int rnn_rows, const float* __restrict__ row_max,
+    const float* __restrict__ row_sumexp, ItemRec* __restrict__ rec) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -192,6 +204,7 @@ __global__ void __launch_bounds__(128) decide_kernel(
   const int L = clamp_ell(ell, b, gamma, lane == 0 ? err : nullptr);
   const int k = lane + 1;
   bool reject = false;
+  float m_own = 0.f, lns_own = 0.f;      // this lane's row: M and log S
   if (k <= L) {
     const int row = b * gamma + (k - 1);
     // the token, its target logit and the row partials are independent loads: issue them
@@ -215,25 +228,34 @@ __global__ void __launch_bounds__(128) decide_kernel(
     } else {
       set_device_error(err, DSPARK_ERR_DEVICE_CHECK);
     }
-    M_t[row] = m;
-    lnS_t[row] = logf(s);
-    p_t[row] = p;
+    m_own = m;
+    lns_own = logf(s);
     const float u = u01(draw_block(seed, 0u, (uint32_t)k, (uint32_t)b, 1u).x);
     reject = q_tok ? !(u < p / q_tok[row]) : !(u < p);
   }
   const unsigned rej = __ballot_sync(0xffffffffu, reject);
   const int j = rej ? __ffs(rej) : 0;    // first rejected position, 0 if none
   const int acc = j ? j - 1 : L;
+  // the rejected row's target normalisers, from the lane that owns it
+  const float m_j = __shfl_sync(0xffffffffu, m_own, j ? j - 1 : 0);
+  const float lns_j = __shfl_sync(0xffffffffu, lns_own, j ? j - 1 : 0);
   for (int i = lane; i <= gamma; i += 32)
     out_tokens[(size_t)b * (gamma + 1) + i] = i < acc ? tokens[(size_t)b * gamma + i] : -1;
   if (lane == 0) {
     accept_len[b] = acc;
     n_out[b] = acc + 1;
     fallback[b] = 0;
+    ItemRec r;
+    r.excl = -1;
+    r.slot = 0;
+    r.off_a = r.off_b = r.pad0 = r.pad1 = 0.f;
     if (j && !q_tok) {
       mode[b] = kModePointResidual;
       pos[b] = j;
       slot_of[b] = -1;
+      r.md = kModePointResidual;
+      r.k = j;
+      r.excl = tokens[(size_t)b * gamma + (j - 1)];
     } else if (j) {
       mode[b] = kModeResidual;
       pos[b] = j;
@@ -243,11 +265,20 @@ __global__ void __launch_bounds__(128) decide_kernel(
       slot_of[b] = slot;
       res_prev[slot] = rnn_rows ? b * gamma + (j - 1)
                                 : ((j == 1) ? anchor[b] : tokens[(size_t)b * gamma + (j - 2)]);
+      const size_t o = (size_t)b * gamma + (j - 1);
+      r.md = kModeResidual;
+      r.k = j;
+      r.slot = slot;
+      r.off_a = m_j + lns_j;                          // log P = T - off_a
+      r.off_b = row_max[o] + logf(row_sumexp[o]);     // log Q = z - off_b
     } else {
       mode[b] = kModeBonus;
       pos[b] = L + 1;
       slot_of[b] = -1;
+      r.md = kModeBonus;
+      r.k = L + 1;
     }
+    rec[b] = r;
   }
 }
 
@@ -389,11 +420,8 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
 // one, so HBM latency overlaps the scoring.
 __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const float* __restrict__ T, const float* __restrict__ U, const float* __restrict__ bias,
-    const float* __restrict__ row_max, const float* __restrict__ row_sumexp,
-    const float* __restrict__ M_t, const float* __restrict__ lnS_t,
-    const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
-    const int32_t* __restrict__ slot_of, const int32_t* __restrict__ tokens, int B, int gamma,
-    int V, uint64_t seed, int splits, RowState* __restrict__ partials, int* err) {
+    const ItemRec* __restrict__ rec, int B, int gamma, int V, uint64_t seed, int splits,
+    RowState* __restrict__ partials, int* err) {
   extern __shared__ float4 fs_buf[];            // [2][3][kVerSeg / 4]
   __shared__ uint64_t full[2];
   __shared__ RowState red[32];
@@ -405,34 +433,28 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     fence_mbar_init_cta();
   }
   __syncthreads();
-  pdl_wait();                   // mode and pos come from the decision kernel
+  pdl_wait();                   // the records come from the decision kernel
   pdl_launch_dependents();
   const int n_items = B * splits, G = gridDim.x;
   constexpr int kSlot = kVerSeg / 4;            // float4 per array slot
-  // What an item needs besides its rows, loaded by thread 0 one item ahead of its copies and
-  // published with them (the expect-tx arrival releases the record): the mode, the row, the
-  // residual's log normalisers and the excluded token.
+  // An item's record (its request's, from the decision kernel) is loaded by thread 0 one
+  // item ahead of its copies, two independent loads used only at the next item, and
+  // published with the copies (the expect-tx arrival releases it).
   struct ItemMeta {
     int md, k, excl, slot;
     float off_a, off_b;
   };
   __shared__ ItemMeta meta_s[2];
   auto load_meta = [&](int item) -> ItemMeta {  // thread 0
+    const int4* src = reinterpret_cast<const int4*>(rec + item / splits);
+    const int4 a = __ldcg(src), c = __ldcg(src + 1);
     ItemMeta m;
-    const int b = item / splits;
-    m.md = mode[b];
-    m.k = pos[b];
-    m.excl = -1;
-    m.slot = 0;
-    m.off_a = m.off_b = 0.f;
-    if (m.md == kModeResidual) {
-      const size_t o = (size_t)b * gamma + (m.k - 1);
-      m.slot = slot_of[b];
-      m.off_b = row_max[o] + logf(row_sumexp[o]);   // log Q = z - off_b
-      m.off_a = M_t[o] + lnS_t[o];                  // log P = T - off_a
-    } else if (m.md == kModePointResidual) {
-      m.excl = tokens[(size_t)b * gamma + (m.k - 1)];
-    }
+    m.md = a.x;
+    m.k = a.y;
+    m.excl = a.z;
+    m.slot = a.w;
+    m.off_a = __int_as_float(c.x);
+    m.off_b = __int_as_float(c.y);
     return m;
   };
   auto issue = [&](int item, int buf, const ItemMeta& m) {   // thread 0
@@ -588,24 +610,22 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   RowState* part = ws_at<RowState>(ws, p.off_part);
   float2* part_stats = reinterpret_cast<float2*>(part);
   RowState* part_ver = part + (size_t)B * gamma * p.stats.splits;
-  float* M_t = ws_at<float>(ws, p.off_M);
-  float* lnS_t = ws_at<float>(ws, p.off_lnS);
-  float* p_t = ws_at<float>(ws, p.off_p);
   int32_t* mode = ws_at<int32_t>(ws, p.off_mode);
   int32_t* pos = ws_at<int32_t>(ws, p.off_pos);
   int32_t* res_prev = ws_at<int32_t>(ws, p.off_prev);
   int32_t* slot_of = ws_at<int32_t>(ws, p.off_slot);
   int* n_res = ws_at<int>(ws, p.off_nres);
   int32_t* fb = ws_at<int32_t>(ws, p.off_fallback);
+  ItemRec* rec = ws_at<ItemRec>(ws, p.off_rec);
 
   cudaError_t e = launch_pdl(target_stats_kernel, dim3(p.stats.splits, B * gamma < 65535 ? B * gamma : 65535),
                              dim3(kSampleThreads), 0, stream, T, ell, B, gamma, V,
                              p.stats.splits, part_stats, n_res);
   if (e != cudaSuccess) return e;
   e = launch_pdl(decide_kernel, dim3(cdiv(B, 4)), dim3(128), 0, stream, T, anchor, tokens, q_tok,
-                 (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, M_t, lnS_t,
-                 p_t, accept_len, out_tokens, n_out, mode, pos, res_prev, slot_of, n_res, fb,
-                 err, E_all ? 1 : 0);
+                 (const float2*)part_stats, p.stats.splits, ell, B, gamma, V, seed, accept_len,
+                 out_tokens, n_out, mode, pos, res_prev, slot_of, n_res, fb,
+                 err, E_all ? 1 : 0, row_max, row_sumexp, rec);
   if (e != cudaSuccess) return e;
   if (!point_mass) {
     // only the rejected requests' rows, in the slots the decision kernel gave them
@@ -615,10 +635,8 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
     if (e != cudaSuccess) return e;
   }
   e = launch_pdl(final_sample_kernel, dim3(final_sample_grid(B * p.ver.splits)),
-                 dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias, row_max,
-                 row_sumexp, (const float*)M_t, (const float*)lnS_t, (const int32_t*)mode,
-                 (const int32_t*)pos, (const int32_t*)slot_of, tokens, B, gamma, V, seed,
-                 p.ver.splits, part_ver, err);
+                 dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias,
+                 (const ItemRec*)rec, B, gamma, V, seed, p.ver.splits, part_ver, err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(finalize_kernel, dim3(B), dim3(kSampleThreads), 0, stream, T,
                  (const RowState*)part_ver, p.ver.splits, gamma, V, seed, (const int32_t*)mode,
