@@ -523,7 +523,13 @@ def run_ours(args, w):
     pipe.run([w.seed + i for i in range(n_e2e)], [hin] * n_e2e, [hout] * n_e2e)
     torch.cuda.current_stream().synchronize()
     e2e_s = (time.perf_counter() - t0) / n_e2e
-    h2d, d2h = step.step_bytes()
+    # bytes per step: the copied inputs, the target rows each step fetched (its
+    # sum_b (l_b + 1), replayed here on the same inputs and seeds) and the tokens back
+    rows = []
+    for i in range(n_e2e):
+        step.first_launch(w.seed + i)
+        rows.append(int(step.sched_out[1].item()))
+    h2d, d2h = step.step_bytes(B_total=float(np.mean(rows)))
 
     # the other workloads, each measured the same way on every replica (barriers included)
     per_workload = {}

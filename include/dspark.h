@@ -420,6 +420,24 @@ dspark_status dspark_draft_confidence_schedule(
  */
 void dspark_testing_set_wait_limit(long long wait_cycles, int unreachable_barrier);
 
+/*
+ * The rows of the target logits that a verification reads under the schedule ell, copied
+ * from T_src into T (both [B][gamma + 1][V] fp32, 16-byte aligned): T[b, j] for
+ * 0 <= j <= ell[b], the verified positions' rows and the row the final token is drawn
+ * from (billytse.dev DSpark page, section 1: the target scores the scheduled prefix; the
+ * later rows are never read).  T_src may be host memory that the device reads directly
+ * (pinned or registered with CUDA, or pageable memory on systems whose GPU reads it): a
+ * kernel fetches the rows over the host link, so a step whose target logits arrive in host
+ * memory moves only the rows it verifies; device memory works too.  The other rows of T
+ * are left as they are.  ell (device, B entries) is the scheduler's output; an entry
+ * outside [0, gamma] is clamped and reported as DSPARK_ERR_DEVICE_CHECK through the status
+ * word of `workspace` (any workspace of this library; only its status word is used, so 256
+ * bytes suffice).  DSPARK_ERR_INVALID_ARG when T_src is host memory the device cannot read.
+ */
+dspark_status dspark_copy_target_rows(const float* T_src, float* T, const int32_t* ell, int B,
+                                      int gamma, int V, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,6 +58,7 @@ SIGNATURES = [
     ("dspark_draft_confidence_schedule", _I, [_P, _P, _P, _P, _P, _P, _F, _P, _I, _I, _I, _I, _I, _I,
                                               _U64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     ("dspark_testing_set_wait_limit", None, [ctypes.c_longlong, _I]),
+    ("dspark_copy_target_rows", _I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
 ]
 
 _lib = None
@@ -268,6 +269,17 @@ def draft_confidence_schedule(U, W1, W2p, anchor, h, w_c, b_c: float, sps, seed:
         _ptr(draft_out["row_sumexp"]), _ptr(c), _ptr(a), _ptr(ell), _ptr(Bt), _ptr(th),
         ctypes.c_void_p(ws.ptr), ws.nbytes, _stream(stream)))
     return draft_out, (c, a), (ell, Bt, th)
+
+
+def copy_target_rows(T_src, T, ell, ws: Workspace, stream=None):
+    """T[b, j] for j <= ell[b] (the rows a verification under schedule ell reads) from
+    T_src into the device tensor T ([B, gamma + 1, V] fp32 both).  T_src may be a pinned
+    host tensor: a kernel reads the rows over the host link."""
+    B, g1, V = T.shape
+    _check("dspark_copy_target_rows", lib().dspark_copy_target_rows(
+        _ptr(T_src), _ptr(T), _ptr(ell), B, g1 - 1, V, ctypes.c_void_p(ws.ptr), ws.nbytes,
+        _stream(stream)))
+    return T
 
 
 def schedule(a, sps, ws: Workspace, out=None, stream=None):
@@ -532,12 +544,17 @@ class Step:
             self.hp = torch.empty((B, gamma, 3 * r), dtype=f32, device=d)
             self.draft_out["E"] = torch.empty((B, gamma, r), dtype=f32, device=d)
 
-    def run(self, seed: int, stream=None, t: int = 0):
+    def run(self, seed: int, stream=None, t: int = 0, T_host=None):
+        """One step.  T_host: the step's target logits in host memory (pinned); then only
+        the rows the verification reads (T[b, j], j <= l_b) are fetched into dev["T"], once
+        the schedule is known."""
         x = self.dev
         B, gamma = x["U"].shape[:2]
         if self.fused:
             # draft, confidence, survival and schedule in one launch, then verification
             d, (ell, _, _) = self.first_launch(seed, stream)
+            if T_host is not None:
+                copy_target_rows(T_host, x["T"], ell, self.ws, stream)
             verify_packed(x["T"], x["U"], x["W1"], self.W2p, x["anchor"], d["tokens"], d["q_tok"],
                           d["row_max"], d["row_sumexp"], ell, seed, self.ws, self.verify_out, stream)
             return self
@@ -551,6 +568,8 @@ class Step:
             c, a = confidence(x["h"], x["anchor"], d["tokens"], x["W1"], x["w_c"], self.b_c, self.ws,
                               self.conf_out, stream)
             ell = self._schedule(a, stream, t)
+        if T_host is not None:
+            copy_target_rows(T_host, x["T"], ell, self.ws, stream)
         if self.sampling == "greedy":
             verify_greedy(x["T"], d["tokens"], ell, seed, self.ws, self.verify_out, stream)
         elif self.head == "rnn":
@@ -624,8 +643,11 @@ class Step:
         return graphs
 
     # per-step inputs (the backbone's and the target's outputs); the weights, the
-    # confidence head and the SPS table stay resident on the device
+    # confidence head and the SPS table stay resident on the device.  The target logits T
+    # are fetched row by row by the step itself (only the rows it verifies); the others
+    # are copied whole.
     STEP_INPUTS = ("U", "T", "h", "anchor")
+    COPIED_INPUTS = ("U", "h", "anchor")
     STEP_OUTPUTS = ("out_tokens", "accept_len", "n_out")
 
     def pinned_host_buffers(self):
@@ -643,9 +665,9 @@ class Step:
         torch = _torch()
         s = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(s):
-            for k in self.STEP_INPUTS:
+            for k in self.COPIED_INPUTS:
                 self.dev[k].copy_(host_in[k], non_blocking=True)
-            self.run(seed, s)
+            self.run(seed, s, T_host=host_in["T"])
             for k in self.STEP_OUTPUTS:
                 host_out[k].copy_(self.verify_out[k], non_blocking=True)
         return host_out
@@ -654,9 +676,13 @@ class Step:
         """A HostPipeline over this step (see there)."""
         return HostPipeline(self)
 
-    def step_bytes(self):
-        """(host->device, device->host) bytes of one run_from_host call."""
-        h2d = sum(self.dev[k].numel() * self.dev[k].element_size() for k in self.STEP_INPUTS)
+    def step_bytes(self, B_total: Optional[float] = None):
+        """(host->device, device->host) bytes of one run_from_host call: the copied inputs,
+        plus the target rows fetched, B_total = sum_b (l_b + 1) rows of V fp32 (all
+        B (gamma + 1) rows when B_total is None)."""
+        h2d = sum(self.dev[k].numel() * self.dev[k].element_size() for k in self.COPIED_INPUTS)
+        B, g1, V = self.dev["T"].shape
+        h2d += (B * g1 if B_total is None else B_total) * V * self.dev["T"].element_size()
         d2h = sum(self.verify_out[k].numel() * self.verify_out[k].element_size() for k in self.STEP_OUTPUTS)
         return int(h2d), int(d2h)
 
@@ -678,11 +704,13 @@ class HostPipeline:
     overlapped with the current step's kernels.
 
     The step's per-step inputs get a second device copy; step i reads input set i % 2,
-    whose copies run on a separate copy stream and are ordered before the step by an
-    event, and step i + 2's copies into the same set wait for an event recorded after
-    step i's kernels.  Every step's inputs are still copied from the host and every
-    step's verified tokens are copied back, on the step's stream.  The step object is
-    given its own dictionary of device tensors, so the caller's dictionary is unchanged.
+    whose copies (U, h, anchor) run on a separate copy stream and are ordered before the
+    step by an event, and step i + 2's copies into the same set wait for an event recorded
+    after step i's kernels.  The target logits stay in host memory: step i fetches the
+    rows it verifies into its set once its schedule is known (Step.run with T_host).  Every
+    step's inputs still come from the host and every step's verified tokens are copied
+    back, on the step's stream.  The step object is given its own dictionary of device
+    tensors, so the caller's dictionary is unchanged.
     """
 
     def __init__(self, step: "Step"):
@@ -701,8 +729,8 @@ class HostPipeline:
         b = i % 2
         with torch.cuda.stream(self.copy_stream):
             self.copy_stream.wait_event(self.free[b])
-            for k, v in self.sets[b].items():
-                v.copy_(host_in[k], non_blocking=True)
+            for k in self.step.COPIED_INPUTS:
+                self.sets[b][k].copy_(host_in[k], non_blocking=True)
             self.ready[b].record(self.copy_stream)
 
     def run(self, seeds, host_ins, host_outs, stream=None):
@@ -721,7 +749,7 @@ class HostPipeline:
             b = i % 2
             s.wait_event(self.ready[b])
             self.step.dev.update(self.sets[b])
-            self.step.run(seeds[i], s, t=i)
+            self.step.run(seeds[i], s, t=i, T_host=host_ins[i]["T"])
             self.free[b].record(s)
             with torch.cuda.stream(s):
                 for k in self.step.STEP_OUTPUTS:

@@ -391,4 +391,32 @@ void dspark_testing_set_wait_limit(long long wait_cycles, int unreachable_barrie
   set_draft_wait_limit(wait_cycles > 0 ? wait_cycles : 0, unreachable_barrier ? (1u << 30) : 0u);
 }
 
+dspark_status dspark_copy_target_rows(const float* T_src, float* T, const int32_t* ell, int B,
+                                      int gamma, int V, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
+  dspark_status st = check_shape(B, gamma, V, 16, 0);
+  if (st != DSPARK_OK) return st;
+  if (!aligned(T_src, 16) || !aligned(T, 16) || !aligned(ell, 4) || !aligned(workspace, 256) ||
+      workspace_bytes < 256)
+    return DSPARK_ERR_INVALID_ARG;
+  // the source must be memory the device reads: device or managed memory, host memory
+  // pinned or registered with CUDA, or pageable host memory where the device reads it
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, T_src) != cudaSuccess) {
+    cudaGetLastError();
+    return DSPARK_ERR_INVALID_ARG;
+  }
+  if (attr.type == cudaMemoryTypeUnregistered) {
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess ||
+        !pageable)
+      return DSPARK_ERR_INVALID_ARG;
+  }
+  if (launch_copy_target_rows(T_src, T, ell, B, gamma, V, ws_at<int>(workspace, 0), stream) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
 }  // extern "C"

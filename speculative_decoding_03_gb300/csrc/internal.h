@@ -256,6 +256,10 @@ cudaError_t launch_schedule(const float* a, int R, int gamma, const float* sps,
 cudaError_t launch_schedule_threshold(const float* a, int R, int gamma, float threshold,
                                       int32_t* ell, int32_t* B_total, cudaStream_t stream);
 
+// T[b, j] for j <= ell[b] from T_src (memory the device reads, host memory included) into T
+cudaError_t launch_copy_target_rows(const float* T_src, float* T, const int32_t* ell, int B,
+                                    int gamma, int V, int* err, cudaStream_t stream);
+
 // E_all (null for the Markov head): the RNN head's output rows [B][gamma][r] of the draft
 cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const uint16_t* W1,
                           const uint16_t* W2, const uint16_t* W2p, const float* E_all,

@@ -93,6 +93,17 @@ def test_verify_confidence_and_bias_validation():
     assert L.dspark_markov_bias(FAKE, FAKE, FAKE, 1, 4, 1000, 16, FAKE, None, 1 << 20, None) == INVALID
 
 
+def test_copy_target_rows_validation():
+    L = ds.lib()
+    # null source, misaligned destination, workspace without a status word, bad shapes
+    assert L.dspark_copy_target_rows(None, FAKE, FAKE, 4, 4, 1000, FAKE, 256, None) == INVALID
+    assert L.dspark_copy_target_rows(FAKE, FAKE + 4, FAKE, 4, 4, 1000, FAKE, 256, None) == INVALID
+    assert L.dspark_copy_target_rows(FAKE, FAKE, FAKE, 4, 4, 1000, FAKE, 128, None) == INVALID
+    assert L.dspark_copy_target_rows(FAKE, FAKE, FAKE, 0, 4, 1000, FAKE, 256, None) == INVALID
+    assert L.dspark_copy_target_rows(FAKE, FAKE, FAKE, 4, 33, 1000, FAKE, 256, None) == UNSUPPORTED
+    assert L.dspark_copy_target_rows(FAKE, FAKE, FAKE, 4, 4, 1004, FAKE, 256, None) == UNSUPPORTED
+
+
 def _compile(compiler, std, source, extra=()):
     import shutil
     import subprocess
