@@ -45,8 +45,6 @@ __device__ __forceinline__ void named_bar_sync_n(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-constexpr int kBiasWarps = 6;                 // producer, MMA, 4 epilogue warps
-constexpr int kBiasThreads = kBiasWarps * 32;
 constexpr int kBiasStages = 4;                // W2 K-chunk ring (16 KB each at 64 rows)
 constexpr int kBiasDepth = 4;                 // accumulators in tensor memory
 constexpr int kBiasKChunkMax = 64;
@@ -63,6 +61,12 @@ struct BiasSmem {
   static constexpr int kEBufs = NB == 256 ? 1 : 2;
   static constexpr int kDepth = NB == 256 ? 2 : kBiasDepth;
   static constexpr int kBytes = kOffE + kEBufs * kEBytes;
+  // warps: producer, MMA, then the epilogue warps, one per tensor-memory lane quarter and
+  // column half of a 256-row pass (eight: a pass's 256 x 128 fp32 results per tile and its
+  // operand gather take two warps per quarter), one per quarter otherwise
+  static constexpr int kEpiWarps = NB == 256 ? 8 : 4;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kEpiThreads = kEpiWarps * 32;
 };
 
 __device__ __forceinline__ uint32_t bf16_bits_rne(float x) {
@@ -71,7 +75,7 @@ __device__ __forceinline__ uint32_t bf16_bits_rne(float x) {
 }
 
 template <int NB, bool Split>
-__global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
+__global__ void __launch_bounds__(BiasSmem<NB, Split>::kThreads) bias_gemm_kernel(
     const __grid_constant__ CUtensorMap w2_map, const uint16_t* __restrict__ W2p,
     const uint16_t* __restrict__ W1, const float* __restrict__ Ef, int table_rows,
     const int32_t* __restrict__ prev, int prev_stride, int B, const int* __restrict__ n_rows,
@@ -101,7 +105,10 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
   if (threadIdx.x == 0) {
     for (int i = 0; i < kBiasStages; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 1); }
     for (int i = 0; i < S::kEBufs; ++i) { mbar_init(&e_full[i], 1); mbar_init(&e_empty[i], 1); }
-    for (int i = 0; i < S::kDepth; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+    for (int i = 0; i < S::kDepth; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], S::kEpiWarps);
+    }
     mbar_init(&mma_drain, 1);
     mbar_init(&count_ready, 1);
     abort_s = 0;
@@ -229,8 +236,10 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
     // --------------------------------------------- epilogue: E gather, TMEM -> bias rows
     pdl_wait();                 // prev (and the row count) may come from the previous kernel
     pdl_launch_dependents();
-    const int et = threadIdx.x - 64;              // 0 .. 127
+    constexpr int kEpiT = S::kEpiThreads;
+    const int et = threadIdx.x - 64;              // 0 .. kEpiT - 1
     const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;             // column half (eight epilogue warps)
     const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
     const int kchunks = r >> 3;                   // 16-byte chunks per W1 row
     if (et == 0) {
@@ -243,7 +252,7 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
       jobs_s = rows > NB ? (rows + NB - 1) / NB : 1;
       mbar_arrive(&count_ready);                  // release: rows_s and jobs_s first
     }
-    named_bar_sync_n(kBiasNamedBar, 128);
+    named_bar_sync_n(kBiasNamedBar, kEpiT);
     const int rows = *(volatile int*)&rows_s;
     const int n_jobs = *(volatile int*)&jobs_s;
     uint32_t tc = 0;
@@ -253,11 +262,11 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
       // E = W1[prev_b] as the K-major, 128-byte-swizzled B operand: 16-byte chunk c of row n
       // goes to chunk (c % 8) ^ (n % 8) of line n of K-block c / 8
       if (et == 0) wait1(&e_empty[eb], ((job / S::kEBufs) & 1) ^ 1);
-      named_bar_sync_n(kBiasNamedBar, 128);
+      named_bar_sync_n(kBiasNamedBar, kEpiT);
       uint8_t* sE = smem + S::kOffE + eb * S::kEBytes;
       // the pass's predecessor rows, once (checked here), then the operand rows; a 256-row
       // pass keeps four 16-byte loads in flight per thread (measured: one is best at 128)
-      for (int n = et; n < NB; n += 128) {
+      for (int n = et; n < NB; n += kEpiT) {
         const int b = b0 + n;
         int pv = -1;
         if (b < rows) {
@@ -269,14 +278,14 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
         }
         pv_s[n] = pv;
       }
-      named_bar_sync_n(kBiasNamedBar, 128);
+      named_bar_sync_n(kBiasNamedBar, kEpiT);
       if (!*(volatile int*)&abort_s) {
         constexpr int kBatch = NB == 256 ? 4 : 1;
-        for (int idx0 = et; idx0 < NB * kchunks; idx0 += 128 * kBatch) {
+        for (int idx0 = et; idx0 < NB * kchunks; idx0 += kEpiT * kBatch) {
           uint4 val[kBatch], lo[kBatch];
 #pragma unroll
           for (int u = 0; u < kBatch; ++u) {
-            const int idx = idx0 + 128 * u;
+            const int idx = idx0 + kEpiT * u;
             val[u] = make_uint4(0u, 0u, 0u, 0u);
             lo[u] = val[u];
             if (idx < NB * kchunks) {
@@ -305,7 +314,7 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
           }
 #pragma unroll
           for (int u = 0; u < kBatch; ++u) {
-            const int idx = idx0 + 128 * u;
+            const int idx = idx0 + kEpiT * u;
             if (idx < NB * kchunks) {
               const int n = idx / kchunks, c = idx - n * kchunks;
               const size_t off = (size_t)(c >> 3) * NB * 128 + (size_t)n * 128 + (((c & 7) ^ (n & 7)) << 4);
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync_n(kBiasNamedBar, 128);
+      named_bar_sync_n(kBiasNamedBar, kEpiT);
       if (et == 0) mbar_arrive(&e_full[eb]);
       for (int t = 0; t < my_tiles; ++t, ++tc) {
         const int ab = tc % S::kDepth;
@@ -324,15 +333,47 @@ __global__ void __launch_bounds__(kBiasThreads) bias_gemm_kernel(
         if (!__all_sync(0xffffffffu, ok)) continue;
         tc_fence_after_sync();
         const int v = (t_lo + t) * kGemmTileV + q * 32 + lane;
-        // 16 columns (rows b) at a time; the accumulator is released after the last
-#pragma unroll 1
-        for (int c16 = 0; c16 < NB && b0 + c16 < rows; c16 += 16) {
-          uint32_t vals[16];
-          tmem_ld_32x32b_sync<16>(trow + (uint32_t)(ab * NB + c16), vals);
+        // this warp's columns (rows b) 16 at a time (in a 256-row pass the next 16 load from
+        // tensor memory while the current ones are stored); the accumulator is released
+        // after the last
+        constexpr int kCols = NB / (S::kEpiWarps / 4);
+        const int c_beg = half * kCols;
+        const int c_end = min(c_beg + kCols, rows - b0);
+        const uint32_t tacc = trow + (uint32_t)(ab * NB);
+        auto store16 = [&](const uint32_t (&vals)[16], int c) {
           if (v < V) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (b0 + c16 + j < rows) out[(size_t)(b0 + c16 + j) * V + v] = __uint_as_float(vals[j]);
+              if (b0 + c + j < rows) out[(size_t)(b0 + c + j) * V + v] = __uint_as_float(vals[j]);
+          }
+        };
+        if constexpr (NB < 256) {
+          // (one column run per quarter: 16 columns at a time, each load waited for)
+#pragma unroll 1
+          for (int c = 0; c < NB && b0 + c < rows; c += 16) {
+            uint32_t vals[16];
+            tmem_ld_32x32b_sync<16>(tacc + (uint32_t)c, vals);
+            if (v < V) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (b0 + c + j < rows) out[(size_t)(b0 + c + j) * V + v] = __uint_as_float(vals[j]);
+            }
+          }
+        } else if (c_beg < c_end) {
+          uint32_t va[16], vb[16];
+          tmem_ld_32x32b_x16_async(tacc + (uint32_t)c_beg, va);
+          tmem_ld_wait();
+#pragma unroll 1
+          for (int c = c_beg; c < c_end; c += 32) {
+            const bool more = c + 16 < c_end, more2 = c + 32 < c_end;
+            if (more) tmem_ld_32x32b_x16_async(tacc + (uint32_t)(c + 16), vb);
+            store16(va, c);
+            if (more) {
+              tmem_ld_wait();
+              if (more2) tmem_ld_32x32b_x16_async(tacc + (uint32_t)(c + 32), va);
+              store16(vb, c + 16);
+              if (more2) tmem_ld_wait();
+            }
           }
         }
         tc_fence_before_sync();
@@ -354,7 +395,8 @@ int bias_grid(int n_tiles) {
     const size_t smem = BiasSmem<NB, Split>::kBytes + 1024;
     if (cudaFuncSetAttribute(bias_gemm_kernel<NB, Split>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_gemm_kernel<NB, Split>, kBiasThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_gemm_kernel<NB, Split>,
+                                                      BiasSmem<NB, Split>::kThreads,
                                                       smem) != cudaSuccess)
       return -1;
     return per;
@@ -400,7 +442,7 @@ cudaError_t launch_bias_nb(const CUtensorMap& w2_map, const uint16_t* W2p, const
                            int* err, cudaStream_t stream) {
   const int grid = bias_grid<NB, Split>(n_tiles);
   if (grid <= 0) return cudaErrorInvalidConfiguration;
-  return launch_pdl(bias_gemm_kernel<NB, Split>, dim3(grid), dim3(kBiasThreads),
+  return launch_pdl(bias_gemm_kernel<NB, Split>, dim3(grid), dim3(BiasSmem<NB, Split>::kThreads),
                     (size_t)BiasSmem<NB, Split>::kBytes + 1024, stream, w2_map, W2p, W1, Ef,
                     table_rows, prev, prev_stride, B, n_rows, V, r, kc, n_tiles, out, err);
 }
