@@ -62,9 +62,9 @@ struct BiasSmem {
   static constexpr int kDepth = NB == 256 ? 2 : kBiasDepth;
   static constexpr int kBytes = kOffE + kEBufs * kEBytes;
   // warps: producer, MMA, then the epilogue warps, one per tensor-memory lane quarter and
-  // column half of a 256-row pass (eight: a pass's 256 x 128 fp32 results per tile and its
-  // operand gather take two warps per quarter), one per quarter otherwise
-  static constexpr int kEpiWarps = NB == 256 ? 8 : 4;
+  // column half of a pass of 128 or 256 rows (eight: such a pass's fp32 results per tile
+  // and its operand gather take two warps per quarter), one per quarter otherwise
+  static constexpr int kEpiWarps = NB >= 128 ? 8 : 4;
   static constexpr int kThreads = (2 + kEpiWarps) * 32;
   static constexpr int kEpiThreads = kEpiWarps * 32;
 };
@@ -333,9 +333,9 @@ __global__ void __launch_bounds__(BiasSmem<NB, Split>::kThreads) bias_gemm_kerne
         if (!__all_sync(0xffffffffu, ok)) continue;
         tc_fence_after_sync();
         const int v = (t_lo + t) * kGemmTileV + q * 32 + lane;
-        // this warp's columns (rows b) 16 at a time (in a 256-row pass the next 16 load from
-        // tensor memory while the current ones are stored); the accumulator is released
-        // after the last
+        // this warp's columns (rows b) 16 at a time (in a pass of 128 or more rows the next 16
+        // load from tensor memory while the current ones are stored); the accumulator is
+        // released after the last
         constexpr int kCols = NB / (S::kEpiWarps / 4);
         const int c_beg = half * kCols;
         const int c_end = min(c_beg + kCols, rows - b0);
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(BiasSmem<NB, Split>::kThreads) bias_gemm_kerne
               if (b0 + c + j < rows) out[(size_t)(b0 + c + j) * V + v] = __uint_as_float(vals[j]);
           }
         };
-        if constexpr (NB < 256) {
+        if constexpr (NB < 128) {
           // (one column run per quarter: 16 columns at a time, each load waited for)
 #pragma unroll 1
           for (int c = 0; c < NB && b0 + c < rows; c += 16) {
