@@ -63,7 +63,8 @@ struct Plan {
   RowSplit stats, ver;
   // byte offsets into the workspace
   size_t off_err, off_draft, off_bias, off_part, off_mode,
-      off_pos, off_prev, off_slot, off_nres, off_fallback, off_rec, off_rnn_state, total;
+      off_pos, off_prev, off_slot, off_nres, off_fallback, off_rec, off_cand_n, off_cand,
+      off_rnn_state, total;
 };
 
 inline Plan make_plan(int B, int gamma, int V, int r, int H) {
@@ -75,7 +76,7 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_err = o; o += 256;
   p.off_draft = o; o = align_up(o + draft_region_bytes(B, gamma), 256);
   p.off_bias = o; o = align_up(o + (size_t)B * V * sizeof(float), 256);
-  const size_t parts = (size_t)B * gamma * p.stats.splits + (size_t)B * p.ver.splits;
+  const size_t parts = (size_t)B * gamma * p.stats.splits;
   p.off_part = o; o = align_up(o + parts * sizeof(RowState), 256);
   p.off_mode = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_pos = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
@@ -84,6 +85,9 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_nres = o; o += 256;                                              // residual count
   p.off_fallback = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_rec = o; o = align_up(o + (size_t)B * 32, 256);                 // final-draw records
+  // the final draw's candidates: a count and up to 64 entries of 16 bytes per segment
+  p.off_cand_n = o; o = align_up(o + (size_t)B * p.ver.splits * sizeof(int), 256);
+  p.off_cand = o; o = align_up(o + (size_t)B * p.ver.splits * 64 * 16, 256);
   // RNN head: state [2][B][r] fp32, then the current position's rows [B][2][r] bf16
   // RNN head: kRnnStateCopies copies of the state [2][B][r] fp32 and of the E rows [B][2][r] bf16
   p.off_rnn_state = o;

@@ -51,16 +51,6 @@ __device__ __forceinline__ int clamp_ell(const int32_t* ell, int b, int gamma, i
   return L;
 }
 
-__device__ __forceinline__ RowState load_partial(const RowState* src) {
-  RowState q;
-  q.m = __ldcg(&src->m);
-  q.s = __ldcg(&src->s);
-  q.score = __ldcg(&src->score);
-  q.z = __ldcg(&src->z);
-  q.idx = __ldcg(&src->idx);
-  return q;
-}
-
 // mbarrier and 1-D bulk copy (global -> shared, completing on an mbarrier)
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -113,13 +103,6 @@ __device__ __forceinline__ float rcp_approx_ftz(float x) {
 // Gumbel value of the 32-bit draw x: g = -log(-log1p(-w)), w = 1 - U01(x).
 __device__ __forceinline__ float gumbel_of(uint32_t x) {
   return -logf(exp1_from_w(one_minus_u01(x)));
-}
-
-// (one warp; every lane gets the merged state)
-__device__ __forceinline__ RowState merge_partials(const RowState* base, int splits) {
-  RowState acc = row_state_empty();
-  for (int i = threadIdx.x & 31; i < splits; i += 32) acc = row_state_merge(acc, load_partial(base + i));
-  return row_state_warp_reduce(acc);
 }
 
 // ---------------------------------------------------------------------- target stats
@@ -307,16 +290,43 @@ __device__ __forceinline__ float block_max_f(float x, float* red) {
   return x;
 }
 
+// A logit of a segment that the exponential race keeps (its upper bound reaches the
+// segment's best lower bound): index, target logit, draft logit z (residual rows) and the
+// draw's w = 1 - u.  A segment hands up to kCandMax of them to the finalize kernel, which
+// scores them exactly; a segment with more scores them itself.
+struct __align__(16) Cand {
+  int idx;
+  float t, z, w;
+};
+constexpr int kCandMax = 64;
+
+// The exact race score of one logit, the unfiltered scan's fp32 formula: residual rows
+// log(P - Q) - log E = log Q + log(expm1(log P - log Q)) - log E (for log P - log Q > 20 it
+// is log P to within 2e-9), else T - log E; E = -log1p(-w) from the draw's w.
+__device__ __forceinline__ float exact_score(bool residual, float t, float z, float w, float off_a,
+                                             float off_b) {
+  if (residual) {
+    const float lq = z - off_b;
+    const float d = (t - off_a) - lq;          // log(P / Q) > 0
+    const float lres = d > 20.f ? lq + d : lq + logf(expm1f(d));
+    return lres - logf(exp1_from_w(w));
+  }
+  return t - logf(exp1_from_w(w));
+}
+
 // One CTA scores one segment of kVerSeg logits of one row: t / zz hold this thread's
 // kVerVec float4 of T and of z = U + bias (residual rows only), v0 the first vocabulary
 // index of the thread's first float4.  Not residual: the race over T alone with random
-// stream `stream`, skipping index `excl` (-1: none).  Every thread of the CTA calls it;
-// returns the CTA's best (score, index) in every thread.
-__device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
-                                                 const float4 (&zz)[kVerVec], int v0, int V,
-                                                 bool residual, float off_a, float off_b,
-                                                 uint32_t stream, int excl, uint64_t seed,
-                                                 int k, int b, RowState* red, float* redf) {
+// stream `stream`, skipping index `excl` (-1: none).  Every thread of the CTA calls it.
+// The segment's candidates go to cand_s (their count to *cnt_s, zero on entry); returns
+// their count, or, when they do not fit, -1 with the CTA's best (score, index), which the
+// CTA then scored itself, in `best` (every thread).
+__device__ __forceinline__ int race_segment(const float4 (&t)[kVerVec],
+                                            const float4 (&zz)[kVerVec], int v0, int V,
+                                            bool residual, float off_a, float off_b,
+                                            uint32_t stream, int excl, uint64_t seed, int k,
+                                            int b, RowState* red, float* redf, Cand* cand_s,
+                                            int* cnt_s, RowState& best) {
   if (!residual) {
     // bonus: reference = the CTA's largest logit (exp(T - m) <= 1)
     float m = -INFINITY;
@@ -359,13 +369,14 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
     }
   }
   const float L = block_max_f(Lt, redf);
-  // phase 2: exact scores of the logits whose upper bound reaches L
-  RowState st = row_state_empty();
+  // phase 2: the logits whose upper bound reaches L into the shared candidate list
+  unsigned cms[kVerVec];
 #pragma unroll
   for (int j = 0; j < kVerVec; ++j) {
     unsigned cm = 0u;
 #pragma unroll
     for (int i = 0; i < 4; ++i) cm |= (r_hi[j][i] >= 0.f && r_hi[j][i] >= L * w[j][i] ? 1u : 0u) << i;
+    cms[j] = cm;
     if (cm == 0u) continue;
     const int v = v0 + j * 4 * kSampleThreads;
     const float tv[4] = {t[j].x, t[j].y, t[j].z, t[j].w};
@@ -373,17 +384,33 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       if (!((cm >> i) & 1u)) continue;
-      float score;
-      if (residual) {
-        const float lq = zv[i] - off_b;
-        const float d = (tv[i] - off_a) - lq;          // log(P / Q) > 0
-        // log(P - Q) = log Q + log(expm1(log P - log Q)), accurate when P ~ Q; for
-        // d > 20 it is log P to within 2e-9
-        const float lres = d > 20.f ? lq + d : lq + logf(expm1f(d));
-        score = lres - logf(exp1_from_w(w[j][i]));   // g = -log E, from phase 1's w
-      } else {
-        score = tv[i] - logf(exp1_from_w(w[j][i]));
+      const int slot = atomicAdd(cnt_s, 1);
+      if (slot < kCandMax) {
+        Cand c;
+        c.idx = v + i;
+        c.t = tv[i];
+        c.z = zv[i];
+        c.w = w[j][i];
+        cand_s[slot] = c;
       }
+    }
+  }
+  __syncthreads();
+  const int n = *(volatile int*)cnt_s;
+  if (n <= kCandMax) return n;
+  // more candidates than the list holds (rare): score them here
+  RowState st = row_state_empty();
+#pragma unroll
+  for (int j = 0; j < kVerVec; ++j) {
+    const unsigned cm = cms[j];
+    if (cm == 0u) continue;
+    const int v = v0 + j * 4 * kSampleThreads;
+    const float tv[4] = {t[j].x, t[j].y, t[j].z, t[j].w};
+    const float zv[4] = {zz[j].x, zz[j].y, zz[j].z, zz[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (!((cm >> i) & 1u)) continue;
+      const float score = exact_score(residual, tv[i], zv[i], w[j][i], off_a, off_b);
       if (better(score, v + i, st.score, st.idx)) {
         st.score = score;
         st.idx = v + i;
@@ -408,22 +435,26 @@ __device__ __forceinline__ RowState race_segment(const float4 (&t)[kVerVec],
   for (int wi = 1; wi < kSampleThreads / 32; ++wi)
     if (better(red[wi].score, red[wi].idx, sc, ix)) { sc = red[wi].score; ix = red[wi].idx; }
   __syncthreads();
-  RowState out = row_state_empty();
-  out.score = sc;
-  out.idx = ix;
-  return out;
+  best = row_state_empty();
+  best.score = sc;
+  best.idx = ix;
+  return -1;
 }
 
 // Persistent: CTA g scores the segments (b, seg) = items g, g + G, ... (item = b * splits +
 // seg).  Thread 0 brings the next item's rows into the other half of a double buffer with
 // 1-D bulk copies (T, and U and bias for residual rows) while the CTA scores the current
-// one, so HBM latency overlaps the scoring.
+// one, so HBM latency overlaps the scoring.  An item's output is its candidates
+// (cand[item * kCandMax ..], count in cand_n[item]), or, count -1, the (index, score) of
+// its best in cand[item * kCandMax] when it scored them itself.
 __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const float* __restrict__ T, const float* __restrict__ U, const float* __restrict__ bias,
     const ItemRec* __restrict__ rec, int B, int gamma, int V, uint64_t seed, int splits,
-    RowState* __restrict__ partials, int* err) {
+    int* __restrict__ cand_n, Cand* __restrict__ cand, int* err) {
   extern __shared__ float4 fs_buf[];            // [2][3][kVerSeg / 4]
   __shared__ uint64_t full[2];
+  __shared__ Cand cand_s[kCandMax];
+  __shared__ int cnt_s;
   __shared__ RowState red[32];
   __shared__ float redf[kSampleThreads / 32];
   const int tid = threadIdx.x;
@@ -496,7 +527,10 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const ItemMeta m = meta_s[buf];
     const int md = m.md, k = m.k;
     const bool residual = md == kModeResidual;
-    if (md != kModeNone && __syncthreads_and(ok)) {
+    if (tid == 0) cnt_s = 0;                    // (ordered by the barrier below)
+    if (md != kModeNone && !__syncthreads_and(ok)) {
+      if (tid == 0) cand_n[item] = 0;
+    } else if (md != kModeNone) {
       const int v0 = seg * kVerSeg + 4 * tid;
       const int n4 = (min(kVerSeg, V - seg * kVerSeg) + 3) / 4;
       const float4* src = fs_buf + (size_t)buf * 3 * kSlot;
@@ -514,38 +548,67 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
       const float off_a = m.off_a, off_b = m.off_b;   // residual: log P = T - off_a, log Q = z - off_b
       const uint32_t stream = md == kModeBonus ? 3u : 2u;
       const int excl = m.excl;
-      const RowState st =
-          race_segment(t, zz, v0, V, residual, off_a, off_b, stream, excl, seed, k, b, red, redf);
-      if (tid == 0) partials[item] = st;
+      RowState best;
+      const int n = race_segment(t, zz, v0, V, residual, off_a, off_b, stream, excl, seed, k, b,
+                                 red, redf, cand_s, &cnt_s, best);
+      Cand* dst = cand + (size_t)item * kCandMax;
+      if (n >= 0) {
+        if (tid < n) dst[tid] = cand_s[tid];
+        if (tid == 0) cand_n[item] = n;
+      } else if (tid == 0) {
+        Cand c;
+        c.idx = best.idx;
+        c.t = best.score;
+        c.z = c.w = 0.f;
+        dst[0] = c;
+        cand_n[item] = -1;
+      }
     }
     __syncthreads();            // every thread is done with this buffer before it is refilled
   }
 }
 
-// One CTA per request.  Warp 0 merges the row's partials; the best (score, index) is the
-// token.  If the residual's support came out empty in fp32 (no partial has an index), the
-// whole CTA draws the fallback instead: Gumbel-max over T[b, j] with the residual's random
-// stream (a path the acceptance rule practically never takes, so it is not split further).
+// One CTA per request: warp w scores the candidates of segments w, w + 8, .. exactly (a
+// lane per candidate) and the block's best (score, index) is the token.  If the residual's
+// support came out empty in fp32 (no segment has a candidate), the whole CTA draws the
+// fallback instead: Gumbel-max over T[b, j] with the residual's random stream (a path the
+// acceptance rule practically never takes, so it is not split further).
 __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(
-    const float* __restrict__ T, const RowState* __restrict__ partials, int splits, int gamma,
-    int V, uint64_t seed, const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
+    const float* __restrict__ T, const ItemRec* __restrict__ rec, const int* __restrict__ cand_n,
+    const Cand* __restrict__ cand, int splits, int gamma, int V, uint64_t seed,
+    const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
     const int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ fallback) {
   __shared__ RowState red[32];
-  __shared__ int best_s;
   pdl_wait();
   pdl_launch_dependents();
   const int b = blockIdx.x;
   const int md = mode[b];
   if (md == kModeNone) return;
-  if (threadIdx.x < 32) {
-    const RowState acc = merge_partials(partials + (size_t)b * splits, splits);
-    if (threadIdx.x == 0) best_s = acc.idx;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool residual = md == kModeResidual;
+  const float off_a = __ldcg(&rec[b].off_a), off_b = __ldcg(&rec[b].off_b);
+  RowState acc = row_state_empty();
+  for (int seg = warp; seg < splits; seg += kSampleThreads / 32) {
+    const size_t item = (size_t)b * splits + seg;
+    const int n = __ldcg(cand_n + item);
+    const Cand* src = cand + item * kCandMax;
+    if (n < 0) {
+      if (lane == 0) {
+        const Cand c = src[0];
+        if (better(c.t, c.idx, acc.score, acc.idx)) { acc.score = c.t; acc.idx = c.idx; }
+      }
+      continue;
+    }
+    for (int i = lane; i < (n < kCandMax ? n : kCandMax); i += 32) {
+      const Cand c = src[i];
+      const float score = exact_score(residual, c.t, c.z, c.w, off_a, off_b);
+      if (better(score, c.idx, acc.score, acc.idx)) { acc.score = score; acc.idx = c.idx; }
+    }
   }
-  __syncthreads();
-  const int best = best_s;
-  if (best >= 0) {
-    if (threadIdx.x == 0) out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = best;
+  acc = row_state_block_reduce(acc, red);
+  if (acc.idx >= 0) {
+    if (threadIdx.x == 0) out_tokens[(size_t)b * (gamma + 1) + accept_len[b]] = acc.idx;
     return;
   }
   // fallback
@@ -609,7 +672,8 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   float* bias = ws_at<float>(ws, p.off_bias);
   RowState* part = ws_at<RowState>(ws, p.off_part);
   float2* part_stats = reinterpret_cast<float2*>(part);
-  RowState* part_ver = part + (size_t)B * gamma * p.stats.splits;
+  int* cand_n = ws_at<int>(ws, p.off_cand_n);
+  Cand* cand = ws_at<Cand>(ws, p.off_cand);
   int32_t* mode = ws_at<int32_t>(ws, p.off_mode);
   int32_t* pos = ws_at<int32_t>(ws, p.off_pos);
   int32_t* res_prev = ws_at<int32_t>(ws, p.off_prev);
@@ -636,11 +700,12 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   }
   e = launch_pdl(final_sample_kernel, dim3(final_sample_grid(B * p.ver.splits)),
                  dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias,
-                 (const ItemRec*)rec, B, gamma, V, seed, p.ver.splits, part_ver, err);
+                 (const ItemRec*)rec, B, gamma, V, seed, p.ver.splits, cand_n, cand, err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(finalize_kernel, dim3(B), dim3(kSampleThreads), 0, stream, T,
-                 (const RowState*)part_ver, p.ver.splits, gamma, V, seed, (const int32_t*)mode,
-                 (const int32_t*)pos, (const int32_t*)accept_len, out_tokens, fb);
+                 (const ItemRec*)rec, (const int*)cand_n, (const Cand*)cand, p.ver.splits, gamma,
+                 V, seed, (const int32_t*)mode, (const int32_t*)pos, (const int32_t*)accept_len,
+                 out_tokens, fb);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
