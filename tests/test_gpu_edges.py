@@ -5,7 +5,8 @@ The shapes cover: one request and one position; the smallest vocabulary (8, one 
 decision warp); a second request chunk holding a single request; a rank that is not a
 multiple of 32 (r = 48, 16-row K chunks); a vocabulary of exactly one tile.  They also
 cover the acceptance extremes: every position accepted (target = draft distribution,
-bonus from the last row) and every first position rejected (a target peaked elsewhere).
+bonus from the last row) and every first position rejected (a target peaked elsewhere),
+and a residual whose every logit is a race candidate.
 The tie band and tolerances are those of the main parity tests.
 """
 import numpy as np
@@ -128,6 +129,37 @@ def test_target_peaked_elsewhere_rejects_every_first_position():
     np.testing.assert_array_equal(v["n_out"], 1)
     np.testing.assert_array_equal(v["out_tokens"][:, 0], peak)       # the residual's mass
     np.testing.assert_array_equal(v["out_tokens"][:, 1:], -1)
+
+
+def test_residual_whose_every_logit_is_a_race_candidate():
+    """A residual with P barely above Q on every logit: the target row is the draft's own
+    logits except the drafted token, 30 lower, so position 1 is rejected and P - Q is about
+    q(x_1) Q everywhere else, below the race's error allowance: no lower bound survives and
+    every logit of a segment is a candidate (more than a segment's candidate list holds, so
+    the segments score them themselves).  The draw matches the oracle wherever the oracle's
+    top-two gap is above the fp32 rounding of log(P - Q) (about 1e-2 here)."""
+    _need_gpu()
+    B, gamma, V, r, seed = 16, 2, 8192, 16, 23
+    rng = np.random.default_rng(seed)
+    U = rng.normal(0, 0.1, size=(B, gamma, V)).astype(np.float32)     # q(x) ~ 1 / V
+    W1 = np.zeros((V, r), np.uint16)                                  # z = U exactly
+    W2 = workloads.f32_to_bf16_bits(rng.normal(0, 0.02, size=(r, V)).astype(np.float32))
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    d0 = oracle.draft(U, W1, W2, anchor, seed)
+    T = np.concatenate([U, rng.normal(0, 1, size=(B, 1, V)).astype(np.float32)], axis=1)
+    T[np.arange(B), 0, d0["tokens"][:, 0]] -= 30.0
+    ell = np.full(B, gamma, np.int32)
+    d, v = _run(U, T, W1, W2, anchor, ell, seed)
+    np.testing.assert_array_equal(d["tokens"][:, 0], d0["tokens"][:, 0])
+    np.testing.assert_array_equal(v["accept_len"], 0)
+    np.testing.assert_array_equal(v["n_out"], 1)
+    assert np.all(v["out_tokens"][:, 0] != d0["tokens"][:, 0])      # outside the residual
+    assert np.all((v["out_tokens"][:, 0] >= 0) & (v["out_tokens"][:, 0] < V))
+    ref = oracle.verify(T, U, W1, W2, anchor, d0["tokens"], ell, seed)
+    np.testing.assert_array_equal(ref["accept_len"], 0)
+    clear = ref["gap"] > 5e-2
+    assert clear.sum() >= B // 2
+    np.testing.assert_array_equal(v["out_tokens"][clear, 0], ref["out_tokens"][clear, 0])
 
 
 def test_verify_with_more_rows_than_a_grid_dimension():
