@@ -47,12 +47,12 @@ DRAFT_SOURCES = ("draft.cu", "sm100_ptx.cuh", "common.cuh", "internal.h")
 FIRST_KERNEL = ("draft_lanes_kernel via dspark_draft_confidence_schedule (bias contraction, "
                 "sampling, confidence and schedule, all gamma positions)")
 VERIFY_KERNELS = 5          # target statistics, decision, bias rows, final draw, finalize
-FUSED_SCHEDULE_ITEMS = 384  # the draft launch schedules in its first CTA up to this B*gamma
+FUSED_SCHEDULE_ITEMS = 4096  # the draft launch schedules up to this B*gamma itself
 
 
 def launches_per_step(w) -> int:
     """Kernels of one benchmarked step: one launch drafts, scores confidence and (up to
-    384 items) schedules; larger batches schedule in a launch of their own; then the
+    4096 items) schedules; larger batches schedule in a launch of their own; then the
     verification's kernels."""
     return 1 + (0 if w.B * w.gamma <= FUSED_SCHEDULE_ITEMS else 1) + VERIFY_KERNELS
 

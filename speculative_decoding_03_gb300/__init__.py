@@ -246,7 +246,7 @@ def draft_confidence_schedule(U, W1, W2p, anchor, h, w_c, b_c: float, sps, seed:
                               draft_out: Optional[Dict] = None, conf_out=None, sched_out=None,
                               stream=None):
     """draft (packed W2), confidence, survival and schedule in one launch (two when
-    B * gamma > 384: the scheduler kernel follows)."""
+    B * gamma > 4096: the scheduler kernel follows)."""
     torch = _torch()
     B, gamma, V = U.shape
     r = W1.shape[1]

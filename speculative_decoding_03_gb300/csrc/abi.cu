@@ -139,6 +139,7 @@ dspark_status dspark_draft_confidence_schedule(
   DraftStepArgs step;
   step.h = h; step.w_c = w_c; step.b_c = b_c; step.H = H; step.c = c; step.a = a;
   step.sps = sps; step.ell = ell; step.B_total = B_total; step.theta = theta;
+  step.sched_keys = ws_at<unsigned long long>(workspace, p.off_sched);
   int* err = ws_at<int>(workspace, p.off_err);
   const cudaError_t e = launch_draft_lanes(W1, nullptr, W2p, U, anchor, B, gamma, V, r, seed,
                                            false, tokens, q_tok, row_max, row_sumexp,

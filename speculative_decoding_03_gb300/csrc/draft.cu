@@ -150,11 +150,14 @@ struct LParams {
   int H;
   float* c_out;                    // [B][gamma]
   float* a_out;                    // [B][gamma]
-  // the prefix scheduler, run by CTA 0 after the last position (ell null: not run here)
+  // the prefix scheduler, run after the last position (ell null: not run here): by CTA 0
+  // alone when sched_keys is null, else every CTA ranks a share of the items and CTA 0
+  // scans them in the order they give (sched_keys: the sorted keys, B gamma words)
   const float* sps;
   int32_t* ell;
   int32_t* B_total;
   double* theta;
+  unsigned long long* sched_keys;
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -302,6 +305,48 @@ __device__ __forceinline__ void finalize_row(const LParams& p, int b, int c, int
     p.row_max[o] = m;
     p.row_sumexp[o] = s;
   }
+}
+
+// The scheduler's items ranked by the whole grid (up to kGridScheduleItems of them): every
+// CTA builds all N keys (the scheduler's order, distinct) in shared memory and counts, for
+// each item of its share [cta N / G, (cta + 1) N / G), the keys below it, the count split
+// over kThreads / share threads (a share of at most kThreads items); the item's key goes
+// to sched_keys[rank].  rank_s: kThreads words of shared memory.
+__device__ __noinline__ void schedule_ranks(const float* a, int N, int gamma,
+                                            unsigned long long* sched_keys,
+                                            unsigned long long* keys, int* rank_s, int G,
+                                            int cta) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < N; i += kThreads) {
+    const int r = i / gamma, j = i - r * gamma;
+    keys[i] = schedule_key(__ldcg(a + i), r, j);
+  }
+  rank_s[tid] = 0;
+  __syncthreads();
+  const int i0 = (int)((long long)cta * N / G), i1 = (int)((long long)(cta + 1) * N / G);
+  const int m = i1 - i0;
+  if (m > 0 && m <= kThreads) {
+    const int P = kThreads / m;                   // threads per item
+    const int k = tid / P, sp = tid - k * P;
+    if (k < m) {
+      const unsigned long long mine = keys[i0 + k];
+      const int j0 = (int)((long long)sp * N / P), j1 = (int)((long long)(sp + 1) * N / P);
+      int cnt = 0;
+      for (int jj = j0; jj < j1; ++jj) cnt += keys[jj] < mine ? 1 : 0;
+      atomicAdd(&rank_s[k], cnt);
+    }
+    __syncthreads();
+    if (tid < m) sched_keys[rank_s[tid]] = keys[i0 + tid];
+  } else if (m > kThreads) {
+    // (a grid of fewer than N / kThreads CTAs: whole items per thread)
+    for (int k = tid; k < m; k += kThreads) {
+      const unsigned long long mine = keys[i0 + k];
+      int cnt = 0;
+      for (int jj = 0; jj < N; ++jj) cnt += keys[jj] < mine ? 1 : 0;
+      sched_keys[cnt] = mine;
+    }
+  }
+  __syncthreads();                                // the ranks are stored before the arrival
 }
 
 template <int NBJ, bool Greedy>
@@ -1068,16 +1113,47 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
-  // The prefix scheduler over every request's survivals, by CTA 0 once the last position
-  // is done: every CTA wrote its survivals before its last grid arrival, which the
-  // samplers' final wait acquired and the barrier above passed on to every thread.  The
-  // W2 ring (its copies and MMAs drained) holds the keys.
-  if (p.ell && cta == 0 && !*(volatile int*)&abort_s) {
+  // The prefix scheduler over every request's survivals once the last position is done:
+  // every CTA wrote its survivals before its last grid arrival, which the samplers' final
+  // wait acquired and the barrier above passed on to every thread.  The W2 and U rings
+  // (their copies and MMAs drained) hold the keys.
+  if (p.ell && !*(volatile int*)&abort_s) {
+    const int N = p.B * p.gamma;
     int Npad = 2;
-    while (Npad < p.B * p.gamma) Npad <<= 1;
-    schedule_block<false>(p.a_out, p.B, p.gamma, Npad, p.sps, nullptr, nullptr, p.ell, p.B_total,
-                   p.theta, reinterpret_cast<unsigned long long*>(smem + S::kOffW),
-                   (size_t)S::kWStages * kWStageBytes);
+    while (Npad < N) Npad <<= 1;
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + S::kOffW);
+    const size_t key_bytes = (size_t)(S::kOffMerge - S::kOffW);
+    if (!p.sched_keys) {
+      if (cta == 0)
+        schedule_block<false>(p.a_out, p.B, p.gamma, Npad, p.sps, nullptr, nullptr, p.ell,
+                              p.B_total, p.theta, keys, key_bytes);
+    } else {
+      schedule_ranks(p.a_out, N, p.gamma, p.sched_keys, keys,
+                     reinterpret_cast<int*>(smem + S::kOffMerge), G, cta);
+      // count in once more; CTA 0 waits for every share, then scans in that order
+      if (threadIdx.x == 0 && !*(volatile int*)&abort_s)
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.grid_count) : "memory");
+      if (cta == 0) {
+        if (threadIdx.x == 0) {
+          const unsigned int target = (unsigned int)G * (unsigned int)(p.gamma + 1) + p.grid_extra;
+          const long long t0 = sm_cycles();
+          while (ld_acquire_u32(p.grid_count) < target) {
+            if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
+              set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+              atomicExch(&abort_s, 1);
+              break;
+            }
+          }
+        }
+        __syncthreads();
+        if (!*(volatile int*)&abort_s) {
+          for (int i = threadIdx.x; i < N; i += kThreads) keys[i] = __ldcg(p.sched_keys + i);
+          __syncthreads();
+          schedule_block<false>(p.a_out, p.B, p.gamma, Npad, p.sps, nullptr, nullptr, p.ell,
+                                p.B_total, p.theta, keys, key_bytes, /*presorted=*/true);
+        }
+      }
+    }
   }
 }
 
@@ -1165,7 +1241,7 @@ size_t draft_region_bytes(int B, int gamma) {
 
 int draft_kchunk(int r) { return (r % 64 == 0) ? 64 : (r % 32 == 0) ? 32 : 16; }
 
-int draft_fused_schedule_limit() { return kThreads; }
+int draft_fused_schedule_limit() { return kGridScheduleItems; }
 
 cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,
                                const float* U, const int32_t* anchor, int B, int gamma, int V,
@@ -1212,6 +1288,9 @@ cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uin
     p.c_out = step->c; p.a_out = step->a;
     if (step->ell && (long long)B * gamma <= kThreads) {
       p.sps = step->sps; p.ell = step->ell; p.B_total = step->B_total; p.theta = step->theta;
+    } else if (step->ell && step->sched_keys && (long long)B * gamma <= kGridScheduleItems) {
+      p.sps = step->sps; p.ell = step->ell; p.B_total = step->B_total; p.theta = step->theta;
+      p.sched_keys = step->sched_keys;
     }
   }
   cudaError_t e = cudaMemsetAsync(base + part_bytes, 0,

@@ -19,6 +19,8 @@ constexpr int kTargetCtas = 608;         // CTAs a row-sampling launch aims for 
 constexpr int kMaxScheduleItems = 16384; // R * gamma handled by the one-CTA scheduler
 constexpr int kGemmTileV = 128;          // vocabulary rows per tensor-core tile (MMA M)
 constexpr int kDraftMaxCtas = 160;       // upper bound of the persistent draft grid
+// scheduler items (B gamma) the step's first launch ranks itself (more: a scheduler kernel)
+constexpr int kGridScheduleItems = 4096;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -63,8 +65,8 @@ struct Plan {
   RowSplit stats, ver;
   // byte offsets into the workspace
   size_t off_err, off_draft, off_bias, off_part, off_mode,
-      off_pos, off_prev, off_slot, off_nres, off_fallback, off_rec, off_cand_n, off_cand,
-      off_rnn_state, total;
+      off_pos, off_prev, off_slot, off_nres, off_fallback, off_rec, off_sched, off_cand_n,
+      off_cand, off_rnn_state, total;
 };
 
 inline Plan make_plan(int B, int gamma, int V, int r, int H) {
@@ -85,6 +87,9 @@ inline Plan make_plan(int B, int gamma, int V, int r, int H) {
   p.off_nres = o; o += 256;                                              // residual count
   p.off_fallback = o; o = align_up(o + (size_t)B * sizeof(int32_t), 256);
   p.off_rec = o; o = align_up(o + (size_t)B * 32, 256);                 // final-draw records
+  // the first launch's scheduler keys in ranked order (batches of 385 .. 4096 items)
+  p.off_sched = o;
+  if ((long long)B * gamma <= kGridScheduleItems) o = align_up(o + (size_t)B * gamma * 8, 256);
   // the final draw's candidates: a count and up to 64 entries of 16 bytes per segment
   p.off_cand_n = o; o = align_up(o + (size_t)B * p.ver.splits * sizeof(int), 256);
   p.off_cand = o; o = align_up(o + (size_t)B * p.ver.splits * 64 * 16, 256);
@@ -165,7 +170,8 @@ cudaError_t launch_bias_gemm_rows(const uint16_t* W2, const uint16_t* W2p, const
 // `region` holds draft_region_bytes(B, gamma) of workspace
 // with `step` (may be null) the same launch also computes the confidence head and the
 // survivals at every position boundary, and, when B * gamma <= draft_fused_schedule_limit(),
-// runs the prefix scheduler in its CTA 0 after the last position
+// runs the prefix scheduler after the last position (up to 384 items in CTA 0, more with
+// the grid ranking the items into step->sched_keys)
 struct DraftStepArgs {
   const float* h;      // [B][gamma][H]
   const float* w_c;    // [H + r]
@@ -177,6 +183,7 @@ struct DraftStepArgs {
   int32_t* ell;
   int32_t* B_total;
   double* theta;
+  unsigned long long* sched_keys;   // [B gamma] scratch when B gamma > 384 (the grid ranks)
 };
 int draft_fused_schedule_limit();
 cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uint16_t* W2p,

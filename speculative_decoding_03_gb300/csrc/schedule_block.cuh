@@ -23,6 +23,12 @@ static __device__ __forceinline__ long long fixed_point_a(float a) {
   return (long long)((m + (1ull << (-sh - 1))) >> (-sh));
 }
 
+// The sort key of item i = r gamma + j: (A desc, r asc, j asc) as one 64-bit integer.
+static __device__ __forceinline__ unsigned long long schedule_key(float a, int r, int j) {
+  return ((unsigned long long)(4294967296LL - fixed_point_a(a)) << 21) |
+         ((unsigned long long)r << 5) | (unsigned long long)j;
+}
+
 static __device__ __forceinline__ double theta_at(long long R, long long S, float sps) {
   return __dmul_rn((double)(R * 4294967296LL + S), (double)sps);
 }
@@ -167,12 +173,15 @@ static __device__ void schedule_radix_sort(const float* __restrict__ a, int N, u
 // count.  K_out (may be null) receives that count.  kRadix: whether the radix path is
 // compiled in (the scheduler kernel; the blocks that run the scheduler inside another
 // kernel keep their registers for it).
+// presorted: keys[0 .. N) already hold the N items' keys in ascending order (a is then
+// not read).
 template <bool kRadix>
 static __device__ void schedule_block(const float* __restrict__ a, int R, int gamma, int Npad,
                                const float* __restrict__ sps, const int32_t* K_in,
                                int32_t* K_out, int32_t* __restrict__ ell,
                                int32_t* __restrict__ B_total, double* __restrict__ theta,
-                               unsigned long long* keys, size_t scratch_bytes) {
+                               unsigned long long* keys, size_t scratch_bytes,
+                               bool presorted = false) {
   __shared__ long long warp_tot[32];
   __shared__ int first_fail, k_in_s;
   __shared__ float sps_s[kSchedThreads + 1];   // sps[R .. R + N] when N <= nthr
@@ -180,21 +189,19 @@ static __device__ void schedule_block(const float* __restrict__ a, int R, int ga
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int N = R * gamma;
   const bool small = N <= nthr;
-  const bool radix = kRadix && !small && nthr == kSchedThreads && N <= kMaxScheduleItems &&
-                     scratch_bytes >= schedule_radix_bytes(N);
+  const bool radix = kRadix && !presorted && !small && nthr == kSchedThreads &&
+                     N <= kMaxScheduleItems && scratch_bytes >= schedule_radix_bytes(N);
   // the SPS table entries the scan reads, fetched together with the expected returns
   if (small)
     for (int i = tid; i <= N; i += nthr) sps_s[i] = sps[R + i];
   if (R <= nthr && tid < R) cnt_s[tid] = 0;
   if (tid < 32) warp_tot[tid] = 0;
 
-  for (int i = tid; i < (radix ? 0 : Npad); i += nthr) {
+  for (int i = tid; i < (radix || presorted ? 0 : Npad); i += nthr) {
     unsigned long long key = ~0ull;
     if (i < N) {
       const int r = i / gamma, j = i - r * gamma;
-      const long long A = fixed_point_a(a[i]);
-      key = ((unsigned long long)(4294967296LL - A) << 21) | ((unsigned long long)r << 5) |
-            (unsigned long long)j;
+      key = schedule_key(a[i], r, j);
     }
     keys[i] = key;
   }
@@ -208,7 +215,8 @@ static __device__ void schedule_block(const float* __restrict__ a, int R, int ga
 
   uint32_t* rK = nullptr;
   uint16_t* rI = nullptr;
-  if (kRadix && radix) {
+  if (presorted) {
+  } else if (kRadix && radix) {
     schedule_radix_sort(a, N, reinterpret_cast<uint8_t*>(keys), &rK, &rI);
   } else if (small) {
     // small batches: every key is distinct, so its rank is the number of smaller keys;

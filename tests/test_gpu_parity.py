@@ -458,6 +458,28 @@ def test_draft_confidence_schedule_in_one_launch(name):
     assert ws.status() == 0
 
 
+def test_first_launch_ranks_more_items_than_threads_per_cta():
+    """The first launch's grid ranking with shares larger than a CTA's threads (1000
+    requests x 2 positions on a 5-tile vocabulary: a grid of 5 CTAs, 400 items each): the
+    schedule equals the scheduler's on the same survivals."""
+    _need_gpu()
+    w = workloads.scaled(workloads.get("scheduler_stress"), B=1000, gamma=2, V=520, r=128, H=8)
+    inp = workloads.generate(w, with_T=False)
+    dev = _dev(inp)
+    ws = _ws(w)
+    W2p = ds.pack_w2(dev["W2"])
+    d, (c, a), (ell, Bt, th) = ds.draft_confidence_schedule(
+        dev["U"], dev["W1"], W2p, dev["anchor"], dev["h"], dev["w_c"], float(inp.b_c), dev["sps"],
+        w.seed, ws)
+    ell1, Bt1, th1 = ds.schedule(a, dev["sps"], ws)
+    np.testing.assert_array_equal(ell.cpu().numpy(), ell1.cpu().numpy())
+    assert int(Bt.item()) == int(Bt1.item()) and float(th.item()) == float(th1.item())
+    ell_r, Bt_r, th_r = oracle.schedule(a.cpu().numpy(), inp.sps)
+    np.testing.assert_array_equal(ell.cpu().numpy(), ell_r)
+    assert int(Bt.item()) == Bt_r and float(th.item()) == th_r
+    assert ws.status() == 0
+
+
 def test_schedule_with_exactly_one_block_of_items():
     """R * gamma equal to the scheduler's thread count (the last SPS entry is staged too)."""
     _need_gpu()
