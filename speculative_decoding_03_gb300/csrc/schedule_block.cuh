@@ -183,6 +183,7 @@ static __device__ void schedule_block(const float* __restrict__ a, int R, int ga
                                unsigned long long* keys, size_t scratch_bytes,
                                bool presorted = false) {
   __shared__ long long warp_tot[32];
+  __shared__ long long a_top_s;
   __shared__ int first_fail, k_in_s;
   __shared__ float sps_s[kSchedThreads + 1];   // sps[R .. R + N] when N <= nthr
   __shared__ int cnt_s[kSchedThreads];         // admitted items per request when R <= nthr
@@ -210,8 +211,32 @@ static __device__ void schedule_block(const float* __restrict__ a, int R, int ga
   if (tid == 0) {
     first_fail = N + 1;
     k_in_s = K_in ? *K_in : -1;     // read before K_out (which may alias it) is written
+    a_top_s = 0;
   }
   __syncthreads();
+
+  if (kRadix && radix && k_in_s < 0) {
+    // The scan stops at the first item when even the largest expected return does not raise
+    // Theta; then nothing is admitted and no order is needed (without a capacity): the
+    // outputs are those of the full scan, from one block-wide maximum of A.
+    long long top = 0;
+    for (int i = tid; i < N; i += nthr) top = max(top, fixed_point_a(a[i]));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) top = max(top, __shfl_xor_sync(0xffffffffu, top, d));
+    if ((tid & 31) == 0) atomicMax(reinterpret_cast<unsigned long long*>(&a_top_s), (unsigned long long)top);
+    __syncthreads();
+    const double th0 = theta_at(R, 0, sps[R]);
+    if (!(theta_at(R, a_top_s, sps[R + 1]) > th0)) {
+      if (R <= nthr && tid < R) ell[tid] = 0;       // (more requests were zeroed above)
+      if (tid == 0) {
+        if (K_out) *K_out = 0;
+        *B_total = R;
+        *theta = th0 / 4294967296.0;
+      }
+      __syncthreads();
+      return;
+    }
+  }
 
   uint32_t* rK = nullptr;
   uint16_t* rI = nullptr;
