@@ -499,12 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     // compile-time K steps per stage (KS) and stages per tile (NKC, 0: a runtime count),
     // descriptors are advanced by adds to their start-address field (every operand lies
     // below 256 KB, so the sum never carries into the stride fields), and the waits spin
-    // on test_wait (one spinning lane costs the others nothing) instead of suspending.
+    // on test_wait (one spinning lane costs the others little) for 32-request jobs, whose
+    // hand-offs are short, and suspend for larger ones.
     auto spin_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
       if (mbar_test_wait(bar, parity)) return true;
       const long long t0 = sm_cycles();
       for (;;) {
-        if (mbar_test_wait(bar, parity)) return true;
+        if (NBJ >= 64 ? mbar_try_wait_sleep(bar, parity) : mbar_test_wait(bar, parity)) return true;
         if (*(volatile int*)&abort_s) return false;
         if (sm_cycles() - t0 > p.wait_cycles) {
           set_device_error(p.err, DSPARK_ERR_TIMEOUT);
