@@ -568,8 +568,8 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
   }
 }
 
-// One CTA per request: warp w scores the candidates of segments w, w + 8, .. exactly (a
-// lane per candidate) and the block's best (score, index) is the token.  If the residual's
+// One CTA per request: thread t scores the candidates of segments t, t + 256, .. exactly
+// and the block's best (score, index) is the token.  If the residual's
 // support came out empty in fp32 (no segment has a candidate), the whole CTA draws the
 // fallback instead: Gumbel-max over T[b, j] with the residual's random stream (a path the
 // acceptance rule practically never takes, so it is not split further).
@@ -585,22 +585,20 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(
   const int b = blockIdx.x;
   const int md = mode[b];
   if (md == kModeNone) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool residual = md == kModeResidual;
   const float off_a = __ldcg(&rec[b].off_a), off_b = __ldcg(&rec[b].off_b);
+  // thread t takes segments t, t + 256, ..: every segment's few candidates in one round
   RowState acc = row_state_empty();
-  for (int seg = warp; seg < splits; seg += kSampleThreads / 32) {
+  for (int seg = threadIdx.x; seg < splits; seg += kSampleThreads) {
     const size_t item = (size_t)b * splits + seg;
     const int n = __ldcg(cand_n + item);
     const Cand* src = cand + item * kCandMax;
     if (n < 0) {
-      if (lane == 0) {
-        const Cand c = src[0];
-        if (better(c.t, c.idx, acc.score, acc.idx)) { acc.score = c.t; acc.idx = c.idx; }
-      }
+      const Cand c = src[0];
+      if (better(c.t, c.idx, acc.score, acc.idx)) { acc.score = c.t; acc.idx = c.idx; }
       continue;
     }
-    for (int i = lane; i < (n < kCandMax ? n : kCandMax); i += 32) {
+    for (int i = 0; i < (n < kCandMax ? n : kCandMax); ++i) {
       const Cand c = src[i];
       const float score = exact_score(residual, c.t, c.z, c.w, off_a, off_b);
       if (better(score, c.idx, acc.score, acc.idx)) { acc.score = score; acc.idx = c.idx; }
