@@ -168,6 +168,14 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_release_cta_shared_u32(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_cta_shared_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
 __device__ __forceinline__ unsigned long long ld_volatile_shared_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
@@ -365,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   __shared__ float surv_s[kConfSlots];   // a_{k-1} of this CTA's requests
   __shared__ float hdot_s[kConfSlots];   // h_k . w_c[0:H] of the same
   __shared__ int conf_done_s;
+  __shared__ unsigned int grid_seen_s;   // the barrier count the samplers' poller last saw
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -393,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     mbar_init(&mma_drain, 1);
     abort_s = 0;
     conf_done_s = 0;
+    grid_seen_s = 0u;
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < NBJ; i += kThreads) thr[i] = 0ull;   // below every tagged key
@@ -587,7 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
       const int H4 = p.H >> 2;
       const float4* wv = reinterpret_cast<const float4*>(p.w_c);
       bool ok = true;
-      for (int k = 1; k <= p.gamma && ok; ++k) {
+      // (a CTA holds requests cta, cta + G, ..: none when cta >= B)
+      for (int k = 1; k <= p.gamma && ok && cta < p.B; ++k) {
         int i = 0;
         for (int bb = cta; bb < p.B; bb += G, ++i) {
           const float4* hv = reinterpret_cast<const float4*>(p.h + ((size_t)bb * p.gamma + (k - 1)) * p.H);
@@ -611,12 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
           if (lane == 0) hdot_s[i] = d;
         }
         if (k >= 2) {
-          // x_{k-1} is final once every CTA has arrived for position k - 1 (a bounded,
-          // sleeping poll: this warp is off the samplers' critical path)
+          // x_{k-1} is final once every CTA has arrived for position k - 1, which the
+          // samplers' poller publishes in shared memory (a bounded, sleeping poll: this warp
+          // is off the samplers' critical path, and polling the grid counter itself would
+          // add a poller per CTA on its line)
           if (lane == 0) {
             const unsigned int target = (unsigned int)G * (unsigned int)(k - 1) + p.grid_extra;
             const long long t0 = sm_cycles();
-            while (ld_acquire_u32(p.grid_count) < target) {
+            while (ld_acquire_cta_shared_u32(&grid_seen_s) < target) {
               if (*(volatile int*)&abort_s) { ok = false; break; }
               if (sm_cycles() - t0 > p.wait_cycles) {
                 set_device_error(p.err, DSPARK_ERR_TIMEOUT);
@@ -697,13 +710,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     auto grid_wait = [&](unsigned int target) {
       if (stid == 0 && !*(volatile int*)&abort_s) {
         const long long t0 = sm_cycles();
-        while (ld_acquire_u32(p.grid_count) < target) {
+        unsigned int seen;
+        while ((seen = ld_acquire_u32(p.grid_count)) < target) {
           if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
             set_device_error(p.err, DSPARK_ERR_TIMEOUT);
             atomicExch(&abort_s, 1);
             break;
           }
         }
+        // this CTA's confidence warp follows the barrier through this word
+        if (seen >= target) st_release_cta_shared_u32(&grid_seen_s, seen);
       }
       named_bar_sync(kBarSamplers, kSamplerThreads);
     };
