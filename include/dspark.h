@@ -385,8 +385,10 @@ dspark_status dspark_last_device_status(void* workspace, cudaStream_t stream);
  * confidence head and survival of position k (weigao.cc DSpark-vs-MTP page, "3.
  * confidence head"; billytse.dev DSpark page, section 5) in a warp of its own, the h_k part
  * while position k - 1 is drawn and the rest once x_{k-1} is known; after the last position
- * it runs the prefix scheduler (billytse.dev sections 6 and 7): in one CTA when
- * B * gamma <= 384, with every CTA ranking a share of the items when B * gamma <= 4096;
+ * it runs the prefix scheduler (billytse.dev sections 6 and 7): when B * gamma <= 384, in
+ * the confidence warps of the CTAs that hold no request while the last position is drawn
+ * (else in one CTA after it), with every CTA ranking a share of the items when
+ * B * gamma <= 4096;
  * larger batches get the scheduler kernel as a second launch.  Outputs and their meaning are those of the three
  * calls (tokens, q_tok, row_max, row_sumexp; c, a; ell, B_total, theta); the draft's
  * outputs are identical to dspark_draft_packed's, c and a agree with dspark_confidence's to

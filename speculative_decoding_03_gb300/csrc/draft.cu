@@ -135,6 +135,8 @@ struct LParams {
   RowState* partials;              // [3][B][G], position k in slot k % 3
   unsigned long long* keys;        // [gamma][B], zeroed before launch
   unsigned int* grid_count;        // zeroed before launch
+  unsigned int* conf_count;        // (the next word) CTAs whose survivals are all written
+  unsigned int* rank_count;        // (the word after) idle CTAs that ranked their items
   int32_t* tokens;
   float* q_tok;
   float* row_max;
@@ -158,6 +160,10 @@ struct LParams {
   int32_t* B_total;
   double* theta;
   unsigned long long* sched_keys;
+  // B gamma <= kThreads on a grid of more than B CTAs: the confidence warps of the CTAs
+  // that hold no request rank the scheduler's items while the last position is drawn, and
+  // the last CTA's scans them (sched_keys: the ranked keys)
+  int sched_warp;
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -315,6 +321,86 @@ __device__ __forceinline__ void finalize_row(const LParams& p, int b, int c, int
   }
 }
 
+// One warp's share of the scheduler's ranking (N = R gamma <= kThreads items): the keys of
+// all N items in shared memory (keys), then, for each item of share w of W, the number of
+// keys below it (counted over the lanes) as its rank: sched_keys[rank] = its key.
+__device__ __noinline__ void warp_rank_share(const float* a, int R, int gamma, int w, int W,
+                                             unsigned long long* keys,
+                                             unsigned long long* sched_keys) {
+  const int lane = threadIdx.x & 31;
+  const int N = R * gamma;
+  for (int i = lane; i < N; i += 32) {
+    const int r = i / gamma, j = i - r * gamma;
+    keys[i] = schedule_key(__ldcg(a + i), r, j);
+  }
+  __syncwarp();
+  const int i0 = (int)((long long)w * N / W), i1 = (int)((long long)(w + 1) * N / W);
+  for (int it = i0; it < i1; ++it) {
+    const unsigned long long mine = keys[it];
+    int cnt = 0;
+    for (int j = lane; j < N; j += 32) cnt += keys[j] < mine ? 1 : 0;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, d);
+    if (lane == 0) sched_keys[cnt] = mine;
+  }
+  __syncwarp();
+}
+
+// The scheduler's scan on one warp over the N = R gamma <= kThreads keys in ascending order
+// (keys, shared memory): the exact sums and Theta test of schedule_block (the same first
+// non-rise), lane L scanning the contiguous items [L per, (L + 1) per); cnt: R words of
+// shared memory for the per-request counts.
+__device__ __noinline__ void warp_scan_schedule(int R, int gamma, const float* sps, int32_t* ell,
+                                                int32_t* B_total, double* theta,
+                                                const unsigned long long* keys, int* cnt) {
+  const int lane = threadIdx.x & 31;
+  const int N = R * gamma;
+  for (int r = lane; r < R; r += 32) cnt[r] = 0;
+  auto A_of = [&](int n) { return 4294967296LL - (long long)(keys[n] >> 21); };
+  const int per = (N + 31) / 32;
+  const int c0 = min(N, lane * per), c1 = min(N, c0 + per);
+  long long local = 0;
+  for (int i = c0; i < c1; ++i) local += A_of(i);
+  long long incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  long long S = incl - local;
+  int fail = N + 1;
+  if (c0 < c1) {
+    double th_prev = theta_at(R, S, sps[R + c0]);
+    for (int i = c0; i < c1; ++i) {
+      S += A_of(i);
+      const double th = theta_at(R, S, sps[R + i + 1]);
+      if (!(th > th_prev)) {
+        fail = i + 1;
+        break;
+      }
+      th_prev = th;
+    }
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) fail = min(fail, __shfl_xor_sync(0xffffffffu, fail, d));
+  const int admitted = fail - 1;
+  __syncwarp();
+  for (int i = lane; i < admitted; i += 32) atomicAdd(&cnt[(int)((keys[i] >> 5) & 0xFFFFull)], 1);
+  __syncwarp();
+  for (int r = lane; r < R; r += 32) ell[r] = cnt[r];
+  if (admitted == 0) {
+    if (lane == 0) {
+      *B_total = R;
+      *theta = theta_at(R, 0, sps[R]) / 4294967296.0;
+    }
+  } else if (admitted - 1 >= c0 && admitted - 1 < c1) {
+    long long Sa = incl - local;
+    for (int i = c0; i < admitted; ++i) Sa += A_of(i);
+    *B_total = R + admitted;
+    *theta = theta_at(R, Sa, sps[R + admitted]) / 4294967296.0;
+  }
+}
+
 // The scheduler's items ranked by the whole grid (up to kGridScheduleItems of them): every
 // CTA builds all N keys (the scheduler's order, distinct) in shared memory and counts, for
 // each item of its share [cta N / G, (cta + 1) N / G), the keys below it, the count split
@@ -373,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   __shared__ float surv_s[kConfSlots];   // a_{k-1} of this CTA's requests
   __shared__ float hdot_s[kConfSlots];   // h_k . w_c[0:H] of the same
   __shared__ int conf_done_s;
+  __shared__ unsigned long long sched_warp_keys[kThreads];   // the scheduling warp's keys
   __shared__ unsigned int grid_seen_s;   // the barrier count the samplers' poller last saw
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -679,10 +766,48 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
         }
       }
       // c and a are ordered before the flag the samplers wait for ahead of their last
-      // grid arrival
+      // grid arrival (and, for the scheduling warp, before this CTA's count)
       __threadfence();
       __syncwarp();
       if (lane == 0) *(volatile int*)&conf_done_s = 1;
+      if (p.sched_warp && cta < p.B && ok && lane == 0)
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.conf_count) : "memory");
+      if (p.sched_warp && cta >= p.B) {
+        // A CTA without requests: once every requesting CTA has written its survivals, rank
+        // a share of the scheduler's items; the last CTA then scans them all
+        auto wait_count = [&](const unsigned int* cnt, unsigned int target) -> bool {
+          bool go = true;
+          if (lane == 0) {
+            const long long t0 = sm_cycles();
+            while (ld_acquire_u32(cnt) < target) {
+              if (*(volatile int*)&abort_s || sm_cycles() - t0 > p.wait_cycles) {
+                if (!*(volatile int*)&abort_s) {
+                  set_device_error(p.err, DSPARK_ERR_TIMEOUT);
+                  atomicExch(&abort_s, 1);
+                }
+                go = false;
+                break;
+              }
+              __nanosleep(128);
+            }
+          }
+          __syncwarp();   // the other lanes' reads follow lane 0's acquire
+          return __shfl_sync(0xffffffffu, go, 0);
+        };
+        const int W = G - p.B;
+        if (wait_count(p.conf_count, (unsigned int)p.B)) {
+          warp_rank_share(p.a_out, p.B, p.gamma, cta - p.B, W, sched_warp_keys, p.sched_keys);
+          if (lane == 0)
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.rank_count) : "memory");
+          if (cta == G - 1 && wait_count(p.rank_count, (unsigned int)W)) {
+            const int N = p.B * p.gamma;
+            for (int i = lane; i < N; i += 32) sched_warp_keys[i] = __ldcg(p.sched_keys + i);
+            __syncwarp();
+            warp_scan_schedule(p.B, p.gamma, p.sps, p.ell, p.B_total, p.theta, sched_warp_keys,
+                               reinterpret_cast<int*>(hdot_s));
+          }
+        }
+      }
     }
   } else if (warp < kSamplers) {
     // ----------------------------------------------------------------------- samplers
@@ -1134,7 +1259,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
   // every CTA wrote its survivals before its last grid arrival, which the samplers' final
   // wait acquired and the barrier above passed on to every thread.  The W2 and U rings
   // (their copies and MMAs drained) hold the keys.
-  if (p.ell && !*(volatile int*)&abort_s) {
+  if (p.ell && !p.sched_warp && !*(volatile int*)&abort_s) {
     const int N = p.B * p.gamma;
     int Npad = 2;
     while (Npad < N) Npad <<= 1;
@@ -1289,6 +1414,8 @@ cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uin
   char* base = static_cast<char*>(region);
   p.partials = reinterpret_cast<RowState*>(base);
   p.grid_count = reinterpret_cast<unsigned int*>(base + part_bytes);
+  p.conf_count = p.grid_count + 1;
+  p.rank_count = p.grid_count + 2;
   p.keys = reinterpret_cast<unsigned long long*>(base + part_bytes + 256);
   p.tokens = tokens;
   p.q_tok = q_tok;
@@ -1305,6 +1432,8 @@ cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uin
     p.c_out = step->c; p.a_out = step->a;
     if (step->ell && (long long)B * gamma <= kThreads) {
       p.sps = step->sps; p.ell = step->ell; p.B_total = step->B_total; p.theta = step->theta;
+      p.sched_warp = grid > B && step->sched_keys ? 1 : 0;
+      p.sched_keys = step->sched_keys;
     } else if (step->ell && step->sched_keys && (long long)B * gamma <= kGridScheduleItems) {
       p.sps = step->sps; p.ell = step->ell; p.B_total = step->B_total; p.theta = step->theta;
       p.sched_keys = step->sched_keys;
