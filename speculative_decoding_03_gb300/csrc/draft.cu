@@ -132,6 +132,7 @@ struct LParams {
   int B, gamma, V, r;
   int n_tiles, n_chunks, kc;       // kc = rank rows per W2 stage (<= 64)
   uint64_t seed;
+  PhiloxKeys philox;               // the generator's round keys for this seed
   RowState* partials;              // [3][B][G], position k in slot k % 3
   unsigned long long* keys;        // [gamma][B], zeroed before launch
   unsigned int* grid_count;        // zeroed before launch
@@ -210,21 +211,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Philox4x32 with one 32x32->64 multiply per product (the definition of common.cuh: same
-// rounds, constants and key schedule).
-__device__ __forceinline__ uint4 philox_wide(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int round = 0; round < kPhiloxRounds; ++round) {
-    const unsigned long long p0 = (unsigned long long)0xD2511F53u * c.x;
-    const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
-                   (uint32_t)p0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
-  }
-  return c;
 }
 
 __device__ __forceinline__ int token_of_key(unsigned long long key) {
@@ -820,7 +806,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
     const int sidx = (sw >> 2) * S::kCopies + quad / (NBJ / 32);
     const int c0 = sidx * S::kCols;
     const uint32_t lane_base = tmem_base + ((uint32_t)(32 * quad) << 16);
-    const uint32_t k0 = (uint32_t)p.seed, k1 = (uint32_t)(p.seed >> 32);
     float* merge = reinterpret_cast<float*>(smem + S::kOffMerge);
     // U tile address of this thread's first column: box c0 / 32, row ml, 16-byte chunk
     // (c0 % 32) / 4 (two chunks per octet), 128-byte swizzle (chunk ^ row % 8)
@@ -1074,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_lanes_kernel(
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const uint4 d = philox_wide(make_uint4((uint32_t)(v >> 2) + (uint32_t)q, (uint32_t)k,
-                                                       (uint32_t)b, 0u), k0, k1);
+                                                       (uint32_t)b, 0u), p.philox);
                 dw[4 * q + 0] = d.x; dw[4 * q + 1] = d.y; dw[4 * q + 2] = d.z; dw[4 * q + 3] = d.w;
               }
               unsigned cm = 0u;
@@ -1410,6 +1395,7 @@ cudaError_t launch_draft_lanes(const uint16_t* W1, const uint16_t* W2, const uin
     return cudaErrorNotSupported;
   p.kc = draft_kchunk(r);
   p.seed = seed;
+  p.philox = philox_keys(seed);
   const size_t part_bytes = align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256);
   char* base = static_cast<char*>(region);
   p.partials = reinterpret_cast<RowState*>(base);

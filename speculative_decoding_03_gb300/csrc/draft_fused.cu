@@ -104,6 +104,7 @@ struct DraftParams {
   int B, gamma, V, r;
   int n_tiles, n_chunks, kc;       // kc = K rows per W2 stage (<= 64)
   uint64_t seed;
+  PhiloxKeys philox;               // the generator's round keys for this seed
   RowState* partials;              // [3][B][G], position k in slot k % 3
   unsigned long long* keys;        // [gamma][B], zeroed before launch
   unsigned int* grid_count;        // zeroed before launch
@@ -175,21 +176,6 @@ __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
-}
-
-// Philox4x32 with one 32x32->64 multiply per product (the definition of common.cuh:
-// same rounds, constants and key schedule).
-__device__ __forceinline__ uint4 philox_wide(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int round = 0; round < kPhiloxRounds; ++round) {
-    const unsigned long long p0 = (unsigned long long)0xD2511F53u * c.x;
-    const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
-                   (uint32_t)p0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
-  }
-  return c;
 }
 
 __device__ __forceinline__ int token_of_key(unsigned long long key) {
@@ -655,7 +641,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
     constexpr int RPW = NB / kSamplers;           // requests per sampler warp
     const int sw = warp - kFirstSampler;
     const int stid = threadIdx.x - kFirstSampler * 32;
-    const uint32_t k0 = (uint32_t)p.seed, k1 = (uint32_t)(p.seed >> 32);
     uint32_t tc = 0;
     // RNN head: a recurrence CTA stages its rows of Wrec (gate, candidate and output of its
     // dpc state entries) in shared memory once, when they fit; the samplers' named barrier
@@ -910,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
 #pragma unroll
           for (int i = 0; i < RPW; ++i)
             d[i] = philox_wide(make_uint4((uint32_t)(v >> 2), (uint32_t)k,
-                                          (uint32_t)(c * NB + sw * RPW + i), 0u), k0, k1);
+                                          (uint32_t)(c * NB + sw * RPW + i), 0u), p.philox);
           // D: softmax sums and the cheap candidate test exp(z - Mr) > Tf * w
           float e[RPW][4], w[RPW][4];
           unsigned cm[RPW];
@@ -1120,6 +1105,7 @@ cudaError_t launch_draft_common(const uint16_t* W1, const uint16_t* W2, const ui
   p.n_chunks = cdiv(B, NB);
   p.kc = draft_kchunk(r);   // divides r (r % 16 == 0)
   p.seed = seed;
+  p.philox = philox_keys(seed);
   const size_t part_bytes = align_up((size_t)3 * B * kDraftMaxCtas * sizeof(RowState), 256);
   char* base = static_cast<char*>(region);
   p.partials = reinterpret_cast<RowState*>(base);

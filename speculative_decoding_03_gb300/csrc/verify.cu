@@ -324,7 +324,7 @@ __device__ __forceinline__ float exact_score(bool residual, float t, float z, fl
 __device__ __forceinline__ int race_segment(const float4 (&t)[kVerVec],
                                             const float4 (&zz)[kVerVec], int v0, int V,
                                             bool residual, float off_a, float off_b,
-                                            uint32_t stream, int excl, uint64_t seed, int k,
+                                            uint32_t stream, int excl, const PhiloxKeys& keys, int k,
                                             int b, RowState* red, float* redf, Cand* cand_s,
                                             int* cnt_s, RowState& best) {
   if (!residual) {
@@ -341,7 +341,7 @@ __device__ __forceinline__ int race_segment(const float4 (&t)[kVerVec],
 #pragma unroll
   for (int j = 0; j < kVerVec; ++j) {
     const int v = v0 + j * 4 * kSampleThreads;
-    const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, stream);
+    const uint4 dr = draw_block(keys, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, stream);
     const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w};
     const float tv[4] = {t[j].x, t[j].y, t[j].z, t[j].w};
     const float zv[4] = {zz[j].x, zz[j].y, zz[j].z, zz[j].w};
@@ -449,7 +449,7 @@ __device__ __forceinline__ int race_segment(const float4 (&t)[kVerVec],
 // its best in cand[item * kCandMax] when it scored them itself.
 __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
     const float* __restrict__ T, const float* __restrict__ U, const float* __restrict__ bias,
-    const ItemRec* __restrict__ rec, int B, int gamma, int V, uint64_t seed, int splits,
+    const ItemRec* __restrict__ rec, int B, int gamma, int V, const PhiloxKeys keys, int splits,
     int* __restrict__ cand_n, Cand* __restrict__ cand, int* err) {
   extern __shared__ float4 fs_buf[];            // [2][3][kVerSeg / 4]
   __shared__ uint64_t full[2];
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
       const uint32_t stream = md == kModeBonus ? 3u : 2u;
       const int excl = m.excl;
       RowState best;
-      const int n = race_segment(t, zz, v0, V, residual, off_a, off_b, stream, excl, seed, k, b,
+      const int n = race_segment(t, zz, v0, V, residual, off_a, off_b, stream, excl, keys, k, b,
                                  red, redf, cand_s, &cnt_s, best);
       Cand* dst = cand + (size_t)item * kCandMax;
       if (n >= 0) {
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kSampleThreads) final_sample_kernel(
 // acceptance rule practically never takes, so it is not split further).
 __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(
     const float* __restrict__ T, const ItemRec* __restrict__ rec, const int* __restrict__ cand_n,
-    const Cand* __restrict__ cand, int splits, int gamma, int V, uint64_t seed,
+    const Cand* __restrict__ cand, int splits, int gamma, int V, const PhiloxKeys keys,
     const int32_t* __restrict__ mode, const int32_t* __restrict__ pos,
     const int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ fallback) {
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(
   for (int v = 4 * threadIdx.x; v < V; v += 4 * kSampleThreads) {
     const float4 t4 = ld_stream_f4(Trow + v);
     const float t[4] = {t4.x, t4.y, t4.z, t4.w};
-    const uint4 dr = draw_block(seed, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 2u);
+    const uint4 dr = draw_block(keys, (uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 2u);
     const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -678,6 +678,7 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   int32_t* slot_of = ws_at<int32_t>(ws, p.off_slot);
   int* n_res = ws_at<int>(ws, p.off_nres);
   int32_t* fb = ws_at<int32_t>(ws, p.off_fallback);
+  const PhiloxKeys keys = philox_keys(seed);
   ItemRec* rec = ws_at<ItemRec>(ws, p.off_rec);
 
   cudaError_t e = launch_pdl(target_stats_kernel, dim3(p.stats.splits, B * gamma < 65535 ? B * gamma : 65535),
@@ -698,11 +699,11 @@ cudaError_t launch_verify(const Plan& p, const float* T, const float* U, const u
   }
   e = launch_pdl(final_sample_kernel, dim3(final_sample_grid(B * p.ver.splits)),
                  dim3(kSampleThreads), kFinalSmem, stream, T, U, (const float*)bias,
-                 (const ItemRec*)rec, B, gamma, V, seed, p.ver.splits, cand_n, cand, err);
+                 (const ItemRec*)rec, B, gamma, V, keys, p.ver.splits, cand_n, cand, err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(finalize_kernel, dim3(B), dim3(kSampleThreads), 0, stream, T,
                  (const ItemRec*)rec, (const int*)cand_n, (const Cand*)cand, p.ver.splits, gamma,
-                 V, seed, (const int32_t*)mode, (const int32_t*)pos, (const int32_t*)accept_len,
+                 V, keys, (const int32_t*)mode, (const int32_t*)pos, (const int32_t*)accept_len,
                  out_tokens, fb);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
