@@ -937,7 +937,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(
                 sm &= sm - 1u;
                 const float wj = j == 0 ? w[i][0] : j == 1 ? w[i][1] : j == 2 ? w[i][2] : w[i][3];
                 const float zj = j == 0 ? z[i][0] : j == 1 ? z[i][1] : j == 2 ? z[i][2] : z[i][3];
-                const float scj = zj - logf(exp1_from_w(wj));
+                // E accurate (log1p), its logarithm the fast one (within 3 ulp of log E)
+                const float scj = zj - __logf(exp1_from_w(wj));
                 if (scj > sc) { sc = scj; sv = v + j; szz = zj; }
               }
               // the warp's best (largest score, then smallest index): two integer reductions,
