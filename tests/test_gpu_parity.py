@@ -480,6 +480,31 @@ def test_first_launch_ranks_more_items_than_threads_per_cta():
     assert ws.status() == 0
 
 
+@pytest.mark.parametrize("B,gamma,V", [(12, 32, 1664), (8, 4, 1024), (3, 2, 65536), (2, 1, 8192)])
+def test_first_launch_scheduler_placements(B, gamma, V):
+    """The first launch schedules up to 384 items in the confidence warps of the CTAs that
+    hold no request (one such CTA ranking all 384 items; 149 of them sharing 6 items, most
+    shares empty), or, with no such CTA (as many CTAs as requests), in CTA 0 after the last
+    position: the schedule equals the scheduler's on the same survivals, and the oracle's."""
+    _need_gpu()
+    w = workloads.scaled(workloads.get("qwen3_4b_like"), B=B, gamma=gamma, V=V, r=64, H=16)
+    inp = workloads.generate(w, with_T=False)
+    dev = _dev(inp)
+    ws = _ws(w)
+    W2p = ds.pack_w2(dev["W2"])
+    for seed in (w.seed, w.seed + 1):
+        d, (c, a), (ell, Bt, th) = ds.draft_confidence_schedule(
+            dev["U"], dev["W1"], W2p, dev["anchor"], dev["h"], dev["w_c"], float(inp.b_c),
+            dev["sps"], seed, ws)
+        ell1, Bt1, th1 = ds.schedule(a, dev["sps"], ws)
+        np.testing.assert_array_equal(ell.cpu().numpy(), ell1.cpu().numpy())
+        assert int(Bt.item()) == int(Bt1.item()) and float(th.item()) == float(th1.item())
+        ell_r, Bt_r, th_r = oracle.schedule(a.cpu().numpy(), inp.sps)
+        np.testing.assert_array_equal(ell.cpu().numpy(), ell_r)
+        assert int(Bt.item()) == Bt_r and float(th.item()) == th_r
+    assert ws.status() == 0
+
+
 def test_schedule_with_exactly_one_block_of_items():
     """R * gamma equal to the scheduler's thread count (the last SPS entry is staged too)."""
     _need_gpu()
