@@ -307,6 +307,18 @@ def measure_workload(w, args, world: int, rank: int, local: int, barrier, dist=N
     res = step.results()
     first_ms = time_graphs(step.capture([w.seed + 20 + j for j in range(n_ring)], first_only=True))
     draft_ms = time_graphs(step.capture([w.seed + 30 + j for j in range(n_ring)], draft_only=True))
+    # the verification alone (the last step's drafts and schedule), in a graph ring of its
+    # own: its target rows and W2 stay warmer in L2 than after a draft
+    x, d, ell = dev, step.draft_out, step.sched_out[0]
+    vgs = []
+    for j in range(n_ring):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ds.verify_packed(x["T"], x["U"], x["W1"], step.W2p, x["anchor"], d["tokens"], d["q_tok"],
+                             d["row_max"], d["row_sumexp"], ell, w.seed + 40 + j, step.ws,
+                             step.verify_out)
+        vgs.append(g)
+    verify_ms = time_graphs(vgs)
     peak, peak_kind = _peaks()
     fbytes, dbytes = first_launch_bytes(w), draft_bytes(w)
     sbytes = step_bytes(w, res["n_out"], res["accept_len"], res["ell"])
@@ -323,8 +335,9 @@ def measure_workload(w, args, world: int, rank: int, local: int, barrier, dist=N
                         "unit": "GB/s", "frac": sbytes / (ms * 1e-3) / 1e9 / peak},
            "accept": {"mean_ell": float(np.mean(res["ell"])),
                       "mean_accept_len": float(np.mean(res["accept_len"])), "B_total": res["B_total"]},
+           "verify_alone_ms": verify_ms,
            "gpu_launches_per_step": launches_per_step(w)}
-    del step, dev
+    del step, dev, vgs
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, min(w.B, args.ref_requests))
