@@ -89,12 +89,13 @@ __device__ __forceinline__ uint4 philox_wide(uint4 c, const PhiloxKeys& rk) {
 }
 
 // U01(x) = ((x >> 9) + 1/2) 2^-23 and its exact complement 1 - U01(x); both are exact in
-// fp32 (24 significant bits at most).
+// fp32 (24 significant bits at most).  Built without an integer conversion: the float with
+// bits 0x4B000000 | n is 2^23 + n, and one fused multiply-add removes 2^23 - 1/2.
 __device__ __forceinline__ float u01(uint32_t x) {
-  return (__uint2float_rn(x >> 9) + 0.5f) * 0x1.0p-23f;
+  return fmaf(__uint_as_float(0x4B000000u | (x >> 9)), 0x1.0p-23f, -(1.f - 0x1.0p-24f));
 }
 __device__ __forceinline__ float one_minus_u01(uint32_t x) {
-  return (__uint2float_rn((~x) >> 9) + 0.5f) * 0x1.0p-23f;
+  return fmaf(__uint_as_float(0x4B000000u | ((~x) >> 9)), 0x1.0p-23f, -(1.f - 0x1.0p-24f));
 }
 
 // The Exp(1) variate E = -log(u) = -log1p(-w), accurate near u -> 1 (small w), which is
