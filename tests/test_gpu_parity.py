@@ -480,12 +480,15 @@ def test_first_launch_ranks_more_items_than_threads_per_cta():
     assert ws.status() == 0
 
 
-@pytest.mark.parametrize("B,gamma,V", [(12, 32, 1664), (8, 4, 1024), (3, 2, 65536), (2, 1, 8192)])
+@pytest.mark.parametrize("B,gamma,V", [(12, 32, 1664), (8, 4, 1024), (3, 2, 65536), (2, 1, 8192),
+                                        (256, 16, 1024), (241, 17, 1024)])
 def test_first_launch_scheduler_placements(B, gamma, V):
     """The first launch schedules up to 384 items in the confidence warps of the CTAs that
     hold no request (one such CTA ranking all 384 items; 149 of them sharing 6 items, most
     shares empty), or, with no such CTA (as many CTAs as requests), in CTA 0 after the last
-    position: the schedule equals the scheduler's on the same survivals, and the oracle's."""
+    position; up to 4096 items with the whole grid ranking (exactly 4096 here), beyond that
+    with the scheduler kernel after the launch (4097): the schedule equals the scheduler's
+    on the same survivals, and the oracle's."""
     _need_gpu()
     w = workloads.scaled(workloads.get("qwen3_4b_like"), B=B, gamma=gamma, V=V, r=64, H=16)
     inp = workloads.generate(w, with_T=False)
